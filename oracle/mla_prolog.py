@@ -1,0 +1,176 @@
+"""MLA prolog oracle (MlaPrologV2 / MlaPreprocess inference prolog) — TEST INFRASTRUCTURE ONLY.
+
+Plain float64 restatement of the MlaPrologV2 README, "功能说明" (computation formulas):
+
+    c^Q  = RmsNorm(x · W^DQ)                      q^C = c^Q · W^UQ        q^N = q^C · W^UK
+    q^R  = ROPE(c^Q · W^QR)
+    c^KV = RmsNorm(x · W^DKV)   -> kv_cache        k^R = ROPE(x · W^KR)  -> kr_cache
+
+with the RmsNorm of the same section (epsilon added to the mean of squares, inside the root; the
+aclnnMlaPreprocessV2 "Formula" RMS agrees) and the half-and-half RoPE of aclnnQkvRmsNormRopeCache,
+"Formulas" (3), which the MLA pages name (ROPE) but do not define.
+
+Readings where the pages are silent (each is also listed in the design notes):
+
+* Rounding points.  float64 throughout, rounded to bf16 only where a tensor becomes the input of a
+  bf16 matmul (c^Q; the q^C nope slice) and at the outputs (query, query_rope, the caches).
+* Fused weights.  weight_dkv_kr columns are [W^DKV (Hckv) | W^KR (Dr)]; weight_uq_qr columns are
+  grouped per head n as [W^UQ_n (D) | W^QR_n (Dr)].  The pages give only the fused shapes
+  ("约束说明" dtype/shape matrix: (He, Hckv+Dr), (Hcq, N*(D+Dr))).
+* Partial quant ("部分量化"): c^Q (bf16) is multiplied by smooth_scales_cq, quantised per token
+  symmetrically with scale = amax/127, round half to even, clamp to [-127, 127]; the int8 matmul
+  accumulates exactly and is dequantised by scale_t * dequant_scale_w_uq_qr[column].  The quantised
+  code is decided in float32, the precision of the kernel (the pages fix none).
+* Cache quant: value / quant_scale (the aclnnQkvRmsNormRopeCache "Formulas" (4) rule
+  kQuant = kRoPE / kScale), round half to even, clamp to [-128, 127], decided in float32.
+* cache_index: slot i goes to block i // BlockSize, row i % BlockSize (Nkv = 1); i = -1 skips the
+  row (aclnnQkvRmsNormRopeCache, "Other restrictions"); other out-of-range values are skipped too
+  (the CUDA path also flags them).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .rounding import round_bf16, saturate_int8_rne
+
+
+def rms_norm(h: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """gamma * h / sqrt(mean(h^2) + eps) along the last axis (MlaPrologV2 README, RmsNorm公式)."""
+    h = np.asarray(h, dtype=np.float64)
+    mean_sq = np.mean(h * h, axis=-1, keepdims=True)
+    return np.asarray(gamma, dtype=np.float64) * h / np.sqrt(mean_sq + eps)
+
+
+def rope_half_and_half(y: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
+    """y*cos + cat(-y2, y1)*sin with y1, y2 the two halves of the last axis
+    (aclnnQkvRmsNormRopeCache, "Formulas" (3) RoPE (Half-and-Half))."""
+    y = np.asarray(y, dtype=np.float64)
+    half = y.shape[-1] // 2
+    y1, y2 = y[..., :half], y[..., half:]
+    rotated = np.concatenate([-y2, y1], axis=-1)
+    return y * np.asarray(cos, np.float64) + rotated * np.asarray(sin, np.float64)
+
+
+def dynamic_quant_per_token(c_q: np.ndarray, smooth: np.ndarray):
+    """Per-token symmetric int8 quant of c^Q after smoothing (MlaPrologV2 README, parameter
+    smooth_scales_cq: "RmsNormCq输出动态量化参数"; formula is the reading stated in the module
+    docstring).  Returns (codes int8 (T,Hcq), scale float32 (T,)).  Decided in float32."""
+    s = np.asarray(c_q, np.float32) * np.asarray(smooth, np.float32).reshape(1, -1)
+    amax = np.max(np.abs(s), axis=-1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    q = (s / safe[:, None]).astype(np.float32)
+    codes = saturate_int8_rne(q, -127, 127)
+    codes[scale == 0] = 0
+    return codes, scale
+
+
+def cache_quant(v: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """int8 code of v / scale per channel, round half to even, clamp to [-128,127], in float32
+    (MlaPrologV2 README quant_scale_ckv / quant_scale_ckr; the division rule of
+    aclnnQkvRmsNormRopeCache "Formulas" (4))."""
+    q = (np.asarray(v, np.float64).astype(np.float32)
+         / np.asarray(scale, np.float32).reshape(1, -1)).astype(np.float32)
+    return saturate_int8_rne(q)
+
+
+def scatter_rows(cache: np.ndarray, rows: np.ndarray, cache_index: np.ndarray) -> np.ndarray:
+    """Copy of ``cache`` (BlockNum, BlockSize, 1, H) with row t stored at slot cache_index[t]
+    (MlaPrologV2 README k^C = Cache(c^KV), k^R = Cache(...); "-1 skips" from
+    aclnnQkvRmsNormRopeCache "Other restrictions")."""
+    out = cache.copy()
+    block_num, block_size = cache.shape[0], cache.shape[1]
+    for t, i in enumerate(np.asarray(cache_index).reshape(-1).tolist()):
+        if i < 0 or i >= block_num * block_size:
+            continue
+        out[i // block_size, i % block_size, 0, :] = rows[t]
+    return out
+
+
+def mla_prolog(token_x, weight_dq, weight_uq_qr, weight_uk, weight_dkv_kr,
+               rmsnorm_gamma_cq, rmsnorm_gamma_ckv, rope_sin, rope_cos, cache_index,
+               kv_cache, kr_cache, rmsnorm_epsilon_cq, rmsnorm_epsilon_ckv,
+               dequant_scale_w_uq_qr=None, smooth_scales_cq=None,
+               quant_scale_ckv=None, quant_scale_ckr=None) -> dict:
+    """The whole prolog for T tokens.
+
+    Inputs are numpy arrays holding the exact values of the operator inputs (bf16 values as
+    float64; int8 weights/caches as int8).  token_x is (T, He) (the BSH form (B,S,He) is the same
+    memory and is flattened by the caller).  Returns a dict with query (T,N,Hckv), query_rope
+    (T,N,Dr) as float64 holding bf16 values, and the updated kv_cache / kr_cache (float64 bf16
+    values, or int8 when the caches are quantised).
+    """
+    x = np.asarray(token_x, np.float64)
+    T, He = x.shape
+    N, D, Hckv = weight_uk.shape
+    Dr = np.asarray(rope_sin).shape[-1]
+    Hcq = weight_dq.shape[1]
+    sin = np.asarray(rope_sin, np.float64).reshape(T, Dr)
+    cos = np.asarray(rope_cos, np.float64).reshape(T, Dr)
+
+    # Query path: c^Q = RmsNorm(x · W^DQ), rounded to bf16 as the next matmul's input.
+    h_q = x @ np.asarray(weight_dq, np.float64)
+    c_q = round_bf16(rms_norm(h_q, rmsnorm_gamma_cq, rmsnorm_epsilon_cq))
+
+    # c^Q · [W^UQ | W^QR]
+    if np.asarray(weight_uq_qr).dtype == np.int8:
+        codes, scale_t = dynamic_quant_per_token(c_q, smooth_scales_cq)
+        acc = codes.astype(np.int64) @ np.asarray(weight_uq_qr).astype(np.int64)   # exact
+        u = (acc.astype(np.float64) * scale_t.astype(np.float64)[:, None]
+             * np.asarray(dequant_scale_w_uq_qr, np.float64).reshape(1, -1))
+    else:
+        u = c_q @ np.asarray(weight_uq_qr, np.float64)
+    u = u.reshape(T, N, D + Dr)
+    q_c = round_bf16(u[:, :, :D])                  # q^C, input of the W^UK matmul
+    q_r = u[:, :, D:]                              # c^Q · W^QR, before ROPE
+
+    w_uk = np.asarray(weight_uk, np.float64)
+    q_n = np.empty((T, N, Hckv), np.float64)
+    for n in range(N):                             # q^N = q^C · W^UK, per head
+        q_n[:, n, :] = q_c[:, n, :] @ w_uk[n]
+    query = round_bf16(q_n)
+    query_rope = round_bf16(rope_half_and_half(q_r, cos[:, None, :], sin[:, None, :]))
+
+    # Key path: c^KV = RmsNorm(x · W^DKV), k^R = ROPE(x · W^KR)
+    h_kvr = x @ np.asarray(weight_dkv_kr, np.float64)
+    c_kv = rms_norm(h_kvr[:, :Hckv], rmsnorm_gamma_ckv, rmsnorm_epsilon_ckv)
+    k_r = rope_half_and_half(h_kvr[:, Hckv:Hckv + Dr], cos, sin)
+
+    if np.asarray(kv_cache).dtype == np.int8:
+        kv_rows = cache_quant(c_kv, quant_scale_ckv)
+    else:
+        kv_rows = round_bf16(c_kv)
+    if np.asarray(kr_cache).dtype == np.int8:
+        kr_rows = cache_quant(k_r, quant_scale_ckr)
+    else:
+        kr_rows = round_bf16(k_r)
+
+    return {
+        "query": query,
+        "query_rope": query_rope,
+        "kv_cache": scatter_rows(np.asarray(kv_cache), kv_rows, cache_index),
+        "kr_cache": scatter_rows(np.asarray(kr_cache), kr_rows, cache_index),
+        # intermediates, exposed for tests only
+        "c_q": c_q,
+        "c_kv": c_kv,
+        "k_r": k_r,
+    }
+
+
+def mla_prolog_tokens(inputs: dict, token_ids) -> dict:
+    """The prolog restricted to a subset of tokens (tokens are independent).  Caches are not
+    scattered; the rows that would be stored are returned instead."""
+    ids = np.asarray(token_ids)
+    sub = dict(inputs)
+    sub["token_x"] = np.asarray(inputs["token_x"])[ids]
+    sub["rope_sin"] = np.asarray(inputs["rope_sin"]).reshape(-1, np.asarray(inputs["rope_sin"]).shape[-1])[ids]
+    sub["rope_cos"] = np.asarray(inputs["rope_cos"]).reshape(-1, np.asarray(inputs["rope_cos"]).shape[-1])[ids]
+    sub["cache_index"] = -np.ones(len(ids), np.int64)   # no scatter
+    out = mla_prolog(**sub)
+    kv_dtype = np.asarray(inputs["kv_cache"]).dtype
+    kr_dtype = np.asarray(inputs["kr_cache"]).dtype
+    out["kv_rows"] = (cache_quant(out["c_kv"], inputs["quant_scale_ckv"]) if kv_dtype == np.int8
+                      else round_bf16(out["c_kv"]))
+    out["kr_rows"] = (cache_quant(out["k_r"], inputs["quant_scale_ckr"]) if kr_dtype == np.int8
+                      else round_bf16(out["k_r"]))
+    return out

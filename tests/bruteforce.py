@@ -1,0 +1,153 @@
+"""Scalar brute-force restatements used to pin the oracle on tiny inputs (test helper).
+
+Written independently of ``oracle/``: plain Python floats and ints, one output element at a time,
+and a rounding routine that works on the IEEE-754 bit pattern with integer arithmetic (the oracle
+rounds through frexp/ldexp instead).  Valid only for tiny shapes and normal-range values.
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+
+def _bits(x: float) -> int:
+    return struct.unpack("<Q", struct.pack("<d", x))[0]
+
+
+def _float(b: int) -> float:
+    return struct.unpack("<d", struct.pack("<Q", b))[0]
+
+
+def rne_keep_bits(x: float, keep: int) -> float:
+    """Round a normal float64 to ``keep`` explicit mantissa bits, ties to even, on its bit pattern."""
+    if x == 0.0 or math.isinf(x) or math.isnan(x):
+        return x
+    drop = 52 - keep
+    b = _bits(x)
+    lsb = (b >> drop) & 1
+    b += (1 << (drop - 1)) - 1 + lsb
+    b &= ~((1 << drop) - 1)
+    return _float(b)
+
+
+def bf16(x: float) -> float:
+    return rne_keep_bits(x, 7)
+
+
+def fp16(x: float) -> float:
+    return rne_keep_bits(x, 10)
+
+
+def f32(x: float) -> float:
+    """float64 -> nearest float32 (struct packs with round-to-nearest-even)."""
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
+def int8_code(q: float, lo: int, hi: int) -> int:
+    r = round(q)                    # Python rounds half to even
+    return max(lo, min(hi, r))
+
+
+def rope_element(y, cos, sin, j):
+    d = len(y)
+    h = d // 2
+    partner = -y[j + h] if j < h else y[j - h]
+    return y[j] * cos[j] + partner * sin[j]
+
+
+def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_cache, kr_cache,
+                          eps_cq, eps_ckv, dqw=None, smooth=None, qs_ckv=None, qs_ckr=None):
+    """All arguments are nested Python lists.  Returns dict of nested lists."""
+    T, He = len(x), len(x[0])
+    Hcq = len(wdq[0])
+    N, D, Hckv = len(wuk), len(wuk[0]), len(wuk[0][0])
+    Dr = len(sin[0])
+    int8_w = isinstance(wuq[0][0], int)
+    query = [[[0.0] * Hckv for _ in range(N)] for _ in range(T)]
+    query_rope = [[[0.0] * Dr for _ in range(N)] for _ in range(T)]
+    kv = [[[list(r) for r in row] for row in blk] for blk in kv_cache]
+    kr = [[[list(r) for r in row] for row in blk] for blk in kr_cache]
+    bs = len(kv_cache[0])
+    for t in range(T):
+        hq = [sum(x[t][k] * wdq[k][c] for k in range(He)) for c in range(Hcq)]
+        rms = math.sqrt(sum(v * v for v in hq) / Hcq + eps_cq)
+        cq = [bf16(gcq[c] * hq[c] / rms) for c in range(Hcq)]
+        if int8_w:
+            s = [f32(cq[c] * smooth[c]) for c in range(Hcq)]
+            amax = max(abs(v) for v in s)
+            scale = f32(amax / 127.0)
+            codes = [0 if scale == 0 else int8_code(f32(v / scale), -127, 127) for v in s]
+        for n in range(N):
+            base = n * (D + Dr)
+            u = []
+            for jj in range(D + Dr):
+                col = base + jj
+                if int8_w:
+                    acc = sum(codes[c] * wuq[c][col] for c in range(Hcq))
+                    u.append(acc * scale * dqw[col])
+                else:
+                    u.append(sum(cq[c] * wuq[c][col] for c in range(Hcq)))
+            qc = [bf16(v) for v in u[:D]]
+            r = u[D:]
+            for c2 in range(Hckv):
+                query[t][n][c2] = bf16(sum(qc[d] * wuk[n][d][c2] for d in range(D)))
+            for j in range(Dr):
+                query_rope[t][n][j] = bf16(rope_element(r, cos[t], sin[t], j))
+        hkv = [sum(x[t][k] * wdkv[k][c] for k in range(He)) for c in range(Hckv + Dr)]
+        rms = math.sqrt(sum(v * v for v in hkv[:Hckv]) / Hckv + eps_ckv)
+        ckv = [gckv[c] * hkv[c] / rms for c in range(Hckv)]
+        kr_row = [rope_element(hkv[Hckv:], cos[t], sin[t], j) for j in range(Dr)]
+        i = idx[t]
+        if 0 <= i < len(kv_cache) * bs:
+            if qs_ckv is not None:
+                kv[i // bs][i % bs][0] = [int8_code(f32(f32(ckv[c]) / qs_ckv[c]), -128, 127)
+                                          for c in range(Hckv)]
+            else:
+                kv[i // bs][i % bs][0] = [bf16(v) for v in ckv]
+            if qs_ckr is not None:
+                kr[i // bs][i % bs][0] = [int8_code(f32(f32(kr_row[j]) / qs_ckr[j]), -128, 127)
+                                          for j in range(Dr)]
+            else:
+                kr[i // bs][i % bs][0] = [bf16(v) for v in kr_row]
+    return {"query": query, "query_rope": query_rope, "kv_cache": kv, "kr_cache": kr}
+
+
+def qkv_bruteforce(qkv, gq, gk, cos, sin, idx, k_cache, v_cache, eps, Nq, Nk, Nv, ks=None,
+                   vs=None):
+    """qkv: T rows of (Nq+Nk+Nv)*D floats."""
+    T = len(qkv)
+    D = len(qkv[0]) // (Nq + Nk + Nv)
+    q_out = [[[0.0] * D for _ in range(Nq)] for _ in range(T)]
+    kc = [[[list(r) for r in row] for row in blk] for blk in k_cache]
+    vc = [[[list(r) for r in row] for row in blk] for blk in v_cache]
+    bs = len(k_cache[0])
+    for t in range(T):
+        heads = [qkv[t][h * D:(h + 1) * D] for h in range(Nq + Nk + Nv)]
+        k_rows, v_rows = [], []
+        for h in range(Nq + Nk):
+            xh = heads[h]
+            g = gq if h < Nq else gk
+            rms = math.sqrt(sum(v * v for v in xh) / D + eps)
+            y = [xh[j] / rms * g[j] for j in range(D)]
+            e = [rope_element(y, cos[t], sin[t], j) for j in range(D)]
+            if h < Nq:
+                q_out[t][h] = [fp16(v) for v in e]
+            else:
+                hk = h - Nq
+                if ks is not None:
+                    k_rows.append([int8_code(f32(f32(e[j]) / ks[hk][j]), -128, 127)
+                                   for j in range(D)])
+                else:
+                    k_rows.append([fp16(v) for v in e])
+        for hv in range(Nv):
+            vh = heads[Nq + Nk + hv]
+            if vs is not None:
+                v_rows.append([int8_code(f32(f32(vh[j]) / vs[hv][j]), -128, 127)
+                               for j in range(D)])
+            else:
+                v_rows.append([fp16(v) for v in vh])
+        i = idx[t]
+        if 0 <= i < len(k_cache) * bs:
+            kc[i // bs][i % bs] = k_rows
+            vc[i // bs][i % bs] = v_rows
+    return {"q_out": q_out, "k_cache": kc, "v_cache": vc}

@@ -1,0 +1,96 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check the pins catch them.
+
+Each mutation rewrites one line of ``oracle/mla_prolog.py`` or ``oracle/qkv_rms_norm_rope_cache.py``
+in a private module copy; the brute-force pin must then fail.  The real oracle is untouched.
+"""
+import importlib.util
+import os
+import sys
+import types
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import bruteforce as bf
+from tests.test_oracle_pins import _brute, _tiny_mla, _tiny_qkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _mutant(fname, old, new):
+    path = os.path.join(ROOT, "oracle", fname)
+    src = open(path).read()
+    assert src.count(old) == 1, (fname, old)
+    mod = types.ModuleType("oracle._mutant")
+    mod.__package__ = "oracle"
+    exec(compile(src.replace(old, new), path, "exec"), mod.__dict__)
+    return mod
+
+
+MLA_MUTATIONS = [
+    ("eps outside the root", "np.sqrt(mean_sq + eps)", "(np.sqrt(mean_sq) + eps * 1e5)"),
+    ("sum instead of mean", "np.mean(h * h, axis=-1, keepdims=True)",
+     "np.sum(h * h, axis=-1, keepdims=True)"),
+    ("rope sign", "rotated = np.concatenate([-y2, y1], axis=-1)",
+     "rotated = np.concatenate([y2, -y1], axis=-1)"),
+    ("nope/rope order in a head", "q_c = round_bf16(u[:, :, :D])", "q_c = round_bf16(u[:, :, Dr:])"),
+    ("rope slice", "q_r = u[:, :, D:]", "q_r = u[:, :, :Dr]"),
+    ("kv/kr column order", "h_kvr[:, :Hckv], rmsnorm_gamma_ckv",
+     "h_kvr[:, Dr:], rmsnorm_gamma_ckv"),
+    ("gamma dropped", "return np.asarray(gamma, dtype=np.float64) * h / np.sqrt(mean_sq + eps)",
+     "return h / np.sqrt(mean_sq + eps)"),
+    ("slot block/offset swapped", "out[i // block_size, i % block_size, 0, :] = rows[t]",
+     "out[i % block_num, i // block_num, 0, :] = rows[t]"),
+    ("dequant scale dropped", "* np.asarray(dequant_scale_w_uq_qr, np.float64).reshape(1, -1))",
+     ")"),
+    ("cache quant multiplies", "/ np.asarray(scale, np.float32).reshape(1, -1)).astype(np.float32)",
+     "* np.asarray(scale, np.float32).reshape(1, -1)).astype(np.float32)"),
+    ("missing bf16 round of q^C", "q_c = round_bf16(u[:, :, :D])", "q_c = u[:, :, :D] * (1 + 2**-9)"),
+]
+
+
+@pytest.mark.parametrize("label,old,new", MLA_MUTATIONS, ids=[m[0] for m in MLA_MUTATIONS])
+def test_mla_pins_catch_mutation(label, old, new):
+    mod = _mutant("mla_prolog.py", old, new)
+    int8 = "dequant" in label or "quant" in label
+    rng = np.random.default_rng(31)
+    inp = _tiny_mla(rng, int8=int8, int8_cache="cache quant" in label)
+    want = _brute(inp)
+    got = mod.mla_prolog(**inp)
+    same = True
+    for key in ("query", "query_rope", "kv_cache", "kr_cache"):
+        same &= np.allclose(np.asarray(got[key], np.float64), np.array(want[key], np.float64),
+                            rtol=1e-12, atol=1e-14)
+    assert not same, f"mutation '{label}' not detected"
+
+
+QKV_MUTATIONS = [
+    ("split k/v swapped", "k, v = x[:, :Nq, :], x[:, Nq:Nq + Nk, :], x[:, Nq + Nk:, :]",
+     "k, v = x[:, :Nq, :], x[:, Nq + Nk:, :], x[:, Nq:Nq + Nk, :]"),
+    ("v normalised too", "v_rows = _quant(v, np.asarray(v_scale).reshape(1, Nv, D))",
+     "v_rows = _quant(rms_norm(v, 1.0, epsilon), np.asarray(v_scale).reshape(1, Nv, D))"),
+    ("k gamma from q", "k_emb = rope_half_and_half(rms_norm(k, gamma_k, epsilon), cos, sin)",
+     "k_emb = rope_half_and_half(rms_norm(k, gamma_q, epsilon), cos, sin)"),
+]
+
+
+@pytest.mark.parametrize("label,old,new", QKV_MUTATIONS, ids=[m[0] for m in QKV_MUTATIONS])
+def test_qkv_pins_catch_mutation(label, old, new):
+    mod = _mutant("qkv_rms_norm_rope_cache.py", old, new)
+    rng = np.random.default_rng(32)
+    inp = _tiny_qkv(rng, quant=True)
+    got = mod.qkv_rms_norm_rope_cache(**inp)
+    ref = oracle.qkv_rms_norm_rope_cache(**inp)
+    L = lambda a: np.asarray(a).tolist()
+    want = bf.qkv_bruteforce(L(inp["qkv"]), L(inp["gamma_q"]), L(inp["gamma_k"]), L(inp["cos"]),
+                             L(inp["sin"]), L(inp["index"]),
+                             np.asarray(inp["k_cache"]).astype(int).tolist(),
+                             np.asarray(inp["v_cache"]).astype(int).tolist(), inp["epsilon"],
+                             inp["Nq"], inp["Nk"], inp["Nv"], ks=L(inp["k_scale"]),
+                             vs=L(inp["v_scale"]))
+    assert np.array_equal(ref["k_cache"], np.array(want["k_cache"], np.int8))
+    detected = (not np.allclose(got["q_out"], np.array(want["q_out"]))
+                or not np.array_equal(got["k_cache"], np.array(want["k_cache"], np.int8))
+                or not np.array_equal(got["v_cache"], np.array(want["v_cache"], np.int8)))
+    assert detected, f"mutation '{label}' not detected"
