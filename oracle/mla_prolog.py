@@ -174,3 +174,22 @@ def mla_prolog_tokens(inputs: dict, token_ids) -> dict:
     out["kr_rows"] = (cache_quant(out["k_r"], inputs["quant_scale_ckr"]) if kr_dtype == np.int8
                       else round_bf16(out["k_r"]))
     return out
+
+
+def mla_key_rows(token_x, weight_dkv_kr, rmsnorm_gamma_ckv, rope_sin, rope_cos,
+                 rmsnorm_epsilon_ckv, Hckv, kv_dtype_int8=False, kr_dtype_int8=False,
+                 quant_scale_ckv=None, quant_scale_ckr=None, **_unused) -> tuple:
+    """Only the key path of ``mla_prolog`` (c^KV = RmsNorm(x·W^DKV), k^R = ROPE(x·W^KR)), as the
+    rows the cache would receive for every token: (kv_rows, kr_rows).  Same formulas and
+    rounding as ``mla_prolog``; used to check every written cache slot of large workloads."""
+    x = np.asarray(token_x, np.float64)
+    T = x.shape[0]
+    Dr = np.asarray(rope_sin).shape[-1]
+    sin = np.asarray(rope_sin, np.float64).reshape(T, Dr)
+    cos = np.asarray(rope_cos, np.float64).reshape(T, Dr)
+    h_kvr = x @ np.asarray(weight_dkv_kr, np.float64)
+    c_kv = rms_norm(h_kvr[:, :Hckv], rmsnorm_gamma_ckv, rmsnorm_epsilon_ckv)
+    k_r = rope_half_and_half(h_kvr[:, Hckv:Hckv + Dr], cos, sin)
+    kv = cache_quant(c_kv, quant_scale_ckv) if kv_dtype_int8 else round_bf16(c_kv)
+    kr = cache_quant(k_r, quant_scale_ckr) if kr_dtype_int8 else round_bf16(k_r)
+    return kv, kr

@@ -13,14 +13,14 @@ Readings (the parameter table is lost from the page): gamma_q and gamma_k have s
 are shared by all heads of their kind; sin and cos have shape (B*S, D) and are shared by all
 heads; k_scale (Nk, D) and v_scale (Nv, D) are per channel; the cache layout is
 (BlockNum, BlockSize, N, D) with slot i at block i // BlockSize, row i % BlockSize; qOut is
-rounded to fp16; int8 codes round half to even, clamp to [-128, 127], decided in float32.
+rounded to the dtype of qkv (fp16 or bf16); int8 codes round half to even, clamp to [-128, 127], decided in float32.
 """
 from __future__ import annotations
 
 import numpy as np
 
 from .mla_prolog import rms_norm, rope_half_and_half
-from .rounding import round_fp16, saturate_int8_rne
+from .rounding import round_bf16, round_fp16, saturate_int8_rne
 
 
 def _quant(v: np.ndarray, scale: np.ndarray) -> np.ndarray:
@@ -30,12 +30,14 @@ def _quant(v: np.ndarray, scale: np.ndarray) -> np.ndarray:
 
 
 def qkv_rms_norm_rope_cache(qkv, gamma_q, gamma_k, cos, sin, index, k_cache, v_cache,
-                            epsilon, Nq, Nk, Nv, k_scale=None, v_scale=None) -> dict:
+                            epsilon, Nq, Nk, Nv, k_scale=None, v_scale=None,
+                            out_dtype: str = "fp16") -> dict:
     """qkv: (..., (Nq+Nk+Nv)*D) values; caches (BlockNum, BlockSize, Nk|Nv, D).
 
-    Returns q_out (T, Nq, D) float64 fp16 values and the updated caches (int8 when quantised,
-    else float64 fp16 values).
+    Returns q_out (T, Nq, D) as float64 values of ``out_dtype`` ("fp16" or "bf16", the dtype of
+    qkv) and the updated caches (int8 when quantised, else float64 values of ``out_dtype``).
     """
+    rnd = round_fp16 if out_dtype == "fp16" else round_bf16
     qkv = np.asarray(qkv, np.float64)
     D = qkv.shape[-1] // (Nq + Nk + Nv)
     x = qkv.reshape(-1, Nq + Nk + Nv, D)
@@ -51,8 +53,8 @@ def qkv_rms_norm_rope_cache(qkv, gamma_q, gamma_k, cos, sin, index, k_cache, v_c
         k_rows = _quant(k_emb, np.asarray(k_scale).reshape(1, Nk, D))
         v_rows = _quant(v, np.asarray(v_scale).reshape(1, Nv, D))
     else:
-        k_rows = round_fp16(k_emb)
-        v_rows = round_fp16(v)
+        k_rows = rnd(k_emb)
+        v_rows = rnd(v)
 
     k_out = np.asarray(k_cache).copy()
     v_out = np.asarray(v_cache).copy()
@@ -62,5 +64,5 @@ def qkv_rms_norm_rope_cache(qkv, gamma_q, gamma_k, cos, sin, index, k_cache, v_c
             continue
         k_out[i // block_size, i % block_size] = k_rows[t]
         v_out[i // block_size, i % block_size] = v_rows[t]
-    return {"q_out": round_fp16(q_emb), "k_cache": k_out, "v_cache": v_out,
+    return {"q_out": rnd(q_emb), "k_cache": k_out, "v_cache": v_out,
             "k_rows": k_rows, "v_rows": v_rows}

@@ -130,6 +130,8 @@ def rope_tables(positions: torch.Tensor, dim: int, dtype, base: float = 10000.0)
 
 def _slots(g, case_index_mode, T, B, S, block_num, block_size, n_skip):
     total = block_num * block_size
+    if total == 0:
+        return torch.full((T,), -1, dtype=torch.int64)   # empty cache: nothing can be stored
     if case_index_mode == "random":
         if T > total:
             raise ValueError("more tokens than cache slots")

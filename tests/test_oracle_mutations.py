@@ -21,7 +21,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def _mutant(fname, old, new):
     path = os.path.join(ROOT, "oracle", fname)
     src = open(path).read()
-    assert src.count(old) == 1, (fname, old)
+    assert src.count(old) >= 1, (fname, old)
     mod = types.ModuleType("oracle._mutant")
     mod.__package__ = "oracle"
     exec(compile(src.replace(old, new), path, "exec"), mod.__dict__)
