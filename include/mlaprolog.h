@@ -1,0 +1,226 @@
+/*
+ * libmlaprolog — C ABI of the GB300 (sm_103a) MLA prolog and QKV RmsNorm-RoPE-cache operators.
+ *
+ * Operation definitions:
+ *   - MLA prolog: MlaPrologV2 README (gitcode ops-transformer, attention/mla_prolog_v2),
+ *     section 功能说明 (formulas c^Q = RmsNorm(x·W^DQ), q^C = c^Q·W^UQ, q^N = q^C·W^UK,
+ *     q^R = ROPE(c^Q·W^QR), c^KV = RmsNorm(x·W^DKV) -> kv_cache, k^R = ROPE(x·W^KR) -> kr_cache),
+ *     parameter table 参数说明, and shape/dtype/scenario matrix 约束说明.
+ *   - QkvRmsNormRopeCache: aclnnQkvRmsNormRopeCache, "Formulas" (1) SplitVD, (2) RmsNorm,
+ *     (3) RoPE half-and-half, (4) Quant, and "Other restrictions" (index semantics).
+ *   - Two-phase calling pattern (size/validate, then execute on a stream):
+ *     aclnnMlaPreprocessV2 / aclnnQkvRmsNormRopeCache, the GetWorkspaceSize + execute pair.
+ *
+ * Conventions for every call:
+ *   - All tensor data pointers are DEVICE pointers of the current CUDA device, dense, row-major
+ *     (C-contiguous) in the logical shape given.  Shapes use at most 4 dimensions.
+ *   - The caller owns every buffer (inputs, outputs, caches, workspace, prepacked weights).  The
+ *     library never allocates device memory and keeps no per-call state between calls.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Execute calls
+ *     are asynchronous on that stream; errors of the launch itself are returned, errors found by
+ *     the kernels (bad cache indices, timeouts) are latched in the workspace error word and
+ *     returned by mlap_check_errors().
+ *   - A status other than MLAP_OK leaves outputs and caches untouched (nothing is launched) and
+ *     sets a human-readable reason retrievable with mlap_last_error() (thread-local).
+ */
+#ifndef MLAPROLOG_H
+#define MLAPROLOG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+typedef enum {
+  MLAP_DTYPE_INVALID = 0,
+  MLAP_DTYPE_BF16 = 1,
+  MLAP_DTYPE_FP16 = 2,
+  MLAP_DTYPE_FP32 = 3,
+  MLAP_DTYPE_INT8 = 4,
+  MLAP_DTYPE_INT64 = 5
+} mlap_dtype_t;
+
+/* A dense row-major tensor.  data == NULL means "absent" for optional parameters. */
+typedef struct {
+  void* data;
+  int32_t dtype;     /* mlap_dtype_t */
+  int32_t ndim;      /* 0..4 */
+  int64_t shape[4];
+} mlap_tensor_t;
+
+typedef enum {
+  MLAP_OK = 0,
+  MLAP_ERR_NULL = 1,         /* a required pointer is NULL */
+  MLAP_ERR_SHAPE = 2,        /* shapes disagree with the 约束说明 shape table */
+  MLAP_ERR_DTYPE = 3,        /* a dtype outside the parameter table */
+  MLAP_ERR_UNSUPPORTED = 4,  /* a valid combination this build does not implement */
+  MLAP_ERR_WORKSPACE = 5,    /* workspace missing or smaller than the size call returned */
+  MLAP_ERR_CUDA = 6,         /* a CUDA runtime/driver call failed */
+  MLAP_ERR_INDEX_RANGE = 7,  /* kernels met a cache index outside [-1, BlockNum*BlockSize) */
+  MLAP_ERR_TIMEOUT = 8       /* a kernel's bounded wait ran out and the kernel returned early */
+} mlap_status_t;
+
+/* ============================================================================================ */
+/* MLA prolog (MlaPrologV2 / MlaPreprocess inference prolog)                                     */
+/* ============================================================================================ */
+
+/* Symbols (约束说明): T = B*S tokens, He hidden, Hcq q-latent, Hckv kv-latent, N heads,
+ * D = 128 nope head dim, Dr rope head dim (even), Nkv = 1.
+ *
+ * Scenarios (约束说明 scenario matrix) are selected by dtypes and optional pointers:
+ *   non-quant:                   all bf16; every dequant/quant/smooth scale absent.
+ *   partial quant, kv non-quant: weight_uq_qr int8 with dequant_scale_w_uq_qr (1, N*(D+Dr)) fp32
+ *                                and smooth_scales_cq (1, Hcq) fp32; caches bf16.
+ *   partial quant, kv quant:     as above, plus kv_cache/kr_cache int8 with quant_scale_ckv
+ *                                (1, Hckv) and quant_scale_ckr (1, Dr) fp32 (value / scale,
+ *                                round half to even, saturate to [-128, 127]).
+ *   full quant:                  not implemented (MLAP_ERR_UNSUPPORTED).
+ * dequant_scale_x, dequant_scale_w_dq, dequant_scale_w_dkv_kr are reserved outside full quant
+ * and must be absent (data == NULL), else MLAP_ERR_UNSUPPORTED. */
+typedef struct {
+  mlap_tensor_t token_x;            /* bf16 (T, He) or (B, S, He) */
+  mlap_tensor_t weight_dq;          /* prepacked W^DQ; logical shape (He, Hcq) bf16 */
+  mlap_tensor_t weight_uq_qr;       /* prepacked [W^UQ|W^QR]; logical (Hcq, N*(D+Dr)) bf16|int8,
+                                       columns per head n: [D nope | Dr rope] */
+  mlap_tensor_t weight_uk;          /* prepacked W^UK; logical (N, D, Hckv) bf16 */
+  mlap_tensor_t weight_dkv_kr;      /* prepacked [W^DKV|W^KR]; logical (He, Hckv+Dr) bf16 */
+  mlap_tensor_t rmsnorm_gamma_cq;   /* bf16 (Hcq) */
+  mlap_tensor_t rmsnorm_gamma_ckv;  /* bf16 (Hckv) */
+  mlap_tensor_t rope_sin;           /* bf16 (T, Dr) or (B, S, Dr), half-and-half layout */
+  mlap_tensor_t rope_cos;           /* bf16, same shape as rope_sin */
+  mlap_tensor_t cache_index;        /* int64 (T) or (B, S); -1 = do not store this token */
+  mlap_tensor_t kv_cache;           /* in/out (BlockNum, BlockSize, 1, Hckv) bf16|int8 */
+  mlap_tensor_t kr_cache;           /* in/out (BlockNum, BlockSize, 1, Dr) bf16|int8 */
+  mlap_tensor_t dequant_scale_x;        /* reserved: must be absent */
+  mlap_tensor_t dequant_scale_w_dq;     /* reserved: must be absent */
+  mlap_tensor_t dequant_scale_w_uq_qr;  /* fp32 (1, N*(D+Dr)), partial quant only */
+  mlap_tensor_t dequant_scale_w_dkv_kr; /* reserved: must be absent */
+  mlap_tensor_t quant_scale_ckv;        /* fp32 (1, Hckv), int8 kv_cache only */
+  mlap_tensor_t quant_scale_ckr;        /* fp32 (1, Dr), int8 kr_cache only */
+  mlap_tensor_t smooth_scales_cq;       /* fp32 (1, Hcq), partial quant only */
+  mlap_tensor_t query;              /* out bf16 (T, N, Hckv) or (B, S, N, Hckv) = q^N */
+  mlap_tensor_t query_rope;         /* out bf16 (T, N, Dr) or (B, S, N, Dr) = q^R */
+  mlap_tensor_t dequant_scale_q_nope; /* out, full quant only; may be absent, never written */
+  double rmsnorm_epsilon_cq;
+  double rmsnorm_epsilon_ckv;
+  const char* cache_mode;           /* NULL or "PA_BSND" (ND paged cache); others unsupported */
+} mlap_args_t;
+
+/* Which weight a prepack call handles. */
+typedef enum {
+  MLAP_WEIGHT_DQ = 0,      /* (He, Hcq) */
+  MLAP_WEIGHT_UQ_QR = 1,   /* (Hcq, N*(D+Dr)), bf16 or int8 */
+  MLAP_WEIGHT_UK = 2,      /* (N, D, Hckv) */
+  MLAP_WEIGHT_DKV_KR = 3   /* (He, Hckv+Dr) */
+} mlap_weight_t;
+
+/* Bytes of device memory a prepacked copy of `w` needs.  `w` describes the row-major weight as
+ * the parameter table gives it ((k, n) for the matmul weights, 约束说明 "(k，n)"); N, D, Dr are
+ * the head geometry (used by MLAP_WEIGHT_UQ_QR and MLAP_WEIGHT_UK, ignored otherwise).
+ * w->data may be NULL here.  Errors: MLAP_ERR_NULL, MLAP_ERR_SHAPE, MLAP_ERR_DTYPE. */
+mlap_status_t mlap_prepack_size(const mlap_tensor_t* w, int32_t which, int32_t N, int32_t D,
+                                int32_t Dr, size_t* bytes);
+
+/* Repack a row-major device weight into the layout the kernels stream (K-major rows, the
+ * W^UQ|W^QR rows grouped as all nope rows then all rope rows with each RoPE pair adjacent,
+ * W^UK transposed per head).  Runs once per model load, asynchronously on `stream`; `dst` is a
+ * caller-owned device buffer of mlap_prepack_size() bytes and must not alias w->data.  The
+ * prepacked buffer is then passed in mlap_args_t with the ORIGINAL logical shape and dtype. */
+mlap_status_t mlap_prepack_weights(const mlap_tensor_t* w, int32_t which, int32_t N, int32_t D,
+                                   int32_t Dr, void* dst, void* stream);
+
+/* Phase 1 (validation and sizing; no device work, no CUDA context needed).  Checks every
+ * argument against the parameter table and the shape/dtype/scenario matrix and returns the
+ * workspace bytes execute needs for these shapes.  Errors: NULL, SHAPE, DTYPE, UNSUPPORTED. */
+mlap_status_t mlap_get_workspace_size(const mlap_args_t* args, size_t* bytes);
+
+/* Zero the workspace's error word and counters.  Call once after allocating a workspace (or
+ * cudaMemset the first 256 bytes to 0).  Asynchronous on `stream`. */
+mlap_status_t mlap_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Phase 2: run the prolog on `stream`.  Re-validates the arguments (same errors as phase 1),
+ * plus MLAP_ERR_WORKSPACE if workspace_bytes is below the phase-1 size, MLAP_ERR_CUDA if a launch
+ * fails.  T == 0: returns MLAP_OK with nothing launched.  BlockNum*BlockSize == 0: outputs are
+ * computed and the caches are not touched.  Writes query, query_rope and the cache rows named by
+ * cache_index; every other cache row stays bit-identical.  Indices outside [-1, BlockNum*
+ * BlockSize) are skipped and latched (see mlap_check_errors).  Indices must be unique (caller
+ * contract); with repeats the row stored in that slot is unspecified.  Results are bitwise
+ * deterministic for a given device and shapes.  The workspace must not be shared by calls that
+ * may run concurrently. */
+mlap_status_t mlap_execute(const mlap_args_t* args, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Synchronise `stream`, read and clear the workspace error word.  Returns MLAP_OK,
+ * MLAP_ERR_INDEX_RANGE or MLAP_ERR_TIMEOUT (index errors take precedence), or MLAP_ERR_CUDA. */
+mlap_status_t mlap_check_errors(void* workspace, void* stream);
+
+/* ============================================================================================ */
+/* QkvRmsNormRopeCache (aclnnQkvRmsNormRopeCache)                                                */
+/* ============================================================================================ */
+
+/* qkv (B, S, (Nq+Nk+Nv)*D) or (T, (Nq+Nk+Nv)*D), fp16 or bf16, D = 128 (the page: "Currently,
+ * only 128 is supported"), Nk == Nv.  Per token:
+ *   q, k, v = SplitVD(qkv);  q, k <- RoPE_half_and_half(RmsNorm(., gamma, epsilon), cos, sin);
+ *   q_out = q;  k_cache[index] = Quant(k);  v_cache[index] = Quant(v)
+ * Quant: none when k_scale/v_scale are absent (caches have qkv's dtype), symmetric
+ * (value / scale, round half to even, saturate to [-128,127]) when present (caches int8).
+ * Scales must be nonzero (caller contract, "Other restrictions"). */
+typedef struct {
+  mlap_tensor_t qkv;       /* fp16|bf16 */
+  mlap_tensor_t gamma_q;   /* (D), dtype of qkv, shared by all q heads */
+  mlap_tensor_t gamma_k;   /* (D), dtype of qkv, shared by all k heads */
+  mlap_tensor_t cos;       /* (T, D) or (B, S, D), dtype of qkv, shared by all heads */
+  mlap_tensor_t sin;       /* same as cos */
+  mlap_tensor_t index;     /* int64 (T) or (B, S); values in [-1, BlockNum*BlockSize), unique */
+  mlap_tensor_t k_cache;   /* in/out (BlockNum, BlockSize, Nk, D) int8 or dtype of qkv */
+  mlap_tensor_t v_cache;   /* in/out (BlockNum, BlockSize, Nv, D), same dtype as k_cache */
+  mlap_tensor_t k_scale;   /* fp32 (Nk, D) or absent */
+  mlap_tensor_t v_scale;   /* fp32 (Nv, D) or absent */
+  mlap_tensor_t k_offset;  /* asymmetric quant offsets: not implemented, must be absent */
+  mlap_tensor_t v_offset;  /* must be absent */
+  mlap_tensor_t q_out;     /* out (T, Nq, D) or (B, S, Nq, D), dtype of qkv */
+  int32_t Nq, Nk, Nv;
+  double epsilon;
+  const char* cache_mode;  /* NULL or "PA_BSND"; "PA_NZ" is unsupported */
+} qkvrnrc_args_t;
+
+/* Phase 1: validate and size.  BlockNum must satisfy BlockNum >= ceil(S/BlockSize)*B
+ * ("Input shape restrictions").  Errors: NULL, SHAPE, DTYPE, UNSUPPORTED. */
+mlap_status_t qkvrnrc_get_workspace_size(const qkvrnrc_args_t* args, size_t* bytes);
+
+/* Phase 2: run on `stream`.  Same workspace conventions as mlap_execute (initialise once with
+ * mlap_workspace_init; read index errors with mlap_check_errors). */
+mlap_status_t qkvrnrc_execute(const qkvrnrc_args_t* args, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* ============================================================================================ */
+/* Utilities                                                                                     */
+/* ============================================================================================ */
+
+/* Static string naming a status code. */
+const char* mlap_status_string(mlap_status_t status);
+
+/* Reason for the last non-OK status returned on this thread ("" if none). */
+const char* mlap_last_error(void);
+
+/* Per-kernel timing of mlap_execute for profiling (CUDA events recorded on the execute stream
+ * around each kernel).  mlap_timer_create makes a timer for up to max_calls timed calls;
+ * mlap_execute_timed is mlap_execute plus event records (it inserts no synchronisation);
+ * mlap_timer_read synchronises, writes the milliseconds of kernel k of call c to
+ * ms[c * MLAP_TIMER_PHASES + k] for the calls recorded so far, and resets the timer.
+ * Phases: 0 down-projection, 1 RmsNorm/RoPE/scatter, 2 up-projection, 3 absorb. */
+#define MLAP_TIMER_PHASES 4
+mlap_status_t mlap_timer_create(void** timer, int32_t max_calls);
+mlap_status_t mlap_execute_timed(const mlap_args_t* args, void* workspace,
+                                 size_t workspace_bytes, void* stream, void* timer);
+mlap_status_t mlap_timer_read(void* timer, float* ms, int32_t* calls_recorded);
+mlap_status_t mlap_timer_destroy(void* timer);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLAPROLOG_H */

@@ -1,0 +1,840 @@
+// libmlaprolog host API: argument validation against the operator documentation, workspace
+// planning, TMA descriptor encoding and the kernel launch sequence.
+//
+// Validation follows the MlaPrologV2 README parameter table (参数说明) and shape/dtype/scenario
+// matrix (约束说明), and the aclnnQkvRmsNormRopeCache "Input shape restrictions"; the two-phase
+// size-then-execute pattern follows the aclnn GetWorkspaceSize + execute pair.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "mlaprolog.h"
+
+using namespace mlap;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mlap_status_t fail(mlap_status_t code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+#define CHECK_STATUS(expr)              \
+  do {                                  \
+    mlap_status_t _s = (expr);          \
+    if (_s != MLAP_OK) return _s;       \
+  } while (0)
+
+size_t dtype_bytes(int32_t dt) {
+  switch (dt) {
+    case MLAP_DTYPE_BF16:
+    case MLAP_DTYPE_FP16: return 2;
+    case MLAP_DTYPE_FP32: return 4;
+    case MLAP_DTYPE_INT8: return 1;
+    case MLAP_DTYPE_INT64: return 8;
+    default: return 0;
+  }
+}
+
+int64_t numel(const mlap_tensor_t& t) {
+  int64_t n = 1;
+  for (int i = 0; i < t.ndim; ++i) n *= t.shape[i];
+  return n;
+}
+
+std::string shape_str(const mlap_tensor_t& t) {
+  std::string s = "(";
+  for (int i = 0; i < t.ndim; ++i) s += (i ? "," : "") + std::to_string(t.shape[i]);
+  return s + ")";
+}
+
+bool present(const mlap_tensor_t& t) { return t.data != nullptr; }
+
+mlap_status_t need(const mlap_tensor_t& t, const char* name, bool allow_empty) {
+  if (t.ndim < 0 || t.ndim > 4) return fail(MLAP_ERR_SHAPE, std::string(name) + ": ndim out of range");
+  for (int i = 0; i < t.ndim; ++i)
+    if (t.shape[i] < 0) return fail(MLAP_ERR_SHAPE, std::string(name) + ": negative dimension");
+  if (t.data == nullptr && !(allow_empty && numel(t) == 0))
+    return fail(MLAP_ERR_NULL, std::string(name) + " is NULL");
+  if (t.data != nullptr && (reinterpret_cast<uintptr_t>(t.data) & 15u) != 0)
+    return fail(MLAP_ERR_UNSUPPORTED, std::string(name) + ": data pointer not 16-byte aligned");
+  return MLAP_OK;
+}
+
+mlap_status_t want_dtype(const mlap_tensor_t& t, const char* name, int32_t dt) {
+  if (t.dtype != dt) return fail(MLAP_ERR_DTYPE, std::string(name) + ": unexpected dtype");
+  return MLAP_OK;
+}
+
+mlap_status_t want_shape(const mlap_tensor_t& t, const char* name, std::initializer_list<int64_t> s) {
+  bool ok = t.ndim == static_cast<int32_t>(s.size());
+  int i = 0;
+  for (int64_t d : s) {
+    if (!ok) break;
+    ok = t.shape[i++] == d;
+  }
+  if (!ok) return fail(MLAP_ERR_SHAPE, std::string(name) + ": shape " + shape_str(t) + " does not match");
+  return MLAP_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ----------------------------------------------------------------------------------------------
+// MLA prolog shapes
+struct MlaDims {
+  int64_t T, B, S;
+  bool bsh;
+  int64_t He, Hcq, Hckv, N, D, Dr, BlockNum, BlockSize;
+  bool w_int8, kv_int8, kr_int8;
+};
+
+constexpr int kSwapMaxT = 256;   // decode orientation (weights as MMA rows) up to this many tokens
+constexpr int kMaxSplits = 16;
+
+mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
+  if (a == nullptr) return fail(MLAP_ERR_NULL, "args is NULL");
+  const mlap_tensor_t& x = a->token_x;
+  // token_x: (T, He) or (B, S, He)  (约束说明: BS合轴 or not)
+  if (x.ndim == 2) {
+    d->bsh = false;
+    d->T = x.shape[0];
+    d->B = x.shape[0];
+    d->S = 1;
+    d->He = x.shape[1];
+  } else if (x.ndim == 3) {
+    d->bsh = true;
+    d->B = x.shape[0];
+    d->S = x.shape[1];
+    d->T = d->B * d->S;
+    d->He = x.shape[2];
+  } else {
+    return fail(MLAP_ERR_SHAPE, "token_x must be (T, He) or (B, S, He)");
+  }
+  CHECK_STATUS(need(x, "token_x", true));
+  if (x.dtype == MLAP_DTYPE_INT8)
+    return fail(MLAP_ERR_UNSUPPORTED, "int8 token_x is the full-quant scenario (not implemented)");
+  CHECK_STATUS(want_dtype(x, "token_x", MLAP_DTYPE_BF16));
+
+  // weights (logical shapes (k, n); data = prepacked buffers)
+  const mlap_tensor_t& wdq = a->weight_dq;
+  CHECK_STATUS(need(wdq, "weight_dq", false));
+  if (wdq.dtype == MLAP_DTYPE_INT8)
+    return fail(MLAP_ERR_UNSUPPORTED, "int8 weight_dq is the full-quant scenario (not implemented)");
+  CHECK_STATUS(want_dtype(wdq, "weight_dq", MLAP_DTYPE_BF16));
+  if (wdq.ndim != 2 || wdq.shape[0] != d->He) return fail(MLAP_ERR_SHAPE, "weight_dq must be (He, Hcq)");
+  d->Hcq = wdq.shape[1];
+
+  const mlap_tensor_t& wuk = a->weight_uk;
+  CHECK_STATUS(need(wuk, "weight_uk", false));
+  CHECK_STATUS(want_dtype(wuk, "weight_uk", MLAP_DTYPE_BF16));
+  if (wuk.ndim != 3) return fail(MLAP_ERR_SHAPE, "weight_uk must be (N, D, Hckv)");
+  d->N = wuk.shape[0];
+  d->D = wuk.shape[1];
+  d->Hckv = wuk.shape[2];
+
+  const mlap_tensor_t& sn = a->rope_sin;
+  CHECK_STATUS(need(sn, "rope_sin", true));
+  if (sn.ndim < 1) return fail(MLAP_ERR_SHAPE, "rope_sin must be (T, Dr) or (B, S, Dr)");
+  d->Dr = sn.shape[sn.ndim - 1];
+
+  if (d->D != 128) return fail(MLAP_ERR_UNSUPPORTED, "D (weight_uk dim 1) must be 128");
+  if (d->Dr <= 0 || (d->Dr & 1)) return fail(MLAP_ERR_UNSUPPORTED, "Dr must be positive and even");
+  if (d->N <= 0 || d->Hckv <= 0 || d->Hcq <= 0 || d->He <= 0)
+    return fail(MLAP_ERR_SHAPE, "N, Hckv, Hcq and He must be positive");
+  if ((d->He % 8) || (d->Hcq % 8))
+    return fail(MLAP_ERR_UNSUPPORTED, "He and Hcq must be multiples of 8 (16-byte TMA row pitch)");
+
+  const mlap_tensor_t& wuq = a->weight_uq_qr;
+  CHECK_STATUS(need(wuq, "weight_uq_qr", false));
+  CHECK_STATUS(want_shape(wuq, "weight_uq_qr", {d->Hcq, d->N * (d->D + d->Dr)}));
+  if (wuq.dtype == MLAP_DTYPE_INT8) d->w_int8 = true;
+  else if (wuq.dtype == MLAP_DTYPE_BF16) d->w_int8 = false;
+  else return fail(MLAP_ERR_DTYPE, "weight_uq_qr must be bf16 or int8");
+
+  const mlap_tensor_t& wkv = a->weight_dkv_kr;
+  CHECK_STATUS(need(wkv, "weight_dkv_kr", false));
+  if (wkv.dtype == MLAP_DTYPE_INT8)
+    return fail(MLAP_ERR_UNSUPPORTED, "int8 weight_dkv_kr is the full-quant scenario (not implemented)");
+  CHECK_STATUS(want_dtype(wkv, "weight_dkv_kr", MLAP_DTYPE_BF16));
+  CHECK_STATUS(want_shape(wkv, "weight_dkv_kr", {d->He, d->Hckv + d->Dr}));
+
+  CHECK_STATUS(need(a->rmsnorm_gamma_cq, "rmsnorm_gamma_cq", false));
+  CHECK_STATUS(want_dtype(a->rmsnorm_gamma_cq, "rmsnorm_gamma_cq", MLAP_DTYPE_BF16));
+  CHECK_STATUS(want_shape(a->rmsnorm_gamma_cq, "rmsnorm_gamma_cq", {d->Hcq}));
+  CHECK_STATUS(need(a->rmsnorm_gamma_ckv, "rmsnorm_gamma_ckv", false));
+  CHECK_STATUS(want_dtype(a->rmsnorm_gamma_ckv, "rmsnorm_gamma_ckv", MLAP_DTYPE_BF16));
+  CHECK_STATUS(want_shape(a->rmsnorm_gamma_ckv, "rmsnorm_gamma_ckv", {d->Hckv}));
+
+  // token-shaped inputs / outputs: BSH or TND, all in the same form as token_x
+  const mlap_tensor_t& cs = a->rope_cos;
+  CHECK_STATUS(need(cs, "rope_cos", true));
+  CHECK_STATUS(want_dtype(sn, "rope_sin", MLAP_DTYPE_BF16));
+  CHECK_STATUS(want_dtype(cs, "rope_cos", MLAP_DTYPE_BF16));
+  const mlap_tensor_t& ci = a->cache_index;
+  CHECK_STATUS(need(ci, "cache_index", true));
+  CHECK_STATUS(want_dtype(ci, "cache_index", MLAP_DTYPE_INT64));
+  const mlap_tensor_t& q = a->query;
+  const mlap_tensor_t& qr = a->query_rope;
+  CHECK_STATUS(need(q, "query", true));
+  CHECK_STATUS(need(qr, "query_rope", true));
+  if (q.dtype == MLAP_DTYPE_INT8)
+    return fail(MLAP_ERR_UNSUPPORTED, "int8 query is the full-quant scenario (not implemented)");
+  CHECK_STATUS(want_dtype(q, "query", MLAP_DTYPE_BF16));
+  CHECK_STATUS(want_dtype(qr, "query_rope", MLAP_DTYPE_BF16));
+  if (d->bsh) {
+    CHECK_STATUS(want_shape(sn, "rope_sin", {d->B, d->S, d->Dr}));
+    CHECK_STATUS(want_shape(cs, "rope_cos", {d->B, d->S, d->Dr}));
+    CHECK_STATUS(want_shape(ci, "cache_index", {d->B, d->S}));
+    CHECK_STATUS(want_shape(q, "query", {d->B, d->S, d->N, d->Hckv}));
+    CHECK_STATUS(want_shape(qr, "query_rope", {d->B, d->S, d->N, d->Dr}));
+  } else {
+    CHECK_STATUS(want_shape(sn, "rope_sin", {d->T, d->Dr}));
+    CHECK_STATUS(want_shape(cs, "rope_cos", {d->T, d->Dr}));
+    CHECK_STATUS(want_shape(ci, "cache_index", {d->T}));
+    CHECK_STATUS(want_shape(q, "query", {d->T, d->N, d->Hckv}));
+    CHECK_STATUS(want_shape(qr, "query_rope", {d->T, d->N, d->Dr}));
+  }
+
+  // caches (BlockNum, BlockSize, Nkv = 1, H)
+  const mlap_tensor_t& kv = a->kv_cache;
+  const mlap_tensor_t& kr = a->kr_cache;
+  if (kv.ndim != 4 || kr.ndim != 4) return fail(MLAP_ERR_SHAPE, "caches must be (BlockNum, BlockSize, Nkv, H)");
+  d->BlockNum = kv.shape[0];
+  d->BlockSize = kv.shape[1];
+  CHECK_STATUS(need(kv, "kv_cache", true));
+  CHECK_STATUS(need(kr, "kr_cache", true));
+  if (kv.shape[2] != 1 || kr.shape[2] != 1) return fail(MLAP_ERR_UNSUPPORTED, "Nkv must be 1");
+  CHECK_STATUS(want_shape(kv, "kv_cache", {d->BlockNum, d->BlockSize, 1, d->Hckv}));
+  CHECK_STATUS(want_shape(kr, "kr_cache", {d->BlockNum, d->BlockSize, 1, d->Dr}));
+  auto cache_dt = [](const mlap_tensor_t& c, const char* n, bool* i8) -> mlap_status_t {
+    if (c.dtype == MLAP_DTYPE_INT8) *i8 = true;
+    else if (c.dtype == MLAP_DTYPE_BF16) *i8 = false;
+    else return fail(MLAP_ERR_DTYPE, std::string(n) + " must be bf16 or int8");
+    return MLAP_OK;
+  };
+  CHECK_STATUS(cache_dt(kv, "kv_cache", &d->kv_int8));
+  CHECK_STATUS(cache_dt(kr, "kr_cache", &d->kr_int8));
+
+  // scenario matrix (约束说明)
+  if (present(a->dequant_scale_x) || present(a->dequant_scale_w_dq) ||
+      present(a->dequant_scale_w_dkv_kr))
+    return fail(MLAP_ERR_UNSUPPORTED,
+                "dequant_scale_x / _w_dq / _w_dkv_kr are reserved outside full quant and must be NULL");
+  if (d->kv_int8 != d->kr_int8)
+    return fail(MLAP_ERR_UNSUPPORTED, "kv_cache and kr_cache must both be int8 or both bf16 outside full quant");
+  if (d->w_int8) {
+    CHECK_STATUS(need(a->dequant_scale_w_uq_qr, "dequant_scale_w_uq_qr", false));
+    CHECK_STATUS(want_dtype(a->dequant_scale_w_uq_qr, "dequant_scale_w_uq_qr", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_shape(a->dequant_scale_w_uq_qr, "dequant_scale_w_uq_qr", {1, d->N * (d->D + d->Dr)}));
+    CHECK_STATUS(need(a->smooth_scales_cq, "smooth_scales_cq", false));
+    CHECK_STATUS(want_dtype(a->smooth_scales_cq, "smooth_scales_cq", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_shape(a->smooth_scales_cq, "smooth_scales_cq", {1, d->Hcq}));
+  } else {
+    if (present(a->dequant_scale_w_uq_qr) || present(a->smooth_scales_cq))
+      return fail(MLAP_ERR_UNSUPPORTED, "dequant_scale_w_uq_qr / smooth_scales_cq need an int8 weight_uq_qr");
+    if (d->kv_int8) return fail(MLAP_ERR_UNSUPPORTED, "int8 caches need the partial-quant scenario");
+  }
+  if (d->kv_int8) {
+    CHECK_STATUS(need(a->quant_scale_ckv, "quant_scale_ckv", false));
+    CHECK_STATUS(want_dtype(a->quant_scale_ckv, "quant_scale_ckv", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_shape(a->quant_scale_ckv, "quant_scale_ckv", {1, d->Hckv}));
+    CHECK_STATUS(need(a->quant_scale_ckr, "quant_scale_ckr", false));
+    CHECK_STATUS(want_dtype(a->quant_scale_ckr, "quant_scale_ckr", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_shape(a->quant_scale_ckr, "quant_scale_ckr", {1, d->Dr}));
+  } else if (present(a->quant_scale_ckv) || present(a->quant_scale_ckr)) {
+    return fail(MLAP_ERR_UNSUPPORTED, "quant_scale_ckv / quant_scale_ckr need int8 caches");
+  }
+  if (a->cache_mode != nullptr && std::strcmp(a->cache_mode, "PA_BSND") != 0)
+    return fail(MLAP_ERR_UNSUPPORTED, std::string("cache_mode '") + a->cache_mode + "' not supported (PA_BSND only)");
+  if (!(a->rmsnorm_epsilon_cq >= 0.0) || !(a->rmsnorm_epsilon_ckv >= 0.0))
+    return fail(MLAP_ERR_SHAPE, "rmsnorm epsilons must be non-negative");
+  if (d->T > (int64_t(1) << 30)) return fail(MLAP_ERR_UNSUPPORTED, "too many tokens");
+  return MLAP_OK;
+}
+
+struct MlaWs {
+  size_t part, cq, qc, scale, total;
+  int split_cap;
+};
+
+MlaWs mla_ws_layout(const MlaDims& d) {
+  MlaWs w;
+  const bool swap = d.T <= kSwapMaxT;
+  w.split_cap = swap ? kMaxSplits : 1;
+  const int64_t ntot = d.Hcq + d.Hckv + d.Dr;
+  size_t off = 256;   // error word and spare header
+  w.part = off;
+  off += align_up(static_cast<size_t>(w.split_cap) * d.T * ntot * 4, 256);
+  w.cq = off;
+  off += align_up(static_cast<size_t>(d.T) * d.Hcq * 2, 256);
+  w.qc = off;
+  off += align_up(static_cast<size_t>(d.T) * d.N * d.D * 2, 256);
+  w.scale = off;
+  off += align_up(static_cast<size_t>(d.T) * 4, 256);
+  w.total = off;
+  return w;
+}
+
+// ----------------------------------------------------------------------------------------------
+// TMA descriptors
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D K-major bf16 operand: `rows` rows of `inner` elements, `pitch` elements apart; box of
+// 64 elements x box_rows rows, 128-byte swizzle, zero fill outside the tensor.
+mlap_status_t make_tmap(CUtensorMap* m, const void* base, int64_t inner, int64_t rows,
+                        int64_t pitch_elems, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return fail(MLAP_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MLAP_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string(int(r)) + ")");
+  return MLAP_OK;
+}
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+int swap_bn(int64_t T) {
+  int bn = 16;
+  while (bn < T) bn *= 2;
+  return bn;
+}
+
+mlap_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(MLAP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct Timer {
+  std::vector<cudaEvent_t> ev;   // (MLAP_TIMER_PHASES + 1) per call
+  int max_calls = 0;
+  int calls = 0;
+};
+
+mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStream_t stream,
+                      Timer* timer) {
+  MlaDims d;
+  CHECK_STATUS(validate_mla(a, &d));
+  if (d.T == 0) return MLAP_OK;
+  const MlaWs L = mla_ws_layout(d);
+  if (ws == nullptr || ws_bytes < L.total) return fail(MLAP_ERR_WORKSPACE, "workspace too small");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(MLAP_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (d.w_int8) return fail(MLAP_ERR_UNSUPPORTED, "int8 weight_uq_qr path not built yet");
+
+  int dev = 0, sms = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "device query");
+
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  uint32_t* err = reinterpret_cast<uint32_t*>(wsb);
+  float* part = reinterpret_cast<float*>(wsb + L.part);
+  __nv_bfloat16* cq = reinterpret_cast<__nv_bfloat16*>(wsb + L.cq);
+  __nv_bfloat16* qc = reinterpret_cast<__nv_bfloat16*>(wsb + L.qc);
+  float* scale_t = reinterpret_cast<float*>(wsb + L.scale);
+
+  const bool swap = d.T <= kSwapMaxT;
+  const int64_t Ntot = d.Hcq + d.Hckv + d.Dr;
+  const int64_t Mup = d.N * (d.D + d.Dr);
+  const int64_t slots = d.BlockNum * d.BlockSize;
+  const int bn_t = swap_bn(d.T);
+
+  auto rec = [&](int phase) -> mlap_status_t {
+    if (timer == nullptr) return MLAP_OK;
+    cudaError_t e = cudaEventRecord(timer->ev[timer->calls * (MLAP_TIMER_PHASES + 1) + phase], stream);
+    return e == cudaSuccess ? MLAP_OK : cuda_fail(e, "cudaEventRecord");
+  };
+  if (timer != nullptr && timer->calls >= timer->max_calls) return fail(MLAP_ERR_UNSUPPORTED, "timer full");
+
+  // ---- 1. down-projection x·[W^DQ | W^DKV|W^KR]  (fp32 K-split partials)
+  GemmLaunch g{};
+  g.stream = stream;
+  g.pdl = true;
+  g.err = err;
+  g.swap = swap;
+  DownParams dp{part, static_cast<int32_t>(d.T), static_cast<int32_t>(d.Hcq),
+                static_cast<int32_t>(d.Hckv + d.Dr), static_cast<int32_t>(Ntot), 0};
+  {
+    const int kb = ceil_div(d.He, 64);
+    if (swap) {
+      const int seg = ceil_div(d.Hcq, 128);
+      CHECK_STATUS(make_tmap(&g.a0, a->weight_dq.data, d.He, d.Hcq, d.He, 128));
+      CHECK_STATUS(make_tmap(&g.a1, a->weight_dkv_kr.data, d.He, d.Hckv + d.Dr, d.He, 128));
+      CHECK_STATUS(make_tmap(&g.b0, a->token_x.data, d.He, d.T, d.He, bn_t));
+      g.b1 = g.b0;
+      g.bn = bn_t;
+      g.geo.m_tiles = seg + ceil_div(d.Hckv + d.Dr, 128);
+      g.geo.n_tiles = 1;
+      g.geo.a_seg_tiles = seg;
+      g.geo.b_seg_tiles = 1;
+      int splits = sms / g.geo.m_tiles;
+      if (splits > L.split_cap) splits = L.split_cap;
+      if (splits > kb) splits = kb;
+      if (splits < 1) splits = 1;
+      g.geo.splits = splits;
+      dp.seg_tiles = seg;
+    } else {
+      const int seg = ceil_div(d.Hcq, 192);
+      CHECK_STATUS(make_tmap(&g.a0, a->token_x.data, d.He, d.T, d.He, 128));
+      g.a1 = g.a0;
+      CHECK_STATUS(make_tmap(&g.b0, a->weight_dq.data, d.He, d.Hcq, d.He, 192));
+      CHECK_STATUS(make_tmap(&g.b1, a->weight_dkv_kr.data, d.He, d.Hckv + d.Dr, d.He, 192));
+      g.bn = 192;
+      g.geo.m_tiles = ceil_div(d.T, 128);
+      g.geo.n_tiles = seg + ceil_div(d.Hckv + d.Dr, 192);
+      g.geo.a_seg_tiles = g.geo.m_tiles;
+      g.geo.b_seg_tiles = seg;
+      g.geo.splits = 1;
+      dp.seg_tiles = seg;
+    }
+    g.geo.batches = 1;
+    g.geo.k_blocks = kb;
+    g.geo.num_units = g.geo.m_tiles * g.geo.n_tiles * g.geo.splits;
+    g.grid = g.geo.num_units < sms ? g.geo.num_units : sms;
+    CHECK_STATUS(rec(0));
+    ce = launch_down(g, dp);
+    if (ce != cudaSuccess) return cuda_fail(ce, "down-projection launch");
+  }
+
+  // ---- 2. RmsNorm(c^Q), RmsNorm(c^KV), RoPE(k^R), cache quant + scatter
+  {
+    FinalizeParams fp{};
+    fp.part = part;
+    fp.splits = g.geo.splits;
+    fp.T = static_cast<int32_t>(d.T);
+    fp.Hcq = static_cast<int32_t>(d.Hcq);
+    fp.Hckv = static_cast<int32_t>(d.Hckv);
+    fp.Dr = static_cast<int32_t>(d.Dr);
+    fp.Ntot = static_cast<int32_t>(Ntot);
+    fp.gamma_cq = static_cast<const __nv_bfloat16*>(a->rmsnorm_gamma_cq.data);
+    fp.gamma_ckv = static_cast<const __nv_bfloat16*>(a->rmsnorm_gamma_ckv.data);
+    fp.eps_cq = static_cast<float>(a->rmsnorm_epsilon_cq);
+    fp.eps_ckv = static_cast<float>(a->rmsnorm_epsilon_ckv);
+    fp.cos = static_cast<const __nv_bfloat16*>(a->rope_cos.data);
+    fp.sin = static_cast<const __nv_bfloat16*>(a->rope_sin.data);
+    fp.cache_index = static_cast<const int64_t*>(a->cache_index.data);
+    fp.slots = slots;
+    fp.kv_cache = a->kv_cache.data;
+    fp.kr_cache = a->kr_cache.data;
+    fp.kv_int8 = d.kv_int8;
+    fp.kr_int8 = d.kr_int8;
+    fp.qs_ckv = static_cast<const float*>(a->quant_scale_ckv.data);
+    fp.qs_ckr = static_cast<const float*>(a->quant_scale_ckr.data);
+    fp.cq_out = cq;
+    fp.smooth = d.w_int8 ? static_cast<const float*>(a->smooth_scales_cq.data) : nullptr;
+    fp.scale_t = scale_t;
+    fp.err = err;
+    CHECK_STATUS(rec(1));
+    ce = launch_finalize(fp, stream, true);
+    if (ce != cudaSuccess) return cuda_fail(ce, "norm/rope/scatter launch");
+  }
+
+  // ---- 3. up-projection c^Q·[W^UQ|W^QR] -> q^C (bf16 workspace) and query_rope
+  {
+    GemmLaunch u{};
+    u.stream = stream;
+    u.pdl = true;
+    u.err = err;
+    u.swap = swap;
+    if (swap) {
+      CHECK_STATUS(make_tmap(&u.a0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 128));
+      u.a1 = u.a0;
+      CHECK_STATUS(make_tmap(&u.b0, cq, d.Hcq, d.T, d.Hcq, bn_t));
+      u.b1 = u.b0;
+      u.bn = bn_t;
+      u.geo.m_tiles = ceil_div(Mup, 128);
+      u.geo.n_tiles = 1;
+    } else {
+      CHECK_STATUS(make_tmap(&u.a0, cq, d.Hcq, d.T, d.Hcq, 128));
+      u.a1 = u.a0;
+      CHECK_STATUS(make_tmap(&u.b0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 256));
+      u.b1 = u.b0;
+      u.bn = 256;
+      u.geo.m_tiles = ceil_div(d.T, 128);
+      u.geo.n_tiles = ceil_div(Mup, 256);
+    }
+    u.geo.a_seg_tiles = u.geo.m_tiles;
+    u.geo.b_seg_tiles = u.geo.n_tiles;
+    u.geo.batches = 1;
+    u.geo.splits = 1;
+    u.geo.k_blocks = ceil_div(d.Hcq, 64);
+    u.geo.num_units = u.geo.m_tiles * u.geo.n_tiles;
+    u.grid = u.geo.num_units < sms ? u.geo.num_units : sms;
+    UpParams up{qc,
+                static_cast<__nv_bfloat16*>(a->query_rope.data),
+                static_cast<const __nv_bfloat16*>(a->rope_cos.data),
+                static_cast<const __nv_bfloat16*>(a->rope_sin.data),
+                scale_t,
+                static_cast<const float*>(a->dequant_scale_w_uq_qr.data),
+                static_cast<int32_t>(d.T), static_cast<int32_t>(d.N), static_cast<int32_t>(d.D),
+                static_cast<int32_t>(d.Dr)};
+    CHECK_STATUS(rec(2));
+    ce = launch_up(u, up, d.w_int8);
+    if (ce != cudaSuccess) return cuda_fail(ce, "up-projection launch");
+  }
+
+  // ---- 4. absorb q^N = q^C · W^UK per head -> query
+  {
+    GemmLaunch b{};
+    b.stream = stream;
+    b.pdl = true;
+    b.err = err;
+    b.swap = swap;
+    if (swap) {
+      CHECK_STATUS(make_tmap(&b.a0, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, 128));
+      b.a1 = b.a0;
+      CHECK_STATUS(make_tmap(&b.b0, qc, d.N * d.D, d.T, d.N * d.D, bn_t));
+      b.b1 = b.b0;
+      b.bn = bn_t;
+      b.geo.m_tiles = ceil_div(d.Hckv, 128);
+      b.geo.n_tiles = 1;
+      b.geo.a_x_batch = 0;
+      b.geo.a_y_batch = static_cast<int32_t>(d.Hckv);
+      b.geo.b_x_batch = static_cast<int32_t>(d.D);
+      b.geo.b_y_batch = 0;
+    } else {
+      CHECK_STATUS(make_tmap(&b.a0, qc, d.N * d.D, d.T, d.N * d.D, 128));
+      b.a1 = b.a0;
+      CHECK_STATUS(make_tmap(&b.b0, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, 256));
+      b.b1 = b.b0;
+      b.bn = 256;
+      b.geo.m_tiles = ceil_div(d.T, 128);
+      b.geo.n_tiles = ceil_div(d.Hckv, 256);
+      b.geo.a_x_batch = static_cast<int32_t>(d.D);
+      b.geo.a_y_batch = 0;
+      b.geo.b_x_batch = 0;
+      b.geo.b_y_batch = static_cast<int32_t>(d.Hckv);
+    }
+    b.geo.a_seg_tiles = b.geo.m_tiles;
+    b.geo.b_seg_tiles = b.geo.n_tiles;
+    b.geo.batches = static_cast<int32_t>(d.N);
+    b.geo.splits = 1;
+    b.geo.k_blocks = ceil_div(d.D, 64);
+    b.geo.num_units = b.geo.m_tiles * b.geo.n_tiles * b.geo.batches;
+    b.grid = b.geo.num_units < sms ? b.geo.num_units : sms;
+    AbsorbParams ap{static_cast<__nv_bfloat16*>(a->query.data), static_cast<int32_t>(d.T),
+                    static_cast<int32_t>(d.N), static_cast<int32_t>(d.Hckv)};
+    CHECK_STATUS(rec(3));
+    ce = launch_absorb(b, ap);
+    if (ce != cudaSuccess) return cuda_fail(ce, "absorb launch");
+    CHECK_STATUS(rec(4));
+  }
+  if (timer != nullptr) timer->calls++;
+  return MLAP_OK;
+}
+
+// ----------------------------------------------------------------------------------------------
+// QkvRmsNormRopeCache
+struct QkvDims {
+  int64_t T, B, S;
+  bool bsh;
+  int64_t D, BlockNum, BlockSize;
+  bool quant, bf16;
+};
+
+mlap_status_t validate_qkv(const qkvrnrc_args_t* a, QkvDims* d) {
+  if (a == nullptr) return fail(MLAP_ERR_NULL, "args is NULL");
+  const int64_t Nq = a->Nq, Nk = a->Nk, Nv = a->Nv;
+  if (Nq <= 0 || Nk <= 0 || Nv <= 0) return fail(MLAP_ERR_SHAPE, "Nq, Nk, Nv must be positive");
+  if (Nk != Nv) return fail(MLAP_ERR_SHAPE, "SplitVD requires Nk == Nv");
+  const mlap_tensor_t& x = a->qkv;
+  int64_t width;
+  if (x.ndim == 2) {
+    d->bsh = false; d->T = x.shape[0]; d->B = x.shape[0]; d->S = 1; width = x.shape[1];
+  } else if (x.ndim == 3) {
+    d->bsh = true; d->B = x.shape[0]; d->S = x.shape[1]; d->T = d->B * d->S; width = x.shape[2];
+  } else {
+    return fail(MLAP_ERR_SHAPE, "qkv must be (T, Nqkv*D) or (B, S, Nqkv*D)");
+  }
+  CHECK_STATUS(need(x, "qkv", true));
+  if (x.dtype == MLAP_DTYPE_FP16) d->bf16 = false;
+  else if (x.dtype == MLAP_DTYPE_BF16) d->bf16 = true;
+  else return fail(MLAP_ERR_DTYPE, "qkv must be fp16 or bf16");
+  if (width % (Nq + Nk + Nv)) return fail(MLAP_ERR_SHAPE, "qkv width is not a multiple of Nq+Nk+Nv");
+  d->D = width / (Nq + Nk + Nv);
+  if (d->D != 128) return fail(MLAP_ERR_UNSUPPORTED, "head dim D must be 128");
+  for (auto* pr : {&a->gamma_q, &a->gamma_k}) {
+    CHECK_STATUS(need(*pr, "gamma", false));
+    CHECK_STATUS(want_dtype(*pr, "gamma", x.dtype));
+    CHECK_STATUS(want_shape(*pr, "gamma", {d->D}));
+  }
+  for (auto* pr : {&a->cos, &a->sin}) {
+    CHECK_STATUS(need(*pr, "cos/sin", true));
+    CHECK_STATUS(want_dtype(*pr, "cos/sin", x.dtype));
+    if (d->bsh) CHECK_STATUS(want_shape(*pr, "cos/sin", {d->B, d->S, d->D}));
+    else CHECK_STATUS(want_shape(*pr, "cos/sin", {d->T, d->D}));
+  }
+  CHECK_STATUS(need(a->index, "index", true));
+  CHECK_STATUS(want_dtype(a->index, "index", MLAP_DTYPE_INT64));
+  if (d->bsh) CHECK_STATUS(want_shape(a->index, "index", {d->B, d->S}));
+  else CHECK_STATUS(want_shape(a->index, "index", {d->T}));
+  CHECK_STATUS(need(a->q_out, "q_out", true));
+  CHECK_STATUS(want_dtype(a->q_out, "q_out", x.dtype));
+  if (d->bsh) CHECK_STATUS(want_shape(a->q_out, "q_out", {d->B, d->S, Nq, d->D}));
+  else CHECK_STATUS(want_shape(a->q_out, "q_out", {d->T, Nq, d->D}));
+  const mlap_tensor_t& kc = a->k_cache;
+  const mlap_tensor_t& vc = a->v_cache;
+  if (kc.ndim != 4 || vc.ndim != 4) return fail(MLAP_ERR_SHAPE, "caches must be (BlockNum, BlockSize, N, D)");
+  d->BlockNum = kc.shape[0];
+  d->BlockSize = kc.shape[1];
+  CHECK_STATUS(need(kc, "k_cache", true));
+  CHECK_STATUS(need(vc, "v_cache", true));
+  CHECK_STATUS(want_shape(kc, "k_cache", {d->BlockNum, d->BlockSize, Nk, d->D}));
+  CHECK_STATUS(want_shape(vc, "v_cache", {d->BlockNum, d->BlockSize, Nv, d->D}));
+  if (kc.dtype != vc.dtype) return fail(MLAP_ERR_DTYPE, "k_cache and v_cache dtypes differ");
+  if (present(a->k_offset) || present(a->v_offset))
+    return fail(MLAP_ERR_UNSUPPORTED, "asymmetric quant (k_offset / v_offset) not implemented");
+  d->quant = present(a->k_scale) || present(a->v_scale);
+  if (d->quant) {
+    CHECK_STATUS(want_dtype(kc, "k_cache", MLAP_DTYPE_INT8));
+    CHECK_STATUS(need(a->k_scale, "k_scale", false));
+    CHECK_STATUS(need(a->v_scale, "v_scale", false));
+    CHECK_STATUS(want_dtype(a->k_scale, "k_scale", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_dtype(a->v_scale, "v_scale", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_shape(a->k_scale, "k_scale", {Nk, d->D}));
+    CHECK_STATUS(want_shape(a->v_scale, "v_scale", {Nv, d->D}));
+  } else {
+    CHECK_STATUS(want_dtype(kc, "k_cache", x.dtype));
+  }
+  if (a->cache_mode != nullptr && std::strcmp(a->cache_mode, "PA_BSND") != 0)
+    return fail(MLAP_ERR_UNSUPPORTED, std::string("cache_mode '") + a->cache_mode + "' not supported (PA_BSND only)");
+  if (d->bsh && d->BlockSize > 0 && d->T > 0 &&
+      d->BlockNum < (d->S + d->BlockSize - 1) / d->BlockSize * d->B)
+    return fail(MLAP_ERR_SHAPE, "BlockNum must be >= ceil(S / BlockSize) * B");
+  if (!(a->epsilon >= 0.0)) return fail(MLAP_ERR_SHAPE, "epsilon must be non-negative");
+  return MLAP_OK;
+}
+
+}  // namespace
+
+// ================================================================================================
+extern "C" {
+
+const char* mlap_status_string(mlap_status_t s) {
+  switch (s) {
+    case MLAP_OK: return "MLAP_OK";
+    case MLAP_ERR_NULL: return "MLAP_ERR_NULL";
+    case MLAP_ERR_SHAPE: return "MLAP_ERR_SHAPE";
+    case MLAP_ERR_DTYPE: return "MLAP_ERR_DTYPE";
+    case MLAP_ERR_UNSUPPORTED: return "MLAP_ERR_UNSUPPORTED";
+    case MLAP_ERR_WORKSPACE: return "MLAP_ERR_WORKSPACE";
+    case MLAP_ERR_CUDA: return "MLAP_ERR_CUDA";
+    case MLAP_ERR_INDEX_RANGE: return "MLAP_ERR_INDEX_RANGE";
+    case MLAP_ERR_TIMEOUT: return "MLAP_ERR_TIMEOUT";
+    default: return "MLAP_ERR_UNKNOWN";
+  }
+}
+
+const char* mlap_last_error(void) { return g_last_error.c_str(); }
+
+mlap_status_t mlap_prepack_size(const mlap_tensor_t* w, int32_t which, int32_t N, int32_t D,
+                                int32_t Dr, size_t* bytes) {
+  if (w == nullptr || bytes == nullptr) return fail(MLAP_ERR_NULL, "NULL argument");
+  const size_t eb = dtype_bytes(w->dtype);
+  switch (which) {
+    case MLAP_WEIGHT_DQ:
+    case MLAP_WEIGHT_DKV_KR:
+      if (w->dtype != MLAP_DTYPE_BF16) return fail(MLAP_ERR_DTYPE, "weight must be bf16");
+      if (w->ndim != 2) return fail(MLAP_ERR_SHAPE, "weight must be 2-D (k, n)");
+      break;
+    case MLAP_WEIGHT_UQ_QR:
+      if (w->dtype != MLAP_DTYPE_BF16 && w->dtype != MLAP_DTYPE_INT8)
+        return fail(MLAP_ERR_DTYPE, "weight_uq_qr must be bf16 or int8");
+      if (w->ndim != 2 || N <= 0 || D <= 0 || Dr <= 0 || (Dr & 1) ||
+          w->shape[1] != int64_t(N) * (D + Dr))
+        return fail(MLAP_ERR_SHAPE, "weight_uq_qr must be (Hcq, N*(D+Dr)) with even Dr");
+      break;
+    case MLAP_WEIGHT_UK:
+      if (w->dtype != MLAP_DTYPE_BF16) return fail(MLAP_ERR_DTYPE, "weight_uk must be bf16");
+      if (w->ndim != 3) return fail(MLAP_ERR_SHAPE, "weight_uk must be (N, D, Hckv)");
+      break;
+    default:
+      return fail(MLAP_ERR_UNSUPPORTED, "unknown weight id");
+  }
+  for (int i = 0; i < w->ndim; ++i)
+    if (w->shape[i] <= 0) return fail(MLAP_ERR_SHAPE, "weight dimensions must be positive");
+  *bytes = static_cast<size_t>(numel(*w)) * eb;
+  return MLAP_OK;
+}
+
+mlap_status_t mlap_prepack_weights(const mlap_tensor_t* w, int32_t which, int32_t N, int32_t D,
+                                   int32_t Dr, void* dst, void* stream) {
+  size_t bytes = 0;
+  CHECK_STATUS(mlap_prepack_size(w, which, N, D, Dr, &bytes));
+  if (w->data == nullptr || dst == nullptr) return fail(MLAP_ERR_NULL, "NULL weight or destination");
+  PrepackParams p{};
+  p.src = w->data;
+  p.dst = dst;
+  p.elem_bytes = static_cast<int32_t>(dtype_bytes(w->dtype));
+  p.perm = kPermIdentity;
+  p.N = N;
+  p.D = D;
+  p.Dr = Dr;
+  if (which == MLAP_WEIGHT_UK) {
+    p.batches = static_cast<int32_t>(w->shape[0]);
+    p.K = static_cast<int32_t>(w->shape[1]);
+    p.C = static_cast<int32_t>(w->shape[2]);
+    p.R = p.C;
+  } else {
+    p.batches = 1;
+    p.K = static_cast<int32_t>(w->shape[0]);
+    p.C = static_cast<int32_t>(w->shape[1]);
+    p.R = p.C;
+    if (which == MLAP_WEIGHT_UQ_QR) p.perm = kPermUqQr;
+  }
+  cudaError_t e = launch_prepack(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prepack launch");
+  return MLAP_OK;
+}
+
+mlap_status_t mlap_get_workspace_size(const mlap_args_t* args, size_t* bytes) {
+  if (bytes == nullptr) return fail(MLAP_ERR_NULL, "bytes is NULL");
+  MlaDims d;
+  CHECK_STATUS(validate_mla(args, &d));
+  *bytes = mla_ws_layout(d).total;
+  return MLAP_OK;
+}
+
+mlap_status_t mlap_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr) return fail(MLAP_ERR_NULL, "workspace is NULL");
+  if (ws_bytes < 256) return fail(MLAP_ERR_WORKSPACE, "workspace smaller than its 256-byte header");
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return MLAP_OK;
+}
+
+mlap_status_t mlap_execute(const mlap_args_t* args, void* ws, size_t ws_bytes, void* stream) {
+  return mla_run(args, ws, ws_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+mlap_status_t mlap_check_errors(void* ws, void* stream) {
+  if (ws == nullptr) return fail(MLAP_ERR_NULL, "workspace is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(word), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the error word");
+  if (word & kErrIndexRange) return fail(MLAP_ERR_INDEX_RANGE, "a cache index was outside [-1, BlockNum*BlockSize)");
+  if (word & kErrTimeout) return fail(MLAP_ERR_TIMEOUT, "a kernel wait timed out");
+  return MLAP_OK;
+}
+
+mlap_status_t qkvrnrc_get_workspace_size(const qkvrnrc_args_t* args, size_t* bytes) {
+  if (bytes == nullptr) return fail(MLAP_ERR_NULL, "bytes is NULL");
+  QkvDims d;
+  CHECK_STATUS(validate_qkv(args, &d));
+  *bytes = 256;
+  return MLAP_OK;
+}
+
+mlap_status_t qkvrnrc_execute(const qkvrnrc_args_t* a, void* ws, size_t ws_bytes, void* stream) {
+  QkvDims d;
+  CHECK_STATUS(validate_qkv(a, &d));
+  if (d.T == 0) return MLAP_OK;
+  if (ws == nullptr || ws_bytes < 256) return fail(MLAP_ERR_WORKSPACE, "workspace too small");
+  int dev = 0, sms = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "device query");
+  QkvParams p{};
+  p.qkv = a->qkv.data;
+  p.gamma_q = a->gamma_q.data;
+  p.gamma_k = a->gamma_k.data;
+  p.cos = a->cos.data;
+  p.sin = a->sin.data;
+  p.index = static_cast<const int64_t*>(a->index.data);
+  p.slots = d.BlockNum * d.BlockSize;
+  p.k_cache = a->k_cache.data;
+  p.v_cache = a->v_cache.data;
+  p.k_scale = d.quant ? static_cast<const float*>(a->k_scale.data) : nullptr;
+  p.v_scale = d.quant ? static_cast<const float*>(a->v_scale.data) : nullptr;
+  p.q_out = a->q_out.data;
+  p.T = static_cast<int32_t>(d.T);
+  p.Nq = a->Nq;
+  p.Nk = a->Nk;
+  p.Nv = a->Nv;
+  p.eps = static_cast<float>(a->epsilon);
+  p.bf16 = d.bf16;
+  p.err = static_cast<uint32_t*>(ws);
+  ce = launch_qkv_rnrc(p, static_cast<cudaStream_t>(stream), sms);
+  if (ce != cudaSuccess) return cuda_fail(ce, "QkvRmsNormRopeCache launch");
+  return MLAP_OK;
+}
+
+mlap_status_t mlap_timer_create(void** timer, int32_t max_calls) {
+  if (timer == nullptr) return fail(MLAP_ERR_NULL, "timer is NULL");
+  if (max_calls <= 0) return fail(MLAP_ERR_SHAPE, "max_calls must be positive");
+  Timer* t = new Timer();
+  t->max_calls = max_calls;
+  t->ev.resize(static_cast<size_t>(max_calls) * (MLAP_TIMER_PHASES + 1));
+  for (auto& e : t->ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      delete t;
+      return fail(MLAP_ERR_CUDA, "cudaEventCreate failed");
+    }
+  }
+  *timer = t;
+  return MLAP_OK;
+}
+
+mlap_status_t mlap_execute_timed(const mlap_args_t* args, void* ws, size_t ws_bytes, void* stream,
+                                 void* timer) {
+  if (timer == nullptr) return fail(MLAP_ERR_NULL, "timer is NULL");
+  return mla_run(args, ws, ws_bytes, static_cast<cudaStream_t>(stream), static_cast<Timer*>(timer));
+}
+
+mlap_status_t mlap_timer_read(void* timer, float* ms, int32_t* calls_recorded) {
+  if (timer == nullptr || calls_recorded == nullptr) return fail(MLAP_ERR_NULL, "NULL argument");
+  Timer* t = static_cast<Timer*>(timer);
+  for (int c = 0; c < t->calls; ++c) {
+    for (int k = 0; k < MLAP_TIMER_PHASES; ++k) {
+      cudaEvent_t e0 = t->ev[c * (MLAP_TIMER_PHASES + 1) + k];
+      cudaEvent_t e1 = t->ev[c * (MLAP_TIMER_PHASES + 1) + k + 1];
+      if (cudaEventSynchronize(e1) != cudaSuccess) return fail(MLAP_ERR_CUDA, "cudaEventSynchronize failed");
+      float v = 0.f;
+      if (cudaEventElapsedTime(&v, e0, e1) != cudaSuccess) return fail(MLAP_ERR_CUDA, "cudaEventElapsedTime failed");
+      if (ms) ms[c * MLAP_TIMER_PHASES + k] = v;
+    }
+  }
+  *calls_recorded = t->calls;
+  t->calls = 0;
+  return MLAP_OK;
+}
+
+mlap_status_t mlap_timer_destroy(void* timer) {
+  if (timer == nullptr) return MLAP_OK;
+  Timer* t = static_cast<Timer*>(timer);
+  for (auto& e : t->ev) cudaEventDestroy(e);
+  delete t;
+  return MLAP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+// Persistent, warp-specialised tcgen05 GEMM used by every contraction of the MLA prolog.
+//
+//   C[m, n] = sum_k A[m, k] * B[n, k]      (both operands K-major bf16, fp32 accumulation)
+//
+// A and B arrive through TMA tensor maps (128-byte swizzle, 64-element K blocks).  A tile of
+// BM=128 rows of A and BN rows of B is accumulated in tensor memory (TMEM) by one thread issuing
+// tcgen05.mma; four epilogue warps read the accumulator back with tcgen05.ld and hand each row's
+// values to an epilogue functor (the fused RmsNorm-input, RoPE, bf16 rounding, scatter, ...).
+// TMEM holds two accumulators so the epilogue of one tile overlaps the MMAs of the next.
+//
+// Warp roles (256 threads):  warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM owner,
+// warp 3 = idle, warps 4..7 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+//
+// Work units: (m tile, n tile, batch, k split), m fastest, distributed round-robin over a grid
+// of at most one CTA per SM.  Either operand may be "segmented": tiles below *_seg_tiles come
+// from the first tensor map, the rest from the second (rebased to row 0), which lets one GEMM
+// run over two separately stored weights (W^DQ and W^DKV|W^KR) without copying them together.
+#pragma once
+#include "ptx.cuh"
+
+namespace mlap {
+
+struct GemmGeometry {
+  int32_t m_tiles, n_tiles, batches, splits;
+  int32_t k_blocks;                 // ceil(K / 64)
+  int32_t a_seg_tiles, b_seg_tiles; // tiles of A (B) served by the first map
+  int32_t a_x_batch, a_y_batch;     // per-batch offsets of the TMA coordinates (elements, rows)
+  int32_t b_x_batch, b_y_batch;
+  int32_t num_units;
+};
+
+template <int BN_>
+struct GemmCfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = BN_;
+  static constexpr int BK = 64;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM_LIMIT = 232448;          // 227 KB opt-in per CTA
+  static constexpr int RESERVED = 1024 + 256;         // alignment slack + barriers
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + RESERVED;
+  static constexpr int CH = BN >= 32 ? 32 : BN;       // epilogue column chunk
+  static constexpr int ACC_COLS = 2 * BN;
+  static constexpr uint32_t TMEM_COLS =
+      ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static constexpr int THREADS = 256;
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16,256]");
+  static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-B alignment");
+  static_assert(STAGES >= 2, "pipeline needs two stages");
+};
+
+__device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& tm, int& tn, int& b,
+                                            int& s) {
+  tm = u % g.m_tiles;
+  u /= g.m_tiles;
+  tn = u % g.n_tiles;
+  u /= g.n_tiles;
+  b = u % g.batches;
+  s = u / g.batches;
+}
+
+// Epilogue functor contract:
+//   __device__ void operator()(int row, int col0, int batch, int split, const float* v) const;
+// called by all 32 lanes of an epilogue warp together (it may shuffle across lanes), with `row`
+// the tile-space row of A handled by this lane (may lie beyond the matrix: the functor masks),
+// `col0` the tile-space column of v[0], and CH consecutive accumulator columns in v.
+template <int BN, class Epi>
+__global__ void __launch_bounds__(256, 1)
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
+                     const __grid_constant__ CUtensorMap tmA1,
+                     const __grid_constant__ CUtensorMap tmB0,
+                     const __grid_constant__ CUtensorMap tmB1, const GemmGeometry geo,
+                     const Epi epi, uint32_t* __restrict__ err_word) {
+  using Cfg = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* smemA = smem;
+  uint8_t* smemB = smem + Cfg::STAGES * Cfg::A_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + Cfg::STAGES;
+  uint64_t* accf_bar = empty_bar + Cfg::STAGES;
+  uint64_t* acce_bar = accf_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA0);
+    prefetch_tmap(&tmA1);
+    prefetch_tmap(&tmB0);
+    prefetch_tmap(&tmB1);
+  }
+  if (warp == 1 && lane == 0) {
+    for (int i = 0; i < Cfg::STAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf_bar[i], 1);
+      mbar_init(&acce_bar[i], 4);
+    }
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Let the next kernel in the stream start its prologue; wait for the previous one's results.
+  grid_launch_dependents();
+  grid_dependency_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < geo.num_units && ok; u += gridDim.x) {
+        int tm, tn, b, s;
+        decode_unit(geo, u, tm, tn, b, s);
+        const int kb0 = (s * geo.k_blocks) / geo.splits;
+        const int kb1 = ((s + 1) * geo.k_blocks) / geo.splits;
+        const bool a_first = tm < geo.a_seg_tiles;
+        const bool b_first = tn < geo.b_seg_tiles;
+        const CUtensorMap* mapA = a_first ? &tmA0 : &tmA1;
+        const CUtensorMap* mapB = b_first ? &tmB0 : &tmB1;
+        const int ay = (a_first ? tm : tm - geo.a_seg_tiles) * Cfg::BM + b * geo.a_y_batch;
+        const int by = (b_first ? tn : tn - geo.b_seg_tiles) * Cfg::BN + b * geo.b_y_batch;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], Cfg::STAGE_BYTES);
+          tma_load_2d(smemA + stage * Cfg::A_BYTES, mapA, &full_bar[stage],
+                      kb * Cfg::BK + b * geo.a_x_batch, ay);
+          tma_load_2d(smemB + stage * Cfg::B_BYTES, mapB, &full_bar[stage],
+                      kb * Cfg::BK + b * geo.b_x_batch, by);
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // Give up cleanly: let every load already issued land before the CTA exits.  The last
+        // fill of stage i has parity `phase` if i < stage (this lap), else `phase ^ 1`.
+        for (int i = 0; i < Cfg::STAGES; ++i) {
+          const uint32_t par = (i < stage) ? phase : (phase ^ 1u);
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&full_bar[i], par) && globaltimer_ns() - t0 < 20000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int iter = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < geo.num_units && ok; u += gridDim.x, ++iter) {
+        int tm, tn, b, s;
+        decode_unit(geo, u, tm, tn, b, s);
+        const int kb0 = (s * geo.k_blocks) / geo.splits;
+        const int kb1 = ((s + 1) * geo.k_blocks) / geo.splits;
+        const int buf = iter & 1;
+        const uint32_t use = static_cast<uint32_t>(iter >> 1);
+        if (!mbar_wait(&acce_bar[buf], (use & 1u) ^ 1u, abort_flag)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_u32(smemA + stage * Cfg::A_BYTES);
+          const uint32_t b_addr = smem_u32(smemB + stage * Cfg::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < Cfg::BK / 16; ++kk) {
+            umma_bf16_ss(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
+                         sdesc_kmajor_sw128(b_addr + kk * 32), Cfg::IDESC,
+                         (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);   // frees this smem stage once the MMAs have read it
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(&accf_bar[buf]);   // accumulator ready for the epilogue
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    int iter = 0;
+    for (int u = blockIdx.x; u < geo.num_units; u += gridDim.x, ++iter) {
+      int tm, tn, b, s;
+      decode_unit(geo, u, tm, tn, b, s);
+      const int buf = iter & 1;
+      const uint32_t use = static_cast<uint32_t>(iter >> 1);
+      if (!mbar_wait(&accf_bar[buf], use & 1u, abort_flag)) break;
+      tc_fence_after_sync();
+      const int row = tm * Cfg::BM + q * 32 + lane;
+      const uint32_t t_addr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::BN);
+#pragma unroll 1
+      for (int c = 0; c < Cfg::BN; c += Cfg::CH) {
+        float v[Cfg::CH];
+        if constexpr (Cfg::CH == 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_addr + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        } else {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(t_addr + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+        }
+        epi(row, tn * Cfg::BN + c, b, s, v);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[buf]);
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(err_word, kErrTimeout);
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace mlap

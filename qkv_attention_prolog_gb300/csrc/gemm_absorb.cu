@@ -1,0 +1,21 @@
+// Per-head absorb q^N = q^C·W^UK (MlaPrologV2 README: q^N formula), batched over heads.
+#include "gemm_launch.cuh"
+
+namespace mlap {
+
+cudaError_t launch_absorb(const GemmLaunch& L, const AbsorbParams& p) {
+  if (L.swap) {
+    switch (L.bn) {
+      case 16: return launch_gemm_t<16>(L, EpiAbsorb<true, 16>{p});
+      case 32: return launch_gemm_t<32>(L, EpiAbsorb<true, 32>{p});
+      case 64: return launch_gemm_t<64>(L, EpiAbsorb<true, 32>{p});
+      case 128: return launch_gemm_t<128>(L, EpiAbsorb<true, 32>{p});
+      case 256: return launch_gemm_t<256>(L, EpiAbsorb<true, 32>{p});
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (L.bn != 256) return cudaErrorInvalidValue;
+  return launch_gemm_t<256>(L, EpiAbsorb<false, 32>{p});
+}
+
+}  // namespace mlap

@@ -1,0 +1,21 @@
+// Down-projection x·[W^DQ | W^DKV | W^KR] (MlaPrologV2 README: c^Q, c^KV and k^R formulas).
+#include "gemm_launch.cuh"
+
+namespace mlap {
+
+cudaError_t launch_down(const GemmLaunch& L, const DownParams& p) {
+  if (L.swap) {
+    switch (L.bn) {
+      case 16: return launch_gemm_t<16>(L, EpiDown<true, 128, 16>{p});
+      case 32: return launch_gemm_t<32>(L, EpiDown<true, 128, 32>{p});
+      case 64: return launch_gemm_t<64>(L, EpiDown<true, 128, 32>{p});
+      case 128: return launch_gemm_t<128>(L, EpiDown<true, 128, 32>{p});
+      case 256: return launch_gemm_t<256>(L, EpiDown<true, 128, 32>{p});
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (L.bn != 192) return cudaErrorInvalidValue;
+  return launch_gemm_t<192>(L, EpiDown<false, 192, 32>{p});
+}
+
+}  // namespace mlap

@@ -1,0 +1,89 @@
+// Internal launch interfaces shared by the host API (api.cu) and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "gemm.cuh"
+#include "epilogues.cuh"
+
+namespace mlap {
+
+// One launch of umma_gemm_kernel: the four tensor maps (first/second segment of A and B),
+// the tile geometry, the N tile width, the orientation and the grid.
+struct GemmLaunch {
+  CUtensorMap a0, a1, b0, b1;
+  GemmGeometry geo;
+  int bn;
+  bool swap;
+  bool a_int8;       // A operand is an int8 weight converted to bf16 in shared memory
+  int grid;
+  cudaStream_t stream;
+  bool pdl;
+  uint32_t* err;
+};
+
+cudaError_t launch_down(const GemmLaunch& L, const DownParams& p);
+cudaError_t launch_up(const GemmLaunch& L, const UpParams& p, bool int8);
+cudaError_t launch_absorb(const GemmLaunch& L, const AbsorbParams& p);
+
+// RmsNorm of c^Q (+ dynamic int8 quant) and c^KV, RoPE of k^R, cache quant and scatter; one CTA
+// per token, summing the down-projection's K-split partials in split order.
+struct FinalizeParams {
+  const float* part;
+  int32_t splits, T, Hcq, Hckv, Dr, Ntot;
+  const __nv_bfloat16* gamma_cq;
+  const __nv_bfloat16* gamma_ckv;
+  float eps_cq, eps_ckv;
+  const __nv_bfloat16* cos;
+  const __nv_bfloat16* sin;
+  const int64_t* cache_index;
+  int64_t slots;               // BlockNum * BlockSize (0: no cache update)
+  void* kv_cache;
+  void* kr_cache;
+  int32_t kv_int8, kr_int8;
+  const float* qs_ckv;
+  const float* qs_ckr;
+  __nv_bfloat16* cq_out;       // (T, Hcq): bf16 c^Q, or int8 codes held exactly in bf16
+  const float* smooth;         // non-null: quantise c^Q per token
+  float* scale_t;              // (T) per-token scale of the quantised c^Q
+  uint32_t* err;
+};
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl);
+
+// Weight prepack: dst[b][i][k] = src[b][k][perm(i)]  (a transpose with a row permutation).
+enum PermKind : int32_t { kPermIdentity = 0, kPermUqQr = 1 };
+struct PrepackParams {
+  const void* src;
+  void* dst;
+  int32_t elem_bytes;          // 1 or 2
+  int32_t K, C, R, batches;    // src (batches, K, C); dst (batches, R, K)
+  int32_t perm;                // PermKind
+  int32_t N, D, Dr;            // head geometry for kPermUqQr
+};
+cudaError_t launch_prepack(const PrepackParams& p, cudaStream_t stream);
+
+// QkvRmsNormRopeCache streaming kernel.
+struct QkvParams {
+  const void* qkv;             // (T, (Nq+Nk+Nv)*D) fp16|bf16
+  const void* gamma_q;
+  const void* gamma_k;
+  const void* cos;
+  const void* sin;
+  const int64_t* index;
+  int64_t slots;
+  void* k_cache;
+  void* v_cache;
+  const float* k_scale;        // null: no quant
+  const float* v_scale;
+  void* q_out;
+  int32_t T, Nq, Nk, Nv;
+  float eps;
+  int32_t bf16;                // element type of qkv: 0 fp16, 1 bf16
+  uint32_t* err;
+};
+cudaError_t launch_qkv_rnrc(const QkvParams& p, cudaStream_t stream, int sm_count);
+
+}  // namespace mlap

@@ -1,0 +1,147 @@
+"""GPU parity of the MLA prolog (CUDA path through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import qkv_attention_prolog_gb300 as pkg
+from oracle.mla_prolog import mla_key_rows, mla_prolog_tokens
+from tests.gpu_util import (assert_close, check_cache, f64, oracle_inputs, run_mla)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _full_check(case, bsh=False):
+    cpu = synthetic.make_mla_inputs(case)
+    d = case.dims
+    t, prolog, status = run_mla(cpu, d, case.eps, bsh=bsh)
+    assert status == 0, f"kernel error status {status}"
+    ref = oracle.mla_prolog(**oracle_inputs(cpu), rmsnorm_epsilon_cq=case.eps,
+                            rmsnorm_epsilon_ckv=case.eps)
+    assert_close(f64(t["query"]).reshape(d.T, d.N, d.Hckv), ref["query"], "query")
+    assert_close(f64(t["query_rope"]).reshape(d.T, d.N, d.Dr), ref["query_rope"], "query_rope")
+    idx = cpu["cache_index"].numpy()
+    sub = mla_prolog_tokens(oracle_inputs(cpu), np.arange(d.T))
+    check_cache(t["kv_cache"], cpu["kv_cache"], sub["kv_rows"], idx, "kv_cache")
+    check_cache(t["kr_cache"], cpu["kr_cache"], sub["kr_rows"], idx, "kr_cache")
+    return t, prolog
+
+
+def test_tiny_bf16():
+    _full_check(synthetic.MLA_TINY)
+
+
+SHAPES = [
+    dict(B=1, S=1),                                   # single token
+    dict(B=3, S=1, N=2),                              # ragged token tile
+    dict(B=17, S=1, Hckv=256, N=4),                   # BN 32 in the decode orientation
+    dict(B=2, S=65, He=512, Hcq=256, N=3),            # T=130: BN 256, ragged rope tail (N*Dr)
+    dict(B=3, S=100, He=384, Hcq=192, Hckv=128, N=2),  # T=300: prefill orientation, ragged M
+    dict(B=1, S=200, He=320, Hcq=136, Hckv=96, N=2, Dr=32),  # ragged K, Hcq, Hckv tiles
+]
+
+
+@pytest.mark.parametrize("kw", SHAPES, ids=[str(i) for i in range(len(SHAPES))])
+def test_shapes(kw):
+    kw = dict(kw)
+    block_num = max(1, (kw["B"] * kw["S"] + 127) // 128 + 1)
+    case = synthetic.small_mla_case("shape", block_num=block_num, n_skip=1, **kw)
+    _full_check(case)
+
+
+def test_bsh_layout_matches_tnd():
+    case = synthetic.small_mla_case("bsh", B=4, S=5, N=2, block_num=1)
+    t_bsh, _ = _full_check(case, bsh=True)
+    t_tnd, _ = _full_check(case, bsh=False)
+    assert torch.equal(t_bsh["query"].reshape(-1), t_tnd["query"].reshape(-1))
+
+
+def test_decode_T128():
+    _full_check(synthetic.MLA_DECODE)
+
+
+def test_prefill_T8192_sampled():
+    case = synthetic.MLA_PREFILL
+    cpu = synthetic.make_mla_inputs(case)
+    d = case.dims
+    t, _, status = run_mla(cpu, d, case.eps)
+    assert status == 0
+    inp = oracle_inputs(cpu)
+    rng = np.random.default_rng(0)
+    sample = np.sort(np.concatenate([rng.choice(d.T, 254, replace=False), [0, d.T - 1]]))
+    sub = mla_prolog_tokens(inp, sample)
+    assert_close(f64(t["query"])[sample], sub["query"], "query (sampled tokens)")
+    assert_close(f64(t["query_rope"])[sample], sub["query_rope"], "query_rope (sampled tokens)")
+    kv, kr = mla_key_rows(**inp, Hckv=d.Hckv)
+    idx = cpu["cache_index"].numpy()
+    check_cache(t["kv_cache"], cpu["kv_cache"], kv, idx, "kv_cache (every slot)")
+    check_cache(t["kr_cache"], cpu["kr_cache"], kr, idx, "kr_cache (every slot)")
+
+
+def test_deterministic_bitwise():
+    case = synthetic.MLA_DECODE
+    cpu = synthetic.make_mla_inputs(case)
+    t1, prolog, _ = run_mla(cpu, case.dims, case.eps)
+    t2, _, _ = run_mla(cpu, case.dims, case.eps, prolog=prolog)
+    for k in ("query", "query_rope", "kv_cache", "kr_cache"):
+        assert torch.equal(t1[k].view(torch.uint8), t2[k].view(torch.uint8)), k
+
+
+def test_empty_tokens():
+    case = synthetic.small_mla_case("empty", B=0, S=1)
+    cpu = synthetic.make_mla_inputs(case)
+    t, _, status = run_mla(cpu, case.dims, case.eps)
+    assert status == 0
+    assert torch.equal(t["kv_cache"].cpu().view(torch.uint8), cpu["kv_cache"].view(torch.uint8))
+
+
+def test_empty_cache_computes_outputs():
+    case = synthetic.small_mla_case("skv0", B=4, S=1, block_num=0)
+    cpu = synthetic.make_mla_inputs(case)
+    cpu["cache_index"] = torch.full((4,), -1, dtype=torch.int64)
+    cpu["cache_index"][1] = 5    # out of range of an empty cache: ignored, not an error
+    t, _, status = run_mla(cpu, case.dims, case.eps)
+    assert status == 0
+    ref = oracle.mla_prolog(**oracle_inputs(cpu), rmsnorm_epsilon_cq=case.eps,
+                            rmsnorm_epsilon_ckv=case.eps)
+    assert_close(f64(t["query"]), ref["query"], "query")
+
+
+def test_out_of_range_index_is_skipped_and_reported():
+    case = synthetic.small_mla_case("oob", B=4, S=1, block_num=2)
+    cpu = synthetic.make_mla_inputs(case)
+    cpu["cache_index"] = torch.tensor([3, 256, -7, 10], dtype=torch.int64)
+    t, prolog, status = run_mla(cpu, case.dims, case.eps)
+    assert status == 7       # MLAP_ERR_INDEX_RANGE
+    sub = mla_prolog_tokens(oracle_inputs(cpu), np.arange(4))
+    check_cache(t["kv_cache"], cpu["kv_cache"], sub["kv_rows"], cpu["cache_index"].numpy(),
+                "kv_cache")
+    # the error word is cleared by the read
+    assert pkg.mlap_check_errors(prolog.ws) == 0
+
+
+def test_outputs_have_no_stray_writes():
+    # outputs live inside larger poisoned buffers: bytes around them must not change
+    case = synthetic.small_mla_case("canary", B=5, S=1, N=3, block_num=1)
+    cpu = synthetic.make_mla_inputs(case)
+    d = case.dims
+    dev = torch.device("cuda")
+    t = {k: v.to(dev) for k, v in cpu.items() if isinstance(v, torch.Tensor)}
+    guard = 4096
+    qbuf = torch.full((guard * 2 + d.T * d.N * d.Hckv,), 7.0, dtype=torch.bfloat16, device=dev)
+    rbuf = torch.full((guard * 2 + d.T * d.N * d.Dr,), 7.0, dtype=torch.bfloat16, device=dev)
+    t["query"] = qbuf[guard:guard + d.T * d.N * d.Hckv].view(d.T, d.N, d.Hckv)
+    t["query_rope"] = rbuf[guard:guard + d.T * d.N * d.Dr].view(d.T, d.N, d.Dr)
+    prolog = pkg.MlaProlog({k: t[k] for k in ("weight_dq", "weight_uq_qr", "weight_uk",
+                                              "weight_dkv_kr")}, d.N, d.D, d.Dr)
+    prolog.run({k: v for k, v in t.items() if not k.startswith("weight_")}, case.eps, case.eps)
+    torch.cuda.synchronize()
+    for buf, n in ((qbuf, d.T * d.N * d.Hckv), (rbuf, d.T * d.N * d.Dr)):
+        assert bool((buf[:guard] == 7.0).all()) and bool((buf[guard + n:] == 7.0).all())
