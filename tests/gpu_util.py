@@ -97,5 +97,8 @@ def run_mla(cpu: dict, dims, eps, device="cuda", bsh=False, prolog=None):
     return t, prolog, status
 
 
-def oracle_inputs(cpu: dict) -> dict:
-    return {k: f64(v) for k, v in cpu.items() if isinstance(v, torch.Tensor)}
+def oracle_inputs(cpu: dict, eps: float) -> dict:
+    inp = {k: f64(v) for k, v in cpu.items() if isinstance(v, torch.Tensor)}
+    inp["rmsnorm_epsilon_cq"] = eps
+    inp["rmsnorm_epsilon_ckv"] = eps
+    return inp

@@ -23,12 +23,11 @@ def _full_check(case, bsh=False):
     d = case.dims
     t, prolog, status = run_mla(cpu, d, case.eps, bsh=bsh)
     assert status == 0, f"kernel error status {status}"
-    ref = oracle.mla_prolog(**oracle_inputs(cpu), rmsnorm_epsilon_cq=case.eps,
-                            rmsnorm_epsilon_ckv=case.eps)
+    ref = oracle.mla_prolog(**oracle_inputs(cpu, case.eps))
     assert_close(f64(t["query"]).reshape(d.T, d.N, d.Hckv), ref["query"], "query")
     assert_close(f64(t["query_rope"]).reshape(d.T, d.N, d.Dr), ref["query_rope"], "query_rope")
     idx = cpu["cache_index"].numpy()
-    sub = mla_prolog_tokens(oracle_inputs(cpu), np.arange(d.T))
+    sub = mla_prolog_tokens(oracle_inputs(cpu, case.eps), np.arange(d.T))
     check_cache(t["kv_cache"], cpu["kv_cache"], sub["kv_rows"], idx, "kv_cache")
     check_cache(t["kr_cache"], cpu["kr_cache"], sub["kr_rows"], idx, "kr_cache")
     return t, prolog
@@ -73,7 +72,7 @@ def test_prefill_T8192_sampled():
     d = case.dims
     t, _, status = run_mla(cpu, d, case.eps)
     assert status == 0
-    inp = oracle_inputs(cpu)
+    inp = oracle_inputs(cpu, case.eps)
     rng = np.random.default_rng(0)
     sample = np.sort(np.concatenate([rng.choice(d.T, 254, replace=False), [0, d.T - 1]]))
     sub = mla_prolog_tokens(inp, sample)
@@ -109,8 +108,7 @@ def test_empty_cache_computes_outputs():
     cpu["cache_index"][1] = 5    # out of range of an empty cache: ignored, not an error
     t, _, status = run_mla(cpu, case.dims, case.eps)
     assert status == 0
-    ref = oracle.mla_prolog(**oracle_inputs(cpu), rmsnorm_epsilon_cq=case.eps,
-                            rmsnorm_epsilon_ckv=case.eps)
+    ref = oracle.mla_prolog(**oracle_inputs(cpu, case.eps))
     assert_close(f64(t["query"]), ref["query"], "query")
 
 
@@ -120,7 +118,7 @@ def test_out_of_range_index_is_skipped_and_reported():
     cpu["cache_index"] = torch.tensor([3, 256, -7, 10], dtype=torch.int64)
     t, prolog, status = run_mla(cpu, case.dims, case.eps)
     assert status == 7       # MLAP_ERR_INDEX_RANGE
-    sub = mla_prolog_tokens(oracle_inputs(cpu), np.arange(4))
+    sub = mla_prolog_tokens(oracle_inputs(cpu, case.eps), np.arange(4))
     check_cache(t["kv_cache"], cpu["kv_cache"], sub["kv_rows"], cpu["cache_index"].numpy(),
                 "kv_cache")
     # the error word is cleared by the read
