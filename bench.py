@@ -46,6 +46,8 @@ def _parse():
                     choices=["decode", "prefill", "tiny", "partial_quant", "qkv"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--timer-calls", type=int, default=200,
+                    help="calls timed kernel by kernel for the roofline entry")
     return ap.parse_args()
 
 
@@ -324,15 +326,17 @@ def run_ours(args, rank, local, world):
         assert pkg.mlap_check_errors(s[2], stream) == 0, "kernel error during the timed region"
 
     # per-kernel durations (CUDA events around each launch on the execute stream)
-    timer = pkg.Timer(200)
+    n_timed = max(2, args.timer_calls)
+    timer = pkg.Timer(n_timed)
     with torch.cuda.stream(stream):
-        for i in range(200):
+        for i in range(n_timed):
             t, a, ws = sets[i % n_sets]
             timer.execute(a, ws, stream)
     per = timer.read()
     timer.close()
     names = ["down", "norm_scatter", "up", "absorb"]
-    avg_ms = {n: statistics.mean(r[k] for r in per[10:]) for k, n in enumerate(names)}
+    per = per[min(10, len(per) // 2):]
+    avg_ms = {n: statistics.mean(r[k] for r in per) for k, n in enumerate(names)}
     dominant = max(names, key=lambda n: avg_ms[n])
     tensor_bound = args.workload == "prefill"
     if tensor_bound:
