@@ -219,6 +219,35 @@ mlap_status_t mlap_execute_timed(const mlap_args_t* args, void* workspace,
 mlap_status_t mlap_timer_read(void* timer, float* ms, int32_t* calls_recorded);
 mlap_status_t mlap_timer_destroy(void* timer);
 
+/* ============================================================================================ */
+/* Allocation-free MLA prolog                                                                    */
+/* ============================================================================================ */
+
+/* The operator pages have no counterpart to this call: it exists for callers that cannot
+ * allocate device memory or pass a workspace, such as a plugin whose host framework owns every
+ * device buffer and only hands over the tensors it manages, a latency-critical loop that cannot
+ * pay cudaMalloc's implicit device synchronisation, or a plain C caller without a device
+ * allocator.
+ *
+ * Same arguments, validation, kernels and results as mlap_execute, but no workspace: the scratch
+ * lives in a static device array of MLAP_NO_ALLOC_SCRATCH_BYTES inside the library, which every
+ * GPU that uses this call keeps until the process exits.  The caller still passes all inputs and
+ * outputs.  The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine).
+ *   - Shapes whose workspace (mlap_get_workspace_size) exceeds MLAP_NO_ALLOC_SCRATCH_BYTES are
+ *     rejected with MLAP_ERR_WORKSPACE before any device work.  With the decode shapes
+ *     (He 7168, Hcq 1536, Hckv 512, N 128, D 128, Dr 64) calls with T <= 147 or
+ *     257 <= T <= 568 tokens fit (up to 256 tokens the down-projection keeps up to 16 K-split
+ *     partials, above that one).
+ *   - The first call on each device looks up the array's device address with that device
+ *     current; make that first call before any stream capture on the device.
+ *   - Every call on a device shares the one array and clears its error word first; calls that
+ *     may overlap on the GPU (different streams, or other threads) race on it and must be
+ *     serialised by the caller.  Kernel-detected cache-index errors are skipped on the device
+ *     and are not reported by this call (use mlap_execute + mlap_check_errors to see them). */
+#define MLAP_NO_ALLOC_SCRATCH_BYTES (24u * 1024u * 1024u)
+mlap_status_t mlap_execute_no_alloc(const mlap_args_t* args, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

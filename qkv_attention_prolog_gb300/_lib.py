@@ -32,7 +32,7 @@ EXPORTS = ["mlap_prepack_size", "mlap_prepack_weights", "mlap_get_workspace_size
            "mlap_workspace_init", "mlap_execute", "mlap_check_errors",
            "qkvrnrc_get_workspace_size", "qkvrnrc_execute", "mlap_status_string",
            "mlap_last_error", "mlap_timer_create", "mlap_execute_timed", "mlap_timer_read",
-           "mlap_timer_destroy"]
+           "mlap_timer_destroy", "mlap_execute_no_alloc"]
 
 
 class MlapError(RuntimeError):
@@ -107,6 +107,7 @@ def load() -> ctypes.CDLL:
         "mlap_timer_read": (st, [vp, ctypes.POINTER(ctypes.c_float),
                                  ctypes.POINTER(ctypes.c_int32)]),
         "mlap_timer_destroy": (st, [vp]),
+        "mlap_execute_no_alloc": (st, [A, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -216,6 +217,13 @@ def mlap_workspace_init(ws: torch.Tensor, stream=None):
 def mlap_execute(args: mlap_args_t, ws: torch.Tensor, stream=None):
     _check(load().mlap_execute(ctypes.byref(args), ws.data_ptr(), ws.numel() * ws.element_size(),
                                _stream_ptr(stream)), "mlap_execute")
+
+
+def mlap_execute_no_alloc(args: mlap_args_t, stream=None):
+    """mlap_execute without a workspace: the library's static device scratch is used instead
+    (for callers that cannot allocate device memory; see include/mlaprolog.h)."""
+    _check(load().mlap_execute_no_alloc(ctypes.byref(args), _stream_ptr(stream)),
+           "mlap_execute_no_alloc")
 
 
 def mlap_check_errors(ws: torch.Tensor, stream=None) -> int:

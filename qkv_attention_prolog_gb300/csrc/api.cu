@@ -838,3 +838,56 @@ mlap_status_t mlap_timer_destroy(void* timer) {
 }
 
 }  // extern "C"
+
+// ================================================================================================
+// Allocation-free MLA prolog.
+//
+// Some callers cannot hand the library a workspace: a plugin whose host framework owns every
+// device buffer and passes in only the tensors it manages, a latency-critical serving loop that
+// may not pay cudaMalloc's implicit device synchronisation, or a plain C caller with no device
+// allocator of its own.  mlap_execute_no_alloc runs the same kernels as mlap_execute with its
+// scratch (K-split partials, c^Q, q^C, error word) in the fixed-size array below.  Every GPU that
+// uses this entry point keeps the array until the process exits.
+static __device__ __align__(256) uint8_t g_mlap_static_scratch[MLAP_NO_ALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" mlap_status_t mlap_execute_no_alloc(const mlap_args_t* args, void* stream) {
+  MlaDims d;
+  CHECK_STATUS(validate_mla(args, &d));
+  const size_t need = mla_ws_layout(d).total;
+  if (need > static_cast<size_t>(MLAP_NO_ALLOC_SCRATCH_BYTES))
+    return fail(MLAP_ERR_WORKSPACE,
+                "mlap_execute_no_alloc: these shapes need " + std::to_string(need) +
+                    " bytes of scratch; the static scratch holds " +
+                    std::to_string(static_cast<size_t>(MLAP_NO_ALLOC_SCRATCH_BYTES)) +
+                    " (use mlap_execute with a caller workspace)");
+  if (d.T == 0) return MLAP_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MLAP_ERR_UNSUPPORTED, "device ordinal too large");
+  void* scratch = nullptr;
+  {
+    // Once per device, with that device current: the array's name is only a host-side stand-in,
+    // so the kernels get the device address the runtime reports for it.
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (g_static_scratch_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_mlap_static_scratch);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+      g_static_scratch_ptr[dev] = p;
+    }
+    scratch = g_static_scratch_ptr[dev];
+  }
+  // The array keeps the previous call's contents; only the error word must start at zero (every
+  // other scratch byte a call reads was written earlier in the same call).
+  e = cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch header");
+  return mla_run(args, scratch, static_cast<size_t>(MLAP_NO_ALLOC_SCRATCH_BYTES),
+                 static_cast<cudaStream_t>(stream), nullptr);
+}
