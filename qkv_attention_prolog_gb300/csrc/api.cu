@@ -143,11 +143,11 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
   d->Dr = sn.shape[sn.ndim - 1];
 
   if (d->D != 128) return fail(MLAP_ERR_UNSUPPORTED, "D (weight_uk dim 1) must be 128");
-  if (d->Dr <= 0 || (d->Dr & 1)) return fail(MLAP_ERR_UNSUPPORTED, "Dr must be positive and even");
+  if (d->Dr <= 0 || (d->Dr % 32)) return fail(MLAP_ERR_UNSUPPORTED, "Dr must be a positive multiple of 32");
   if (d->N <= 0 || d->Hckv <= 0 || d->Hcq <= 0 || d->He <= 0)
     return fail(MLAP_ERR_SHAPE, "N, Hckv, Hcq and He must be positive");
-  if ((d->He % 8) || (d->Hcq % 8))
-    return fail(MLAP_ERR_UNSUPPORTED, "He and Hcq must be multiples of 8 (16-byte TMA row pitch)");
+  if ((d->He % 8) || (d->Hcq % 8) || (d->Hckv % 8))
+    return fail(MLAP_ERR_UNSUPPORTED, "He, Hcq and Hckv must be multiples of 8 (16-byte TMA pitch)");
 
   const mlap_tensor_t& wuq = a->weight_uq_qr;
   CHECK_STATUS(need(wuq, "weight_uq_qr", false));
@@ -319,6 +319,28 @@ mlap_status_t make_tmap(CUtensorMap* m, const void* base, int64_t inner, int64_t
   return MLAP_OK;
 }
 
+// Output map for the epilogue's TMA stores: `rank` dims (innermost first), byte strides of dims
+// 1.., box sizes, element type and swizzle matching the staging tile layout.
+mlap_status_t make_out_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rank,
+                           std::initializer_list<int64_t> dims, std::initializer_list<int64_t> strides,
+                           std::initializer_list<int> box, CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return fail(MLAP_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  int i = 0;
+  for (int64_t v : dims) d[i++] = static_cast<cuuint64_t>(v);
+  i = 0;
+  for (int64_t v : strides) st[i++] = static_cast<cuuint64_t>(v);
+  i = 0;
+  for (int v : box) b[i++] = static_cast<cuuint32_t>(v);
+  CUresult r = enc(m, dt, rank, const_cast<void*>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   sw, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MLAP_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (" + std::to_string(int(r)) + ")");
+  return MLAP_OK;
+}
+
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 int swap_bn(int64_t T) {
@@ -378,8 +400,8 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   g.pdl = true;
   g.err = err;
   g.swap = swap;
-  DownParams dp{part, static_cast<int32_t>(d.T), static_cast<int32_t>(d.Hcq),
-                static_cast<int32_t>(d.Hckv + d.Dr), static_cast<int32_t>(Ntot), 0};
+  DownParams dp{0};
+  const int ch_t = swap ? (bn_t < 32 ? bn_t : 32) : 32;   // tokens per epilogue store box
   {
     const int kb = ceil_div(d.He, 64);
     if (swap) {
@@ -416,6 +438,14 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     g.geo.batches = 1;
     g.geo.k_blocks = kb;
     g.geo.num_units = g.geo.m_tiles * g.geo.n_tiles * g.geo.splits;
+    // partials part[s][t][f]: W^DQ columns and W^DKV|W^KR columns as two 3-D (f, t, s) maps
+    const int64_t row_b = Ntot * 4, split_b = d.T * Ntot * 4;
+    CHECK_STATUS(make_out_map(&g.o0, part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                              {d.Hcq, d.T, g.geo.splits}, {row_b, split_b}, {32, ch_t, 1},
+                              CU_TENSOR_MAP_SWIZZLE_128B));
+    CHECK_STATUS(make_out_map(&g.o1, part + d.Hcq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                              {d.Hckv + d.Dr, d.T, g.geo.splits}, {row_b, split_b}, {32, ch_t, 1},
+                              CU_TENSOR_MAP_SWIZZLE_128B));
     g.grid = g.geo.num_units < sms ? g.geo.num_units : sms;
     CHECK_STATUS(rec(0));
     ce = launch_down(g, dp);
@@ -486,9 +516,12 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.geo.k_blocks = ceil_div(d.Hcq, 64);
     u.geo.num_units = u.geo.m_tiles * u.geo.n_tiles;
     u.grid = u.geo.num_units < sms ? u.geo.num_units : sms;
-    UpParams up{qc,
-                static_cast<__nv_bfloat16*>(a->query_rope.data),
-                static_cast<const __nv_bfloat16*>(a->rope_cos.data),
+    CHECK_STATUS(make_out_map(&u.o0, qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, {d.N * d.D, d.T},
+                              {d.N * d.D * 2}, {32, ch_t}, CU_TENSOR_MAP_SWIZZLE_64B));
+    CHECK_STATUS(make_out_map(&u.o1, a->query_rope.data, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                              {d.Dr, d.N, d.T}, {d.Dr * 2, d.N * d.Dr * 2}, {16, 1, ch_t},
+                              CU_TENSOR_MAP_SWIZZLE_32B));
+    UpParams up{static_cast<const __nv_bfloat16*>(a->rope_cos.data),
                 static_cast<const __nv_bfloat16*>(a->rope_sin.data),
                 scale_t,
                 static_cast<const float*>(a->dequant_scale_w_uq_qr.data),
@@ -538,8 +571,11 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.geo.k_blocks = ceil_div(d.D, 64);
     b.geo.num_units = b.geo.m_tiles * b.geo.n_tiles * b.geo.batches;
     b.grid = b.geo.num_units < sms ? b.geo.num_units : sms;
-    AbsorbParams ap{static_cast<__nv_bfloat16*>(a->query.data), static_cast<int32_t>(d.T),
-                    static_cast<int32_t>(d.N), static_cast<int32_t>(d.Hckv)};
+    CHECK_STATUS(make_out_map(&b.o0, a->query.data, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                              {d.Hckv, d.N, d.T}, {d.Hckv * 2, d.N * d.Hckv * 2}, {32, 1, ch_t},
+                              CU_TENSOR_MAP_SWIZZLE_64B));
+    b.o1 = b.o0;
+    AbsorbParams ap{0};
     CHECK_STATUS(rec(3));
     ce = launch_absorb(b, ap);
     if (ce != cudaSuccess) return cuda_fail(ce, "absorb launch");

@@ -2,66 +2,109 @@
 //
 // "SWAP" selects the decode orientation: A = the weight (its output features are the MMA's
 // M = 128 rows), B = the activations (tokens are the MMA's N).  Without SWAP (prefill),
-// A = activations (tokens are rows) and B = the weight.  The functors translate tile-space
-// (row, column) back to (token, feature) and fuse the step that follows each contraction.
+// A = activations (tokens are rows) and B = the weight.
+//
+// Every epilogue warp owns a 32 x CH block of the accumulator (32 TMEM lanes x CH columns).  The
+// functor fuses the step that follows the contraction, writes the block into a per-warp shared
+// memory staging tile laid out exactly as the TMA store box expects (token-major rows, the
+// store map's swizzle applied), and returns the stores to issue.  Output tails (tokens beyond T,
+// features beyond the matrix) are clipped by the store's tensor map, so no lane masks writes.
 #pragma once
 #include <cuda_bf16.h>
-#include "ptx.cuh"
+#include "gemm.cuh"
 
 namespace mlap {
+
+// Swizzled staging addresses: element (row r, column c) of a tile whose rows are 128 B (fp32 x32,
+// SWIZZLE_128B), 64 B (bf16 x32, SWIZZLE_64B) or 32 B (bf16 x16, SWIZZLE_32B).  The 16-byte chunk
+// index is XORed with row bits as the TMA swizzle modes define; tiles start 1024-B aligned.
+__device__ __forceinline__ uint32_t sw128_f32(int r, int c) {
+  return r * 128 + ((((c >> 2) ^ (r & 7)) & 7) << 4) + (c & 3) * 4;
+}
+__device__ __forceinline__ uint32_t sw64_bf16(int r, int c) {
+  return r * 64 + ((((c >> 3) ^ ((r >> 1) & 3)) & 3) << 4) + (c & 7) * 2;
+}
+
+__device__ __forceinline__ void st_f32(uint8_t* sb, uint32_t off, float v) {
+  *reinterpret_cast<float*>(sb + off) = v;
+}
+__device__ __forceinline__ void st_bf16(uint8_t* sb, uint32_t off, float v) {
+  *reinterpret_cast<__nv_bfloat16*>(sb + off) = __float2bfloat16_rn(v);
+}
+
+// Lane-as-row writes of 32 consecutive fp32 values (float4 chunks; the swizzle keeps the 32
+// lanes' 16-byte writes on distinct banks).
+__device__ __forceinline__ void stage_row_f32(uint8_t* sb, int r, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(sb + r * 128 + (((c ^ (r & 7)) & 7) << 4)) =
+        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
+// Lane-as-row writes of 32 consecutive values rounded to bf16 (4 chunks of 8, SWIZZLE_64B).
+__device__ __forceinline__ void stage_row_bf16x32(uint8_t* sb, int r, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(sb + r * 64 + (((c ^ ((r >> 1) & 3)) & 3) << 4)) = pack_bf16x8(v + 8 * c);
+}
+
+// Lane-as-row writes of 16 consecutive values rounded to bf16 (2 chunks of 8, SWIZZLE_32B).
+__device__ __forceinline__ void stage_row_bf16x16(uint8_t* sb, int r, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+    *reinterpret_cast<uint4*>(sb + r * 32 + (((c ^ ((r >> 2) & 1)) & 1) << 4)) = pack_bf16x8(v + 8 * c);
+}
+
+__device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* p, float* out) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+  const __nv_bfloat16* ea = reinterpret_cast<const __nv_bfloat16*>(&a);
+  const __nv_bfloat16* eb = reinterpret_cast<const __nv_bfloat16*>(&b);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    out[i] = __bfloat162float(ea[i]);
+    out[8 + i] = __bfloat162float(eb[i]);
+  }
+}
 
 // ----------------------------------------------------------------------------------------------
 // Down-projection  [h_q | h_kv | h_kr] = x · [W^DQ | W^DKV | W^KR]   (MlaPrologV2 README, c^Q and
 // c^KV / k^R formulas).  The weight is two tensor maps (W^DQ, W^DKV|W^KR) seen as one operand
-// with `seg_tiles` tiles in the first.  The fp32 result of K-split s goes to
-// part[s][t][f], f in [0, Hcq + Hckv + Dr); the norm step sums the splits in order.
+// with `seg_tiles` tiles in the first.  K-split s writes its fp32 partial to part[s][t][f]; the
+// two output maps cover the W^DQ columns and the W^DKV|W^KR columns of part, 3-D (f, t, s).
 struct DownParams {
-  float* part;
-  int32_t T, Hcq, Nseg2, Ntot, seg_tiles;
+  int32_t seg_tiles;
 };
 
 template <bool SWAP, int TILE_W, int CH>
 struct EpiDown {
   DownParams p;
 
-  __device__ __forceinline__ int feature(int i) const {
+  __device__ __forceinline__ int operator()(int m0, int n0, int, int s, const float (&v)[CH],
+                                            uint8_t* sb, StoreOp (&ops)[2]) const {
+    const int lane = threadIdx.x & 31;
     const int b0 = p.seg_tiles * TILE_W;
-    if (i < b0) return i < p.Hcq ? i : -1;
-    const int i2 = i - b0;
-    return i2 < p.Nseg2 ? p.Hcq + i2 : -1;
-  }
-
-  __device__ __forceinline__ void operator()(int row, int col0, int, int s, const float* v) const {
-    float* out = p.part + static_cast<size_t>(s) * p.T * p.Ntot;
     if constexpr (SWAP) {
-      const int f = feature(row);
-      if (f < 0) return;
 #pragma unroll
-      for (int j = 0; j < CH; ++j) {
-        const int t = col0 + j;
-        if (t < p.T) out[static_cast<size_t>(t) * p.Ntot + f] = v[j];
-      }
+      for (int j = 0; j < CH; ++j) st_f32(sb, sw128_f32(j, lane), v[j]);
+      const bool first = m0 < b0;
+      ops[0] = {first ? 0 : 1, 3, first ? m0 : m0 - b0, n0, s, 0};
     } else {
-      const int t = row;
-      if (t >= p.T) return;
-      float* dst = out + static_cast<size_t>(t) * p.Ntot;
-      const int f0 = feature(col0);
-      const int fl = feature(col0 + CH - 1);
-      const bool contiguous = f0 >= 0 && fl == f0 + CH - 1;
-      const size_t off = static_cast<size_t>(s) * p.T * p.Ntot + static_cast<size_t>(t) * p.Ntot + f0;
-      if (contiguous && (off % 4) == 0) {
-        float4* d4 = reinterpret_cast<float4*>(dst + f0);
-#pragma unroll
-        for (int j = 0; j < CH / 4; ++j)
-          d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-          const int f = feature(col0 + j);
-          if (f >= 0) dst[f] = v[j];
-        }
-      }
+      stage_row_f32(sb, lane, v);
+      const bool first = n0 < b0;
+      ops[0] = {first ? 0 : 1, 3, first ? n0 : n0 - b0, m0, s, 0};
     }
+    return 1;
   }
 };
 
@@ -69,11 +112,10 @@ struct EpiDown {
 // Up-projection  [q^C | q_r] = c^Q · W^UQ_QR  (MlaPrologV2 README q^C and q^R formulas) with the
 // weight prepacked as rows [all heads' nope columns (n*D + d) | all heads' rope columns, each
 // head's pair (j, j + Dr/2) stored adjacently].  Fused: bf16 rounding of q^C (the next matmul's
-// input), half-and-half RoPE of q_r into query_rope, and for an int8 weight the dequant
-// acc * scale_t[t] * dequant_scale_w_uq_qr[column].
+// input, first output map: q^C (T, N*D)), half-and-half RoPE of q_r (aclnnQkvRmsNormRopeCache
+// "Formulas" (3)) into query_rope (second output map: 3-D (Dr, N, T)), and for an int8 weight
+// the dequant acc * scale_t[t] * dequant_scale_w_uq_qr[column].
 struct UpParams {
-  __nv_bfloat16* qc;            // (T, N*D)
-  __nv_bfloat16* qrope;         // (T, N, Dr)
   const __nv_bfloat16* cos;     // (T, Dr)
   const __nv_bfloat16* sin;     // (T, Dr)
   const float* scale_t;         // (T) per-token dequant scale, int8 path
@@ -94,149 +136,135 @@ struct EpiUp {
     return n * (p.D + p.Dr) + p.D + (q >> 1) + (q & 1) * (p.Dr >> 1);
   }
 
-  __device__ __forceinline__ float cs(const __nv_bfloat16* tab, int t, int j) const {
-    return __bfloat162float(tab[static_cast<size_t>(t) * p.Dr + j]);
+  // RoPE of one token's 16 adjacent (j, j + Dr/2) pairs y[2i], y[2i+1], i < 16, i.e. pairs
+  // p0 .. p0+15 of one head; the results are staged at row r of two 16-wide bf16 tiles holding
+  // output columns p0.. and p0+Dr/2.. (offsets 0 and 1024 of the staging buffer).
+  __device__ __forceinline__ void rope_row(uint8_t* sb, int r, int t, int p0, const float* y) const {
+    float c0[16], s0[16], c1[16], s1[16];
+    if (t < p.T) {
+      const size_t row = static_cast<size_t>(t) * p.Dr;
+      load_bf16x16(p.cos + row + p0, c0);
+      load_bf16x16(p.sin + row + p0, s0);
+      load_bf16x16(p.cos + row + p0 + (p.Dr >> 1), c1);
+      load_bf16x16(p.sin + row + p0 + (p.Dr >> 1), s1);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) c0[i] = s0[i] = c1[i] = s1[i] = 0.f;
+    }
+    float oa[16], ob[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float y0 = y[2 * i], y1 = y[2 * i + 1];
+      oa[i] = y0 * c0[i] - y1 * s0[i];
+      ob[i] = y1 * c1[i] + y0 * s1[i];
+    }
+    stage_row_bf16x16(sb, r, oa);
+    stage_row_bf16x16(sb + 1024, r, ob);
   }
 
-  __device__ __forceinline__ void operator()(int row, int col0, int, int, const float* v) const {
+  __device__ __forceinline__ int operator()(int m0, int n0, int, int, const float (&v)[CH],
+                                            uint8_t* sb, StoreOp (&ops)[2]) const {
+    const int lane = threadIdx.x & 31;
     const int nd = p.N * p.D;
     const int M = p.N * (p.D + p.Dr);
     if constexpr (SWAP) {
-      const int f = row;
-      if (f - (threadIdx.x & 31) < nd) {             // warp-uniform: nope rows (nd % 32 == 0)
-        if (f >= nd) return;
-        const float dq = INT8 ? p.dqw[orig_col(f)] : 1.f;
+      // lane = weight row f = m0 + lane, v[j] = token n0 + j
+      const int f = m0 + lane;
+      float w[CH];
+      if constexpr (INT8) {
+        const float dq = f < M ? __ldg(p.dqw + orig_col(f)) : 0.f;
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
-          const int t = col0 + j;
-          if (t < p.T) {
-            const float val = INT8 ? v[j] * p.scale_t[t] * dq : v[j];
-            p.qc[static_cast<size_t>(t) * nd + f] = __float2bfloat16_rn(val);
-          }
-        }
-      } else {                                        // rope rows: partner is lane ^ 1
-        const bool valid = f < M;
-        const int r = f - nd;
-        const int n = r / p.Dr, q = r % p.Dr;
-        const int e = q & 1;
-        const int jj = (q >> 1) + e * (p.Dr >> 1);
-        const float dq = (INT8 && valid) ? p.dqw[orig_col(f)] : 1.f;
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-          const int t = col0 + j;
-          const bool tv = t < p.T;
-          const float val = INT8 ? (tv && valid ? v[j] * p.scale_t[t] * dq : 0.f) : v[j];
-          const float partner = __shfl_xor_sync(0xffffffffu, val, 1);
-          if (valid && tv) {
-            const float c = cs(p.cos, t, jj), s = cs(p.sin, t, jj);
-            const float out = e ? (val * c + partner * s) : (val * c - partner * s);
-            p.qrope[(static_cast<size_t>(t) * p.N + n) * p.Dr + jj] = __float2bfloat16_rn(out);
-          }
-        }
-      }
-    } else {
-      const int t = row;
-      if (t >= p.T) return;
-      const float st = INT8 ? p.scale_t[t] : 1.f;
-      if (col0 < nd) {
-        __nv_bfloat16* dst = p.qc + static_cast<size_t>(t) * nd + col0;
-        const bool full = col0 + CH <= nd;
-        if (full && ((static_cast<size_t>(t) * nd + col0) % 8) == 0) {
-#pragma unroll
-          for (int j = 0; j < CH / 8; ++j) {
-            uint4 pk;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              float a = v[8 * j + 2 * h], b = v[8 * j + 2 * h + 1];
-              if (INT8) {
-                a *= st * p.dqw[orig_col(col0 + 8 * j + 2 * h)];
-                b *= st * p.dqw[orig_col(col0 + 8 * j + 2 * h + 1)];
-              }
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
-              w[h] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            reinterpret_cast<uint4*>(dst)[j] = pk;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < CH; ++j) {
-            if (col0 + j < nd) {
-              float a = v[j];
-              if (INT8) a *= st * p.dqw[orig_col(col0 + j)];
-              dst[j] = __float2bfloat16_rn(a);
-            }
-          }
+          const int t = n0 + j;
+          w[j] = t < p.T ? v[j] * __ldg(p.scale_t + t) * dq : 0.f;
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < CH; j += 2) {
-          const int f = col0 + j;
-          if (f >= M) continue;
-          const int r = f - nd;
-          const int n = r / p.Dr, pp = (r % p.Dr) >> 1;
-          float y0 = v[j], y1 = v[j + 1];
-          if (INT8) {
-            y0 *= st * p.dqw[orig_col(f)];
-            y1 *= st * p.dqw[orig_col(f + 1)];
-          }
-          const int j0 = pp, j1 = pp + (p.Dr >> 1);
-          const float o0 = y0 * cs(p.cos, t, j0) - y1 * cs(p.sin, t, j0);
-          const float o1 = y1 * cs(p.cos, t, j1) + y0 * cs(p.sin, t, j1);
-          __nv_bfloat16* dst = p.qrope + (static_cast<size_t>(t) * p.N + n) * p.Dr;
-          dst[j0] = __float2bfloat16_rn(o0);
-          dst[j1] = __float2bfloat16_rn(o1);
+        for (int j = 0; j < CH; ++j) w[j] = v[j];
+      }
+      if (m0 < nd) {   // nope rows (nd is a multiple of 128: the whole block is nope)
+#pragma unroll
+        for (int j = 0; j < CH; ++j) st_bf16(sb, sw64_bf16(j, lane), w[j]);
+        ops[0] = {0, 2, m0, n0, 0, 0};
+        return 1;
+      }
+      // rope rows: transpose through the staging tile (fp32), then each lane takes one token
+#pragma unroll
+      for (int j = 0; j < CH; ++j) st_f32(sb, sw128_f32(j, lane), w[j]);
+      __syncwarp();
+      float y[32];
+      if (lane < CH) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 q =
+              *reinterpret_cast<const float4*>(sb + lane * 128 + (((c ^ (lane & 7)) & 7) << 4));
+          y[4 * c] = q.x;
+          y[4 * c + 1] = q.y;
+          y[4 * c + 2] = q.z;
+          y[4 * c + 3] = q.w;
         }
       }
+      __syncwarp();
+      const int r0 = m0 - nd;                 // first rope row of the block (Dr % 32 == 0)
+      const int n = r0 / p.Dr, p0 = (r0 % p.Dr) >> 1;
+      if (lane < CH) rope_row(sb, lane, n0 + lane, p0, y);
+      ops[0] = {1, 3, p0, n, n0, 0};
+      ops[1] = {1, 3, p0 + (p.Dr >> 1), n, n0, 1024};
+      return 2;
+    } else {
+      // lane = token t = m0 + lane, v[j] = prepacked column n0 + j
+      const int t = m0 + lane;
+      float w[32];
+      if constexpr (INT8) {
+        const float st = t < p.T ? __ldg(p.scale_t + t) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int f = n0 + j;
+          w[j] = f < M ? v[j] * st * __ldg(p.dqw + orig_col(f)) : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = v[j];
+      }
+      if (n0 < nd) {
+        stage_row_bf16x32(sb, lane, w);
+        ops[0] = {0, 2, n0, m0, 0, 0};
+        return 1;
+      }
+      const int r0 = n0 - nd;
+      const int n = r0 / p.Dr, p0 = (r0 % p.Dr) >> 1;
+      rope_row(sb, lane, t, p0, w);
+      ops[0] = {1, 3, p0, n, m0, 0};
+      ops[1] = {1, 3, p0 + (p.Dr >> 1), n, m0, 1024};
+      return 2;
     }
   }
 };
 
 // ----------------------------------------------------------------------------------------------
 // Absorb  q^N[t, n, :] = q^C[t, n, :] · W^UK[n]  (MlaPrologV2 README q^N formula), batched over
-// heads n; W^UK prepacked per head as (Hckv, D) so it is K-major.  Output query (T, N, Hckv) bf16.
+// heads n; W^UK prepacked per head as (Hckv, D) so it is K-major.  Output map: query as 3-D
+// (Hckv, N, T) bf16.
 struct AbsorbParams {
-  __nv_bfloat16* query;
-  int32_t T, N, Hckv;
+  int32_t unused;
 };
 
 template <bool SWAP, int CH>
 struct EpiAbsorb {
   AbsorbParams p;
 
-  __device__ __forceinline__ void operator()(int row, int col0, int n, int, const float* v) const {
+  __device__ __forceinline__ int operator()(int m0, int n0, int n, int, const float (&v)[CH],
+                                            uint8_t* sb, StoreOp (&ops)[2]) const {
+    const int lane = threadIdx.x & 31;
     if constexpr (SWAP) {
-      const int c = row;
-      if (c >= p.Hckv) return;
 #pragma unroll
-      for (int j = 0; j < CH; ++j) {
-        const int t = col0 + j;
-        if (t < p.T)
-          p.query[(static_cast<size_t>(t) * p.N + n) * p.Hckv + c] = __float2bfloat16_rn(v[j]);
-      }
+      for (int j = 0; j < CH; ++j) st_bf16(sb, sw64_bf16(j, lane), v[j]);
+      ops[0] = {0, 3, m0, n, n0, 0};
     } else {
-      const int t = row;
-      if (t >= p.T) return;
-      __nv_bfloat16* dst = p.query + (static_cast<size_t>(t) * p.N + n) * p.Hckv + col0;
-      const bool full = col0 + CH <= p.Hckv;
-      if (full && (((static_cast<size_t>(t) * p.N + n) * p.Hckv + col0) % 8) == 0) {
-#pragma unroll
-        for (int j = 0; j < CH / 8; ++j) {
-          uint4 pk;
-          uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
-            w[h] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          reinterpret_cast<uint4*>(dst)[j] = pk;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < CH; ++j)
-          if (col0 + j < p.Hckv) dst[j] = __float2bfloat16_rn(v[j]);
-      }
+      stage_row_bf16x32(sb, lane, v);
+      ops[0] = {0, 3, n0, n, m0, 0};
     }
+    return 1;
   }
 };
 

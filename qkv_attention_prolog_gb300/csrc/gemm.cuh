@@ -29,6 +29,15 @@ struct GemmGeometry {
   int32_t num_units;
 };
 
+// One TMA store of an epilogue staging tile: which output map, its rank and coordinates, and the
+// tile's byte offset inside the warp's staging buffer.
+struct StoreOp {
+  int32_t which;   // 0: first output map, 1: second
+  int32_t rank;    // 2 or 3
+  int32_t x, y, z;
+  uint32_t soff;
+};
+
 template <int BN_>
 struct GemmCfg {
   static constexpr int BM = 128;
@@ -39,9 +48,11 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SMEM_LIMIT = 232448;          // 227 KB opt-in per CTA
   static constexpr int RESERVED = 1024 + 256;         // alignment slack + barriers
-  static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED) / STAGE_BYTES;
+  static constexpr int EPI_BUF = 4096;                // one staging tile (32 x 32 fp32)
+  static constexpr int EPI_BYTES = 4 * 2 * EPI_BUF;   // 4 epilogue warps, double-buffered
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + RESERVED;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + RESERVED;
   static constexpr int CH = BN >= 32 ? 32 : BN;       // epilogue column chunk
   static constexpr int ACC_COLS = 2 * BN;
   static constexpr uint32_t TMEM_COLS =
@@ -63,17 +74,21 @@ __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& t
   s = u / g.batches;
 }
 
-// Epilogue functor contract:
-//   __device__ void operator()(int row, int col0, int batch, int split, const float* v) const;
-// called by all 32 lanes of an epilogue warp together (it may shuffle across lanes), with `row`
-// the tile-space row of A handled by this lane (may lie beyond the matrix: the functor masks),
-// `col0` the tile-space column of v[0], and CH consecutive accumulator columns in v.
+// Epilogue functor contract (see epilogues.cuh):
+//   __device__ int operator()(int m0, int n0, int batch, int split, const float (&v)[CH],
+//                             uint8_t* stage, StoreOp (&ops)[2]) const;
+// called by all 32 lanes of an epilogue warp together for the 32 x CH accumulator block whose
+// first A row is m0 (lane l holds row m0 + l) and first B row is n0 (v[j] is column n0 + j).  It
+// writes the block's output into the warp's staging buffer and returns the TMA stores (at most
+// two, warp-uniform) that move it to global memory through the two output tensor maps.
 template <int BN, class Epi>
 __global__ void __launch_bounds__(256, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                      const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmB1, const GemmGeometry geo,
+                     const __grid_constant__ CUtensorMap tmB1,
+                     const __grid_constant__ CUtensorMap tmO0,
+                     const __grid_constant__ CUtensorMap tmO1, const GemmGeometry geo,
                      const Epi epi, uint32_t* __restrict__ err_word) {
   using Cfg = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -81,7 +96,8 @@ __global__ void __launch_bounds__(256, 1)
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* smemA = smem;
   uint8_t* smemB = smem + Cfg::STAGES * Cfg::A_BYTES;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+  uint8_t* smemE = smem + Cfg::STAGES * Cfg::STAGE_BYTES;             // epilogue staging
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smemE + Cfg::EPI_BYTES);
   uint64_t* empty_bar = full_bar + Cfg::STAGES;
   uint64_t* accf_bar = empty_bar + Cfg::STAGES;
   uint64_t* acce_bar = accf_bar + 2;
@@ -96,6 +112,8 @@ __global__ void __launch_bounds__(256, 1)
     prefetch_tmap(&tmA1);
     prefetch_tmap(&tmB0);
     prefetch_tmap(&tmB1);
+    prefetch_tmap(&tmO0);
+    prefetch_tmap(&tmO1);
   }
   if (warp == 1 && lane == 0) {
     for (int i = 0; i < Cfg::STAGES; ++i) {
@@ -209,6 +227,8 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    uint8_t* wstage = smemE + q * 2 * Cfg::EPI_BUF;
+    int sel = 0;
     int iter = 0;
     for (int u = blockIdx.x; u < geo.num_units; u += gridDim.x, ++iter) {
       int tm, tn, b, s;
@@ -217,7 +237,7 @@ __global__ void __launch_bounds__(256, 1)
       const uint32_t use = static_cast<uint32_t>(iter >> 1);
       if (!mbar_wait(&accf_bar[buf], use & 1u, abort_flag)) break;
       tc_fence_after_sync();
-      const int row = tm * Cfg::BM + q * 32 + lane;
+      const int m0 = tm * Cfg::BM + q * 32;
       const uint32_t t_addr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::BN);
 #pragma unroll 1
@@ -236,12 +256,33 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
         }
-        epi(row, tn * Cfg::BN + c, b, s, v);
+        if (c + Cfg::CH >= Cfg::BN) {
+          // last TMEM read of this accumulator: hand it back to the MMA warp right away
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce_bar[buf]);
+        }
+        uint8_t* sb = wstage + sel * Cfg::EPI_BUF;
+        sel ^= 1;
+        if (lane == 0) bulk_wait_group_read<1>();   // the store that last read this buffer is done
+        __syncwarp();
+        StoreOp ops[2];
+        const int nops = epi(m0, tn * Cfg::BN + c, b, s, v, sb, ops);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          for (int i = 0; i < nops; ++i) {
+            const CUtensorMap* m = ops[i].which ? &tmO1 : &tmO0;
+            if (ops[i].rank == 2)
+              tma_store_2d(m, sb + ops[i].soff, ops[i].x, ops[i].y);
+            else
+              tma_store_3d(m, sb + ops[i].soff, ops[i].x, ops[i].y, ops[i].z);
+          }
+          bulk_commit_group();
+        }
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce_bar[buf]);
     }
+    if (lane == 0) bulk_wait_group<0>();           // all output writes complete
   }
 
   __syncthreads();

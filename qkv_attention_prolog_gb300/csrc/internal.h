@@ -14,7 +14,8 @@ namespace mlap {
 // One launch of umma_gemm_kernel: the four tensor maps (first/second segment of A and B),
 // the tile geometry, the N tile width, the orientation and the grid.
 struct GemmLaunch {
-  CUtensorMap a0, a1, b0, b1;
+  CUtensorMap a0, a1, b0, b1;   // operand maps (first / second segment)
+  CUtensorMap o0, o1;           // output maps for the epilogue's TMA stores
   GemmGeometry geo;
   int bn;
   bool swap;

@@ -19,6 +19,7 @@ namespace mlap {
 namespace {
 
 constexpr int kNormThreads = 256;
+constexpr int kMaxSplits = 16;   // upper bound on the down-projection's K splits
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -58,12 +59,39 @@ __global__ void __launch_bounds__(kNormThreads)
   grid_launch_dependents();
   grid_dependency_wait();
 
+  // h = sum of the K-split partials, in split order.  All splits of a column are loaded before
+  // the first add so up to kMaxSplits loads per thread are in flight.
   const size_t split_stride = static_cast<size_t>(p.T) * p.Ntot;
   const float* src = p.part + static_cast<size_t>(t) * p.Ntot;
-  for (int f = threadIdx.x; f < p.Ntot; f += blockDim.x) {
-    float a = 0.f;
-    for (int s = 0; s < p.splits; ++s) a += src[s * split_stride + f];
-    h[f] = a;
+  const bool vec = (p.Ntot % 4) == 0;                     // rows then start 16-byte aligned
+  const int ncols = vec ? p.Ntot / 4 : p.Ntot;
+  for (int c = threadIdx.x; c < ncols; c += blockDim.x) {
+    if (vec) {
+      float4 v[kMaxSplits];
+#pragma unroll
+      for (int s = 0; s < kMaxSplits; ++s)
+        if (s < p.splits) v[s] = __ldg(reinterpret_cast<const float4*>(src + s * split_stride) + c);
+      float4 a = v[0];
+#pragma unroll
+      for (int s = 1; s < kMaxSplits; ++s)
+        if (s < p.splits) {
+          a.x += v[s].x;
+          a.y += v[s].y;
+          a.z += v[s].z;
+          a.w += v[s].w;
+        }
+      reinterpret_cast<float4*>(h)[c] = a;
+    } else {
+      float v[kMaxSplits];
+#pragma unroll
+      for (int s = 0; s < kMaxSplits; ++s)
+        if (s < p.splits) v[s] = __ldg(src + s * split_stride + c);
+      float a = v[0];
+#pragma unroll
+      for (int s = 1; s < kMaxSplits; ++s)
+        if (s < p.splits) a += v[s];
+      h[c] = a;
+    }
   }
   __syncthreads();
 
