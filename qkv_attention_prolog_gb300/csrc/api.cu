@@ -152,7 +152,11 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
   const mlap_tensor_t& wuq = a->weight_uq_qr;
   CHECK_STATUS(need(wuq, "weight_uq_qr", false));
   CHECK_STATUS(want_shape(wuq, "weight_uq_qr", {d->Hcq, d->N * (d->D + d->Dr)}));
-  if (wuq.dtype == MLAP_DTYPE_INT8) d->w_int8 = true;
+  if (wuq.dtype == MLAP_DTYPE_INT8) {
+    d->w_int8 = true;
+    if (d->Hcq % 16)
+      return fail(MLAP_ERR_UNSUPPORTED, "int8 weight_uq_qr needs Hcq % 16 == 0 (16-byte TMA row pitch)");
+  }
   else if (wuq.dtype == MLAP_DTYPE_BF16) d->w_int8 = false;
   else return fail(MLAP_ERR_DTYPE, "weight_uq_qr must be bf16 or int8");
 
@@ -341,6 +345,24 @@ mlap_status_t make_out_map(CUtensorMap* m, const void* base, CUtensorMapDataType
   return MLAP_OK;
 }
 
+// 2D int8 weight operand: `rows` rows of `inner` bytes; box of 64 bytes x box_rows rows, no
+// swizzle (the converter warps write the bf16 swizzled layout), zero fill outside.
+mlap_status_t make_tmap_i8(CUtensorMap* m, const void* base, int64_t inner, int64_t rows,
+                           int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return fail(MLAP_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner)};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MLAP_ERR_CUDA, "cuTensorMapEncodeTiled (int8) failed (" + std::to_string(int(r)) + ")");
+  return MLAP_OK;
+}
+
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 int swap_bn(int64_t T) {
@@ -367,7 +389,6 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   const MlaWs L = mla_ws_layout(d);
   if (ws == nullptr || ws_bytes < L.total) return fail(MLAP_ERR_WORKSPACE, "workspace too small");
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(MLAP_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  if (d.w_int8) return fail(MLAP_ERR_UNSUPPORTED, "int8 weight_uq_qr path not built yet");
 
   int dev = 0, sms = 0;
   cudaError_t ce = cudaGetDevice(&dev);
@@ -437,6 +458,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     }
     g.geo.batches = 1;
     g.geo.k_blocks = kb;
+    g.geo.w_op = swap ? 0 : 1;
     g.geo.num_units = g.geo.m_tiles * g.geo.n_tiles * g.geo.splits;
     // partials part[s][t][f]: W^DQ columns and W^DKV|W^KR columns as two 3-D (f, t, s) maps
     const int64_t row_b = Ntot * 4, split_b = d.T * Ntot * 4;
@@ -493,7 +515,10 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.err = err;
     u.swap = swap;
     if (swap) {
-      CHECK_STATUS(make_tmap(&u.a0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 128));
+      if (d.w_int8)
+        CHECK_STATUS(make_tmap_i8(&u.a0, a->weight_uq_qr.data, d.Hcq, Mup, 128));
+      else
+        CHECK_STATUS(make_tmap(&u.a0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 128));
       u.a1 = u.a0;
       CHECK_STATUS(make_tmap(&u.b0, cq, d.Hcq, d.T, d.Hcq, bn_t));
       u.b1 = u.b0;
@@ -503,7 +528,10 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     } else {
       CHECK_STATUS(make_tmap(&u.a0, cq, d.Hcq, d.T, d.Hcq, 128));
       u.a1 = u.a0;
-      CHECK_STATUS(make_tmap(&u.b0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 256));
+      if (d.w_int8)
+        CHECK_STATUS(make_tmap_i8(&u.b0, a->weight_uq_qr.data, d.Hcq, Mup, 256));
+      else
+        CHECK_STATUS(make_tmap(&u.b0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 256));
       u.b1 = u.b0;
       u.bn = 256;
       u.geo.m_tiles = ceil_div(d.T, 128);
@@ -513,6 +541,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.geo.b_seg_tiles = u.geo.n_tiles;
     u.geo.batches = 1;
     u.geo.splits = 1;
+    u.geo.w_op = swap ? 0 : 1;
     u.geo.k_blocks = ceil_div(d.Hcq, 64);
     u.geo.num_units = u.geo.m_tiles * u.geo.n_tiles;
     u.grid = u.geo.num_units < sms ? u.geo.num_units : sms;
@@ -568,6 +597,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.geo.b_seg_tiles = b.geo.n_tiles;
     b.geo.batches = static_cast<int32_t>(d.N);
     b.geo.splits = 1;
+    b.geo.w_op = swap ? 0 : 1;
     b.geo.k_blocks = ceil_div(d.D, 64);
     b.geo.num_units = b.geo.m_tiles * b.geo.n_tiles * b.geo.batches;
     b.grid = b.geo.num_units < sms ? b.geo.num_units : sms;

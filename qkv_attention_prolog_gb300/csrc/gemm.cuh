@@ -4,12 +4,19 @@
 //
 // A and B arrive through TMA tensor maps (128-byte swizzle, 64-element K blocks).  A tile of
 // BM=128 rows of A and BN rows of B is accumulated in tensor memory (TMEM) by one thread issuing
-// tcgen05.mma; four epilogue warps read the accumulator back with tcgen05.ld and hand each row's
-// values to an epilogue functor (the fused RmsNorm-input, RoPE, bf16 rounding, scatter, ...).
-// TMEM holds two accumulators so the epilogue of one tile overlaps the MMAs of the next.
+// tcgen05.mma; four epilogue warps read the accumulator back with tcgen05.ld, hand 32 x 32 blocks
+// to an epilogue functor (the fused rounding, RoPE, dequant, ...) and write its output with TMA
+// stores.  TMEM holds two accumulators so the epilogue of one tile overlaps the MMAs of the next.
 //
-// Warp roles (256 threads):  warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM owner,
-// warp 3 = idle, warps 4..7 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+// One operand is a weight (`w_op`).  Its first pipeline stages are requested before the kernel
+// waits on the previous kernel in the stream (programmatic dependent launch), so the weight
+// stream starts while the producer of the activations is still finishing.  With WQ != 0 the
+// weight is int8: TMA brings the raw int8 tile and four converter warps expand it to bf16 in the
+// swizzled operand layout (exact for |v| <= 127); the MMA then runs in bf16 with fp32
+// accumulation, which is exact for integer partial sums below 2^24.
+//
+// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM owner, warp 3 = idle,
+// warps 4..7 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31), warps 8..11 = int8 converters.
 //
 // Work units: (m tile, n tile, batch, k split), m fastest, distributed round-robin over a grid
 // of at most one CTA per SM.  Either operand may be "segmented": tiles below *_seg_tiles come
@@ -27,6 +34,7 @@ struct GemmGeometry {
   int32_t a_x_batch, a_y_batch;     // per-batch offsets of the TMA coordinates (elements, rows)
   int32_t b_x_batch, b_y_batch;
   int32_t num_units;
+  int32_t w_op;                     // operand holding the weight: 0 = A, 1 = B
 };
 
 // One TMA store of an epilogue staging tile: which output map, its rank and coordinates, and the
@@ -38,29 +46,33 @@ struct StoreOp {
   uint32_t soff;
 };
 
-template <int BN_>
+// WQ: 0 = bf16 weight, 1 = int8 weight in operand A, 2 = int8 weight in operand B.
+template <int BN_, int WQ_ = 0>
 struct GemmCfg {
+  static constexpr int WQ = WQ_;
   static constexpr int BM = 128;
   static constexpr int BN = BN_;
   static constexpr int BK = 64;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int SMEM_LIMIT = 232448;          // 227 KB opt-in per CTA
-  static constexpr int RESERVED = 1024 + 256;         // alignment slack + barriers
-  static constexpr int EPI_BUF = 4096;                // one staging tile (32 x 32 fp32)
-  static constexpr int EPI_BYTES = 4 * 2 * EPI_BUF;   // 4 epilogue warps, double-buffered
+  static constexpr int RAW_ROWS = WQ == 1 ? BM : (WQ == 2 ? BN : 0);
+  static constexpr int RAW_BYTES = RAW_ROWS * BK;      // int8 weight tile
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + RAW_BYTES;
+  static constexpr int SMEM_LIMIT = 232448;            // 227 KB opt-in per CTA
+  static constexpr int RESERVED = 1024 + 512;          // alignment slack + barriers
+  static constexpr int EPI_BUF = 4096;                 // one staging tile (32 x 32 fp32)
+  static constexpr int EPI_BYTES = 4 * 2 * EPI_BUF;    // 4 epilogue warps, double-buffered
   static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + RESERVED;
-  static constexpr int CH = BN >= 32 ? 32 : BN;       // epilogue column chunk
+  static constexpr int CH = BN >= 32 ? 32 : BN;        // epilogue column chunk
   static constexpr int ACC_COLS = 2 * BN;
   static constexpr uint32_t TMEM_COLS =
       ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-  static constexpr int THREADS = 256;
+  static constexpr int THREADS = WQ ? 384 : 256;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16,256]");
-  static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-B alignment");
+  static_assert(B_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages must keep 1024-B alignment");
   static_assert(STAGES >= 2, "pipeline needs two stages");
 };
 
@@ -74,6 +86,35 @@ __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& t
   s = u / g.batches;
 }
 
+// One row of an int8 weight tile (64 values, 64 B) to bf16 in the 128B-swizzled K-major layout
+// (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7)) << 4)).  The four source chunks are visited
+// in a row-dependent order to spread shared-memory banks.
+__device__ __forceinline__ void convert_int8_row(const uint8_t* src_row, uint8_t* dst, int r) {
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int i = (ii + r) & 3;
+    const uint4 raw = *reinterpret_cast<const uint4*>(src_row + i * 16);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float f0 = static_cast<float>(static_cast<int8_t>(w[k] & 0xffu));
+      const float f1 = static_cast<float>(static_cast<int8_t>((w[k] >> 8) & 0xffu));
+      const float f2 = static_cast<float>(static_cast<int8_t>((w[k] >> 16) & 0xffu));
+      const float f3 = static_cast<float>(static_cast<int8_t>(w[k] >> 24));
+      // bf16 of a small integer is the upper half of its fp32 bit pattern (exact for |v| <= 256)
+      out[2 * k] = (__float_as_uint(f0) >> 16) | (__float_as_uint(f1) & 0xffff0000u);
+      out[2 * k + 1] = (__float_as_uint(f2) >> 16) | (__float_as_uint(f3) & 0xffff0000u);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = 2 * i + h;
+      *reinterpret_cast<uint4*>(dst + r * 128 + (((c ^ (r & 7)) & 7) << 4)) =
+          make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+    }
+  }
+}
+
 // Epilogue functor contract (see epilogues.cuh):
 //   __device__ int operator()(int m0, int n0, int batch, int split, const float (&v)[CH],
 //                             uint8_t* stage, StoreOp (&ops)[2]) const;
@@ -81,8 +122,8 @@ __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& t
 // first A row is m0 (lane l holds row m0 + l) and first B row is n0 (v[j] is column n0 + j).  It
 // writes the block's output into the warp's staging buffer and returns the TMA stores (at most
 // two, warp-uniform) that move it to global memory through the two output tensor maps.
-template <int BN, class Epi>
-__global__ void __launch_bounds__(256, 1)
+template <int BN, class Epi, int WQ>
+__global__ void __launch_bounds__(GemmCfg<BN, WQ>::THREADS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                      const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB0,
@@ -90,22 +131,25 @@ __global__ void __launch_bounds__(256, 1)
                      const __grid_constant__ CUtensorMap tmO0,
                      const __grid_constant__ CUtensorMap tmO1, const GemmGeometry geo,
                      const Epi epi, uint32_t* __restrict__ err_word) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, WQ>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* smemA = smem;
-  uint8_t* smemB = smem + Cfg::STAGES * Cfg::A_BYTES;
-  uint8_t* smemE = smem + Cfg::STAGES * Cfg::STAGE_BYTES;             // epilogue staging
+  uint8_t* smemB = smemA + Cfg::STAGES * Cfg::A_BYTES;
+  uint8_t* smemR = smemB + Cfg::STAGES * Cfg::B_BYTES;                  // raw int8 tiles
+  uint8_t* smemE = smemR + Cfg::STAGES * Cfg::RAW_BYTES;                // epilogue staging
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smemE + Cfg::EPI_BYTES);
   uint64_t* empty_bar = full_bar + Cfg::STAGES;
-  uint64_t* accf_bar = empty_bar + Cfg::STAGES;
+  uint64_t* rawf_bar = empty_bar + Cfg::STAGES;
+  uint64_t* accf_bar = rawf_bar + Cfg::STAGES;
   uint64_t* acce_bar = accf_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const bool w_is_a = geo.w_op == 0;
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA0);
@@ -117,8 +161,9 @@ __global__ void __launch_bounds__(256, 1)
   }
   if (warp == 1 && lane == 0) {
     for (int i = 0; i < Cfg::STAGES; ++i) {
-      mbar_init(&full_bar[i], 1);
+      mbar_init(&full_bar[i], WQ ? 1 + 4 : 1);   // producer (+ one arrival per converter warp)
       mbar_init(&empty_bar[i], 1);
+      mbar_init(&rawf_bar[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf_bar[i], 1);
@@ -136,37 +181,81 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Let the next kernel in the stream start its prologue; wait for the previous one's results.
+  // Let the next kernel in the stream start its prologue.  Every role except the producer waits
+  // for the previous kernel's results here; the producer first requests weight tiles.
   grid_launch_dependents();
-  grid_dependency_wait();
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      auto coords = [&](int u, int& tm, int& tn, int& b, int& kb0, int& kb1) {
+        int s;
+        decode_unit(geo, u, tm, tn, b, s);
+        kb0 = (s * geo.k_blocks) / geo.splits;
+        kb1 = ((s + 1) * geo.k_blocks) / geo.splits;
+      };
+      auto load_a = [&](int tm, int b, int kb, uint64_t* bar, void* dst) {
+        const bool first = tm < geo.a_seg_tiles;
+        const int y = (first ? tm : tm - geo.a_seg_tiles) * Cfg::BM + b * geo.a_y_batch;
+        tma_load_2d(dst, first ? &tmA0 : &tmA1, bar, kb * Cfg::BK + b * geo.a_x_batch, y);
+      };
+      auto load_b = [&](int tn, int b, int kb, uint64_t* bar, void* dst) {
+        const bool first = tn < geo.b_seg_tiles;
+        const int y = (first ? tn : tn - geo.b_seg_tiles) * Cfg::BN + b * geo.b_y_batch;
+        tma_load_2d(dst, first ? &tmB0 : &tmB1, bar, kb * Cfg::BK + b * geo.b_x_batch, y);
+      };
+      // weight tile of stage st (bf16 into the operand buffer, or int8 into the raw buffer)
+      auto issue_weight = [&](int st, int tm, int tn, int b, int kb) {
+        if constexpr (WQ != 0) {
+          mbar_arrive_expect_tx(&rawf_bar[st], Cfg::RAW_BYTES);
+          if (WQ == 1) load_a(tm, b, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES);
+          else load_b(tn, b, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES);
+        } else if (w_is_a) {
+          mbar_expect_tx(&full_bar[st], Cfg::A_BYTES);
+          load_a(tm, b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
+        } else {
+          mbar_expect_tx(&full_bar[st], Cfg::B_BYTES);
+          load_b(tn, b, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
+        }
+      };
+      auto issue_act = [&](int st, int tm, int tn, int b, int kb) {
+        if (w_is_a) {
+          mbar_arrive_expect_tx(&full_bar[st], Cfg::B_BYTES);
+          load_b(tn, b, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
+        } else {
+          mbar_arrive_expect_tx(&full_bar[st], Cfg::A_BYTES);
+          load_a(tm, b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
+        }
+      };
+
+      // Weight tiles of this CTA's first stages, before the grid dependency resolves.
+      int pre = 0;
+      if (static_cast<int>(blockIdx.x) < geo.num_units) {
+        int tm, tn, b, kb0, kb1;
+        coords(blockIdx.x, tm, tn, b, kb0, kb1);
+        pre = kb1 - kb0 < Cfg::STAGES ? kb1 - kb0 : Cfg::STAGES;
+        for (int i = 0; i < pre; ++i) issue_weight(i, tm, tn, b, kb0 + i);
+      }
+      grid_dependency_wait();
+
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < geo.num_units && ok; u += gridDim.x) {
-        int tm, tn, b, s;
-        decode_unit(geo, u, tm, tn, b, s);
-        const int kb0 = (s * geo.k_blocks) / geo.splits;
-        const int kb1 = ((s + 1) * geo.k_blocks) / geo.splits;
-        const bool a_first = tm < geo.a_seg_tiles;
-        const bool b_first = tn < geo.b_seg_tiles;
-        const CUtensorMap* mapA = a_first ? &tmA0 : &tmA1;
-        const CUtensorMap* mapB = b_first ? &tmB0 : &tmB1;
-        const int ay = (a_first ? tm : tm - geo.a_seg_tiles) * Cfg::BM + b * geo.a_y_batch;
-        const int by = (b_first ? tn : tn - geo.b_seg_tiles) * Cfg::BN + b * geo.b_y_batch;
+        int tm, tn, b, kb0, kb1;
+        coords(u, tm, tn, b, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
-            ok = false;
-            break;
+          const bool prefetched = u == static_cast<int>(blockIdx.x) && kb - kb0 < pre;
+          if (!prefetched) {
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            issue_weight(stage, tm, tn, b, kb);
           }
-          mbar_arrive_expect_tx(&full_bar[stage], Cfg::STAGE_BYTES);
-          tma_load_2d(smemA + stage * Cfg::A_BYTES, mapA, &full_bar[stage],
-                      kb * Cfg::BK + b * geo.a_x_batch, ay);
-          tma_load_2d(smemB + stage * Cfg::B_BYTES, mapB, &full_bar[stage],
-                      kb * Cfg::BK + b * geo.b_x_batch, by);
+          issue_act(stage, tm, tn, b, kb);
           if (++stage == Cfg::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -180,6 +269,10 @@ __global__ void __launch_bounds__(256, 1)
           const uint32_t par = (i < stage) ? phase : (phase ^ 1u);
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(&full_bar[i], par) && globaltimer_ns() - t0 < 20000000ull) {
+          }
+          if (WQ) {
+            while (!mbar_try_wait(&rawf_bar[i], par) && globaltimer_ns() - t0 < 20000000ull) {
+            }
           }
         }
       }
@@ -224,7 +317,7 @@ __global__ void __launch_bounds__(256, 1)
         if (ok) umma_commit(&accf_bar[buf]);   // accumulator ready for the epilogue
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
     uint8_t* wstage = smemE + q * 2 * Cfg::EPI_BUF;
@@ -283,6 +376,34 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     if (lane == 0) bulk_wait_group<0>();           // all output writes complete
+  } else if (WQ != 0 && warp >= 8) {
+    // ------------------------------------------------------------------ int8 -> bf16 converters
+    const int ct = threadIdx.x - 256;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < geo.num_units && ok; u += gridDim.x) {
+      int tm, tn, b, s;
+      decode_unit(geo, u, tm, tn, b, s);
+      const int kb0 = (s * geo.k_blocks) / geo.splits;
+      const int kb1 = ((s + 1) * geo.k_blocks) / geo.splits;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&rawf_bar[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* raw = smemR + stage * Cfg::RAW_BYTES;
+        uint8_t* dst = WQ == 1 ? smemA + stage * Cfg::A_BYTES : smemB + stage * Cfg::B_BYTES;
+        for (int r = ct; r < Cfg::RAW_ROWS; r += 128) convert_int8_row(raw + r * Cfg::BK, dst, r);
+        fence_proxy_async_shared();              // generic writes -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_bar[stage]);
+        if (++stage == Cfg::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   }
 
   __syncthreads();

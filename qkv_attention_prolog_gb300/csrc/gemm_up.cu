@@ -1,23 +1,30 @@
 // Up-projection c^Q·[W^UQ | W^QR] with fused q^C rounding and query RoPE (MlaPrologV2 README:
-// q^C and q^R formulas; RoPE of aclnnQkvRmsNormRopeCache "Formulas" (3)).
+// q^C and q^R formulas; RoPE of aclnnQkvRmsNormRopeCache "Formulas" (3)), for a bf16 weight or an
+// int8 weight with per-channel dequant (the partial-quant scenario).
 #include "gemm_launch.cuh"
 
 namespace mlap {
 
-cudaError_t launch_up(const GemmLaunch& L, const UpParams& p, bool int8) {
-  if (int8) return cudaErrorNotSupported;
+template <bool INT8>
+static cudaError_t launch_up_t(const GemmLaunch& L, const UpParams& p) {
+  constexpr int WA = INT8 ? 1 : 0;   // int8 weight as operand A (decode orientation)
+  constexpr int WB = INT8 ? 2 : 0;   // int8 weight as operand B (prefill orientation)
   if (L.swap) {
     switch (L.bn) {
-      case 16: return launch_gemm_t<16>(L, EpiUp<true, false, 16>{p});
-      case 32: return launch_gemm_t<32>(L, EpiUp<true, false, 32>{p});
-      case 64: return launch_gemm_t<64>(L, EpiUp<true, false, 32>{p});
-      case 128: return launch_gemm_t<128>(L, EpiUp<true, false, 32>{p});
-      case 256: return launch_gemm_t<256>(L, EpiUp<true, false, 32>{p});
+      case 16: return launch_gemm_t<16, WA>(L, EpiUp<true, INT8, 16>{p});
+      case 32: return launch_gemm_t<32, WA>(L, EpiUp<true, INT8, 32>{p});
+      case 64: return launch_gemm_t<64, WA>(L, EpiUp<true, INT8, 32>{p});
+      case 128: return launch_gemm_t<128, WA>(L, EpiUp<true, INT8, 32>{p});
+      case 256: return launch_gemm_t<256, WA>(L, EpiUp<true, INT8, 32>{p});
       default: return cudaErrorInvalidValue;
     }
   }
   if (L.bn != 256) return cudaErrorInvalidValue;
-  return launch_gemm_t<256>(L, EpiUp<false, false, 32>{p});
+  return launch_gemm_t<256, WB>(L, EpiUp<false, INT8, 32>{p});
+}
+
+cudaError_t launch_up(const GemmLaunch& L, const UpParams& p, bool int8) {
+  return int8 ? launch_up_t<true>(L, p) : launch_up_t<false>(L, p);
 }
 
 }  // namespace mlap

@@ -143,3 +143,28 @@ def test_outputs_have_no_stray_writes():
     torch.cuda.synchronize()
     for buf, n in ((qbuf, d.T * d.N * d.Hckv), (rbuf, d.T * d.N * d.Dr)):
         assert bool((buf[:guard] == 7.0).all()) and bool((buf[guard + n:] == 7.0).all())
+
+
+def test_partial_quant_int8_caches():
+    # int8 weight_uq_qr (per-channel dequant), dynamic per-token c^Q quant, int8 caches
+    _full_check(synthetic.MLA_PARTIAL_QUANT)
+
+
+def test_partial_quant_bf16_caches():
+    _full_check(synthetic.MLA_PARTIAL_QUANT_BF16CACHE)
+
+
+QUANT_SHAPES = [
+    dict(B=5, S=1, He=256, Hcq=128, N=3, cache_dtype="int8"),             # decode orientation
+    dict(B=3, S=100, He=384, Hcq=192, Hckv=128, N=2, cache_dtype="int8"),  # prefill orientation
+    dict(B=2, S=150, He=256, Hcq=144, Hckv=96, N=2, Dr=32, cache_dtype="bf16"),
+]
+
+
+@pytest.mark.parametrize("kw", QUANT_SHAPES, ids=[str(i) for i in range(len(QUANT_SHAPES))])
+def test_partial_quant_shapes(kw):
+    kw = dict(kw)
+    block_num = max(1, (kw["B"] * kw["S"] + 127) // 128 + 1)
+    case = synthetic.small_mla_case("pq", block_num=block_num, n_skip=1,
+                                    weight_uq_qr_dtype="int8", **kw)
+    _full_check(case)
