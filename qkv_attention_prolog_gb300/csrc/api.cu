@@ -365,6 +365,15 @@ mlap_status_t make_tmap_i8(CUtensorMap* m, const void* base, int64_t inner, int6
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
+// Persistent grid with equal work per CTA: the fewest CTAs that still finish the units in the
+// minimum number of rounds (e.g. 192 units on 152 SMs -> 96 CTAs x 2 units instead of a second
+// round that only 40 CTAs run).
+int balanced_grid(int units, int sms) {
+  if (units <= 0) return 1;
+  const int rounds = ceil_div(units, sms);
+  return ceil_div(units, rounds);
+}
+
 int swap_bn(int64_t T) {
   int bn = 16;
   while (bn < T) bn *= 2;
@@ -468,7 +477,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     CHECK_STATUS(make_out_map(&g.o1, part + d.Hcq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                               {d.Hckv + d.Dr, d.T, g.geo.splits}, {row_b, split_b}, {32, ch_t, 1},
                               CU_TENSOR_MAP_SWIZZLE_128B));
-    g.grid = g.geo.num_units < sms ? g.geo.num_units : sms;
+    g.grid = balanced_grid(g.geo.num_units, sms);
     CHECK_STATUS(rec(0));
     ce = launch_down(g, dp);
     if (ce != cudaSuccess) return cuda_fail(ce, "down-projection launch");
@@ -544,7 +553,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.geo.w_op = swap ? 0 : 1;
     u.geo.k_blocks = ceil_div(d.Hcq, 64);
     u.geo.num_units = u.geo.m_tiles * u.geo.n_tiles;
-    u.grid = u.geo.num_units < sms ? u.geo.num_units : sms;
+    u.grid = balanced_grid(u.geo.num_units, sms);
     CHECK_STATUS(make_out_map(&u.o0, qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, {d.N * d.D, d.T},
                               {d.N * d.D * 2}, {32, ch_t}, CU_TENSOR_MAP_SWIZZLE_64B));
     CHECK_STATUS(make_out_map(&u.o1, a->query_rope.data, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
@@ -600,7 +609,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.geo.w_op = swap ? 0 : 1;
     b.geo.k_blocks = ceil_div(d.D, 64);
     b.geo.num_units = b.geo.m_tiles * b.geo.n_tiles * b.geo.batches;
-    b.grid = b.geo.num_units < sms ? b.geo.num_units : sms;
+    b.grid = balanced_grid(b.geo.num_units, sms);
     CHECK_STATUS(make_out_map(&b.o0, a->query.data, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                               {d.Hckv, d.N, d.T}, {d.Hckv * 2, d.N * d.Hckv * 2}, {32, 1, ch_t},
                               CU_TENSOR_MAP_SWIZZLE_64B));

@@ -18,30 +18,39 @@ namespace mlap {
 
 namespace {
 
-constexpr int kNormThreads = 256;
 constexpr int kMaxSplits = 16;   // upper bound on the down-projection's K splits
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
+template <int NT>
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+  }
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
   if (l == 0) red[w] = v;
   __syncthreads();
-  float r = 0.f;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r += red[i];   // fixed order: deterministic
+  float2 r = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) {            // fixed order: deterministic
+    r.x += red[i].x;
+    r.y += red[i].y;
+  }
+  __syncthreads();
   return r;
 }
 
+template <int NT>
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
   if (l == 0) red[w] = v;
   __syncthreads();
   float r = 0.f;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) r = fmaxf(r, red[i]);
+  __syncthreads();
   return r;
 }
 
@@ -51,29 +60,45 @@ __device__ __forceinline__ int8_t quant_i8(float v, float scale, int lo, int hi)
   return static_cast<int8_t>(q);
 }
 
-__global__ void __launch_bounds__(kNormThreads)
-    norm_rope_scatter_kernel(const FinalizeParams p) {
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float* out) {
+  const uint4 r = __ldg(reinterpret_cast<const uint4*>(p));
+  const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&r);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out[i] = __bfloat162float(e[i]);
+}
+
+__device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float* v) {
+  uint4 r;
+  __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) e[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = r;
+}
+
+// One CTA per token.  MAXS bounds the K splits (1: prefill, no split; kMaxSplits: decode), NT is
+// the thread count: with splits every thread issues the loads of all splits of its columns at
+// once (one round of latency), without them the kernel stays small enough for many CTAs per SM.
+template <int MAXS, int NT>
+__global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizeParams p) {
   extern __shared__ float h[];
-  __shared__ float red[32];
+  __shared__ float2 red[NT / 32];
   const int t = blockIdx.x;
   grid_launch_dependents();
   grid_dependency_wait();
 
-  // h = sum of the K-split partials, in split order.  All splits of a column are loaded before
-  // the first add so up to kMaxSplits loads per thread are in flight.
+  // h = sum of the K-split partials, in split order.
   const size_t split_stride = static_cast<size_t>(p.T) * p.Ntot;
   const float* src = p.part + static_cast<size_t>(t) * p.Ntot;
-  const bool vec = (p.Ntot % 4) == 0;                     // rows then start 16-byte aligned
-  const int ncols = vec ? p.Ntot / 4 : p.Ntot;
-  for (int c = threadIdx.x; c < ncols; c += blockDim.x) {
-    if (vec) {
-      float4 v[kMaxSplits];
+  if ((p.Ntot % 4) == 0) {                       // rows start 16-byte aligned
+    const int ncols = p.Ntot / 4;
+    for (int c = threadIdx.x; c < ncols; c += NT) {
+      float4 v[MAXS];
 #pragma unroll
-      for (int s = 0; s < kMaxSplits; ++s)
+      for (int s = 0; s < MAXS; ++s)
         if (s < p.splits) v[s] = __ldg(reinterpret_cast<const float4*>(src + s * split_stride) + c);
       float4 a = v[0];
 #pragma unroll
-      for (int s = 1; s < kMaxSplits; ++s)
+      for (int s = 1; s < MAXS; ++s)
         if (s < p.splits) {
           a.x += v[s].x;
           a.y += v[s].y;
@@ -81,54 +106,58 @@ __global__ void __launch_bounds__(kNormThreads)
           a.w += v[s].w;
         }
       reinterpret_cast<float4*>(h)[c] = a;
-    } else {
-      float v[kMaxSplits];
+    }
+  } else {
+    for (int c = threadIdx.x; c < p.Ntot; c += NT) {
+      float v[MAXS];
 #pragma unroll
-      for (int s = 0; s < kMaxSplits; ++s)
+      for (int s = 0; s < MAXS; ++s)
         if (s < p.splits) v[s] = __ldg(src + s * split_stride + c);
       float a = v[0];
 #pragma unroll
-      for (int s = 1; s < kMaxSplits; ++s)
+      for (int s = 1; s < MAXS; ++s)
         if (s < p.splits) a += v[s];
       h[c] = a;
     }
   }
   __syncthreads();
 
-  // ---- c^Q
-  float ss = 0.f;
-  for (int f = threadIdx.x; f < p.Hcq; f += blockDim.x) ss += h[f] * h[f];
-  ss = block_sum(ss, red);
-  const float rq = 1.0f / sqrtf(ss / static_cast<float>(p.Hcq) + p.eps_cq);
+  // sums of squares of the c^Q and c^KV parts, one reduction
+  const float* hkv = h + p.Hcq;
+  float2 ss = make_float2(0.f, 0.f);
+  for (int f = threadIdx.x; f < p.Hcq; f += NT) ss.x += h[f] * h[f];
+  for (int f = threadIdx.x; f < p.Hckv; f += NT) ss.y += hkv[f] * hkv[f];
+  ss = block_sum2<NT>(ss, red);
+  const float rq = 1.0f / sqrtf(ss.x / static_cast<float>(p.Hcq) + p.eps_cq);
+  const float rkv = 1.0f / sqrtf(ss.y / static_cast<float>(p.Hckv) + p.eps_ckv);
+
+  // ---- c^Q (Hcq % 8 == 0): bf16, or int8 codes held exactly in bf16
   __nv_bfloat16* cq = p.cq_out + static_cast<size_t>(t) * p.Hcq;
   if (p.smooth == nullptr) {
-    for (int f = threadIdx.x; f < p.Hcq; f += blockDim.x)
-      cq[f] = __float2bfloat16_rn(h[f] * rq * __bfloat162float(p.gamma_cq[f]));
+    for (int f = threadIdx.x * 8; f < p.Hcq; f += NT * 8) {
+      float g[8], v[8];
+      load8_bf16(p.gamma_cq + f, g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = h[f + i] * rq * g[i];
+      store8_bf16(cq + f, v);
+    }
   } else {
     float amax = 0.f;
-    for (int f = threadIdx.x; f < p.Hcq; f += blockDim.x) {
-      const float c = __bfloat162float(
-          __float2bfloat16_rn(h[f] * rq * __bfloat162float(p.gamma_cq[f])));
-      amax = fmaxf(amax, fabsf(__fmul_rn(c, p.smooth[f])));
-    }
-    amax = block_max(amax, red);
-    const float scale = __fdiv_rn(amax, 127.0f);
-    for (int f = threadIdx.x; f < p.Hcq; f += blockDim.x) {
+    for (int f = threadIdx.x; f < p.Hcq; f += NT) {
       const float c = __bfloat162float(
           __float2bfloat16_rn(h[f] * rq * __bfloat162float(p.gamma_cq[f])));
       const float s = __fmul_rn(c, p.smooth[f]);
-      const int code = scale > 0.f ? quant_i8(s, scale, -127, 127) : 0;
+      h[f] = s;                                   // own element only: no race
+      amax = fmaxf(amax, fabsf(s));
+    }
+    amax = block_max<NT>(amax, reinterpret_cast<float*>(red));
+    const float scale = __fdiv_rn(amax, 127.0f);
+    for (int f = threadIdx.x; f < p.Hcq; f += NT) {
+      const int code = scale > 0.f ? quant_i8(h[f], scale, -127, 127) : 0;
       cq[f] = __float2bfloat16_rn(static_cast<float>(code));   // exact: |code| <= 127
     }
     if (threadIdx.x == 0) p.scale_t[t] = scale;
   }
-
-  // ---- c^KV
-  const float* hkv = h + p.Hcq;
-  float sk = 0.f;
-  for (int f = threadIdx.x; f < p.Hckv; f += blockDim.x) sk += hkv[f] * hkv[f];
-  sk = block_sum(sk, red);
-  const float rkv = 1.0f / sqrtf(sk / static_cast<float>(p.Hckv) + p.eps_ckv);
 
   if (p.slots <= 0) return;                 // empty caches: outputs only
   const int64_t idx = p.cache_index[t];
@@ -136,17 +165,26 @@ __global__ void __launch_bounds__(kNormThreads)
     if (idx != -1 && threadIdx.x == 0) atomicOr(p.err, kErrIndexRange);
     return;
   }
-  for (int f = threadIdx.x; f < p.Hckv; f += blockDim.x) {
-    const float v = hkv[f] * rkv * __bfloat162float(p.gamma_ckv[f]);
-    if (p.kv_int8)
-      static_cast<int8_t*>(p.kv_cache)[idx * p.Hckv + f] = quant_i8(v, p.qs_ckv[f], -128, 127);
-    else
-      static_cast<__nv_bfloat16*>(p.kv_cache)[idx * p.Hckv + f] = __float2bfloat16_rn(v);
+  // ---- c^KV (Hckv % 8 == 0)
+  for (int f = threadIdx.x * 8; f < p.Hckv; f += NT * 8) {
+    float g[8], v[8];
+    load8_bf16(p.gamma_ckv + f, g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = hkv[f + i] * rkv * g[i];
+    if (p.kv_int8) {
+      uint2 q;
+      int8_t* qb = reinterpret_cast<int8_t*>(&q);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) qb[i] = quant_i8(v[i], p.qs_ckv[f + i], -128, 127);
+      *reinterpret_cast<uint2*>(static_cast<int8_t*>(p.kv_cache) + idx * p.Hckv + f) = q;
+    } else {
+      store8_bf16(static_cast<__nv_bfloat16*>(p.kv_cache) + idx * p.Hckv + f, v);
+    }
   }
   // ---- k^R
   const float* hkr = h + p.Hcq + p.Hckv;
   const int half = p.Dr >> 1;
-  for (int j = threadIdx.x; j < p.Dr; j += blockDim.x) {
+  for (int j = threadIdx.x; j < p.Dr; j += NT) {
     const float y = hkr[j];
     const float partner = j < half ? -hkr[j + half] : hkr[j - half];
     const float c = __bfloat162float(p.cos[static_cast<size_t>(t) * p.Dr + j]);
@@ -198,15 +236,17 @@ __global__ void prepack_kernel(const PrepackParams p) {
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {
   const size_t smem = static_cast<size_t>(p.Ntot) * sizeof(float);
+  const bool split = p.splits > 1;
+  auto kern = split ? norm_rope_scatter_kernel<kMaxSplits, 512> : norm_rope_scatter_kernel<1, 256>;
+  if (p.splits > kMaxSplits) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(norm_rope_scatter_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.T));
-  cfg.blockDim = dim3(kNormThreads);
+  cfg.blockDim = dim3(split ? 512 : 256);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -214,7 +254,7 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool p
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, norm_rope_scatter_kernel, p);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 cudaError_t launch_prepack(const PrepackParams& p, cudaStream_t stream) {
