@@ -416,6 +416,9 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   const int64_t Mup = d.N * (d.D + d.Dr);
   const int64_t slots = d.BlockNum * d.BlockSize;
   const int bn_t = swap_bn(d.T);
+  // decode orientation: units of 256 weight rows (two accumulators) when they fit in TMEM
+  const int mt = 1;                          // two-tile units pay off only with all SMs busy
+  const int wrows = 128 * mt;
 
   auto rec = [&](int phase) -> mlap_status_t {
     if (timer == nullptr) return MLAP_OK;
@@ -430,18 +433,19 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   g.pdl = true;
   g.err = err;
   g.swap = swap;
+  g.mt = swap ? mt : 1;
   DownParams dp{0};
   const int ch_t = swap ? (bn_t < 32 ? bn_t : 32) : 32;   // tokens per epilogue store box
   {
     const int kb = ceil_div(d.He, 64);
     if (swap) {
-      const int seg = ceil_div(d.Hcq, 128);
-      CHECK_STATUS(make_tmap(&g.a0, a->weight_dq.data, d.He, d.Hcq, d.He, 128));
-      CHECK_STATUS(make_tmap(&g.a1, a->weight_dkv_kr.data, d.He, d.Hckv + d.Dr, d.He, 128));
+      const int seg = ceil_div(d.Hcq, wrows);
+      CHECK_STATUS(make_tmap(&g.a0, a->weight_dq.data, d.He, d.Hcq, d.He, wrows));
+      CHECK_STATUS(make_tmap(&g.a1, a->weight_dkv_kr.data, d.He, d.Hckv + d.Dr, d.He, wrows));
       CHECK_STATUS(make_tmap(&g.b0, a->token_x.data, d.He, d.T, d.He, bn_t));
       g.b1 = g.b0;
       g.bn = bn_t;
-      g.geo.m_tiles = seg + ceil_div(d.Hckv + d.Dr, 128);
+      g.geo.m_tiles = seg + ceil_div(d.Hckv + d.Dr, wrows);
       g.geo.n_tiles = 1;
       g.geo.a_seg_tiles = seg;
       g.geo.b_seg_tiles = 1;
@@ -523,16 +527,17 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.pdl = true;
     u.err = err;
     u.swap = swap;
+    u.mt = swap ? mt : 1;
     if (swap) {
       if (d.w_int8)
-        CHECK_STATUS(make_tmap_i8(&u.a0, a->weight_uq_qr.data, d.Hcq, Mup, 128));
+        CHECK_STATUS(make_tmap_i8(&u.a0, a->weight_uq_qr.data, d.Hcq, Mup, wrows));
       else
-        CHECK_STATUS(make_tmap(&u.a0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 128));
+        CHECK_STATUS(make_tmap(&u.a0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, wrows));
       u.a1 = u.a0;
       CHECK_STATUS(make_tmap(&u.b0, cq, d.Hcq, d.T, d.Hcq, bn_t));
       u.b1 = u.b0;
       u.bn = bn_t;
-      u.geo.m_tiles = ceil_div(Mup, 128);
+      u.geo.m_tiles = ceil_div(Mup, wrows);
       u.geo.n_tiles = 1;
     } else {
       CHECK_STATUS(make_tmap(&u.a0, cq, d.Hcq, d.T, d.Hcq, 128));
@@ -577,13 +582,14 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.pdl = true;
     b.err = err;
     b.swap = swap;
+    b.mt = swap ? mt : 1;
     if (swap) {
-      CHECK_STATUS(make_tmap(&b.a0, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, 128));
+      CHECK_STATUS(make_tmap(&b.a0, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, wrows));
       b.a1 = b.a0;
       CHECK_STATUS(make_tmap(&b.b0, qc, d.N * d.D, d.T, d.N * d.D, bn_t));
       b.b1 = b.b0;
       b.bn = bn_t;
-      b.geo.m_tiles = ceil_div(d.Hckv, 128);
+      b.geo.m_tiles = ceil_div(d.Hckv, wrows);
       b.geo.n_tiles = 1;
       b.geo.a_x_batch = 0;
       b.geo.a_y_batch = static_cast<int32_t>(d.Hckv);

@@ -15,6 +15,10 @@
 // swizzled operand layout (exact for |v| <= 127); the MMA then runs in bf16 with fp32
 // accumulation, which is exact for integer partial sums below 2^24.
 //
+// In the decode orientation a unit may hold MT = 2 row tiles of A (256 weight rows): one TMA box
+// brings both, and two MMAs per K step share the B tile, so each weight byte costs half the
+// activation traffic and half the TMA operations.
+//
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM owner, warp 3 = idle,
 // warps 4..7 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31), warps 8..11 = int8 converters.
 //
@@ -47,15 +51,18 @@ struct StoreOp {
 };
 
 // WQ: 0 = bf16 weight, 1 = int8 weight in operand A, 2 = int8 weight in operand B.
-template <int BN_, int WQ_ = 0>
+// MT: 128-row tiles of A per unit (1 or 2), each with its own TMEM accumulator.
+template <int BN_, int WQ_ = 0, int MT_ = 1>
 struct GemmCfg {
   static constexpr int WQ = WQ_;
-  static constexpr int BM = 128;
+  static constexpr int MT = MT_;
+  static constexpr int BM = 128;                       // rows per MMA
+  static constexpr int BM_U = BM * MT;                 // rows of A per unit
   static constexpr int BN = BN_;
   static constexpr int BK = 64;
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int A_BYTES = BM_U * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int RAW_ROWS = WQ == 1 ? BM : (WQ == 2 ? BN : 0);
+  static constexpr int RAW_ROWS = WQ == 1 ? BM_U : (WQ == 2 ? BN : 0);
   static constexpr int RAW_BYTES = RAW_ROWS * BK;      // int8 weight tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + RAW_BYTES;
   static constexpr int SMEM_LIMIT = 232448;            // 227 KB opt-in per CTA
@@ -66,7 +73,7 @@ struct GemmCfg {
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + RESERVED;
   static constexpr int CH = BN >= 32 ? 32 : BN;        // epilogue column chunk
-  static constexpr int ACC_COLS = 2 * BN;
+  static constexpr int ACC_COLS = 2 * MT * BN;         // double-buffered accumulators
   static constexpr uint32_t TMEM_COLS =
       ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
@@ -74,6 +81,8 @@ struct GemmCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16,256]");
   static_assert(B_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages must keep 1024-B alignment");
   static_assert(STAGES >= 2, "pipeline needs two stages");
+  static_assert(ACC_COLS <= 512, "accumulators exceed tensor memory");
+  static_assert(MT == 1 || MT == 2, "one or two row tiles per unit");
 };
 
 __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& tm, int& tn, int& b,
@@ -122,8 +131,8 @@ __device__ __forceinline__ void convert_int8_row(const uint8_t* src_row, uint8_t
 // first A row is m0 (lane l holds row m0 + l) and first B row is n0 (v[j] is column n0 + j).  It
 // writes the block's output into the warp's staging buffer and returns the TMA stores (at most
 // two, warp-uniform) that move it to global memory through the two output tensor maps.
-template <int BN, class Epi, int WQ>
-__global__ void __launch_bounds__(GemmCfg<BN, WQ>::THREADS, 1)
+template <int BN, class Epi, int WQ, int MT>
+__global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                      const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB0,
@@ -131,7 +140,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmO0,
                      const __grid_constant__ CUtensorMap tmO1, const GemmGeometry geo,
                      const Epi epi, uint32_t* __restrict__ err_word) {
-  using Cfg = GemmCfg<BN, WQ>;
+  using Cfg = GemmCfg<BN, WQ, MT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -198,7 +207,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ>::THREADS, 1)
       };
       auto load_a = [&](int tm, int b, int kb, uint64_t* bar, void* dst) {
         const bool first = tm < geo.a_seg_tiles;
-        const int y = (first ? tm : tm - geo.a_seg_tiles) * Cfg::BM + b * geo.a_y_batch;
+        const int y = (first ? tm : tm - geo.a_seg_tiles) * Cfg::BM_U + b * geo.a_y_batch;
         tma_load_2d(dst, first ? &tmA0 : &tmA1, bar, kb * Cfg::BK + b * geo.a_x_batch, y);
       };
       auto load_b = [&](int tn, int b, int kb, uint64_t* bar, void* dst) {
@@ -293,7 +302,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ>::THREADS, 1)
         const uint32_t use = static_cast<uint32_t>(iter >> 1);
         if (!mbar_wait(&acce_bar[buf], (use & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * MT * Cfg::BN);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
             ok = false;
@@ -304,9 +313,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ>::THREADS, 1)
           const uint32_t b_addr = smem_u32(smemB + stage * Cfg::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < Cfg::BK / 16; ++kk) {
-            umma_bf16_ss(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
-                         sdesc_kmajor_sw128(b_addr + kk * 32), Cfg::IDESC,
-                         (kb > kb0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < MT; ++h)
+              umma_bf16_ss(d_tmem + h * Cfg::BN,
+                           sdesc_kmajor_sw128(a_addr + h * Cfg::BM * Cfg::BK * 2 + kk * 32),
+                           sdesc_kmajor_sw128(b_addr + kk * 32), Cfg::IDESC,
+                           (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);   // frees this smem stage once the MMAs have read it
           if (++stage == Cfg::STAGES) {
@@ -330,26 +342,27 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ>::THREADS, 1)
       const uint32_t use = static_cast<uint32_t>(iter >> 1);
       if (!mbar_wait(&accf_bar[buf], use & 1u, abort_flag)) break;
       tc_fence_after_sync();
-      const int m0 = tm * Cfg::BM + q * 32;
-      const uint32_t t_addr =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * Cfg::BN);
 #pragma unroll 1
-      for (int c = 0; c < Cfg::BN; c += Cfg::CH) {
+      for (int hc = 0; hc < MT * Cfg::BN; hc += Cfg::CH) {
+        const int h = hc / Cfg::BN, c = hc % Cfg::BN;
+        const int m0 = tm * Cfg::BM_U + h * Cfg::BM + q * 32;
+        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                static_cast<uint32_t>(buf * MT * Cfg::BN + hc);
         float v[Cfg::CH];
         if constexpr (Cfg::CH == 32) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(t_addr + c, r);
+          tmem_ld_32x32b_x32(t_addr, r);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
         } else {
           uint32_t r[16];
-          tmem_ld_32x32b_x16(t_addr + c, r);
+          tmem_ld_32x32b_x16(t_addr, r);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
         }
-        if (c + Cfg::CH >= Cfg::BN) {
+        if (hc + Cfg::CH >= MT * Cfg::BN) {
           // last TMEM read of this accumulator: hand it back to the MMA warp right away
           tc_fence_before_sync();
           __syncwarp();

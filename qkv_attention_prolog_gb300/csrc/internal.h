@@ -18,6 +18,7 @@ struct GemmLaunch {
   CUtensorMap o0, o1;           // output maps for the epilogue's TMA stores
   GemmGeometry geo;
   int bn;
+  int mt;            // 128-row tiles of A per unit (decode orientation: 1 or 2)
   bool swap;
   bool a_int8;       // A operand is an int8 weight converted to bf16 in shared memory
   int grid;
