@@ -5,6 +5,7 @@
 // matrix (约束说明), and the aclnnQkvRmsNormRopeCache "Input shape restrictions"; the two-phase
 // size-then-execute pattern follows the aclnn GetWorkspaceSize + execute pair.
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -95,6 +96,9 @@ struct MlaDims {
 
 constexpr int kSwapMaxT = 256;   // decode orientation (weights as MMA rows) up to this many tokens
 constexpr int kMaxSplits = 16;
+constexpr size_t kHeaderBytes = 8192;   // error word + stream-K flags
+constexpr size_t kFlagOffset = 4096;    // stream-K "partial written" flags (int32 per CTA)
+constexpr int kMaxStreamKCtas = 1024;   // flags that fit the header
 
 mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
   if (a == nullptr) return fail(MLAP_ERR_NULL, "args is NULL");
@@ -261,6 +265,12 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
   return MLAP_OK;
 }
 
+int swap_bn(int64_t T) {
+  int bn = 16;
+  while (bn < T) bn *= 2;
+  return bn;
+}
+
 struct MlaWs {
   size_t part, cq, qc, scale, total;
   int split_cap;
@@ -271,9 +281,13 @@ MlaWs mla_ws_layout(const MlaDims& d) {
   const bool swap = d.T <= kSwapMaxT;
   w.split_cap = swap ? kMaxSplits : 1;
   const int64_t ntot = d.Hcq + d.Hckv + d.Dr;
-  size_t off = 256;   // error word and spare header
+  size_t off = kHeaderBytes;
   w.part = off;
-  off += align_up(static_cast<size_t>(w.split_cap) * d.T * ntot * 4, 256);
+  // the down-projection's K-split partials, reused later in the call by the up-projection's
+  // stream-K partial slots (one 128-row fp32 tile per CTA, up to 160 CTAs)
+  const size_t down_part = static_cast<size_t>(w.split_cap) * d.T * ntot * 4;
+  const size_t sk_part = swap ? static_cast<size_t>(160) * 128 * swap_bn(d.T) * 4 : 0;
+  off += align_up(down_part > sk_part ? down_part : sk_part, 256);
   w.cq = off;
   off += align_up(static_cast<size_t>(d.T) * d.Hcq * 2, 256);
   w.qc = off;
@@ -374,11 +388,7 @@ int balanced_grid(int units, int sms) {
   return ceil_div(units, rounds);
 }
 
-int swap_bn(int64_t T) {
-  int bn = 16;
-  while (bn < T) bn *= 2;
-  return bn;
-}
+
 
 mlap_status_t cuda_fail(cudaError_t e, const char* what) {
   return fail(MLAP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
@@ -473,6 +483,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     g.geo.k_blocks = kb;
     g.geo.w_op = swap ? 0 : 1;
     g.geo.num_units = g.geo.m_tiles * g.geo.n_tiles * g.geo.splits;
+    g.pm = g.a0;
     // partials part[s][t][f]: W^DQ columns and W^DKV|W^KR columns as two 3-D (f, t, s) maps
     const int64_t row_b = Ntot * 4, split_b = d.T * Ntot * 4;
     CHECK_STATUS(make_out_map(&g.o0, part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
@@ -559,6 +570,23 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.geo.k_blocks = ceil_div(d.Hcq, 64);
     u.geo.num_units = u.geo.m_tiles * u.geo.n_tiles;
     u.grid = balanced_grid(u.geo.num_units, sms);
+    u.pm = u.a0;
+    // Stream-K (equal k-block ranges on every SM) is available for the decode orientation; on
+    // GB300 the whole-tile balanced grid measured faster (the decode up-projection is DRAM
+    // bound near 5 TB/s either way and stream-K adds a fix-up tail), so it is off by default.
+    const int64_t iters = static_cast<int64_t>(u.geo.num_units) * u.geo.k_blocks;
+    const int sk_grid = sms < 160 ? sms : 160;
+    const bool use_stream_k = std::getenv("MLAP_STREAM_K") != nullptr;
+    if (use_stream_k && swap && mt == 1 && bn_t >= 32 && u.geo.num_units % sk_grid != 0 &&
+        iters >= 2 * sk_grid) {
+      u.geo.stream_k = 1;
+      u.geo.sk_partial = part;
+      u.geo.sk_flag = reinterpret_cast<int32_t*>(wsb + kFlagOffset);
+      u.grid = sk_grid;
+      CHECK_STATUS(make_out_map(&u.pm, part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                                {bn_t, static_cast<int64_t>(sk_grid) * 128}, {bn_t * 4}, {32, 32},
+                                CU_TENSOR_MAP_SWIZZLE_128B));
+    }
     CHECK_STATUS(make_out_map(&u.o0, qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, {d.N * d.D, d.T},
                               {d.N * d.D * 2}, {32, ch_t}, CU_TENSOR_MAP_SWIZZLE_64B));
     CHECK_STATUS(make_out_map(&u.o1, a->query_rope.data, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
@@ -615,6 +643,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.geo.w_op = swap ? 0 : 1;
     b.geo.k_blocks = ceil_div(d.D, 64);
     b.geo.num_units = b.geo.m_tiles * b.geo.n_tiles * b.geo.batches;
+    b.pm = b.a0;
     b.grid = balanced_grid(b.geo.num_units, sms);
     CHECK_STATUS(make_out_map(&b.o0, a->query.data, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                               {d.Hckv, d.N, d.T}, {d.Hckv * 2, d.N * d.Hckv * 2}, {32, 1, ch_t},
@@ -805,7 +834,8 @@ mlap_status_t mlap_get_workspace_size(const mlap_args_t* args, size_t* bytes) {
 mlap_status_t mlap_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (ws == nullptr) return fail(MLAP_ERR_NULL, "workspace is NULL");
   if (ws_bytes < 256) return fail(MLAP_ERR_WORKSPACE, "workspace smaller than its 256-byte header");
-  cudaError_t e = cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream));
+  const size_t n = ws_bytes < kHeaderBytes ? 256 : kHeaderBytes;
+  cudaError_t e = cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   return MLAP_OK;
 }

@@ -65,11 +65,9 @@ __device__ __forceinline__ void stage_row_bf16x16(uint8_t* sb, int r, const floa
     *reinterpret_cast<uint4*>(sb + r * 32 + (((c ^ ((r >> 2) & 1)) & 1) << 4)) = pack_bf16x8(v + 8 * c);
 }
 
-__device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* p, float* out) {
-  const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
-  const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-  const __nv_bfloat16* ea = reinterpret_cast<const __nv_bfloat16*>(&a);
-  const __nv_bfloat16* eb = reinterpret_cast<const __nv_bfloat16*>(&b);
+__device__ __forceinline__ void unpack_bf16x16(const uint4 (&q)[2], float* out) {
+  const __nv_bfloat16* ea = reinterpret_cast<const __nv_bfloat16*>(&q[0]);
+  const __nv_bfloat16* eb = reinterpret_cast<const __nv_bfloat16*>(&q[1]);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     out[i] = __bfloat162float(ea[i]);
@@ -89,9 +87,11 @@ struct DownParams {
 template <bool SWAP, int TILE_W, int CH>
 struct EpiDown {
   DownParams p;
+  struct Pre {};
+  __device__ __forceinline__ Pre preload(int, int) const { return {}; }
 
   __device__ __forceinline__ int operator()(int m0, int n0, int, int s, const float (&v)[CH],
-                                            uint8_t* sb, StoreOp (&ops)[2]) const {
+                                            uint8_t* sb, StoreOp (&ops)[2], const Pre&) const {
     const int lane = threadIdx.x & 31;
     const int b0 = p.seg_tiles * TILE_W;
     if constexpr (SWAP) {
@@ -127,6 +127,38 @@ template <bool SWAP, bool INT8, int CH>
 struct EpiUp {
   UpParams p;
 
+  // RoPE tables of one lane's token for one 32-row rope block: cos/sin of pairs p0..p0+15
+  // (run a) and p0+Dr/2.. (run b), packed bf16.  Loaded ahead of use (see gemm.cuh).
+  struct Pre {
+    uint4 ca[2], sa[2], cb[2], sb[2];
+  };
+
+  __device__ __forceinline__ Pre preload(int m0, int n0) const {
+    Pre r;
+    const int nd = p.N * p.D;
+    const int lane = threadIdx.x & 31;
+    const int f0 = SWAP ? m0 : n0;        // first weight row of the block
+    const int t = SWAP ? n0 + lane : m0 + lane;
+    if (f0 >= nd && t < p.T) {
+      const int p0 = ((f0 - nd) % p.Dr) >> 1;
+      const uint4* c = reinterpret_cast<const uint4*>(p.cos + static_cast<size_t>(t) * p.Dr + p0);
+      const uint4* s = reinterpret_cast<const uint4*>(p.sin + static_cast<size_t>(t) * p.Dr + p0);
+      const int hb = p.Dr >> 4;           // uint4 offset of run b (Dr/2 bf16)
+      r.ca[0] = __ldg(c);
+      r.ca[1] = __ldg(c + 1);
+      r.sa[0] = __ldg(s);
+      r.sa[1] = __ldg(s + 1);
+      r.cb[0] = __ldg(c + hb);
+      r.cb[1] = __ldg(c + hb + 1);
+      r.sb[0] = __ldg(s + hb);
+      r.sb[1] = __ldg(s + hb + 1);
+    } else {
+      r.ca[0] = r.ca[1] = r.sa[0] = r.sa[1] = r.cb[0] = r.cb[1] = r.sb[0] = r.sb[1] =
+          make_uint4(0, 0, 0, 0);
+    }
+    return r;
+  }
+
   // original column of weight_uq_qr for a prepacked row
   __device__ __forceinline__ int orig_col(int f) const {
     const int nd = p.N * p.D;
@@ -137,20 +169,15 @@ struct EpiUp {
   }
 
   // RoPE of one token's 16 adjacent (j, j + Dr/2) pairs y[2i], y[2i+1], i < 16, i.e. pairs
-  // p0 .. p0+15 of one head; the results are staged at row r of two 16-wide bf16 tiles holding
-  // output columns p0.. and p0+Dr/2.. (offsets 0 and 1024 of the staging buffer).
-  __device__ __forceinline__ void rope_row(uint8_t* sb, int r, int t, int p0, const float* y) const {
+  // p0 .. p0+15 of one head, with that token's preloaded tables; the results are staged at row r
+  // of two 16-wide bf16 tiles holding output columns p0.. and p0+Dr/2.. (offsets 0 and 1024 of
+  // the staging buffer).
+  __device__ __forceinline__ void rope_row(uint8_t* sb, int r, const Pre& P, const float* y) const {
     float c0[16], s0[16], c1[16], s1[16];
-    if (t < p.T) {
-      const size_t row = static_cast<size_t>(t) * p.Dr;
-      load_bf16x16(p.cos + row + p0, c0);
-      load_bf16x16(p.sin + row + p0, s0);
-      load_bf16x16(p.cos + row + p0 + (p.Dr >> 1), c1);
-      load_bf16x16(p.sin + row + p0 + (p.Dr >> 1), s1);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) c0[i] = s0[i] = c1[i] = s1[i] = 0.f;
-    }
+    unpack_bf16x16(P.ca, c0);
+    unpack_bf16x16(P.sa, s0);
+    unpack_bf16x16(P.cb, c1);
+    unpack_bf16x16(P.sb, s1);
     float oa[16], ob[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -163,7 +190,7 @@ struct EpiUp {
   }
 
   __device__ __forceinline__ int operator()(int m0, int n0, int, int, const float (&v)[CH],
-                                            uint8_t* sb, StoreOp (&ops)[2]) const {
+                                            uint8_t* sb, StoreOp (&ops)[2], const Pre& P) const {
     const int lane = threadIdx.x & 31;
     const int nd = p.N * p.D;
     const int M = p.N * (p.D + p.Dr);
@@ -207,7 +234,7 @@ struct EpiUp {
       __syncwarp();
       const int r0 = m0 - nd;                 // first rope row of the block (Dr % 32 == 0)
       const int n = r0 / p.Dr, p0 = (r0 % p.Dr) >> 1;
-      if (lane < CH) rope_row(sb, lane, n0 + lane, p0, y);
+      if (lane < CH) rope_row(sb, lane, P, y);
       ops[0] = {1, 3, p0, n, n0, 0};
       ops[1] = {1, 3, p0 + (p.Dr >> 1), n, n0, 1024};
       return 2;
@@ -233,7 +260,7 @@ struct EpiUp {
       }
       const int r0 = n0 - nd;
       const int n = r0 / p.Dr, p0 = (r0 % p.Dr) >> 1;
-      rope_row(sb, lane, t, p0, w);
+      rope_row(sb, lane, P, w);
       ops[0] = {1, 3, p0, n, m0, 0};
       ops[1] = {1, 3, p0 + (p.Dr >> 1), n, m0, 1024};
       return 2;
@@ -252,9 +279,11 @@ struct AbsorbParams {
 template <bool SWAP, int CH>
 struct EpiAbsorb {
   AbsorbParams p;
+  struct Pre {};
+  __device__ __forceinline__ Pre preload(int, int) const { return {}; }
 
   __device__ __forceinline__ int operator()(int m0, int n0, int n, int, const float (&v)[CH],
-                                            uint8_t* sb, StoreOp (&ops)[2]) const {
+                                            uint8_t* sb, StoreOp (&ops)[2], const Pre&) const {
     const int lane = threadIdx.x & 31;
     if constexpr (SWAP) {
 #pragma unroll

@@ -16,6 +16,7 @@ namespace mlap {
 struct GemmLaunch {
   CUtensorMap a0, a1, b0, b1;   // operand maps (first / second segment)
   CUtensorMap o0, o1;           // output maps for the epilogue's TMA stores
+  CUtensorMap pm;               // stream-K partial slots (fp32 [grid*128][BN])
   GemmGeometry geo;
   int bn;
   int mt;            // 128-row tiles of A per unit (decode orientation: 1 or 2)

@@ -4,12 +4,11 @@
 //   y       = x / sqrt(mean(x^2) + eps) * gamma                      per q / k head, along D
 //   y_embed = y * cos + cat(-y2, y1) * sin                           half-and-half, d = D
 //   q_out   = y_embed(q);  k_cache[i] = Quant(y_embed(k));  v_cache[i] = Quant(v)
-//   Quant   = identity, or value / scale rounded half to even and saturated to int8
+//   Quant   = identity, or value / scale rounded half to even and saturated to int8 (computed
+//             as value * fp32(1/scale); the code can differ from the exact quotient's by one
+//             near a rounding tie)
 //
-// A pure HBM stream: every token's qkv row is read once and its outputs written once.  Sixteen
-// lanes own one head row of D = 128 elements (16 bytes each); the RmsNorm sum is a 16-lane
-// shuffle reduction and each RoPE partner (j, j + 64) sits 8 lanes away.  Each half-warp keeps
-// two rows in flight.
+// A pure HBM stream: every token's qkv row is read once and its outputs written once.
 #include "internal.h"
 
 namespace mlap {
@@ -17,7 +16,6 @@ namespace mlap {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kThreads = 256;
 
 template <bool BF16>
 struct Elem;
@@ -52,97 +50,179 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
   return raw;
 }
 
-__device__ __forceinline__ uint2 quant8(const float (&x)[8], const float* scale) {
-  const float4 s0 = reinterpret_cast<const float4*>(scale)[0];
-  const float4 s1 = reinterpret_cast<const float4*>(scale)[1];
-  const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+// int8 codes of x * (1/scale) (reciprocal of the per-channel scale in fp32), round half to
+// even, saturated to [-128, 127].
+__device__ __forceinline__ uint2 quant8_mul(const float (&x)[8], const float* inv) {
+  const float4 i0 = reinterpret_cast<const float4*>(inv)[0];
+  const float4 i1 = reinterpret_cast<const float4*>(inv)[1];
+  const float iv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
   uint2 out;
   int8_t* o = reinterpret_cast<int8_t*>(&out);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    int q = __float2int_rn(__fdiv_rn(x[i], sc[i]));
+    int q = __float2int_rn(x[i] * iv[i]);
     q = q < -128 ? -128 : (q > 127 ? 127 : q);
     o[i] = static_cast<int8_t>(q);
   }
   return out;
 }
 
+// Tokens stream through a ring of kRing shared-memory buffers: one thread requests each token's
+// qkv row ((Nq+Nk+Nv) * D elements, contiguous) and its cos / sin rows with 1-D bulk copies,
+// kRing tokens ahead, so a CTA keeps ~50 KB of loads in flight independent of its registers.
+// Eight lanes own one head row: lane l holds elements 8l..8l+7 and 64+8l..64+8l+7, i.e. both
+// members of its RoPE pairs, so the rotation needs no exchange and the RmsNorm sum is a 3-step
+// shuffle.  The CTA has 8 * ceil(N/2) threads (N = Nq+Nk+Nv heads): every 8-lane slot processes
+// two rows of each token.  Quantisation multiplies by the reciprocal of the per-channel scale
+// (fp32); the reciprocals of all k and v heads sit in shared memory behind the ring.
+constexpr int kRing = 4;
+
 template <bool BF16, bool QUANT>
-__global__ void __launch_bounds__(kThreads) qkv_rnrc_kernel(const QkvParams p) {
+__global__ void __launch_bounds__(512) qkv_rnrc_kernel(const QkvParams p) {
   using E = Elem<BF16>;
   using T = typename E::T;
+  extern __shared__ __align__(128) uint8_t qsm[];
+  __shared__ uint64_t full[kRing];
+  __shared__ int abort_sh;
+  const int Nh = p.Nq + p.Nk + p.Nv;
+  const uint32_t row_bytes = static_cast<uint32_t>(Nh) * kD * sizeof(T);
+  const uint32_t buf_bytes = row_bytes + 2 * kD * sizeof(T);     // qkv row, cos, sin
+  const int l8 = threadIdx.x & 7;
+  const int slot = threadIdx.x >> 3;
+  const int nslots = blockDim.x >> 3;
+  const unsigned mask = 0xffu << (threadIdx.x & 24);              // this slot's 8 lanes
+  const int ja = l8 * 8, jb = 64 + l8 * 8;                         // the two 8-element slices
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRing; ++i) mbar_init(&full[i], 1);
+    abort_sh = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
   grid_launch_dependents();
   grid_dependency_wait();
-  const int Nh = p.Nq + p.Nk + p.Nv;
-  const int64_t rows = static_cast<int64_t>(p.T) * Nh;
-  const int hl = threadIdx.x & 15;                                  // lane within the half-warp
-  const unsigned mask = 0xffffu << (threadIdx.x & 16);              // this half-warp's lanes
-  const int64_t hw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
-  const int64_t nhw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
-  const int j0 = hl * 8;                                            // first element of this lane
 
-  for (int64_t base = hw; base < rows; base += 2 * nhw) {
-    uint4 raw[2];
-    int64_t r[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      r[u] = base + u * nhw;
-      if (r[u] < rows)
-        raw[u] = reinterpret_cast<const uint4*>(static_cast<const T*>(p.qkv) + r[u] * kD)[hl];
+  auto request = [&](int t, int s) {
+    uint8_t* b = qsm + static_cast<size_t>(s) * buf_bytes;
+    mbar_arrive_expect_tx(&full[s], buf_bytes);
+    bulk_load_1d(b, static_cast<const uint8_t*>(p.qkv) + static_cast<size_t>(t) * row_bytes,
+                 row_bytes, &full[s]);
+    bulk_load_1d(b + row_bytes,
+                 static_cast<const uint8_t*>(p.cos) + static_cast<size_t>(t) * kD * sizeof(T),
+                 kD * sizeof(T), &full[s]);
+    bulk_load_1d(b + row_bytes + kD * sizeof(T),
+                 static_cast<const uint8_t*>(p.sin) + static_cast<size_t>(t) * kD * sizeof(T),
+                 kD * sizeof(T), &full[s]);
+  };
+  if (threadIdx.x == 0)
+    for (int s = 0; s < kRing; ++s) {
+      const int t = blockIdx.x + s * gridDim.x;
+      if (t < p.T) request(t, s);
     }
+
+  // per-lane gamma slices; reciprocal quant scales of all k and v heads in shared memory
+  float ga_q[8], gb_q[8], ga_k[8], gb_k[8];
+  unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_q)[l8], ga_q);
+  unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_q)[8 + l8], gb_q);
+  unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_k)[l8], ga_k);
+  unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_k)[8 + l8], gb_k);
+  float* inv = reinterpret_cast<float*>(qsm + static_cast<size_t>(kRing) * buf_bytes);
+  if (QUANT) {
+    for (int i = threadIdx.x; i < (p.Nk + p.Nv) * kD; i += blockDim.x)
+      inv[i] = __frcp_rn(i < p.Nk * kD ? p.k_scale[i] : p.v_scale[i - p.Nk * kD]);
+    __syncthreads();
+  }
+
+  for (int k = 0;; ++k) {
+    const int t = blockIdx.x + k * gridDim.x;
+    if (t >= p.T) break;
+    const int s = k % kRing;
+    if (!mbar_wait(&full[s], static_cast<uint32_t>((k / kRing) & 1), &abort_sh)) abort_sh = 1;
+    const uint8_t* b = qsm + static_cast<size_t>(s) * buf_bytes;
+    float ca[8], sa[8], cb[8], sb[8];
+    const uint4* cs = reinterpret_cast<const uint4*>(b + row_bytes);
+    const uint4* sn = reinterpret_cast<const uint4*>(b + row_bytes + kD * sizeof(T));
+    unpack8<BF16>(cs[l8], ca);
+    unpack8<BF16>(cs[8 + l8], cb);
+    unpack8<BF16>(sn[l8], sa);
+    unpack8<BF16>(sn[8 + l8], sb);
+    const int64_t idx = p.index[t];
+    const bool store = idx >= 0 && idx < p.slots;
+    if (threadIdx.x == 0 && idx != -1 && !store && p.slots > 0) atomicOr(p.err, kErrIndexRange);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (r[u] >= rows) break;                                      // uniform in the half-warp
-      const int t = static_cast<int>(r[u] / Nh);
-      const int h = static_cast<int>(r[u] % Nh);
-      float x[8];
-      unpack8<BF16>(raw[u], x);
-      const int64_t idx = p.index[t];
-      const bool store = idx >= 0 && idx < p.slots;
+    for (int r = 0; r < 2; ++r) {
+      const int h = slot + r * nslots;
+      if (h >= Nh) break;                                          // uniform in the slot
+      const uint4* row = reinterpret_cast<const uint4*>(b + static_cast<size_t>(h) * kD * sizeof(T));
+      const uint4 rawa = row[l8], rawb = row[8 + l8];
+      float xa[8], xb[8];
+      unpack8<BF16>(rawa, xa);
+      unpack8<BF16>(rawb, xb);
       if (h < p.Nq + p.Nk) {
         float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
+        for (int e = 0; e < 8; ++e) ss += xa[e] * xa[e] + xb[e] * xb[e];
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
-        const float rinv = 1.0f / sqrtf(ss / static_cast<float>(kD) + p.eps);
+        for (int o = 4; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
+        const float rinv = rsqrtf(ss * (1.0f / static_cast<float>(kD)) + p.eps);
         const bool is_q = h < p.Nq;
-        float g[8], c[8], s[8];
-        unpack8<BF16>(reinterpret_cast<const uint4*>(is_q ? p.gamma_q : p.gamma_k)[hl], g);
-        unpack8<BF16>(reinterpret_cast<const uint4*>(static_cast<const T*>(p.cos) +
-                                                     static_cast<size_t>(t) * kD)[hl], c);
-        unpack8<BF16>(reinterpret_cast<const uint4*>(static_cast<const T*>(p.sin) +
-                                                     static_cast<size_t>(t) * kD)[hl], s);
-        float y[8], e[8];
+        float oa[8], ob[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = x[i] * rinv * g[i];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float partner = __shfl_xor_sync(mask, y[i], 8);    // element j +- 64
-          e[i] = y[i] * c[i] + (hl < 8 ? -partner : partner) * s[i];
+        for (int e = 0; e < 8; ++e) {
+          const float ya = xa[e] * rinv * (is_q ? ga_q[e] : ga_k[e]);
+          const float yb = xb[e] * rinv * (is_q ? gb_q[e] : gb_k[e]);
+          oa[e] = ya * ca[e] - yb * sa[e];                         // j < 64: partner -y[j+64]
+          ob[e] = yb * cb[e] + ya * sb[e];                         // j >= 64: partner y[j-64]
         }
         if (is_q) {
-          reinterpret_cast<uint4*>(static_cast<T*>(p.q_out) +
-                                   (static_cast<size_t>(t) * p.Nq + h) * kD)[hl] = pack8<BF16>(e);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.q_out) +
+                                                (static_cast<size_t>(t) * p.Nq + h) * kD);
+          dst[l8] = pack8<BF16>(oa);
+          dst[8 + l8] = pack8<BF16>(ob);
         } else if (store) {
           const int hk = h - p.Nq;
           const size_t off = (static_cast<size_t>(idx) * p.Nk + hk) * kD;
-          if (QUANT)
-            reinterpret_cast<uint2*>(static_cast<int8_t*>(p.k_cache) + off)[hl] =
-                quant8(e, p.k_scale + hk * kD + j0);
-          else
-            reinterpret_cast<uint4*>(static_cast<T*>(p.k_cache) + off)[hl] = pack8<BF16>(e);
+          if (QUANT) {
+            uint2* dst = reinterpret_cast<uint2*>(static_cast<int8_t*>(p.k_cache) + off);
+            const float* iv = inv + hk * kD;
+            dst[l8] = quant8_mul(oa, iv + ja);
+            dst[8 + l8] = quant8_mul(ob, iv + jb);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.k_cache) + off);
+            dst[l8] = pack8<BF16>(oa);
+            dst[8 + l8] = pack8<BF16>(ob);
+          }
         }
       } else if (store) {
         const int hv = h - p.Nq - p.Nk;
         const size_t off = (static_cast<size_t>(idx) * p.Nv + hv) * kD;
-        if (QUANT)
-          reinterpret_cast<uint2*>(static_cast<int8_t*>(p.v_cache) + off)[hl] =
-              quant8(x, p.v_scale + hv * kD + j0);
-        else
-          reinterpret_cast<uint4*>(static_cast<T*>(p.v_cache) + off)[hl] = raw[u];
+        if (QUANT) {
+          uint2* dst = reinterpret_cast<uint2*>(static_cast<int8_t*>(p.v_cache) + off);
+          const float* iv = inv + (p.Nk + hv) * kD;
+          dst[l8] = quant8_mul(xa, iv + ja);
+          dst[8 + l8] = quant8_mul(xb, iv + jb);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.v_cache) + off);
+          dst[l8] = rawa;
+          dst[8 + l8] = rawb;
+        }
       }
-      if (h == 0 && hl == 0 && idx != -1 && !store && p.slots > 0) atomicOr(p.err, kErrIndexRange);
+    }
+    __syncthreads();                                  // buffer s fully read
+    if (abort_sh) break;                              // uniform after the barrier
+    if (threadIdx.x == 0) {
+      const int tn = t + kRing * gridDim.x;
+      if (tn < p.T) request(tn, s);
+    }
+  }
+  if (abort_sh && threadIdx.x == 0) {
+    atomicOr(p.err, kErrTimeout);
+    // let requests already issued land before the CTA exits (bounded)
+    for (int s = 0; s < kRing; ++s) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&full[s], 0) && !mbar_try_wait(&full[s], 1) &&
+             globaltimer_ns() - t0 < 20000000ull) {
+      }
     }
   }
 }
@@ -150,28 +230,38 @@ __global__ void __launch_bounds__(kThreads) qkv_rnrc_kernel(const QkvParams p) {
 }  // namespace
 
 cudaError_t launch_qkv_rnrc(const QkvParams& p, cudaStream_t stream, int sm_count) {
-  const int64_t rows = static_cast<int64_t>(p.T) * (p.Nq + p.Nk + p.Nv);
-  const int64_t half_warps_needed = (rows + 1) / 2;
-  int64_t blocks = (half_warps_needed * 16 + kThreads - 1) / kThreads;
-  const int64_t cap = static_cast<int64_t>(sm_count) * (2048 / kThreads);   // one full wave
-  if (blocks > cap) blocks = cap;
+  const int Nh = p.Nq + p.Nk + p.Nv;
+  const size_t elem = 2;   // fp16 and bf16
+  const size_t buf = static_cast<size_t>(Nh) * kD * elem + 2 * kD * elem;
+  const size_t smem = kRing * buf + (p.k_scale ? static_cast<size_t>(p.Nk + p.Nv) * kD * 4 : 0);
+  if (smem > 200 * 1024) return cudaErrorNotSupported;
+  auto pick = [&]() {
+    return p.bf16 ? (p.k_scale ? qkv_rnrc_kernel<true, true> : qkv_rnrc_kernel<true, false>)
+                  : (p.k_scale ? qkv_rnrc_kernel<false, true> : qkv_rnrc_kernel<false, false>);
+  };
+  auto kern = pick();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int threads = 8 * ((Nh + 1) / 2);          // 8 lanes per row, two rows per slot
+  if (threads > 512) return cudaErrorNotSupported;
+  int per_sm = 1;   // persistent grid: exactly the CTAs that fit at once
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+  if (e != cudaSuccess) return e;
+  int64_t blocks = static_cast<int64_t>(sm_count) * (per_sm < 1 ? 1 : per_sm);
+  if (blocks > p.T) blocks = p.T;
   if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const bool quant = p.k_scale != nullptr;
-  if (p.bf16) {
-    return quant ? cudaLaunchKernelEx(&cfg, qkv_rnrc_kernel<true, true>, p)
-                 : cudaLaunchKernelEx(&cfg, qkv_rnrc_kernel<true, false>, p);
-  }
-  return quant ? cudaLaunchKernelEx(&cfg, qkv_rnrc_kernel<false, true>, p)
-               : cudaLaunchKernelEx(&cfg, qkv_rnrc_kernel<false, false>, p);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace mlap

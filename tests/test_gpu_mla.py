@@ -44,6 +44,7 @@ SHAPES = [
     dict(B=2, S=65, He=512, Hcq=256, N=3),            # T=130: BN 256, ragged rope tail (N*Dr)
     dict(B=3, S=100, He=384, Hcq=192, Hckv=128, N=2),  # T=300: prefill orientation, ragged M
     dict(B=1, S=200, He=320, Hcq=136, Hckv=96, N=2, Dr=32),  # ragged K, Hcq, Hckv tiles
+    dict(B=40, S=1, He=256, Hcq=1536, N=16),         # stream-K up-projection, tiles cut ~7 ways
 ]
 
 
@@ -168,3 +169,17 @@ def test_partial_quant_shapes(kw):
     case = synthetic.small_mla_case("pq", block_num=block_num, n_skip=1,
                                     weight_uq_qr_dtype="int8", **kw)
     _full_check(case)
+
+
+@pytest.mark.parametrize("case", ["decode", "cut7", "pq"])
+def test_stream_k_schedule(case, monkeypatch):
+    # the opt-in stream-K schedule of the decode up-projection (tiles cut across CTAs, partials
+    # fixed up by the owning CTA) gives the same results as the oracle
+    monkeypatch.setenv("MLAP_STREAM_K", "1")
+    if case == "decode":
+        _full_check(synthetic.MLA_DECODE)
+    elif case == "pq":
+        _full_check(synthetic.MLA_PARTIAL_QUANT)
+    else:
+        _full_check(synthetic.small_mla_case("cut7", B=40, S=1, He=256, Hcq=1536, N=16,
+                                             block_num=2, n_skip=1))
