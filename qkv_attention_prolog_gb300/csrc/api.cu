@@ -4,6 +4,7 @@
 // Validation follows the MlaPrologV2 README parameter table (参数说明) and shape/dtype/scenario
 // matrix (约束说明), and the aclnnQkvRmsNormRopeCache "Input shape restrictions"; the two-phase
 // size-then-execute pattern follows the aclnn GetWorkspaceSize + execute pair.
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -95,6 +96,7 @@ struct MlaDims {
 };
 
 constexpr int kSwapMaxT = 256;   // decode orientation (weights as MMA rows) up to this many tokens
+constexpr int kSplitMaxT = 256;  // down-projection K splits (few output tiles) up to this many tokens
 constexpr int kMaxSplits = 16;
 constexpr size_t kHeaderBytes = 8192;   // error word + stream-K flags
 constexpr size_t kFlagOffset = 4096;    // stream-K "partial written" flags (int32 per CTA)
@@ -279,7 +281,7 @@ struct MlaWs {
 MlaWs mla_ws_layout(const MlaDims& d) {
   MlaWs w;
   const bool swap = d.T <= kSwapMaxT;
-  w.split_cap = swap ? kMaxSplits : 1;
+  w.split_cap = d.T <= kSplitMaxT ? kMaxSplits : 1;
   const int64_t ntot = d.Hcq + d.Hckv + d.Dr;
   size_t off = kHeaderBytes;
   w.part = off;
@@ -379,6 +381,14 @@ mlap_status_t make_tmap_i8(CUtensorMap* m, const void* base, int64_t inner, int6
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
+// The decode-orientation activation operand, read by the GEMM's cp.async loader warps.
+void set_act(GemmGeometry* g, const void* p, int64_t ld, int64_t rows, int64_t cols) {
+  g->act = static_cast<const uint16_t*>(p);
+  g->act_ld = ld;
+  g->act_rows = static_cast<int32_t>(rows);
+  g->act_cols = static_cast<int32_t>(cols);
+}
+
 // Persistent grid with equal work per CTA: the fewest CTAs that still finish the units in the
 // minimum number of rounds (e.g. 192 units on 152 SMs -> 96 CTAs x 2 units instead of a second
 // round that only 40 CTAs run).
@@ -459,6 +469,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       g.geo.n_tiles = 1;
       g.geo.a_seg_tiles = seg;
       g.geo.b_seg_tiles = 1;
+      set_act(&g.geo, a->token_x.data, d.He, d.T, d.He);
       int splits = sms / g.geo.m_tiles;
       if (splits > L.split_cap) splits = L.split_cap;
       if (splits > kb) splits = kb;
@@ -476,7 +487,11 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       g.geo.n_tiles = seg + ceil_div(d.Hckv + d.Dr, 192);
       g.geo.a_seg_tiles = g.geo.m_tiles;
       g.geo.b_seg_tiles = seg;
-      g.geo.splits = 1;
+      int splits = sms / (g.geo.m_tiles * g.geo.n_tiles);
+      if (splits > L.split_cap) splits = L.split_cap;
+      if (splits > kb) splits = kb;
+      if (splits < 1) splits = 1;
+      g.geo.splits = splits;
       dp.seg_tiles = seg;
     }
     g.geo.batches = 1;
@@ -537,9 +552,22 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.stream = stream;
     u.pdl = true;
     u.err = err;
-    u.swap = swap;
-    u.mt = swap ? mt : 1;
-    if (swap) {
+    // Decode with a bf16 weight and one 128-token tile: tokens as MMA rows and an equal range
+    // of weight rows per SM (row-range schedule: 24576 rows on 152 SMs, 160 or 192 each).
+    const bool up_var = swap && !d.w_int8 && d.T <= 128 && Mup % 32 == 0;
+    u.swap = swap && !up_var;
+    u.mt = u.swap ? mt : 1;
+    if (up_var) {
+      CHECK_STATUS(make_tmap(&u.a0, cq, d.Hcq, d.T, d.Hcq, 128));
+      u.a1 = u.a0;
+      CHECK_STATUS(make_tmap(&u.b0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 32));
+      u.b1 = u.b0;
+      u.bn = 256;
+      u.geo.m_tiles = 1;
+      u.geo.n_tiles = 1;
+      u.geo.rr_on = 1;
+      u.geo.rr_rows = static_cast<int32_t>(Mup);
+    } else if (swap) {
       if (d.w_int8)
         CHECK_STATUS(make_tmap_i8(&u.a0, a->weight_uq_qr.data, d.Hcq, Mup, wrows));
       else
@@ -547,6 +575,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       u.a1 = u.a0;
       CHECK_STATUS(make_tmap(&u.b0, cq, d.Hcq, d.T, d.Hcq, bn_t));
       u.b1 = u.b0;
+      set_act(&u.geo, cq, d.Hcq, d.T, d.Hcq);
       u.bn = bn_t;
       u.geo.m_tiles = ceil_div(Mup, wrows);
       u.geo.n_tiles = 1;
@@ -566,10 +595,11 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.geo.b_seg_tiles = u.geo.n_tiles;
     u.geo.batches = 1;
     u.geo.splits = 1;
-    u.geo.w_op = swap ? 0 : 1;
+    u.geo.w_op = u.swap ? 0 : 1;
     u.geo.k_blocks = ceil_div(d.Hcq, 64);
     u.geo.num_units = u.geo.m_tiles * u.geo.n_tiles;
-    u.grid = balanced_grid(u.geo.num_units, sms);
+    u.grid = up_var ? static_cast<int>(std::min<int64_t>(sms, Mup / 32))
+                    : balanced_grid(u.geo.num_units, sms);
     u.pm = u.a0;
     // Stream-K (equal k-block ranges on every SM) is available for the decode orientation; on
     // GB300 the whole-tile balanced grid measured faster (the decode up-projection is DRAM
@@ -577,7 +607,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     const int64_t iters = static_cast<int64_t>(u.geo.num_units) * u.geo.k_blocks;
     const int sk_grid = sms < 160 ? sms : 160;
     const bool use_stream_k = std::getenv("MLAP_STREAM_K") != nullptr;
-    if (use_stream_k && swap && mt == 1 && bn_t >= 32 && u.geo.num_units % sk_grid != 0 &&
+    if (use_stream_k && u.swap && mt == 1 && bn_t >= 32 && u.geo.num_units % sk_grid != 0 &&
         iters >= 2 * sk_grid) {
       u.geo.stream_k = 1;
       u.geo.sk_partial = part;
@@ -587,17 +617,20 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                                 {bn_t, static_cast<int64_t>(sk_grid) * 128}, {bn_t * 4}, {32, 32},
                                 CU_TENSOR_MAP_SWIZZLE_128B));
     }
+    const int ch_u = u.swap ? ch_t : 32;   // tokens per store box: one per lane unless swapped
     CHECK_STATUS(make_out_map(&u.o0, qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, {d.N * d.D, d.T},
-                              {d.N * d.D * 2}, {32, ch_t}, CU_TENSOR_MAP_SWIZZLE_64B));
+                              {d.N * d.D * 2}, {32, ch_u}, CU_TENSOR_MAP_SWIZZLE_64B));
     CHECK_STATUS(make_out_map(&u.o1, a->query_rope.data, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                              {d.Dr, d.N, d.T}, {d.Dr * 2, d.N * d.Dr * 2}, {16, 1, ch_t},
+                              {d.Dr, d.N, d.T}, {d.Dr * 2, d.N * d.Dr * 2}, {16, 1, ch_u},
                               CU_TENSOR_MAP_SWIZZLE_32B));
     UpParams up{static_cast<const __nv_bfloat16*>(a->rope_cos.data),
                 static_cast<const __nv_bfloat16*>(a->rope_sin.data),
                 scale_t,
                 static_cast<const float*>(a->dequant_scale_w_uq_qr.data),
                 static_cast<int32_t>(d.T), static_cast<int32_t>(d.N), static_cast<int32_t>(d.D),
-                static_cast<int32_t>(d.Dr)};
+                static_cast<int32_t>(d.Dr),
+                up_var ? qc : nullptr,
+                up_var ? static_cast<__nv_bfloat16*>(a->query_rope.data) : nullptr};
     CHECK_STATUS(rec(2));
     ce = launch_up(u, up, d.w_int8);
     if (ce != cudaSuccess) return cuda_fail(ce, "up-projection launch");
@@ -609,13 +642,31 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.stream = stream;
     b.pdl = true;
     b.err = err;
-    b.swap = swap;
-    b.mt = swap ? mt : 1;
-    if (swap) {
+    // Decode with one 128-token tile: tokens as MMA rows and the row-range schedule over all
+    // heads' W^UK rows (128 x 512 rows on 152 SMs: 416 or 448 each, cut at head boundaries).
+    const bool ab_var = swap && d.T <= 128 && d.Hckv % 32 == 0;
+    b.swap = swap && !ab_var;
+    b.mt = b.swap ? mt : 1;
+    if (ab_var) {
+      CHECK_STATUS(make_tmap(&b.a0, qc, d.N * d.D, d.T, d.N * d.D, 128));
+      b.a1 = b.a0;
+      CHECK_STATUS(make_tmap(&b.b0, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, 32));
+      b.b1 = b.b0;
+      b.bn = 256;
+      b.geo.m_tiles = 1;
+      b.geo.n_tiles = 1;
+      b.geo.a_x_batch = static_cast<int32_t>(d.D);
+      b.geo.a_y_batch = 0;
+      b.geo.b_x_batch = 0;
+      b.geo.b_y_batch = static_cast<int32_t>(d.Hckv);
+      b.geo.rr_on = 1;
+      b.geo.rr_rows = static_cast<int32_t>(d.Hckv);
+    } else if (swap) {
       CHECK_STATUS(make_tmap(&b.a0, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, wrows));
       b.a1 = b.a0;
       CHECK_STATUS(make_tmap(&b.b0, qc, d.N * d.D, d.T, d.N * d.D, bn_t));
       b.b1 = b.b0;
+      set_act(&b.geo, qc, d.N * d.D, d.T, d.N * d.D);
       b.bn = bn_t;
       b.geo.m_tiles = ceil_div(d.Hckv, wrows);
       b.geo.n_tiles = 1;
@@ -640,16 +691,19 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.geo.b_seg_tiles = b.geo.n_tiles;
     b.geo.batches = static_cast<int32_t>(d.N);
     b.geo.splits = 1;
-    b.geo.w_op = swap ? 0 : 1;
+    b.geo.w_op = b.swap ? 0 : 1;
     b.geo.k_blocks = ceil_div(d.D, 64);
     b.geo.num_units = b.geo.m_tiles * b.geo.n_tiles * b.geo.batches;
     b.pm = b.a0;
-    b.grid = balanced_grid(b.geo.num_units, sms);
+    b.grid = ab_var ? static_cast<int>(std::min<int64_t>(sms, d.N * d.Hckv / 32))
+                    : balanced_grid(b.geo.num_units, sms);
     CHECK_STATUS(make_out_map(&b.o0, a->query.data, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                              {d.Hckv, d.N, d.T}, {d.Hckv * 2, d.N * d.Hckv * 2}, {32, 1, ch_t},
+                              {d.Hckv, d.N, d.T}, {d.Hckv * 2, d.N * d.Hckv * 2}, {32, 1, b.swap ? ch_t : 32},
                               CU_TENSOR_MAP_SWIZZLE_64B));
     b.o1 = b.o0;
-    AbsorbParams ap{0};
+    AbsorbParams ap{ab_var ? static_cast<__nv_bfloat16*>(a->query.data) : nullptr,
+                    static_cast<int32_t>(d.T), static_cast<int32_t>(d.N),
+                    static_cast<int32_t>(d.Hckv)};
     CHECK_STATUS(rec(3));
     ce = launch_absorb(b, ap);
     if (ce != cudaSuccess) return cuda_fail(ce, "absorb launch");

@@ -9,6 +9,12 @@
 // memory staging tile laid out exactly as the TMA store box expects (token-major rows, the
 // store map's swizzle applied), and returns the stores to issue.  Output tails (tokens beyond T,
 // features beyond the matrix) are clipped by the store's tensor map, so no lane masks writes.
+//
+// Given output pointers ("direct" mode, used by the decode launches with tokens as MMA rows) the
+// up-projection and absorb functors instead write their block from registers, each lane 64
+// contiguous bytes of its token's row, and return no TMA store: at decode sizes a TMA store of one 32 x 32 block costs a fraction
+// of a microsecond to issue, which is most of an epilogue chunk, and the tail of the last tile
+// is exposed.  Direct stores mask tokens >= T and features outside the matrix themselves.
 #pragma once
 #include <cuda_bf16.h>
 #include "gemm.cuh"
@@ -95,9 +101,9 @@ struct EpiDown {
     const int lane = threadIdx.x & 31;
     const int b0 = p.seg_tiles * TILE_W;
     if constexpr (SWAP) {
+      const bool first = m0 < b0;
 #pragma unroll
       for (int j = 0; j < CH; ++j) st_f32(sb, sw128_f32(j, lane), v[j]);
-      const bool first = m0 < b0;
       ops[0] = {first ? 0 : 1, 3, first ? m0 : m0 - b0, n0, s, 0};
     } else {
       stage_row_f32(sb, lane, v);
@@ -121,6 +127,8 @@ struct UpParams {
   const float* scale_t;         // (T) per-token dequant scale, int8 path
   const float* dqw;             // (N*(D+Dr)) per-column dequant scale, int8 path
   int32_t T, N, D, Dr;
+  __nv_bfloat16* qc_out;        // direct mode (tokens as MMA rows): q^C (T, N*D), else null
+  __nv_bfloat16* qr_out;        //   and query_rope (T, N, Dr)
 };
 
 template <bool SWAP, bool INT8, int CH>
@@ -144,14 +152,15 @@ struct EpiUp {
       const uint4* c = reinterpret_cast<const uint4*>(p.cos + static_cast<size_t>(t) * p.Dr + p0);
       const uint4* s = reinterpret_cast<const uint4*>(p.sin + static_cast<size_t>(t) * p.Dr + p0);
       const int hb = p.Dr >> 4;           // uint4 offset of run b (Dr/2 bf16)
-      r.ca[0] = __ldg(c);
-      r.ca[1] = __ldg(c + 1);
-      r.sa[0] = __ldg(s);
-      r.sa[1] = __ldg(s + 1);
-      r.cb[0] = __ldg(c + hb);
-      r.cb[1] = __ldg(c + hb + 1);
-      r.sb[0] = __ldg(s + hb);
-      r.sb[1] = __ldg(s + hb + 1);
+      // volatile loads: issued here, a block ahead of their use, not sunk to the use
+      r.ca[0] = ld_nc_v4(c);
+      r.ca[1] = ld_nc_v4(c + 1);
+      r.sa[0] = ld_nc_v4(s);
+      r.sa[1] = ld_nc_v4(s + 1);
+      r.cb[0] = ld_nc_v4(c + hb);
+      r.cb[1] = ld_nc_v4(c + hb + 1);
+      r.sb[0] = ld_nc_v4(s + hb);
+      r.sb[1] = ld_nc_v4(s + hb + 1);
     } else {
       r.ca[0] = r.ca[1] = r.sa[0] = r.sa[1] = r.cb[0] = r.cb[1] = r.sb[0] = r.sb[1] =
           make_uint4(0, 0, 0, 0);
@@ -172,19 +181,23 @@ struct EpiUp {
   // p0 .. p0+15 of one head, with that token's preloaded tables; the results are staged at row r
   // of two 16-wide bf16 tiles holding output columns p0.. and p0+Dr/2.. (offsets 0 and 1024 of
   // the staging buffer).
-  __device__ __forceinline__ void rope_row(uint8_t* sb, int r, const Pre& P, const float* y) const {
+  __device__ __forceinline__ void rope_pairs(const Pre& P, const float* y, float (&oa)[16],
+                                             float (&ob)[16]) const {
     float c0[16], s0[16], c1[16], s1[16];
     unpack_bf16x16(P.ca, c0);
     unpack_bf16x16(P.sa, s0);
     unpack_bf16x16(P.cb, c1);
     unpack_bf16x16(P.sb, s1);
-    float oa[16], ob[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float y0 = y[2 * i], y1 = y[2 * i + 1];
       oa[i] = y0 * c0[i] - y1 * s0[i];
       ob[i] = y1 * c1[i] + y0 * s1[i];
     }
+  }
+  __device__ __forceinline__ void rope_row(uint8_t* sb, int r, const Pre& P, const float* y) const {
+    float oa[16], ob[16];
+    rope_pairs(P, y, oa, ob);
     stage_row_bf16x16(sb, r, oa);
     stage_row_bf16x16(sb + 1024, r, ob);
   }
@@ -253,6 +266,27 @@ struct EpiUp {
 #pragma unroll
         for (int j = 0; j < 32; ++j) w[j] = v[j];
       }
+      if (p.qc_out != nullptr) {   // direct: lane = token, 64 contiguous bytes
+        if (t >= p.T) return 0;
+        if (n0 < nd) {
+          uint4* dst = reinterpret_cast<uint4*>(p.qc_out + static_cast<size_t>(t) * nd + n0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) dst[c] = pack_bf16x8(w + 8 * c);
+          return 0;
+        }
+        const int r0 = n0 - nd;
+        const int n = r0 / p.Dr, p0 = (r0 % p.Dr) >> 1;
+        float oa[16], ob[16];
+        rope_pairs(P, w, oa, ob);
+        __nv_bfloat16* row = p.qr_out + (static_cast<size_t>(t) * p.N + n) * p.Dr;
+        uint4* da = reinterpret_cast<uint4*>(row + p0);
+        uint4* db = reinterpret_cast<uint4*>(row + p0 + (p.Dr >> 1));
+        da[0] = pack_bf16x8(oa);
+        da[1] = pack_bf16x8(oa + 8);
+        db[0] = pack_bf16x8(ob);
+        db[1] = pack_bf16x8(ob + 8);
+        return 0;
+      }
       if (n0 < nd) {
         stage_row_bf16x32(sb, lane, w);
         ops[0] = {0, 2, n0, m0, 0, 0};
@@ -273,7 +307,8 @@ struct EpiUp {
 // heads n; W^UK prepacked per head as (Hckv, D) so it is K-major.  Output map: query as 3-D
 // (Hckv, N, T) bf16.
 struct AbsorbParams {
-  int32_t unused;
+  __nv_bfloat16* out;           // direct mode (tokens as MMA rows): query (T, N, Hckv), else null
+  int32_t T, N, Hckv;
 };
 
 template <bool SWAP, int CH>
@@ -290,6 +325,16 @@ struct EpiAbsorb {
       for (int j = 0; j < CH; ++j) st_bf16(sb, sw64_bf16(j, lane), v[j]);
       ops[0] = {0, 3, m0, n, n0, 0};
     } else {
+      if (p.out != nullptr) {   // direct: lane = token, 64 contiguous bytes
+        const int t = m0 + lane;
+        if (t < p.T) {
+          uint4* dst = reinterpret_cast<uint4*>(
+              p.out + (static_cast<size_t>(t) * p.N + n) * p.Hckv + n0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) dst[c] = pack_bf16x8(v + 8 * c);
+        }
+        return 0;
+      }
       stage_row_bf16x32(sb, lane, v);
       ops[0] = {0, 3, n0, n, m0, 0};
     }

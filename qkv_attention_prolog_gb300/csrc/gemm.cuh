@@ -19,8 +19,16 @@
 // brings both, and two MMAs per K step share the B tile, so each weight byte costs half the
 // activation traffic and half the TMA operations.
 //
+// With ALD the activation operand does not go through TMA: four loader warps copy it from global
+// memory (where it sits in L2: it is small and was just written by the previous kernel) with
+// 16-byte cp.async straight into the swizzled operand layout, and each loader thread's arrival
+// on the stage's full barrier fires when its copies land.  TMA then carries only the weight
+// stream, which is what a memory-bound decode GEMM needs: the activation tile per K step is as
+// large as the weight tile, and sharing the TMA unit's requests with it halved the weight rate.
+//
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM owner, warp 3 = idle,
-// warps 4..7 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31), warps 8..11 = int8 converters.
+// warps 4..7 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31), warps 8..11 = int8 converters
+// (WQ) or activation loaders (ALD).
 //
 // Work units: (m tile, n tile, batch, k split), m fastest, distributed round-robin over a grid
 // of at most one CTA per SM.  In stream-K mode every CTA instead takes an equal contiguous range
@@ -48,6 +56,16 @@ struct GemmGeometry {
   int32_t stream_k;                 // 1: equal (tile, k block) ranges per CTA (splits must be 1)
   float* sk_partial;                // stream-K: per-CTA fp32 partial slots (BM_U * BN floats each)
   int32_t* sk_flag;                 // stream-K: per-CTA "partial written" flags, 0 between calls
+  // ALD: the activation operand (B, decode orientation) as a row-major bf16 matrix
+  const uint16_t* act;              // element (y, x) at act[y * act_ld + x]
+  int64_t act_ld;
+  int32_t act_rows, act_cols;       // extents; copies outside them are zero-filled
+  // Row-range schedule (weight as operand B, m_tiles = 1, no K split): the B rows of all batches,
+  // batches * rr_rows in 32-row chunks, are cut into one equal contiguous range per CTA, and a
+  // range into pieces at batch boundaries and every BN rows.  A piece is loaded as 32-row TMA
+  // boxes and multiplied with N = its row count, so every SM streams the same share of the
+  // weight whatever its row count (no tile rounding, no partial sums).
+  int32_t rr_on, rr_rows;
 };
 
 // One piece of work for a CTA: a tile and its k-block range, and its stream-K role.
@@ -56,6 +74,7 @@ struct Frag {
   int kb0, kb1;
   int kind;      // 0: whole tile; 1: owner of a cut tile; 2: contributor to a cut tile
   int c_last;    // owner: last CTA holding a piece of this tile
+  int row0, rows;   // rows of operand B (within batch b) covered by the piece
 };
 
 // One TMA store of an epilogue staging tile: which output map, its rank and coordinates, and the
@@ -69,10 +88,12 @@ struct StoreOp {
 
 // WQ: 0 = bf16 weight, 1 = int8 weight in operand A, 2 = int8 weight in operand B.
 // MT: 128-row tiles of A per unit (1 or 2), each with its own TMEM accumulator.
-template <int BN_, int WQ_ = 0, int MT_ = 1>
+// ALD: operand B (the activation, decode orientation) is loaded by cp.async loader warps.
+template <int BN_, int WQ_ = 0, int MT_ = 1, int ALD_ = 0>
 struct GemmCfg {
   static constexpr int WQ = WQ_;
   static constexpr int MT = MT_;
+  static constexpr int ALD = ALD_;
   static constexpr int BM = 128;                       // rows per MMA
   static constexpr int BM_U = BM * MT;                 // rows of A per unit
   static constexpr int BN = BN_;
@@ -94,12 +115,14 @@ struct GemmCfg {
   static constexpr uint32_t TMEM_COLS =
       ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-  static constexpr int THREADS = WQ ? 384 : 256;
+  static constexpr int THREADS = (WQ || ALD) ? 384 : 256;
+  static constexpr uint32_t FULL_ARRIVALS = WQ ? 1 + 4 : (ALD ? 1 + 128 : 1);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16,256]");
   static_assert(B_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages must keep 1024-B alignment");
   static_assert(STAGES >= 2, "pipeline needs two stages");
   static_assert(ACC_COLS <= 512, "accumulators exceed tensor memory");
   static_assert(MT == 1 || MT == 2, "one or two row tiles per unit");
+  static_assert(!(ALD && WQ), "cp.async activation loading is for bf16 weights");
 };
 
 __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& tm, int& tn, int& b,
@@ -114,11 +137,16 @@ __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& t
 
 // Iterates this CTA's work; every role walks the same sequence.
 struct FragIter {
-  int u;
+  int u, bn;
   long long i, i1, total;
-  __device__ __forceinline__ explicit FragIter(const GemmGeometry& g) {
+  __device__ __forceinline__ FragIter(const GemmGeometry& g, int bn_) {
     u = blockIdx.x;
-    total = static_cast<long long>(g.num_units) * g.k_blocks;   // stream-K: num_units = tiles
+    bn = bn_;
+    if (g.rr_on) {   // chunk range of this CTA
+      total = static_cast<long long>(g.batches) * (g.rr_rows / 32);
+    } else {
+      total = static_cast<long long>(g.num_units) * g.k_blocks;   // stream-K: num_units = tiles
+    }
     i = total * blockIdx.x / gridDim.x;
     i1 = total * (blockIdx.x + 1) / gridDim.x;
   }
@@ -127,6 +155,27 @@ struct FragIter {
     return static_cast<int>(((it + 1) * gridDim.x - 1) / total);
   }
   __device__ __forceinline__ bool next(const GemmGeometry& g, Frag& f) {
+    if (g.rr_on) {
+      if (i >= i1) return false;
+      const int per_batch = g.rr_rows / 32;
+      const int b = static_cast<int>(i / per_batch);
+      const int c0 = static_cast<int>(i % per_batch);
+      long long n = i1 - i;
+      if (n > per_batch - c0) n = per_batch - c0;
+      if (n > bn / 32) n = bn / 32;
+      f.tm = 0;
+      f.tn = 0;
+      f.b = b;
+      f.s = 0;
+      f.kb0 = 0;
+      f.kb1 = g.k_blocks;
+      f.kind = 0;
+      f.c_last = 0;
+      f.row0 = c0 * 32;
+      f.rows = static_cast<int>(n) * 32;
+      i += n;
+      return true;
+    }
     if (!g.stream_k) {
       if (u >= g.num_units) return false;
       decode_unit(g, u, f.tm, f.tn, f.b, f.s);
@@ -134,6 +183,8 @@ struct FragIter {
       f.kb1 = ((f.s + 1) * g.k_blocks) / g.splits;
       f.kind = 0;
       f.c_last = 0;
+      f.row0 = f.tn * bn;
+      f.rows = bn;
       u += gridDim.x;
       return true;
     }
@@ -144,6 +195,8 @@ struct FragIter {
     const long long end = (i1 - i) < (K - f.kb0) ? f.kb0 + (i1 - i) : K;
     f.kb1 = static_cast<int>(end);
     decode_unit(g, static_cast<int>(tile), f.tm, f.tn, f.b, f.s);
+    f.row0 = f.tn * bn;
+    f.rows = bn;
     if (f.kb0 == 0 && f.kb1 == K) {
       f.kind = 0;
     } else if (f.kb0 == 0) {
@@ -202,8 +255,8 @@ __device__ __forceinline__ void stage_row_f32_sw128(uint8_t* sb, int r, const fl
 // first A row is m0 (lane l holds row m0 + l) and first B row is n0 (v[j] is column n0 + j).  It
 // writes the block's output into the warp's staging buffer and returns the TMA stores (at most
 // two, warp-uniform) that move it to global memory through the two output tensor maps.
-template <int BN, class Epi, int WQ, int MT>
-__global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
+template <int BN, class Epi, int WQ, int MT, int ALD>
+__global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                      const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB0,
@@ -212,7 +265,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmO1,
                      const __grid_constant__ CUtensorMap tmP, const GemmGeometry geo,
                      const Epi epi, uint32_t* __restrict__ err_word) {
-  using Cfg = GemmCfg<BN, WQ, MT>;
+  using Cfg = GemmCfg<BN, WQ, MT, ALD>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -244,7 +297,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
   }
   if (warp == 1 && lane == 0) {
     for (int i = 0; i < Cfg::STAGES; ++i) {
-      mbar_init(&full_bar[i], WQ ? 1 + 4 : 1);   // producer (+ one arrival per converter warp)
+      mbar_init(&full_bar[i], Cfg::FULL_ARRIVALS);   // producer (+ converter warps / loader threads)
       mbar_init(&empty_bar[i], 1);
       mbar_init(&rawf_bar[i], 1);
     }
@@ -279,43 +332,54 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
         const int y = (first ? tm : tm - geo.a_seg_tiles) * Cfg::BM_U + b * geo.a_y_batch;
         tma_load_2d(dst, first ? &tmA0 : &tmA1, bar, kb * Cfg::BK + b * geo.a_x_batch, y);
       };
-      auto load_b = [&](int tn, int b, int kb, uint64_t* bar, void* dst) {
+      auto load_b = [&](const Frag& f, int kb, uint64_t* bar, void* dst) {
+        const int tn = f.tn, b = f.b;
+        if (geo.rr_on) {   // 32-row boxes (single segment)
+          for (int r = 0; r < f.rows; r += 32)
+            tma_load_2d(static_cast<uint8_t*>(dst) + r * 128, &tmB0, bar,
+                        kb * Cfg::BK + b * geo.b_x_batch, f.row0 + r + b * geo.b_y_batch);
+          return;
+        }
         const bool first = tn < geo.b_seg_tiles;
         const int y = (first ? tn : tn - geo.b_seg_tiles) * Cfg::BN + b * geo.b_y_batch;
         tma_load_2d(dst, first ? &tmB0 : &tmB1, bar, kb * Cfg::BK + b * geo.b_x_batch, y);
       };
       // weight tile of stage st (bf16 into the operand buffer, or int8 into the raw buffer)
-      auto issue_weight = [&](int st, int tm, int tn, int b, int kb) {
+      auto issue_weight = [&](int st, const Frag& f, int kb) {
         if constexpr (WQ != 0) {
           mbar_arrive_expect_tx(&rawf_bar[st], Cfg::RAW_BYTES);
-          if (WQ == 1) load_a(tm, b, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES);
-          else load_b(tn, b, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES);
+          if (WQ == 1) load_a(f.tm, f.b, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES);
+          else load_b(f, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES);
+        } else if (ALD) {
+          mbar_arrive_expect_tx(&full_bar[st], Cfg::A_BYTES);
+          load_a(f.tm, f.b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
         } else if (w_is_a) {
           mbar_expect_tx(&full_bar[st], Cfg::A_BYTES);
-          load_a(tm, b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
+          load_a(f.tm, f.b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
         } else {
-          mbar_expect_tx(&full_bar[st], Cfg::B_BYTES);
-          load_b(tn, b, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
+          mbar_expect_tx(&full_bar[st], static_cast<uint32_t>(f.rows) * Cfg::BK * 2);
+          load_b(f, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
         }
       };
-      auto issue_act = [&](int st, int tm, int tn, int b, int kb) {
+      auto issue_act = [&](int st, const Frag& f, int kb) {
+        if (ALD) return;
         if (w_is_a) {
           mbar_arrive_expect_tx(&full_bar[st], Cfg::B_BYTES);
-          load_b(tn, b, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
+          load_b(f, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
         } else {
           mbar_arrive_expect_tx(&full_bar[st], Cfg::A_BYTES);
-          load_a(tm, b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
+          load_a(f.tm, f.b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
         }
       };
 
       // Weight tiles of this CTA's first stages, before the grid dependency resolves.
       int pre = 0;
       {
-        FragIter it0(geo);
+        FragIter it0(geo, Cfg::BN);
         Frag f0;
         if (it0.next(geo, f0)) {
           pre = f0.kb1 - f0.kb0 < Cfg::STAGES ? f0.kb1 - f0.kb0 : Cfg::STAGES;
-          for (int i = 0; i < pre; ++i) issue_weight(i, f0.tm, f0.tn, f0.b, f0.kb0 + i);
+          for (int i = 0; i < pre; ++i) issue_weight(i, f0, f0.kb0 + i);
         }
       }
       grid_dependency_wait();
@@ -323,10 +387,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      FragIter it(geo);
+      FragIter it(geo, Cfg::BN);
       Frag f;
       for (int n = 0; ok && it.next(geo, f); ++n) {
-        const int tm = f.tm, tn = f.tn, b = f.b, kb0 = f.kb0, kb1 = f.kb1;
+        const int kb0 = f.kb0, kb1 = f.kb1;
         for (int kb = kb0; kb < kb1; ++kb) {
           const bool prefetched = n == 0 && kb - kb0 < pre;
           if (!prefetched) {
@@ -334,9 +398,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
               ok = false;
               break;
             }
-            issue_weight(stage, tm, tn, b, kb);
+            issue_weight(stage, f, kb);
           }
-          issue_act(stage, tm, tn, b, kb);
+          issue_act(stage, f, kb);
           if (++stage == Cfg::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -365,7 +429,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
       uint32_t phase = 0;
       int iter = 0;
       bool ok = true;
-      FragIter it(geo);
+      FragIter it(geo, Cfg::BN);
       Frag f;
       for (; ok && it.next(geo, f); ++iter) {
         const int kb0 = f.kb0, kb1 = f.kb1;
@@ -374,11 +438,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
         if (!mbar_wait(&acce_bar[buf], (use & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * MT * Cfg::BN);
+        const uint32_t idesc = geo.rr_on ? idesc_bf16_f32(Cfg::BM, f.rows) : Cfg::IDESC;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
+          if (ALD) fence_proxy_async_shared();   // cp.async (generic proxy) data -> tensor core
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(smemA + stage * Cfg::A_BYTES);
           const uint32_t b_addr = smem_u32(smemB + stage * Cfg::B_BYTES);
@@ -388,7 +454,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
             for (int h = 0; h < MT; ++h)
               umma_bf16_ss(d_tmem + h * Cfg::BN,
                            sdesc_kmajor_sw128(a_addr + h * Cfg::BM * Cfg::BK * 2 + kk * 32),
-                           sdesc_kmajor_sw128(b_addr + kk * 32), Cfg::IDESC,
+                           sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
                            (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);   // frees this smem stage once the MMAs have read it
@@ -406,14 +472,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
     uint8_t* wstage = smemE + q * 2 * Cfg::EPI_BUF;
     int sel = 0;
     int iter = 0;
-    FragIter it(geo);
+    FragIter it(geo, Cfg::BN);
     Frag f;
     for (; it.next(geo, f); ++iter) {
       const int tm = f.tm, tn = f.tn, b = f.b, s = f.s;
       const int buf = iter & 1;
       const uint32_t use = static_cast<uint32_t>(iter >> 1);
+      const int n_row0 = f.row0;                                // this piece's B rows
+      const int ncols = MT * f.rows;                            // accumulator columns
       // inputs the epilogue of the first block needs (e.g. RoPE tables), before the wait
-      typename Epi::Pre pre = epi.preload(tm * Cfg::BM_U + q * 32, tn * Cfg::BN);
+      typename Epi::Pre pre = epi.preload(tm * Cfg::BM_U + q * 32, n_row0);
       if (!mbar_wait(&accf_bar[buf], use & 1u, abort_flag)) break;
       tc_fence_after_sync();
       constexpr int kChunks = MT * Cfg::BN / 32;               // 4 KB partial blocks per warp
@@ -450,7 +518,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
         if (landed > 0 && !mbar_wait(&land_bar[q], 0, abort_flag)) landed = 0;
       }
 #pragma unroll 1
-      for (int hc = 0; hc < MT * Cfg::BN; hc += Cfg::CH) {
+      for (int hc = 0; hc < ncols; hc += Cfg::CH) {
         const int h = hc / Cfg::BN, c = hc % Cfg::BN;
         const int m0 = tm * Cfg::BM_U + h * Cfg::BM + q * 32;
         const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -469,7 +537,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
         }
-        if (hc + Cfg::CH >= MT * Cfg::BN) {
+        if (hc + Cfg::CH >= ncols) {
           // last TMEM read of this accumulator: hand it back to the MMA warp right away
           tc_fence_before_sync();
           __syncwarp();
@@ -509,12 +577,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
           }
           nops = 0;
         } else {
-          nops = epi(m0, tn * Cfg::BN + c, b, s, v, sb, ops, pre);
+          nops = epi(m0, n_row0 + c, b, s, v, sb, ops, pre);
         }
-        if (hc + Cfg::CH < MT * Cfg::BN) {   // the next block's inputs, while this one stores
+        if (hc + Cfg::CH < ncols) {   // the next block's inputs, while this one stores
           const int hn = (hc + Cfg::CH) / Cfg::BN, cn = (hc + Cfg::CH) % Cfg::BN;
-          pre = epi.preload(tm * Cfg::BM_U + hn * Cfg::BM + q * 32, tn * Cfg::BN + cn);
+          pre = epi.preload(tm * Cfg::BM_U + hn * Cfg::BM + q * 32, n_row0 + cn);
         }
+        if (nops == 0 && f.kind != 2) continue;   // written directly from registers
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
@@ -550,14 +619,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
           for (int cc = blockIdx.x + 1; cc <= f.c_last; ++cc) geo.sk_flag[cc] = 0;
       }
     }
-    if (lane == 0) bulk_wait_group<0>();           // all output writes complete
+    // every store has read its staging buffer (the writes themselves complete with the grid)
+    if (lane == 0) bulk_wait_group_read<0>();
   } else if (WQ != 0 && warp >= 8) {
     // ------------------------------------------------------------------ int8 -> bf16 converters
     const int ct = threadIdx.x - 256;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    FragIter it(geo);
+    FragIter it(geo, Cfg::BN);
     Frag f;
     while (ok && it.next(geo, f)) {
       for (int kb = f.kb0; kb < f.kb1; ++kb) {
@@ -577,6 +647,44 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT>::THREADS, 1)
         }
       }
     }
+  } else if (ALD && warp >= 8) {
+    // ------------------------------------------------------------------ activation loaders
+    // Thread t copies 16-byte chunk (t % 8) of rows t / 8, t / 8 + 16, ... of the BN x 64 tile:
+    // eight consecutive lanes read one 128-byte row segment.
+    const int lt = threadIdx.x - 256;
+    const int c = lt & 7;
+    const int r0 = lt >> 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    FragIter it(geo, Cfg::BN);
+    Frag f;
+    while (ok && it.next(geo, f)) {
+      const int y0 = f.tn * Cfg::BN + f.b * geo.b_y_batch;
+      for (int kb = f.kb0; kb < f.kb1; ++kb) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int x = f.b * geo.b_x_batch + kb * Cfg::BK + c * 8;
+        const bool xin = x < geo.act_cols;
+        uint8_t* dst = smemB + stage * Cfg::B_BYTES;
+#pragma unroll
+        for (int i = 0; i < Cfg::BN / 16; ++i) {
+          const int r = r0 + 16 * i;
+          const int y = y0 + r;
+          const bool in = xin && y < geo.act_rows;
+          const uint16_t* src = in ? geo.act + static_cast<int64_t>(y) * geo.act_ld + x : geo.act;
+          cp_async_16(dst + r * 128 + (((c ^ (r & 7)) & 7) << 4), src, in ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(&full_bar[stage]);
+        if (++stage == Cfg::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait_all();                         // nothing of ours lands after the CTA exits
   }
 
   __syncthreads();

@@ -6,15 +6,15 @@ namespace mlap {
 cudaError_t launch_down(const GemmLaunch& L, const DownParams& p) {
   if (L.swap) {
     switch (L.bn) {
-      case 16: return L.mt == 2 ? launch_gemm_t<16, 0, 2>(L, EpiDown<true, 256, 16>{p})
-                           : launch_gemm_t<16, 0, 1>(L, EpiDown<true, 128, 16>{p});
-      case 32: return L.mt == 2 ? launch_gemm_t<32, 0, 2>(L, EpiDown<true, 256, 32>{p})
-                           : launch_gemm_t<32, 0, 1>(L, EpiDown<true, 128, 32>{p});
-      case 64: return L.mt == 2 ? launch_gemm_t<64, 0, 2>(L, EpiDown<true, 256, 32>{p})
-                           : launch_gemm_t<64, 0, 1>(L, EpiDown<true, 128, 32>{p});
-      case 128: return L.mt == 2 ? launch_gemm_t<128, 0, 2>(L, EpiDown<true, 256, 32>{p})
-                           : launch_gemm_t<128, 0, 1>(L, EpiDown<true, 128, 32>{p});
-      case 256: return launch_gemm_t<256, 0, 1>(L, EpiDown<true, 128, 32>{p});
+      case 16: return L.mt == 2 ? launch_gemm_t<16, 0, 2, 1>(L, EpiDown<true, 256, 16>{p})
+                           : launch_gemm_t<16, 0, 1, 1>(L, EpiDown<true, 128, 16>{p});
+      case 32: return L.mt == 2 ? launch_gemm_t<32, 0, 2, 1>(L, EpiDown<true, 256, 32>{p})
+                           : launch_gemm_t<32, 0, 1, 1>(L, EpiDown<true, 128, 32>{p});
+      case 64: return L.mt == 2 ? launch_gemm_t<64, 0, 2, 1>(L, EpiDown<true, 256, 32>{p})
+                           : launch_gemm_t<64, 0, 1, 1>(L, EpiDown<true, 128, 32>{p});
+      case 128: return L.mt == 2 ? launch_gemm_t<128, 0, 2, 1>(L, EpiDown<true, 256, 32>{p})
+                           : launch_gemm_t<128, 0, 1, 1>(L, EpiDown<true, 128, 32>{p});
+      case 256: return launch_gemm_t<256, 0, 1, 1>(L, EpiDown<true, 128, 32>{p});
       default: return cudaErrorInvalidValue;
     }
   }

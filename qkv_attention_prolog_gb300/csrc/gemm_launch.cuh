@@ -4,17 +4,17 @@
 
 namespace mlap {
 
-template <int BN, int WQ = 0, int MT = 1, class Epi>
+template <int BN, int WQ = 0, int MT = 1, int ALD = 0, class Epi>
 cudaError_t launch_gemm_t(const GemmLaunch& L, const Epi& epi) {
-  auto kern = umma_gemm_kernel<BN, Epi, WQ, MT>;
-  constexpr int kSmem = GemmCfg<BN, WQ, MT>::SMEM_BYTES;
+  auto kern = umma_gemm_kernel<BN, Epi, WQ, MT, ALD>;
+  constexpr int kSmem = GemmCfg<BN, WQ, MT, ALD>::SMEM_BYTES;
   // The dynamic shared memory opt-in is a per-device function attribute; setting it on every
   // launch costs little next to the launch itself and stays correct across devices.
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
-  cfg.blockDim = dim3(GemmCfg<BN, WQ, MT>::THREADS);
+  cfg.blockDim = dim3(GemmCfg<BN, WQ, MT, ALD>::THREADS);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = L.stream;
   cudaLaunchAttribute attr[1];

@@ -9,17 +9,18 @@ template <bool INT8>
 static cudaError_t launch_up_t(const GemmLaunch& L, const UpParams& p) {
   constexpr int WA = INT8 ? 1 : 0;   // int8 weight as operand A (decode orientation)
   constexpr int WB = INT8 ? 2 : 0;   // int8 weight as operand B (prefill orientation)
+  constexpr int AL = INT8 ? 0 : 1;   // bf16 weight: activation through the cp.async loaders
   if (L.swap) {
     switch (L.bn) {
-      case 16: return L.mt == 2 ? launch_gemm_t<16, WA, 2>(L, EpiUp<true, INT8, 16>{p})
-                           : launch_gemm_t<16, WA, 1>(L, EpiUp<true, INT8, 16>{p});
-      case 32: return L.mt == 2 ? launch_gemm_t<32, WA, 2>(L, EpiUp<true, INT8, 32>{p})
-                           : launch_gemm_t<32, WA, 1>(L, EpiUp<true, INT8, 32>{p});
-      case 64: return L.mt == 2 ? launch_gemm_t<64, WA, 2>(L, EpiUp<true, INT8, 32>{p})
-                           : launch_gemm_t<64, WA, 1>(L, EpiUp<true, INT8, 32>{p});
-      case 128: return L.mt == 2 ? launch_gemm_t<128, WA, 2>(L, EpiUp<true, INT8, 32>{p})
-                           : launch_gemm_t<128, WA, 1>(L, EpiUp<true, INT8, 32>{p});
-      case 256: return launch_gemm_t<256, WA, 1>(L, EpiUp<true, INT8, 32>{p});
+      case 16: return L.mt == 2 ? launch_gemm_t<16, WA, 2, AL>(L, EpiUp<true, INT8, 16>{p})
+                           : launch_gemm_t<16, WA, 1, AL>(L, EpiUp<true, INT8, 16>{p});
+      case 32: return L.mt == 2 ? launch_gemm_t<32, WA, 2, AL>(L, EpiUp<true, INT8, 32>{p})
+                           : launch_gemm_t<32, WA, 1, AL>(L, EpiUp<true, INT8, 32>{p});
+      case 64: return L.mt == 2 ? launch_gemm_t<64, WA, 2, AL>(L, EpiUp<true, INT8, 32>{p})
+                           : launch_gemm_t<64, WA, 1, AL>(L, EpiUp<true, INT8, 32>{p});
+      case 128: return L.mt == 2 ? launch_gemm_t<128, WA, 2, AL>(L, EpiUp<true, INT8, 32>{p})
+                           : launch_gemm_t<128, WA, 1, AL>(L, EpiUp<true, INT8, 32>{p});
+      case 256: return launch_gemm_t<256, WA, 1, AL>(L, EpiUp<true, INT8, 32>{p});
       default: return cudaErrorInvalidValue;
     }
   }
