@@ -12,9 +12,9 @@
 //
 // Given output pointers ("direct" mode, used by the decode launches with tokens as MMA rows) the
 // up-projection and absorb functors instead write their block from registers, each lane 64
-// contiguous bytes of its token's row, and return no TMA store: at decode sizes a TMA store of one 32 x 32 block costs a fraction
-// of a microsecond to issue, which is most of an epilogue chunk, and the tail of the last tile
-// is exposed.  Direct stores mask tokens >= T and features outside the matrix themselves.
+// contiguous bytes of its token's row, and return no TMA store: at decode sizes a TMA store of
+// one 32 x 32 block costs a fraction of a microsecond to issue, which is most of an epilogue
+// chunk, and the tail of the last tile is exposed.  Direct stores mask tokens >= T themselves.
 #pragma once
 #include <cuda_bf16.h>
 #include "gemm.cuh"
