@@ -236,8 +236,8 @@ mlap_status_t mlap_timer_destroy(void* timer);
  * routine).
  *   - Shapes whose workspace (mlap_get_workspace_size) exceeds MLAP_NO_ALLOC_SCRATCH_BYTES are
  *     rejected with MLAP_ERR_WORKSPACE before any device work.  With the decode shapes
- *     (He 7168, Hcq 1536, Hckv 512, N 128, D 128, Dr 64) calls with T <= 147 or
- *     257 <= T <= 568 tokens fit (up to 256 tokens the down-projection keeps up to 16 K-split
+ *     (He 7168, Hcq 1536, Hckv 512, N 128, D 128, Dr 64) calls with T <= 128 or
+ *     257 <= T <= 567 tokens fit (up to 256 tokens the down-projection keeps up to 16 K-split
  *     partials, above that one).
  *   - The first call on each device looks up the array's device address with that device
  *     current; make that first call before any stream capture on the device.

@@ -565,7 +565,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       u.bn = 256;
       u.geo.m_tiles = 1;
       u.geo.n_tiles = 1;
-      u.geo.rr_on = 1;
+      u.rr = true;
       u.geo.rr_rows = static_cast<int32_t>(Mup);
     } else if (swap) {
       if (d.w_int8)
@@ -659,7 +659,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       b.geo.a_y_batch = 0;
       b.geo.b_x_batch = 0;
       b.geo.b_y_batch = static_cast<int32_t>(d.Hckv);
-      b.geo.rr_on = 1;
+      b.rr = true;
       b.geo.rr_rows = static_cast<int32_t>(d.Hckv);
     } else if (swap) {
       CHECK_STATUS(make_tmap(&b.a0, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, wrows));

@@ -10,11 +10,12 @@
 // store map's swizzle applied), and returns the stores to issue.  Output tails (tokens beyond T,
 // features beyond the matrix) are clipped by the store's tensor map, so no lane masks writes.
 //
-// Given output pointers ("direct" mode, used by the decode launches with tokens as MMA rows) the
-// up-projection and absorb functors instead write their block from registers, each lane 64
-// contiguous bytes of its token's row, and return no TMA store: at decode sizes a TMA store of
-// one 32 x 32 block costs a fraction of a microsecond to issue, which is most of an epilogue
-// chunk, and the tail of the last tile is exposed.  Direct stores mask tokens >= T themselves.
+// In "direct" mode (template flag; the decode launches with tokens as MMA rows and the row-range
+// schedule) the up-projection and absorb functors instead write their block from registers, each
+// lane 64 contiguous bytes of its token's row, and return no TMA store: at decode sizes a TMA
+// store of one 32 x 32 block costs a fraction of a microsecond to issue, which is most of an
+// epilogue chunk, and the tail of the last tile is exposed.  Direct stores mask tokens >= T
+// themselves.  The flag is compile-time so that the other launches keep their code unchanged.
 #pragma once
 #include <cuda_bf16.h>
 #include "gemm.cuh"
@@ -92,6 +93,7 @@ struct DownParams {
 
 template <bool SWAP, int TILE_W, int CH>
 struct EpiDown {
+  static constexpr bool kDirect = false;
   DownParams p;
   struct Pre {};
   __device__ __forceinline__ Pre preload(int, int) const { return {}; }
@@ -127,12 +129,15 @@ struct UpParams {
   const float* scale_t;         // (T) per-token dequant scale, int8 path
   const float* dqw;             // (N*(D+Dr)) per-column dequant scale, int8 path
   int32_t T, N, D, Dr;
-  __nv_bfloat16* qc_out;        // direct mode (tokens as MMA rows): q^C (T, N*D), else null
+  __nv_bfloat16* qc_out;        // direct mode: q^C (T, N*D)
   __nv_bfloat16* qr_out;        //   and query_rope (T, N, Dr)
 };
 
-template <bool SWAP, bool INT8, int CH>
+// DIRECT: the row-range decode launch (tokens as MMA rows, outputs written from registers).
+template <bool SWAP, bool INT8, int CH, bool DIRECT = false>
 struct EpiUp {
+  static constexpr bool kDirect = DIRECT;
+  static_assert(!DIRECT || (!SWAP && !INT8), "direct stores: bf16 weight, tokens as MMA rows");
   UpParams p;
 
   // RoPE tables of one lane's token for one 32-row rope block: cos/sin of pairs p0..p0+15
@@ -152,15 +157,14 @@ struct EpiUp {
       const uint4* c = reinterpret_cast<const uint4*>(p.cos + static_cast<size_t>(t) * p.Dr + p0);
       const uint4* s = reinterpret_cast<const uint4*>(p.sin + static_cast<size_t>(t) * p.Dr + p0);
       const int hb = p.Dr >> 4;           // uint4 offset of run b (Dr/2 bf16)
-      // volatile loads: issued here, a block ahead of their use, not sunk to the use
-      r.ca[0] = ld_nc_v4(c);
-      r.ca[1] = ld_nc_v4(c + 1);
-      r.sa[0] = ld_nc_v4(s);
-      r.sa[1] = ld_nc_v4(s + 1);
-      r.cb[0] = ld_nc_v4(c + hb);
-      r.cb[1] = ld_nc_v4(c + hb + 1);
-      r.sb[0] = ld_nc_v4(s + hb);
-      r.sb[1] = ld_nc_v4(s + hb + 1);
+      r.ca[0] = __ldg(c);
+      r.ca[1] = __ldg(c + 1);
+      r.sa[0] = __ldg(s);
+      r.sa[1] = __ldg(s + 1);
+      r.cb[0] = __ldg(c + hb);
+      r.cb[1] = __ldg(c + hb + 1);
+      r.sb[0] = __ldg(s + hb);
+      r.sb[1] = __ldg(s + hb + 1);
     } else {
       r.ca[0] = r.ca[1] = r.sa[0] = r.sa[1] = r.cb[0] = r.cb[1] = r.sb[0] = r.sb[1] =
           make_uint4(0, 0, 0, 0);
@@ -266,7 +270,7 @@ struct EpiUp {
 #pragma unroll
         for (int j = 0; j < 32; ++j) w[j] = v[j];
       }
-      if (p.qc_out != nullptr) {   // direct: lane = token, 64 contiguous bytes
+      if constexpr (DIRECT) {   // lane = token, 64 contiguous bytes
         if (t >= p.T) return 0;
         if (n0 < nd) {
           uint4* dst = reinterpret_cast<uint4*>(p.qc_out + static_cast<size_t>(t) * nd + n0);
@@ -307,12 +311,14 @@ struct EpiUp {
 // heads n; W^UK prepacked per head as (Hckv, D) so it is K-major.  Output map: query as 3-D
 // (Hckv, N, T) bf16.
 struct AbsorbParams {
-  __nv_bfloat16* out;           // direct mode (tokens as MMA rows): query (T, N, Hckv), else null
+  __nv_bfloat16* out;           // direct mode: query (T, N, Hckv)
   int32_t T, N, Hckv;
 };
 
-template <bool SWAP, int CH>
+template <bool SWAP, int CH, bool DIRECT = false>
 struct EpiAbsorb {
+  static constexpr bool kDirect = DIRECT;
+  static_assert(!DIRECT || !SWAP, "direct stores: tokens as MMA rows");
   AbsorbParams p;
   struct Pre {};
   __device__ __forceinline__ Pre preload(int, int) const { return {}; }
@@ -325,7 +331,7 @@ struct EpiAbsorb {
       for (int j = 0; j < CH; ++j) st_bf16(sb, sw64_bf16(j, lane), v[j]);
       ops[0] = {0, 3, m0, n, n0, 0};
     } else {
-      if (p.out != nullptr) {   // direct: lane = token, 64 contiguous bytes
+      if constexpr (DIRECT) {   // lane = token, 64 contiguous bytes
         const int t = m0 + lane;
         if (t < p.T) {
           uint4* dst = reinterpret_cast<uint4*>(

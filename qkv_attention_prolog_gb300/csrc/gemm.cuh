@@ -65,7 +65,7 @@ struct GemmGeometry {
   // range into pieces at batch boundaries and every BN rows.  A piece is loaded as 32-row TMA
   // boxes and multiplied with N = its row count, so every SM streams the same share of the
   // weight whatever its row count (no tile rounding, no partial sums).
-  int32_t rr_on, rr_rows;
+  int32_t rr_rows;
 };
 
 // One piece of work for a CTA: a tile and its k-block range, and its stream-K role.
@@ -74,7 +74,7 @@ struct Frag {
   int kb0, kb1;
   int kind;      // 0: whole tile; 1: owner of a cut tile; 2: contributor to a cut tile
   int c_last;    // owner: last CTA holding a piece of this tile
-  int row0, rows;   // rows of operand B (within batch b) covered by the piece
+  int row0, rows;   // row-range schedule: rows of operand B (within batch b) of the piece
 };
 
 // One TMA store of an epilogue staging tile: which output map, its rank and coordinates, and the
@@ -135,14 +135,15 @@ __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& t
   s = u / g.batches;
 }
 
-// Iterates this CTA's work; every role walks the same sequence.
+// Iterates this CTA's work; every role walks the same sequence.  RR: the row-range schedule
+// (compile-time, so that the other launches carry none of its code).
+template <bool RR, int BN>
 struct FragIter {
-  int u, bn;
+  int u;
   long long i, i1, total;
-  __device__ __forceinline__ FragIter(const GemmGeometry& g, int bn_) {
+  __device__ __forceinline__ explicit FragIter(const GemmGeometry& g) {
     u = blockIdx.x;
-    bn = bn_;
-    if (g.rr_on) {   // chunk range of this CTA
+    if constexpr (RR) {   // chunk range of this CTA
       total = static_cast<long long>(g.batches) * (g.rr_rows / 32);
     } else {
       total = static_cast<long long>(g.num_units) * g.k_blocks;   // stream-K: num_units = tiles
@@ -155,14 +156,14 @@ struct FragIter {
     return static_cast<int>(((it + 1) * gridDim.x - 1) / total);
   }
   __device__ __forceinline__ bool next(const GemmGeometry& g, Frag& f) {
-    if (g.rr_on) {
+    if constexpr (RR) {
       if (i >= i1) return false;
       const int per_batch = g.rr_rows / 32;
       const int b = static_cast<int>(i / per_batch);
       const int c0 = static_cast<int>(i % per_batch);
       long long n = i1 - i;
       if (n > per_batch - c0) n = per_batch - c0;
-      if (n > bn / 32) n = bn / 32;
+      if (n > BN / 32) n = BN / 32;
       f.tm = 0;
       f.tn = 0;
       f.b = b;
@@ -183,8 +184,6 @@ struct FragIter {
       f.kb1 = ((f.s + 1) * g.k_blocks) / g.splits;
       f.kind = 0;
       f.c_last = 0;
-      f.row0 = f.tn * bn;
-      f.rows = bn;
       u += gridDim.x;
       return true;
     }
@@ -195,8 +194,6 @@ struct FragIter {
     const long long end = (i1 - i) < (K - f.kb0) ? f.kb0 + (i1 - i) : K;
     f.kb1 = static_cast<int>(end);
     decode_unit(g, static_cast<int>(tile), f.tm, f.tn, f.b, f.s);
-    f.row0 = f.tn * bn;
-    f.rows = bn;
     if (f.kb0 == 0 && f.kb1 == K) {
       f.kind = 0;
     } else if (f.kb0 == 0) {
@@ -266,6 +263,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmP, const GemmGeometry geo,
                      const Epi epi, uint32_t* __restrict__ err_word) {
   using Cfg = GemmCfg<BN, WQ, MT, ALD>;
+  constexpr bool RR = Epi::kDirect;   // the row-range launches are the direct-store ones
+  using Iter = FragIter<RR, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -334,7 +333,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
       };
       auto load_b = [&](const Frag& f, int kb, uint64_t* bar, void* dst) {
         const int tn = f.tn, b = f.b;
-        if (geo.rr_on) {   // 32-row boxes (single segment)
+        if constexpr (RR) {   // 32-row boxes (single segment)
           for (int r = 0; r < f.rows; r += 32)
             tma_load_2d(static_cast<uint8_t*>(dst) + r * 128, &tmB0, bar,
                         kb * Cfg::BK + b * geo.b_x_batch, f.row0 + r + b * geo.b_y_batch);
@@ -357,7 +356,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
           mbar_expect_tx(&full_bar[st], Cfg::A_BYTES);
           load_a(f.tm, f.b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
         } else {
-          mbar_expect_tx(&full_bar[st], static_cast<uint32_t>(f.rows) * Cfg::BK * 2);
+          mbar_expect_tx(&full_bar[st], RR ? static_cast<uint32_t>(f.rows) * Cfg::BK * 2
+                                           : static_cast<uint32_t>(Cfg::B_BYTES));
           load_b(f, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
         }
       };
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
       // Weight tiles of this CTA's first stages, before the grid dependency resolves.
       int pre = 0;
       {
-        FragIter it0(geo, Cfg::BN);
+        Iter it0(geo);
         Frag f0;
         if (it0.next(geo, f0)) {
           pre = f0.kb1 - f0.kb0 < Cfg::STAGES ? f0.kb1 - f0.kb0 : Cfg::STAGES;
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      FragIter it(geo, Cfg::BN);
+      Iter it(geo);
       Frag f;
       for (int n = 0; ok && it.next(geo, f); ++n) {
         const int kb0 = f.kb0, kb1 = f.kb1;
@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
       uint32_t phase = 0;
       int iter = 0;
       bool ok = true;
-      FragIter it(geo, Cfg::BN);
+      Iter it(geo);
       Frag f;
       for (; ok && it.next(geo, f); ++iter) {
         const int kb0 = f.kb0, kb1 = f.kb1;
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
         if (!mbar_wait(&acce_bar[buf], (use & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * MT * Cfg::BN);
-        const uint32_t idesc = geo.rr_on ? idesc_bf16_f32(Cfg::BM, f.rows) : Cfg::IDESC;
+        const uint32_t idesc = RR ? idesc_bf16_f32(Cfg::BM, f.rows) : Cfg::IDESC;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
             ok = false;
@@ -472,14 +472,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     uint8_t* wstage = smemE + q * 2 * Cfg::EPI_BUF;
     int sel = 0;
     int iter = 0;
-    FragIter it(geo, Cfg::BN);
+    Iter it(geo);
     Frag f;
     for (; it.next(geo, f); ++iter) {
       const int tm = f.tm, tn = f.tn, b = f.b, s = f.s;
       const int buf = iter & 1;
       const uint32_t use = static_cast<uint32_t>(iter >> 1);
-      const int n_row0 = f.row0;                                // this piece's B rows
-      const int ncols = MT * f.rows;                            // accumulator columns
+      const int n_row0 = RR ? f.row0 : tn * Cfg::BN;            // this piece's B rows
+      const int ncols = RR ? MT * f.rows : MT * Cfg::BN;        // accumulator columns
       // inputs the epilogue of the first block needs (e.g. RoPE tables), before the wait
       typename Epi::Pre pre = epi.preload(tm * Cfg::BM_U + q * 32, n_row0);
       if (!mbar_wait(&accf_bar[buf], use & 1u, abort_flag)) break;
@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
           const int hn = (hc + Cfg::CH) / Cfg::BN, cn = (hc + Cfg::CH) % Cfg::BN;
           pre = epi.preload(tm * Cfg::BM_U + hn * Cfg::BM + q * 32, n_row0 + cn);
         }
-        if (nops == 0 && f.kind != 2) continue;   // written directly from registers
+        if constexpr (Epi::kDirect) continue;   // written directly from registers
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    FragIter it(geo, Cfg::BN);
+    Iter it(geo);
     Frag f;
     while (ok && it.next(geo, f)) {
       for (int kb = f.kb0; kb < f.kb1; ++kb) {
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    FragIter it(geo, Cfg::BN);
+    Iter it(geo);
     Frag f;
     while (ok && it.next(geo, f)) {
       const int y0 = f.tn * Cfg::BN + f.b * geo.b_y_batch;

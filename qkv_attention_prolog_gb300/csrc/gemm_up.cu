@@ -25,6 +25,9 @@ static cudaError_t launch_up_t(const GemmLaunch& L, const UpParams& p) {
     }
   }
   if (L.bn != 256) return cudaErrorInvalidValue;
+  if constexpr (!INT8) {
+    if (L.rr) return launch_gemm_t<256>(L, EpiUp<false, false, 32, true>{p});
+  }
   return launch_gemm_t<256, WB>(L, EpiUp<false, INT8, 32>{p});
 }
 

@@ -22,6 +22,7 @@ struct GemmLaunch {
   int mt;            // 128-row tiles of A per unit (decode orientation: 1 or 2)
   bool swap;
   bool a_int8;       // A operand is an int8 weight converted to bf16 in shared memory
+  bool rr;           // row-range schedule with direct epilogue stores (decode, tokens as rows)
   int grid;
   cudaStream_t stream;
   bool pdl;

@@ -78,33 +78,13 @@ __device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float* v) {
 // One CTA per token.  MAXS bounds the K splits (1: prefill, no split; kMaxSplits: decode), NT is
 // the thread count: with splits every thread issues the loads of all splits of its columns at
 // once (one round of latency), without them the kernel stays small enough for many CTAs per SM.
-// The kernel is latency bound, so it keeps its global round trips to one after the grid
-// dependency: the RmsNorm gammas (weights, not written by the previous kernel) are staged in
-// shared memory before the wait, and the per-call inputs (cache_index, cos / sin) are requested
-// together with the partials.
 template <int MAXS, int NT>
 __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizeParams p) {
-  extern __shared__ float h[];                   // Ntot sums | gamma_cq | gamma_ckv (fp32)
+  extern __shared__ float h[];
   __shared__ float2 red[NT / 32];
   const int t = blockIdx.x;
-  float* g_cq = h + p.Ntot;
-  float* g_ckv = g_cq + p.Hcq;
   grid_launch_dependents();
-  for (int f = threadIdx.x * 8; f < p.Hcq + p.Hckv; f += NT * 8) {   // Hcq % 8 == 0
-    float g[8];
-    load8_bf16(f < p.Hcq ? p.gamma_cq + f : p.gamma_ckv + (f - p.Hcq), g);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) g_cq[f + i] = g[i];                      // g_ckv follows g_cq
-  }
   grid_dependency_wait();
-
-  const bool cache = p.slots > 0;
-  const int64_t idx = cache ? p.cache_index[t] : -1;
-  float kr_cos = 0.f, kr_sin = 0.f;                 // k^R element threadIdx.x (Dr <= NT)
-  if (cache && threadIdx.x < p.Dr) {
-    kr_cos = __bfloat162float(p.cos[static_cast<size_t>(t) * p.Dr + threadIdx.x]);
-    kr_sin = __bfloat162float(p.sin[static_cast<size_t>(t) * p.Dr + threadIdx.x]);
-  }
 
   // h = sum of the K-split partials, in split order.
   const size_t split_stride = static_cast<size_t>(p.T) * p.Ntot;
@@ -155,15 +135,17 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   __nv_bfloat16* cq = p.cq_out + static_cast<size_t>(t) * p.Hcq;
   if (p.smooth == nullptr) {
     for (int f = threadIdx.x * 8; f < p.Hcq; f += NT * 8) {
-      float v[8];
+      float g[8], v[8];
+      load8_bf16(p.gamma_cq + f, g);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = h[f + i] * rq * g_cq[f + i];
+      for (int i = 0; i < 8; ++i) v[i] = h[f + i] * rq * g[i];
       store8_bf16(cq + f, v);
     }
   } else {
     float amax = 0.f;
     for (int f = threadIdx.x; f < p.Hcq; f += NT) {
-      const float c = __bfloat162float(__float2bfloat16_rn(h[f] * rq * g_cq[f]));
+      const float c = __bfloat162float(
+          __float2bfloat16_rn(h[f] * rq * __bfloat162float(p.gamma_cq[f])));
       const float s = __fmul_rn(c, p.smooth[f]);
       h[f] = s;                                   // own element only: no race
       amax = fmaxf(amax, fabsf(s));
@@ -177,16 +159,18 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     if (threadIdx.x == 0) p.scale_t[t] = scale;
   }
 
-  if (!cache) return;                       // empty caches: outputs only
+  if (p.slots <= 0) return;                 // empty caches: outputs only
+  const int64_t idx = p.cache_index[t];
   if (idx < 0 || idx >= p.slots) {
     if (idx != -1 && threadIdx.x == 0) atomicOr(p.err, kErrIndexRange);
     return;
   }
   // ---- c^KV (Hckv % 8 == 0)
   for (int f = threadIdx.x * 8; f < p.Hckv; f += NT * 8) {
-    float v[8];
+    float g[8], v[8];
+    load8_bf16(p.gamma_ckv + f, g);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = hkv[f + i] * rkv * g_ckv[f + i];
+    for (int i = 0; i < 8; ++i) v[i] = hkv[f + i] * rkv * g[i];
     if (p.kv_int8) {
       uint2 q;
       int8_t* qb = reinterpret_cast<int8_t*>(&q);
@@ -203,10 +187,8 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   for (int j = threadIdx.x; j < p.Dr; j += NT) {
     const float y = hkr[j];
     const float partner = j < half ? -hkr[j + half] : hkr[j - half];
-    const float c = j == static_cast<int>(threadIdx.x)
-                        ? kr_cos : __bfloat162float(p.cos[static_cast<size_t>(t) * p.Dr + j]);
-    const float s = j == static_cast<int>(threadIdx.x)
-                        ? kr_sin : __bfloat162float(p.sin[static_cast<size_t>(t) * p.Dr + j]);
+    const float c = __bfloat162float(p.cos[static_cast<size_t>(t) * p.Dr + j]);
+    const float s = __bfloat162float(p.sin[static_cast<size_t>(t) * p.Dr + j]);
     const float v = y * c + partner * s;
     if (p.kr_int8)
       static_cast<int8_t*>(p.kr_cache)[idx * p.Dr + j] = quant_i8(v, p.qs_ckr[j], -128, 127);
@@ -253,11 +235,9 @@ __global__ void prepack_kernel(const PrepackParams p) {
 }  // namespace
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {
-  const size_t smem = static_cast<size_t>(p.Ntot + p.Hcq + p.Hckv) * sizeof(float);
+  const size_t smem = static_cast<size_t>(p.Ntot) * sizeof(float);
   const bool split = p.splits > 1;
-  constexpr int kSplitThreads = 576;   // 18 warps: one float4 column of the 2112-wide sums each
-  auto kern = split ? norm_rope_scatter_kernel<kMaxSplits, kSplitThreads>
-                    : norm_rope_scatter_kernel<1, 256>;
+  auto kern = split ? norm_rope_scatter_kernel<kMaxSplits, 512> : norm_rope_scatter_kernel<1, 256>;
   if (p.splits > kMaxSplits) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     cudaError_t e =
@@ -266,7 +246,7 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool p
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.T));
-  cfg.blockDim = dim3(split ? kSplitThreads : 256);
+  cfg.blockDim = dim3(split ? 512 : 256);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
