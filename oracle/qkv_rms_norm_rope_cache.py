@@ -5,15 +5,22 @@ Plain float64 restatement of aclnnQkvRmsNormRopeCache, "Formulas":
   (1) SplitVD: q = qkv[..., :Nq*D], k = qkv[..., Nq*D:(Nq+Nk)*D], v = qkv[..., (Nq+Nk)*D:]
   (2) RmsNorm per head along D: y = x / sqrt(mean(x^2) + eps) * gamma      (q and k)
   (3) RoPE (half-and-half) on the RmsNorm output, d = D                    (q and k)
-  (4) Quant: none (kQuant = kRoPE, vQuant = v) or symmetric (kRoPE / kScale, v / vScale)
+  (4) Quant: none (kQuant = kRoPE, vQuant = v), symmetric (kRoPE / kScale, v / vScale) or
+      asymmetric (kRoPE / kScale + kOffset, v / vScale + vOffset)
 
-and "Other restrictions": index in [-1, BlockNum*BlockSize), -1 skips the update.
+and "Other restrictions": index in [-1, BlockNum*BlockSize), -1 skips the update.  The API
+function's optional outputs qBeforeQuant, kBeforeQuant, vBeforeQuant are the three tensors that
+enter "Quant": q and k after RmsNorm and RoPE, v as split.
 
 Readings (the parameter table is lost from the page): gamma_q and gamma_k have shape (D,) and
 are shared by all heads of their kind; sin and cos have shape (B*S, D) and are shared by all
 heads; k_scale (Nk, D) and v_scale (Nv, D) are per channel; the cache layout is
 (BlockNum, BlockSize, N, D) with slot i at block i // BlockSize, row i % BlockSize; qOut is
 rounded to the dtype of qkv (fp16 or bf16); int8 codes round half to even, clamp to [-128, 127], decided in float32.
+Asymmetric quant: k_offset (Nk, D) and v_offset (Nv, D) are per-channel float32 offsets added to
+the float32 quotient before rounding.  The before-quant outputs are dense (T, N, D) tensors in
+the dtype of qkv, one row per token whatever its index (they are not cache writes); qBeforeQuant
+equals qOut because the formulas never quantise q.
 """
 from __future__ import annotations
 
@@ -23,19 +30,22 @@ from .mla_prolog import rms_norm, rope_half_and_half
 from .rounding import round_bf16, round_fp16, saturate_int8_rne
 
 
-def _quant(v: np.ndarray, scale: np.ndarray) -> np.ndarray:
+def _quant(v: np.ndarray, scale: np.ndarray, offset=None) -> np.ndarray:
     q = (np.asarray(v, np.float64).astype(np.float32)
          / np.asarray(scale, np.float32)).astype(np.float32)
+    if offset is not None:                               # asymmetric: + offset, in float32
+        q = (q + np.asarray(offset, np.float32)).astype(np.float32)
     return saturate_int8_rne(q)
 
 
 def qkv_rms_norm_rope_cache(qkv, gamma_q, gamma_k, cos, sin, index, k_cache, v_cache,
                             epsilon, Nq, Nk, Nv, k_scale=None, v_scale=None,
-                            out_dtype: str = "fp16") -> dict:
+                            out_dtype: str = "fp16", k_offset=None, v_offset=None) -> dict:
     """qkv: (..., (Nq+Nk+Nv)*D) values; caches (BlockNum, BlockSize, Nk|Nv, D).
 
     Returns q_out (T, Nq, D) as float64 values of ``out_dtype`` ("fp16" or "bf16", the dtype of
-    qkv) and the updated caches (int8 when quantised, else float64 values of ``out_dtype``).
+    qkv), the updated caches (int8 when quantised, else float64 values of ``out_dtype``), and the
+    before-quant tensors q_before (T, Nq, D), k_before (T, Nk, D), v_before (T, Nv, D).
     """
     rnd = round_fp16 if out_dtype == "fp16" else round_bf16
     qkv = np.asarray(qkv, np.float64)
@@ -50,8 +60,10 @@ def qkv_rms_norm_rope_cache(qkv, gamma_q, gamma_k, cos, sin, index, k_cache, v_c
 
     quantised = np.asarray(k_cache).dtype == np.int8
     if quantised:
-        k_rows = _quant(k_emb, np.asarray(k_scale).reshape(1, Nk, D))
-        v_rows = _quant(v, np.asarray(v_scale).reshape(1, Nv, D))
+        ko = None if k_offset is None else np.asarray(k_offset).reshape(1, Nk, D)
+        vo = None if v_offset is None else np.asarray(v_offset).reshape(1, Nv, D)
+        k_rows = _quant(k_emb, np.asarray(k_scale).reshape(1, Nk, D), ko)
+        v_rows = _quant(v, np.asarray(v_scale).reshape(1, Nv, D), vo)
     else:
         k_rows = rnd(k_emb)
         v_rows = rnd(v)
@@ -65,4 +77,5 @@ def qkv_rms_norm_rope_cache(qkv, gamma_q, gamma_k, cos, sin, index, k_cache, v_c
         k_out[i // block_size, i % block_size] = k_rows[t]
         v_out[i // block_size, i % block_size] = v_rows[t]
     return {"q_out": rnd(q_emb), "k_cache": k_out, "v_cache": v_out,
-            "k_rows": k_rows, "v_rows": v_rows}
+            "k_rows": k_rows, "v_rows": v_rows,
+            "q_before": rnd(q_emb), "k_before": rnd(k_emb), "v_before": rnd(v)}

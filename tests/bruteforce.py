@@ -113,11 +113,13 @@ def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_c
 
 
 def qkv_bruteforce(qkv, gq, gk, cos, sin, idx, k_cache, v_cache, eps, Nq, Nk, Nv, ks=None,
-                   vs=None):
+                   vs=None, ko=None, vo=None):
     """qkv: T rows of (Nq+Nk+Nv)*D floats."""
     T = len(qkv)
     D = len(qkv[0]) // (Nq + Nk + Nv)
     q_out = [[[0.0] * D for _ in range(Nq)] for _ in range(T)]
+    k_before = [[[0.0] * D for _ in range(Nk)] for _ in range(T)]
+    v_before = [[[0.0] * D for _ in range(Nv)] for _ in range(T)]
     kc = [[[list(r) for r in row] for row in blk] for blk in k_cache]
     vc = [[[list(r) for r in row] for row in blk] for blk in v_cache]
     bs = len(k_cache[0])
@@ -134,15 +136,19 @@ def qkv_bruteforce(qkv, gq, gk, cos, sin, idx, k_cache, v_cache, eps, Nq, Nk, Nv
                 q_out[t][h] = [fp16(v) for v in e]
             else:
                 hk = h - Nq
+                k_before[t][hk] = [fp16(v) for v in e]
                 if ks is not None:
-                    k_rows.append([int8_code(f32(f32(e[j]) / ks[hk][j]), -128, 127)
+                    off = [0.0] * D if ko is None else ko[hk]
+                    k_rows.append([int8_code(f32(f32(f32(e[j]) / ks[hk][j]) + off[j]), -128, 127)
                                    for j in range(D)])
                 else:
                     k_rows.append([fp16(v) for v in e])
         for hv in range(Nv):
             vh = heads[Nq + Nk + hv]
+            v_before[t][hv] = [fp16(v) for v in vh]
             if vs is not None:
-                v_rows.append([int8_code(f32(f32(vh[j]) / vs[hv][j]), -128, 127)
+                off = [0.0] * D if vo is None else vo[hv]
+                v_rows.append([int8_code(f32(f32(f32(vh[j]) / vs[hv][j]) + off[j]), -128, 127)
                                for j in range(D)])
             else:
                 v_rows.append([fp16(v) for v in vh])
@@ -150,4 +156,5 @@ def qkv_bruteforce(qkv, gq, gk, cos, sin, idx, k_cache, v_cache, eps, Nq, Nk, Nv
         if 0 <= i < len(k_cache) * bs:
             kc[i // bs][i % bs] = k_rows
             vc[i // bs][i % bs] = v_rows
-    return {"q_out": q_out, "k_cache": kc, "v_cache": vc}
+    return {"q_out": q_out, "k_cache": kc, "v_cache": vc, "q_before": q_out,
+            "k_before": k_before, "v_before": v_before}

@@ -13,7 +13,7 @@ import pytest
 
 import oracle
 from tests import bruteforce as bf
-from tests.test_oracle_pins import _brute, _tiny_mla, _tiny_qkv
+from tests.test_oracle_pins import _brute, _qkv_brute, _tiny_mla, _tiny_qkv
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -68,8 +68,17 @@ def test_mla_pins_catch_mutation(label, old, new):
 QKV_MUTATIONS = [
     ("split k/v swapped", "k, v = x[:, :Nq, :], x[:, Nq:Nq + Nk, :], x[:, Nq + Nk:, :]",
      "k, v = x[:, :Nq, :], x[:, Nq + Nk:, :], x[:, Nq:Nq + Nk, :]"),
-    ("v normalised too", "v_rows = _quant(v, np.asarray(v_scale).reshape(1, Nv, D))",
-     "v_rows = _quant(rms_norm(v, 1.0, epsilon), np.asarray(v_scale).reshape(1, Nv, D))"),
+    ("v normalised too", "v_rows = _quant(v, np.asarray(v_scale).reshape(1, Nv, D), vo)",
+     "v_rows = _quant(rms_norm(v, 1.0, epsilon), np.asarray(v_scale).reshape(1, Nv, D), vo)"),
+    ("offset subtracted", "q = (q + np.asarray(offset, np.float32))",
+     "q = (q - np.asarray(offset, np.float32))"),
+    ("v offset ignored", "vo = None if v_offset is None else np.asarray(v_offset).reshape(1, Nv, D)",
+     "vo = None"),
+    ("offset added after rounding", "return saturate_int8_rne(q)",
+     "return saturate_int8_rne(q - (0 if offset is None else np.asarray(offset, np.float32))) + "
+     "(0 if offset is None else np.rint(np.asarray(offset, np.float32)))"),
+    ("v_before normalised", '"v_before": rnd(v)', '"v_before": rnd(rms_norm(v, 1.0, epsilon))'),
+    ("k_before before RoPE", '"k_before": rnd(k_emb)', '"k_before": rnd(rms_norm(k, gamma_k, epsilon))'),
     ("k gamma from q", "k_emb = rope_half_and_half(rms_norm(k, gamma_k, epsilon), cos, sin)",
      "k_emb = rope_half_and_half(rms_norm(k, gamma_q, epsilon), cos, sin)"),
 ]
@@ -79,18 +88,14 @@ QKV_MUTATIONS = [
 def test_qkv_pins_catch_mutation(label, old, new):
     mod = _mutant("qkv_rms_norm_rope_cache.py", old, new)
     rng = np.random.default_rng(32)
-    inp = _tiny_qkv(rng, quant=True)
+    inp = _tiny_qkv(rng, quant="asym")
     got = mod.qkv_rms_norm_rope_cache(**inp)
     ref = oracle.qkv_rms_norm_rope_cache(**inp)
-    L = lambda a: np.asarray(a).tolist()
-    want = bf.qkv_bruteforce(L(inp["qkv"]), L(inp["gamma_q"]), L(inp["gamma_k"]), L(inp["cos"]),
-                             L(inp["sin"]), L(inp["index"]),
-                             np.asarray(inp["k_cache"]).astype(int).tolist(),
-                             np.asarray(inp["v_cache"]).astype(int).tolist(), inp["epsilon"],
-                             inp["Nq"], inp["Nk"], inp["Nv"], ks=L(inp["k_scale"]),
-                             vs=L(inp["v_scale"]))
+    want = _qkv_brute(inp)
     assert np.array_equal(ref["k_cache"], np.array(want["k_cache"], np.int8))
     detected = (not np.allclose(got["q_out"], np.array(want["q_out"]))
                 or not np.array_equal(got["k_cache"], np.array(want["k_cache"], np.int8))
-                or not np.array_equal(got["v_cache"], np.array(want["v_cache"], np.int8)))
+                or not np.array_equal(got["v_cache"], np.array(want["v_cache"], np.int8))
+                or any(not np.allclose(got[k], np.array(want[k]), rtol=1e-12, atol=1e-14)
+                       for k in ("q_before", "k_before", "v_before")))
     assert detected, f"mutation '{label}' not detected"

@@ -334,6 +334,9 @@ def _tiny_qkv(rng, quant, T=4, Nq=3, Nk=2, Nv=2, D=8, block_num=3, block_size=2)
     if quant:
         inp["k_scale"] = rng.uniform(0.02, 0.1, (Nk, D)).astype(np.float32)
         inp["v_scale"] = rng.uniform(0.02, 0.1, (Nv, D)).astype(np.float32)
+        if quant == "asym":
+            inp["k_offset"] = rng.uniform(-8, 8, (Nk, D)).astype(np.float32)
+            inp["v_offset"] = rng.uniform(-8, 8, (Nv, D)).astype(np.float32)
         inp["k_cache"] = rng.integers(-128, 128, (block_num, block_size, Nk, D)).astype(np.int8)
         inp["v_cache"] = rng.integers(-128, 128, (block_num, block_size, Nv, D)).astype(np.int8)
     else:
@@ -342,19 +345,26 @@ def _tiny_qkv(rng, quant, T=4, Nq=3, Nk=2, Nv=2, D=8, block_num=3, block_size=2)
     return inp
 
 
-@pytest.mark.parametrize("quant", [False, True])
-def test_qkv_matches_brute_force(quant):
-    rng = np.random.default_rng(20 + quant)
-    inp = _tiny_qkv(rng, quant)
-    got = oracle.qkv_rms_norm_rope_cache(**inp)
+def _qkv_brute(inp):
     L = lambda a: np.asarray(a).tolist()
     cache = lambda a: np.asarray(a).astype(int).tolist() if np.asarray(a).dtype == np.int8 else L(a)
-    want = bf.qkv_bruteforce(L(inp["qkv"]), L(inp["gamma_q"]), L(inp["gamma_k"]), L(inp["cos"]),
+    opt = lambda k: L(inp[k]) if inp.get(k) is not None else None
+    return bf.qkv_bruteforce(L(inp["qkv"]), L(inp["gamma_q"]), L(inp["gamma_k"]), L(inp["cos"]),
                              L(inp["sin"]), L(inp["index"]), cache(inp["k_cache"]),
                              cache(inp["v_cache"]), inp["epsilon"], inp["Nq"], inp["Nk"],
-                             inp["Nv"], ks=L(inp["k_scale"]) if quant else None,
-                             vs=L(inp["v_scale"]) if quant else None)
+                             inp["Nv"], ks=opt("k_scale"), vs=opt("v_scale"), ko=opt("k_offset"),
+                             vo=opt("v_offset"))
+
+
+@pytest.mark.parametrize("quant", [False, True, "asym"])
+def test_qkv_matches_brute_force(quant):
+    rng = np.random.default_rng(20 + (2 if quant == "asym" else int(quant)))
+    inp = _tiny_qkv(rng, quant)
+    got = oracle.qkv_rms_norm_rope_cache(**inp)
+    want = _qkv_brute(inp)
     np.testing.assert_allclose(got["q_out"], np.array(want["q_out"]), rtol=1e-12, atol=1e-14)
+    for key in ("q_before", "k_before", "v_before"):
+        np.testing.assert_allclose(got[key], np.array(want[key]), rtol=1e-12, atol=1e-14)
     for key in ("k_cache", "v_cache"):
         if quant:
             np.testing.assert_array_equal(got[key], np.array(want[key], np.int8))
@@ -382,3 +392,58 @@ def test_qkv_split_positions():
     np.testing.assert_array_equal(out["v_cache"][1, 1], np.array(vals[Nq + Nk:])[:, None] * np.ones(D))
     # the -1 / untouched slots keep their bytes
     assert out["k_cache"][0].tobytes() == inp["k_cache"][0].tobytes()
+
+
+def test_qkv_asym_zero_offset_is_symmetric():
+    # kRoPE / kScale + 0 is the symmetric rule
+    rng = np.random.default_rng(23)
+    inp = _tiny_qkv(rng, "asym")
+    inp["k_offset"] = np.zeros_like(inp["k_offset"])
+    inp["v_offset"] = np.zeros_like(inp["v_offset"])
+    asym = oracle.qkv_rms_norm_rope_cache(**inp)
+    sym = oracle.qkv_rms_norm_rope_cache(**{k: v for k, v in inp.items() if "offset" not in k})
+    for key in ("k_cache", "v_cache", "k_rows", "v_rows"):
+        np.testing.assert_array_equal(asym[key], sym[key])
+
+
+def test_qkv_asym_integer_offset_shifts_codes():
+    # With an integer offset o and no saturation, rne(x / s + o) = rne(x / s) + o: every code
+    # moves by exactly o (checked away from the clamp by keeping |x / s| small).
+    rng = np.random.default_rng(24)
+    inp = _tiny_qkv(rng, "asym")
+    Nk, Nv, D = inp["Nk"], inp["Nv"], 8
+    inp["k_scale"] = np.full((Nk, D), 0.25, np.float32)
+    inp["v_scale"] = np.full((Nv, D), 0.25, np.float32)
+    inp["k_offset"] = rng.integers(-20, 21, (Nk, D)).astype(np.float32)
+    inp["v_offset"] = rng.integers(-20, 21, (Nv, D)).astype(np.float32)
+    asym = oracle.qkv_rms_norm_rope_cache(**inp)
+    sym = oracle.qkv_rms_norm_rope_cache(**{k: v for k, v in inp.items() if "offset" not in k})
+    assert np.abs(sym["k_rows"]).max() < 100 and np.abs(sym["v_rows"]).max() < 100
+    np.testing.assert_array_equal(asym["k_rows"].astype(int),
+                                  sym["k_rows"].astype(int) + inp["k_offset"].astype(int)[None])
+    np.testing.assert_array_equal(asym["v_rows"].astype(int),
+                                  sym["v_rows"].astype(int) + inp["v_offset"].astype(int)[None])
+
+
+def test_qkv_asym_offset_saturates():
+    rng = np.random.default_rng(25)
+    inp = _tiny_qkv(rng, "asym")
+    inp["k_offset"] = np.full_like(inp["k_offset"], 400.0)
+    inp["v_offset"] = np.full_like(inp["v_offset"], -400.0)
+    out = oracle.qkv_rms_norm_rope_cache(**inp)
+    assert (out["k_rows"] == 127).all() and (out["v_rows"] == -128).all()
+
+
+def test_qkv_before_quant_outputs():
+    # vBeforeQuant is the split v slice itself; qBeforeQuant is qOut; kBeforeQuant is the k row
+    # that the quantiser consumes, so requantising it reproduces the cache codes away from ties.
+    rng = np.random.default_rng(26)
+    inp = _tiny_qkv(rng, True)
+    out = oracle.qkv_rms_norm_rope_cache(**inp)
+    T, Nq, Nk, Nv, D = 4, inp["Nq"], inp["Nk"], inp["Nv"], 8
+    x = np.asarray(inp["qkv"]).reshape(T, Nq + Nk + Nv, D)
+    np.testing.assert_array_equal(out["v_before"], x[:, Nq + Nk:, :])
+    np.testing.assert_array_equal(out["q_before"], out["q_out"])
+    requant = np.clip(np.rint(out["k_before"] / np.asarray(inp["k_scale"], np.float64)[None]),
+                      -128, 127)
+    assert np.abs(requant - out["k_rows"]).max() <= 1
