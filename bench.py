@@ -43,7 +43,7 @@ def _parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "tiny", "partial_quant", "qkv"])
+                    choices=["decode", "prefill", "tiny", "partial_quant", "qkv", "qkv_asym"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--timer-calls", type=int, default=200,
@@ -55,7 +55,7 @@ def _case(name):
     import synthetic
     return {"decode": synthetic.MLA_DECODE, "prefill": synthetic.MLA_PREFILL,
             "tiny": synthetic.MLA_TINY, "partial_quant": synthetic.MLA_PARTIAL_QUANT,
-            "qkv": synthetic.QKV_EPILOGUE}[name]
+            "qkv": synthetic.QKV_EPILOGUE, "qkv_asym": synthetic.QKV_EPILOGUE_ASYM}[name]
 
 
 # ------------------------------------------------------------------------------- byte/flop model
@@ -207,7 +207,10 @@ def oracle_tokens_per_s(case, budget_s=12.0, sample_tokens=4):
                 f(cpu["sin"])[:ntok], cpu["index"].numpy()[:ntok], cpu["k_cache"].numpy(),
                 cpu["v_cache"].numpy(), case.eps, d.Nq, d.Nk, d.Nv, cpu["k_scale"].numpy(),
                 cpu["v_scale"].numpy())
-        call = lambda: oracle.qkv_rms_norm_rope_cache(*args)
+        kw = {}
+        if case.quant == "asymmetric":
+            kw = {"k_offset": cpu["k_offset"].numpy(), "v_offset": cpu["v_offset"].numpy()}
+        call = lambda: oracle.qkv_rms_norm_rope_cache(*args, **kw)
         sample = f"{ntok} tokens of the {case.name} workload per oracle call"
     else:
         import torch
@@ -269,7 +272,7 @@ def run_ours(args, rank, local, world):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     case = _case(args.workload)
-    is_qkv = args.workload == "qkv"
+    is_qkv = args.workload.startswith("qkv")
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
 
     if is_qkv:
@@ -428,11 +431,16 @@ def run_qkv(args, case, dev, rank, world, hbm, peak_kind):
     t["cos"] = t["cos"].reshape(d.B, d.S, d.D)
     t["sin"] = t["sin"].reshape(d.B, d.S, d.D)
     t["index"] = t["index"].reshape(d.B, d.S)
+    if case.before_quant:
+        for name, n in (("q_before_quant", d.Nq), ("k_before_quant", d.Nk), ("v_before_quant", d.Nv)):
+            t[name] = torch.empty(d.B, d.S, n, d.D, dtype=torch.float16, device=dev)
     a = pkg.make_qkv_args(t, d.Nq, d.Nk, d.Nv, case.eps)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
     nb = (d.T * (d.Nq + d.Nk + d.Nv) * d.D * 2 + d.T * d.Nq * d.D * 2
           + d.T * (d.Nk + d.Nv) * d.D + 2 * d.T * d.D * 2 + d.T * 8)
+    if case.before_quant:        # the three dense before-quant outputs
+        nb += d.T * (d.Nq + d.Nk + d.Nv) * d.D * 2
     steps = args.steps or 2000
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -463,10 +471,12 @@ def run_qkv(args, case, dev, rank, world, hbm, peak_kind):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
             "data": "synthetic", "config": {"workload": case.name, "B": d.B, "S": d.S,
                                             "Nq": d.Nq, "Nk": d.Nk, "Nv": d.Nv, "D": d.D,
+                                            "quant": case.quant,
+                                            "before_quant_outputs": case.before_quant,
                                             "l2": f"inputs {nb/1e6:.0f} MB > 129 MB L2"},
             "roofline": {"bound": "hbm", "kernel": "qkv_rnrc", "achieved": round(achieved, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                         "peak_kind": peak_kind, "traffic": _ncu_traffic("qkv_rnrc", "qkv")},
+                         "peak_kind": peak_kind, "traffic": _ncu_traffic("qkv_rnrc", args.workload)},
             "clocks": clk.summary(), "gpu_launches": steps}
 
 

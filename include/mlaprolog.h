@@ -165,9 +165,15 @@ mlap_status_t mlap_check_errors(void* workspace, void* stream);
  * only 128 is supported"), Nk == Nv.  Per token:
  *   q, k, v = SplitVD(qkv);  q, k <- RoPE_half_and_half(RmsNorm(., gamma, epsilon), cos, sin);
  *   q_out = q;  k_cache[index] = Quant(k);  v_cache[index] = Quant(v)
- * Quant: none when k_scale/v_scale are absent (caches have qkv's dtype), symmetric
- * (value / scale, round half to even, saturate to [-128,127]) when present (caches int8).
- * Scales must be nonzero (caller contract, "Other restrictions"). */
+ * Quant ("Formulas" (4)): none when k_scale/v_scale are absent (caches have qkv's dtype);
+ * symmetric (value / scale) when the scales are present; asymmetric (value / scale + offset)
+ * when k_offset/v_offset are present too; the int8 code rounds half to even and saturates to
+ * [-128,127].  It is computed as value * fp32(1/scale) (+ offset) in fp32, so a code can differ
+ * from the exact quotient's by one near a rounding tie.  Scales must be nonzero (caller
+ * contract, "Other restrictions").
+ * Optional outputs (the API function's qBeforeQuant / kBeforeQuant / vBeforeQuant): the tensors
+ * that enter Quant, dense in token order (one row per token, including index -1), in qkv's dtype:
+ * q after RoPE (equal to q_out), k after RoPE, v as split. */
 typedef struct {
   mlap_tensor_t qkv;       /* fp16|bf16 */
   mlap_tensor_t gamma_q;   /* (D), dtype of qkv, shared by all q heads */
@@ -179,9 +185,12 @@ typedef struct {
   mlap_tensor_t v_cache;   /* in/out (BlockNum, BlockSize, Nv, D), same dtype as k_cache */
   mlap_tensor_t k_scale;   /* fp32 (Nk, D) or absent */
   mlap_tensor_t v_scale;   /* fp32 (Nv, D) or absent */
-  mlap_tensor_t k_offset;  /* asymmetric quant offsets: not implemented, must be absent */
-  mlap_tensor_t v_offset;  /* must be absent */
+  mlap_tensor_t k_offset;  /* fp32 (Nk, D) or absent: asymmetric quant (needs the scales) */
+  mlap_tensor_t v_offset;  /* fp32 (Nv, D), present exactly when k_offset is */
   mlap_tensor_t q_out;     /* out (T, Nq, D) or (B, S, Nq, D), dtype of qkv */
+  mlap_tensor_t q_before_quant;  /* optional out, same layout and dtype as q_out */
+  mlap_tensor_t k_before_quant;  /* optional out (T, Nk, D) or (B, S, Nk, D), dtype of qkv */
+  mlap_tensor_t v_before_quant;  /* optional out (T, Nv, D) or (B, S, Nv, D), dtype of qkv */
   int32_t Nq, Nk, Nv;
   double epsilon;
   const char* cache_mode;  /* NULL or "PA_BSND"; "PA_NZ" is unsupported */

@@ -62,7 +62,8 @@ class mlap_args_t(ctypes.Structure):
 
 
 _QKV_TENSORS = ["qkv", "gamma_q", "gamma_k", "cos", "sin", "index", "k_cache", "v_cache",
-                "k_scale", "v_scale", "k_offset", "v_offset", "q_out"]
+                "k_scale", "v_scale", "k_offset", "v_offset", "q_out", "q_before_quant",
+                "k_before_quant", "v_before_quant"]
 
 
 class qkvrnrc_args_t(ctypes.Structure):

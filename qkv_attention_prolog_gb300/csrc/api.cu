@@ -719,7 +719,7 @@ struct QkvDims {
   int64_t T, B, S;
   bool bsh;
   int64_t D, BlockNum, BlockSize;
-  bool quant, bf16;
+  bool quant, asym, bf16;
 };
 
 mlap_status_t validate_qkv(const qkvrnrc_args_t* a, QkvDims* d) {
@@ -772,9 +772,29 @@ mlap_status_t validate_qkv(const qkvrnrc_args_t* a, QkvDims* d) {
   CHECK_STATUS(want_shape(kc, "k_cache", {d->BlockNum, d->BlockSize, Nk, d->D}));
   CHECK_STATUS(want_shape(vc, "v_cache", {d->BlockNum, d->BlockSize, Nv, d->D}));
   if (kc.dtype != vc.dtype) return fail(MLAP_ERR_DTYPE, "k_cache and v_cache dtypes differ");
-  if (present(a->k_offset) || present(a->v_offset))
-    return fail(MLAP_ERR_UNSUPPORTED, "asymmetric quant (k_offset / v_offset) not implemented");
   d->quant = present(a->k_scale) || present(a->v_scale);
+  d->asym = present(a->k_offset) || present(a->v_offset);
+  if (d->asym) {
+    if (!d->quant) return fail(MLAP_ERR_UNSUPPORTED, "k_offset / v_offset need k_scale / v_scale");
+    CHECK_STATUS(need(a->k_offset, "k_offset", false));
+    CHECK_STATUS(need(a->v_offset, "v_offset", false));
+    CHECK_STATUS(want_dtype(a->k_offset, "k_offset", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_dtype(a->v_offset, "v_offset", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_shape(a->k_offset, "k_offset", {Nk, d->D}));
+    CHECK_STATUS(want_shape(a->v_offset, "v_offset", {Nv, d->D}));
+  }
+  {   // optional before-quant outputs
+    const mlap_tensor_t* outs[3] = {&a->q_before_quant, &a->k_before_quant, &a->v_before_quant};
+    const char* names[3] = {"q_before_quant", "k_before_quant", "v_before_quant"};
+    const int64_t heads[3] = {Nq, Nk, Nv};
+    for (int i = 0; i < 3; ++i) {
+      if (!present(*outs[i])) continue;
+      CHECK_STATUS(need(*outs[i], names[i], true));
+      CHECK_STATUS(want_dtype(*outs[i], names[i], x.dtype));
+      if (d->bsh) CHECK_STATUS(want_shape(*outs[i], names[i], {d->B, d->S, heads[i], d->D}));
+      else CHECK_STATUS(want_shape(*outs[i], names[i], {d->T, heads[i], d->D}));
+    }
+  }
   if (d->quant) {
     CHECK_STATUS(want_dtype(kc, "k_cache", MLAP_DTYPE_INT8));
     CHECK_STATUS(need(a->k_scale, "k_scale", false));
@@ -941,6 +961,11 @@ mlap_status_t qkvrnrc_execute(const qkvrnrc_args_t* a, void* ws, size_t ws_bytes
   p.v_cache = a->v_cache.data;
   p.k_scale = d.quant ? static_cast<const float*>(a->k_scale.data) : nullptr;
   p.v_scale = d.quant ? static_cast<const float*>(a->v_scale.data) : nullptr;
+  p.k_offset = d.asym ? static_cast<const float*>(a->k_offset.data) : nullptr;
+  p.v_offset = d.asym ? static_cast<const float*>(a->v_offset.data) : nullptr;
+  p.q_before = present(a->q_before_quant) ? a->q_before_quant.data : nullptr;
+  p.k_before = present(a->k_before_quant) ? a->k_before_quant.data : nullptr;
+  p.v_before = present(a->v_before_quant) ? a->v_before_quant.data : nullptr;
   p.q_out = a->q_out.data;
   p.T = static_cast<int32_t>(d.T);
   p.Nq = a->Nq;

@@ -82,6 +82,11 @@ struct QkvParams {
   void* v_cache;
   const float* k_scale;        // null: no quant
   const float* v_scale;
+  const float* k_offset;       // null: symmetric quant
+  const float* v_offset;
+  void* q_before;              // optional dense before-quant outputs (null: not written)
+  void* k_before;
+  void* v_before;
   void* q_out;
   int32_t T, Nq, Nk, Nv;
   float eps;

@@ -4,9 +4,12 @@
 //   y       = x / sqrt(mean(x^2) + eps) * gamma                      per q / k head, along D
 //   y_embed = y * cos + cat(-y2, y1) * sin                           half-and-half, d = D
 //   q_out   = y_embed(q);  k_cache[i] = Quant(y_embed(k));  v_cache[i] = Quant(v)
-//   Quant   = identity, or value / scale rounded half to even and saturated to int8 (computed
-//             as value * fp32(1/scale); the code can differ from the exact quotient's by one
-//             near a rounding tie)
+//   Quant   = identity, value / scale (symmetric) or value / scale + offset (asymmetric),
+//             rounded half to even and saturated to int8 (computed as value * fp32(1/scale)
+//             (+ offset) in fp32; the code can differ from the exact quotient's by one near a
+//             rounding tie)
+//   optional qBeforeQuant / kBeforeQuant / vBeforeQuant: the tensors entering Quant, dense per
+//             token (the API function's optional outputs)
 //
 // A pure HBM stream: every token's qkv row is read once and its outputs written once.
 #include "internal.h"
@@ -50,17 +53,25 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
   return raw;
 }
 
-// int8 codes of x * (1/scale) (reciprocal of the per-channel scale in fp32), round half to
-// even, saturated to [-128, 127].
-__device__ __forceinline__ uint2 quant8_mul(const float (&x)[8], const float* inv) {
+// int8 codes of x * (1/scale) (+ offset) (reciprocal of the per-channel scale in fp32), round
+// half to even, saturated to [-128, 127].
+template <bool ASYM>
+__device__ __forceinline__ uint2 quant8_mul(const float (&x)[8], const float* inv, const float* off) {
   const float4 i0 = reinterpret_cast<const float4*>(inv)[0];
   const float4 i1 = reinterpret_cast<const float4*>(inv)[1];
   const float iv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+  float ov[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if constexpr (ASYM) {
+    const float4 o0 = reinterpret_cast<const float4*>(off)[0];
+    const float4 o1 = reinterpret_cast<const float4*>(off)[1];
+    ov[0] = o0.x; ov[1] = o0.y; ov[2] = o0.z; ov[3] = o0.w;
+    ov[4] = o1.x; ov[5] = o1.y; ov[6] = o1.z; ov[7] = o1.w;
+  }
   uint2 out;
   int8_t* o = reinterpret_cast<int8_t*>(&out);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    int q = __float2int_rn(x[i] * iv[i]);
+    int q = ASYM ? __float2int_rn(__fadd_rn(x[i] * iv[i], ov[i])) : __float2int_rn(x[i] * iv[i]);
     q = q < -128 ? -128 : (q > 127 ? 127 : q);
     o[i] = static_cast<int8_t>(q);
   }
@@ -74,11 +85,14 @@ __device__ __forceinline__ uint2 quant8_mul(const float (&x)[8], const float* in
 // members of its RoPE pairs, so the rotation needs no exchange and the RmsNorm sum is a 3-step
 // shuffle.  The CTA has 8 * ceil(N/2) threads (N = Nq+Nk+Nv heads): every 8-lane slot processes
 // two rows of each token.  Quantisation multiplies by the reciprocal of the per-channel scale
-// (fp32); the reciprocals of all k and v heads sit in shared memory behind the ring.
+// (fp32); the reciprocals (and asymmetric offsets) of all k and v heads sit in shared memory
+// behind the ring.  QM: 0 no quant, 1 symmetric, 2 asymmetric.
 constexpr int kRing = 4;
 
-template <bool BF16, bool QUANT>
+template <bool BF16, int QM>
 __global__ void __launch_bounds__(512) qkv_rnrc_kernel(const QkvParams p) {
+  constexpr bool QUANT = QM != 0;
+  constexpr bool ASYM = QM == 2;
   using E = Elem<BF16>;
   using T = typename E::T;
   extern __shared__ __align__(128) uint8_t qsm[];
@@ -127,9 +141,12 @@ __global__ void __launch_bounds__(512) qkv_rnrc_kernel(const QkvParams p) {
   unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_k)[l8], ga_k);
   unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_k)[8 + l8], gb_k);
   float* inv = reinterpret_cast<float*>(qsm + static_cast<size_t>(kRing) * buf_bytes);
+  float* offs = inv + (p.Nk + p.Nv) * kD;            // asymmetric offsets, same layout
   if (QUANT) {
-    for (int i = threadIdx.x; i < (p.Nk + p.Nv) * kD; i += blockDim.x)
+    for (int i = threadIdx.x; i < (p.Nk + p.Nv) * kD; i += blockDim.x) {
       inv[i] = __frcp_rn(i < p.Nk * kD ? p.k_scale[i] : p.v_scale[i - p.Nk * kD]);
+      if (ASYM) offs[i] = i < p.Nk * kD ? p.k_offset[i] : p.v_offset[i - p.Nk * kD];
+    }
     __syncthreads();
   }
 
@@ -175,32 +192,55 @@ __global__ void __launch_bounds__(512) qkv_rnrc_kernel(const QkvParams p) {
           ob[e] = yb * cb[e] + ya * sb[e];                         // j >= 64: partner y[j-64]
         }
         if (is_q) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.q_out) +
-                                                (static_cast<size_t>(t) * p.Nq + h) * kD);
-          dst[l8] = pack8<BF16>(oa);
-          dst[8 + l8] = pack8<BF16>(ob);
-        } else if (store) {
+          const uint4 qa = pack8<BF16>(oa), qb = pack8<BF16>(ob);
+          const size_t row = (static_cast<size_t>(t) * p.Nq + h) * kD;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.q_out) + row);
+          dst[l8] = qa;
+          dst[8 + l8] = qb;
+          if (p.q_before != nullptr) {
+            uint4* bq = reinterpret_cast<uint4*>(static_cast<T*>(p.q_before) + row);
+            bq[l8] = qa;
+            bq[8 + l8] = qb;
+          }
+        } else {
           const int hk = h - p.Nq;
-          const size_t off = (static_cast<size_t>(idx) * p.Nk + hk) * kD;
-          if (QUANT) {
-            uint2* dst = reinterpret_cast<uint2*>(static_cast<int8_t*>(p.k_cache) + off);
-            const float* iv = inv + hk * kD;
-            dst[l8] = quant8_mul(oa, iv + ja);
-            dst[8 + l8] = quant8_mul(ob, iv + jb);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.k_cache) + off);
-            dst[l8] = pack8<BF16>(oa);
-            dst[8 + l8] = pack8<BF16>(ob);
+          if (p.k_before != nullptr) {   // dense, whatever the token's index
+            uint4* bk = reinterpret_cast<uint4*>(static_cast<T*>(p.k_before) +
+                                                 (static_cast<size_t>(t) * p.Nk + hk) * kD);
+            bk[l8] = pack8<BF16>(oa);
+            bk[8 + l8] = pack8<BF16>(ob);
+          }
+          if (store) {
+            const size_t off = (static_cast<size_t>(idx) * p.Nk + hk) * kD;
+            if (QUANT) {
+              uint2* dst = reinterpret_cast<uint2*>(static_cast<int8_t*>(p.k_cache) + off);
+              const float* iv = inv + hk * kD;
+              const float* ov = offs + hk * kD;
+              dst[l8] = quant8_mul<ASYM>(oa, iv + ja, ov + ja);
+              dst[8 + l8] = quant8_mul<ASYM>(ob, iv + jb, ov + jb);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.k_cache) + off);
+              dst[l8] = pack8<BF16>(oa);
+              dst[8 + l8] = pack8<BF16>(ob);
+            }
           }
         }
-      } else if (store) {
+      } else {
         const int hv = h - p.Nq - p.Nk;
+        if (p.v_before != nullptr) {
+          uint4* bv = reinterpret_cast<uint4*>(static_cast<T*>(p.v_before) +
+                                               (static_cast<size_t>(t) * p.Nv + hv) * kD);
+          bv[l8] = rawa;
+          bv[8 + l8] = rawb;
+        }
+        if (!store) continue;
         const size_t off = (static_cast<size_t>(idx) * p.Nv + hv) * kD;
         if (QUANT) {
           uint2* dst = reinterpret_cast<uint2*>(static_cast<int8_t*>(p.v_cache) + off);
           const float* iv = inv + (p.Nk + hv) * kD;
-          dst[l8] = quant8_mul(xa, iv + ja);
-          dst[8 + l8] = quant8_mul(xb, iv + jb);
+          const float* ov = offs + (p.Nk + hv) * kD;
+          dst[l8] = quant8_mul<ASYM>(xa, iv + ja, ov + ja);
+          dst[8 + l8] = quant8_mul<ASYM>(xb, iv + jb, ov + jb);
         } else {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.v_cache) + off);
           dst[l8] = rawa;
@@ -233,11 +273,15 @@ cudaError_t launch_qkv_rnrc(const QkvParams& p, cudaStream_t stream, int sm_coun
   const int Nh = p.Nq + p.Nk + p.Nv;
   const size_t elem = 2;   // fp16 and bf16
   const size_t buf = static_cast<size_t>(Nh) * kD * elem + 2 * kD * elem;
-  const size_t smem = kRing * buf + (p.k_scale ? static_cast<size_t>(p.Nk + p.Nv) * kD * 4 : 0);
+  const int qm = p.k_scale == nullptr ? 0 : (p.k_offset == nullptr ? 1 : 2);
+  const size_t smem = kRing * buf + static_cast<size_t>(qm) * (p.Nk + p.Nv) * kD * 4;
   if (smem > 200 * 1024) return cudaErrorNotSupported;
   auto pick = [&]() {
-    return p.bf16 ? (p.k_scale ? qkv_rnrc_kernel<true, true> : qkv_rnrc_kernel<true, false>)
-                  : (p.k_scale ? qkv_rnrc_kernel<false, true> : qkv_rnrc_kernel<false, false>);
+    if (p.bf16)
+      return qm == 0 ? qkv_rnrc_kernel<true, 0> : (qm == 1 ? qkv_rnrc_kernel<true, 1>
+                                                            : qkv_rnrc_kernel<true, 2>);
+    return qm == 0 ? qkv_rnrc_kernel<false, 0> : (qm == 1 ? qkv_rnrc_kernel<false, 1>
+                                                           : qkv_rnrc_kernel<false, 2>);
   };
   auto kern = pick();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -96,13 +96,18 @@ class QkvCase:
     name: str
     dims: QkvDims
     seed: int
-    quant: str = "symmetric"   # "none" (fp16 caches) or "symmetric" (int8 caches)
+    quant: str = "symmetric"   # "none" (fp16 caches), "symmetric" or "asymmetric" (int8 caches)
+    before_quant: bool = False # request the optional qBeforeQuant / kBeforeQuant / vBeforeQuant
     skip_frac: float = 0.01
     eps: float = 1e-6
 
 
 QKV_EPILOGUE = QkvCase("qkv_rnrc_fp16_16x1024", QkvDims(B=16, S=1024, Nq=32, Nk=8, Nv=8),
                        seed=1004)
+# Same shapes with asymmetric quant (offsets ~ U(-16, 16)) and the three before-quant outputs.
+QKV_EPILOGUE_ASYM = QkvCase("qkv_rnrc_fp16_16x1024_asym_bq",
+                            QkvDims(B=16, S=1024, Nq=32, Nk=8, Nv=8), seed=1005,
+                            quant="asymmetric", before_quant=True)
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -216,9 +221,12 @@ def make_qkv_inputs(case: QkvCase) -> dict:
     if n_skip:
         idx[torch.randperm(T, generator=g)[:n_skip]] = -1
     inp["index"] = idx
-    if case.quant == "symmetric":
+    if case.quant in ("symmetric", "asymmetric"):
         inp["k_scale"] = _uniform(g, (d.Nk, d.D), 0.02, 0.1)
         inp["v_scale"] = _uniform(g, (d.Nv, d.D), 0.02, 0.1)
+        if case.quant == "asymmetric":
+            inp["k_offset"] = _uniform(g, (d.Nk, d.D), -16.0, 16.0)
+            inp["v_offset"] = _uniform(g, (d.Nv, d.D), -16.0, 16.0)
         inp["k_cache"] = torch.randint(-128, 128, (d.block_num, d.block_size, d.Nk, d.D),
                                        generator=g, dtype=torch.int8)
         inp["v_cache"] = torch.randint(-128, 128, (d.block_num, d.block_size, d.Nv, d.D),

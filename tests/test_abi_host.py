@@ -211,7 +211,26 @@ def test_qkv_validation():
     assert _qstatus(_qargs(_qkv(Nk=2, Nv=3), Nk=2, Nv=3)) == 2   # Nk must equal Nv
     t = _qkv()
     t["k_offset"] = Fake((2, 128), torch.float32)
-    assert _qstatus(_qargs(t)) == 4                          # asymmetric quant not built
+    assert _qstatus(_qargs(t)) == 1                          # asymmetric needs both offsets
+    t["v_offset"] = Fake((2, 128), torch.float32)
+    assert _qstatus(_qargs(t)) == 0                          # asymmetric quant
+    t["v_offset"] = Fake((2, 128), torch.float16)
+    assert _qstatus(_qargs(t)) == 3                          # offsets are fp32
+    t["v_offset"] = Fake((2, 64), torch.float32)
+    assert _qstatus(_qargs(t)) == 2                          # per channel (Nv, D)
+    t = _qkv(quant=False)
+    t["k_offset"] = Fake((2, 128), torch.float32)
+    t["v_offset"] = Fake((2, 128), torch.float32)
+    assert _qstatus(_qargs(t)) == 4                          # offsets without scales
+    t = _qkv()                                               # before-quant outputs
+    t["q_before_quant"] = Fake((16, 4, 128), torch.float16)
+    t["k_before_quant"] = Fake((16, 2, 128), torch.float16)
+    t["v_before_quant"] = Fake((16, 2, 128), torch.float16)
+    assert _qstatus(_qargs(t)) == 0
+    t["k_before_quant"] = Fake((16, 4, 128), torch.float16)
+    assert _qstatus(_qargs(t)) == 2
+    t["k_before_quant"] = Fake((16, 2, 128), torch.bfloat16)
+    assert _qstatus(_qargs(t)) == 3
     t = _qkv()
     t["q_out"] = Fake((16, 4, 128), torch.bfloat16)
     assert _qstatus(_qargs(t)) == 3

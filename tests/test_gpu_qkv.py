@@ -20,10 +20,12 @@ def _build():
 def _run(case, dtype=torch.float16, tnd=False):
     cpu = synthetic.make_qkv_inputs(case)
     d = case.dims
+    quant = case.quant in ("symmetric", "asymmetric")
+    asym = case.quant == "asymmetric"
     if dtype != torch.float16:
         for k in ("qkv", "gamma_q", "gamma_k", "cos", "sin"):
             cpu[k] = cpu[k].to(dtype)
-        if case.quant != "symmetric":
+        if not quant:
             cpu["k_cache"] = cpu["k_cache"].to(dtype)
             cpu["v_cache"] = cpu["v_cache"].to(dtype)
     dev = torch.device("cuda")
@@ -33,25 +35,31 @@ def _run(case, dtype=torch.float16, tnd=False):
         t["cos"] = t["cos"].reshape(d.T, d.D)
         t["sin"] = t["sin"].reshape(d.T, d.D)
         t["q_out"] = torch.full((d.T, d.Nq, d.D), float("nan"), dtype=dtype, device=dev)
+        lead = (d.T,)
     else:
         t["qkv"] = t["qkv"].reshape(d.B, d.S, -1)
         t["cos"] = t["cos"].reshape(d.B, d.S, d.D)
         t["sin"] = t["sin"].reshape(d.B, d.S, d.D)
         t["index"] = t["index"].reshape(d.B, d.S)
         t["q_out"] = torch.full((d.B, d.S, d.Nq, d.D), float("nan"), dtype=dtype, device=dev)
+        lead = (d.B, d.S)
+    if case.before_quant:
+        for name, n in (("q_before_quant", d.Nq), ("k_before_quant", d.Nk), ("v_before_quant", d.Nv)):
+            t[name] = torch.full(lead + (n, d.D), float("nan"), dtype=dtype, device=dev)
     a = pkg.make_qkv_args(t, d.Nq, d.Nk, d.Nv, case.eps)
     ws = torch.empty(pkg.qkvrnrc_get_workspace_size(a), dtype=torch.uint8, device=dev)
     pkg.mlap_workspace_init(ws)
     pkg.qkvrnrc_execute(a, ws)
     torch.cuda.synchronize()
     status = pkg.mlap_check_errors(ws)
-    quant = case.quant == "symmetric"
     ref = oracle.qkv_rms_norm_rope_cache(
         f64(cpu["qkv"]), f64(cpu["gamma_q"]), f64(cpu["gamma_k"]), f64(cpu["cos"]),
         f64(cpu["sin"]), cpu["index"].numpy(), f64(cpu["k_cache"]), f64(cpu["v_cache"]),
         case.eps, d.Nq, d.Nk, d.Nv,
         cpu["k_scale"].numpy() if quant else None, cpu["v_scale"].numpy() if quant else None,
-        out_dtype="bf16" if dtype == torch.bfloat16 else "fp16")
+        out_dtype="bf16" if dtype == torch.bfloat16 else "fp16",
+        k_offset=cpu["k_offset"].numpy() if asym else None,
+        v_offset=cpu["v_offset"].numpy() if asym else None)
     return t, cpu, ref, status
 
 
@@ -63,6 +71,14 @@ def _check(case, dtype=torch.float16, tnd=False):
     idx = cpu["index"].numpy()
     check_cache(t["k_cache"], cpu["k_cache"], ref["k_rows"].reshape(d.T, -1), idx, "k_cache")
     check_cache(t["v_cache"], cpu["v_cache"], ref["v_rows"].reshape(d.T, -1), idx, "v_cache")
+    if case.before_quant:
+        qb = t["q_before_quant"].reshape(d.T, d.Nq, d.D)
+        assert torch.equal(qb.view(torch.int16), t["q_out"].reshape(d.T, d.Nq, d.D).view(torch.int16))
+        assert_close(f64(t["k_before_quant"]).reshape(d.T, d.Nk, d.D), ref["k_before"], "k_before")
+        # v is stored as split: bit-identical to the input slice
+        v_in = cpu["qkv"].reshape(d.T, d.Nq + d.Nk + d.Nv, d.D)[:, d.Nq + d.Nk:, :]
+        vb = t["v_before_quant"].reshape(d.T, d.Nv, d.D).cpu()
+        assert torch.equal(vb.view(torch.int16), v_in.contiguous().view(torch.int16))
 
 
 def test_qkv_full_workload():
@@ -112,3 +128,24 @@ def test_qkv_index_errors_reported():
         case.eps, d.Nq, d.Nk, d.Nv, cpu["k_scale"].numpy(), cpu["v_scale"].numpy())
     check_cache(t["k_cache"], cpu["k_cache"], ref["k_rows"].reshape(d.T, -1),
                 cpu["index"].numpy(), "k_cache")
+
+
+def test_qkv_asymmetric_before_quant_full_workload():
+    _check(synthetic.QKV_EPILOGUE_ASYM)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_qkv_asymmetric_before_quant_small(dtype):
+    # ragged token count, -1 indices, both input dtypes, TND and BSH
+    case = synthetic.QkvCase("small_asym", synthetic.QkvDims(B=3, S=37, Nq=4, Nk=2, Nv=2,
+                                                             block_num=4), seed=77,
+                             quant="asymmetric", before_quant=True, skip_frac=0.1)
+    _check(case, dtype)
+    _check(case, dtype, tnd=True)
+
+
+def test_qkv_before_quant_without_quant():
+    case = synthetic.QkvCase("small_bq", synthetic.QkvDims(B=2, S=5, Nq=2, Nk=1, Nv=1,
+                                                           block_num=2), seed=78,
+                             quant="none", before_quant=True)
+    _check(case)
