@@ -23,6 +23,17 @@ Readings where the pages are silent (each is also listed in the design notes):
   code is decided in float32, the precision of the kernel (the pages fix none).
 * Cache quant: value / quant_scale (the aclnnQkvRmsNormRopeCache "Formulas" (4) rule
   kQuant = kRoPE / kScale), round half to even, clamp to [-128, 127], decided in float32.
+* Full quant ("全量化", the scenario matrix of "约束说明"): token_x int8 with the per-token
+  dequant_scale_x (T, 1), weight_dq and weight_dkv_kr int8 with per-channel dequant_scale_w_dq
+  (1, Hcq) and dequant_scale_w_dkv_kr (1, Hckv+Dr).  Reading: the int8 matmuls accumulate
+  exactly and are dequantised as acc * dequant_scale_x[t] * dequant_scale_w[column]; from there
+  the path is the partial-quant one.  With the quantised kv_cache column, query is int8
+  "pertoken_head": per token and head, scale = amax over Hckv of q^N / 127, code = q^N / scale
+  rounded half to even and clamped to [-127, 127] (the c^Q rule), decided in float32;
+  dequant_scale_q_nope (T, N, 1) returns the scale (0 and all-zero codes when amax = 0).  The
+  pages call that cache quant "pertensor" but give quant_scale_ckv the shape (1, Hckv); the
+  shape is followed (one scale per channel, the cache-quant rule above); kr_cache stays bf16
+  there ("无需赋值" for quant_scale_ckr).
 * cache_index: slot i goes to block i // BlockSize, row i % BlockSize (Nkv = 1); i = -1 skips the
   row (aclnnQkvRmsNormRopeCache, "Other restrictions"); other out-of-range values are skipped too
   (the CUDA path also flags them).
@@ -74,6 +85,20 @@ def cache_quant(v: np.ndarray, scale: np.ndarray) -> np.ndarray:
     return saturate_int8_rne(q)
 
 
+def quant_per_token_head(q_n: np.ndarray):
+    """int8 query "pertoken_head" (MlaPrologV2 README, scenario matrix: query INT8 in full quant
+    with quantised kv_cache; dequant_scale_q_nope (T, N, 1)): per token and head symmetric, scale
+    = amax / 127, round half to even, clamp to [-127, 127], in float32.  Returns (codes (T, N, H)
+    int8, scale (T, N) float32)."""
+    s = np.asarray(q_n, np.float64).astype(np.float32)
+    amax = np.max(np.abs(s), axis=-1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    codes = saturate_int8_rne((s / safe[..., None]).astype(np.float32), -127, 127)
+    codes[scale == 0] = 0
+    return codes, scale
+
+
 def scatter_rows(cache: np.ndarray, rows: np.ndarray, cache_index: np.ndarray) -> np.ndarray:
     """Copy of ``cache`` (BlockNum, BlockSize, 1, H) with row t stored at slot cache_index[t]
     (MlaPrologV2 README k^C = Cache(c^KV), k^R = Cache(...); "-1 skips" from
@@ -91,15 +116,20 @@ def mla_prolog(token_x, weight_dq, weight_uq_qr, weight_uk, weight_dkv_kr,
                rmsnorm_gamma_cq, rmsnorm_gamma_ckv, rope_sin, rope_cos, cache_index,
                kv_cache, kr_cache, rmsnorm_epsilon_cq, rmsnorm_epsilon_ckv,
                dequant_scale_w_uq_qr=None, smooth_scales_cq=None,
-               quant_scale_ckv=None, quant_scale_ckr=None) -> dict:
+               quant_scale_ckv=None, quant_scale_ckr=None, dequant_scale_x=None,
+               dequant_scale_w_dq=None, dequant_scale_w_dkv_kr=None,
+               query_int8: bool = False) -> dict:
     """The whole prolog for T tokens.
 
     Inputs are numpy arrays holding the exact values of the operator inputs (bf16 values as
     float64; int8 weights/caches as int8).  token_x is (T, He) (the BSH form (B,S,He) is the same
     memory and is flattened by the caller).  Returns a dict with query (T,N,Hckv), query_rope
     (T,N,Dr) as float64 holding bf16 values, and the updated kv_cache / kr_cache (float64 bf16
-    values, or int8 when the caches are quantised).
+    values, or int8 when the caches are quantised).  Full quant: token_x, weight_dq and
+    weight_dkv_kr int8 with their dequant scales; query_int8 returns int8 query codes and
+    dequant_scale_q_nope (T, N).
     """
+    x_int8 = np.asarray(token_x).dtype == np.int8
     x = np.asarray(token_x, np.float64)
     T, He = x.shape
     N, D, Hckv = weight_uk.shape
@@ -108,8 +138,17 @@ def mla_prolog(token_x, weight_dq, weight_uq_qr, weight_uk, weight_dkv_kr,
     sin = np.asarray(rope_sin, np.float64).reshape(T, Dr)
     cos = np.asarray(rope_cos, np.float64).reshape(T, Dr)
 
+    def down(w, w_scale):
+        """x · W, or for int8 x and W the exact integer product dequantised per token and column."""
+        if not x_int8:
+            return x @ np.asarray(w, np.float64)
+        acc = np.asarray(token_x).astype(np.int64) @ np.asarray(w).astype(np.int64)   # exact
+        return (acc.astype(np.float64)
+                * np.asarray(dequant_scale_x, np.float64).reshape(-1, 1)
+                * np.asarray(w_scale, np.float64).reshape(1, -1))
+
     # Query path: c^Q = RmsNorm(x · W^DQ), rounded to bf16 as the next matmul's input.
-    h_q = x @ np.asarray(weight_dq, np.float64)
+    h_q = down(weight_dq, dequant_scale_w_dq)
     c_q = round_bf16(rms_norm(h_q, rmsnorm_gamma_cq, rmsnorm_epsilon_cq))
 
     # c^Q · [W^UQ | W^QR]
@@ -128,11 +167,15 @@ def mla_prolog(token_x, weight_dq, weight_uq_qr, weight_uk, weight_dkv_kr,
     q_n = np.empty((T, N, Hckv), np.float64)
     for n in range(N):                             # q^N = q^C · W^UK, per head
         q_n[:, n, :] = q_c[:, n, :] @ w_uk[n]
-    query = round_bf16(q_n)
+    scale_q = None
+    if query_int8:
+        query, scale_q = quant_per_token_head(q_n)
+    else:
+        query = round_bf16(q_n)
     query_rope = round_bf16(rope_half_and_half(q_r, cos[:, None, :], sin[:, None, :]))
 
     # Key path: c^KV = RmsNorm(x · W^DKV), k^R = ROPE(x · W^KR)
-    h_kvr = x @ np.asarray(weight_dkv_kr, np.float64)
+    h_kvr = down(weight_dkv_kr, dequant_scale_w_dkv_kr)
     c_kv = rms_norm(h_kvr[:, :Hckv], rmsnorm_gamma_ckv, rmsnorm_epsilon_ckv)
     k_r = rope_half_and_half(h_kvr[:, Hckv:Hckv + Dr], cos, sin)
 
@@ -150,6 +193,7 @@ def mla_prolog(token_x, weight_dq, weight_uq_qr, weight_uk, weight_dkv_kr,
         "query_rope": query_rope,
         "kv_cache": scatter_rows(np.asarray(kv_cache), kv_rows, cache_index),
         "kr_cache": scatter_rows(np.asarray(kr_cache), kr_rows, cache_index),
+        "dequant_scale_q_nope": scale_q,
         # intermediates, exposed for tests only
         "c_q": c_q,
         "c_kv": c_kv,
@@ -166,6 +210,8 @@ def mla_prolog_tokens(inputs: dict, token_ids) -> dict:
     sub["rope_sin"] = np.asarray(inputs["rope_sin"]).reshape(-1, np.asarray(inputs["rope_sin"]).shape[-1])[ids]
     sub["rope_cos"] = np.asarray(inputs["rope_cos"]).reshape(-1, np.asarray(inputs["rope_cos"]).shape[-1])[ids]
     sub["cache_index"] = -np.ones(len(ids), np.int64)   # no scatter
+    if inputs.get("dequant_scale_x") is not None:
+        sub["dequant_scale_x"] = np.asarray(inputs["dequant_scale_x"]).reshape(-1, 1)[ids]
     out = mla_prolog(**sub)
     kv_dtype = np.asarray(inputs["kv_cache"]).dtype
     kr_dtype = np.asarray(inputs["kr_cache"]).dtype
@@ -178,7 +224,8 @@ def mla_prolog_tokens(inputs: dict, token_ids) -> dict:
 
 def mla_key_rows(token_x, weight_dkv_kr, rmsnorm_gamma_ckv, rope_sin, rope_cos,
                  rmsnorm_epsilon_ckv, Hckv, kv_dtype_int8=False, kr_dtype_int8=False,
-                 quant_scale_ckv=None, quant_scale_ckr=None, **_unused) -> tuple:
+                 quant_scale_ckv=None, quant_scale_ckr=None, dequant_scale_x=None,
+                 dequant_scale_w_dkv_kr=None, **_unused) -> tuple:
     """Only the key path of ``mla_prolog`` (c^KV = RmsNorm(x·W^DKV), k^R = ROPE(x·W^KR)), as the
     rows the cache would receive for every token: (kv_rows, kr_rows).  Same formulas and
     rounding as ``mla_prolog``; used to check every written cache slot of large workloads."""
@@ -187,7 +234,12 @@ def mla_key_rows(token_x, weight_dkv_kr, rmsnorm_gamma_ckv, rope_sin, rope_cos,
     Dr = np.asarray(rope_sin).shape[-1]
     sin = np.asarray(rope_sin, np.float64).reshape(T, Dr)
     cos = np.asarray(rope_cos, np.float64).reshape(T, Dr)
-    h_kvr = x @ np.asarray(weight_dkv_kr, np.float64)
+    if np.asarray(token_x).dtype == np.int8:      # full quant: exact product, then dequant
+        acc = np.asarray(token_x).astype(np.int64) @ np.asarray(weight_dkv_kr).astype(np.int64)
+        h_kvr = (acc.astype(np.float64) * np.asarray(dequant_scale_x, np.float64).reshape(-1, 1)
+                 * np.asarray(dequant_scale_w_dkv_kr, np.float64).reshape(1, -1))
+    else:
+        h_kvr = x @ np.asarray(weight_dkv_kr, np.float64)
     c_kv = rms_norm(h_kvr[:, :Hckv], rmsnorm_gamma_ckv, rmsnorm_epsilon_ckv)
     k_r = rope_half_and_half(h_kvr[:, Hckv:Hckv + Dr], cos, sin)
     kv = cache_quant(c_kv, quant_scale_ckv) if kv_dtype_int8 else round_bf16(c_kv)

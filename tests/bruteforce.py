@@ -56,8 +56,10 @@ def rope_element(y, cos, sin, j):
 
 
 def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_cache, kr_cache,
-                          eps_cq, eps_ckv, dqw=None, smooth=None, qs_ckv=None, qs_ckr=None):
-    """All arguments are nested Python lists.  Returns dict of nested lists."""
+                          eps_cq, eps_ckv, dqw=None, smooth=None, qs_ckv=None, qs_ckr=None,
+                          dsx=None, dsw_dq=None, dsw_dkv=None, query_int8=False):
+    """All arguments are nested Python lists.  Returns dict of nested lists.  Full quant: x, wdq,
+    wdkv hold ints and dsx (T), dsw_dq (Hcq), dsw_dkv (Hckv+Dr) their dequant scales."""
     T, He = len(x), len(x[0])
     Hcq = len(wdq[0])
     N, D, Hckv = len(wuk), len(wuk[0]), len(wuk[0][0])
@@ -68,8 +70,11 @@ def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_c
     kv = [[[list(r) for r in row] for row in blk] for blk in kv_cache]
     kr = [[[list(r) for r in row] for row in blk] for blk in kr_cache]
     bs = len(kv_cache[0])
+    scale_q = [[0.0] * N for _ in range(T)]
     for t in range(T):
         hq = [sum(x[t][k] * wdq[k][c] for k in range(He)) for c in range(Hcq)]
+        if dsx is not None:                   # exact integer sums, dequantised
+            hq = [hq[c] * dsx[t] * dsw_dq[c] for c in range(Hcq)]
         rms = math.sqrt(sum(v * v for v in hq) / Hcq + eps_cq)
         cq = [bf16(gcq[c] * hq[c] / rms) for c in range(Hcq)]
         if int8_w:
@@ -89,11 +94,20 @@ def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_c
                     u.append(sum(cq[c] * wuq[c][col] for c in range(Hcq)))
             qc = [bf16(v) for v in u[:D]]
             r = u[D:]
-            for c2 in range(Hckv):
-                query[t][n][c2] = bf16(sum(qc[d] * wuk[n][d][c2] for d in range(D)))
+            qn = [sum(qc[d] * wuk[n][d][c2] for d in range(D)) for c2 in range(Hckv)]
+            if query_int8:
+                s = [f32(v) for v in qn]
+                amax = max(abs(v) for v in s)
+                sc = f32(amax / 127.0)
+                scale_q[t][n] = sc
+                query[t][n] = [0 if sc == 0 else int8_code(f32(v / sc), -127, 127) for v in s]
+            else:
+                query[t][n] = [bf16(v) for v in qn]
             for j in range(Dr):
                 query_rope[t][n][j] = bf16(rope_element(r, cos[t], sin[t], j))
         hkv = [sum(x[t][k] * wdkv[k][c] for k in range(He)) for c in range(Hckv + Dr)]
+        if dsx is not None:
+            hkv = [hkv[c] * dsx[t] * dsw_dkv[c] for c in range(Hckv + Dr)]
         rms = math.sqrt(sum(v * v for v in hkv[:Hckv]) / Hckv + eps_ckv)
         ckv = [gckv[c] * hkv[c] / rms for c in range(Hckv)]
         kr_row = [rope_element(hkv[Hckv:], cos[t], sin[t], j) for j in range(Dr)]
@@ -109,7 +123,8 @@ def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_c
                                           for j in range(Dr)]
             else:
                 kr[i // bs][i % bs][0] = [bf16(v) for v in kr_row]
-    return {"query": query, "query_rope": query_rope, "kv_cache": kv, "kr_cache": kr}
+    return {"query": query, "query_rope": query_rope, "kv_cache": kv, "kr_cache": kr,
+            "dequant_scale_q_nope": scale_q}
 
 
 def qkv_bruteforce(qkv, gq, gk, cos, sin, idx, k_cache, v_cache, eps, Nq, Nk, Nv, ks=None,

@@ -65,6 +65,34 @@ def test_mla_pins_catch_mutation(label, old, new):
     assert not same, f"mutation '{label}' not detected"
 
 
+FULL_QUANT_MUTATIONS = [
+    ("x dequant dropped", "* np.asarray(dequant_scale_x, np.float64).reshape(-1, 1)", ""),
+    ("W^DKV dequant from W^DQ", "h_kvr = down(weight_dkv_kr, dequant_scale_w_dkv_kr)",
+     "h_kvr = down(weight_dkv_kr, np.full_like(dequant_scale_w_dkv_kr, np.mean(dequant_scale_w_dq)))"),
+    ("query codes truncated", "codes = saturate_int8_rne((s / safe[..., None]).astype(np.float32), -127, 127)",
+     "codes = np.clip(np.trunc(s / safe[..., None]), -127, 127).astype(np.int8)"),
+    ("query scale per token", "amax = np.max(np.abs(s), axis=-1)\n    scale = (amax / np.float32(127.0)).astype(np.float32)\n    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)\n    codes = saturate_int8_rne(",
+     "amax = np.max(np.abs(s), axis=(-2, -1), keepdims=True) + 0 * s[..., 0:1]\n    amax = amax[..., 0]\n    scale = (amax / np.float32(127.0)).astype(np.float32)\n    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)\n    codes = saturate_int8_rne("),
+]
+
+
+@pytest.mark.parametrize("label,old,new", FULL_QUANT_MUTATIONS, ids=[m[0] for m in FULL_QUANT_MUTATIONS])
+def test_full_quant_pins_catch_mutation(label, old, new):
+    mod = _mutant("mla_prolog.py", old, new)
+    rng = np.random.default_rng(33)
+    inp = _tiny_mla(rng, True, True, full=True)
+    want = _brute(inp)
+    got = mod.mla_prolog(**inp)
+    same = np.array_equal(np.asarray(got["query"]), np.array(want["query"], np.int8))
+    same &= np.array_equal(np.asarray(got["dequant_scale_q_nope"]),
+                           np.array(want["dequant_scale_q_nope"], np.float32))
+    for key in ("query_rope", "kr_cache"):
+        same &= np.allclose(np.asarray(got[key], np.float64), np.array(want[key], np.float64),
+                            rtol=1e-12, atol=1e-14)
+    same &= np.array_equal(np.asarray(got["kv_cache"]), np.array(want["kv_cache"], np.int8))
+    assert not same, f"mutation '{label}' not detected"
+
+
 QKV_MUTATIONS = [
     ("split k/v swapped", "k, v = x[:, :Nq, :], x[:, Nq:Nq + Nk, :], x[:, Nq + Nk:, :]",
      "k, v = x[:, :Nq, :], x[:, Nq + Nk:, :], x[:, Nq:Nq + Nk, :]"),

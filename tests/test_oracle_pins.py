@@ -165,7 +165,8 @@ def test_dynamic_quant_properties():
 
 # ----------------------------------------------------------------------------- MLA prolog
 
-def _tiny_mla(rng, int8=False, int8_cache=False, T=3, He=8, Hcq=6, Hckv=5, N=2, D=4, Dr=4):
+def _tiny_mla(rng, int8=False, int8_cache=False, T=3, He=8, Hcq=6, Hckv=5, N=2, D=4, Dr=4,
+              full=False):
     bfr = lambda *s: oracle.round_bf16(rng.standard_normal(s) * 0.5)
     inp = dict(
         token_x=bfr(T, He), weight_dq=bfr(He, Hcq), weight_uk=bfr(N, D, Hckv),
@@ -182,11 +183,21 @@ def _tiny_mla(rng, int8=False, int8_cache=False, T=3, He=8, Hcq=6, Hckv=5, N=2, 
         inp["smooth_scales_cq"] = rng.uniform(0.5, 1.5, (1, Hcq)).astype(np.float32)
     else:
         inp["weight_uq_qr"] = bfr(Hcq, N * (D + Dr))
+    if full:   # full quant: int8 x and down-projection weights with their dequant scales
+        i8 = lambda *s: rng.integers(-127, 128, s).astype(np.int8)
+        inp["token_x"], inp["weight_dq"], inp["weight_dkv_kr"] = i8(T, He), i8(He, Hcq), i8(He, Hckv + Dr)
+        inp["dequant_scale_x"] = rng.uniform(2e-3, 8e-3, (T, 1)).astype(np.float32)
+        inp["dequant_scale_w_dq"] = rng.uniform(2e-3, 8e-3, (1, Hcq)).astype(np.float32)
+        inp["dequant_scale_w_dkv_kr"] = rng.uniform(2e-3, 8e-3, (1, Hckv + Dr)).astype(np.float32)
     if int8_cache:
         inp["kv_cache"] = rng.integers(-128, 128, (3, 2, 1, Hckv)).astype(np.int8)
-        inp["kr_cache"] = rng.integers(-128, 128, (3, 2, 1, Dr)).astype(np.int8)
         inp["quant_scale_ckv"] = rng.uniform(0.01, 0.05, (1, Hckv)).astype(np.float32)
-        inp["quant_scale_ckr"] = rng.uniform(0.01, 0.05, (1, Dr)).astype(np.float32)
+        if full:   # full quant keeps kr_cache bf16 and query becomes int8
+            inp["kr_cache"] = bfr(3, 2, 1, Dr)
+            inp["query_int8"] = True
+        else:
+            inp["kr_cache"] = rng.integers(-128, 128, (3, 2, 1, Dr)).astype(np.int8)
+            inp["quant_scale_ckr"] = rng.uniform(0.01, 0.05, (1, Dr)).astype(np.float32)
     else:
         inp["kv_cache"] = bfr(3, 2, 1, Hckv)
         inp["kr_cache"] = bfr(3, 2, 1, Dr)
@@ -194,7 +205,8 @@ def _tiny_mla(rng, int8=False, int8_cache=False, T=3, He=8, Hcq=6, Hckv=5, N=2, 
 
 
 def _brute(inp):
-    L = lambda a: np.asarray(a).tolist()
+    L = lambda a: (np.asarray(a).astype(int).tolist() if np.asarray(a).dtype == np.int8
+                   else np.asarray(a).tolist())
     f = lambda a: None if a is None else np.asarray(a, np.float64).reshape(-1).tolist()
     wuq = np.asarray(inp["weight_uq_qr"])
     wuq = wuq.astype(int).tolist() if wuq.dtype == np.int8 else wuq.tolist()
@@ -208,17 +220,27 @@ def _brute(inp):
         kr.astype(int).tolist() if kr.dtype == np.int8 else kr.tolist(),
         inp["rmsnorm_epsilon_cq"], inp["rmsnorm_epsilon_ckv"],
         dqw=f(inp.get("dequant_scale_w_uq_qr")), smooth=f(inp.get("smooth_scales_cq")),
-        qs_ckv=f(inp.get("quant_scale_ckv")), qs_ckr=f(inp.get("quant_scale_ckr")))
+        qs_ckv=f(inp.get("quant_scale_ckv")), qs_ckr=f(inp.get("quant_scale_ckr")),
+        dsx=f(inp.get("dequant_scale_x")), dsw_dq=f(inp.get("dequant_scale_w_dq")),
+        dsw_dkv=f(inp.get("dequant_scale_w_dkv_kr")), query_int8=inp.get("query_int8", False))
 
 
-@pytest.mark.parametrize("int8,int8_cache", [(False, False), (True, False), (True, True)])
-def test_mla_prolog_matches_brute_force(int8, int8_cache):
-    rng = np.random.default_rng(11 + int8 + 2 * int8_cache)
-    inp = _tiny_mla(rng, int8, int8_cache)
+@pytest.mark.parametrize("int8,int8_cache,full", [(False, False, False), (True, False, False),
+                                                  (True, True, False), (True, False, True),
+                                                  (True, True, True)])
+def test_mla_prolog_matches_brute_force(int8, int8_cache, full):
+    rng = np.random.default_rng(11 + int8 + 2 * int8_cache + 4 * full)
+    inp = _tiny_mla(rng, int8, int8_cache, full=full)
     got = oracle.mla_prolog(**inp)
     want = _brute(inp)
     for key in ("query", "query_rope"):
-        np.testing.assert_allclose(got[key], np.array(want[key]), rtol=1e-12, atol=1e-14)
+        if np.asarray(got[key]).dtype == np.int8:
+            np.testing.assert_array_equal(got[key], np.array(want[key], np.int8))
+        else:
+            np.testing.assert_allclose(got[key], np.array(want[key]), rtol=1e-12, atol=1e-14)
+    if inp.get("query_int8"):
+        np.testing.assert_array_equal(got["dequant_scale_q_nope"],
+                                      np.array(want["dequant_scale_q_nope"], np.float32))
     for key in ("kv_cache", "kr_cache"):
         if got[key].dtype == np.int8:
             np.testing.assert_array_equal(got[key], np.array(want[key], np.int8))
@@ -447,3 +469,49 @@ def test_qkv_before_quant_outputs():
     requant = np.clip(np.rint(out["k_before"] / np.asarray(inp["k_scale"], np.float64)[None]),
                       -128, 127)
     assert np.abs(requant - out["k_rows"]).max() <= 1
+
+
+def test_full_quant_k_rope_is_linear_in_dequant_scale_x():
+    # k^R = ROPE(x · W^KR) has no normalisation: doubling a token's dequant_scale_x doubles its
+    # k^R row exactly (a power of two commutes with the bf16 rounding); c^KV, normalised, stays.
+    rng = np.random.default_rng(40)
+    inp = _tiny_mla(rng, True, False, full=True)
+    inp["cache_index"] = np.array([0, 1, 2], np.int64)
+    a = oracle.mla_prolog(**inp)
+    inp2 = dict(inp)
+    inp2["dequant_scale_x"] = inp["dequant_scale_x"] * np.array([[2.0], [1.0], [1.0]], np.float32)
+    b = oracle.mla_prolog(**inp2)
+    np.testing.assert_array_equal(b["kr_cache"][0, 0], 2 * a["kr_cache"][0, 0])
+    np.testing.assert_array_equal(b["kr_cache"][0, 1], a["kr_cache"][0, 1])
+    np.testing.assert_allclose(b["c_kv"][0], a["c_kv"][0], rtol=1e-3)   # up to eps
+
+
+def test_full_quant_integer_products_are_exact():
+    # with unit dequant scales the down-projection is the integer matrix product
+    rng = np.random.default_rng(41)
+    inp = _tiny_mla(rng, True, False, full=True)
+    for k in ("dequant_scale_x", "dequant_scale_w_dq", "dequant_scale_w_dkv_kr"):
+        inp[k] = np.ones_like(inp[k])
+    out = oracle.mla_prolog(**inp)
+    h = np.asarray(inp["token_x"]).astype(np.int64) @ np.asarray(inp["weight_dkv_kr"]).astype(np.int64)
+    Hckv = 5
+    want = oracle.rope_half_and_half(h[:, Hckv:].astype(np.float64),
+                                     np.asarray(inp["rope_cos"], np.float64),
+                                     np.asarray(inp["rope_sin"], np.float64))
+    np.testing.assert_allclose(out["k_r"], want, rtol=1e-15)
+
+
+def test_query_int8_per_token_head():
+    # codes * scale reconstructs q^N within half a step, and the largest |q^N| of each (token,
+    # head) maps to +-127
+    rng = np.random.default_rng(42)
+    inp = _tiny_mla(rng, True, True, full=True)
+    out = oracle.mla_prolog(**inp)
+    inp_f = dict(inp)
+    inp_f["query_int8"] = False
+    ref = oracle.mla_prolog(**inp_f)          # bf16 query of the same computation
+    codes = out["query"].astype(np.float64)
+    scale = out["dequant_scale_q_nope"].astype(np.float64)[..., None]
+    assert (np.abs(codes).max(axis=-1) == 127).all()
+    err = np.abs(codes * scale - ref["query"])
+    assert (err <= 0.5 * scale * (1 + 1e-6) + np.abs(ref["query"]) * 2.0 ** -8).all()
