@@ -93,6 +93,8 @@ struct MlaDims {
   bool bsh;
   int64_t He, Hcq, Hckv, N, D, Dr, BlockNum, BlockSize;
   bool w_int8, kv_int8, kr_int8;
+  bool full;         // full quant: int8 token_x, W^DQ and W^DKV|W^KR (with dequant scales)
+  bool query_int8;   // full quant with int8 kv_cache: int8 query + dequant_scale_q_nope
 };
 
 constexpr int kSwapMaxT = 256;   // decode orientation (weights as MMA rows) up to this many tokens
@@ -122,16 +124,14 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
     return fail(MLAP_ERR_SHAPE, "token_x must be (T, He) or (B, S, He)");
   }
   CHECK_STATUS(need(x, "token_x", true));
-  if (x.dtype == MLAP_DTYPE_INT8)
-    return fail(MLAP_ERR_UNSUPPORTED, "int8 token_x is the full-quant scenario (not implemented)");
-  CHECK_STATUS(want_dtype(x, "token_x", MLAP_DTYPE_BF16));
+  d->full = x.dtype == MLAP_DTYPE_INT8;   // 全量化: int8 token_x
+  if (!d->full) CHECK_STATUS(want_dtype(x, "token_x", MLAP_DTYPE_BF16));
+  const int wdt = d->full ? MLAP_DTYPE_INT8 : MLAP_DTYPE_BF16;   // W^DQ, W^DKV|W^KR dtype
 
   // weights (logical shapes (k, n); data = prepacked buffers)
   const mlap_tensor_t& wdq = a->weight_dq;
   CHECK_STATUS(need(wdq, "weight_dq", false));
-  if (wdq.dtype == MLAP_DTYPE_INT8)
-    return fail(MLAP_ERR_UNSUPPORTED, "int8 weight_dq is the full-quant scenario (not implemented)");
-  CHECK_STATUS(want_dtype(wdq, "weight_dq", MLAP_DTYPE_BF16));
+  CHECK_STATUS(want_dtype(wdq, "weight_dq", wdt));
   if (wdq.ndim != 2 || wdq.shape[0] != d->He) return fail(MLAP_ERR_SHAPE, "weight_dq must be (He, Hcq)");
   d->Hcq = wdq.shape[1];
 
@@ -154,6 +154,8 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
     return fail(MLAP_ERR_SHAPE, "N, Hckv, Hcq and He must be positive");
   if ((d->He % 8) || (d->Hcq % 8) || (d->Hckv % 8))
     return fail(MLAP_ERR_UNSUPPORTED, "He, Hcq and Hckv must be multiples of 8 (16-byte TMA pitch)");
+  if (d->full && (d->He % 16))
+    return fail(MLAP_ERR_UNSUPPORTED, "full quant needs He % 16 == 0 (16-byte int8 row pitch)");
 
   const mlap_tensor_t& wuq = a->weight_uq_qr;
   CHECK_STATUS(need(wuq, "weight_uq_qr", false));
@@ -168,9 +170,7 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
 
   const mlap_tensor_t& wkv = a->weight_dkv_kr;
   CHECK_STATUS(need(wkv, "weight_dkv_kr", false));
-  if (wkv.dtype == MLAP_DTYPE_INT8)
-    return fail(MLAP_ERR_UNSUPPORTED, "int8 weight_dkv_kr is the full-quant scenario (not implemented)");
-  CHECK_STATUS(want_dtype(wkv, "weight_dkv_kr", MLAP_DTYPE_BF16));
+  CHECK_STATUS(want_dtype(wkv, "weight_dkv_kr", wdt));
   CHECK_STATUS(want_shape(wkv, "weight_dkv_kr", {d->He, d->Hckv + d->Dr}));
 
   CHECK_STATUS(need(a->rmsnorm_gamma_cq, "rmsnorm_gamma_cq", false));
@@ -192,9 +192,8 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
   const mlap_tensor_t& qr = a->query_rope;
   CHECK_STATUS(need(q, "query", true));
   CHECK_STATUS(need(qr, "query_rope", true));
-  if (q.dtype == MLAP_DTYPE_INT8)
-    return fail(MLAP_ERR_UNSUPPORTED, "int8 query is the full-quant scenario (not implemented)");
-  CHECK_STATUS(want_dtype(q, "query", MLAP_DTYPE_BF16));
+  d->query_int8 = q.dtype == MLAP_DTYPE_INT8;   // checked against the scenario below
+  if (!d->query_int8) CHECK_STATUS(want_dtype(q, "query", MLAP_DTYPE_BF16));
   CHECK_STATUS(want_dtype(qr, "query_rope", MLAP_DTYPE_BF16));
   if (d->bsh) {
     CHECK_STATUS(want_shape(sn, "rope_sin", {d->B, d->S, d->Dr}));
@@ -231,12 +230,40 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
   CHECK_STATUS(cache_dt(kr, "kr_cache", &d->kr_int8));
 
   // scenario matrix (约束说明)
-  if (present(a->dequant_scale_x) || present(a->dequant_scale_w_dq) ||
-      present(a->dequant_scale_w_dkv_kr))
-    return fail(MLAP_ERR_UNSUPPORTED,
-                "dequant_scale_x / _w_dq / _w_dkv_kr are reserved outside full quant and must be NULL");
-  if (d->kv_int8 != d->kr_int8)
-    return fail(MLAP_ERR_UNSUPPORTED, "kv_cache and kr_cache must both be int8 or both bf16 outside full quant");
+  if (d->full) {
+    // 全量化: per-token dequant of x, per-channel dequant of W^DQ and W^DKV|W^KR, int8 W^UQ|W^QR;
+    // kr_cache stays bf16; an int8 kv_cache makes the query int8 per token and head
+    const mlap_tensor_t& dsx = a->dequant_scale_x;
+    CHECK_STATUS(need(dsx, "dequant_scale_x", false));
+    CHECK_STATUS(want_dtype(dsx, "dequant_scale_x", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_shape(dsx, "dequant_scale_x", {d->T, 1}));
+    CHECK_STATUS(need(a->dequant_scale_w_dq, "dequant_scale_w_dq", false));
+    CHECK_STATUS(want_dtype(a->dequant_scale_w_dq, "dequant_scale_w_dq", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_shape(a->dequant_scale_w_dq, "dequant_scale_w_dq", {1, d->Hcq}));
+    CHECK_STATUS(need(a->dequant_scale_w_dkv_kr, "dequant_scale_w_dkv_kr", false));
+    CHECK_STATUS(want_dtype(a->dequant_scale_w_dkv_kr, "dequant_scale_w_dkv_kr", MLAP_DTYPE_FP32));
+    CHECK_STATUS(want_shape(a->dequant_scale_w_dkv_kr, "dequant_scale_w_dkv_kr", {1, d->Hckv + d->Dr}));
+    if (!d->w_int8) return fail(MLAP_ERR_UNSUPPORTED, "full quant needs an int8 weight_uq_qr");
+    if (d->kr_int8) return fail(MLAP_ERR_UNSUPPORTED, "full quant keeps kr_cache bf16");
+    if (present(a->quant_scale_ckr))
+      return fail(MLAP_ERR_UNSUPPORTED, "quant_scale_ckr is not used in full quant");
+    if (d->query_int8 != d->kv_int8)
+      return fail(MLAP_ERR_UNSUPPORTED, "full quant: query is int8 exactly when kv_cache is int8");
+    if (d->query_int8) {
+      const mlap_tensor_t& sq = a->dequant_scale_q_nope;
+      CHECK_STATUS(need(sq, "dequant_scale_q_nope", false));
+      CHECK_STATUS(want_dtype(sq, "dequant_scale_q_nope", MLAP_DTYPE_FP32));
+      CHECK_STATUS(want_shape(sq, "dequant_scale_q_nope", {d->T, d->N, 1}));
+    }
+  } else {
+    if (present(a->dequant_scale_x) || present(a->dequant_scale_w_dq) ||
+        present(a->dequant_scale_w_dkv_kr))
+      return fail(MLAP_ERR_UNSUPPORTED,
+                  "dequant_scale_x / _w_dq / _w_dkv_kr are reserved outside full quant and must be NULL");
+    if (d->query_int8) return fail(MLAP_ERR_DTYPE, "int8 query is the full-quant scenario");
+    if (d->kv_int8 != d->kr_int8)
+      return fail(MLAP_ERR_UNSUPPORTED, "kv_cache and kr_cache must both be int8 or both bf16 outside full quant");
+  }
   if (d->w_int8) {
     CHECK_STATUS(need(a->dequant_scale_w_uq_qr, "dequant_scale_w_uq_qr", false));
     CHECK_STATUS(want_dtype(a->dequant_scale_w_uq_qr, "dequant_scale_w_uq_qr", MLAP_DTYPE_FP32));
@@ -253,10 +280,13 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
     CHECK_STATUS(need(a->quant_scale_ckv, "quant_scale_ckv", false));
     CHECK_STATUS(want_dtype(a->quant_scale_ckv, "quant_scale_ckv", MLAP_DTYPE_FP32));
     CHECK_STATUS(want_shape(a->quant_scale_ckv, "quant_scale_ckv", {1, d->Hckv}));
+  }
+  if (d->kr_int8) {
     CHECK_STATUS(need(a->quant_scale_ckr, "quant_scale_ckr", false));
     CHECK_STATUS(want_dtype(a->quant_scale_ckr, "quant_scale_ckr", MLAP_DTYPE_FP32));
     CHECK_STATUS(want_shape(a->quant_scale_ckr, "quant_scale_ckr", {1, d->Dr}));
-  } else if (present(a->quant_scale_ckv) || present(a->quant_scale_ckr)) {
+  }
+  if ((!d->kv_int8 && present(a->quant_scale_ckv)) || (!d->kr_int8 && present(a->quant_scale_ckr))) {
     return fail(MLAP_ERR_UNSUPPORTED, "quant_scale_ckv / quant_scale_ckr need int8 caches");
   }
   if (a->cache_mode != nullptr && std::strcmp(a->cache_mode, "PA_BSND") != 0)
@@ -274,7 +304,7 @@ int swap_bn(int64_t T) {
 }
 
 struct MlaWs {
-  size_t part, cq, qc, scale, total;
+  size_t part, cq, qc, scale, xb, qn, total;
   int split_cap;
 };
 
@@ -296,6 +326,10 @@ MlaWs mla_ws_layout(const MlaDims& d) {
   off += align_up(static_cast<size_t>(d.T) * d.N * d.D * 2, 256);
   w.scale = off;
   off += align_up(static_cast<size_t>(d.T) * 4, 256);
+  w.xb = off;   // full quant: token_x widened to bf16 (exact) for the down-projection
+  if (d.full) off += align_up(static_cast<size_t>(d.T) * d.He * 2, 256);
+  w.qn = off;   // int8 query: q^N in bf16 before the per-token-head quant
+  if (d.query_int8) off += align_up(static_cast<size_t>(d.T) * d.N * d.Hckv * 2, 256);
   w.total = off;
   return w;
 }
@@ -456,20 +490,28 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   g.mt = swap ? mt : 1;
   DownParams dp{0};
   const int ch_t = swap ? (bn_t < 32 ? bn_t : 32) : 32;   // tokens per epilogue store box
+  // full quant: the int8 activation is widened to bf16 first (exact), the int8 weights are
+  // expanded in shared memory by the GEMM's converter warps, and the integer products are
+  // dequantised per token and column after the K-split sum (norm kernel)
+  const void* xact = d.full ? static_cast<const void*>(wsb + L.xb) : a->token_x.data;
+  g.a_int8 = d.full;
+  auto wmap = [&](CUtensorMap* m, const void* w, int64_t rows, int box) {
+    return d.full ? make_tmap_i8(m, w, d.He, rows, box) : make_tmap(m, w, d.He, rows, d.He, box);
+  };
   {
     const int kb = ceil_div(d.He, 64);
     if (swap) {
       const int seg = ceil_div(d.Hcq, wrows);
-      CHECK_STATUS(make_tmap(&g.a0, a->weight_dq.data, d.He, d.Hcq, d.He, wrows));
-      CHECK_STATUS(make_tmap(&g.a1, a->weight_dkv_kr.data, d.He, d.Hckv + d.Dr, d.He, wrows));
-      CHECK_STATUS(make_tmap(&g.b0, a->token_x.data, d.He, d.T, d.He, bn_t));
+      CHECK_STATUS(wmap(&g.a0, a->weight_dq.data, d.Hcq, wrows));
+      CHECK_STATUS(wmap(&g.a1, a->weight_dkv_kr.data, d.Hckv + d.Dr, wrows));
+      CHECK_STATUS(make_tmap(&g.b0, xact, d.He, d.T, d.He, bn_t));
       g.b1 = g.b0;
       g.bn = bn_t;
       g.geo.m_tiles = seg + ceil_div(d.Hckv + d.Dr, wrows);
       g.geo.n_tiles = 1;
       g.geo.a_seg_tiles = seg;
       g.geo.b_seg_tiles = 1;
-      set_act(&g.geo, a->token_x.data, d.He, d.T, d.He);
+      set_act(&g.geo, xact, d.He, d.T, d.He);
       int splits = sms / g.geo.m_tiles;
       if (splits > L.split_cap) splits = L.split_cap;
       if (splits > kb) splits = kb;
@@ -478,10 +520,10 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       dp.seg_tiles = seg;
     } else {
       const int seg = ceil_div(d.Hcq, 192);
-      CHECK_STATUS(make_tmap(&g.a0, a->token_x.data, d.He, d.T, d.He, 128));
+      CHECK_STATUS(make_tmap(&g.a0, xact, d.He, d.T, d.He, 128));
       g.a1 = g.a0;
-      CHECK_STATUS(make_tmap(&g.b0, a->weight_dq.data, d.He, d.Hcq, d.He, 192));
-      CHECK_STATUS(make_tmap(&g.b1, a->weight_dkv_kr.data, d.He, d.Hckv + d.Dr, d.He, 192));
+      CHECK_STATUS(wmap(&g.b0, a->weight_dq.data, d.Hcq, 192));
+      CHECK_STATUS(wmap(&g.b1, a->weight_dkv_kr.data, d.Hckv + d.Dr, 192));
       g.bn = 192;
       g.geo.m_tiles = ceil_div(d.T, 128);
       g.geo.n_tiles = seg + ceil_div(d.Hckv + d.Dr, 192);
@@ -509,6 +551,11 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                               CU_TENSOR_MAP_SWIZZLE_128B));
     g.grid = balanced_grid(g.geo.num_units, sms);
     CHECK_STATUS(rec(0));
+    if (d.full) {
+      ce = launch_widen_int8(static_cast<const int8_t*>(a->token_x.data),
+                             reinterpret_cast<__nv_bfloat16*>(wsb + L.xb), d.T * d.He, stream);
+      if (ce != cudaSuccess) return cuda_fail(ce, "token_x widening launch");
+    }
     ce = launch_down(g, dp);
     if (ce != cudaSuccess) return cuda_fail(ce, "down-projection launch");
   }
@@ -541,6 +588,11 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     fp.smooth = d.w_int8 ? static_cast<const float*>(a->smooth_scales_cq.data) : nullptr;
     fp.scale_t = scale_t;
     fp.err = err;
+    if (d.full) {
+      fp.dsx = static_cast<const float*>(a->dequant_scale_x.data);
+      fp.dsw_q = static_cast<const float*>(a->dequant_scale_w_dq.data);
+      fp.dsw_kv = static_cast<const float*>(a->dequant_scale_w_dkv_kr.data);
+    }
     CHECK_STATUS(rec(1));
     ce = launch_finalize(fp, stream, true);
     if (ce != cudaSuccess) return cuda_fail(ce, "norm/rope/scatter launch");
@@ -697,16 +749,25 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.pm = b.a0;
     b.grid = ab_var ? static_cast<int>(std::min<int64_t>(sms, d.N * d.Hckv / 32))
                     : balanced_grid(b.geo.num_units, sms);
-    CHECK_STATUS(make_out_map(&b.o0, a->query.data, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    // an int8 query is quantised per token and head from a bf16 q^N staged in the workspace
+    __nv_bfloat16* qn_out = d.query_int8 ? reinterpret_cast<__nv_bfloat16*>(wsb + L.qn)
+                                         : static_cast<__nv_bfloat16*>(a->query.data);
+    CHECK_STATUS(make_out_map(&b.o0, qn_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                               {d.Hckv, d.N, d.T}, {d.Hckv * 2, d.N * d.Hckv * 2}, {32, 1, b.swap ? ch_t : 32},
                               CU_TENSOR_MAP_SWIZZLE_64B));
     b.o1 = b.o0;
-    AbsorbParams ap{ab_var ? static_cast<__nv_bfloat16*>(a->query.data) : nullptr,
+    AbsorbParams ap{ab_var ? qn_out : nullptr,
                     static_cast<int32_t>(d.T), static_cast<int32_t>(d.N),
                     static_cast<int32_t>(d.Hckv)};
     CHECK_STATUS(rec(3));
     ce = launch_absorb(b, ap);
     if (ce != cudaSuccess) return cuda_fail(ce, "absorb launch");
+    if (d.query_int8) {
+      ce = launch_query_quant(qn_out, static_cast<int8_t*>(a->query.data),
+                              static_cast<float*>(a->dequant_scale_q_nope.data), d.T * d.N,
+                              static_cast<int32_t>(d.Hckv), stream);
+      if (ce != cudaSuccess) return cuda_fail(ce, "query quant launch");
+    }
     CHECK_STATUS(rec(4));
   }
   if (timer != nullptr) timer->calls++;
@@ -844,7 +905,8 @@ mlap_status_t mlap_prepack_size(const mlap_tensor_t* w, int32_t which, int32_t N
   switch (which) {
     case MLAP_WEIGHT_DQ:
     case MLAP_WEIGHT_DKV_KR:
-      if (w->dtype != MLAP_DTYPE_BF16) return fail(MLAP_ERR_DTYPE, "weight must be bf16");
+      if (w->dtype != MLAP_DTYPE_BF16 && w->dtype != MLAP_DTYPE_INT8)
+        return fail(MLAP_ERR_DTYPE, "weight must be bf16 or int8 (full quant)");
       if (w->ndim != 2) return fail(MLAP_ERR_SHAPE, "weight must be 2-D (k, n)");
       break;
     case MLAP_WEIGHT_UQ_QR:

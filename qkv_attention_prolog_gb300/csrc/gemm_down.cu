@@ -3,7 +3,25 @@
 
 namespace mlap {
 
+// Full quant: int8 W^DQ and W^DKV|W^KR expanded to bf16 by the converter warps (exact); the
+// activation is the bf16-widened int8 token_x.
+static cudaError_t launch_down_int8(const GemmLaunch& L, const DownParams& p) {
+  if (L.swap) {
+    switch (L.bn) {
+      case 16: return launch_gemm_t<16, 1, 1>(L, EpiDown<true, 128, 16>{p});
+      case 32: return launch_gemm_t<32, 1, 1>(L, EpiDown<true, 128, 32>{p});
+      case 64: return launch_gemm_t<64, 1, 1>(L, EpiDown<true, 128, 32>{p});
+      case 128: return launch_gemm_t<128, 1, 1>(L, EpiDown<true, 128, 32>{p});
+      case 256: return launch_gemm_t<256, 1, 1>(L, EpiDown<true, 128, 32>{p});
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (L.bn != 192) return cudaErrorInvalidValue;
+  return launch_gemm_t<192, 2>(L, EpiDown<false, 192, 32>{p});
+}
+
 cudaError_t launch_down(const GemmLaunch& L, const DownParams& p) {
+  if (L.a_int8) return launch_down_int8(L, p);
   if (L.swap) {
     switch (L.bn) {
       case 16: return L.mt == 2 ? launch_gemm_t<16, 0, 2, 1>(L, EpiDown<true, 256, 16>{p})

@@ -54,8 +54,19 @@ struct FinalizeParams {
   const float* smooth;         // non-null: quantise c^Q per token
   float* scale_t;              // (T) per-token scale of the quantised c^Q
   uint32_t* err;
+  const float* dsx;            // full quant: h *= dsx[t] * (dsw_q | dsw_kv)[column] (null: none)
+  const float* dsw_q;
+  const float* dsw_kv;
 };
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl);
+
+// Full quant: int8 token_x widened to bf16 (exact), n elements (a multiple of 16).
+cudaError_t launch_widen_int8(const int8_t* x, __nv_bfloat16* out, int64_t n, cudaStream_t stream);
+
+// int8 query per token and head: rows of H bf16 values -> int8 codes (scale = amax / 127, round
+// half to even, clamp to [-127, 127]) and the per-row fp32 scale (dequant_scale_q_nope).
+cudaError_t launch_query_quant(const __nv_bfloat16* qn, int8_t* q, float* scale, int64_t rows,
+                               int32_t H, cudaStream_t stream);
 
 // Weight prepack: dst[b][i][k] = src[b][k][perm(i)]  (a transpose with a row permutation).
 enum PermKind : int32_t { kPermIdentity = 0, kPermUqQr = 1 };

@@ -11,6 +11,8 @@
 //              (half-and-half rule of aclnnQkvRmsNormRopeCache "Formulas" (3))
 //   int8 caches: rne(value / quant_scale[j]) saturated to [-128, 127] ("Formulas" (4) division).
 //   cache_index = -1 skips the token; other values outside [0, slots) are skipped and latched.
+//   full quant: h *= dequant_scale_x[t] * dequant_scale_w[column] after the split sum (the int8
+//   products are exact), and the two helper kernels below (token_x widening, int8 query).
 // With Nkv = 1 and a dense (BlockNum, BlockSize, 1, H) cache, slot i is row i of the cache.
 #include "internal.h"
 
@@ -121,6 +123,12 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     }
   }
   __syncthreads();
+  if (p.dsx != nullptr) {   // full quant: dequant the exact integer products per token and column
+    const float sx = p.dsx[t];
+    for (int c = threadIdx.x; c < p.Ntot; c += NT)
+      h[c] *= sx * (c < p.Hcq ? p.dsw_q[c] : p.dsw_kv[c - p.Hcq]);
+    __syncthreads();
+  }
 
   // sums of squares of the c^Q and c^KV parts, one reduction
   const float* hkv = h + p.Hcq;
@@ -232,7 +240,73 @@ __global__ void prepack_kernel(const PrepackParams p) {
   }
 }
 
+// Full quant: 16 int8 values -> 16 bf16 per thread and step (exact: |v| <= 128).
+__global__ void widen_int8_kernel(const int8_t* __restrict__ x, __nv_bfloat16* __restrict__ out,
+                                  int64_t n16) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 raw = reinterpret_cast<const uint4*>(x)[i];
+    const int8_t* v = reinterpret_cast<const int8_t*>(&raw);
+    float f[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) f[k] = static_cast<float>(v[k]);
+    store8_bf16(out + i * 16, f);
+    store8_bf16(out + i * 16 + 8, f + 8);
+  }
+}
+
+// int8 query per token and head (MlaPrologV2 README scenario matrix: query INT8 "pertoken_head"
+// with dequant_scale_q_nope): one warp per (token, head) row of H values; scale = amax / 127,
+// code = rne(v / scale) clamped to [-127, 127] (all-zero row: codes 0, scale 0), in fp32.
+__global__ void query_quant_kernel(const __nv_bfloat16* __restrict__ qn, int8_t* __restrict__ q,
+                                   float* __restrict__ scale, int64_t rows, int32_t H) {
+  const int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;                        // warp-uniform
+  const __nv_bfloat16* src = qn + row * H;
+  float amax = 0.f;
+  for (int c = lane * 8; c < H; c += 256) {
+    float v[8];
+    load8_bf16(src + c, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float sc = __fdiv_rn(amax, 127.0f);
+  int8_t* dst = q + row * H;
+  for (int c = lane * 8; c < H; c += 256) {
+    float v[8];
+    load8_bf16(src + c, v);
+    uint2 out;
+    int8_t* o = reinterpret_cast<int8_t*>(&out);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = sc > 0.f ? quant_i8(v[k], sc, -127, 127) : 0;
+    *reinterpret_cast<uint2*>(dst + c) = out;
+  }
+  if (lane == 0) scale[row] = sc;
+}
+
 }  // namespace
+
+cudaError_t launch_widen_int8(const int8_t* x, __nv_bfloat16* out, int64_t n, cudaStream_t stream) {
+  if (n % 16) return cudaErrorInvalidValue;
+  const int64_t n16 = n / 16;
+  int64_t blocks = (n16 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  widen_int8_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, out, n16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_query_quant(const __nv_bfloat16* qn, int8_t* q, float* scale, int64_t rows,
+                               int32_t H, cudaStream_t stream) {
+  if (H % 8) return cudaErrorInvalidValue;
+  const int64_t blocks = (rows * 32 + 255) / 256;
+  if (blocks < 1) return cudaSuccess;
+  query_quant_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(qn, q, scale, rows, H);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {
   const size_t smem = static_cast<size_t>(p.Ntot) * sizeof(float);

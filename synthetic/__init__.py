@@ -54,6 +54,10 @@ class MlaCase:
     n_skip: int = 0            # number of cache_index entries set to -1
     pos_mode: str = "random"   # "random": positions in [0,4096); "sequence": 0..S-1 per sequence
     eps: float = 1e-6
+    # full quant ("全量化"): int8 token_x, weight_dq, weight_dkv_kr with their dequant scales
+    # (weight_uq_qr_dtype must be "int8"); with cache_dtype "int8" only kv_cache is int8 and
+    # the query is int8 per token and head
+    full_quant: bool = False
 
 
 # The five workloads.  Sizes, distributions and cache layouts follow the stated workload recipe.
@@ -71,6 +75,11 @@ MLA_PARTIAL_QUANT = MlaCase("partial_quant_int8cache_T64",
 # partial quant with bf16 kv_cache (the scenario's other column)
 MLA_PARTIAL_QUANT_BF16CACHE = replace(MLA_PARTIAL_QUANT, name="partial_quant_bf16cache_T64",
                                       cache_dtype="bf16", seed=1005)
+# full quant, both kv_cache columns, at the partial-quant shapes
+MLA_FULL_QUANT = replace(MLA_PARTIAL_QUANT, name="full_quant_int8cache_T64", seed=1006,
+                         full_quant=True)
+MLA_FULL_QUANT_BF16CACHE = replace(MLA_PARTIAL_QUANT, name="full_quant_bf16cache_T64",
+                                   seed=1007, full_quant=True, cache_dtype="bf16")
 
 
 @dataclass(frozen=True)
@@ -169,7 +178,18 @@ def make_mla_inputs(case: MlaCase) -> dict:
     def w(k, n):
         return (torch.randn(k, n, generator=g) / math.sqrt(k)).to(bf16)
 
-    inp["weight_dq"] = w(d.He, d.Hcq)
+    def i8(*shape):
+        return torch.randint(-127, 128, shape, generator=g, dtype=torch.int8)
+
+    if case.full_quant:
+        # int8 x and down-projection weights; dequant scales sized so that x·W is O(1):
+        # sum over He of U[-127,127]^2 products has std ~ 5e4*sqrt(He/100), times ~2.2e-6
+        inp["token_x"] = i8(T, d.He)
+        inp["dequant_scale_x"] = _uniform(g, (T, 1), 1e-3, 2e-3)
+        inp["weight_dq"] = i8(d.He, d.Hcq)
+        inp["dequant_scale_w_dq"] = _uniform(g, (1, d.Hcq), 1e-3, 2e-3)
+    else:
+        inp["weight_dq"] = w(d.He, d.Hcq)
     if case.weight_uq_qr_dtype == "int8":
         inp["weight_uq_qr"] = torch.randint(-127, 128, (d.Hcq, d.N * (d.D + d.Dr)), generator=g,
                                             dtype=torch.int8)
@@ -178,7 +198,11 @@ def make_mla_inputs(case: MlaCase) -> dict:
     else:
         inp["weight_uq_qr"] = w(d.Hcq, d.N * (d.D + d.Dr))
     inp["weight_uk"] = (torch.randn(d.N, d.D, d.Hckv, generator=g) / math.sqrt(d.D)).to(bf16)
-    inp["weight_dkv_kr"] = w(d.He, d.Hckv + d.Dr)
+    if case.full_quant:
+        inp["weight_dkv_kr"] = i8(d.He, d.Hckv + d.Dr)
+        inp["dequant_scale_w_dkv_kr"] = _uniform(g, (1, d.Hckv + d.Dr), 1e-3, 2e-3)
+    else:
+        inp["weight_dkv_kr"] = w(d.He, d.Hckv + d.Dr)
     inp["rmsnorm_gamma_cq"] = _uniform(g, (d.Hcq,), 0.5, 1.5, bf16)
     inp["rmsnorm_gamma_ckv"] = _uniform(g, (d.Hckv,), 0.5, 1.5, bf16)
     if case.pos_mode == "random":
@@ -188,7 +212,12 @@ def make_mla_inputs(case: MlaCase) -> dict:
     inp["rope_sin"], inp["rope_cos"] = rope_tables(pos, d.Dr, bf16)
     inp["cache_index"] = _slots(g, case.index_mode, T, d.B, d.S, d.block_num, d.block_size,
                                 case.n_skip)
-    if case.cache_dtype == "int8":
+    if case.cache_dtype == "int8" and case.full_quant:   # kv int8 per channel, kr stays bf16
+        inp["kv_cache"] = torch.randint(-128, 128, (d.block_num, d.block_size, 1, d.Hckv),
+                                        generator=g, dtype=torch.int8)
+        inp["kr_cache"] = torch.randn(d.block_num, d.block_size, 1, d.Dr, generator=g).to(bf16)
+        inp["quant_scale_ckv"] = _uniform(g, (1, d.Hckv), 0.01, 0.05)
+    elif case.cache_dtype == "int8":
         inp["kv_cache"] = torch.randint(-128, 128, (d.block_num, d.block_size, 1, d.Hckv),
                                         generator=g, dtype=torch.int8)
         inp["kr_cache"] = torch.randint(-128, 128, (d.block_num, d.block_size, 1, d.Dr),

@@ -82,7 +82,15 @@ def mla_device_tensors(cpu: dict, dims, device, bsh=False):
     # poison the outputs so unwritten elements show up
     t["query"].fill_(float("nan"))
     t["query_rope"].fill_(float("nan"))
+    if query_int8(cpu):   # full quant with int8 kv_cache: int8 query per token and head
+        t["query"] = torch.full(t["query"].shape, 99, dtype=torch.int8, device=device)
+        t["dequant_scale_q_nope"] = torch.full((dims.T, dims.N, 1), float("nan"),
+                                               dtype=torch.float32, device=device)
     return t
+
+
+def query_int8(cpu: dict) -> bool:
+    return cpu["token_x"].dtype == torch.int8 and cpu["kv_cache"].dtype == torch.int8
 
 
 def run_mla(cpu: dict, dims, eps, device="cuda", bsh=False, prolog=None):
@@ -101,4 +109,5 @@ def oracle_inputs(cpu: dict, eps: float) -> dict:
     inp = {k: f64(v) for k, v in cpu.items() if isinstance(v, torch.Tensor)}
     inp["rmsnorm_epsilon_cq"] = eps
     inp["rmsnorm_epsilon_ckv"] = eps
+    inp["query_int8"] = query_int8(cpu)
     return inp

@@ -58,7 +58,7 @@ class Fake:
 
 
 def _mla(T=128, He=7168, Hcq=1536, Hckv=512, N=128, D=128, Dr=64, BN=16, bsh=False,
-         w_int8=False, cache_int8=False):
+         w_int8=False, cache_int8=False, full=False):
     bf, i8, f32 = torch.bfloat16, torch.int8, torch.float32
     tok = (T // 2, 2) if bsh else (T,)
     t = {
@@ -78,6 +78,18 @@ def _mla(T=128, He=7168, Hcq=1536, Hckv=512, N=128, D=128, Dr=64, BN=16, bsh=Fal
     if cache_int8:
         t["quant_scale_ckv"] = Fake((1, Hckv), f32)
         t["quant_scale_ckr"] = Fake((1, Dr), f32)
+    if full:   # 全量化: int8 x and down weights with dequant scales, int8 W^UQ|W^QR
+        t["token_x"] = Fake(tok + (He,), i8)
+        t["weight_dq"] = Fake((He, Hcq), i8)
+        t["weight_dkv_kr"] = Fake((He, Hckv + Dr), i8)
+        t["dequant_scale_x"] = Fake((T, 1), f32)
+        t["dequant_scale_w_dq"] = Fake((1, Hcq), f32)
+        t["dequant_scale_w_dkv_kr"] = Fake((1, Hckv + Dr), f32)
+        t["kr_cache"] = Fake((BN, 128, 1, Dr), bf)
+        t.pop("quant_scale_ckr", None)
+        if cache_int8:   # int8 kv_cache: int8 query per token and head
+            t["query"] = Fake(tok + (N, Hckv), i8)
+            t["dequant_scale_q_nope"] = Fake((T, N, 1), f32)
     return t
 
 
@@ -122,7 +134,7 @@ def test_workspace_grows_with_tokens():
     (lambda t: t.__setitem__("cache_index", Fake((128,), torch.int8)), 3),
     (lambda t: t.__setitem__("weight_uk", Fake((128, 64, 512), torch.bfloat16)), 4),   # D != 128
     (lambda t: t.__setitem__("dequant_scale_x", Fake((128, 1), torch.float32)), 4),
-    (lambda t: t.__setitem__("token_x", Fake((128, 7168), torch.int8)), 4),           # full quant
+    (lambda t: t.__setitem__("token_x", Fake((128, 7168), torch.int8)), 3),   # full quant: int8 W^DQ
     (lambda t: t.__setitem__("kv_cache", Fake((16, 128, 2, 512), torch.bfloat16)), 4),  # Nkv != 1
     (lambda t: t.__setitem__("quant_scale_ckv", Fake((1, 512), torch.float32)), 4),
     (lambda t: t.__setitem__("query_rope", Fake((128, 128, 64), torch.float32)), 3),
@@ -234,3 +246,33 @@ def test_qkv_validation():
     t = _qkv()
     t["q_out"] = Fake((16, 4, 128), torch.bfloat16)
     assert _qstatus(_qargs(t)) == 3
+
+
+def test_full_quant_scenarios():
+    assert _status(_args(_mla(w_int8=True, full=True)))[0] == 0               # kv_cache bf16
+    assert _status(_args(_mla(w_int8=True, cache_int8=True, full=True)))[0] == 0
+    assert _status(_args(_mla(w_int8=True, cache_int8=True, full=True, bsh=True)))[0] == 0
+    t = _mla(w_int8=True, full=True)
+    t.pop("dequant_scale_x")
+    assert _status(_args(t))[0] == 1
+    t = _mla(w_int8=True, full=True)
+    t["dequant_scale_w_dq"] = Fake((1, 1536), torch.bfloat16)
+    assert _status(_args(t))[0] == 3
+    t = _mla(full=True)                                   # full quant needs an int8 W^UQ|W^QR
+    t.pop("dequant_scale_w_uq_qr", None)
+    assert _status(_args(t))[0] == 4
+    t = _mla(w_int8=True, cache_int8=True, full=True)
+    t["kr_cache"] = Fake((16, 128, 1, 64), torch.int8)    # kr_cache stays bf16
+    assert _status(_args(t))[0] == 4
+    t = _mla(w_int8=True, cache_int8=True, full=True)
+    t["query"] = Fake((128, 128, 512), torch.bfloat16)    # int8 kv_cache -> int8 query
+    assert _status(_args(t))[0] == 4
+    t = _mla(w_int8=True, cache_int8=True, full=True)
+    t["dequant_scale_q_nope"] = Fake((128, 128), torch.float32)
+    assert _status(_args(t))[0] == 2
+    t = _mla(w_int8=True)
+    t["query"] = Fake((128, 128, 512), torch.int8)        # int8 query outside full quant
+    assert _status(_args(t))[0] == 3
+    # full quant needs its own workspace regions (widened x, staged q^N)
+    assert _status(_args(_mla(w_int8=True, cache_int8=True, full=True)))[1] > \
+        _status(_args(_mla(w_int8=True, cache_int8=True)))[1]

@@ -7,7 +7,8 @@ import oracle
 import synthetic
 import qkv_attention_prolog_gb300 as pkg
 from oracle.mla_prolog import mla_key_rows, mla_prolog_tokens
-from tests.gpu_util import (assert_close, check_cache, f64, oracle_inputs, run_mla)
+from tests.gpu_util import (assert_close, assert_int8_close, check_cache, f64, oracle_inputs,
+                            run_mla)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,7 +25,12 @@ def _full_check(case, bsh=False):
     t, prolog, status = run_mla(cpu, d, case.eps, bsh=bsh)
     assert status == 0, f"kernel error status {status}"
     ref = oracle.mla_prolog(**oracle_inputs(cpu, case.eps))
-    assert_close(f64(t["query"]).reshape(d.T, d.N, d.Hckv), ref["query"], "query")
+    if t["query"].dtype == torch.int8:   # full quant: codes within 1 LSB, scales in tolerance
+        assert_int8_close(f64(t["query"]).reshape(d.T, d.N, d.Hckv), ref["query"], "query")
+        assert_close(f64(t["dequant_scale_q_nope"]).reshape(d.T, d.N), ref["dequant_scale_q_nope"],
+                     "dequant_scale_q_nope")
+    else:
+        assert_close(f64(t["query"]).reshape(d.T, d.N, d.Hckv), ref["query"], "query")
     assert_close(f64(t["query_rope"]).reshape(d.T, d.N, d.Dr), ref["query_rope"], "query_rope")
     idx = cpu["cache_index"].numpy()
     sub = mla_prolog_tokens(oracle_inputs(cpu, case.eps), np.arange(d.T))
@@ -183,3 +189,35 @@ def test_stream_k_schedule(case, monkeypatch):
     else:
         _full_check(synthetic.small_mla_case("cut7", B=40, S=1, He=256, Hcq=1536, N=16,
                                              block_num=2, n_skip=1))
+
+
+def test_full_quant_int8_cache():
+    # int8 token_x / W^DQ / W^DKV|W^KR (per-token, per-channel dequant), int8 kv_cache, bf16
+    # kr_cache, int8 query per token and head with dequant_scale_q_nope
+    _full_check(synthetic.MLA_FULL_QUANT)
+
+
+def test_full_quant_bf16_cache():
+    _full_check(synthetic.MLA_FULL_QUANT_BF16CACHE)
+
+
+FULL_QUANT_SHAPES = [
+    dict(B=5, S=1, He=256, Hcq=128, N=3, cache_dtype="int8"),              # decode orientation
+    dict(B=3, S=100, He=384, Hcq=192, Hckv=128, N=2, cache_dtype="int8"),   # prefill orientation
+    dict(B=2, S=150, He=256, Hcq=144, Hckv=96, N=2, Dr=32, cache_dtype="bf16"),
+]
+
+
+@pytest.mark.parametrize("kw", FULL_QUANT_SHAPES, ids=[str(i) for i in range(len(FULL_QUANT_SHAPES))])
+def test_full_quant_shapes(kw):
+    kw = dict(kw)
+    block_num = max(1, (kw["B"] * kw["S"] + 127) // 128 + 1)
+    case = synthetic.small_mla_case("fq", block_num=block_num, n_skip=1, full_quant=True,
+                                    weight_uq_qr_dtype="int8", **kw)
+    _full_check(case)
+
+
+def test_full_quant_bsh():
+    case = synthetic.small_mla_case("fq_bsh", B=4, S=5, N=2, block_num=1, full_quant=True,
+                                    weight_uq_qr_dtype="int8", cache_dtype="int8")
+    _full_check(case, bsh=True)
