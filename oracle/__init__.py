@@ -13,19 +13,20 @@ readings below fix.  Every function cites the passage of the operator documentat
   ("功能说明" formulas, "参数说明" parameter table, "约束说明" shape and scenario matrix);
 * "aclnnQkvRmsNormRopeCache" = the CANN API page of that name ("Formulas" (1)-(4),
   "Other restrictions");
-* "aclnnMlaPreprocessV2" = the CANN API page of that name (RmsNorm formula).
+* "aclnnMlaPreprocessV2" = the CANN API page of that name ("Formula": RMS, RmsNorm and the input
+  RmsNormQuant).
 
 Pins: every function here is pinned by ``tests/test_oracle_pins.py`` against closed forms,
 invariants, library routines for special cases and brute force on tiny inputs.  No function is
 left with parity unpinned.
 """
 from .rounding import round_bf16, round_fp16, round_fp32, saturate_int8_rne
-from .mla_prolog import (rms_norm, rope_half_and_half, dynamic_quant_per_token, cache_quant,
-                         mla_prolog, scatter_rows)
+from .mla_prolog import (rms_norm, rms_norm_quant, rope_half_and_half, dynamic_quant_per_token,
+                         cache_quant, mla_prolog, scatter_rows)
 from .qkv_rms_norm_rope_cache import qkv_rms_norm_rope_cache
 
 __all__ = [
-    "round_bf16", "round_fp16", "round_fp32", "saturate_int8_rne", "rms_norm",
+    "round_bf16", "round_fp16", "round_fp32", "saturate_int8_rne", "rms_norm", "rms_norm_quant",
     "rope_half_and_half", "dynamic_quant_per_token", "cache_quant", "mla_prolog",
     "scatter_rows", "qkv_rms_norm_rope_cache",
 ]

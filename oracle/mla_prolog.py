@@ -34,6 +34,13 @@ Readings where the pages are silent (each is also listed in the design notes):
   pages call that cache quant "pertensor" but give quant_scale_ckv the shape (1, Hckv); the
   shape is followed (one scale per channel, the cache-quant rule above); kr_cache stays bf16
   there ("无需赋值" for quant_scale_ckr).
+* Input RmsNormQuant (aclnnMlaPreprocessV2, "Formula", RmsNormQuant): when its parameters are
+  given, x is replaced ahead of the down-projection by (gamma * x / RMS(x) + bias) * deqScale,
+  RMS(x) = sqrt(mean over He of x^2 + epsilon).  Readings: gamma and bias are per hidden channel
+  (He) bf16 values, deqScale is float32 per channel (He) or one value for all channels; the
+  printed formula has no rounding to an integer grid, so the result is rounded to bf16, the type
+  of the down-projection's operand (the rounding-point rule above), and the step composes with
+  the bf16-x scenarios only (non-quant, partial quant).
 * cache_index: slot i goes to block i // BlockSize, row i % BlockSize (Nkv = 1); i = -1 skips the
   row (aclnnQkvRmsNormRopeCache, "Other restrictions"); other out-of-range values are skipped too
   (the CUDA path also flags them).
@@ -60,6 +67,17 @@ def rope_half_and_half(y: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.nd
     y1, y2 = y[..., :half], y[..., half:]
     rotated = np.concatenate([-y2, y1], axis=-1)
     return y * np.asarray(cos, np.float64) + rotated * np.asarray(sin, np.float64)
+
+
+def rms_norm_quant(x: np.ndarray, gamma: np.ndarray, bias: np.ndarray, deq_scale,
+                   eps: float) -> np.ndarray:
+    """(gamma * x / RMS(x) + bias) * deqScale along the last axis with RMS(x) = sqrt(mean(x^2) +
+    eps) (aclnnMlaPreprocessV2, "Formula": RMS, RmsNorm, RmsNormQuant).  float64, unrounded;
+    deq_scale is one value per channel or a single value."""
+    x = np.asarray(x, dtype=np.float64)
+    rms = np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    normed = np.asarray(gamma, np.float64).reshape(-1) * x / rms
+    return (normed + np.asarray(bias, np.float64).reshape(-1)) * np.asarray(deq_scale, np.float64).reshape(-1)
 
 
 def dynamic_quant_per_token(c_q: np.ndarray, smooth: np.ndarray):
@@ -118,7 +136,8 @@ def mla_prolog(token_x, weight_dq, weight_uq_qr, weight_uk, weight_dkv_kr,
                dequant_scale_w_uq_qr=None, smooth_scales_cq=None,
                quant_scale_ckv=None, quant_scale_ckr=None, dequant_scale_x=None,
                dequant_scale_w_dq=None, dequant_scale_w_dkv_kr=None,
-               query_int8: bool = False) -> dict:
+               query_int8: bool = False, rms_norm_quant_gamma=None, rms_norm_quant_bias=None,
+               rms_norm_quant_deq_scale=None, rms_norm_quant_epsilon=None) -> dict:
     """The whole prolog for T tokens.
 
     Inputs are numpy arrays holding the exact values of the operator inputs (bf16 values as
@@ -127,10 +146,14 @@ def mla_prolog(token_x, weight_dq, weight_uq_qr, weight_uk, weight_dkv_kr,
     (T,N,Dr) as float64 holding bf16 values, and the updated kv_cache / kr_cache (float64 bf16
     values, or int8 when the caches are quantised).  Full quant: token_x, weight_dq and
     weight_dkv_kr int8 with their dequant scales; query_int8 returns int8 query codes and
-    dequant_scale_q_nope (T, N).
+    dequant_scale_q_nope (T, N).  rms_norm_quant_*: the input RmsNormQuant of
+    aclnnMlaPreprocessV2 applied to token_x first (bf16 x only).
     """
     x_int8 = np.asarray(token_x).dtype == np.int8
     x = np.asarray(token_x, np.float64)
+    if rms_norm_quant_gamma is not None:           # x' = bf16((RmsNorm(x) + bias) * deqScale)
+        x = round_bf16(rms_norm_quant(x, rms_norm_quant_gamma, rms_norm_quant_bias,
+                                      rms_norm_quant_deq_scale, rms_norm_quant_epsilon))
     T, He = x.shape
     N, D, Hckv = weight_uk.shape
     Dr = np.asarray(rope_sin).shape[-1]
@@ -225,11 +248,16 @@ def mla_prolog_tokens(inputs: dict, token_ids) -> dict:
 def mla_key_rows(token_x, weight_dkv_kr, rmsnorm_gamma_ckv, rope_sin, rope_cos,
                  rmsnorm_epsilon_ckv, Hckv, kv_dtype_int8=False, kr_dtype_int8=False,
                  quant_scale_ckv=None, quant_scale_ckr=None, dequant_scale_x=None,
-                 dequant_scale_w_dkv_kr=None, **_unused) -> tuple:
+                 dequant_scale_w_dkv_kr=None, rms_norm_quant_gamma=None,
+                 rms_norm_quant_bias=None, rms_norm_quant_deq_scale=None,
+                 rms_norm_quant_epsilon=None, **_unused) -> tuple:
     """Only the key path of ``mla_prolog`` (c^KV = RmsNorm(x·W^DKV), k^R = ROPE(x·W^KR)), as the
     rows the cache would receive for every token: (kv_rows, kr_rows).  Same formulas and
     rounding as ``mla_prolog``; used to check every written cache slot of large workloads."""
     x = np.asarray(token_x, np.float64)
+    if rms_norm_quant_gamma is not None:
+        x = round_bf16(rms_norm_quant(x, rms_norm_quant_gamma, rms_norm_quant_bias,
+                                      rms_norm_quant_deq_scale, rms_norm_quant_epsilon))
     T = x.shape[0]
     Dr = np.asarray(rope_sin).shape[-1]
     sin = np.asarray(rope_sin, np.float64).reshape(T, Dr)

@@ -57,9 +57,11 @@ def rope_element(y, cos, sin, j):
 
 def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_cache, kr_cache,
                           eps_cq, eps_ckv, dqw=None, smooth=None, qs_ckv=None, qs_ckr=None,
-                          dsx=None, dsw_dq=None, dsw_dkv=None, query_int8=False):
+                          dsx=None, dsw_dq=None, dsw_dkv=None, query_int8=False, xg=None, xb=None,
+                          xd=None, eps_x=None):
     """All arguments are nested Python lists.  Returns dict of nested lists.  Full quant: x, wdq,
-    wdkv hold ints and dsx (T), dsw_dq (Hcq), dsw_dkv (Hckv+Dr) their dequant scales."""
+    wdkv hold ints and dsx (T), dsw_dq (Hcq), dsw_dkv (Hckv+Dr) their dequant scales.  xg, xb,
+    xd, eps_x: input RmsNormQuant gamma (He), bias (He), deqScale (He or one value), epsilon."""
     T, He = len(x), len(x[0])
     Hcq = len(wdq[0])
     N, D, Hckv = len(wuk), len(wuk[0]), len(wuk[0][0])
@@ -72,7 +74,12 @@ def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_c
     bs = len(kv_cache[0])
     scale_q = [[0.0] * N for _ in range(T)]
     for t in range(T):
-        hq = [sum(x[t][k] * wdq[k][c] for k in range(He)) for c in range(Hcq)]
+        xt = x[t]
+        if xg is not None:                    # (gamma*x/RMS(x) + bias) * deqScale, then bf16
+            rms_x = math.sqrt(sum(v * v for v in xt) / He + eps_x)
+            xt = [bf16((xg[k] * xt[k] / rms_x + xb[k]) * xd[k if len(xd) > 1 else 0])
+                  for k in range(He)]
+        hq = [sum(xt[k] * wdq[k][c] for k in range(He)) for c in range(Hcq)]
         if dsx is not None:                   # exact integer sums, dequantised
             hq = [hq[c] * dsx[t] * dsw_dq[c] for c in range(Hcq)]
         rms = math.sqrt(sum(v * v for v in hq) / Hcq + eps_cq)
@@ -105,7 +112,7 @@ def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_c
                 query[t][n] = [bf16(v) for v in qn]
             for j in range(Dr):
                 query_rope[t][n][j] = bf16(rope_element(r, cos[t], sin[t], j))
-        hkv = [sum(x[t][k] * wdkv[k][c] for k in range(He)) for c in range(Hckv + Dr)]
+        hkv = [sum(xt[k] * wdkv[k][c] for k in range(He)) for c in range(Hckv + Dr)]
         if dsx is not None:
             hkv = [hkv[c] * dsx[t] * dsw_dkv[c] for c in range(Hckv + Dr)]
         rms = math.sqrt(sum(v * v for v in hkv[:Hckv]) / Hckv + eps_ckv)

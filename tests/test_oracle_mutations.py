@@ -93,6 +93,31 @@ def test_full_quant_pins_catch_mutation(label, old, new):
     assert not same, f"mutation '{label}' not detected"
 
 
+XNORM_MUTATIONS = [
+    ("bias after deqScale", "return (normed + np.asarray(bias, np.float64).reshape(-1)) * np.asarray(deq_scale, np.float64).reshape(-1)",
+     "return normed * np.asarray(deq_scale, np.float64).reshape(-1) + np.asarray(bias, np.float64).reshape(-1)"),
+    ("x eps outside the root", "rms = np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)",
+     "rms = np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps * 1e3"),
+    ("x gamma dropped", "normed = np.asarray(gamma, np.float64).reshape(-1) * x / rms", "normed = x / rms"),
+    ("x' not rounded", "x = round_bf16(rms_norm_quant(x, rms_norm_quant_gamma, rms_norm_quant_bias,\n                                      rms_norm_quant_deq_scale, rms_norm_quant_epsilon))\n    T, He",
+     "x = rms_norm_quant(x, rms_norm_quant_gamma, rms_norm_quant_bias,\n                                      rms_norm_quant_deq_scale, rms_norm_quant_epsilon) * (1 + 2**-10)\n    T, He"),
+]
+
+
+@pytest.mark.parametrize("label,old,new", XNORM_MUTATIONS, ids=[m[0] for m in XNORM_MUTATIONS])
+def test_rms_norm_quant_pins_catch_mutation(label, old, new):
+    mod = _mutant("mla_prolog.py", old, new)
+    rng = np.random.default_rng(34)
+    inp = _tiny_mla(rng, xnorm="channel")
+    want = _brute(inp)
+    got = mod.mla_prolog(**inp)
+    same = True
+    for key in ("query", "query_rope", "kv_cache", "kr_cache"):
+        same &= np.allclose(np.asarray(got[key], np.float64), np.array(want[key], np.float64),
+                            rtol=1e-12, atol=1e-14)
+    assert not same, f"mutation '{label}' not detected"
+
+
 QKV_MUTATIONS = [
     ("split k/v swapped", "k, v = x[:, :Nq, :], x[:, Nq:Nq + Nk, :], x[:, Nq + Nk:, :]",
      "k, v = x[:, :Nq, :], x[:, Nq + Nk:, :], x[:, Nq:Nq + Nk, :]"),

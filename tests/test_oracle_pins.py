@@ -100,6 +100,34 @@ def test_rmsnorm_closed_forms():
     np.testing.assert_allclose(oracle.rms_norm(h, gam, 0.0), want, rtol=1e-13)
 
 
+def test_rms_norm_quant_golden():
+    for case in _golden("rms_norm_quant_worked.json")["cases"]:
+        y = oracle.rms_norm_quant(np.array(case["x"]), np.array(case["gamma"]),
+                                  np.array(case["bias"]), np.array(case["deq_scale"]), case["eps"])
+        np.testing.assert_allclose(y, case["y"], rtol=1e-15, atol=1e-15)
+
+
+def test_rms_norm_quant_closed_forms():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((6, 64))
+    gam, b = rng.uniform(0.5, 1.5, 64), rng.uniform(-1, 1, 64)
+    d = rng.uniform(0.5, 2.0, 64)
+    y = oracle.rms_norm_quant(x, gam, b, d, 0.0)
+    # invariant to positive scaling of the row when eps = 0
+    np.testing.assert_allclose(oracle.rms_norm_quant(x * 19.0, gam, b, d, 0.0), y, rtol=1e-13)
+    # bias 0 and deqScale 1: the textbook root-mean-square normalisation via the Euclidean norm
+    want = gam * x / (np.linalg.norm(x, axis=-1, keepdims=True) / math.sqrt(64))
+    np.testing.assert_allclose(oracle.rms_norm_quant(x, gam, np.zeros(64), np.ones(1), 0.0), want,
+                               rtol=1e-13)
+    # affine in the bias with slope deqScale, linear in deqScale
+    np.testing.assert_allclose(oracle.rms_norm_quant(x, gam, b + 0.25, d, 0.0) - y, 0.25 * d
+                               + 0 * y, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(oracle.rms_norm_quant(x, gam, b, 3.0 * d, 0.0), 3.0 * y, rtol=1e-13)
+    # one deqScale for all channels equals the same value repeated per channel
+    np.testing.assert_array_equal(oracle.rms_norm_quant(x, gam, b, np.array([1.5]), 1e-3),
+                                  oracle.rms_norm_quant(x, gam, b, np.full(64, 1.5), 1e-3))
+
+
 # ----------------------------------------------------------------------------- RoPE
 
 def test_rope_golden():
@@ -166,7 +194,7 @@ def test_dynamic_quant_properties():
 # ----------------------------------------------------------------------------- MLA prolog
 
 def _tiny_mla(rng, int8=False, int8_cache=False, T=3, He=8, Hcq=6, Hckv=5, N=2, D=4, Dr=4,
-              full=False):
+              full=False, xnorm=None):
     bfr = lambda *s: oracle.round_bf16(rng.standard_normal(s) * 0.5)
     inp = dict(
         token_x=bfr(T, He), weight_dq=bfr(He, Hcq), weight_uk=bfr(N, D, Hckv),
@@ -201,6 +229,12 @@ def _tiny_mla(rng, int8=False, int8_cache=False, T=3, He=8, Hcq=6, Hckv=5, N=2, 
     else:
         inp["kv_cache"] = bfr(3, 2, 1, Hckv)
         inp["kr_cache"] = bfr(3, 2, 1, Dr)
+    if xnorm is not None:   # input RmsNormQuant: "channel" deqScale per He channel, else one value
+        inp["rms_norm_quant_gamma"] = oracle.round_bf16(rng.uniform(0.5, 1.5, He))
+        inp["rms_norm_quant_bias"] = oracle.round_bf16(rng.uniform(-0.5, 0.5, He))
+        inp["rms_norm_quant_deq_scale"] = (rng.uniform(0.5, 2.0, He if xnorm == "channel" else 1)
+                                           .astype(np.float32))
+        inp["rms_norm_quant_epsilon"] = 1e-4
     return inp
 
 
@@ -222,15 +256,18 @@ def _brute(inp):
         dqw=f(inp.get("dequant_scale_w_uq_qr")), smooth=f(inp.get("smooth_scales_cq")),
         qs_ckv=f(inp.get("quant_scale_ckv")), qs_ckr=f(inp.get("quant_scale_ckr")),
         dsx=f(inp.get("dequant_scale_x")), dsw_dq=f(inp.get("dequant_scale_w_dq")),
-        dsw_dkv=f(inp.get("dequant_scale_w_dkv_kr")), query_int8=inp.get("query_int8", False))
+        dsw_dkv=f(inp.get("dequant_scale_w_dkv_kr")), query_int8=inp.get("query_int8", False),
+        xg=f(inp.get("rms_norm_quant_gamma")), xb=f(inp.get("rms_norm_quant_bias")),
+        xd=f(inp.get("rms_norm_quant_deq_scale")), eps_x=inp.get("rms_norm_quant_epsilon"))
 
 
-@pytest.mark.parametrize("int8,int8_cache,full", [(False, False, False), (True, False, False),
-                                                  (True, True, False), (True, False, True),
-                                                  (True, True, True)])
-def test_mla_prolog_matches_brute_force(int8, int8_cache, full):
-    rng = np.random.default_rng(11 + int8 + 2 * int8_cache + 4 * full)
-    inp = _tiny_mla(rng, int8, int8_cache, full=full)
+@pytest.mark.parametrize("int8,int8_cache,full,xnorm", [
+    (False, False, False, None), (True, False, False, None), (True, True, False, None),
+    (True, False, True, None), (True, True, True, None), (False, False, False, "channel"),
+    (True, True, False, "tensor")])
+def test_mla_prolog_matches_brute_force(int8, int8_cache, full, xnorm):
+    rng = np.random.default_rng(11 + int8 + 2 * int8_cache + 4 * full + 8 * (xnorm is not None))
+    inp = _tiny_mla(rng, int8, int8_cache, full=full, xnorm=xnorm)
     got = oracle.mla_prolog(**inp)
     want = _brute(inp)
     for key in ("query", "query_rope"):
