@@ -43,7 +43,8 @@ def _parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "tiny", "partial_quant", "qkv", "qkv_asym"])
+                    choices=["decode", "prefill", "tiny", "partial_quant", "full_quant", "xnorm",
+                             "qkv", "qkv_asym"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--timer-calls", type=int, default=200,
@@ -55,27 +56,35 @@ def _case(name):
     import synthetic
     return {"decode": synthetic.MLA_DECODE, "prefill": synthetic.MLA_PREFILL,
             "tiny": synthetic.MLA_TINY, "partial_quant": synthetic.MLA_PARTIAL_QUANT,
+            "full_quant": synthetic.MLA_FULL_QUANT, "xnorm": synthetic.MLA_XNORM,
             "qkv": synthetic.QKV_EPILOGUE, "qkv_asym": synthetic.QKV_EPILOGUE_ASYM}[name]
 
 
 # ------------------------------------------------------------------------------- byte/flop model
-def mla_model(d, w_int8=False, cache_int8=False):
-    """Algorithmic bytes and FLOPs per call and per kernel (each tensor read or written once)."""
+def mla_model(d, w_int8=False, cache_int8=False, full=False, xnorm=False):
+    """Algorithmic bytes and FLOPs per call and per kernel (each tensor read or written once).
+    full: full quant (int8 x and down weights; int8 kv_cache -> bf16 kr_cache, int8 query).
+    xnorm: the input RmsNormQuant, whose gamma, bias and deqScale (He each) are read once more
+    (its normalised x is an intermediate, like the K-split partials, and is not counted)."""
     T, He, Hcq, Hckv, N, D, Dr = d.T, d.He, d.Hcq, d.Hckv, d.N, d.D, d.Dr
     wb = 1 if w_int8 else 2
-    cb = 1 if cache_int8 else 2
+    db = 1 if full else 2                       # x and the down-projection weights
+    kvb = 1 if cache_int8 else 2
+    krb = 1 if cache_int8 and not full else 2
+    qb = 1 if cache_int8 and full else 2        # query
     tables = 2 * T * Dr * 2
+    xparams = He * (2 + 2 + 4) if xnorm else 0
     k = {}
-    k["down"] = {"bytes": He * (Hcq + Hckv + Dr) * 2 + T * He * 2,
+    k["down"] = {"bytes": He * (Hcq + Hckv + Dr) * db + T * He * db + xparams,
                  "flops": 2 * T * He * (Hcq + Hckv + Dr)}
-    k["norm_scatter"] = {"bytes": T * Hcq * 2 + T * (Hckv + Dr) * cb + tables, "flops": 0}
+    k["norm_scatter"] = {"bytes": T * Hcq * 2 + T * (Hckv * kvb + Dr * krb) + tables, "flops": 0}
     k["up"] = {"bytes": Hcq * N * (D + Dr) * wb + T * Hcq * 2 + T * N * D * 2 + T * N * Dr * 2
                + tables, "flops": 2 * T * Hcq * N * (D + Dr)}
-    k["absorb"] = {"bytes": N * D * Hckv * 2 + T * N * D * 2 + T * N * Hckv * 2,
+    k["absorb"] = {"bytes": N * D * Hckv * 2 + T * N * D * 2 + T * N * Hckv * qb,
                    "flops": 2 * T * N * D * Hckv}
-    path_bytes = (He * (Hcq + Hckv + Dr) * 2 + Hcq * N * (D + Dr) * wb + N * D * Hckv * 2
-                  + T * He * 2 + T * N * Hckv * 2 + T * N * Dr * 2 + T * (Hckv + Dr) * cb + tables
-                  + T * 8)
+    path_bytes = (He * (Hcq + Hckv + Dr) * db + Hcq * N * (D + Dr) * wb + N * D * Hckv * 2
+                  + T * He * db + T * N * Hckv * qb + T * N * Dr * 2 + T * (Hckv * kvb + Dr * krb)
+                  + tables + T * 8 + xparams)
     path_flops = sum(v["flops"] for v in k.values())
     return k, path_bytes, path_flops
 
@@ -220,6 +229,9 @@ def oracle_tokens_per_s(case, budget_s=12.0, sample_tokens=4):
                if isinstance(v, torch.Tensor)}
         inp["rmsnorm_epsilon_cq"] = case.eps
         inp["rmsnorm_epsilon_ckv"] = case.eps
+        inp["query_int8"] = case.full_quant and case.cache_dtype == "int8"
+        if case.x_norm is not None:
+            inp["rms_norm_quant_epsilon"] = case.eps
         ntok = min(case.dims.T, sample_tokens)
         ids = np.arange(ntok)
         call = lambda: mla_prolog_tokens(inp, ids)
@@ -251,11 +263,14 @@ def _mla_sets(case, dev, n_sets):
         t = {k: v.to(dev) for k, v in cpu.items() if isinstance(v, torch.Tensor)}
         t["query"] = torch.empty(d.T, d.N, d.Hckv, dtype=torch.bfloat16, device=dev)
         t["query_rope"] = torch.empty(d.T, d.N, d.Dr, dtype=torch.bfloat16, device=dev)
+        if case.full_quant and case.cache_dtype == "int8":   # int8 query per token and head
+            t["query"] = torch.empty(d.T, d.N, d.Hckv, dtype=torch.int8, device=dev)
+            t["dequant_scale_q_nope"] = torch.empty(d.T, d.N, 1, dtype=torch.float32, device=dev)
         packed = pkg.prepack_mla_weights({k: t.pop(k) for k in ("weight_dq", "weight_uq_qr",
                                                                 "weight_uk", "weight_dkv_kr")},
                                          d.N, d.D, d.Dr)
         t.update(packed)
-        a = pkg.make_mla_args(t, case.eps, case.eps)
+        a = pkg.make_mla_args(t, case.eps, case.eps, eps_x=case.eps)
         ws = torch.empty(pkg.mlap_get_workspace_size(a), dtype=torch.uint8, device=dev)
         pkg.mlap_workspace_init(ws)
         sets.append((t, a, ws))
@@ -281,13 +296,18 @@ def run_ours(args, rank, local, world):
     d = case.dims
     w_int8 = case.weight_uq_qr_dtype == "int8"
     c_int8 = case.cache_dtype == "int8"
-    kern, path_bytes, path_flops = mla_model(d, w_int8, c_int8)
+    kern, path_bytes, path_flops = mla_model(d, w_int8, c_int8, case.full_quant,
+                                             case.x_norm is not None)
+    # down, norm/scatter, up, absorb; full quant adds the token_x widening and, with an int8
+    # query, its per-token-head quantisation; the input RmsNormQuant adds its own kernel
+    launches_per_call = (4 + (1 + c_int8 if case.full_quant else 0)
+                         + (1 if case.x_norm is not None else 0))
     n_sets = max(1, math.ceil(3 * L2_BYTES / path_bytes) + 1) if path_bytes < 2 * L2_BYTES else 1
     cpu, sets = _mla_sets(case, dev, n_sets)
     stream = torch.cuda.Stream(dev)
 
     steps = args.steps or {"decode": 40000, "tiny": 40000, "partial_quant": 40000,
-                           "prefill": 1500}[args.workload]
+                           "full_quant": 40000, "xnorm": 40000, "prefill": 1500}[args.workload]
     warm = max(3, args.warmup)
     with torch.cuda.stream(stream):
         for i in range(warm):
@@ -374,13 +394,15 @@ def run_ours(args, rank, local, world):
             "config": {"workload": case.name, "T": d.T, "B": d.B, "S": d.S, "He": d.He,
                        "Hcq": d.Hcq, "Hckv": d.Hckv, "N": d.N, "D": d.D, "Dr": d.Dr,
                        "weight_uq_qr": case.weight_uq_qr_dtype, "caches": case.cache_dtype,
+                       "token_x_and_down_weights": "int8" if case.full_quant else "bf16",
+                       "input_rms_norm_quant": case.x_norm,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": (f"rotating {n_sets} input sets of {path_bytes/1e6:.1f} MB "
                               f"({n_sets*path_bytes/1e6:.0f} MB > 129 MB L2)" if n_sets > 1
                               else f"inputs {path_bytes/1e6:.0f} MB > 129 MB L2"),
                        "timing": f"CUDA graph of {per_graph} execute calls replayed {replays}x"},
             "roofline": roof, "path_roofline": path_roof, "clocks": clk.summary(),
-            "e2e": e2e, "gpu_launches": 4 * steps}
+            "e2e": e2e, "gpu_launches": launches_per_call * steps}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_tokens_per_s(case)
         line["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": cores,
@@ -397,7 +419,7 @@ def run_e2e(args, case, cpu, s0, dev, stream):
     per_call_in = ["token_x", "rope_sin", "rope_cos", "cache_index"]
     host_in = {k: cpu[k].pin_memory() for k in per_call_in}
     host_out = {k: torch.empty(t[k].shape, dtype=t[k].dtype).pin_memory()
-                for k in ("query", "query_rope")}
+                for k in ("query", "query_rope", "dequant_scale_q_nope") if k in t}
     bi = sum(v.numel() * v.element_size() for v in host_in.values())
     bo = sum(v.numel() * v.element_size() for v in host_out.values())
     steps = max(3, args.e2e_steps)

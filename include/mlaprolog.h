@@ -22,6 +22,13 @@
  *     returned by mlap_check_errors().
  *   - A status other than MLAP_OK leaves outputs and caches untouched (nothing is launched) and
  *     sets a human-readable reason retrievable with mlap_last_error() (thread-local).
+ *   - The kernels of a call use programmatic dependent launch: each may start while the kernel
+ *     before it in the stream is finishing and read the inputs it only reads (weights, RoPE
+ *     tables, norm parameters and scales) before it waits for that kernel.  A caller's own kernel
+ *     that immediately precedes a call in the stream and itself triggers programmatic dependent
+ *     launch (griddepcontrol.launch_dependents) must therefore not write those inputs; any other
+ *     preceding stream work (copies, kernels without that trigger) is complete before the call's
+ *     first kernel starts.
  */
 #ifndef MLAPROLOG_H
 #define MLAPROLOG_H
@@ -77,16 +84,32 @@ typedef enum {
  *   partial quant, kv quant:     as above, plus kv_cache/kr_cache int8 with quant_scale_ckv
  *                                (1, Hckv) and quant_scale_ckr (1, Dr) fp32 (value / scale,
  *                                round half to even, saturate to [-128, 127]).
- *   full quant:                  not implemented (MLAP_ERR_UNSUPPORTED).
+ *   full quant:                  token_x int8 with dequant_scale_x (T, 1) fp32; weight_dq and
+ *                                weight_dkv_kr int8 with dequant_scale_w_dq (1, Hcq) and
+ *                                dequant_scale_w_dkv_kr (1, Hckv+Dr) fp32 (the integer products are
+ *                                dequantised as acc * scale_x[t] * scale_w[column]); weight_uq_qr
+ *                                int8 as in partial quant; kr_cache bf16.  With an int8 kv_cache
+ *                                (quant_scale_ckv (1, Hckv)) the query is int8 per token and head
+ *                                (scale = amax/127, written to dequant_scale_q_nope (T, N, 1));
+ *                                with a bf16 kv_cache the query is bf16.
  * dequant_scale_x, dequant_scale_w_dq, dequant_scale_w_dkv_kr are reserved outside full quant
- * and must be absent (data == NULL), else MLAP_ERR_UNSUPPORTED. */
+ * and must be absent (data == NULL), else MLAP_ERR_UNSUPPORTED.
+ *
+ * Input RmsNormQuant (aclnnMlaPreprocessV2, "Formula": RMS, RmsNorm, RmsNormQuant), optional:
+ * with rms_norm_quant_gamma, _bias and _deq_scale present (all three or none), every token row
+ * of token_x is replaced ahead of the down-projection by
+ *     x'[t, k] = bf16((gamma[k] * x[t, k] / RMS(x[t]) + bias[k]) * deqScale[k]),
+ *     RMS(x[t]) = sqrt(mean over k of x[t, k]^2 + rms_norm_quant_epsilon),
+ * computed in fp32 (one value of deqScale may serve every channel).  It composes with the
+ * bf16-token_x scenarios only (non-quant, partial quant); with full quant the call returns
+ * MLAP_ERR_UNSUPPORTED.  token_x itself is only read. */
 typedef struct {
-  mlap_tensor_t token_x;            /* bf16 (T, He) or (B, S, He) */
-  mlap_tensor_t weight_dq;          /* prepacked W^DQ; logical shape (He, Hcq) bf16 */
+  mlap_tensor_t token_x;            /* bf16|int8 (T, He) or (B, S, He) */
+  mlap_tensor_t weight_dq;          /* prepacked W^DQ; logical shape (He, Hcq) bf16|int8 */
   mlap_tensor_t weight_uq_qr;       /* prepacked [W^UQ|W^QR]; logical (Hcq, N*(D+Dr)) bf16|int8,
                                        columns per head n: [D nope | Dr rope] */
   mlap_tensor_t weight_uk;          /* prepacked W^UK; logical (N, D, Hckv) bf16 */
-  mlap_tensor_t weight_dkv_kr;      /* prepacked [W^DKV|W^KR]; logical (He, Hckv+Dr) bf16 */
+  mlap_tensor_t weight_dkv_kr;      /* prepacked [W^DKV|W^KR]; logical (He, Hckv+Dr) bf16|int8 */
   mlap_tensor_t rmsnorm_gamma_cq;   /* bf16 (Hcq) */
   mlap_tensor_t rmsnorm_gamma_ckv;  /* bf16 (Hckv) */
   mlap_tensor_t rope_sin;           /* bf16 (T, Dr) or (B, S, Dr), half-and-half layout */
@@ -94,18 +117,24 @@ typedef struct {
   mlap_tensor_t cache_index;        /* int64 (T) or (B, S); -1 = do not store this token */
   mlap_tensor_t kv_cache;           /* in/out (BlockNum, BlockSize, 1, Hckv) bf16|int8 */
   mlap_tensor_t kr_cache;           /* in/out (BlockNum, BlockSize, 1, Dr) bf16|int8 */
-  mlap_tensor_t dequant_scale_x;        /* reserved: must be absent */
-  mlap_tensor_t dequant_scale_w_dq;     /* reserved: must be absent */
-  mlap_tensor_t dequant_scale_w_uq_qr;  /* fp32 (1, N*(D+Dr)), partial quant only */
-  mlap_tensor_t dequant_scale_w_dkv_kr; /* reserved: must be absent */
+  mlap_tensor_t dequant_scale_x;        /* fp32 (T, 1) or (B*S, 1), full quant only */
+  mlap_tensor_t dequant_scale_w_dq;     /* fp32 (1, Hcq), full quant only */
+  mlap_tensor_t dequant_scale_w_uq_qr;  /* fp32 (1, N*(D+Dr)), partial and full quant */
+  mlap_tensor_t dequant_scale_w_dkv_kr; /* fp32 (1, Hckv+Dr), full quant only */
   mlap_tensor_t quant_scale_ckv;        /* fp32 (1, Hckv), int8 kv_cache only */
   mlap_tensor_t quant_scale_ckr;        /* fp32 (1, Dr), int8 kr_cache only */
-  mlap_tensor_t smooth_scales_cq;       /* fp32 (1, Hcq), partial quant only */
-  mlap_tensor_t query;              /* out bf16 (T, N, Hckv) or (B, S, N, Hckv) = q^N */
+  mlap_tensor_t smooth_scales_cq;       /* fp32 (1, Hcq), partial and full quant */
+  mlap_tensor_t query;              /* out (T, N, Hckv) or (B, S, N, Hckv) = q^N; bf16, or int8
+                                       in full quant with an int8 kv_cache */
   mlap_tensor_t query_rope;         /* out bf16 (T, N, Dr) or (B, S, N, Dr) = q^R */
-  mlap_tensor_t dequant_scale_q_nope; /* out, full quant only; may be absent, never written */
+  mlap_tensor_t dequant_scale_q_nope; /* out fp32 (T, N, 1) or (B*S, N, 1) with an int8 query;
+                                         otherwise may be absent and is never written */
+  mlap_tensor_t rms_norm_quant_gamma;     /* optional bf16 (He): input RmsNormQuant gamma */
+  mlap_tensor_t rms_norm_quant_bias;      /* optional bf16 (He): input RmsNormQuant bias */
+  mlap_tensor_t rms_norm_quant_deq_scale; /* optional fp32 (He) or (1): input RmsNormQuant deqScale */
   double rmsnorm_epsilon_cq;
   double rmsnorm_epsilon_ckv;
+  double rms_norm_quant_epsilon;    /* input RmsNormQuant epsilon (>= 0; read when it is on) */
   const char* cache_mode;           /* NULL or "PA_BSND" (ND paged cache); others unsupported */
 } mlap_args_t;
 
@@ -220,7 +249,9 @@ const char* mlap_last_error(void);
  * mlap_execute_timed is mlap_execute plus event records (it inserts no synchronisation);
  * mlap_timer_read synchronises, writes the milliseconds of kernel k of call c to
  * ms[c * MLAP_TIMER_PHASES + k] for the calls recorded so far, and resets the timer.
- * Phases: 0 down-projection, 1 RmsNorm/RoPE/scatter, 2 up-projection, 3 absorb. */
+ * Phases: 0 down-projection (with the input RmsNormQuant or the full-quant token_x widening
+ * ahead of it when those run), 1 RmsNorm/RoPE/scatter, 2 up-projection, 3 absorb (with the int8
+ * query quantisation after it in full quant). */
 #define MLAP_TIMER_PHASES 4
 mlap_status_t mlap_timer_create(void** timer, int32_t max_calls);
 mlap_status_t mlap_execute_timed(const mlap_args_t* args, void* workspace,
@@ -245,7 +276,8 @@ mlap_status_t mlap_timer_destroy(void* timer);
  * routine).
  *   - Shapes whose workspace (mlap_get_workspace_size) exceeds MLAP_NO_ALLOC_SCRATCH_BYTES are
  *     rejected with MLAP_ERR_WORKSPACE before any device work.  With the decode shapes
- *     (He 7168, Hcq 1536, Hckv 512, N 128, D 128, Dr 64) calls with T <= 128 or
+ *     (He 7168, Hcq 1536, Hckv 512, N 128, D 128, Dr 64) in the non-quant scenario without
+ *     the input RmsNormQuant (which adds T * He * 2 bytes, as full quant does), calls with T <= 128 or
  *     257 <= T <= 567 tokens fit (up to 256 tokens the down-projection keeps up to 16 K-split
  *     partials, above that one).
  *   - The first call on each device looks up the array's device address with that device

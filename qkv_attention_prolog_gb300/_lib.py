@@ -52,13 +52,15 @@ _MLA_TENSORS = ["token_x", "weight_dq", "weight_uq_qr", "weight_uk", "weight_dkv
                 "kv_cache", "kr_cache", "dequant_scale_x", "dequant_scale_w_dq",
                 "dequant_scale_w_uq_qr", "dequant_scale_w_dkv_kr", "quant_scale_ckv",
                 "quant_scale_ckr", "smooth_scales_cq", "query", "query_rope",
-                "dequant_scale_q_nope"]
+                "dequant_scale_q_nope", "rms_norm_quant_gamma", "rms_norm_quant_bias",
+                "rms_norm_quant_deq_scale"]
 
 
 class mlap_args_t(ctypes.Structure):
     _fields_ = ([(n, mlap_tensor_t) for n in _MLA_TENSORS]
                 + [("rmsnorm_epsilon_cq", ctypes.c_double),
-                   ("rmsnorm_epsilon_ckv", ctypes.c_double), ("cache_mode", ctypes.c_char_p)])
+                   ("rmsnorm_epsilon_ckv", ctypes.c_double),
+                   ("rms_norm_quant_epsilon", ctypes.c_double), ("cache_mode", ctypes.c_char_p)])
 
 
 _QKV_TENSORS = ["qkv", "gamma_q", "gamma_k", "cos", "sin", "index", "k_cache", "v_cache",
@@ -190,15 +192,19 @@ def prepack(w: torch.Tensor, which: int, N=0, D=0, Dr=0, stream=None) -> PackedW
     return PackedWeight(mlap_prepack_weights(w, which, N, D, Dr, stream), w.shape, w.dtype)
 
 
-def make_mla_args(tensors: dict, eps_cq=1e-6, eps_ckv=1e-6, cache_mode=None) -> mlap_args_t:
+def make_mla_args(tensors: dict, eps_cq=1e-6, eps_ckv=1e-6, cache_mode=None,
+                  eps_x=None) -> mlap_args_t:
     """Fill mlap_args_t from a dict keyed by the parameter-table names; weights may be
-    PackedWeight.  Missing optional keys are absent."""
+    PackedWeight.  Missing optional keys are absent.  eps_x (the input RmsNormQuant epsilon)
+    defaults to tensors["rms_norm_quant_epsilon"] when that key is present, else 1e-6."""
     a = mlap_args_t()
     for name in _MLA_TENSORS:
         v = tensors.get(name)
         setattr(a, name, v.desc() if isinstance(v, PackedWeight) else tensor_desc(v))
     a.rmsnorm_epsilon_cq = float(eps_cq)
     a.rmsnorm_epsilon_ckv = float(eps_ckv)
+    a.rms_norm_quant_epsilon = float(tensors.get("rms_norm_quant_epsilon", 1e-6) if eps_x is None
+                                     else eps_x)
     a.cache_mode = cache_mode.encode() if cache_mode else None
     return a
 

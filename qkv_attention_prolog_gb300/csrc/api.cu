@@ -95,6 +95,8 @@ struct MlaDims {
   bool w_int8, kv_int8, kr_int8;
   bool full;         // full quant: int8 token_x, W^DQ and W^DKV|W^KR (with dequant scales)
   bool query_int8;   // full quant with int8 kv_cache: int8 query + dequant_scale_q_nope
+  bool xnorm;        // input RmsNormQuant ahead of the down-projection
+  bool xnorm_deq_per_channel;
 };
 
 constexpr int kSwapMaxT = 256;   // decode orientation (weights as MMA rows) up to this many tokens
@@ -289,6 +291,31 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
   if ((!d->kv_int8 && present(a->quant_scale_ckv)) || (!d->kr_int8 && present(a->quant_scale_ckr))) {
     return fail(MLAP_ERR_UNSUPPORTED, "quant_scale_ckv / quant_scale_ckr need int8 caches");
   }
+  // input RmsNormQuant (aclnnMlaPreprocessV2 "Formula"): all three parameters or none
+  const int xn = present(a->rms_norm_quant_gamma) + present(a->rms_norm_quant_bias) +
+                 present(a->rms_norm_quant_deq_scale);
+  d->xnorm = xn == 3;
+  d->xnorm_deq_per_channel = false;
+  if (xn != 0 && xn != 3)
+    return fail(MLAP_ERR_NULL, "rms_norm_quant_gamma, _bias and _deq_scale are given together or not at all");
+  if (d->xnorm) {
+    if (d->full) return fail(MLAP_ERR_UNSUPPORTED, "the input RmsNormQuant needs a bf16 token_x (not full quant)");
+    if (d->He > 10240) return fail(MLAP_ERR_UNSUPPORTED, "the input RmsNormQuant supports He <= 10240");
+    CHECK_STATUS(need(a->rms_norm_quant_gamma, "rms_norm_quant_gamma", false));
+    CHECK_STATUS(want_dtype(a->rms_norm_quant_gamma, "rms_norm_quant_gamma", MLAP_DTYPE_BF16));
+    CHECK_STATUS(want_shape(a->rms_norm_quant_gamma, "rms_norm_quant_gamma", {d->He}));
+    CHECK_STATUS(need(a->rms_norm_quant_bias, "rms_norm_quant_bias", false));
+    CHECK_STATUS(want_dtype(a->rms_norm_quant_bias, "rms_norm_quant_bias", MLAP_DTYPE_BF16));
+    CHECK_STATUS(want_shape(a->rms_norm_quant_bias, "rms_norm_quant_bias", {d->He}));
+    const mlap_tensor_t& dq = a->rms_norm_quant_deq_scale;
+    CHECK_STATUS(need(dq, "rms_norm_quant_deq_scale", false));
+    CHECK_STATUS(want_dtype(dq, "rms_norm_quant_deq_scale", MLAP_DTYPE_FP32));
+    if (dq.ndim == 1 && dq.shape[0] == d->He) d->xnorm_deq_per_channel = true;
+    else if (!(dq.ndim == 1 && dq.shape[0] == 1))
+      return fail(MLAP_ERR_SHAPE, "rms_norm_quant_deq_scale must be (He) or (1)");
+    if (!(a->rms_norm_quant_epsilon >= 0.0))
+      return fail(MLAP_ERR_SHAPE, "rms_norm_quant_epsilon must be non-negative");
+  }
   if (a->cache_mode != nullptr && std::strcmp(a->cache_mode, "PA_BSND") != 0)
     return fail(MLAP_ERR_UNSUPPORTED, std::string("cache_mode '") + a->cache_mode + "' not supported (PA_BSND only)");
   if (!(a->rmsnorm_epsilon_cq >= 0.0) || !(a->rmsnorm_epsilon_ckv >= 0.0))
@@ -326,8 +353,9 @@ MlaWs mla_ws_layout(const MlaDims& d) {
   off += align_up(static_cast<size_t>(d.T) * d.N * d.D * 2, 256);
   w.scale = off;
   off += align_up(static_cast<size_t>(d.T) * 4, 256);
-  w.xb = off;   // full quant: token_x widened to bf16 (exact) for the down-projection
-  if (d.full) off += align_up(static_cast<size_t>(d.T) * d.He * 2, 256);
+  w.xb = off;   // the down-projection's bf16 operand when it is not token_x itself: token_x
+                // widened (full quant) or after the input RmsNormQuant
+  if (d.full || d.xnorm) off += align_up(static_cast<size_t>(d.T) * d.He * 2, 256);
   w.qn = off;   // int8 query: q^N in bf16 before the per-token-head quant
   if (d.query_int8) off += align_up(static_cast<size_t>(d.T) * d.N * d.Hckv * 2, 256);
   w.total = off;
@@ -493,7 +521,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   // full quant: the int8 activation is widened to bf16 first (exact), the int8 weights are
   // expanded in shared memory by the GEMM's converter warps, and the integer products are
   // dequantised per token and column after the K-split sum (norm kernel)
-  const void* xact = d.full ? static_cast<const void*>(wsb + L.xb) : a->token_x.data;
+  const void* xact = d.full || d.xnorm ? static_cast<const void*>(wsb + L.xb) : a->token_x.data;
   g.a_int8 = d.full;
   auto wmap = [&](CUtensorMap* m, const void* w, int64_t rows, int box) {
     return d.full ? make_tmap_i8(m, w, d.He, rows, box) : make_tmap(m, w, d.He, rows, d.He, box);
@@ -551,6 +579,17 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                               CU_TENSOR_MAP_SWIZZLE_128B));
     g.grid = balanced_grid(g.geo.num_units, sms);
     CHECK_STATUS(rec(0));
+    if (d.xnorm) {
+      ce = launch_rms_norm_quant(static_cast<const __nv_bfloat16*>(a->token_x.data),
+                                 static_cast<const __nv_bfloat16*>(a->rms_norm_quant_gamma.data),
+                                 static_cast<const __nv_bfloat16*>(a->rms_norm_quant_bias.data),
+                                 static_cast<const float*>(a->rms_norm_quant_deq_scale.data),
+                                 d.xnorm_deq_per_channel,
+                                 static_cast<float>(a->rms_norm_quant_epsilon),
+                                 reinterpret_cast<__nv_bfloat16*>(wsb + L.xb), d.T,
+                                 static_cast<int32_t>(d.He), stream);
+      if (ce != cudaSuccess) return cuda_fail(ce, "input RmsNormQuant launch");
+    }
     if (d.full) {
       ce = launch_widen_int8(static_cast<const int8_t*>(a->token_x.data),
                              reinterpret_cast<__nv_bfloat16*>(wsb + L.xb), d.T * d.He, stream);

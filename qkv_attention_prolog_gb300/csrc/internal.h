@@ -60,6 +60,15 @@ struct FinalizeParams {
 };
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl);
 
+// Input RmsNormQuant ahead of the down-projection: out[t] = bf16((gamma * x[t] / RMS(x[t]) + bias)
+// * deq) for T rows of He bf16 values (He a multiple of 8, at most 10240); deq holds He values, or
+// one value for every channel when deq_per_channel is false.  Launched with programmatic
+// dependent launch (waits for the preceding kernel before reading).
+cudaError_t launch_rms_norm_quant(const __nv_bfloat16* x, const __nv_bfloat16* gamma,
+                                  const __nv_bfloat16* bias, const float* deq, bool deq_per_channel,
+                                  float eps, __nv_bfloat16* out, int64_t T, int32_t He,
+                                  cudaStream_t stream);
+
 // Full quant: int8 token_x widened to bf16 (exact), n elements (a multiple of 16).
 cudaError_t launch_widen_int8(const int8_t* x, __nv_bfloat16* out, int64_t n, cudaStream_t stream);
 

@@ -13,6 +13,7 @@
 //   cache_index = -1 skips the token; other values outside [0, slots) are skipped and latched.
 //   full quant: h *= dequant_scale_x[t] * dequant_scale_w[column] after the split sum (the int8
 //   products are exact), and the two helper kernels below (token_x widening, int8 query).
+// rms_norm_quant_kernel: the optional input RmsNormQuant that runs ahead of the down-projection.
 // With Nkv = 1 and a dense (BlockNum, BlockSize, 1, H) cache, slot i is row i of the cache.
 #include "internal.h"
 
@@ -243,6 +244,7 @@ __global__ void prepack_kernel(const PrepackParams p) {
 // Full quant: 16 int8 values -> 16 bf16 per thread and step (exact: |v| <= 128).
 __global__ void widen_int8_kernel(const int8_t* __restrict__ x, __nv_bfloat16* __restrict__ out,
                                   int64_t n16) {
+  grid_dependency_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint4 raw = reinterpret_cast<const uint4*>(x)[i];
@@ -253,6 +255,7 @@ __global__ void widen_int8_kernel(const int8_t* __restrict__ x, __nv_bfloat16* _
     store8_bf16(out + i * 16, f);
     store8_bf16(out + i * 16 + 8, f + 8);
   }
+  grid_launch_dependents();   // after this thread's loads: the next grid's prefetch waits for them
 }
 
 // int8 query per token and head (MlaPrologV2 README scenario matrix: query INT8 "pertoken_head"
@@ -262,6 +265,7 @@ __global__ void query_quant_kernel(const __nv_bfloat16* __restrict__ qn, int8_t*
                                    float* __restrict__ scale, int64_t rows, int32_t H) {
   const int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  grid_dependency_wait();                         // q^N comes from the absorb GEMM
   if (row >= rows) return;                        // warp-uniform
   const __nv_bfloat16* src = qn + row * H;
   float amax = 0.f;
@@ -273,6 +277,7 @@ __global__ void query_quant_kernel(const __nv_bfloat16* __restrict__ qn, int8_t*
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  grid_launch_dependents();
   const float sc = __fdiv_rn(amax, 127.0f);
   int8_t* dst = q + row * H;
   for (int c = lane * 8; c < H; c += 256) {
@@ -287,7 +292,116 @@ __global__ void query_quant_kernel(const __nv_bfloat16* __restrict__ qn, int8_t*
   if (lane == 0) scale[row] = sc;
 }
 
+// Input RmsNormQuant (aclnnMlaPreprocessV2, "Formula": RMS, RmsNorm, RmsNormQuant), one CTA per
+// token: x'[k] = bf16((gamma[k] * x[k] / RMS(x) + bias[k]) * deqScale[k]) with RMS(x) =
+// sqrt(mean(x^2) + eps), all in fp32.  The row stays in registers between the sum of squares and
+// the store: NV 16-byte vectors per thread cover He <= 8 * NT * NV.  PRE (few tokens) also holds
+// gamma, bias and deqScale in registers, read before the wait on the preceding kernel; without it
+// (many tokens) the kernel stays small enough for several CTAs per SM and reads them after the
+// reduction.  The dependent down-projection is released once this CTA's row has arrived: an
+// earlier release lets its weight prefetch queue ahead of these loads in DRAM.
+template <int NT, int NV, bool PRE>
+__global__ void __launch_bounds__(NT) rms_norm_quant_kernel(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
+    const __nv_bfloat16* __restrict__ bias, const float* __restrict__ deq, int deq_per_channel,
+    float eps, __nv_bfloat16* __restrict__ out, int32_t He) {
+  __shared__ float2 red[NT / 32];
+  const int nvec = He >> 3;
+  auto load_params = [&](int i, float* g, float* b, float* d) {
+    load8_bf16(gamma + i * 8, g);
+    load8_bf16(bias + i * 8, b);
+    if (deq_per_channel) {
+      const float4 d0 = __ldg(reinterpret_cast<const float4*>(deq) + 2 * i);
+      const float4 d1 = __ldg(reinterpret_cast<const float4*>(deq) + 2 * i + 1);
+      d[0] = d0.x; d[1] = d0.y; d[2] = d0.z; d[3] = d0.w;
+      d[4] = d1.x; d[5] = d1.y; d[6] = d1.z; d[7] = d1.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) d[k] = __ldg(deq);
+    }
+  };
+  constexpr int NP = PRE ? NV : 1;
+  float g[NP][8], b[NP][8], d[NP][8];
+  if constexpr (PRE) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+      if (threadIdx.x + v * NT < nvec) load_params(threadIdx.x + v * NT, g[v], b[v], d[v]);
+  }
+  grid_dependency_wait();
+  const uint4* row = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.x) * He);
+  uint4 raw[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int i = threadIdx.x + v * NT;
+    if (i < nvec) raw[v] = __ldg(row + i);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if (threadIdx.x + v * NT < nvec) {
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[v]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float f = __bfloat162float(e[k]);
+        ss += f * f;
+      }
+    }
+  }
+  const float2 tot = block_sum2<NT>(make_float2(ss, 0.f), red);
+  grid_launch_dependents();
+  const float r = 1.0f / sqrtf(tot.x / static_cast<float>(He) + eps);
+  __nv_bfloat16* dst = out + static_cast<size_t>(blockIdx.x) * He;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int i = threadIdx.x + v * NT;
+    if (i < nvec) {
+      const int p = PRE ? v : 0;
+      if constexpr (!PRE) load_params(i, g[0], b[0], d[0]);
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[v]);
+      float y[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) y[k] = (g[p][k] * (__bfloat162float(e[k]) * r) + b[p][k]) * d[p][k];
+      store8_bf16(dst + i * 8, y);
+    }
+  }
+}
+
+constexpr int kXnMaxHe = 10240;   // 8 * 256 * 5 = 8 * 128 * 10
+constexpr int kXnFewTokens = 512;
+
+// A launch with programmatic stream serialization: the kernel may start while the preceding
+// kernel in the stream finishes and waits for it with griddepcontrol.wait.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 }  // namespace
+
+cudaError_t launch_rms_norm_quant(const __nv_bfloat16* x, const __nv_bfloat16* gamma,
+                                  const __nv_bfloat16* bias, const float* deq, bool deq_per_channel,
+                                  float eps, __nv_bfloat16* out, int64_t T, int32_t He,
+                                  cudaStream_t stream) {
+  if ((He % 8) || He > kXnMaxHe) return cudaErrorInvalidValue;
+  if (T < 1) return cudaSuccess;
+  const int dpc = deq_per_channel ? 1 : 0;
+  const dim3 grid(static_cast<unsigned>(T));
+  if (T <= kXnFewTokens)
+    return launch_pdl(rms_norm_quant_kernel<256, 5, true>, grid, dim3(256), stream, x, gamma,
+                      bias, deq, dpc, eps, out, He);
+  return launch_pdl(rms_norm_quant_kernel<128, 10, false>, grid, dim3(128), stream, x, gamma, bias,
+                    deq, dpc, eps, out, He);
+}
 
 cudaError_t launch_widen_int8(const int8_t* x, __nv_bfloat16* out, int64_t n, cudaStream_t stream) {
   if (n % 16) return cudaErrorInvalidValue;
@@ -295,8 +409,8 @@ cudaError_t launch_widen_int8(const int8_t* x, __nv_bfloat16* out, int64_t n, cu
   int64_t blocks = (n16 + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
-  widen_int8_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, out, n16);
-  return cudaGetLastError();
+  return launch_pdl(widen_int8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), stream, x,
+                    out, n16);
 }
 
 cudaError_t launch_query_quant(const __nv_bfloat16* qn, int8_t* q, float* scale, int64_t rows,
@@ -304,8 +418,8 @@ cudaError_t launch_query_quant(const __nv_bfloat16* qn, int8_t* q, float* scale,
   if (H % 8) return cudaErrorInvalidValue;
   const int64_t blocks = (rows * 32 + 255) / 256;
   if (blocks < 1) return cudaSuccess;
-  query_quant_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(qn, q, scale, rows, H);
-  return cudaGetLastError();
+  return launch_pdl(query_quant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), stream, qn,
+                    q, scale, rows, H);
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {

@@ -30,10 +30,10 @@ class MlaProlog:
         self.packed = prepack_mla_weights(weights, N, D, Dr, stream)
         self.ws = None
 
-    def args(self, tensors: dict, eps_cq=1e-6, eps_ckv=1e-6, cache_mode=None):
+    def args(self, tensors: dict, eps_cq=1e-6, eps_ckv=1e-6, cache_mode=None, eps_x=None):
         merged = dict(tensors)
         merged.update(self.packed)
-        return _lib.make_mla_args(merged, eps_cq, eps_ckv, cache_mode)
+        return _lib.make_mla_args(merged, eps_cq, eps_ckv, cache_mode, eps_x)
 
     def ensure_workspace(self, args, device) -> torch.Tensor:
         need = _lib.mlap_get_workspace_size(args)
@@ -42,8 +42,10 @@ class MlaProlog:
             _lib.mlap_workspace_init(self.ws)
         return self.ws
 
-    def run(self, tensors: dict, eps_cq=1e-6, eps_ckv=1e-6, cache_mode=None, stream=None):
-        a = self.args(tensors, eps_cq, eps_ckv, cache_mode)
+    def run(self, tensors: dict, eps_cq=1e-6, eps_ckv=1e-6, cache_mode=None, stream=None,
+            eps_x=None):
+        """eps_x: epsilon of the input RmsNormQuant (used when its parameters are present)."""
+        a = self.args(tensors, eps_cq, eps_ckv, cache_mode, eps_x)
         ws = self.ensure_workspace(a, tensors["token_x"].device)
         _lib.mlap_execute(a, ws, stream)
         return a

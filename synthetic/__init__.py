@@ -58,6 +58,9 @@ class MlaCase:
     # (weight_uq_qr_dtype must be "int8"); with cache_dtype "int8" only kv_cache is int8 and
     # the query is int8 per token and head
     full_quant: bool = False
+    # input RmsNormQuant (aclnnMlaPreprocessV2) ahead of the down-projection: None (off),
+    # "channel" (deqScale per hidden channel) or "tensor" (one deqScale)
+    x_norm: str | None = None
 
 
 # The five workloads.  Sizes, distributions and cache layouts follow the stated workload recipe.
@@ -80,6 +83,8 @@ MLA_FULL_QUANT = replace(MLA_PARTIAL_QUANT, name="full_quant_int8cache_T64", see
                          full_quant=True)
 MLA_FULL_QUANT_BF16CACHE = replace(MLA_PARTIAL_QUANT, name="full_quant_bf16cache_T64",
                                    seed=1007, full_quant=True, cache_dtype="bf16")
+# the input RmsNormQuant of aclnnMlaPreprocessV2 ahead of the decode prolog
+MLA_XNORM = replace(MLA_DECODE, name="decode_xnorm_T128", seed=1008, x_norm="channel")
 
 
 @dataclass(frozen=True)
@@ -229,6 +234,12 @@ def make_mla_inputs(case: MlaCase) -> dict:
         inp["kr_cache"] = torch.randn(d.block_num, d.block_size, 1, d.Dr, generator=g).to(bf16)
     inp["rmsnorm_epsilon_cq"] = case.eps
     inp["rmsnorm_epsilon_ckv"] = case.eps
+    if case.x_norm is not None:   # drawn last: the other inputs match the case without it
+        inp["rms_norm_quant_gamma"] = _uniform(g, (d.He,), 0.5, 1.5, bf16)
+        inp["rms_norm_quant_bias"] = _uniform(g, (d.He,), -0.25, 0.25, bf16)
+        inp["rms_norm_quant_deq_scale"] = _uniform(g, (d.He if case.x_norm == "channel" else 1,),
+                                                   0.5, 2.0)
+        inp["rms_norm_quant_epsilon"] = case.eps
     return inp
 
 

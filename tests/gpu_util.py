@@ -99,7 +99,7 @@ def run_mla(cpu: dict, dims, eps, device="cuda", bsh=False, prolog=None):
         prolog = pkg.MlaProlog({k: t[k] for k in ("weight_dq", "weight_uq_qr", "weight_uk",
                                                   "weight_dkv_kr")}, dims.N, dims.D, dims.Dr)
     run_t = {k: v for k, v in t.items() if not k.startswith("weight_")}
-    prolog.run(run_t, eps, eps)
+    prolog.run(run_t, eps, eps, eps_x=cpu.get("rms_norm_quant_epsilon"))
     torch.cuda.synchronize()
     status = pkg.mlap_check_errors(prolog.ws)
     return t, prolog, status
@@ -110,4 +110,6 @@ def oracle_inputs(cpu: dict, eps: float) -> dict:
     inp["rmsnorm_epsilon_cq"] = eps
     inp["rmsnorm_epsilon_ckv"] = eps
     inp["query_int8"] = query_int8(cpu)
+    if "rms_norm_quant_gamma" in cpu:
+        inp["rms_norm_quant_epsilon"] = cpu["rms_norm_quant_epsilon"]
     return inp

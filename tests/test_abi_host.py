@@ -58,7 +58,7 @@ class Fake:
 
 
 def _mla(T=128, He=7168, Hcq=1536, Hckv=512, N=128, D=128, Dr=64, BN=16, bsh=False,
-         w_int8=False, cache_int8=False, full=False):
+         w_int8=False, cache_int8=False, full=False, xnorm=None):
     bf, i8, f32 = torch.bfloat16, torch.int8, torch.float32
     tok = (T // 2, 2) if bsh else (T,)
     t = {
@@ -90,16 +90,21 @@ def _mla(T=128, He=7168, Hcq=1536, Hckv=512, N=128, D=128, Dr=64, BN=16, bsh=Fal
         if cache_int8:   # int8 kv_cache: int8 query per token and head
             t["query"] = Fake(tok + (N, Hckv), i8)
             t["dequant_scale_q_nope"] = Fake((T, N, 1), f32)
+    if xnorm is not None:   # input RmsNormQuant; deqScale per channel or one value
+        t["rms_norm_quant_gamma"] = Fake((He,), bf)
+        t["rms_norm_quant_bias"] = Fake((He,), bf)
+        t["rms_norm_quant_deq_scale"] = Fake((He if xnorm == "channel" else 1,), f32)
     return t
 
 
-def _args(t, cache_mode=None, eps=1e-6):
+def _args(t, cache_mode=None, eps=1e-6, eps_x=1e-6):
     a = _lib.mlap_args_t()
     for name in _lib._MLA_TENSORS:
         v = t.get(name)
         setattr(a, name, v.desc() if v is not None else _lib.tensor_desc(None))
     a.rmsnorm_epsilon_cq = eps
     a.rmsnorm_epsilon_ckv = eps
+    a.rms_norm_quant_epsilon = eps_x
     a.cache_mode = cache_mode.encode() if cache_mode else None
     return a
 
@@ -276,3 +281,35 @@ def test_full_quant_scenarios():
     # full quant needs its own workspace regions (widened x, staged q^N)
     assert _status(_args(_mla(w_int8=True, cache_int8=True, full=True)))[1] > \
         _status(_args(_mla(w_int8=True, cache_int8=True)))[1]
+
+
+def test_rms_norm_quant_validation():
+    # accepted with the bf16-x scenarios, deqScale per channel or one value
+    assert _status(_args(_mla(xnorm="channel")))[0] == 0
+    assert _status(_args(_mla(xnorm="tensor", bsh=True)))[0] == 0
+    assert _status(_args(_mla(xnorm="channel", w_int8=True, cache_int8=True)))[0] == 0
+    # the down-projection reads the normalised copy from the workspace: T * He * 2 more bytes
+    assert (_status(_args(_mla(xnorm="channel")))[1]
+            - _status(_args(_mla()))[1]) == 128 * 7168 * 2
+    # all three parameters or none
+    for name in ("rms_norm_quant_gamma", "rms_norm_quant_bias", "rms_norm_quant_deq_scale"):
+        t = _mla(xnorm="channel")
+        t.pop(name)
+        assert _status(_args(t))[0] == 1, name
+    t = _mla(xnorm="channel")
+    t["rms_norm_quant_gamma"] = Fake((7168,), torch.float32)
+    assert _status(_args(t))[0] == 3
+    t = _mla(xnorm="channel")
+    t["rms_norm_quant_bias"] = Fake((7167,), torch.bfloat16)
+    assert _status(_args(t))[0] == 2
+    t = _mla(xnorm="channel")
+    t["rms_norm_quant_deq_scale"] = Fake((2,), torch.float32)
+    assert _status(_args(t))[0] == 2
+    t = _mla(xnorm="channel")
+    t["rms_norm_quant_deq_scale"] = Fake((7168,), torch.bfloat16)
+    assert _status(_args(t))[0] == 3
+    assert _status(_args(_mla(xnorm="channel"), eps_x=-1.0))[0] == 2
+    # not with full quant (int8 token_x), nor above He = 10240
+    assert _status(_args(_mla(xnorm="channel", w_int8=True, full=True)))[0] == 4
+    assert _status(_args(_mla(He=10496, xnorm="channel")))[0] == 4
+    assert _status(_args(_mla(He=10240, xnorm="channel")))[0] == 0

@@ -221,3 +221,37 @@ def test_full_quant_bsh():
     case = synthetic.small_mla_case("fq_bsh", B=4, S=5, N=2, block_num=1, full_quant=True,
                                     weight_uq_qr_dtype="int8", cache_dtype="int8")
     _full_check(case, bsh=True)
+
+
+# ---- input RmsNormQuant (aclnnMlaPreprocessV2) ahead of the down-projection
+
+def test_rms_norm_quant_decode():
+    # the decode workload with the input RmsNormQuant (deqScale per channel)
+    _full_check(synthetic.MLA_XNORM)
+
+
+XNORM_SHAPES = [
+    dict(B=3, S=1, He=264, N=2, x_norm="channel"),              # ragged He over the threads
+    dict(B=2, S=1, He=10240, Hcq=256, N=2, x_norm="tensor"),    # largest He, one deqScale
+    dict(B=3, S=100, He=384, Hcq=192, Hckv=128, N=2, x_norm="channel"),   # prefill orientation
+    dict(B=5, S=1, He=256, Hcq=128, N=3, x_norm="tensor", weight_uq_qr_dtype="int8",
+         cache_dtype="int8"),                                   # with partial quant
+    dict(B=2, S=300, He=264, Hcq=128, N=2, x_norm="channel"),   # many tokens: the other kernel
+]
+
+
+@pytest.mark.parametrize("kw", XNORM_SHAPES, ids=[str(i) for i in range(len(XNORM_SHAPES))])
+def test_rms_norm_quant_shapes(kw):
+    kw = dict(kw)
+    block_num = max(1, (kw["B"] * kw["S"] + 127) // 128 + 1)
+    case = synthetic.small_mla_case("xnorm", block_num=block_num, n_skip=1, **kw)
+    _full_check(case)
+
+
+def test_rms_norm_quant_bsh_leaves_token_x():
+    case = synthetic.small_mla_case("xnorm_bsh", B=4, S=5, N=2, block_num=1, x_norm="channel")
+    cpu = synthetic.make_mla_inputs(case)
+    t, _ = _full_check(case, bsh=True)
+    # token_x is only read: the normalised copy lives in the workspace
+    assert torch.equal(t["token_x"].reshape(cpu["token_x"].shape).cpu().view(torch.int16),
+                       cpu["token_x"].view(torch.int16))
