@@ -252,6 +252,7 @@ mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
     if (d->query_int8 != d->kv_int8)
       return fail(MLAP_ERR_UNSUPPORTED, "full quant: query is int8 exactly when kv_cache is int8");
     if (d->query_int8) {
+      if (d->Hckv > 1024) return fail(MLAP_ERR_UNSUPPORTED, "an int8 query needs Hckv <= 1024");
       const mlap_tensor_t& sq = a->dequant_scale_q_nope;
       CHECK_STATUS(need(sq, "dequant_scale_q_nope", false));
       CHECK_STATUS(want_dtype(sq, "dequant_scale_q_nope", MLAP_DTYPE_FP32));

@@ -210,23 +210,30 @@ struct FragIter {
 
 // One row of an int8 weight tile (64 values, 64 B) to bf16 in the 128B-swizzled K-major layout
 // (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7)) << 4)).  The four source chunks are visited
-// in a row-dependent order to spread shared-memory banks.
+// in a row-dependent order to spread shared-memory banks.  Conversion by the 2^23 magic number:
+// with u = v + 128 in [0, 255], the fp32 with bits 0x4B000000 | u is 2^23 + u exactly, so one
+// byte permute and one add give v in fp32 (exact); a bf16 holds every |v| <= 128 exactly, so the
+// upper half of the fp32 is the bf16.  This keeps the conversion on the full-rate ALU and FMA
+// pipes.
+__device__ __forceinline__ uint32_t int8x2_to_bf16x2(uint32_t biased, int k0) {
+  const float f0 = __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7540u | k0)) - 8388736.0f;
+  const float f1 =
+      __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7540u | (k0 + 1))) - 8388736.0f;
+  return __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
+}
+
 __device__ __forceinline__ void convert_int8_row(const uint8_t* src_row, uint8_t* dst, int r) {
 #pragma unroll
   for (int ii = 0; ii < 4; ++ii) {
     const int i = (ii + r) & 3;
     const uint4 raw = *reinterpret_cast<const uint4*>(src_row + i * 16);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    const uint32_t w[4] = {raw.x ^ 0x80808080u, raw.y ^ 0x80808080u, raw.z ^ 0x80808080u,
+                           raw.w ^ 0x80808080u};
     uint32_t out[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float f0 = static_cast<float>(static_cast<int8_t>(w[k] & 0xffu));
-      const float f1 = static_cast<float>(static_cast<int8_t>((w[k] >> 8) & 0xffu));
-      const float f2 = static_cast<float>(static_cast<int8_t>((w[k] >> 16) & 0xffu));
-      const float f3 = static_cast<float>(static_cast<int8_t>(w[k] >> 24));
-      // bf16 of a small integer is the upper half of its fp32 bit pattern (exact for |v| <= 256)
-      out[2 * k] = (__float_as_uint(f0) >> 16) | (__float_as_uint(f1) & 0xffff0000u);
-      out[2 * k + 1] = (__float_as_uint(f2) >> 16) | (__float_as_uint(f3) & 0xffff0000u);
+      out[2 * k] = int8x2_to_bf16x2(w[k], 0);
+      out[2 * k + 1] = int8x2_to_bf16x2(w[k], 2);
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {

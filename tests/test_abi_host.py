@@ -278,6 +278,9 @@ def test_full_quant_scenarios():
     t = _mla(w_int8=True)
     t["query"] = Fake((128, 128, 512), torch.int8)        # int8 query outside full quant
     assert _status(_args(t))[0] == 3
+    # an int8 query row is quantised from registers: Hckv <= 1024
+    assert _status(_args(_mla(Hckv=1024, w_int8=True, cache_int8=True, full=True)))[0] == 0
+    assert _status(_args(_mla(Hckv=1032, w_int8=True, cache_int8=True, full=True)))[0] == 4
     # full quant needs its own workspace regions (widened x, staged q^N)
     assert _status(_args(_mla(w_int8=True, cache_int8=True, full=True)))[1] > \
         _status(_args(_mla(w_int8=True, cache_int8=True)))[1]
