@@ -360,6 +360,15 @@ def run_ours(args, rank, local, world):
     names = ["down", "norm_scatter", "up", "absorb"]
     per = per[min(10, len(per) // 2):]
     avg_ms = {n: statistics.mean(r[k] for r in per) for k, n in enumerate(names)}
+    if avg_ms["absorb"] == 0.0:
+        # the decode launch fuses the absorb into the up-projection (the timer's absorb phase is
+        # empty): one kernel, whose algorithmic bytes are both weights, c^Q and both outputs
+        avg_ms = {"down": avg_ms["down"], "norm_scatter": avg_ms["norm_scatter"],
+                  "up_absorb": avg_ms["up"]}
+        names = list(avg_ms)
+        kern["up_absorb"] = {
+            "bytes": kern["up"]["bytes"] + kern["absorb"]["bytes"] - 2 * d.T * d.N * d.D * 2,
+            "flops": kern["up"]["flops"] + kern["absorb"]["flops"]}
     dominant = max(names, key=lambda n: avg_ms[n])
     tensor_bound = args.workload == "prefill"
     if tensor_bound:

@@ -102,6 +102,7 @@ struct MlaDims {
 constexpr int kSwapMaxT = 256;   // decode orientation (weights as MMA rows) up to this many tokens
 constexpr int kSplitMaxT = 256;  // down-projection K splits (few output tiles) up to this many tokens
 constexpr int kMaxSplits = 16;
+constexpr int kFusedMinHeads = 64;   // the fused decode up/absorb runs one CTA per head
 constexpr size_t kHeaderBytes = 8192;   // error word + stream-K flags
 constexpr size_t kFlagOffset = 4096;    // stream-K "partial written" flags (int32 per CTA)
 constexpr int kMaxStreamKCtas = 1024;   // flags that fit the header
@@ -469,6 +470,7 @@ mlap_status_t cuda_fail(cudaError_t e, const char* what) {
 
 struct Timer {
   std::vector<cudaEvent_t> ev;   // (MLAP_TIMER_PHASES + 1) per call
+  std::vector<uint8_t> fused;    // per call: up-projection and absorb ran as one kernel
   int max_calls = 0;
   int calls = 0;
 };
@@ -638,8 +640,31 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     if (ce != cudaSuccess) return cuda_fail(ce, "norm/rope/scatter launch");
   }
 
+  // ---- 3+4 fused at decode: one CTA per head runs the up-projection, keeps q^C in shared
+  // memory and multiplies it by the head's W^UK (up_absorb.cu)
+  const bool fused = swap && !d.w_int8 && d.N >= kFusedMinHeads &&
+                     up_absorb_supported(d.T, d.N, d.D, d.Dr, d.Hckv);
+  if (fused) {
+    CUtensorMap tcq, tw, tuk;
+    CHECK_STATUS(make_tmap(&tcq, cq, d.Hcq, d.T, d.Hcq, 128));
+    CHECK_STATUS(make_tmap(&tw, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 32));
+    CHECK_STATUS(make_tmap(&tuk, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, 32));
+    UpAbsorbParams ua{static_cast<const __nv_bfloat16*>(a->rope_cos.data),
+                      static_cast<const __nv_bfloat16*>(a->rope_sin.data),
+                      static_cast<__nv_bfloat16*>(a->query_rope.data),
+                      static_cast<__nv_bfloat16*>(a->query.data),
+                      static_cast<int32_t>(d.T), static_cast<int32_t>(d.N),
+                      static_cast<int32_t>(d.Hcq), static_cast<int32_t>(d.Hckv)};
+    CHECK_STATUS(rec(2));
+    ce = launch_up_absorb(tcq, tw, tuk, ua, err, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "fused up-projection/absorb launch");
+    CHECK_STATUS(rec(3));
+    CHECK_STATUS(rec(4));
+    if (timer != nullptr) timer->fused[timer->calls] = 1;
+  }
+
   // ---- 3. up-projection c^Q·[W^UQ|W^QR] -> q^C (bf16 workspace) and query_rope
-  {
+  if (!fused) {
     GemmLaunch u{};
     u.stream = stream;
     u.pdl = true;
@@ -729,7 +754,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   }
 
   // ---- 4. absorb q^N = q^C · W^UK per head -> query
-  {
+  if (!fused) {
     GemmLaunch b{};
     b.stream = stream;
     b.pdl = true;
@@ -1087,6 +1112,7 @@ mlap_status_t mlap_timer_create(void** timer, int32_t max_calls) {
   Timer* t = new Timer();
   t->max_calls = max_calls;
   t->ev.resize(static_cast<size_t>(max_calls) * (MLAP_TIMER_PHASES + 1));
+  t->fused.assign(static_cast<size_t>(max_calls), 0);
   for (auto& e : t->ev) {
     if (cudaEventCreate(&e) != cudaSuccess) {
       delete t;
@@ -1113,11 +1139,13 @@ mlap_status_t mlap_timer_read(void* timer, float* ms, int32_t* calls_recorded) {
       if (cudaEventSynchronize(e1) != cudaSuccess) return fail(MLAP_ERR_CUDA, "cudaEventSynchronize failed");
       float v = 0.f;
       if (cudaEventElapsedTime(&v, e0, e1) != cudaSuccess) return fail(MLAP_ERR_CUDA, "cudaEventElapsedTime failed");
+      if (k == 3 && t->fused[c]) v = 0.f;   // no separate absorb kernel ran
       if (ms) ms[c * MLAP_TIMER_PHASES + k] = v;
     }
   }
   *calls_recorded = t->calls;
   t->calls = 0;
+  std::fill(t->fused.begin(), t->fused.end(), 0);
   return MLAP_OK;
 }
 

@@ -31,6 +31,22 @@ struct GemmLaunch {
 
 cudaError_t launch_down(const GemmLaunch& L, const DownParams& p);
 cudaError_t launch_up(const GemmLaunch& L, const UpParams& p, bool int8);
+
+// Fused decode up-projection + absorb, one CTA per head (up_absorb.cu): tokens as MMA rows,
+// q^C kept in shared memory, query_rope and query written directly.
+struct UpAbsorbParams {
+  const __nv_bfloat16* cos;     // (T, Dr)
+  const __nv_bfloat16* sin;     // (T, Dr)
+  __nv_bfloat16* qr_out;        // query_rope (T, N, Dr)
+  __nv_bfloat16* q_out;         // query (T, N, Hckv)
+  int32_t T, N, Hcq, Hckv;
+};
+bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hckv);
+// tmCq: c^Q (T, Hcq) bf16, box 64 x 128; tmW: prepacked W^UQ|W^QR (N*(D+Dr) rows of Hcq), box
+// 64 x 32; tmUk: prepacked W^UK (N*Hckv rows of D), box 64 x 32; all 128B-swizzled.
+cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
+                             const CUtensorMap& tmUk, const UpAbsorbParams& p, uint32_t* err,
+                             cudaStream_t stream);
 cudaError_t launch_absorb(const GemmLaunch& L, const AbsorbParams& p);
 
 // RmsNorm of c^Q (+ dynamic int8 quant) and c^KV, RoPE of k^R, cache quant and scatter; one CTA

@@ -1,0 +1,360 @@
+// Fused up-projection and absorb for decode (MlaPrologV2 README, 功能说明: q^C = c^Q·W^UQ,
+// q^R = ROPE(c^Q·W^QR), q^N = q^C·W^UK), one CTA per head n, tokens as the MMA's M = 128 rows:
+//
+//   1. [q^C_n | q_r,n] = c^Q · [W^UQ_n | W^QR_n]   K = Hcq, N = D + Dr = 192 columns in TMEM
+//   2. epilogue: q^C_n rounded to bf16 into shared memory, laid out as the next MMA's A operand;
+//      q_r,n rotated (half-and-half RoPE of aclnnQkvRmsNormRopeCache "Formulas" (3)) -> query_rope
+//   3. q^N_n = q^C_n · W^UK_n                         K = D, N = Hckv (chunks of 256 columns)
+//   4. epilogue: q^N_n rounded to bf16 -> query
+//
+// q^C never leaves the SM, and the head's W^UK tiles stream through the same pipeline right
+// behind its W^UQ|W^QR tiles, so one launch replaces two kernels and their boundary.  Weights are
+// prepacked K-major: W^UQ|W^QR rows [all heads' nope rows n*D + d | all heads' rope rows, pairs
+// (j, j + Dr/2) adjacent], W^UK as (N, Hckv, D).
+//
+// Roles: warp 0 lane 0 TMA producer, warp 1 lane 0 MMA issuer, warp 2 TMEM owner, warps 4..7
+// epilogue (warp 4 + q owns TMEM lanes 32q..32q+31, i.e. tokens 32q..32q+31).  Every mbarrier
+// wait is bounded; on a timeout the CTA lets its issued loads land, frees TMEM and latches the
+// error word.
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "internal.h"
+
+namespace mlap {
+
+namespace {
+
+constexpr int kUaThreads = 256;
+constexpr int kUaStages = 4;
+constexpr int kUaBK = 64;                              // K elements per stage
+constexpr int kUaA = 128 * kUaBK * 2;                  // c^Q tile: 128 tokens x 64 (16 KB)
+constexpr int kUaB = 256 * kUaBK * 2;                  // weight tile: up to 256 rows (32 KB)
+constexpr int kUaStage = kUaA + kUaB;
+constexpr int kUaQc = 2 * 128 * kUaBK * 2;             // q^C operand: 128 tokens x D = 128
+constexpr int kUaBars = 512;
+constexpr int kUaSmem = kUaStages * kUaStage + kUaQc + kUaBars + 1024;   // + alignment slack
+constexpr uint32_t kUaUpCol = 256;                     // TMEM column of the up accumulator
+constexpr int kD = 128;
+constexpr int kDr = 64;
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+}
+
+__device__ __forceinline__ void unpack16(uint4 a, uint4 b, float* out) {
+  const __nv_bfloat16* ea = reinterpret_cast<const __nv_bfloat16*>(&a);
+  const __nv_bfloat16* eb = reinterpret_cast<const __nv_bfloat16*>(&b);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    out[i] = __bfloat162float(ea[i]);
+    out[8 + i] = __bfloat162float(eb[i]);
+  }
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__global__ void __launch_bounds__(kUaThreads, 1)
+    up_absorb_kernel(const __grid_constant__ CUtensorMap tmCq,   // c^Q (T, Hcq), box 64 x 128
+                     const __grid_constant__ CUtensorMap tmW,    // W^UQ|W^QR rows, box 64 x 32
+                     const __grid_constant__ CUtensorMap tmUk,   // W^UK rows, box 64 x 32
+                     const UpAbsorbParams p, uint32_t* __restrict__ err_word) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* qc = smem + kUaStages * kUaStage;           // q^C operand (two 64-wide K blocks)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(qc + kUaQc);
+  uint64_t* empty_bar = full_bar + kUaStages;
+  uint64_t* up_bar = empty_bar + kUaStages;            // up accumulator complete
+  uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, up accumulator drained
+  uint64_t* ab_bar = qc_bar + 1;                       // absorb accumulator complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x;                            // head
+  const int kb_up = (p.Hcq + kUaBK - 1) / kUaBK;
+  const int nh = (p.Hckv + 255) / 256;                 // absorb column chunks
+
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmCq);
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmUk);
+  }
+  if (warp == 1 && lane == 0) {
+    for (int i = 0; i < kUaStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(up_bar, 1);
+    mbar_init(qc_bar, 4);
+    mbar_init(ab_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  grid_launch_dependents();
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) grid_dependency_wait();
+
+  if (producer) {
+    // ------------------------------------------------------------------ TMA producer
+    int fills[kUaStages] = {0, 0, 0, 0};
+    // head n's W^UQ rows (D) then its W^QR rows (Dr), 32-row boxes, into the stage's B tile
+    auto issue_w = [&](int st, int kb) {
+      uint8_t* b = smem + st * kUaStage + kUaA;
+      mbar_expect_tx(&full_bar[st], (kD + kDr) * kUaBK * 2);
+      for (int r = 0; r < kD; r += 32)
+        tma_load_2d(b + r * 128, &tmW, &full_bar[st], kb * kUaBK, n * kD + r);
+      for (int r = 0; r < kDr; r += 32)
+        tma_load_2d(b + (kD + r) * 128, &tmW, &full_bar[st], kb * kUaBK,
+                    p.N * kD + n * kDr + r);
+    };
+    const int pre = kb_up < kUaStages ? kb_up : kUaStages;
+    for (int i = 0; i < pre; ++i) issue_w(i, i);      // weights do not depend on earlier kernels
+    grid_dependency_wait();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int kb = 0; ok && kb < kb_up; ++kb) {
+      if (kb >= pre) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        issue_w(stage, kb);
+      }
+      mbar_arrive_expect_tx(&full_bar[stage], kUaA);
+      tma_load_2d(smem + stage * kUaStage, &tmCq, &full_bar[stage], kb * kUaBK, 0);
+      ++fills[stage];
+      if (++stage == kUaStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    // head n's W^UK rows, chunk h of 256 rows, K block kb2 of D
+    for (int h = 0; ok && h < nh; ++h) {
+      const int rows = p.Hckv - h * 256 < 256 ? p.Hckv - h * 256 : 256;
+      for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* b = smem + stage * kUaStage + kUaA;
+        mbar_arrive_expect_tx(&full_bar[stage], rows * kUaBK * 2);
+        for (int r = 0; r < rows; r += 32)
+          tma_load_2d(b + r * 128, &tmUk, &full_bar[stage], kb2 * kUaBK, n * p.Hckv + h * 256 + r);
+        ++fills[stage];
+        if (++stage == kUaStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (*abort_flag) {
+      // let every issued load land before the CTA exits (the last fill of stage i has parity
+      // (fills[i] - 1) & 1; prefetched weights count toward the fill of their k block)
+      const uint64_t t0 = globaltimer_ns();
+      for (int i = 0; i < kUaStages; ++i) {
+        if (fills[i] == 0 && i >= pre) continue;
+        const uint32_t par = static_cast<uint32_t>((fills[i] > 0 ? fills[i] : 1) - 1) & 1u;
+        while (!mbar_try_wait(&full_bar[i], par) && globaltimer_ns() - t0 < 20000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t idesc_up = idesc_bf16_f32(128, kD + kDr);
+      for (int kb = 0; kb < kb_up; ++kb) {
+        if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a = smem_u32(smem + stage * kUaStage);
+        const uint32_t b = a + kUaA;
+#pragma unroll
+        for (int kk = 0; kk < kUaBK / 16; ++kk)
+          umma_bf16_ss(tmem_base + kUaUpCol, sdesc_kmajor_sw128(a + kk * 32),
+                       sdesc_kmajor_sw128(b + kk * 32), idesc_up, (kb > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&empty_bar[stage]);
+        if (++stage == kUaStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) {
+        umma_commit(up_bar);
+        ok = mbar_wait(qc_bar, 0, abort_flag);        // q^C staged, up accumulator read
+      }
+      if (ok) {
+        tc_fence_after_sync();
+        const uint32_t qa = smem_u32(qc);
+        for (int h = 0; ok && h < nh; ++h) {
+          const int rows = p.Hckv - h * 256 < 256 ? p.Hckv - h * 256 : 256;
+          const uint32_t idesc_ab = idesc_bf16_f32(128, rows);
+          for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2) {
+            if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t b = smem_u32(smem + stage * kUaStage) + kUaA;
+#pragma unroll
+            for (int kk = 0; kk < kUaBK / 16; ++kk)
+              umma_bf16_ss(tmem_base + static_cast<uint32_t>(h * 256),
+                           sdesc_kmajor_sw128(qa + kb2 * (128 * kUaBK * 2) + kk * 32),
+                           sdesc_kmajor_sw128(b + kk * 32), idesc_ab,
+                           (kb2 > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&empty_bar[stage]);
+            if (++stage == kUaStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (ok) umma_commit(ab_bar);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp - 4;
+    const int t = q * 32 + lane;                       // token of this lane
+    const bool live = t < p.T;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // RoPE tables of this token: pairs 0..15 and 16..31 at columns j and j + Dr/2
+    uint4 cs[2][4], sn[2][4];
+    if (live) {
+      const uint4* c = reinterpret_cast<const uint4*>(p.cos + static_cast<size_t>(t) * kDr);
+      const uint4* s = reinterpret_cast<const uint4*>(p.sin + static_cast<size_t>(t) * kDr);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {   // uint4 i covers columns 8i..8i+7
+        cs[i >> 1][i & 1] = __ldg(c + i);
+        sn[i >> 1][i & 1] = __ldg(s + i);
+        cs[i >> 1][2 + (i & 1)] = __ldg(c + 4 + i);
+        sn[i >> 1][2 + (i & 1)] = __ldg(s + 4 + i);
+      }
+    }
+    bool ok = mbar_wait(up_bar, 0, abort_flag);
+    if (ok) {
+      tc_fence_after_sync();
+      // q^C: bf16 into the K-major, 128B-swizzled A operand (token t = row t)
+#pragma unroll 1
+      for (int c = 0; c < kD; c += 32) {
+        float v[32];
+        tmem_ld32(lane_base + kUaUpCol + c, v);
+        uint8_t* row = qc + (c / kUaBK) * (128 * kUaBK * 2) + t * 128;
+        const int ch0 = (c % kUaBK) / 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(row + ((((ch0 + j) ^ (t & 7)) & 7) << 4)) = pack8(v + 8 * j);
+      }
+      // q_r: 32 columns = pairs p0..p0+15 (p0 = 0, 16) of this head, RoPE, -> query_rope
+#pragma unroll
+      for (int blk = 0; blk < kDr / 32; ++blk) {
+        float y[32];
+        tmem_ld32(lane_base + kUaUpCol + kD + blk * 32, y);
+        if (live) {
+          float c0[16], s0[16], c1[16], s1[16];
+          unpack16(cs[blk][0], cs[blk][1], c0);
+          unpack16(sn[blk][0], sn[blk][1], s0);
+          unpack16(cs[blk][2], cs[blk][3], c1);
+          unpack16(sn[blk][2], sn[blk][3], s1);
+          float oa[16], ob[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float y0 = y[2 * i], y1 = y[2 * i + 1];
+            oa[i] = y0 * c0[i] - y1 * s0[i];
+            ob[i] = y1 * c1[i] + y0 * s1[i];
+          }
+          __nv_bfloat16* out = p.qr_out + (static_cast<size_t>(t) * p.N + n) * kDr + blk * 16;
+          uint4* da = reinterpret_cast<uint4*>(out);
+          uint4* db = reinterpret_cast<uint4*>(out + kDr / 2);
+          da[0] = pack8(oa);
+          da[1] = pack8(oa + 8);
+          db[0] = pack8(ob);
+          db[1] = pack8(ob + 8);
+        }
+      }
+      tc_fence_before_sync();
+      fence_proxy_async_shared();                      // q^C stores -> visible to the MMA
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qc_bar);
+      ok = mbar_wait(ab_bar, 0, abort_flag);
+    }
+    if (ok) {
+      tc_fence_after_sync();
+      __nv_bfloat16* out = p.q_out + (static_cast<size_t>(t) * p.N + n) * p.Hckv;
+#pragma unroll 1
+      for (int c = 0; c < p.Hckv; c += 32) {
+        float v[32];
+        tmem_ld32(lane_base + static_cast<uint32_t>(c), v);
+        if (live) {
+          uint4* d = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d[j] = pack8(v + 8 * j);
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(err_word, kErrTimeout);
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace
+
+bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hckv) {
+  return T >= 1 && T <= 128 && N >= 1 && D == kD && Dr == kDr && Hckv >= 32 && Hckv <= 512 &&
+         Hckv % 32 == 0;
+}
+
+cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
+                             const CUtensorMap& tmUk, const UpAbsorbParams& p, uint32_t* err,
+                             cudaStream_t stream) {
+  cudaError_t e =
+      cudaFuncSetAttribute(up_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUaSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.N));
+  cfg.blockDim = dim3(kUaThreads);
+  cfg.dynamicSmemBytes = kUaSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, up_absorb_kernel, tmCq, tmW, tmUk, p, err);
+}
+
+}  // namespace mlap

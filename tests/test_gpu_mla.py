@@ -255,3 +255,21 @@ def test_rms_norm_quant_bsh_leaves_token_x():
     # token_x is only read: the normalised copy lives in the workspace
     assert torch.equal(t["token_x"].reshape(cpu["token_x"].shape).cpu().view(torch.int16),
                        cpu["token_x"].view(torch.int16))
+
+
+# ---- fused decode up-projection + absorb (one CTA per head, T <= 128, N >= 64, bf16 weight)
+
+FUSED_SHAPES = [
+    dict(B=1, S=1, N=64),                                          # single token
+    dict(B=100, S=1, He=256, Hcq=136, Hckv=288, N=64),             # ragged K, absorb 256 + 32
+    dict(B=33, S=1, He=320, Hcq=192, Hckv=96, N=80),               # 80 heads, one short chunk
+    dict(B=4, S=32, He=256, Hcq=128, Hckv=512, N=64),              # BSH-shaped T = 128
+]
+
+
+@pytest.mark.parametrize("kw", FUSED_SHAPES, ids=[str(i) for i in range(len(FUSED_SHAPES))])
+def test_fused_up_absorb_shapes(kw):
+    kw = dict(kw)
+    block_num = max(1, (kw["B"] * kw["S"] + 127) // 128 + 1)
+    case = synthetic.small_mla_case("fused", block_num=block_num, n_skip=1, **kw)
+    _full_check(case, bsh=kw["S"] > 1)
