@@ -654,7 +654,8 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                       static_cast<__nv_bfloat16*>(a->query_rope.data),
                       static_cast<__nv_bfloat16*>(a->query.data),
                       static_cast<int32_t>(d.T), static_cast<int32_t>(d.N),
-                      static_cast<int32_t>(d.Hcq), static_cast<int32_t>(d.Hckv)};
+                      static_cast<int32_t>(d.Hcq), static_cast<int32_t>(d.Hckv), 2, 0};
+    up_absorb_plan(sms, static_cast<int>(d.N), &ua.k, &ua.R);
     CHECK_STATUS(rec(2));
     ce = launch_up_absorb(tcq, tw, tuk, ua, err, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "fused up-projection/absorb launch");

@@ -40,7 +40,11 @@ struct UpAbsorbParams {
   __nv_bfloat16* qr_out;        // query_rope (T, N, Dr)
   __nv_bfloat16* q_out;         // query (T, N, Hckv)
   int32_t T, N, Hcq, Hckv;
+  int32_t k;                    // W^QR blocks of 32 rows kept by each head CTA (0, 1 or 2)
+  int32_t R;                    // CTAs after the N head CTAs that take the other W^QR blocks
 };
+// k and R for `sms` SMs and N heads (grid = N + R)
+void up_absorb_plan(int sms, int N, int* k, int* R);
 bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hckv);
 // tmCq: c^Q (T, Hcq) bf16, box 64 x 128; tmW: prepacked W^UQ|W^QR (N*(D+Dr) rows of Hcq), box
 // 64 x 32; tmUk: prepacked W^UK (N*Hckv rows of D), box 64 x 32; all 128B-swizzled.

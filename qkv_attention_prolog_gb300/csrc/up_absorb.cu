@@ -12,6 +12,12 @@
 // prepacked K-major: W^UQ|W^QR rows [all heads' nope rows n*D + d | all heads' rope rows, pairs
 // (j, j + Dr/2) adjacent], W^UK as (N, Hckv, D).
 //
+// Each SM streams its weights at a bounded rate (about 40 GB/s on GB300 however they are
+// fetched), so the SMs without a head take W^QR work: the rope rows come in 2N blocks of 32
+// (block g = head g/2, pairs 16*(g%2)..+15).  With R such "rope CTAs" (blockIdx >= N), a head CTA
+// keeps k of its own blocks (2, 1 or 0) and the rope CTAs share the others evenly, at most 6
+// blocks (192 rows) each; a rope CTA runs only the up-projection and RoPE.
+//
 // Roles: warp 0 lane 0 TMA producer, warp 1 lane 0 MMA issuer, warp 2 TMEM owner, warps 4..7
 // epilogue (warp 4 + q owns TMEM lanes 32q..32q+31, i.e. tokens 32q..32q+31).  Every mbarrier
 // wait is bounded; on a timeout the CTA lets its issued loads land, frees TMEM and latches the
@@ -65,6 +71,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// This CTA's share: head CTA (blockIdx < N) or rope CTA, and its rope blocks g_j = g0 + gs * j,
+// j < nrope (kept in registers: the producer's issue path is latency-critical).
+struct UaPlan {
+  bool head;
+  int nrope, g0, gs;
+};
+
+__device__ __forceinline__ UaPlan ua_plan(const UpAbsorbParams& p) {
+  UaPlan pl;
+  const int b = blockIdx.x;
+  if (b < p.N) {
+    pl.head = true;
+    pl.nrope = p.k;
+    pl.g0 = 2 * b;
+    pl.gs = 1;
+  } else {
+    const int r = b - p.N;
+    const int total = p.k == 1 ? p.N : 2 * p.N;        // blocks the rope CTAs share
+    const int i0 = static_cast<int>(static_cast<long long>(total) * r / p.R);
+    const int i1 = static_cast<int>(static_cast<long long>(total) * (r + 1) / p.R);
+    pl.head = false;
+    pl.nrope = i1 - i0 < 6 ? i1 - i0 : 6;
+    pl.g0 = p.k == 1 ? 2 * i0 + 1 : i0;
+    pl.gs = p.k == 1 ? 2 : 1;
+  }
+  return pl;
+}
+
 __global__ void __launch_bounds__(kUaThreads, 1)
     up_absorb_kernel(const __grid_constant__ CUtensorMap tmCq,   // c^Q (T, Hcq), box 64 x 128
                      const __grid_constant__ CUtensorMap tmW,    // W^UQ|W^QR rows, box 64 x 32
@@ -84,9 +118,11 @@ __global__ void __launch_bounds__(kUaThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n = blockIdx.x;                            // head
+  const UaPlan pl = ua_plan(p);
+  const int n = blockIdx.x;                            // head (head CTAs)
   const int kb_up = (p.Hcq + kUaBK - 1) / kUaBK;
-  const int nh = (p.Hckv + 255) / 256;                 // absorb column chunks
+  const int nh = pl.head ? (p.Hckv + 255) / 256 : 0;   // absorb column chunks
+  const int up_rows = (pl.head ? kD : 0) + 32 * pl.nrope;   // B rows of the up-projection
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmCq);
@@ -120,15 +156,21 @@ __global__ void __launch_bounds__(kUaThreads, 1)
   if (producer) {
     // ------------------------------------------------------------------ TMA producer
     int fills[kUaStages] = {0, 0, 0, 0};
-    // head n's W^UQ rows (D) then its W^QR rows (Dr), 32-row boxes, into the stage's B tile
+    // head n's W^UQ rows (D), then this CTA's rope blocks: up to six 32-row boxes per tile,
+    // their first weight rows computed once
+    const int nbox = up_rows / 32;
+    int ybox[6];
+#pragma unroll
+    for (int j = 0; j < 6; ++j) {
+      const int jr = pl.head ? j - kD / 32 : j;       // rope block index of box j
+      ybox[j] = jr < 0 ? n * kD + 32 * j : p.N * kD + 32 * (pl.g0 + pl.gs * jr);
+    }
     auto issue_w = [&](int st, int kb) {
       uint8_t* b = smem + st * kUaStage + kUaA;
-      mbar_expect_tx(&full_bar[st], (kD + kDr) * kUaBK * 2);
-      for (int r = 0; r < kD; r += 32)
-        tma_load_2d(b + r * 128, &tmW, &full_bar[st], kb * kUaBK, n * kD + r);
-      for (int r = 0; r < kDr; r += 32)
-        tma_load_2d(b + (kD + r) * 128, &tmW, &full_bar[st], kb * kUaBK,
-                    p.N * kD + n * kDr + r);
+      mbar_expect_tx(&full_bar[st], static_cast<uint32_t>(up_rows) * kUaBK * 2);
+#pragma unroll
+      for (int j = 0; j < 6; ++j)
+        if (j < nbox) tma_load_2d(b + j * 4096, &tmW, &full_bar[st], kb * kUaBK, ybox[j]);
     };
     const int pre = kb_up < kUaStages ? kb_up : kUaStages;
     for (int i = 0; i < pre; ++i) issue_w(i, i);      // weights do not depend on earlier kernels
@@ -188,7 +230,7 @@ __global__ void __launch_bounds__(kUaThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const uint32_t idesc_up = idesc_bf16_f32(128, kD + kDr);
+      const uint32_t idesc_up = idesc_bf16_f32(128, up_rows);
       for (int kb = 0; kb < kb_up; ++kb) {
         if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
           ok = false;
@@ -207,11 +249,9 @@ __global__ void __launch_bounds__(kUaThreads, 1)
           phase ^= 1u;
         }
       }
-      if (ok) {
-        umma_commit(up_bar);
-        ok = mbar_wait(qc_bar, 0, abort_flag);        // q^C staged, up accumulator read
-      }
-      if (ok) {
+      if (ok) umma_commit(up_bar);
+      if (ok && pl.head) ok = mbar_wait(qc_bar, 0, abort_flag);   // q^C staged, acc read
+      if (ok && pl.head) {
         tc_fence_after_sync();
         const uint32_t qa = smem_u32(qc);
         for (int h = 0; ok && h < nh; ++h) {
@@ -262,28 +302,34 @@ __global__ void __launch_bounds__(kUaThreads, 1)
     bool ok = mbar_wait(up_bar, 0, abort_flag);
     if (ok) {
       tc_fence_after_sync();
-      // q^C: bf16 into the K-major, 128B-swizzled A operand (token t = row t)
+      int col = 0;
+      if (pl.head) {
+        // q^C: bf16 into the K-major, 128B-swizzled A operand (token t = row t)
 #pragma unroll 1
-      for (int c = 0; c < kD; c += 32) {
-        float v[32];
-        tmem_ld32(lane_base + kUaUpCol + c, v);
-        uint8_t* row = qc + (c / kUaBK) * (128 * kUaBK * 2) + t * 128;
-        const int ch0 = (c % kUaBK) / 8;
+        for (; col < kD; col += 32) {
+          float v[32];
+          tmem_ld32(lane_base + kUaUpCol + col, v);
+          uint8_t* row = qc + (col / kUaBK) * (128 * kUaBK * 2) + t * 128;
+          const int ch0 = (col % kUaBK) / 8;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(row + ((((ch0 + j) ^ (t & 7)) & 7) << 4)) = pack8(v + 8 * j);
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(row + ((((ch0 + j) ^ (t & 7)) & 7) << 4)) = pack8(v + 8 * j);
+        }
       }
-      // q_r: 32 columns = pairs p0..p0+15 (p0 = 0, 16) of this head, RoPE, -> query_rope
-#pragma unroll
-      for (int blk = 0; blk < kDr / 32; ++blk) {
+      // rope blocks: 32 columns = pairs p0..p0+15 (p0 = 16 * (g % 2)) of head g / 2, RoPE,
+      // -> query_rope
+#pragma unroll 1
+      for (int j = 0; j < pl.nrope; ++j, col += 32) {
         float y[32];
-        tmem_ld32(lane_base + kUaUpCol + kD + blk * 32, y);
+        tmem_ld32(lane_base + kUaUpCol + col, y);
+        const int g = pl.g0 + pl.gs * j;
+        const int half = g & 1;
         if (live) {
           float c0[16], s0[16], c1[16], s1[16];
-          unpack16(cs[blk][0], cs[blk][1], c0);
-          unpack16(sn[blk][0], sn[blk][1], s0);
-          unpack16(cs[blk][2], cs[blk][3], c1);
-          unpack16(sn[blk][2], sn[blk][3], s1);
+          unpack16(half ? cs[1][0] : cs[0][0], half ? cs[1][1] : cs[0][1], c0);
+          unpack16(half ? sn[1][0] : sn[0][0], half ? sn[1][1] : sn[0][1], s0);
+          unpack16(half ? cs[1][2] : cs[0][2], half ? cs[1][3] : cs[0][3], c1);
+          unpack16(half ? sn[1][2] : sn[0][2], half ? sn[1][3] : sn[0][3], s1);
           float oa[16], ob[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -291,7 +337,8 @@ __global__ void __launch_bounds__(kUaThreads, 1)
             oa[i] = y0 * c0[i] - y1 * s0[i];
             ob[i] = y1 * c1[i] + y0 * s1[i];
           }
-          __nv_bfloat16* out = p.qr_out + (static_cast<size_t>(t) * p.N + n) * kDr + blk * 16;
+          __nv_bfloat16* out =
+              p.qr_out + (static_cast<size_t>(t) * p.N + (g >> 1)) * kDr + half * 16;
           uint4* da = reinterpret_cast<uint4*>(out);
           uint4* db = reinterpret_cast<uint4*>(out + kDr / 2);
           da[0] = pack8(oa);
@@ -300,13 +347,15 @@ __global__ void __launch_bounds__(kUaThreads, 1)
           db[1] = pack8(ob + 8);
         }
       }
-      tc_fence_before_sync();
-      fence_proxy_async_shared();                      // q^C stores -> visible to the MMA
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qc_bar);
-      ok = mbar_wait(ab_bar, 0, abort_flag);
+      if (pl.head) {
+        tc_fence_before_sync();
+        fence_proxy_async_shared();                    // q^C stores -> visible to the MMA
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qc_bar);
+        ok = mbar_wait(ab_bar, 0, abort_flag);
+      }
     }
-    if (ok) {
+    if (ok && pl.head) {
       tc_fence_after_sync();
       __nv_bfloat16* out = p.q_out + (static_cast<size_t>(t) * p.N + n) * p.Hckv;
 #pragma unroll 1
@@ -333,6 +382,22 @@ __global__ void __launch_bounds__(kUaThreads, 1)
 
 }  // namespace
 
+void up_absorb_plan(int sms, int N, int* k, int* R) {
+  // rope blocks per head CTA (k) and rope CTAs (R) so that the CTAs stream about the same weight
+  // bytes and a rope CTA takes at most 6 blocks
+  *R = sms - N;
+  if (*R > 0 && 2 * N <= 6 * *R) {
+    *k = 0;
+    if (*R > 2 * N) *R = 2 * N;
+  } else if (*R > 0 && N <= 6 * *R) {
+    *k = 1;
+    if (*R > N) *R = N;
+  } else {
+    *k = 2;
+    *R = 0;
+  }
+}
+
 bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hckv) {
   return T >= 1 && T <= 128 && N >= 1 && D == kD && Dr == kDr && Hckv >= 32 && Hckv <= 512 &&
          Hckv % 32 == 0;
@@ -345,7 +410,7 @@ cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
       cudaFuncSetAttribute(up_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUaSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.N));
+  cfg.gridDim = dim3(static_cast<unsigned>(p.N + p.R));
   cfg.blockDim = dim3(kUaThreads);
   cfg.dynamicSmemBytes = kUaSmem;
   cfg.stream = stream;

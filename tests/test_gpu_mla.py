@@ -264,6 +264,7 @@ FUSED_SHAPES = [
     dict(B=100, S=1, He=256, Hcq=136, Hckv=288, N=64),             # ragged K, absorb 256 + 32
     dict(B=33, S=1, He=320, Hcq=192, Hckv=96, N=80),               # 80 heads, one short chunk
     dict(B=4, S=32, He=256, Hcq=128, Hckv=512, N=64),              # BSH-shaped T = 128
+    dict(B=3, S=1, He=256, Hcq=128, Hckv=64, N=128),               # heads keep one W^QR block
 ]
 
 
