@@ -99,26 +99,39 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def _kernel_source_hash():
+# Sources of each timed kernel: a recorded DRAM traffic figure stays valid while they are unchanged.
+KERNEL_SOURCES = {
+    "up_absorb": ["up_absorb.cu", "ptx.cuh"],
+    "down": ["gemm_down.cu", "gemm.cuh", "epilogues.cuh", "gemm_launch.cuh", "ptx.cuh"],
+    "up": ["gemm_up.cu", "gemm.cuh", "epilogues.cuh", "gemm_launch.cuh", "ptx.cuh"],
+    "absorb": ["gemm_absorb.cu", "gemm.cuh", "epilogues.cuh", "gemm_launch.cuh", "ptx.cuh"],
+    "norm_scatter": ["mla_norm_scatter.cu"],
+    "qkv_rnrc": ["qkv_rnrc.cu"],
+}
+
+
+def kernel_source_hash(kernel_key):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "qkv_attention_prolog_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel_key]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def _ncu_traffic(kernel_key, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel's
+    current sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
+        ent = rec[workload][kernel_key]
     except Exception:
         return None
-    if rec.get("source_hash") != _kernel_source_hash():
+    if ent.get("sources") != kernel_source_hash(kernel_key):
         return None
-    return rec.get(workload, {}).get(kernel_key)
+    return ent.get("bytes")
 
 
 # ------------------------------------------------------------------------------- clocks
