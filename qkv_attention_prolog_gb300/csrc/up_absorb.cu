@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(kUaThreads, 1)
   uint64_t* empty_bar = full_bar + kUaStages;
   uint64_t* up_bar = empty_bar + kUaStages;            // up accumulator complete
   uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, up accumulator drained
-  uint64_t* ab_bar = qc_bar + 1;                       // absorb accumulator complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 1);
+  uint64_t* ab_bar = qc_bar + 1;                       // absorb chunk h complete (h < 2)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(kUaThreads, 1)
     }
     mbar_init(up_bar, 1);
     mbar_init(qc_bar, 4);
-    mbar_init(ab_bar, 1);
+    mbar_init(&ab_bar[0], 1);
+    mbar_init(&ab_bar[1], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -276,8 +277,8 @@ __global__ void __launch_bounds__(kUaThreads, 1)
               phase ^= 1u;
             }
           }
+          if (ok) umma_commit(&ab_bar[h]);   // its stores overlap the next chunk's W^UK loads
         }
-        if (ok) umma_commit(ab_bar);
       }
     }
   } else if (warp >= 4) {
@@ -352,20 +353,23 @@ __global__ void __launch_bounds__(kUaThreads, 1)
         fence_proxy_async_shared();                    // q^C stores -> visible to the MMA
         __syncwarp();
         if (lane == 0) mbar_arrive(qc_bar);
-        ok = mbar_wait(ab_bar, 0, abort_flag);
       }
     }
     if (ok && pl.head) {
-      tc_fence_after_sync();
       __nv_bfloat16* out = p.q_out + (static_cast<size_t>(t) * p.N + n) * p.Hckv;
+      for (int h = 0; h < nh; ++h) {
+        if (!mbar_wait(&ab_bar[h], 0, abort_flag)) break;
+        tc_fence_after_sync();
+        const int c1 = p.Hckv < (h + 1) * 256 ? p.Hckv : (h + 1) * 256;
 #pragma unroll 1
-      for (int c = 0; c < p.Hckv; c += 32) {
-        float v[32];
-        tmem_ld32(lane_base + static_cast<uint32_t>(c), v);
-        if (live) {
-          uint4* d = reinterpret_cast<uint4*>(out + c);
+        for (int c = h * 256; c < c1; c += 32) {
+          float v[32];
+          tmem_ld32(lane_base + static_cast<uint32_t>(c), v);
+          if (live) {
+            uint4* d = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) d[j] = pack8(v + 8 * j);
+            for (int j = 0; j < 4; ++j) d[j] = pack8(v + 8 * j);
+          }
         }
       }
     }
