@@ -102,7 +102,10 @@ struct MlaDims {
 constexpr int kSwapMaxT = 256;   // decode orientation (weights as MMA rows) up to this many tokens
 constexpr int kSplitMaxT = 256;  // down-projection K splits (few output tiles) up to this many tokens
 constexpr int kMaxSplits = 16;
-constexpr int kFusedMinHeads = 64;   // the fused decode up/absorb runs one CTA per head
+// The fused decode up/absorb runs one CTA per head (SMs left over take W^QR rows); from the
+// smallest head count of the pages on it beats the separate kernels (16 heads, T = 8: 20.1 ->
+// 15.0 µs per call).
+constexpr int kFusedMinHeads = 16;
 constexpr size_t kHeaderBytes = 8192;   // error word + stream-K flags
 constexpr size_t kFlagOffset = 4096;    // stream-K "partial written" flags (int32 per CTA)
 constexpr int kMaxStreamKCtas = 1024;   // flags that fit the header
@@ -642,23 +645,36 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
 
   // ---- 3+4 fused at decode: one CTA per head runs the up-projection, keeps q^C in shared
   // memory and multiplies it by the head's W^UK (up_absorb.cu)
-  const bool fused = swap && !d.w_int8 && d.N >= kFusedMinHeads &&
+  const bool fused = swap && d.N >= kFusedMinHeads &&
                      up_absorb_supported(d.T, d.N, d.D, d.Dr, d.Hckv);
   if (fused) {
     CUtensorMap tcq, tw, tuk;
     CHECK_STATUS(make_tmap(&tcq, cq, d.Hcq, d.T, d.Hcq, 128));
-    CHECK_STATUS(make_tmap(&tw, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 32));
+    if (d.w_int8)
+      CHECK_STATUS(make_tmap_i8(&tw, a->weight_uq_qr.data, d.Hcq, Mup, 32));
+    else
+      CHECK_STATUS(make_tmap(&tw, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 32));
     CHECK_STATUS(make_tmap(&tuk, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, 32));
+    // an int8 query is quantised per token and head from a bf16 q^N staged in the workspace
+    __nv_bfloat16* qn_out = d.query_int8 ? reinterpret_cast<__nv_bfloat16*>(wsb + L.qn)
+                                         : static_cast<__nv_bfloat16*>(a->query.data);
     UpAbsorbParams ua{static_cast<const __nv_bfloat16*>(a->rope_cos.data),
                       static_cast<const __nv_bfloat16*>(a->rope_sin.data),
                       static_cast<__nv_bfloat16*>(a->query_rope.data),
-                      static_cast<__nv_bfloat16*>(a->query.data),
+                      qn_out,
                       static_cast<int32_t>(d.T), static_cast<int32_t>(d.N),
-                      static_cast<int32_t>(d.Hcq), static_cast<int32_t>(d.Hckv), 2, 0};
+                      static_cast<int32_t>(d.Hcq), static_cast<int32_t>(d.Hckv),
+                      scale_t, static_cast<const float*>(a->dequant_scale_w_uq_qr.data), 2, 0};
     up_absorb_plan(sms, static_cast<int>(d.N), &ua.k, &ua.R);
     CHECK_STATUS(rec(2));
-    ce = launch_up_absorb(tcq, tw, tuk, ua, err, stream);
+    ce = launch_up_absorb(tcq, tw, tuk, ua, d.w_int8, err, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "fused up-projection/absorb launch");
+    if (d.query_int8) {
+      ce = launch_query_quant(qn_out, static_cast<int8_t*>(a->query.data),
+                              static_cast<float*>(a->dequant_scale_q_nope.data), d.T * d.N,
+                              static_cast<int32_t>(d.Hckv), stream);
+      if (ce != cudaSuccess) return cuda_fail(ce, "query quant launch");
+    }
     CHECK_STATUS(rec(3));
     CHECK_STATUS(rec(4));
     if (timer != nullptr) timer->fused[timer->calls] = 1;

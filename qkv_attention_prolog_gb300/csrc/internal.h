@@ -40,17 +40,20 @@ struct UpAbsorbParams {
   __nv_bfloat16* qr_out;        // query_rope (T, N, Dr)
   __nv_bfloat16* q_out;         // query (T, N, Hckv)
   int32_t T, N, Hcq, Hckv;
+  const float* scale_t;         // int8 weight: per-token c^Q quant scale (T)
+  const float* dqw;             // int8 weight: dequant_scale_w_uq_qr (N*(D+Dr))
   int32_t k;                    // W^QR blocks of 32 rows kept by each head CTA (0, 1 or 2)
   int32_t R;                    // CTAs after the N head CTAs that take the other W^QR blocks
 };
 // k and R for `sms` SMs and N heads (grid = N + R)
 void up_absorb_plan(int sms, int N, int* k, int* R);
 bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hckv);
-// tmCq: c^Q (T, Hcq) bf16, box 64 x 128; tmW: prepacked W^UQ|W^QR (N*(D+Dr) rows of Hcq), box
-// 64 x 32; tmUk: prepacked W^UK (N*Hckv rows of D), box 64 x 32; all 128B-swizzled.
+// tmCq: c^Q (T, Hcq) bf16, box 64 x 128, 128B-swizzled; tmW: prepacked W^UQ|W^QR
+// (N*(D+Dr) rows of Hcq), box 64 x 32, bf16 128B-swizzled or int8 unswizzled (int8 = true);
+// tmUk: prepacked W^UK (N*Hckv rows of D), box 64 x 32, 128B-swizzled.
 cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
-                             const CUtensorMap& tmUk, const UpAbsorbParams& p, uint32_t* err,
-                             cudaStream_t stream);
+                             const CUtensorMap& tmUk, const UpAbsorbParams& p, bool int8,
+                             uint32_t* err, cudaStream_t stream);
 cudaError_t launch_absorb(const GemmLaunch& L, const AbsorbParams& p);
 
 // RmsNorm of c^Q (+ dynamic int8 quant) and c^KV, RoPE of k^R, cache quant and scatter; one CTA

@@ -19,9 +19,11 @@
 // blocks (192 rows) each; a rope CTA runs only the up-projection and RoPE.
 //
 // Roles: warp 0 lane 0 TMA producer, warp 1 lane 0 MMA issuer, warp 2 TMEM owner, warps 4..7
-// epilogue (warp 4 + q owns TMEM lanes 32q..32q+31, i.e. tokens 32q..32q+31).  Every mbarrier
-// wait is bounded; on a timeout the CTA lets its issued loads land, frees TMEM and latches the
-// error word.
+// epilogue (warp 4 + q owns TMEM lanes 32q..32q+31, i.e. tokens 32q..32q+31), and with an int8
+// W^UQ|W^QR (partial and full quant) warps 8..11 expand each raw int8 tile to bf16 in the
+// operand layout (exact), the epilogue dequantising acc * scale_t[t] * dequant_scale_w_uq_qr[col]
+// before q^C is rounded and q_r rotated.  Every mbarrier wait is bounded; on a timeout the CTA
+// lets its issued loads land, frees TMEM and latches the error word.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -31,15 +33,21 @@ namespace mlap {
 
 namespace {
 
-constexpr int kUaThreads = 256;
-constexpr int kUaStages = 4;
 constexpr int kUaBK = 64;                              // K elements per stage
 constexpr int kUaA = 128 * kUaBK * 2;                  // c^Q tile: 128 tokens x 64 (16 KB)
 constexpr int kUaB = 256 * kUaBK * 2;                  // weight tile: up to 256 rows (32 KB)
-constexpr int kUaStage = kUaA + kUaB;
 constexpr int kUaQc = 2 * 128 * kUaBK * 2;             // q^C operand: 128 tokens x D = 128
 constexpr int kUaBars = 512;
-constexpr int kUaSmem = kUaStages * kUaStage + kUaQc + kUaBars + 1024;   // + alignment slack
+
+template <bool INT8>
+struct UaCfg {
+  static constexpr int THREADS = INT8 ? 384 : 256;
+  static constexpr int STAGES = INT8 ? 3 : 4;
+  static constexpr int RAW = INT8 ? 192 * kUaBK : 0;   // raw int8 weight tile (192 rows max)
+  static constexpr int STAGE = kUaA + kUaB + RAW;
+  static constexpr int SMEM = STAGES * STAGE + kUaQc + kUaBars + 1024;   // + alignment slack
+  static_assert(STAGE % 1024 == 0 && SMEM <= 232448, "shared memory layout");
+};
 constexpr uint32_t kUaUpCol = 256;                     // TMEM column of the up accumulator
 constexpr int kD = 128;
 constexpr int kDr = 64;
@@ -99,18 +107,23 @@ __device__ __forceinline__ UaPlan ua_plan(const UpAbsorbParams& p) {
   return pl;
 }
 
-__global__ void __launch_bounds__(kUaThreads, 1)
+template <bool INT8>
+__global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     up_absorb_kernel(const __grid_constant__ CUtensorMap tmCq,   // c^Q (T, Hcq), box 64 x 128
                      const __grid_constant__ CUtensorMap tmW,    // W^UQ|W^QR rows, box 64 x 32
                      const __grid_constant__ CUtensorMap tmUk,   // W^UK rows, box 64 x 32
                      const UpAbsorbParams p, uint32_t* __restrict__ err_word) {
+  using Cfg = UaCfg<INT8>;
+  constexpr int kUaStages = Cfg::STAGES;
+  constexpr int kUaStage = Cfg::STAGE;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* qc = smem + kUaStages * kUaStage;           // q^C operand (two 64-wide K blocks)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(qc + kUaQc);
   uint64_t* empty_bar = full_bar + kUaStages;
-  uint64_t* up_bar = empty_bar + kUaStages;            // up accumulator complete
+  uint64_t* rawf_bar = empty_bar + kUaStages;          // int8: raw weight tile landed
+  uint64_t* up_bar = rawf_bar + kUaStages;             // up accumulator complete
   uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, up accumulator drained
   uint64_t* ab_bar = qc_bar + 1;                       // absorb chunk h complete (h < 2)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 2);
@@ -131,8 +144,9 @@ __global__ void __launch_bounds__(kUaThreads, 1)
   }
   if (warp == 1 && lane == 0) {
     for (int i = 0; i < kUaStages; ++i) {
-      mbar_init(&full_bar[i], 1);
+      mbar_init(&full_bar[i], INT8 ? 1 + 4 : 1);   // producer (+ the four converter warps)
       mbar_init(&empty_bar[i], 1);
+      mbar_init(&rawf_bar[i], 1);
     }
     mbar_init(up_bar, 1);
     mbar_init(qc_bar, 4);
@@ -156,7 +170,8 @@ __global__ void __launch_bounds__(kUaThreads, 1)
 
   if (producer) {
     // ------------------------------------------------------------------ TMA producer
-    int fills[kUaStages] = {0, 0, 0, 0};
+    int fills[kUaStages] = {};
+    int rawfills[kUaStages] = {};
     // head n's W^UQ rows (D), then this CTA's rope blocks: up to six 32-row boxes per tile,
     // their first weight rows computed once
     const int nbox = up_rows / 32;
@@ -167,11 +182,20 @@ __global__ void __launch_bounds__(kUaThreads, 1)
       ybox[j] = jr < 0 ? n * kD + 32 * j : p.N * kD + 32 * (pl.g0 + pl.gs * jr);
     }
     auto issue_w = [&](int st, int kb) {
-      uint8_t* b = smem + st * kUaStage + kUaA;
-      mbar_expect_tx(&full_bar[st], static_cast<uint32_t>(up_rows) * kUaBK * 2);
+      if constexpr (INT8) {   // raw int8 rows of 64 B, expanded by the converter warps
+        uint8_t* r = smem + st * kUaStage + kUaA + kUaB;
+        mbar_arrive_expect_tx(&rawf_bar[st], static_cast<uint32_t>(up_rows) * kUaBK);
+        ++rawfills[st];
 #pragma unroll
-      for (int j = 0; j < 6; ++j)
-        if (j < nbox) tma_load_2d(b + j * 4096, &tmW, &full_bar[st], kb * kUaBK, ybox[j]);
+        for (int j = 0; j < 6; ++j)
+          if (j < nbox) tma_load_2d(r + j * 2048, &tmW, &rawf_bar[st], kb * kUaBK, ybox[j]);
+      } else {
+        uint8_t* b = smem + st * kUaStage + kUaA;
+        mbar_expect_tx(&full_bar[st], static_cast<uint32_t>(up_rows) * kUaBK * 2);
+#pragma unroll
+        for (int j = 0; j < 6; ++j)
+          if (j < nbox) tma_load_2d(b + j * 4096, &tmW, &full_bar[st], kb * kUaBK, ybox[j]);
+      }
     };
     const int pre = kb_up < kUaStages ? kb_up : kUaStages;
     for (int i = 0; i < pre; ++i) issue_w(i, i);      // weights do not depend on earlier kernels
@@ -222,6 +246,11 @@ __global__ void __launch_bounds__(kUaThreads, 1)
         if (fills[i] == 0 && i >= pre) continue;
         const uint32_t par = static_cast<uint32_t>((fills[i] > 0 ? fills[i] : 1) - 1) & 1u;
         while (!mbar_try_wait(&full_bar[i], par) && globaltimer_ns() - t0 < 20000000ull) {
+        }
+        if (INT8 && rawfills[i] > 0) {   // the raw tile of stage i's last up-projection fill
+          const uint32_t rp = static_cast<uint32_t>(rawfills[i] - 1) & 1u;
+          while (!mbar_try_wait(&rawf_bar[i], rp) && globaltimer_ns() - t0 < 20000000ull) {
+          }
         }
       }
     }
@@ -281,7 +310,40 @@ __global__ void __launch_bounds__(kUaThreads, 1)
         }
       }
     }
-  } else if (warp >= 4) {
+  } else if (INT8 && warp >= 8) {
+    // ------------------------------------------------------------------ int8 -> bf16 converters
+    const int ct = threadIdx.x - 256;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int kb = 0; kb < kb_up; ++kb) {
+      if (!mbar_wait(&rawf_bar[stage], phase, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* raw = smem + stage * kUaStage + kUaA + kUaB;
+      uint8_t* dst = smem + stage * kUaStage + kUaA;
+      for (int r = ct; r < up_rows; r += 128) convert_int8_row(raw + r * kUaBK, dst, r);
+      fence_proxy_async_shared();                      // generic writes -> the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full_bar[stage]);
+      if (++stage == kUaStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    // the W^UK tiles are bf16: each converter warp only adds its arrival, once the stage's
+    // previous round has been consumed (so that it cannot count toward that round)
+    for (int i = 0; ok && i < nh * (kD / kUaBK); ++i) {
+      if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full_bar[stage]);
+      if (++stage == kUaStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp - 4;
     const int t = q * 32 + lane;                       // token of this lane
@@ -300,6 +362,8 @@ __global__ void __launch_bounds__(kUaThreads, 1)
         sn[i >> 1][2 + (i & 1)] = __ldg(s + 4 + i);
       }
     }
+    // int8 weight: acc * scale_t[t] * dequant_scale_w_uq_qr[original column]
+    const float st = INT8 && live ? __ldg(p.scale_t + t) : 0.f;
     bool ok = mbar_wait(up_bar, 0, abort_flag);
     if (ok) {
       tc_fence_after_sync();
@@ -310,6 +374,11 @@ __global__ void __launch_bounds__(kUaThreads, 1)
         for (; col < kD; col += 32) {
           float v[32];
           tmem_ld32(lane_base + kUaUpCol + col, v);
+          if constexpr (INT8) {   // nope row n*D + col + j is column n*(D+Dr) + col + j
+            const float* dq = p.dqw + n * (kD + kDr) + col;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = v[j] * st * __ldg(dq + j);
+          }
           uint8_t* row = qc + (col / kUaBK) * (128 * kUaBK * 2) + t * 128;
           const int ch0 = (col % kUaBK) / 8;
 #pragma unroll
@@ -325,6 +394,11 @@ __global__ void __launch_bounds__(kUaThreads, 1)
         tmem_ld32(lane_base + kUaUpCol + col, y);
         const int g = pl.g0 + pl.gs * j;
         const int half = g & 1;
+        if constexpr (INT8) {   // rope row i of head g/2 is column D + i/2 + (i%2)*Dr/2
+          const float* dq = p.dqw + (g >> 1) * (kD + kDr) + kD + half * 16;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = y[i] * st * __ldg(dq + (i >> 1) + (i & 1) * (kDr / 2));
+        }
         if (live) {
           float c0[16], s0[16], c1[16], s1[16];
           unpack16(half ? cs[1][0] : cs[0][0], half ? cs[1][1] : cs[0][1], c0);
@@ -407,23 +481,32 @@ bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hc
          Hckv % 32 == 0;
 }
 
-cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
-                             const CUtensorMap& tmUk, const UpAbsorbParams& p, uint32_t* err,
-                             cudaStream_t stream) {
-  cudaError_t e =
-      cudaFuncSetAttribute(up_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUaSmem);
+template <bool INT8>
+static cudaError_t launch_ua_t(const CUtensorMap& tmCq, const CUtensorMap& tmW,
+                               const CUtensorMap& tmUk, const UpAbsorbParams& p, uint32_t* err,
+                               cudaStream_t stream) {
+  auto kern = up_absorb_kernel<INT8>;
+  constexpr int kSmem = UaCfg<INT8>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.N + p.R));
-  cfg.blockDim = dim3(kUaThreads);
-  cfg.dynamicSmemBytes = kUaSmem;
+  cfg.blockDim = dim3(UaCfg<INT8>::THREADS);
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, up_absorb_kernel, tmCq, tmW, tmUk, p, err);
+  return cudaLaunchKernelEx(&cfg, kern, tmCq, tmW, tmUk, p, err);
+}
+
+cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
+                             const CUtensorMap& tmUk, const UpAbsorbParams& p, bool int8,
+                             uint32_t* err, cudaStream_t stream) {
+  return int8 ? launch_ua_t<true>(tmCq, tmW, tmUk, p, err, stream)
+              : launch_ua_t<false>(tmCq, tmW, tmUk, p, err, stream);
 }
 
 }  // namespace mlap

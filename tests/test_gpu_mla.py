@@ -257,7 +257,7 @@ def test_rms_norm_quant_bsh_leaves_token_x():
                        cpu["token_x"].view(torch.int16))
 
 
-# ---- fused decode up-projection + absorb (one CTA per head, T <= 128, N >= 64, bf16 weight)
+# ---- fused decode up-projection + absorb (one CTA per head, T <= 128, N >= 16, bf16 weight)
 
 FUSED_SHAPES = [
     dict(B=1, S=1, N=64),                                          # single token
@@ -265,6 +265,14 @@ FUSED_SHAPES = [
     dict(B=33, S=1, He=320, Hcq=192, Hckv=96, N=80),               # 80 heads, one short chunk
     dict(B=4, S=32, He=256, Hcq=128, Hckv=512, N=64),              # BSH-shaped T = 128
     dict(B=3, S=1, He=256, Hcq=128, Hckv=64, N=128),               # heads keep one W^QR block
+    dict(B=7, S=1, He=256, Hcq=320, Hckv=160, N=32),               # 32 heads + 64 rope CTAs
+    # int8 weight_uq_qr (converter warps, dequant in the epilogue)
+    dict(B=9, S=1, He=256, Hcq=192, Hckv=96, N=16, weight_uq_qr_dtype="int8",
+         cache_dtype="int8"),                                       # partial quant
+    dict(B=5, S=1, He=256, Hcq=144, Hckv=128, N=32, weight_uq_qr_dtype="int8",
+         cache_dtype="bf16"),                                       # ragged K, bf16 caches
+    dict(B=6, S=1, He=256, Hcq=128, Hckv=64, N=128, weight_uq_qr_dtype="int8",
+         cache_dtype="int8", full_quant=True),                      # full quant, int8 query
 ]
 
 
