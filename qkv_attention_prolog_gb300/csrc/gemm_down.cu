@@ -36,6 +36,7 @@ cudaError_t launch_down(const GemmLaunch& L, const DownParams& p) {
       default: return cudaErrorInvalidValue;
     }
   }
+  if (L.bn == 256) return launch_gemm_t<256>(L, EpiDown<false, 256, 32>{p});
   if (L.bn != 192) return cudaErrorInvalidValue;
   return launch_gemm_t<192>(L, EpiDown<false, 192, 32>{p});
 }
