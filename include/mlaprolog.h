@@ -186,6 +186,15 @@ mlap_status_t mlap_execute(const mlap_args_t* args, void* workspace, size_t work
  * MLAP_ERR_INDEX_RANGE or MLAP_ERR_TIMEOUT (index errors take precedence), or MLAP_ERR_CUDA. */
 mlap_status_t mlap_check_errors(void* workspace, void* stream);
 
+/* Exercise the kernels' failure path: launches one kernel that waits, with the same bounded
+ * wait as every kernel of the library, on a barrier that nothing completes.  The wait gives up
+ * after its limit (about 2 s), and the kernel latches the timeout bit in the workspace error
+ * word, so a following mlap_check_errors returns MLAP_ERR_TIMEOUT (and clears the word, as it
+ * always does).  Nothing faults or hangs.
+ * Asynchronous on `stream`.  Errors: MLAP_ERR_NULL, MLAP_ERR_WORKSPACE (fewer than 256 bytes),
+ * MLAP_ERR_CUDA. */
+mlap_status_t mlap_selftest_bounded_wait(void* workspace, size_t workspace_bytes, void* stream);
+
 /* ============================================================================================ */
 /* QkvRmsNormRopeCache (aclnnQkvRmsNormRopeCache)                                                */
 /* ============================================================================================ */

@@ -32,7 +32,7 @@ EXPORTS = ["mlap_prepack_size", "mlap_prepack_weights", "mlap_get_workspace_size
            "mlap_workspace_init", "mlap_execute", "mlap_check_errors",
            "qkvrnrc_get_workspace_size", "qkvrnrc_execute", "mlap_status_string",
            "mlap_last_error", "mlap_timer_create", "mlap_execute_timed", "mlap_timer_read",
-           "mlap_timer_destroy", "mlap_execute_no_alloc"]
+           "mlap_timer_destroy", "mlap_execute_no_alloc", "mlap_selftest_bounded_wait"]
 
 
 class MlapError(RuntimeError):
@@ -101,6 +101,7 @@ def load() -> ctypes.CDLL:
         "mlap_workspace_init": (st, [vp, ctypes.c_size_t, vp]),
         "mlap_execute": (st, [A, vp, ctypes.c_size_t, vp]),
         "mlap_check_errors": (st, [vp, vp]),
+        "mlap_selftest_bounded_wait": (st, [vp, ctypes.c_size_t, vp]),
         "qkvrnrc_get_workspace_size": (st, [Q, sz]),
         "qkvrnrc_execute": (st, [Q, vp, ctypes.c_size_t, vp]),
         "mlap_status_string": (ctypes.c_char_p, [st]),
@@ -236,6 +237,13 @@ def mlap_execute_no_alloc(args: mlap_args_t, stream=None):
 def mlap_check_errors(ws: torch.Tensor, stream=None) -> int:
     """Returns the status code (0 = OK); does not raise for kernel-reported errors."""
     return int(load().mlap_check_errors(ws.data_ptr(), _stream_ptr(stream)))
+
+
+def mlap_selftest_bounded_wait(ws: torch.Tensor, stream=None):
+    """Run the library's bounded wait on a barrier nothing completes (about 2 s on the GPU);
+    mlap_check_errors(ws) then reports MLAP_ERR_TIMEOUT."""
+    _check(load().mlap_selftest_bounded_wait(ws.data_ptr(), ws.numel() * ws.element_size(),
+                                             _stream_ptr(stream)), "mlap_selftest_bounded_wait")
 
 
 # --------------------------------------------------------------------------------- QKV entry

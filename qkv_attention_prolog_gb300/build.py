@@ -15,7 +15,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmlaprolog.so")
 
 SOURCES = ["api.cu", "gemm_down.cu", "gemm_up.cu", "gemm_absorb.cu", "mla_norm_scatter.cu",
-           "qkv_rnrc.cu", "up_absorb.cu"]
+           "qkv_rnrc.cu", "up_absorb.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -1079,6 +1079,15 @@ mlap_status_t mlap_check_errors(void* ws, void* stream) {
   return MLAP_OK;
 }
 
+mlap_status_t mlap_selftest_bounded_wait(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr) return fail(MLAP_ERR_NULL, "workspace is NULL");
+  if (ws_bytes < 256) return fail(MLAP_ERR_WORKSPACE, "workspace smaller than 256 bytes");
+  cudaError_t e = launch_bounded_wait_selftest(static_cast<uint32_t*>(ws),
+                                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self-test launch");
+  return MLAP_OK;
+}
+
 mlap_status_t qkvrnrc_get_workspace_size(const qkvrnrc_args_t* args, size_t* bytes) {
   if (bytes == nullptr) return fail(MLAP_ERR_NULL, "bytes is NULL");
   QkvDims d;

@@ -45,6 +45,10 @@ struct UpAbsorbParams {
   int32_t k;                    // W^QR blocks of 32 rows kept by each head CTA (0, 1 or 2)
   int32_t R;                    // CTAs after the N head CTAs that take the other W^QR blocks
 };
+// One CTA whose bounded mbarrier wait runs out (nothing completes the barrier) and latches
+// kErrTimeout in err_word (selftest.cu).
+cudaError_t launch_bounded_wait_selftest(uint32_t* err_word, cudaStream_t stream);
+
 // k and R for `sms` SMs and N heads (grid = N + R)
 void up_absorb_plan(int sms, int N, int* k, int* R);
 bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hckv);
