@@ -4,7 +4,7 @@
 //   1. [q^C_n | q_r,n] = c^Q · [W^UQ_n | W^QR_n]   K = Hcq, N = D + Dr = 192 columns in TMEM
 //   2. epilogue: q^C_n rounded to bf16 into shared memory, laid out as the next MMA's A operand;
 //      q_r,n rotated (half-and-half RoPE of aclnnQkvRmsNormRopeCache "Formulas" (3)) -> query_rope
-//   3. q^N_n = q^C_n · W^UK_n                         K = D, N = Hckv (chunks of 256 columns)
+//   3. q^N_n = q^C_n · W^UK_n                         K = D, N = Hckv (chunks of 192 columns)
 //   4. epilogue: q^N_n rounded to bf16 -> query
 //
 // q^C never leaves the SM, and the head's W^UK tiles stream through the same pipeline right
@@ -35,14 +35,16 @@ namespace {
 
 constexpr int kUaBK = 64;                              // K elements per stage
 constexpr int kUaA = 128 * kUaBK * 2;                  // c^Q tile: 128 tokens x 64 (16 KB)
-constexpr int kUaB = 256 * kUaBK * 2;                  // weight tile: up to 256 rows (32 KB)
+constexpr int kUaWRows = 192;                          // weight tile rows: D + Dr, W^UK chunks
+constexpr int kUaB = kUaWRows * kUaBK * 2;             // 24 KB
 constexpr int kUaQc = 2 * 128 * kUaBK * 2;             // q^C operand: 128 tokens x D = 128
 constexpr int kUaBars = 512;
 
 template <bool INT8>
 struct UaCfg {
   static constexpr int THREADS = INT8 ? 384 : 256;
-  static constexpr int STAGES = INT8 ? 3 : 4;
+  static constexpr int STAGES = INT8 ? 3 : 4;   // bf16: 198 KB in all, which leaves room on
+                                                 // an SM for a CTA of the kernel before it
   static constexpr int RAW = INT8 ? 192 * kUaBK : 0;   // raw int8 weight tile (192 rows max)
   static constexpr int STAGE = kUaA + kUaB + RAW;
   static constexpr int SMEM = STAGES * STAGE + kUaQc + kUaBars + 1024;   // + alignment slack
@@ -125,8 +127,8 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   uint64_t* rawf_bar = empty_bar + kUaStages;          // int8: raw weight tile landed
   uint64_t* up_bar = rawf_bar + kUaStages;             // up accumulator complete
   uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, up accumulator drained
-  uint64_t* ab_bar = qc_bar + 1;                       // absorb chunk h complete (h < 2)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 2);
+  uint64_t* ab_bar = qc_bar + 1;                       // absorb chunk h complete (h < 3)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   const UaPlan pl = ua_plan(p);
   const int n = blockIdx.x;                            // head (head CTAs)
   const int kb_up = (p.Hcq + kUaBK - 1) / kUaBK;
-  const int nh = pl.head ? (p.Hckv + 255) / 256 : 0;   // absorb column chunks
+  const int nh = pl.head ? (p.Hckv + kUaWRows - 1) / kUaWRows : 0;   // absorb column chunks
   const int up_rows = (pl.head ? kD : 0) + 32 * pl.nrope;   // B rows of the up-projection
 
   if (warp == 0 && lane == 0) {
@@ -150,8 +152,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     }
     mbar_init(up_bar, 1);
     mbar_init(qc_bar, 4);
-    mbar_init(&ab_bar[0], 1);
-    mbar_init(&ab_bar[1], 1);
+    for (int h = 0; h < 3; ++h) mbar_init(&ab_bar[h], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -219,9 +220,9 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         phase ^= 1u;
       }
     }
-    // head n's W^UK rows, chunk h of 256 rows, K block kb2 of D
+    // head n's W^UK rows, chunk h of 192 rows, K block kb2 of D
     for (int h = 0; ok && h < nh; ++h) {
-      const int rows = p.Hckv - h * 256 < 256 ? p.Hckv - h * 256 : 256;
+      const int rows = p.Hckv - h * kUaWRows < kUaWRows ? p.Hckv - h * kUaWRows : kUaWRows;
       for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2) {
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
           ok = false;
@@ -230,7 +231,8 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         uint8_t* b = smem + stage * kUaStage + kUaA;
         mbar_arrive_expect_tx(&full_bar[stage], rows * kUaBK * 2);
         for (int r = 0; r < rows; r += 32)
-          tma_load_2d(b + r * 128, &tmUk, &full_bar[stage], kb2 * kUaBK, n * p.Hckv + h * 256 + r);
+          tma_load_2d(b + r * 128, &tmUk, &full_bar[stage], kb2 * kUaBK,
+                      n * p.Hckv + h * kUaWRows + r);
         ++fills[stage];
         if (++stage == kUaStages) {
           stage = 0;
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         tc_fence_after_sync();
         const uint32_t qa = smem_u32(qc);
         for (int h = 0; ok && h < nh; ++h) {
-          const int rows = p.Hckv - h * 256 < 256 ? p.Hckv - h * 256 : 256;
+          const int rows = p.Hckv - h * kUaWRows < kUaWRows ? p.Hckv - h * kUaWRows : kUaWRows;
           const uint32_t idesc_ab = idesc_bf16_f32(128, rows);
           for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2) {
             if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
             const uint32_t b = smem_u32(smem + stage * kUaStage) + kUaA;
 #pragma unroll
             for (int kk = 0; kk < kUaBK / 16; ++kk)
-              umma_bf16_ss(tmem_base + static_cast<uint32_t>(h * 256),
+              umma_bf16_ss(tmem_base + static_cast<uint32_t>(h * kUaWRows),
                            sdesc_kmajor_sw128(qa + kb2 * (128 * kUaBK * 2) + kk * 32),
                            sdesc_kmajor_sw128(b + kk * 32), idesc_ab,
                            (kb2 > 0 || kk > 0) ? 1u : 0u);
@@ -434,9 +436,9 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       for (int h = 0; h < nh; ++h) {
         if (!mbar_wait(&ab_bar[h], 0, abort_flag)) break;
         tc_fence_after_sync();
-        const int c1 = p.Hckv < (h + 1) * 256 ? p.Hckv : (h + 1) * 256;
+        const int c1 = p.Hckv < (h + 1) * kUaWRows ? p.Hckv : (h + 1) * kUaWRows;
 #pragma unroll 1
-        for (int c = h * 256; c < c1; c += 32) {
+        for (int c = h * kUaWRows; c < c1; c += 32) {
           float v[32];
           tmem_ld32(lane_base + static_cast<uint32_t>(c), v);
           if (live) {
