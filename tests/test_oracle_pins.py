@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from oracle.mla_prolog import mla_prolog_tokens
+from oracle.mla_prolog import mla_key_rows, mla_prolog_tokens
 from tests import bruteforce as bf
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -364,6 +364,24 @@ def test_cache_invariants():
         k = [0, 2].index(t)
         np.testing.assert_array_equal(out["kv_cache"][slot // 2, slot % 2, 0], sub["kv_rows"][k])
         np.testing.assert_array_equal(out["kr_cache"][slot // 2, slot % 2, 0], sub["kr_rows"][k])
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(xnorm="channel"), dict(int8=True, int8_cache=True),
+                                dict(int8=True, int8_cache=True, full=True)],
+                         ids=["bf16", "rms_norm_quant", "partial_quant", "full_quant"])
+def test_key_rows_agree_with_the_prolog(kw):
+    # mla_key_rows (the key path alone, used for every cache slot of the large GPU workloads)
+    # gives exactly the rows mla_prolog scatters
+    rng = np.random.default_rng(16)
+    inp = _tiny_mla(rng, T=3, **kw)
+    inp["cache_index"] = np.array([0, 3, 5])
+    out = oracle.mla_prolog(**inp)
+    kv, kr = mla_key_rows(**inp, Hckv=inp["weight_uk"].shape[2],
+                          kv_dtype_int8=np.asarray(inp["kv_cache"]).dtype == np.int8,
+                          kr_dtype_int8=np.asarray(inp["kr_cache"]).dtype == np.int8)
+    for t, slot in enumerate([0, 3, 5]):
+        np.testing.assert_array_equal(out["kv_cache"][slot // 2, slot % 2, 0], kv[t])
+        np.testing.assert_array_equal(out["kr_cache"][slot // 2, slot % 2, 0], kr[t])
 
 
 def test_int8_matmul_is_exact_integer_product():
