@@ -40,15 +40,18 @@ constexpr int kUaB = kUaWRows * kUaBK * 2;             // 24 KB
 constexpr int kUaQc = 2 * 128 * kUaBK * 2;             // q^C operand: 128 tokens x D = 128
 constexpr int kUaBars = 512;
 
+// STAGES operand stages (c^Q tile + bf16 weight tile); int8: RSTAGES raw weight tiles in a ring
+// of their own, filled by a second producer thread, so that more of the weight stream is in
+// flight than there are operand stages.
 template <bool INT8>
 struct UaCfg {
   static constexpr int THREADS = INT8 ? 384 : 256;
-  static constexpr int STAGES = INT8 ? 3 : 4;   // bf16: 198 KB in all, which leaves room on
-                                                 // an SM for a CTA of the kernel before it
-  static constexpr int RAW = INT8 ? 192 * kUaBK : 0;   // raw int8 weight tile (192 rows max)
-  static constexpr int STAGE = kUaA + kUaB + RAW;
-  static constexpr int SMEM = STAGES * STAGE + kUaQc + kUaBars + 1024;   // + alignment slack
-  static_assert(STAGE % 1024 == 0 && SMEM <= 232448, "shared memory layout");
+  static constexpr int STAGES = INT8 ? 3 : 4;   // bf16: 198 KB in all
+  static constexpr int RSTAGES = INT8 ? 6 : 0;
+  static constexpr int RAW = 192 * kUaBK;       // raw int8 weight tile (192 rows max)
+  static constexpr int STAGE = kUaA + kUaB;
+  static constexpr int SMEM = STAGES * STAGE + RSTAGES * RAW + kUaQc + kUaBars + 1024;
+  static_assert(STAGE % 1024 == 0 && RAW % 1024 == 0 && SMEM <= 232448, "shared memory layout");
 };
 constexpr uint32_t kUaUpCol = 256;                     // TMEM column of the up accumulator
 constexpr int kD = 128;
@@ -121,11 +124,14 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint8_t* qc = smem + kUaStages * kUaStage;           // q^C operand (two 64-wide K blocks)
+  constexpr int kRS = Cfg::RSTAGES;
+  uint8_t* ring_raw = smem + kUaStages * kUaStage;     // int8: raw weight tiles
+  uint8_t* qc = ring_raw + kRS * Cfg::RAW;             // q^C operand (two 64-wide K blocks)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(qc + kUaQc);
   uint64_t* empty_bar = full_bar + kUaStages;
   uint64_t* rawf_bar = empty_bar + kUaStages;          // int8: raw weight tile landed
-  uint64_t* up_bar = rawf_bar + kUaStages;             // up accumulator complete
+  uint64_t* rawe_bar = rawf_bar + kRS;                 // int8: raw tile converted, slot free
+  uint64_t* up_bar = rawe_bar + (INT8 ? kRS : kUaStages);   // up accumulator complete
   uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, up accumulator drained
   uint64_t* ab_bar = qc_bar + 1;                       // absorb chunk h complete (h < 3)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 3);
@@ -148,7 +154,10 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     for (int i = 0; i < kUaStages; ++i) {
       mbar_init(&full_bar[i], INT8 ? 1 + 4 : 1);   // producer (+ the four converter warps)
       mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < kRS; ++i) {
       mbar_init(&rawf_bar[i], 1);
+      mbar_init(&rawe_bar[i], 4);                   // the four converter warps
     }
     mbar_init(up_bar, 1);
     mbar_init(qc_bar, 4);
@@ -167,12 +176,12 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
 
   grid_launch_dependents();
   const bool producer = warp == 0 && lane == 0;
-  if (!producer) grid_dependency_wait();
+  const bool raw_producer = INT8 && warp == 3 && lane == 0;   // int8 weight tiles only
+  if (!producer && !raw_producer) grid_dependency_wait();
 
   if (producer) {
     // ------------------------------------------------------------------ TMA producer
     int fills[kUaStages] = {};
-    int rawfills[kUaStages] = {};
     // head n's W^UQ rows (D), then this CTA's rope blocks: up to six 32-row boxes per tile,
     // their first weight rows computed once
     const int nbox = up_rows / 32;
@@ -183,14 +192,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       ybox[j] = jr < 0 ? n * kD + 32 * j : p.N * kD + 32 * (pl.g0 + pl.gs * jr);
     }
     auto issue_w = [&](int st, int kb) {
-      if constexpr (INT8) {   // raw int8 rows of 64 B, expanded by the converter warps
-        uint8_t* r = smem + st * kUaStage + kUaA + kUaB;
-        mbar_arrive_expect_tx(&rawf_bar[st], static_cast<uint32_t>(up_rows) * kUaBK);
-        ++rawfills[st];
-#pragma unroll
-        for (int j = 0; j < 6; ++j)
-          if (j < nbox) tma_load_2d(r + j * 2048, &tmW, &rawf_bar[st], kb * kUaBK, ybox[j]);
-      } else {
+      if constexpr (!INT8) {   // (int8 weight tiles come from the raw producer)
         uint8_t* b = smem + st * kUaStage + kUaA;
         mbar_expect_tx(&full_bar[st], static_cast<uint32_t>(up_rows) * kUaBK * 2);
 #pragma unroll
@@ -249,10 +251,40 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         const uint32_t par = static_cast<uint32_t>((fills[i] > 0 ? fills[i] : 1) - 1) & 1u;
         while (!mbar_try_wait(&full_bar[i], par) && globaltimer_ns() - t0 < 20000000ull) {
         }
-        if (INT8 && rawfills[i] > 0) {   // the raw tile of stage i's last up-projection fill
-          const uint32_t rp = static_cast<uint32_t>(rawfills[i] - 1) & 1u;
-          while (!mbar_try_wait(&rawf_bar[i], rp) && globaltimer_ns() - t0 < 20000000ull) {
-          }
+      }
+    }
+  } else if (raw_producer) {
+    // ------------------------------------------------------------------ int8 weight producer
+    // raw int8 rows of 64 B into a ring of kRS tiles, ahead of the operand stages
+    int rawfills[kRS > 0 ? kRS : 1] = {};
+    const int nbox = up_rows / 32;
+    int ybox[6];
+#pragma unroll
+    for (int j = 0; j < 6; ++j) {
+      const int jr = pl.head ? j - kD / 32 : j;
+      ybox[j] = jr < 0 ? n * kD + 32 * j : p.N * kD + 32 * (pl.g0 + pl.gs * jr);
+    }
+    int rs = 0;
+    uint32_t rph = 0;
+    for (int kb = 0; kb < kb_up; ++kb) {
+      if (kb >= kRS && !mbar_wait(&rawe_bar[rs], rph ^ 1u, abort_flag)) break;
+      uint8_t* r = ring_raw + rs * Cfg::RAW;
+      mbar_arrive_expect_tx(&rawf_bar[rs], static_cast<uint32_t>(up_rows) * kUaBK);
+#pragma unroll
+      for (int j = 0; j < 6; ++j)
+        if (j < nbox) tma_load_2d(r + j * 2048, &tmW, &rawf_bar[rs], kb * kUaBK, ybox[j]);
+      ++rawfills[rs];
+      if (++rs == kRS) {
+        rs = 0;
+        rph ^= 1u;
+      }
+    }
+    if (*abort_flag) {   // let every issued raw tile land before the CTA exits
+      const uint64_t t0 = globaltimer_ns();
+      for (int i = 0; i < kRS; ++i) {
+        if (rawfills[i] == 0) continue;
+        const uint32_t par = static_cast<uint32_t>(rawfills[i] - 1) & 1u;
+        while (!mbar_try_wait(&rawf_bar[i], par) && globaltimer_ns() - t0 < 20000000ull) {
         }
       }
     }
@@ -315,23 +347,32 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   } else if (INT8 && warp >= 8) {
     // ------------------------------------------------------------------ int8 -> bf16 converters
     const int ct = threadIdx.x - 256;
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, rs = 0;
+    uint32_t phase = 0, rph = 0;
     bool ok = true;
     for (int kb = 0; kb < kb_up; ++kb) {
-      if (!mbar_wait(&rawf_bar[stage], phase, abort_flag)) {
+      // the raw tile has landed and the operand stage's previous round has been consumed
+      if (!mbar_wait(&rawf_bar[rs], rph, abort_flag) ||
+          !mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
         ok = false;
         break;
       }
-      const uint8_t* raw = smem + stage * kUaStage + kUaA + kUaB;
+      const uint8_t* raw = ring_raw + rs * Cfg::RAW;
       uint8_t* dst = smem + stage * kUaStage + kUaA;
       for (int r = ct; r < up_rows; r += 128) convert_int8_row(raw + r * kUaBK, dst, r);
       fence_proxy_async_shared();                      // generic writes -> the tensor core
       __syncwarp();
-      if (lane == 0) mbar_arrive(&full_bar[stage]);
+      if (lane == 0) {
+        mbar_arrive(&full_bar[stage]);
+        mbar_arrive(&rawe_bar[rs]);                    // raw slot free for the producer
+      }
       if (++stage == kUaStages) {
         stage = 0;
         phase ^= 1u;
+      }
+      if (++rs == kRS) {
+        rs = 0;
+        rph ^= 1u;
       }
     }
     // the W^UK tiles are bf16: each converter warp only adds its arrival, once the stage's
