@@ -19,10 +19,11 @@
 // blocks (192 rows) each; a rope CTA runs only the up-projection and RoPE.
 //
 // Roles: warp 0 lane 0 TMA producer, warp 1 lane 0 MMA issuer, warp 2 TMEM owner, warps 4..7
-// epilogue (warp 4 + q owns TMEM lanes 32q..32q+31, i.e. tokens 32q..32q+31), and with an int8
-// W^UQ|W^QR (partial and full quant) warps 8..11 expand each raw int8 tile to bf16 in the
-// operand layout (exact), the epilogue dequantising acc * scale_t[t] * dequant_scale_w_uq_qr[col]
-// before q^C is rounded and q_r rotated.  Every mbarrier wait is bounded; on a timeout the CTA
+// epilogue (warp 4 + q owns TMEM lanes 32q..32q+31, i.e. tokens 32q..32q+31).  With an int8
+// W^UQ|W^QR (partial and full quant) warp 3 lane 0 loads the raw int8 tiles into a ring of
+// their own, warps 8..11 expand each into the bf16 operand layout (exact), and the epilogue
+// dequantises acc * scale_t[t] * dequant_scale_w_uq_qr[col] before q^C is rounded and q_r
+// rotated.  Every mbarrier wait is bounded; on a timeout the CTA
 // lets its issued loads land, frees TMEM and latches the error word.
 #include <cuda_bf16.h>
 
