@@ -261,8 +261,9 @@ const char* mlap_last_error(void);
  * Phases: 0 down-projection (with the input RmsNormQuant or the full-quant token_x widening
  * ahead of it when those run), 1 RmsNorm/RoPE/scatter, 2 up-projection, 3 absorb (with the int8
  * query quantisation after it in full quant).  Where one kernel runs the up-projection and the
- * absorb together (decode with a bf16 weight_uq_qr, T <= 128, N >= 16, Dr = 64), phase 2 times
- * it and phase 3 reads exactly 0. */
+ * absorb together (decode: T <= 128, N >= 16, D = 128, Dr = 64, Hckv <= 512 and a multiple of
+ * 32), phase 2 times it (and the int8 query quantisation after it in full quant) and phase 3
+ * reads exactly 0. */
 #define MLAP_TIMER_PHASES 4
 mlap_status_t mlap_timer_create(void** timer, int32_t max_calls);
 mlap_status_t mlap_execute_timed(const mlap_args_t* args, void* workspace,
