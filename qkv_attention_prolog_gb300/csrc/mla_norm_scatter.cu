@@ -78,23 +78,30 @@ __device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float* v) {
   *reinterpret_cast<uint4*>(p) = r;
 }
 
-// One CTA per token.  MAXS bounds the K splits (1: prefill, no split; kMaxSplits: decode), NT is
-// the thread count: with splits every thread issues the loads of all splits of its columns at
-// once (one round of latency), without them the kernel stays small enough for many CTAs per SM.
-template <int MAXS, int NT>
+// One CTA per token, or with PARTS two: CTA 2t the c^Q columns of token t, CTA 2t+1 its c^KV and
+// k^R columns (the two norms are independent), so that the c^Q the next kernel waits for comes
+// from a CTA with less than three quarters of the work.  MAXS bounds the K splits (1: prefill, no
+// split), NT is the thread count: with splits every thread issues the loads of all splits of its
+// columns at once (one round of latency), without them the kernel stays small enough for many
+// CTAs per SM.
+template <int MAXS, int NT, bool PARTS = false>
 __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizeParams p) {
   extern __shared__ float h[];
   __shared__ float2 red[NT / 32];
-  const int t = blockIdx.x;
+  const int t = PARTS ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const bool do_q = !PARTS || (blockIdx.x & 1) == 0;
+  const bool do_kv = !PARTS || (blockIdx.x & 1) == 1;
+  const int c0 = do_q ? 0 : p.Hcq;                 // this CTA's columns [c0, c1) of Ntot
+  const int c1 = do_kv ? p.Ntot : p.Hcq;
   grid_launch_dependents();
   grid_dependency_wait();
 
   // h = sum of the K-split partials, in split order.
   const size_t split_stride = static_cast<size_t>(p.T) * p.Ntot;
   const float* src = p.part + static_cast<size_t>(t) * p.Ntot;
-  if ((p.Ntot % 4) == 0) {                       // rows start 16-byte aligned
-    const int ncols = p.Ntot / 4;
-    for (int c = threadIdx.x; c < ncols; c += NT) {
+  if ((p.Ntot % 4) == 0) {                       // rows start 16-byte aligned (Hcq % 8 == 0)
+    const int ncols = c1 / 4;
+    for (int c = c0 / 4 + threadIdx.x; c < ncols; c += NT) {
       float4 v[MAXS];
 #pragma unroll
       for (int s = 0; s < MAXS; ++s)
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
       reinterpret_cast<float4*>(h)[c] = a;
     }
   } else {
-    for (int c = threadIdx.x; c < p.Ntot; c += NT) {
+    for (int c = c0 + threadIdx.x; c < c1; c += NT) {
       float v[MAXS];
 #pragma unroll
       for (int s = 0; s < MAXS; ++s)
@@ -126,7 +133,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   __syncthreads();
   if (p.dsx != nullptr) {   // full quant: dequant the exact integer products per token and column
     const float sx = p.dsx[t];
-    for (int c = threadIdx.x; c < p.Ntot; c += NT)
+    for (int c = c0 + threadIdx.x; c < c1; c += NT)
       h[c] *= sx * (c < p.Hcq ? p.dsw_q[c] : p.dsw_kv[c - p.Hcq]);
     __syncthreads();
   }
@@ -134,15 +141,19 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   // sums of squares of the c^Q and c^KV parts, one reduction
   const float* hkv = h + p.Hcq;
   float2 ss = make_float2(0.f, 0.f);
-  for (int f = threadIdx.x; f < p.Hcq; f += NT) ss.x += h[f] * h[f];
-  for (int f = threadIdx.x; f < p.Hckv; f += NT) ss.y += hkv[f] * hkv[f];
+  if (do_q)
+    for (int f = threadIdx.x; f < p.Hcq; f += NT) ss.x += h[f] * h[f];
+  if (do_kv)
+    for (int f = threadIdx.x; f < p.Hckv; f += NT) ss.y += hkv[f] * hkv[f];
   ss = block_sum2<NT>(ss, red);
   const float rq = 1.0f / sqrtf(ss.x / static_cast<float>(p.Hcq) + p.eps_cq);
   const float rkv = 1.0f / sqrtf(ss.y / static_cast<float>(p.Hckv) + p.eps_ckv);
 
   // ---- c^Q (Hcq % 8 == 0): bf16, or int8 codes held exactly in bf16
   __nv_bfloat16* cq = p.cq_out + static_cast<size_t>(t) * p.Hcq;
-  if (p.smooth == nullptr) {
+  if (!do_q) {
+    // (the c^KV / k^R CTA of a token)
+  } else if (p.smooth == nullptr) {
     for (int f = threadIdx.x * 8; f < p.Hcq; f += NT * 8) {
       float g[8], v[8];
       load8_bf16(p.gamma_cq + f, g);
@@ -168,7 +179,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     if (threadIdx.x == 0) p.scale_t[t] = scale;
   }
 
-  if (p.slots <= 0) return;                 // empty caches: outputs only
+  if (!do_kv || p.slots <= 0) return;       // empty caches: outputs only
   const int64_t idx = p.cache_index[t];
   if (idx < 0 || idx >= p.slots) {
     if (idx != -1 && threadIdx.x == 0) atomicOr(p.err, kErrIndexRange);
@@ -438,7 +449,11 @@ cudaError_t launch_query_quant(const __nv_bfloat16* qn, int8_t* q, float* scale,
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {
   const size_t smem = static_cast<size_t>(p.Ntot) * sizeof(float);
   const bool split = p.splits > 1;
-  auto kern = split ? norm_rope_scatter_kernel<kMaxSplits, 512> : norm_rope_scatter_kernel<1, 256>;
+  // up to 8 K-splits (decode): two CTAs per token, c^Q and c^KV/k^R
+  const bool parts = split && p.splits <= 8;
+  auto kern = !split ? norm_rope_scatter_kernel<1, 256>
+              : parts ? norm_rope_scatter_kernel<8, 256, true>
+                      : norm_rope_scatter_kernel<kMaxSplits, 512>;
   if (p.splits > kMaxSplits) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     cudaError_t e =
@@ -446,8 +461,8 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool p
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.T));
-  cfg.blockDim = dim3(split ? 512 : 256);
+  cfg.gridDim = dim3(static_cast<unsigned>(parts ? 2 * p.T : p.T));
+  cfg.blockDim = dim3(split && !parts ? 512 : 256);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
