@@ -132,9 +132,10 @@ def test_out_of_range_index_is_skipped_and_reported():
     assert pkg.mlap_check_errors(prolog.ws) == 0
 
 
-def test_outputs_have_no_stray_writes():
+@pytest.mark.parametrize("N", [3, 16], ids=["separate_kernels", "fused_kernel"])
+def test_outputs_have_no_stray_writes(N):
     # outputs live inside larger poisoned buffers: bytes around them must not change
-    case = synthetic.small_mla_case("canary", B=5, S=1, N=3, block_num=1)
+    case = synthetic.small_mla_case("canary", B=5, S=1, N=N, block_num=1)
     cpu = synthetic.make_mla_inputs(case)
     d = case.dims
     dev = torch.device("cuda")
@@ -150,6 +151,9 @@ def test_outputs_have_no_stray_writes():
     torch.cuda.synchronize()
     for buf, n in ((qbuf, d.T * d.N * d.Hckv), (rbuf, d.T * d.N * d.Dr)):
         assert bool((buf[:guard] == 7.0).all()) and bool((buf[guard + n:] == 7.0).all())
+    ref = oracle.mla_prolog(**oracle_inputs(cpu, case.eps))
+    assert_close(f64(t["query"]), ref["query"], "query")
+    assert_close(f64(t["query_rope"]), ref["query_rope"], "query_rope")
 
 
 def test_partial_quant_int8_caches():
