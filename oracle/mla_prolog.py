@@ -19,17 +19,17 @@ Readings where the pages are silent (each is also listed in the design notes):
   ("约束说明" dtype/shape matrix: (He, Hckv+Dr), (Hcq, N*(D+Dr))).
 * Partial quant ("部分量化"): c^Q (bf16) is multiplied by smooth_scales_cq, quantised per token
   symmetrically with scale = amax/127, round half to even, clamp to [-127, 127]; the int8 matmul
-  accumulates exactly and is dequantised by scale_t * dequant_scale_w_uq_qr[column].  The quantised
-  code is decided in float32, the precision of the kernel (the pages fix none).
+  accumulates exactly and is dequantised by scale_t * dequant_scale_w_uq_qr[column].  Scale,
+  quotient and code are float64 like everything else here: the pages state only the division.
 * Cache quant: value / quant_scale (the aclnnQkvRmsNormRopeCache "Formulas" (4) rule
-  kQuant = kRoPE / kScale), round half to even, clamp to [-128, 127], decided in float32.
+  kQuant = kRoPE / kScale), round half to even, clamp to [-128, 127], in float64.
 * Full quant ("全量化", the scenario matrix of "约束说明"): token_x int8 with the per-token
   dequant_scale_x (T, 1), weight_dq and weight_dkv_kr int8 with per-channel dequant_scale_w_dq
   (1, Hcq) and dequant_scale_w_dkv_kr (1, Hckv+Dr).  Reading: the int8 matmuls accumulate
   exactly and are dequantised as acc * dequant_scale_x[t] * dequant_scale_w[column]; from there
   the path is the partial-quant one.  With the quantised kv_cache column, query is int8
   "pertoken_head": per token and head, scale = amax over Hckv of q^N / 127, code = q^N / scale
-  rounded half to even and clamped to [-127, 127] (the c^Q rule), decided in float32;
+  rounded half to even and clamped to [-127, 127] (the c^Q rule), in float64;
   dequant_scale_q_nope (T, N, 1) returns the scale (0 and all-zero codes when amax = 0).  The
   pages call that cache quant "pertensor" but give quant_scale_ckv the shape (1, Hckv); the
   shape is followed (one scale per channel, the cache-quant rule above); kr_cache stays bf16
@@ -83,36 +83,34 @@ def rms_norm_quant(x: np.ndarray, gamma: np.ndarray, bias: np.ndarray, deq_scale
 def dynamic_quant_per_token(c_q: np.ndarray, smooth: np.ndarray):
     """Per-token symmetric int8 quant of c^Q after smoothing (MlaPrologV2 README, parameter
     smooth_scales_cq: "RmsNormCq输出动态量化参数"; formula is the reading stated in the module
-    docstring).  Returns (codes int8 (T,Hcq), scale float32 (T,)).  Decided in float32."""
-    s = np.asarray(c_q, np.float32) * np.asarray(smooth, np.float32).reshape(1, -1)
+    docstring).  Returns (codes int8 (T,Hcq), scale float64 (T,)), all in float64."""
+    s = np.asarray(c_q, np.float64) * np.asarray(smooth, np.float64).reshape(1, -1)
     amax = np.max(np.abs(s), axis=-1)
-    scale = (amax / np.float32(127.0)).astype(np.float32)
-    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
-    q = (s / safe[:, None]).astype(np.float32)
-    codes = saturate_int8_rne(q, -127, 127)
+    scale = amax / 127.0
+    safe = np.where(scale > 0, scale, 1.0)
+    codes = saturate_int8_rne(s / safe[:, None], -127, 127)
     codes[scale == 0] = 0
     return codes, scale
 
 
 def cache_quant(v: np.ndarray, scale: np.ndarray) -> np.ndarray:
-    """int8 code of v / scale per channel, round half to even, clamp to [-128,127], in float32
+    """int8 code of v / scale per channel, round half to even, clamp to [-128,127], in float64
     (MlaPrologV2 README quant_scale_ckv / quant_scale_ckr; the division rule of
     aclnnQkvRmsNormRopeCache "Formulas" (4))."""
-    q = (np.asarray(v, np.float64).astype(np.float32)
-         / np.asarray(scale, np.float32).reshape(1, -1)).astype(np.float32)
+    q = np.asarray(v, np.float64) / np.asarray(scale, np.float64).reshape(1, -1)
     return saturate_int8_rne(q)
 
 
 def quant_per_token_head(q_n: np.ndarray):
     """int8 query "pertoken_head" (MlaPrologV2 README, scenario matrix: query INT8 in full quant
     with quantised kv_cache; dequant_scale_q_nope (T, N, 1)): per token and head symmetric, scale
-    = amax / 127, round half to even, clamp to [-127, 127], in float32.  Returns (codes (T, N, H)
-    int8, scale (T, N) float32)."""
-    s = np.asarray(q_n, np.float64).astype(np.float32)
+    = amax / 127, round half to even, clamp to [-127, 127], in float64.  Returns (codes (T, N, H)
+    int8, scale (T, N) float64)."""
+    s = np.asarray(q_n, np.float64)
     amax = np.max(np.abs(s), axis=-1)
-    scale = (amax / np.float32(127.0)).astype(np.float32)
-    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
-    codes = saturate_int8_rne((s / safe[..., None]).astype(np.float32), -127, 127)
+    scale = amax / 127.0
+    safe = np.where(scale > 0, scale, 1.0)
+    codes = saturate_int8_rne(s / safe[..., None], -127, 127)
     codes[scale == 0] = 0
     return codes, scale
 

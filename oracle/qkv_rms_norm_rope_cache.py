@@ -16,9 +16,10 @@ Readings (the parameter table is lost from the page): gamma_q and gamma_k have s
 are shared by all heads of their kind; sin and cos have shape (B*S, D) and are shared by all
 heads; k_scale (Nk, D) and v_scale (Nv, D) are per channel; the cache layout is
 (BlockNum, BlockSize, N, D) with slot i at block i // BlockSize, row i % BlockSize; qOut is
-rounded to the dtype of qkv (fp16 or bf16); int8 codes round half to even, clamp to [-128, 127], decided in float32.
+rounded to the dtype of qkv (fp16 or bf16); int8 codes round half to even, clamp to [-128, 127],
+with the quotient in float64 (the page states only the division).
 Asymmetric quant: k_offset (Nk, D) and v_offset (Nv, D) are per-channel float32 offsets added to
-the float32 quotient before rounding.  The before-quant outputs are dense (T, N, D) tensors in
+the float64 quotient before rounding.  The before-quant outputs are dense (T, N, D) tensors in
 the dtype of qkv, one row per token whatever its index (they are not cache writes); qBeforeQuant
 equals qOut because the formulas never quantise q.
 """
@@ -31,10 +32,10 @@ from .rounding import round_bf16, round_fp16, saturate_int8_rne
 
 
 def _quant(v: np.ndarray, scale: np.ndarray, offset=None) -> np.ndarray:
-    q = (np.asarray(v, np.float64).astype(np.float32)
-         / np.asarray(scale, np.float32)).astype(np.float32)
-    if offset is not None:                               # asymmetric: + offset, in float32
-        q = (q + np.asarray(offset, np.float32)).astype(np.float32)
+    """Quant of "Formulas" (4): v / scale (+ offset), round half to even, clamp, in float64."""
+    q = np.asarray(v, np.float64) / np.asarray(scale, np.float64)
+    if offset is not None:                               # asymmetric: + offset
+        q = q + np.asarray(offset, np.float64)
     return saturate_int8_rne(q)
 
 

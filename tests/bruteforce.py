@@ -38,11 +38,6 @@ def fp16(x: float) -> float:
     return rne_keep_bits(x, 10)
 
 
-def f32(x: float) -> float:
-    """float64 -> nearest float32 (struct packs with round-to-nearest-even)."""
-    return struct.unpack("<f", struct.pack("<f", x))[0]
-
-
 def int8_code(q: float, lo: int, hi: int) -> int:
     r = round(q)                    # Python rounds half to even
     return max(lo, min(hi, r))
@@ -85,10 +80,10 @@ def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_c
         rms = math.sqrt(sum(v * v for v in hq) / Hcq + eps_cq)
         cq = [bf16(gcq[c] * hq[c] / rms) for c in range(Hcq)]
         if int8_w:
-            s = [f32(cq[c] * smooth[c]) for c in range(Hcq)]
+            s = [cq[c] * smooth[c] for c in range(Hcq)]
             amax = max(abs(v) for v in s)
-            scale = f32(amax / 127.0)
-            codes = [0 if scale == 0 else int8_code(f32(v / scale), -127, 127) for v in s]
+            scale = amax / 127.0
+            codes = [0 if scale == 0 else int8_code(v / scale, -127, 127) for v in s]
         for n in range(N):
             base = n * (D + Dr)
             u = []
@@ -103,11 +98,10 @@ def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_c
             r = u[D:]
             qn = [sum(qc[d] * wuk[n][d][c2] for d in range(D)) for c2 in range(Hckv)]
             if query_int8:
-                s = [f32(v) for v in qn]
-                amax = max(abs(v) for v in s)
-                sc = f32(amax / 127.0)
+                amax = max(abs(v) for v in qn)
+                sc = amax / 127.0
                 scale_q[t][n] = sc
-                query[t][n] = [0 if sc == 0 else int8_code(f32(v / sc), -127, 127) for v in s]
+                query[t][n] = [0 if sc == 0 else int8_code(v / sc, -127, 127) for v in qn]
             else:
                 query[t][n] = [bf16(v) for v in qn]
             for j in range(Dr):
@@ -121,12 +115,12 @@ def mla_prolog_bruteforce(x, wdq, wuq, wuk, wdkv, gcq, gckv, sin, cos, idx, kv_c
         i = idx[t]
         if 0 <= i < len(kv_cache) * bs:
             if qs_ckv is not None:
-                kv[i // bs][i % bs][0] = [int8_code(f32(f32(ckv[c]) / qs_ckv[c]), -128, 127)
+                kv[i // bs][i % bs][0] = [int8_code(ckv[c] / qs_ckv[c], -128, 127)
                                           for c in range(Hckv)]
             else:
                 kv[i // bs][i % bs][0] = [bf16(v) for v in ckv]
             if qs_ckr is not None:
-                kr[i // bs][i % bs][0] = [int8_code(f32(f32(kr_row[j]) / qs_ckr[j]), -128, 127)
+                kr[i // bs][i % bs][0] = [int8_code(kr_row[j] / qs_ckr[j], -128, 127)
                                           for j in range(Dr)]
             else:
                 kr[i // bs][i % bs][0] = [bf16(v) for v in kr_row]
@@ -161,7 +155,7 @@ def qkv_bruteforce(qkv, gq, gk, cos, sin, idx, k_cache, v_cache, eps, Nq, Nk, Nv
                 k_before[t][hk] = [fp16(v) for v in e]
                 if ks is not None:
                     off = [0.0] * D if ko is None else ko[hk]
-                    k_rows.append([int8_code(f32(f32(f32(e[j]) / ks[hk][j]) + off[j]), -128, 127)
+                    k_rows.append([int8_code(e[j] / ks[hk][j] + off[j], -128, 127)
                                    for j in range(D)])
                 else:
                     k_rows.append([fp16(v) for v in e])
@@ -170,7 +164,7 @@ def qkv_bruteforce(qkv, gq, gk, cos, sin, idx, k_cache, v_cache, eps, Nq, Nk, Nv
             v_before[t][hv] = [fp16(v) for v in vh]
             if vs is not None:
                 off = [0.0] * D if vo is None else vo[hv]
-                v_rows.append([int8_code(f32(f32(f32(vh[j]) / vs[hv][j]) + off[j]), -128, 127)
+                v_rows.append([int8_code(vh[j] / vs[hv][j] + off[j], -128, 127)
                                for j in range(D)])
             else:
                 v_rows.append([fp16(v) for v in vh])

@@ -44,8 +44,8 @@ MLA_MUTATIONS = [
      "out[i % block_num, i // block_num, 0, :] = rows[t]"),
     ("dequant scale dropped", "* np.asarray(dequant_scale_w_uq_qr, np.float64).reshape(1, -1))",
      ")"),
-    ("cache quant multiplies", "/ np.asarray(scale, np.float32).reshape(1, -1)).astype(np.float32)",
-     "* np.asarray(scale, np.float32).reshape(1, -1)).astype(np.float32)"),
+    ("cache quant multiplies", "q = np.asarray(v, np.float64) / np.asarray(scale, np.float64)",
+     "q = np.asarray(v, np.float64) * np.asarray(scale, np.float64)"),
     ("missing bf16 round of q^C", "q_c = round_bf16(u[:, :, :D])", "q_c = u[:, :, :D] * (1 + 2**-9)"),
 ]
 
@@ -69,10 +69,10 @@ FULL_QUANT_MUTATIONS = [
     ("x dequant dropped", "* np.asarray(dequant_scale_x, np.float64).reshape(-1, 1)", ""),
     ("W^DKV dequant from W^DQ", "h_kvr = down(weight_dkv_kr, dequant_scale_w_dkv_kr)",
      "h_kvr = down(weight_dkv_kr, np.full_like(dequant_scale_w_dkv_kr, np.mean(dequant_scale_w_dq)))"),
-    ("query codes truncated", "codes = saturate_int8_rne((s / safe[..., None]).astype(np.float32), -127, 127)",
+    ("query codes truncated", "codes = saturate_int8_rne(s / safe[..., None], -127, 127)",
      "codes = np.clip(np.trunc(s / safe[..., None]), -127, 127).astype(np.int8)"),
-    ("query scale per token", "amax = np.max(np.abs(s), axis=-1)\n    scale = (amax / np.float32(127.0)).astype(np.float32)\n    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)\n    codes = saturate_int8_rne(",
-     "amax = np.max(np.abs(s), axis=(-2, -1), keepdims=True) + 0 * s[..., 0:1]\n    amax = amax[..., 0]\n    scale = (amax / np.float32(127.0)).astype(np.float32)\n    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)\n    codes = saturate_int8_rne("),
+    ("query scale per token", "amax = np.max(np.abs(s), axis=-1)\n    scale = amax / 127.0\n    safe = np.where(scale > 0, scale, 1.0)\n    codes = saturate_int8_rne(s / safe[..., None]",
+     "amax = np.max(np.abs(s), axis=(-2, -1), keepdims=True) + 0 * s[..., 0:1]\n    amax = amax[..., 0]\n    scale = amax / 127.0\n    safe = np.where(scale > 0, scale, 1.0)\n    codes = saturate_int8_rne(s / safe[..., None]"),
 ]
 
 
@@ -85,7 +85,7 @@ def test_full_quant_pins_catch_mutation(label, old, new):
     got = mod.mla_prolog(**inp)
     same = np.array_equal(np.asarray(got["query"]), np.array(want["query"], np.int8))
     same &= np.array_equal(np.asarray(got["dequant_scale_q_nope"]),
-                           np.array(want["dequant_scale_q_nope"], np.float32))
+                           np.array(want["dequant_scale_q_nope"], np.float64))
     for key in ("query_rope", "kr_cache"):
         same &= np.allclose(np.asarray(got[key], np.float64), np.array(want[key], np.float64),
                             rtol=1e-12, atol=1e-14)
@@ -123,13 +123,13 @@ QKV_MUTATIONS = [
      "k, v = x[:, :Nq, :], x[:, Nq + Nk:, :], x[:, Nq:Nq + Nk, :]"),
     ("v normalised too", "v_rows = _quant(v, np.asarray(v_scale).reshape(1, Nv, D), vo)",
      "v_rows = _quant(rms_norm(v, 1.0, epsilon), np.asarray(v_scale).reshape(1, Nv, D), vo)"),
-    ("offset subtracted", "q = (q + np.asarray(offset, np.float32))",
-     "q = (q - np.asarray(offset, np.float32))"),
+    ("offset subtracted", "q = q + np.asarray(offset, np.float64)",
+     "q = q - np.asarray(offset, np.float64)"),
     ("v offset ignored", "vo = None if v_offset is None else np.asarray(v_offset).reshape(1, Nv, D)",
      "vo = None"),
     ("offset added after rounding", "return saturate_int8_rne(q)",
-     "return saturate_int8_rne(q - (0 if offset is None else np.asarray(offset, np.float32))) + "
-     "(0 if offset is None else np.rint(np.asarray(offset, np.float32)))"),
+     "return saturate_int8_rne(q - (0 if offset is None else np.asarray(offset, np.float64))) + "
+     "(0 if offset is None else np.rint(np.asarray(offset, np.float64)))"),
     ("v_before normalised", '"v_before": rnd(v)', '"v_before": rnd(rms_norm(v, 1.0, epsilon))'),
     ("k_before before RoPE", '"k_before": rnd(k_emb)', '"k_before": rnd(rms_norm(k, gamma_k, epsilon))'),
     ("k gamma from q", "k_emb = rope_half_and_half(rms_norm(k, gamma_k, epsilon), cos, sin)",

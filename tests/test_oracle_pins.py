@@ -277,7 +277,7 @@ def test_mla_prolog_matches_brute_force(int8, int8_cache, full, xnorm):
             np.testing.assert_allclose(got[key], np.array(want[key]), rtol=1e-12, atol=1e-14)
     if inp.get("query_int8"):
         np.testing.assert_array_equal(got["dequant_scale_q_nope"],
-                                      np.array(want["dequant_scale_q_nope"], np.float32))
+                                      np.array(want["dequant_scale_q_nope"], np.float64))
     for key in ("kv_cache", "kr_cache"):
         if got[key].dtype == np.int8:
             np.testing.assert_array_equal(got[key], np.array(want[key], np.int8))
