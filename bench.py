@@ -1,18 +1,23 @@
 """Throughput of the MLA prolog on GB300 (and of the CPU oracle as the reference arm).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|prefill|tiny|partial_quant|qkv]
+                    [--workload decode|prefill|tiny|partial_quant|full_quant|xnorm|qkv|qkv_asym]
 
 One step = one full prolog call (down-projection, RmsNorm/RoPE/scatter, up-projection with query
 RoPE, per-head absorb) over one batch of seeded synthetic inputs.  The default workload is the
-bf16 decode configuration (T=128 tokens, He=7168, Hcq=1536, Hckv=512, N=128, D=128, Dr=64).
+bf16 decode configuration (T=128 tokens, He=7168, Hcq=1536, Hckv=512, N=128, D=128, Dr=64); the
+same run also measures the bf16 prefill configuration (T=8192) and reports it in a `prefill`
+object of the same line.
 
 `value` is device-timed whole-job throughput (tokens/s over all ranks) with inputs resident in
 HBM: K steps replayed from a CUDA graph of the C-ABI execute call, rotating over enough input sets
 (weights, activations, caches) that each step's working set has left L2 by the time it recurs.
-`e2e` is the same metric through the C-ABI call from pinned host buffers, host<->device copies of
-the step's inputs and outputs inside the timed region.  Multi-GPU runs are independent replicas
-(the prolog shards by tokens with no exchange step): one process per GPU, max time over ranks.
+Per-kernel times come from %globaltimer stamps the kernels write inside the same pipelined calls
+(mlap_execute_stamped), not from events between launches.  `e2e` is the same metric through the
+C-ABI call from pinned host buffers, host<->device copies of the step's inputs and outputs inside
+the timed region.  Multi-GPU runs are independent replicas (the prolog shards by tokens with no
+exchange step): one process per GPU (torchrun, or spawned here when --gpus N > 1 is given without
+a launcher), max time over ranks.
 """
 from __future__ import annotations
 
@@ -47,8 +52,14 @@ def _parse():
                              "qkv", "qkv_asym"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--timer-calls", type=int, default=200,
-                    help="calls timed kernel by kernel for the roofline entry")
+    ap.add_argument("--stamp-calls", type=int, default=64,
+                    help="pipelined calls whose kernels record execution stamps (per-kernel times)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill measurement that the default decode run adds")
+    ap.add_argument("--prefill-steps", type=int, default=60)
+    ap.add_argument("--oracle-full-call", action="store_true",
+                    help="also time one oracle call over the whole workload (host cores)")
+    ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -186,11 +197,17 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------- distributed
 def _dist_setup(n_gpus):
+    """Rank, local rank and world size.  Under a launcher (WORLD_SIZE set) the world must match
+    --gpus; the ranks meet over gloo (host-side barrier and max-over-ranks only: the replicas
+    exchange no data)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if "WORLD_SIZE" in os.environ and n_gpus not in (None, world):
+        raise SystemExit(f"bench.py: --gpus {n_gpus} but WORLD_SIZE={world}")
     if world > 1:
         import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group("gloo")
     return rank, local, world
 
@@ -211,44 +228,74 @@ def _max_over_ranks(v, world):
     return float(t.item())
 
 
+def _spawned_rank(rank, world, port, argv):
+    """One replica started by `--gpus N` without a launcher (torch.multiprocessing, spawn)."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      LOCAL_RANK=str(rank), WORLD_SIZE=str(world))
+    sys.argv = [sys.argv[0]] + list(argv)
+    main()
+
+
+def _spawn_replicas(n, argv):
+    import socket
+    import torch.multiprocessing as mp
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    mp.start_processes(_spawned_rank, args=(n, port, argv), nprocs=n, join=True,
+                       start_method="spawn")
+
+
 # ------------------------------------------------------------------------------- oracle baseline
-def oracle_tokens_per_s(case, budget_s=12.0, sample_tokens=4):
-    """Time the oracle as it stands on a bounded token sample of the workload (host cores)."""
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _oracle_call(case, sample_tokens, offset=0):
+    """A closure running the oracle as it stands on `sample_tokens` tokens of the workload
+    (tokens are independent), and a description of the sample."""
     import numpy as np
     import oracle
     import synthetic
     from oracle.mla_prolog import mla_prolog_tokens
 
     if isinstance(case, synthetic.QkvCase):
+        import torch
         cpu = synthetic.make_qkv_inputs(case)
         d = case.dims
-        f = lambda t: t.to(__import__("torch").float64).numpy()
-        ntok = min(d.T, 64)
-        qkv = f(cpu["qkv"]).reshape(d.T, -1)[:ntok]
-        args = (qkv, f(cpu["gamma_q"]), f(cpu["gamma_k"]), f(cpu["cos"])[:ntok],
-                f(cpu["sin"])[:ntok], cpu["index"].numpy()[:ntok], cpu["k_cache"].numpy(),
-                cpu["v_cache"].numpy(), case.eps, d.Nq, d.Nk, d.Nv, cpu["k_scale"].numpy(),
-                cpu["v_scale"].numpy())
+        f = lambda t: t.to(torch.float64).numpy()
+        ntok = min(d.T, sample_tokens)
+        ids = (offset + np.arange(ntok)) % d.T
+        qkv = f(cpu["qkv"]).reshape(d.T, -1)[ids]
+        args = (qkv, f(cpu["gamma_q"]), f(cpu["gamma_k"]), f(cpu["cos"]).reshape(d.T, -1)[ids],
+                f(cpu["sin"]).reshape(d.T, -1)[ids], cpu["index"].numpy().reshape(-1)[ids],
+                cpu["k_cache"].numpy(), cpu["v_cache"].numpy(), case.eps, d.Nq, d.Nk, d.Nv,
+                cpu["k_scale"].numpy(), cpu["v_scale"].numpy())
         kw = {}
         if case.quant == "asymmetric":
             kw = {"k_offset": cpu["k_offset"].numpy(), "v_offset": cpu["v_offset"].numpy()}
-        call = lambda: oracle.qkv_rms_norm_rope_cache(*args, **kw)
-        sample = f"{ntok} tokens of the {case.name} workload per oracle call"
-    else:
-        import torch
-        cpu = synthetic.make_mla_inputs(case)
-        inp = {k: (v.numpy() if v.dtype in (torch.int8, torch.int64) else
-                   v.to(torch.float64).numpy()) for k, v in cpu.items()
-               if isinstance(v, torch.Tensor)}
-        inp["rmsnorm_epsilon_cq"] = case.eps
-        inp["rmsnorm_epsilon_ckv"] = case.eps
-        inp["query_int8"] = case.full_quant and case.cache_dtype == "int8"
-        if case.x_norm is not None:
-            inp["rms_norm_quant_epsilon"] = case.eps
-        ntok = min(case.dims.T, sample_tokens)
-        ids = np.arange(ntok)
-        call = lambda: mla_prolog_tokens(inp, ids)
-        sample = f"{ntok} tokens of the {case.name} workload per oracle call"
+        return (lambda: oracle.qkv_rms_norm_rope_cache(*args, **kw)), ntok
+    import torch
+    cpu = synthetic.make_mla_inputs(case)
+    inp = {k: (v.numpy() if v.dtype in (torch.int8, torch.int64) else
+               v.to(torch.float64).numpy()) for k, v in cpu.items()
+           if isinstance(v, torch.Tensor)}
+    inp["rmsnorm_epsilon_cq"] = case.eps
+    inp["rmsnorm_epsilon_ckv"] = case.eps
+    inp["query_int8"] = case.full_quant and case.cache_dtype == "int8"
+    if case.x_norm is not None:
+        inp["rms_norm_quant_epsilon"] = case.eps
+    ntok = min(case.dims.T, sample_tokens)
+    ids = (offset + np.arange(ntok)) % case.dims.T
+    return (lambda: mla_prolog_tokens(inp, ids)), ntok
+
+
+def _oracle_rate(case, budget_s, sample_tokens, offset=0):
+    call, ntok = _oracle_call(case, sample_tokens, offset)
     t0 = time.perf_counter()
     calls = 0
     while True:
@@ -257,11 +304,68 @@ def oracle_tokens_per_s(case, budget_s=12.0, sample_tokens=4):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    try:
-        cores = len(os.sched_getaffinity(0))
-    except Exception:
-        cores = os.cpu_count()
-    return calls * ntok / el, cores, f"{sample}; {calls} calls in {el:.1f} s"
+    return calls * ntok / el, calls, el, ntok
+
+
+def _oracle_worker(spec):
+    """Entry of a child process (single-threaded BLAS): time the oracle on its own token sample
+    and print the rate as JSON."""
+    a = json.loads(spec)
+    rate, calls, el, ntok = _oracle_rate(_case(a["workload"]), a["budget"], a["tokens"], a["offset"])
+    print(json.dumps({"rate": rate, "calls": calls, "elapsed": el, "tokens": ntok}), flush=True)
+
+
+def _single_thread_env():
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+              "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env.pop("WORLD_SIZE", None)
+    env.pop("RANK", None)
+    env.pop("LOCAL_RANK", None)
+    return env
+
+
+def oracle_baselines(workload, budget_s=10.0, sample_tokens=4):
+    """The oracle as it stands, on the host cores, on bounded token samples of the workload:
+    one single-threaded process, then one single-threaded process per core in the affinity set,
+    each on its own sample (tokens are independent), run at once.  Returns the single-thread
+    rate, the all-core rate (sum over processes), the core count and a description."""
+    cores = _cores()
+    env = _single_thread_env()
+
+    def launch(offset):
+        spec = json.dumps({"workload": workload, "budget": budget_s, "tokens": sample_tokens,
+                           "offset": offset})
+        return subprocess.Popen([sys.executable, os.path.abspath(__file__), "--oracle-worker",
+                                 spec], stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                text=True, env=env, cwd=ROOT)
+
+    def collect(ps):
+        out = []
+        for pr in ps:
+            o, e = pr.communicate()
+            if pr.returncode != 0:
+                raise RuntimeError(f"oracle worker failed: {e[-2000:]}")
+            out.append(json.loads(o.strip().splitlines()[-1]))
+        return out
+
+    single = collect([launch(0)])[0]
+    allc = collect([launch(i * sample_tokens) for i in range(cores)])
+    rate_all = sum(r["rate"] for r in allc)
+    sample = (f"{single['tokens']} tokens of the {_case(workload).name} workload per oracle call, "
+              f"{budget_s:.0f} s per process; single thread: {single['calls']} calls in "
+              f"{single['elapsed']:.1f} s; all cores: {cores} single-threaded processes on "
+              f"disjoint token samples at once")
+    return single["rate"], rate_all, cores, sample
+
+
+def oracle_full_call(workload):
+    """Seconds for one oracle call over every token of the workload (default BLAS threads)."""
+    call, ntok = _oracle_call(_case(workload), 1 << 30)
+    t0 = time.perf_counter()
+    call()
+    return time.perf_counter() - t0, ntok
 
 
 # ------------------------------------------------------------------------------- our arm
@@ -291,37 +395,52 @@ def _mla_sets(case, dev, n_sets):
     return cpu, sets
 
 
-def run_ours(args, rank, local, world):
+def _stamped_kernel_times(run_one, n_calls, stream, dev):
+    """Per-kernel times inside pipelined calls: a CUDA graph of n_calls consecutive stamped calls
+    (the same launches as the timed graph), replayed twice; the second replay's stamps are read.
+    Returns {kernel: {"span_us", "dep_to_end_us"}} averaged over the calls (the first few, still
+    ramping up after the graph launch, are dropped)."""
     import torch
     import qkv_attention_prolog_gb300 as pkg
-    from qkv_attention_prolog_gb300 import build as _build
+    stamps = pkg.stamps_buffer(dev, n_calls)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_calls):
+            run_one(i, stamps[i], torch.cuda.current_stream())
+    for _ in range(2):
+        stamps.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+    skip = min(4, n_calls // 2)
+    acc = {}
+    for i in range(skip, n_calls):
+        for k, v in pkg.read_stamps(stamps[i]).items():
+            a = acc.setdefault(k, {"span": [], "dep": []})
+            a["span"].append(v["span_ns"] / 1e3)
+            if v["dep_to_end_ns"] is not None:
+                a["dep"].append(v["dep_to_end_ns"] / 1e3)
+    out = {k: {"span_us": round(statistics.mean(v["span"]), 3),
+               "dep_to_end_us": round(statistics.mean(v["dep"]), 3) if v["dep"] else None}
+           for k, v in acc.items()}
+    last = pkg.read_stamps(stamps[n_calls - 1])
+    timeline = {k: {"start_us": round(v["start_ns"] / 1e3, 3), "end_us": round(v["end_ns"] / 1e3, 3)}
+                for k, v in last.items()}
+    del g
+    return out, timeline
 
-    _build.build()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    case = _case(args.workload)
-    is_qkv = args.workload.startswith("qkv")
-    hbm, tf_burst, tf_sus, peak_kind = _peaks()
 
-    if is_qkv:
-        return run_qkv(args, case, dev, rank, world, hbm, peak_kind)
-
+def measure_mla(args, case, dev, stream, steps, warm, world, stamp_calls, sample_clocks=True):
+    """Device-timed calls of one MLA workload and its per-kernel stamps."""
+    import torch
+    import qkv_attention_prolog_gb300 as pkg
     d = case.dims
     w_int8 = case.weight_uq_qr_dtype == "int8"
     c_int8 = case.cache_dtype == "int8"
     kern, path_bytes, path_flops = mla_model(d, w_int8, c_int8, case.full_quant,
                                              case.x_norm is not None)
-    # down, norm/scatter, up, absorb; full quant adds the token_x widening and, with an int8
-    # query, its per-token-head quantisation; the input RmsNormQuant adds its own kernel
-    launches_per_call = (4 + (1 + c_int8 if case.full_quant else 0)
-                         + (1 if case.x_norm is not None else 0))
     n_sets = max(1, math.ceil(3 * L2_BYTES / path_bytes) + 1) if path_bytes < 2 * L2_BYTES else 1
     cpu, sets = _mla_sets(case, dev, n_sets)
-    stream = torch.cuda.Stream(dev)
-
-    steps = args.steps or {"decode": 40000, "tiny": 40000, "partial_quant": 40000,
-                           "full_quant": 40000, "xnorm": 40000, "prefill": 1500}[args.workload]
-    warm = max(3, args.warmup)
     with torch.cuda.stream(stream):
         for i in range(warm):
             t, a, ws = sets[i % n_sets]
@@ -329,7 +448,8 @@ def run_ours(args, rank, local, world):
     stream.synchronize()
 
     # CUDA graph of `per_graph` consecutive steps over the rotating sets
-    per_graph = n_sets * max(1, 64 // n_sets) if steps >= 64 else n_sets
+    per_graph = n_sets * max(1, 64 // n_sets) if steps >= 64 else min(n_sets, steps)
+    per_graph = max(1, per_graph)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(per_graph):
@@ -345,74 +465,113 @@ def run_ours(args, rank, local, world):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(replays):
-                g.replay()
-            ev1.record(stream)
-        stream.synchronize()
+    clk = ClockSampler(dev.index) if sample_clocks else None
+    if clk is not None:
+        clk.__enter__()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    if clk is not None:
+        clk.__exit__(None, None, None)
     torch.cuda.synchronize()
     _barrier(world)
-    ms_total = ev0.elapsed_time(ev1)
-    ms_total = _max_over_ranks(ms_total, world)
+    ms_total = _max_over_ranks(ev0.elapsed_time(ev1), world)
     ms_step = ms_total / steps
-    value = d.T * world * steps / (ms_total / 1e3)
-    for s in sets:
-        assert pkg.mlap_check_errors(s[2], stream) == 0, "kernel error during the timed region"
+    del g
+    for s_ in sets:
+        assert pkg.mlap_check_errors(s_[2], stream) == 0, "kernel error during the timed region"
 
-    # per-kernel durations (CUDA events around each launch on the execute stream)
-    n_timed = max(2, args.timer_calls)
-    timer = pkg.Timer(n_timed)
-    with torch.cuda.stream(stream):
-        for i in range(n_timed):
-            t, a, ws = sets[i % n_sets]
-            timer.execute(a, ws, stream)
-    per = timer.read()
-    timer.close()
-    names = ["down", "norm_scatter", "up", "absorb"]
-    per = per[min(10, len(per) // 2):]
-    avg_ms = {n: statistics.mean(r[k] for r in per) for k, n in enumerate(names)}
-    if avg_ms["absorb"] == 0.0:
-        # the decode launch fuses the absorb into the up-projection (the timer's absorb phase is
-        # empty): one kernel, whose algorithmic bytes are both weights, c^Q and both outputs
-        avg_ms = {"down": avg_ms["down"], "norm_scatter": avg_ms["norm_scatter"],
-                  "up_absorb": avg_ms["up"]}
-        names = list(avg_ms)
-        launches_per_call -= 1
+    def run_one(i, st, strm):
+        t, a, ws = sets[i % n_sets]
+        pkg.mlap_execute_stamped(a, ws, st, strm)
+
+    per, timeline = _stamped_kernel_times(run_one, max(8, stamp_calls), stream, dev)
+    for s_ in sets:
+        assert pkg.mlap_check_errors(s_[2], stream) == 0, "kernel error during the stamped calls"
+    if "up" in per and "absorb" not in per:
+        # the decode launch runs the up-projection and the absorb in one kernel: its algorithmic
+        # bytes are both weights, c^Q and both outputs (q^C stays on chip)
+        per["up_absorb"] = per.pop("up")
+        timeline["up_absorb"] = timeline.pop("up")
         kern["up_absorb"] = {
             "bytes": kern["up"]["bytes"] + kern["absorb"]["bytes"] - 2 * d.T * d.N * d.D * 2,
             "flops": kern["up"]["flops"] + kern["absorb"]["flops"]}
-    dominant = max(names, key=lambda n: avg_ms[n])
-    tensor_bound = args.workload == "prefill"
+    # down, norm/scatter, up (+ absorb); full quant adds the token_x widening and, with an int8
+    # query, its per-token-head quantisation; the input RmsNormQuant adds its own kernel
+    launches = (len(per) + (1 + c_int8 if case.full_quant else 0)
+                + (1 if case.x_norm is not None else 0))
+    return {"case": case, "cpu": cpu, "sets": sets, "kern": kern, "path_bytes": path_bytes,
+            "path_flops": path_flops, "ms_step": ms_step, "steps": steps, "n_sets": n_sets,
+            "per_graph": per_graph, "replays": replays, "per_kernel": per,
+            "timeline": timeline, "clocks": clk.summary() if clk is not None else None,
+            "launches_per_call": launches}
+
+
+def _roofline(m, tensor_bound, hbm, tf_sus, peak_kind, workload):
+    """Roofline entry of the dominant kernel: algorithmic bytes (FLOPs) per launch over its mean
+    span inside the pipelined calls (earliest CTA start to latest CTA end)."""
+    per, kern = m["per_kernel"], m["kern"]
+    dominant = max(per, key=lambda n: per[n]["span_us"])
+    span_s = per[dominant]["span_us"] / 1e6
     if tensor_bound:
-        achieved = kern[dominant]["flops"] / (avg_ms[dominant] / 1e3) / 1e12
-        peak = tf_sus
-        roof = {"bound": "tensor", "unit": "TFLOP/s", "peak": peak}
+        achieved = kern[dominant]["flops"] / span_s / 1e12
+        roof = {"bound": "tensor", "unit": "TFLOP/s", "peak": tf_sus,
+                "peak_note": "sustained bf16 (kernel timed inside a long step)"}
     else:
-        achieved = kern[dominant]["bytes"] / (avg_ms[dominant] / 1e3) / 1e9
-        peak = hbm
-        roof = {"bound": "hbm", "unit": "GB/s", "peak": peak}
+        achieved = kern[dominant]["bytes"] / span_s / 1e9
+        roof = {"bound": "hbm", "unit": "GB/s", "peak": hbm}
     roof.update({"kernel": dominant, "achieved": round(achieved, 1),
-                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                 "traffic": _ncu_traffic(dominant, args.workload),
-                 "algorithmic_per_launch": kern[dominant]["bytes"] if not tensor_bound
-                 else kern[dominant]["flops"],
-                 "avg_launch_us": round(avg_ms[dominant] * 1e3, 3),
-                 "per_kernel_us": {n: round(avg_ms[n] * 1e3, 3) for n in names}})
-    path_time = max(path_bytes / (hbm * 1e9), path_flops / (tf_sus * 1e12))
-    path_roof = {"bytes": path_bytes, "flops": path_flops,
-                 "roofline_us": round(path_time * 1e6, 3),
-                 "frac": round(path_time / (ms_step / 1e3), 4),
-                 "bound": "tensor" if path_flops / (tf_sus * 1e12) > path_bytes / (hbm * 1e9)
-                 else "hbm"}
+                 "frac": round(achieved / roof["peak"], 4), "peak_kind": peak_kind,
+                 "traffic": _ncu_traffic(dominant, workload),
+                 "algorithmic_per_launch": kern[dominant]["flops" if tensor_bound else "bytes"],
+                 "avg_launch_us": per[dominant]["span_us"],
+                 "timing": "kernel span from %globaltimer stamps inside pipelined calls",
+                 "per_kernel_us": {n: v["span_us"] for n, v in per.items()},
+                 "per_kernel_dep_to_end_us": {n: v["dep_to_end_us"] for n, v in per.items()}})
+    return roof
 
-    e2e = run_e2e(args, case, cpu, sets[0], dev, stream)
 
-    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-            "steps": steps, "warmup": warm, "ms_per_step": round(ms_step, 6),
-            "us_per_call": round(ms_step * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+def _path_roofline(m, hbm, tf_sus):
+    path_time = max(m["path_bytes"] / (hbm * 1e9), m["path_flops"] / (tf_sus * 1e12))
+    return {"bytes": m["path_bytes"], "flops": m["path_flops"],
+            "roofline_us": round(path_time * 1e6, 3),
+            "frac": round(path_time / (m["ms_step"] / 1e3), 4),
+            "bound": ("tensor" if m["path_flops"] / (tf_sus * 1e12) > m["path_bytes"] / (hbm * 1e9)
+                      else "hbm")}
+
+
+def run_ours(args, rank, local, world):
+    import torch
+    from qkv_attention_prolog_gb300 import build as _build
+
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    case = _case(args.workload)
+    is_qkv = args.workload.startswith("qkv")
+    hbm, tf_burst, tf_sus, peak_kind = _peaks()
+
+    if is_qkv:
+        return run_qkv(args, case, dev, rank, world, hbm, peak_kind)
+
+    d = case.dims
+    stream = torch.cuda.Stream(dev)
+    steps = args.steps or {"decode": 40000, "tiny": 40000, "partial_quant": 40000,
+                           "full_quant": 40000, "xnorm": 40000, "prefill": 1500}[args.workload]
+    warm = max(3, args.warmup)
+    m = measure_mla(args, case, dev, stream, steps, warm, world, args.stamp_calls)
+    tensor_bound = args.workload == "prefill"
+    roof = _roofline(m, tensor_bound, hbm, tf_sus, peak_kind, args.workload)
+    path_roof = _path_roofline(m, hbm, tf_sus)
+    e2e = run_e2e(args, case, m["cpu"], m["sets"][0], dev, stream)
+    ms_step = m["ms_step"]
+    line = {"metric": METRIC, "value": round(d.T * world * m["steps"] / (ms_step * m["steps"] / 1e3), 1),
+            "unit": UNIT, "n_gpus": world, "steps": m["steps"], "warmup": warm,
+            "ms_per_step": round(ms_step, 6), "us_per_call": round(ms_step * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; shapes and distributions of the workload recipe)",
             "config": {"workload": case.name, "T": d.T, "B": d.B, "S": d.S, "He": d.He,
                        "Hcq": d.Hcq, "Hckv": d.Hckv, "N": d.N, "D": d.D, "Dr": d.Dr,
@@ -420,17 +579,51 @@ def run_ours(args, rank, local, world):
                        "token_x_and_down_weights": "int8" if case.full_quant else "bf16",
                        "input_rms_norm_quant": case.x_norm,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": (f"rotating {n_sets} input sets of {path_bytes/1e6:.1f} MB "
-                              f"({n_sets*path_bytes/1e6:.0f} MB > 129 MB L2)" if n_sets > 1
-                              else f"inputs {path_bytes/1e6:.0f} MB > 129 MB L2"),
-                       "timing": f"CUDA graph of {per_graph} execute calls replayed {replays}x"},
-            "roofline": roof, "path_roofline": path_roof, "clocks": clk.summary(),
-            "e2e": e2e, "gpu_launches": launches_per_call * steps}
+                       "l2": (f"rotating {m['n_sets']} input sets of {m['path_bytes']/1e6:.1f} MB "
+                              f"({m['n_sets']*m['path_bytes']/1e6:.0f} MB > 129 MB L2)"
+                              if m["n_sets"] > 1
+                              else f"inputs {m['path_bytes']/1e6:.0f} MB > 129 MB L2"),
+                       "timing": (f"CUDA graph of {m['per_graph']} execute calls replayed "
+                                  f"{m['replays']}x")},
+            "roofline": roof, "path_roofline": path_roof, "clocks": m["clocks"],
+            "timeline_us": m["timeline"],
+            "e2e": e2e, "gpu_launches": m["launches_per_call"] * m["steps"]}
+    del m
+    if args.workload == "decode" and not args.no_prefill:
+        torch.cuda.empty_cache()
+        line["prefill"] = run_prefill_leg(args, dev, stream, world, hbm, tf_burst, tf_sus,
+                                          peak_kind)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, sample = oracle_tokens_per_s(case)
-        line["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": cores,
-                                "kind": "oracle", "sample": sample}
+        single, allc, cores, sample = oracle_baselines(args.workload)
+        line["cpu_baseline"] = {"value": round(allc, 3), "unit": UNIT, "cores": cores,
+                                "kind": "oracle", "single_thread": round(single, 3),
+                                "all_cores": round(allc, 3), "sample": sample}
+    if args.oracle_full_call:
+        sec, ntok = oracle_full_call(args.workload)
+        line["oracle_full_call"] = {"seconds": round(sec, 2), "tokens": ntok,
+                                    "tokens_per_s": round(ntok / sec, 2), "cores": _cores()}
     return line
+
+
+def run_prefill_leg(args, dev, stream, world, hbm, tf_burst, tf_sus, peak_kind):
+    """The bf16 prefill workload (T=8192) in the same process: microseconds per call, the path
+    against the sustained tensor peak, and the per-kernel stamps."""
+    import synthetic
+    case = synthetic.MLA_PREFILL
+    m = measure_mla(args, case, dev, stream, max(4, args.prefill_steps), 3, world,
+                    min(16, args.stamp_calls))
+    roof = _roofline(m, True, hbm, tf_sus, peak_kind, "prefill")
+    path_roof = _path_roofline(m, hbm, tf_sus)
+    ms = m["ms_step"]
+    out = {"workload": case.name, "us_per_call": round(ms * 1e3, 3),
+           "tokens_per_s": round(case.dims.T * world / (ms / 1e3), 1), "steps": m["steps"],
+           "roofline": roof, "path_roofline": path_roof,
+           "path_frac_of_burst": round(m["path_flops"] / (ms / 1e3) / 1e12 / tf_burst, 4),
+           "timeline_us": m["timeline"], "clocks": m["clocks"],
+           "timing": (f"CUDA graph of {m['per_graph']} execute calls replayed {m['replays']}x; "
+                      f"inputs {m['path_bytes']/1e6:.0f} MB > 129 MB L2")}
+    del m
+    return out
 
 
 def _blob(tensors, names, device, pinned=False):
@@ -534,8 +727,9 @@ def run_qkv(args, case, dev, rank, world, hbm, peak_kind):
     if case.before_quant:        # the three dense before-quant outputs
         nb += d.T * (d.Nq + d.Nk + d.Nv) * d.D * 2
     steps = args.steps or 2000
+    warm = max(3, args.warmup)
     with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
+        for _ in range(warm):
             pkg.qkvrnrc_execute(a, ws, stream)
         g = torch.cuda.CUDAGraph()
         stream.synchronize()
@@ -557,10 +751,16 @@ def run_qkv(args, case, dev, rank, world, hbm, peak_kind):
             e1.record(stream)
         stream.synchronize()
     ms = _max_over_ranks(e0.elapsed_time(e1), world) / steps
-    achieved = nb / (ms / 1e3) / 1e9
+    del g
+    assert pkg.mlap_check_errors(ws, stream) == 0, "kernel error during the timed region"
+    per, timeline = _stamped_kernel_times(
+        lambda i, st, strm: pkg.qkvrnrc_execute_stamped(a, ws, st, strm), 16, stream, dev)
+    span_us = per["qkv_rnrc"]["span_us"]
+    achieved = nb / (span_us / 1e6) / 1e9
     e2e = run_qkv_e2e(args, case, cpu, t, d, dev, stream)
     return {"metric": METRIC, "value": round(d.T * world / (ms / 1e3), 1), "unit": UNIT,
-            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+            "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": round(ms, 6),
+            "us_per_call": round(ms * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
             "data": "synthetic", "config": {"workload": case.name, "B": d.B, "S": d.S,
                                             "Nq": d.Nq, "Nk": d.Nk, "Nv": d.Nv, "D": d.D,
@@ -569,7 +769,12 @@ def run_qkv(args, case, dev, rank, world, hbm, peak_kind):
                                             "l2": f"inputs {nb/1e6:.0f} MB > 129 MB L2"},
             "roofline": {"bound": "hbm", "kernel": "qkv_rnrc", "achieved": round(achieved, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                         "peak_kind": peak_kind, "traffic": _ncu_traffic("qkv_rnrc", args.workload)},
+                         "peak_kind": peak_kind, "traffic": _ncu_traffic("qkv_rnrc", args.workload),
+                         "algorithmic_per_launch": nb, "avg_launch_us": span_us,
+                         "timing": "kernel span from %globaltimer stamps inside pipelined calls",
+                         "per_kernel_dep_to_end_us": {"qkv_rnrc": per["qkv_rnrc"]["dep_to_end_us"]}},
+            "path_roofline": {"bytes": nb, "roofline_us": round(nb / (hbm * 1e9) * 1e6, 3),
+                              "frac": round(nb / (hbm * 1e9) / (ms / 1e3), 4), "bound": "hbm"},
             "clocks": clk.summary(), "e2e": e2e, "gpu_launches": steps}
 
 
@@ -633,20 +838,24 @@ def run_qkv_e2e(args, case, cpu, t, d, dev, stream):
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the CPU oracle as it stands, timed on this host's cores."""
+    """The reference arm: the CPU oracle as it stands, timed on this host's cores (rank 0 only;
+    the other ranks exit without work)."""
     if rank != 0:
         return None
     case = _case(args.workload)
     steps = args.steps or 3
     warm = max(0, min(args.warmup, 1))
-    import synthetic
     per_step_budget = 5.0
     vals = []
+    sample = ""
     for i in range(warm + steps):
-        v, cores, sample = oracle_tokens_per_s(case, budget_s=per_step_budget)
+        v, calls, el, ntok = _oracle_rate(case, per_step_budget, 4)
+        sample = (f"{ntok} tokens of the {case.name} workload per oracle call; {calls} calls in "
+                  f"{el:.1f} s per step")
         if i >= warm:
             vals.append(v)
     v = statistics.mean(vals)
+    cores = _cores()
     cfg = {"workload": case.name}
     return {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT,
             "n_gpus": world, "steps": steps, "warmup": warm,
@@ -661,6 +870,13 @@ def run_reference(args, rank, world):
 
 def main():
     args = _parse()
+    if args.oracle_worker is not None:
+        _oracle_worker(args.oracle_worker)
+        return
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # no launcher: start the N replicas here, one process per GPU
+        _spawn_replicas(args.gpus, sys.argv[1:])
+        return
     rank, local, world = _dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, rank, world)

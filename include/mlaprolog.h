@@ -166,7 +166,7 @@ mlap_status_t mlap_prepack_weights(const mlap_tensor_t* w, int32_t which, int32_
  * workspace bytes execute needs for these shapes.  Errors: NULL, SHAPE, DTYPE, UNSUPPORTED. */
 mlap_status_t mlap_get_workspace_size(const mlap_args_t* args, size_t* bytes);
 
-/* Zero the workspace's error word and counters.  Call once after allocating a workspace (or
+/* Zero the workspace's error word (its first 256 bytes).  Call once after allocating a workspace (or
  * cudaMemset the first 256 bytes to 0).  Asynchronous on `stream`. */
 mlap_status_t mlap_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
@@ -253,23 +253,38 @@ const char* mlap_status_string(mlap_status_t status);
 /* Reason for the last non-OK status returned on this thread ("" if none). */
 const char* mlap_last_error(void);
 
-/* Per-kernel timing of mlap_execute for profiling (CUDA events recorded on the execute stream
- * around each kernel).  mlap_timer_create makes a timer for up to max_calls timed calls;
- * mlap_execute_timed is mlap_execute plus event records (it inserts no synchronisation);
- * mlap_timer_read synchronises, writes the milliseconds of kernel k of call c to
- * ms[c * MLAP_TIMER_PHASES + k] for the calls recorded so far, and resets the timer.
- * Phases: 0 down-projection (with the input RmsNormQuant or the full-quant token_x widening
- * ahead of it when those run), 1 RmsNorm/RoPE/scatter, 2 up-projection, 3 absorb (with the int8
- * query quantisation after it in full quant).  Where one kernel runs the up-projection and the
- * absorb together (decode: T <= 128, N >= 16, D = 128, Dr = 64, Hckv <= 512 and a multiple of
- * 32), phase 2 times it (and the int8 query quantisation after it in full quant) and phase 3
- * reads exactly 0. */
-#define MLAP_TIMER_PHASES 4
-mlap_status_t mlap_timer_create(void** timer, int32_t max_calls);
-mlap_status_t mlap_execute_timed(const mlap_args_t* args, void* workspace,
-                                 size_t workspace_bytes, void* stream, void* timer);
-mlap_status_t mlap_timer_read(void* timer, float* ms, int32_t* calls_recorded);
-mlap_status_t mlap_timer_destroy(void* timer);
+/* Execution stamps, for profiling a call whose kernels overlap (programmatic dependent launch
+ * lets each kernel start while the one before it finishes, so events between the launches would
+ * change what they measure).  mlap_execute_stamped is mlap_execute launching the same kernels in
+ * the same way, each of which also records %globaltimer readings (ns) in `stamps`, a
+ * caller-owned device buffer of MLAP_STAMP_KERNELS * MLAP_STAMP_BLOCK uint64 words, 8-byte
+ * aligned, that the caller zeroes before the call (the call itself adds no work to the stream,
+ * so a stamped call pipelines with its neighbours exactly as an unstamped one).  Each kernel
+ * writes the slot of its kind:
+ *   slot k starts at word k * MLAP_STAMP_BLOCK;
+ *   word 0: bitwise complement of the earliest CTA start, word 1: the latest CTA end;
+ *   words 4 + 4c + i for CTA c < MLAP_STAMP_CTAS: i = 0 start, 1 the wait on the preceding
+ *   kernel returned, 2 the main loop's results ready (accumulator or reduction), 3 end.
+ * A slot whose kernel did not run stays zero.  Slots: MLAP_STAMP_DOWN down-projection;
+ * MLAP_STAMP_NORM RmsNorm/RoPE/quant/scatter; MLAP_STAMP_UP up-projection, or the fused
+ * up-projection and absorb where one kernel runs both (decode: T <= 128, N >= 16, D = 128,
+ * Dr = 64, Hckv <= 512 and a multiple of 32); MLAP_STAMP_ABSORB the separate absorb;
+ * MLAP_STAMP_QKV the QkvRmsNormRopeCache kernel (qkvrnrc_execute_stamped).  The small helper
+ * kernels (input RmsNormQuant, token_x widening, int8 query quantisation) record nothing.
+ * Same errors as the execute calls, plus MLAP_ERR_NULL for a NULL `stamps`.  Stamps are
+ * profiling aids with the resolution of %globaltimer; nothing in the results depends on them. */
+#define MLAP_STAMP_KERNELS 5
+#define MLAP_STAMP_BLOCK 1024
+#define MLAP_STAMP_CTAS 255
+#define MLAP_STAMP_DOWN 0
+#define MLAP_STAMP_NORM 1
+#define MLAP_STAMP_UP 2
+#define MLAP_STAMP_ABSORB 3
+#define MLAP_STAMP_QKV 4
+mlap_status_t mlap_execute_stamped(const mlap_args_t* args, void* workspace,
+                                   size_t workspace_bytes, void* stream, uint64_t* stamps);
+mlap_status_t qkvrnrc_execute_stamped(const qkvrnrc_args_t* args, void* workspace,
+                                      size_t workspace_bytes, void* stream, uint64_t* stamps);
 
 /* ============================================================================================ */
 /* Allocation-free MLA prolog                                                                    */
@@ -289,11 +304,12 @@ mlap_status_t mlap_timer_destroy(void* timer);
  *   - Shapes whose workspace (mlap_get_workspace_size) exceeds MLAP_NO_ALLOC_SCRATCH_BYTES are
  *     rejected with MLAP_ERR_WORKSPACE before any device work.  With the decode shapes
  *     (He 7168, Hcq 1536, Hckv 512, N 128, D 128, Dr 64) in the non-quant scenario without
- *     the input RmsNormQuant (which adds T * He * 2 bytes, as full quant does), calls with T <= 128 or
- *     257 <= T <= 567 tokens fit (up to 256 tokens the down-projection keeps up to 16 K-split
+ *     the input RmsNormQuant (which adds T * He * 2 bytes, as full quant does), calls with T <= 147 or
+ *     257 <= T <= 568 tokens fit (up to 256 tokens the down-projection keeps up to 16 K-split
  *     partials, above that one).
- *   - The first call on each device looks up the array's device address with that device
- *     current; make that first call before any stream capture on the device.
+ *   - Every call looks up the array's device address on the current device (the first lookup on
+ *     a device may load the library's device code there); make the first call on each device
+ *     before any stream capture on it.
  *   - Every call on a device shares the one array and clears its error word first; calls that
  *     may overlap on the GPU (different streams, or other threads) race on it and must be
  *     serialised by the caller.  Kernel-detected cache-index errors are skipped on the device

@@ -17,7 +17,11 @@ LIB_PATH = os.path.join(_PKG, "libmlaprolog.so")
 MLAP_DTYPE_INVALID, MLAP_DTYPE_BF16, MLAP_DTYPE_FP16, MLAP_DTYPE_FP32, MLAP_DTYPE_INT8, \
     MLAP_DTYPE_INT64 = range(6)
 MLAP_WEIGHT_DQ, MLAP_WEIGHT_UQ_QR, MLAP_WEIGHT_UK, MLAP_WEIGHT_DKV_KR = range(4)
-MLAP_TIMER_PHASES = 4
+# execution stamps (include/mlaprolog.h): slots of MLAP_STAMP_BLOCK uint64 words
+MLAP_STAMP_KERNELS, MLAP_STAMP_BLOCK, MLAP_STAMP_CTAS = 5, 1024, 255
+MLAP_STAMP_DOWN, MLAP_STAMP_NORM, MLAP_STAMP_UP, MLAP_STAMP_ABSORB, MLAP_STAMP_QKV = range(5)
+STAMP_NAMES = {MLAP_STAMP_DOWN: "down", MLAP_STAMP_NORM: "norm_scatter", MLAP_STAMP_UP: "up",
+               MLAP_STAMP_ABSORB: "absorb", MLAP_STAMP_QKV: "qkv_rnrc"}
 
 STATUS_NAMES = {0: "MLAP_OK", 1: "MLAP_ERR_NULL", 2: "MLAP_ERR_SHAPE", 3: "MLAP_ERR_DTYPE",
                 4: "MLAP_ERR_UNSUPPORTED", 5: "MLAP_ERR_WORKSPACE", 6: "MLAP_ERR_CUDA",
@@ -31,8 +35,8 @@ _TORCH_DTYPE = {torch.bfloat16: MLAP_DTYPE_BF16, torch.float16: MLAP_DTYPE_FP16,
 EXPORTS = ["mlap_prepack_size", "mlap_prepack_weights", "mlap_get_workspace_size",
            "mlap_workspace_init", "mlap_execute", "mlap_check_errors",
            "qkvrnrc_get_workspace_size", "qkvrnrc_execute", "mlap_status_string",
-           "mlap_last_error", "mlap_timer_create", "mlap_execute_timed", "mlap_timer_read",
-           "mlap_timer_destroy", "mlap_execute_no_alloc", "mlap_selftest_bounded_wait"]
+           "mlap_last_error", "mlap_execute_stamped", "qkvrnrc_execute_stamped",
+           "mlap_execute_no_alloc", "mlap_selftest_bounded_wait"]
 
 
 class MlapError(RuntimeError):
@@ -106,11 +110,8 @@ def load() -> ctypes.CDLL:
         "qkvrnrc_execute": (st, [Q, vp, ctypes.c_size_t, vp]),
         "mlap_status_string": (ctypes.c_char_p, [st]),
         "mlap_last_error": (ctypes.c_char_p, []),
-        "mlap_timer_create": (st, [ctypes.POINTER(vp), ctypes.c_int32]),
-        "mlap_execute_timed": (st, [A, vp, ctypes.c_size_t, vp, vp]),
-        "mlap_timer_read": (st, [vp, ctypes.POINTER(ctypes.c_float),
-                                 ctypes.POINTER(ctypes.c_int32)]),
-        "mlap_timer_destroy": (st, [vp]),
+        "mlap_execute_stamped": (st, [A, vp, ctypes.c_size_t, vp, vp]),
+        "qkvrnrc_execute_stamped": (st, [Q, vp, ctypes.c_size_t, vp, vp]),
         "mlap_execute_no_alloc": (st, [A, vp]),
     }
     for name, (res, args) in sig.items():
@@ -271,28 +272,50 @@ def qkvrnrc_execute(args: qkvrnrc_args_t, ws: torch.Tensor, stream=None):
 
 
 # --------------------------------------------------------------------------------- profiling
-class Timer:
-    """Per-kernel CUDA-event timing of mlap_execute calls (mlap_timer_* in the C ABI)."""
+def stamps_buffer(device, calls: int = 1) -> torch.Tensor:
+    """Device buffer for the execution stamps of `calls` calls (one stamps area per call)."""
+    return torch.zeros(calls, MLAP_STAMP_KERNELS * MLAP_STAMP_BLOCK, dtype=torch.int64,
+                       device=device)
 
-    def __init__(self, max_calls: int):
-        self.h = ctypes.c_void_p()
-        self.max_calls = max_calls
-        _check(load().mlap_timer_create(ctypes.byref(self.h), max_calls), "mlap_timer_create")
 
-    def execute(self, args: mlap_args_t, ws: torch.Tensor, stream=None):
-        _check(load().mlap_execute_timed(ctypes.byref(args), ws.data_ptr(),
-                                         ws.numel() * ws.element_size(), _stream_ptr(stream),
-                                         self.h), "mlap_execute_timed")
+def mlap_execute_stamped(args: mlap_args_t, ws: torch.Tensor, stamps: torch.Tensor, stream=None):
+    """mlap_execute whose kernels also record %globaltimer stamps into `stamps` (one row of
+    stamps_buffer, zeroed by the caller beforehand)."""
+    _check(load().mlap_execute_stamped(ctypes.byref(args), ws.data_ptr(),
+                                       ws.numel() * ws.element_size(), _stream_ptr(stream),
+                                       stamps.data_ptr()), "mlap_execute_stamped")
 
-    def read(self):
-        """List of per-call [down, norm/scatter, up, absorb] milliseconds."""
-        buf = (ctypes.c_float * (self.max_calls * MLAP_TIMER_PHASES))()
-        n = ctypes.c_int32()
-        _check(load().mlap_timer_read(self.h, buf, ctypes.byref(n)), "mlap_timer_read")
-        return [[buf[c * MLAP_TIMER_PHASES + k] for k in range(MLAP_TIMER_PHASES)]
-                for c in range(n.value)]
 
-    def close(self):
-        if self.h:
-            load().mlap_timer_destroy(self.h)
-            self.h = ctypes.c_void_p()
+def qkvrnrc_execute_stamped(args: qkvrnrc_args_t, ws: torch.Tensor, stamps: torch.Tensor,
+                            stream=None):
+    _check(load().qkvrnrc_execute_stamped(ctypes.byref(args), ws.data_ptr(),
+                                          ws.numel() * ws.element_size(), _stream_ptr(stream),
+                                          stamps.data_ptr()), "qkvrnrc_execute_stamped")
+
+
+def read_stamps(stamps_row) -> dict:
+    """Per kernel that ran: its span (earliest CTA start to latest CTA end, ns), the time from
+    the first wait on the preceding kernel returning to the latest end (ns), and the per-CTA
+    stamps [start, dependency resolved, main work done, end] of the first CTAs (ns, relative to
+    the earliest start of the call)."""
+    import numpy as np
+    w = np.asarray(stamps_row.detach().cpu().numpy(), dtype=np.int64).view(np.uint64)
+    blocks = w.reshape(MLAP_STAMP_KERNELS, MLAP_STAMP_BLOCK)
+    starts = [int(~b[0]) for b in blocks if b[1] != 0]
+    if not starts:
+        return {}
+    t0 = min(starts)
+    out = {}
+    for k, b in enumerate(blocks):
+        if b[1] == 0:
+            continue
+        first = int(~b[0])
+        cta = b[4:4 + 4 * MLAP_STAMP_CTAS].reshape(MLAP_STAMP_CTAS, 4).astype(np.int64)
+        used = cta[:, 0] != 0
+        dep = cta[used, 1]
+        dep = dep[dep != 0]
+        out[STAMP_NAMES[k]] = {
+            "start_ns": first - t0, "end_ns": int(b[1]) - t0, "span_ns": int(b[1]) - first,
+            "dep_to_end_ns": (int(b[1]) - int(dep.min())) if dep.size else None,
+            "ctas": np.where(cta[used] != 0, cta[used] - t0, -1).tolist()}
+    return out

@@ -106,9 +106,7 @@ constexpr int kMaxSplits = 16;
 // smallest head count of the pages on it beats the separate kernels (16 heads, T = 8: 20.1 ->
 // 15.0 µs per call).
 constexpr int kFusedMinHeads = 16;
-constexpr size_t kHeaderBytes = 8192;   // error word + stream-K flags
-constexpr size_t kFlagOffset = 4096;    // stream-K "partial written" flags (int32 per CTA)
-constexpr int kMaxStreamKCtas = 1024;   // flags that fit the header
+constexpr size_t kHeaderBytes = 256;    // the error word, padded to the workspace alignment
 
 mlap_status_t validate_mla(const mlap_args_t* a, MlaDims* d) {
   if (a == nullptr) return fail(MLAP_ERR_NULL, "args is NULL");
@@ -347,11 +345,8 @@ MlaWs mla_ws_layout(const MlaDims& d) {
   const int64_t ntot = d.Hcq + d.Hckv + d.Dr;
   size_t off = kHeaderBytes;
   w.part = off;
-  // the down-projection's K-split partials, reused later in the call by the up-projection's
-  // stream-K partial slots (one 128-row fp32 tile per CTA, up to 160 CTAs)
-  const size_t down_part = static_cast<size_t>(w.split_cap) * d.T * ntot * 4;
-  const size_t sk_part = swap ? static_cast<size_t>(160) * 128 * swap_bn(d.T) * 4 : 0;
-  off += align_up(down_part > sk_part ? down_part : sk_part, 256);
+  // the down-projection's K-split partials
+  off += align_up(static_cast<size_t>(w.split_cap) * d.T * ntot * 4, 256);
   w.cq = off;
   off += align_up(static_cast<size_t>(d.T) * d.Hcq * 2, 256);
   w.qc = off;
@@ -471,15 +466,8 @@ mlap_status_t cuda_fail(cudaError_t e, const char* what) {
   return fail(MLAP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-struct Timer {
-  std::vector<cudaEvent_t> ev;   // (MLAP_TIMER_PHASES + 1) per call
-  std::vector<uint8_t> fused;    // per call: up-projection and absorb ran as one kernel
-  int max_calls = 0;
-  int calls = 0;
-};
-
 mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStream_t stream,
-                      Timer* timer) {
+                      uint64_t* stamps) {
   MlaDims d;
   CHECK_STATUS(validate_mla(a, &d));
   if (d.T == 0) return MLAP_OK;
@@ -508,18 +496,13 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   const int mt = 1;                          // two-tile units pay off only with all SMs busy
   const int wrows = 128 * mt;
 
-  auto rec = [&](int phase) -> mlap_status_t {
-    if (timer == nullptr) return MLAP_OK;
-    cudaError_t e = cudaEventRecord(timer->ev[timer->calls * (MLAP_TIMER_PHASES + 1) + phase], stream);
-    return e == cudaSuccess ? MLAP_OK : cuda_fail(e, "cudaEventRecord");
-  };
-  if (timer != nullptr && timer->calls >= timer->max_calls) return fail(MLAP_ERR_UNSUPPORTED, "timer full");
-
   // ---- 1. down-projection x·[W^DQ | W^DKV|W^KR]  (fp32 K-split partials)
   GemmLaunch g{};
   g.stream = stream;
   g.pdl = true;
   g.err = err;
+  g.geo.stamps = stamps;
+  g.geo.stamp_k = MLAP_STAMP_DOWN;
   g.swap = swap;
   g.mt = swap ? mt : 1;
   DownParams dp{0};
@@ -577,7 +560,6 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     g.geo.k_blocks = kb;
     g.geo.w_op = swap ? 0 : 1;
     g.geo.num_units = g.geo.m_tiles * g.geo.n_tiles * g.geo.splits;
-    g.pm = g.a0;
     // partials part[s][t][f]: W^DQ columns and W^DKV|W^KR columns as two 3-D (f, t, s) maps
     const int64_t row_b = Ntot * 4, split_b = d.T * Ntot * 4;
     CHECK_STATUS(make_out_map(&g.o0, part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
@@ -587,7 +569,6 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                               {d.Hckv + d.Dr, d.T, g.geo.splits}, {row_b, split_b}, {32, ch_t, 1},
                               CU_TENSOR_MAP_SWIZZLE_128B));
     g.grid = balanced_grid(g.geo.num_units, sms);
-    CHECK_STATUS(rec(0));
     if (d.xnorm) {
       ce = launch_rms_norm_quant(static_cast<const __nv_bfloat16*>(a->token_x.data),
                                  static_cast<const __nv_bfloat16*>(a->rms_norm_quant_gamma.data),
@@ -636,12 +617,12 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     fp.smooth = d.w_int8 ? static_cast<const float*>(a->smooth_scales_cq.data) : nullptr;
     fp.scale_t = scale_t;
     fp.err = err;
+    fp.stamps = stamps;
     if (d.full) {
       fp.dsx = static_cast<const float*>(a->dequant_scale_x.data);
       fp.dsw_q = static_cast<const float*>(a->dequant_scale_w_dq.data);
       fp.dsw_kv = static_cast<const float*>(a->dequant_scale_w_dkv_kr.data);
     }
-    CHECK_STATUS(rec(1));
     ce = launch_finalize(fp, stream, true);
     if (ce != cudaSuccess) return cuda_fail(ce, "norm/rope/scatter launch");
   }
@@ -667,9 +648,9 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                       qn_out,
                       static_cast<int32_t>(d.T), static_cast<int32_t>(d.N),
                       static_cast<int32_t>(d.Hcq), static_cast<int32_t>(d.Hckv),
-                      scale_t, static_cast<const float*>(a->dequant_scale_w_uq_qr.data), 2, 0};
+                      scale_t, static_cast<const float*>(a->dequant_scale_w_uq_qr.data), 2, 0,
+                      stamps};
     up_absorb_plan(sms, static_cast<int>(d.N), &ua.k, &ua.R);
-    CHECK_STATUS(rec(2));
     ce = launch_up_absorb(tcq, tw, tuk, ua, d.w_int8, err, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "fused up-projection/absorb launch");
     if (d.query_int8) {
@@ -678,9 +659,6 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                               static_cast<int32_t>(d.Hckv), stream);
       if (ce != cudaSuccess) return cuda_fail(ce, "query quant launch");
     }
-    CHECK_STATUS(rec(3));
-    CHECK_STATUS(rec(4));
-    if (timer != nullptr) timer->fused[timer->calls] = 1;
   }
 
   // ---- 3. up-projection c^Q·[W^UQ|W^QR] -> q^C (bf16 workspace) and query_rope
@@ -689,6 +667,8 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.stream = stream;
     u.pdl = true;
     u.err = err;
+    u.geo.stamps = stamps;
+    u.geo.stamp_k = MLAP_STAMP_UP;
     // Decode with a bf16 weight and one 128-token tile: tokens as MMA rows and an equal range
     // of weight rows per SM (row-range schedule: 24576 rows on 152 SMs, 160 or 192 each).
     const bool up_var = swap && !d.w_int8 && d.T <= 128 && Mup % 32 == 0;
@@ -737,23 +717,6 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.geo.num_units = u.geo.m_tiles * u.geo.n_tiles;
     u.grid = up_var ? static_cast<int>(std::min<int64_t>(sms, Mup / 32))
                     : balanced_grid(u.geo.num_units, sms);
-    u.pm = u.a0;
-    // Stream-K (equal k-block ranges on every SM) is available for the decode orientation; on
-    // GB300 the whole-tile balanced grid measured faster (the decode up-projection is DRAM
-    // bound near 5 TB/s either way and stream-K adds a fix-up tail), so it is off by default.
-    const int64_t iters = static_cast<int64_t>(u.geo.num_units) * u.geo.k_blocks;
-    const int sk_grid = sms < 160 ? sms : 160;
-    const bool use_stream_k = std::getenv("MLAP_STREAM_K") != nullptr;
-    if (use_stream_k && u.swap && mt == 1 && bn_t >= 32 && u.geo.num_units % sk_grid != 0 &&
-        iters >= 2 * sk_grid) {
-      u.geo.stream_k = 1;
-      u.geo.sk_partial = part;
-      u.geo.sk_flag = reinterpret_cast<int32_t*>(wsb + kFlagOffset);
-      u.grid = sk_grid;
-      CHECK_STATUS(make_out_map(&u.pm, part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                                {bn_t, static_cast<int64_t>(sk_grid) * 128}, {bn_t * 4}, {32, 32},
-                                CU_TENSOR_MAP_SWIZZLE_128B));
-    }
     const int ch_u = u.swap ? ch_t : 32;   // tokens per store box: one per lane unless swapped
     CHECK_STATUS(make_out_map(&u.o0, qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, {d.N * d.D, d.T},
                               {d.N * d.D * 2}, {32, ch_u}, CU_TENSOR_MAP_SWIZZLE_64B));
@@ -768,7 +731,6 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                 static_cast<int32_t>(d.Dr),
                 up_var ? qc : nullptr,
                 up_var ? static_cast<__nv_bfloat16*>(a->query_rope.data) : nullptr};
-    CHECK_STATUS(rec(2));
     ce = launch_up(u, up, d.w_int8);
     if (ce != cudaSuccess) return cuda_fail(ce, "up-projection launch");
   }
@@ -779,6 +741,8 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.stream = stream;
     b.pdl = true;
     b.err = err;
+    b.geo.stamps = stamps;
+    b.geo.stamp_k = MLAP_STAMP_ABSORB;
     // Decode with one 128-token tile: tokens as MMA rows and the row-range schedule over all
     // heads' W^UK rows (128 x 512 rows on 152 SMs: 416 or 448 each, cut at head boundaries).
     const bool ab_var = swap && d.T <= 128 && d.Hckv % 32 == 0;
@@ -831,7 +795,6 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.geo.w_op = b.swap ? 0 : 1;
     b.geo.k_blocks = ceil_div(d.D, 64);
     b.geo.num_units = b.geo.m_tiles * b.geo.n_tiles * b.geo.batches;
-    b.pm = b.a0;
     b.grid = ab_var ? static_cast<int>(std::min<int64_t>(sms, d.N * d.Hckv / 32))
                     : balanced_grid(b.geo.num_units, sms);
     // an int8 query is quantised per token and head from a bf16 q^N staged in the workspace
@@ -844,7 +807,6 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     AbsorbParams ap{ab_var ? qn_out : nullptr,
                     static_cast<int32_t>(d.T), static_cast<int32_t>(d.N),
                     static_cast<int32_t>(d.Hckv)};
-    CHECK_STATUS(rec(3));
     ce = launch_absorb(b, ap);
     if (ce != cudaSuccess) return cuda_fail(ce, "absorb launch");
     if (d.query_int8) {
@@ -853,9 +815,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                               static_cast<int32_t>(d.Hckv), stream);
       if (ce != cudaSuccess) return cuda_fail(ce, "query quant launch");
     }
-    CHECK_STATUS(rec(4));
   }
-  if (timer != nullptr) timer->calls++;
   return MLAP_OK;
 }
 
@@ -961,6 +921,47 @@ mlap_status_t validate_qkv(const qkvrnrc_args_t* a, QkvDims* d) {
   return MLAP_OK;
 }
 
+mlap_status_t qkv_run(const qkvrnrc_args_t* a, void* ws, size_t ws_bytes, cudaStream_t stream,
+                      uint64_t* stamps) {
+  QkvDims d;
+  CHECK_STATUS(validate_qkv(a, &d));
+  if (d.T == 0) return MLAP_OK;
+  if (ws == nullptr || ws_bytes < 256) return fail(MLAP_ERR_WORKSPACE, "workspace too small");
+  int dev = 0, sms = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "device query");
+  QkvParams p{};
+  p.qkv = a->qkv.data;
+  p.gamma_q = a->gamma_q.data;
+  p.gamma_k = a->gamma_k.data;
+  p.cos = a->cos.data;
+  p.sin = a->sin.data;
+  p.index = static_cast<const int64_t*>(a->index.data);
+  p.slots = d.BlockNum * d.BlockSize;
+  p.k_cache = a->k_cache.data;
+  p.v_cache = a->v_cache.data;
+  p.k_scale = d.quant ? static_cast<const float*>(a->k_scale.data) : nullptr;
+  p.v_scale = d.quant ? static_cast<const float*>(a->v_scale.data) : nullptr;
+  p.k_offset = d.asym ? static_cast<const float*>(a->k_offset.data) : nullptr;
+  p.v_offset = d.asym ? static_cast<const float*>(a->v_offset.data) : nullptr;
+  p.q_before = present(a->q_before_quant) ? a->q_before_quant.data : nullptr;
+  p.k_before = present(a->k_before_quant) ? a->k_before_quant.data : nullptr;
+  p.v_before = present(a->v_before_quant) ? a->v_before_quant.data : nullptr;
+  p.q_out = a->q_out.data;
+  p.T = static_cast<int32_t>(d.T);
+  p.Nq = a->Nq;
+  p.Nk = a->Nk;
+  p.Nv = a->Nv;
+  p.eps = static_cast<float>(a->epsilon);
+  p.bf16 = d.bf16;
+  p.err = static_cast<uint32_t*>(ws);
+  p.stamps = stamps;
+  ce = launch_qkv_rnrc(p, stream, sms);
+  if (ce != cudaSuccess) return cuda_fail(ce, "QkvRmsNormRopeCache launch");
+  return MLAP_OK;
+}
+
 }  // namespace
 
 // ================================================================================================
@@ -1055,8 +1056,7 @@ mlap_status_t mlap_get_workspace_size(const mlap_args_t* args, size_t* bytes) {
 mlap_status_t mlap_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (ws == nullptr) return fail(MLAP_ERR_NULL, "workspace is NULL");
   if (ws_bytes < 256) return fail(MLAP_ERR_WORKSPACE, "workspace smaller than its 256-byte header");
-  const size_t n = ws_bytes < kHeaderBytes ? 256 : kHeaderBytes;
-  cudaError_t e = cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderBytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   return MLAP_OK;
 }
@@ -1097,93 +1097,19 @@ mlap_status_t qkvrnrc_get_workspace_size(const qkvrnrc_args_t* args, size_t* byt
 }
 
 mlap_status_t qkvrnrc_execute(const qkvrnrc_args_t* a, void* ws, size_t ws_bytes, void* stream) {
-  QkvDims d;
-  CHECK_STATUS(validate_qkv(a, &d));
-  if (d.T == 0) return MLAP_OK;
-  if (ws == nullptr || ws_bytes < 256) return fail(MLAP_ERR_WORKSPACE, "workspace too small");
-  int dev = 0, sms = 0;
-  cudaError_t ce = cudaGetDevice(&dev);
-  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (ce != cudaSuccess) return cuda_fail(ce, "device query");
-  QkvParams p{};
-  p.qkv = a->qkv.data;
-  p.gamma_q = a->gamma_q.data;
-  p.gamma_k = a->gamma_k.data;
-  p.cos = a->cos.data;
-  p.sin = a->sin.data;
-  p.index = static_cast<const int64_t*>(a->index.data);
-  p.slots = d.BlockNum * d.BlockSize;
-  p.k_cache = a->k_cache.data;
-  p.v_cache = a->v_cache.data;
-  p.k_scale = d.quant ? static_cast<const float*>(a->k_scale.data) : nullptr;
-  p.v_scale = d.quant ? static_cast<const float*>(a->v_scale.data) : nullptr;
-  p.k_offset = d.asym ? static_cast<const float*>(a->k_offset.data) : nullptr;
-  p.v_offset = d.asym ? static_cast<const float*>(a->v_offset.data) : nullptr;
-  p.q_before = present(a->q_before_quant) ? a->q_before_quant.data : nullptr;
-  p.k_before = present(a->k_before_quant) ? a->k_before_quant.data : nullptr;
-  p.v_before = present(a->v_before_quant) ? a->v_before_quant.data : nullptr;
-  p.q_out = a->q_out.data;
-  p.T = static_cast<int32_t>(d.T);
-  p.Nq = a->Nq;
-  p.Nk = a->Nk;
-  p.Nv = a->Nv;
-  p.eps = static_cast<float>(a->epsilon);
-  p.bf16 = d.bf16;
-  p.err = static_cast<uint32_t*>(ws);
-  ce = launch_qkv_rnrc(p, static_cast<cudaStream_t>(stream), sms);
-  if (ce != cudaSuccess) return cuda_fail(ce, "QkvRmsNormRopeCache launch");
-  return MLAP_OK;
+  return qkv_run(a, ws, ws_bytes, static_cast<cudaStream_t>(stream), nullptr);
 }
 
-mlap_status_t mlap_timer_create(void** timer, int32_t max_calls) {
-  if (timer == nullptr) return fail(MLAP_ERR_NULL, "timer is NULL");
-  if (max_calls <= 0) return fail(MLAP_ERR_SHAPE, "max_calls must be positive");
-  Timer* t = new Timer();
-  t->max_calls = max_calls;
-  t->ev.resize(static_cast<size_t>(max_calls) * (MLAP_TIMER_PHASES + 1));
-  t->fused.assign(static_cast<size_t>(max_calls), 0);
-  for (auto& e : t->ev) {
-    if (cudaEventCreate(&e) != cudaSuccess) {
-      delete t;
-      return fail(MLAP_ERR_CUDA, "cudaEventCreate failed");
-    }
-  }
-  *timer = t;
-  return MLAP_OK;
+mlap_status_t mlap_execute_stamped(const mlap_args_t* args, void* ws, size_t ws_bytes, void* stream,
+                                   uint64_t* stamps) {
+  if (stamps == nullptr) return fail(MLAP_ERR_NULL, "stamps is NULL");
+  return mla_run(args, ws, ws_bytes, static_cast<cudaStream_t>(stream), stamps);
 }
 
-mlap_status_t mlap_execute_timed(const mlap_args_t* args, void* ws, size_t ws_bytes, void* stream,
-                                 void* timer) {
-  if (timer == nullptr) return fail(MLAP_ERR_NULL, "timer is NULL");
-  return mla_run(args, ws, ws_bytes, static_cast<cudaStream_t>(stream), static_cast<Timer*>(timer));
-}
-
-mlap_status_t mlap_timer_read(void* timer, float* ms, int32_t* calls_recorded) {
-  if (timer == nullptr || calls_recorded == nullptr) return fail(MLAP_ERR_NULL, "NULL argument");
-  Timer* t = static_cast<Timer*>(timer);
-  for (int c = 0; c < t->calls; ++c) {
-    for (int k = 0; k < MLAP_TIMER_PHASES; ++k) {
-      cudaEvent_t e0 = t->ev[c * (MLAP_TIMER_PHASES + 1) + k];
-      cudaEvent_t e1 = t->ev[c * (MLAP_TIMER_PHASES + 1) + k + 1];
-      if (cudaEventSynchronize(e1) != cudaSuccess) return fail(MLAP_ERR_CUDA, "cudaEventSynchronize failed");
-      float v = 0.f;
-      if (cudaEventElapsedTime(&v, e0, e1) != cudaSuccess) return fail(MLAP_ERR_CUDA, "cudaEventElapsedTime failed");
-      if (k == 3 && t->fused[c]) v = 0.f;   // no separate absorb kernel ran
-      if (ms) ms[c * MLAP_TIMER_PHASES + k] = v;
-    }
-  }
-  *calls_recorded = t->calls;
-  t->calls = 0;
-  std::fill(t->fused.begin(), t->fused.end(), 0);
-  return MLAP_OK;
-}
-
-mlap_status_t mlap_timer_destroy(void* timer) {
-  if (timer == nullptr) return MLAP_OK;
-  Timer* t = static_cast<Timer*>(timer);
-  for (auto& e : t->ev) cudaEventDestroy(e);
-  delete t;
-  return MLAP_OK;
+mlap_status_t qkvrnrc_execute_stamped(const qkvrnrc_args_t* args, void* ws, size_t ws_bytes,
+                                      void* stream, uint64_t* stamps) {
+  if (stamps == nullptr) return fail(MLAP_ERR_NULL, "stamps is NULL");
+  return qkv_run(args, ws, ws_bytes, static_cast<cudaStream_t>(stream), stamps);
 }
 
 }  // extern "C"
@@ -1199,12 +1125,6 @@ mlap_status_t mlap_timer_destroy(void* timer) {
 // uses this entry point keeps the array until the process exits.
 static __device__ __align__(256) uint8_t g_mlap_static_scratch[MLAP_NO_ALLOC_SCRATCH_BYTES];
 
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_static_scratch_mu;
-void* g_static_scratch_ptr[kMaxDevices] = {};
-}  // namespace
-
 extern "C" mlap_status_t mlap_execute_no_alloc(const mlap_args_t* args, void* stream) {
   MlaDims d;
   CHECK_STATUS(validate_mla(args, &d));
@@ -1216,26 +1136,16 @@ extern "C" mlap_status_t mlap_execute_no_alloc(const mlap_args_t* args, void* st
                     std::to_string(static_cast<size_t>(MLAP_NO_ALLOC_SCRATCH_BYTES)) +
                     " (use mlap_execute with a caller workspace)");
   if (d.T == 0) return MLAP_OK;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(MLAP_ERR_UNSUPPORTED, "device ordinal too large");
+  // The array's name is only a host-side stand-in: the kernels get the device address the runtime
+  // reports for it on the current device.  The lookup is asked for on every call (a host-side
+  // table lookup once the module is loaded), so a context that was torn down and made again
+  // (cudaDeviceReset) gets the array's new address.
   void* scratch = nullptr;
-  {
-    // Once per device, with that device current: the array's name is only a host-side stand-in,
-    // so the kernels get the device address the runtime reports for it.
-    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-    if (g_static_scratch_ptr[dev] == nullptr) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_mlap_static_scratch);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-      g_static_scratch_ptr[dev] = p;
-    }
-    scratch = g_static_scratch_ptr[dev];
-  }
-  // The array keeps the previous call's contents; only the error word must start at zero (every
-  // other scratch byte a call reads was written earlier in the same call).
-  e = cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetSymbolAddress(&scratch, g_mlap_static_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+  // The array keeps the previous call's contents; only the header (the error word) must start at
+  // zero: every other scratch byte a call reads was written earlier in the same call.
+  e = cudaMemsetAsync(scratch, 0, kHeaderBytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch header");
   return mla_run(args, scratch, static_cast<size_t>(MLAP_NO_ALLOC_SCRATCH_BYTES),
                  static_cast<cudaStream_t>(stream), nullptr);

@@ -31,17 +31,12 @@
 // (WQ) or activation loaders (ALD).
 //
 // Work units: (m tile, n tile, batch, k split), m fastest, distributed round-robin over a grid
-// of at most one CTA per SM.  In stream-K mode every CTA instead takes an equal contiguous range
-// of the (tile, k block) iterations; a tile cut by range boundaries is finished by the CTA that
-// holds its first k blocks (it reaches them last): the other CTAs write their fp32 partial to a
-// per-CTA slot and raise a flag, and the owner adds the partials in CTA order (deterministic)
-// before the real epilogue.  Partials move as 4 KB blocks (one per epilogue warp and 32-column
-// chunk, kept in the swizzled staging layout) with 1-D bulk copies; the owner's piece is always
-// its CTA's last, so it lands the blocks in the by then idle pipeline buffers.  Either operand may be "segmented": tiles below *_seg_tiles come
+// of at most one CTA per SM.  Either operand may be "segmented": tiles below *_seg_tiles come
 // from the first tensor map, the rest from the second (rebased to row 0), which lets one GEMM
 // run over two separately stored weights (W^DQ and W^DKV|W^KR) without copying them together.
 #pragma once
 #include "ptx.cuh"
+#include "stamps.cuh"
 
 namespace mlap {
 
@@ -53,9 +48,6 @@ struct GemmGeometry {
   int32_t b_x_batch, b_y_batch;
   int32_t num_units;
   int32_t w_op;                     // operand holding the weight: 0 = A, 1 = B
-  int32_t stream_k;                 // 1: equal (tile, k block) ranges per CTA (splits must be 1)
-  float* sk_partial;                // stream-K: per-CTA fp32 partial slots (BM_U * BN floats each)
-  int32_t* sk_flag;                 // stream-K: per-CTA "partial written" flags, 0 between calls
   // ALD: the activation operand (B, decode orientation) as a row-major bf16 matrix
   const uint16_t* act;              // element (y, x) at act[y * act_ld + x]
   int64_t act_ld;
@@ -66,14 +58,15 @@ struct GemmGeometry {
   // boxes and multiplied with N = its row count, so every SM streams the same share of the
   // weight whatever its row count (no tile rounding, no partial sums).
   int32_t rr_rows;
+  // Optional execution stamps (%globaltimer) of this launch, kernel slot stamp_k (stamps.cuh).
+  uint64_t* stamps;
+  int32_t stamp_k;
 };
 
-// One piece of work for a CTA: a tile and its k-block range, and its stream-K role.
+// One piece of work for a CTA: a tile and its k-block range.
 struct Frag {
   int tm, tn, b, s;
   int kb0, kb1;
-  int kind;      // 0: whole tile; 1: owner of a cut tile; 2: contributor to a cut tile
-  int c_last;    // owner: last CTA holding a piece of this tile
   int row0, rows;   // row-range schedule: rows of operand B (within batch b) of the piece
 };
 
@@ -140,20 +133,15 @@ __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& t
 template <bool RR, int BN>
 struct FragIter {
   int u;
-  long long i, i1, total;
+  long long i, i1;
   __device__ __forceinline__ explicit FragIter(const GemmGeometry& g) {
     u = blockIdx.x;
+    i = i1 = 0;
     if constexpr (RR) {   // chunk range of this CTA
-      total = static_cast<long long>(g.batches) * (g.rr_rows / 32);
-    } else {
-      total = static_cast<long long>(g.num_units) * g.k_blocks;   // stream-K: num_units = tiles
+      const long long total = static_cast<long long>(g.batches) * (g.rr_rows / 32);
+      i = total * blockIdx.x / gridDim.x;
+      i1 = total * (blockIdx.x + 1) / gridDim.x;
     }
-    i = total * blockIdx.x / gridDim.x;
-    i1 = total * (blockIdx.x + 1) / gridDim.x;
-  }
-  // CTA whose range holds iteration it
-  __device__ __forceinline__ int cta_of(long long it) const {
-    return static_cast<int>(((it + 1) * gridDim.x - 1) / total);
   }
   __device__ __forceinline__ bool next(const GemmGeometry& g, Frag& f) {
     if constexpr (RR) {
@@ -170,40 +158,18 @@ struct FragIter {
       f.s = 0;
       f.kb0 = 0;
       f.kb1 = g.k_blocks;
-      f.kind = 0;
-      f.c_last = 0;
       f.row0 = c0 * 32;
       f.rows = static_cast<int>(n) * 32;
       i += n;
       return true;
     }
-    if (!g.stream_k) {
-      if (u >= g.num_units) return false;
-      decode_unit(g, u, f.tm, f.tn, f.b, f.s);
-      f.kb0 = (f.s * g.k_blocks) / g.splits;
-      f.kb1 = ((f.s + 1) * g.k_blocks) / g.splits;
-      f.kind = 0;
-      f.c_last = 0;
-      u += gridDim.x;
-      return true;
-    }
-    if (i >= i1) return false;
-    const long long K = g.k_blocks;
-    const long long tile = i / K;
-    f.kb0 = static_cast<int>(i % K);
-    const long long end = (i1 - i) < (K - f.kb0) ? f.kb0 + (i1 - i) : K;
-    f.kb1 = static_cast<int>(end);
-    decode_unit(g, static_cast<int>(tile), f.tm, f.tn, f.b, f.s);
-    if (f.kb0 == 0 && f.kb1 == K) {
-      f.kind = 0;
-    } else if (f.kb0 == 0) {
-      f.kind = 1;
-      f.c_last = cta_of(tile * K + K - 1);
-    } else {
-      f.kind = 2;
-    }
-    f.c_last = f.kind == 1 ? f.c_last : 0;
-    i += f.kb1 - f.kb0;
+    if (u >= g.num_units) return false;
+    decode_unit(g, u, f.tm, f.tn, f.b, f.s);
+    f.kb0 = (f.s * g.k_blocks) / g.splits;
+    f.kb1 = ((f.s + 1) * g.k_blocks) / g.splits;
+    f.row0 = 0;
+    f.rows = 0;
+    u += gridDim.x;
     return true;
   }
 };
@@ -244,14 +210,6 @@ __device__ __forceinline__ void convert_int8_row(const uint8_t* src_row, uint8_t
   }
 }
 
-// Lane-as-row staging of 32 consecutive fp32 values in the 128B-swizzled TMA store layout.
-__device__ __forceinline__ void stage_row_f32_sw128(uint8_t* sb, int r, const float* v) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    *reinterpret_cast<float4*>(sb + r * 128 + (((c ^ (r & 7)) & 7) << 4)) =
-        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-}
-
 // Epilogue functor contract (see epilogues.cuh):
 //   __device__ int operator()(int m0, int n0, int batch, int split, const float (&v)[CH],
 //                             uint8_t* stage, StoreOp (&ops)[2]) const;
@@ -266,8 +224,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmB0,
                      const __grid_constant__ CUtensorMap tmB1,
                      const __grid_constant__ CUtensorMap tmO0,
-                     const __grid_constant__ CUtensorMap tmO1,
-                     const __grid_constant__ CUtensorMap tmP, const GemmGeometry geo,
+                     const __grid_constant__ CUtensorMap tmO1, const GemmGeometry geo,
                      const Epi epi, uint32_t* __restrict__ err_word) {
   using Cfg = GemmCfg<BN, WQ, MT, ALD>;
   constexpr bool RR = Epi::kDirect;   // the row-range launches are the direct-store ones
@@ -284,13 +241,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
   uint64_t* rawf_bar = empty_bar + Cfg::STAGES;
   uint64_t* accf_bar = rawf_bar + Cfg::STAGES;
   uint64_t* acce_bar = accf_bar + 2;
-  uint64_t* land_bar = acce_bar + 2;                                   // stream-K partial landing
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(land_bar + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const bool w_is_a = geo.w_op == 0;
+  if (threadIdx.x == 0) stamp(geo.stamps, geo.stamp_k, kStampStart);
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA0);
@@ -299,7 +256,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     prefetch_tmap(&tmB1);
     prefetch_tmap(&tmO0);
     prefetch_tmap(&tmO1);
-    if (geo.stream_k) prefetch_tmap(&tmP);
   }
   if (warp == 1 && lane == 0) {
     for (int i = 0; i < Cfg::STAGES; ++i) {
@@ -311,7 +267,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
       mbar_init(&accf_bar[i], 1);
       mbar_init(&acce_bar[i], 4);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&land_bar[i], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -390,6 +345,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
         }
       }
       grid_dependency_wait();
+      stamp(geo.stamps, geo.stamp_k, kStampDep);
 
       int stage = 0;
       uint32_t phase = 0;
@@ -491,39 +447,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
       typename Epi::Pre pre = epi.preload(tm * Cfg::BM_U + q * 32, n_row0);
       if (!mbar_wait(&accf_bar[buf], use & 1u, abort_flag)) break;
       tc_fence_after_sync();
-      constexpr int kChunks = MT * Cfg::BN / 32;               // 4 KB partial blocks per warp
-      constexpr int kLandBlocks = (Cfg::STAGES * Cfg::STAGE_BYTES / 4) / 4096;
-      uint8_t* land = smem + q * (kLandBlocks * 4096);          // idle pipeline buffers
-      int landed = 0;                                           // contributors held in smem
-      if (f.kind == 1) {
-        // owner of a cut tile (always this CTA's last piece): wait until every later piece's
-        // partial is written, then bring this warp's blocks of as many as fit into smem at once
-        const int ncon = f.c_last - static_cast<int>(blockIdx.x);
-        landed = ncon * kChunks <= kLandBlocks ? ncon : kLandBlocks / kChunks;
-        if (lane == 0) {
-          for (int c = blockIdx.x + 1; c <= f.c_last; ++c) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(geo.sk_flag + c) == 0) {
-              if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
-                break;
-              }
-            }
-          }
-          fence_proxy_async_global();
-          if (landed > 0) {
-            mbar_arrive_expect_tx(&land_bar[q], landed * kChunks * 4096);
-            for (int k = 0; k < landed; ++k)
-              for (int ch = 0; ch < kChunks; ++ch)
-                bulk_load_1d(land + (k * kChunks + ch) * 4096,
-                             reinterpret_cast<const uint8_t*>(geo.sk_partial) +
-                                 ((static_cast<size_t>(blockIdx.x + 1 + k) * 4 + q) * kChunks + ch) * 4096,
-                             4096, &land_bar[q]);
-          }
-        }
-        __syncwarp();
-        if (landed > 0 && !mbar_wait(&land_bar[q], 0, abort_flag)) landed = 0;
-      }
+      if (q == 0 && lane == 0) stamp(geo.stamps, geo.stamp_k, kStampMain);
 #pragma unroll 1
       for (int hc = 0; hc < ncols; hc += Cfg::CH) {
         const int h = hc / Cfg::BN, c = hc % Cfg::BN;
@@ -550,42 +474,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[buf]);
         }
-        const int chunk = hc / 32;
-        if (f.kind == 1) {
-          // add the later pieces' partials in CTA order (fixed order: deterministic)
-          for (int cc = blockIdx.x + 1; cc <= f.c_last; ++cc) {
-            const int k = cc - static_cast<int>(blockIdx.x) - 1;
-            const uint8_t* blk =
-                k < landed ? land + (k * kChunks + chunk) * 4096
-                           : reinterpret_cast<const uint8_t*>(geo.sk_partial) +
-                                 ((static_cast<size_t>(cc) * 4 + q) * kChunks + chunk) * 4096;
-#pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-              const uint8_t* a = blk + lane * 128 + (((j4 ^ (lane & 7)) & 7) << 4);
-              const float4 pv = k < landed ? *reinterpret_cast<const float4*>(a)
-                                           : __ldcg(reinterpret_cast<const float4*>(a));
-              v[4 * j4] += pv.x;
-              v[4 * j4 + 1] += pv.y;
-              v[4 * j4 + 2] += pv.z;
-              v[4 * j4 + 3] += pv.w;
-            }
-          }
-        }
         uint8_t* sb = wstage + sel * Cfg::EPI_BUF;
         sel ^= 1;
         if (lane == 0) bulk_wait_group_read<1>();   // the store that last read this buffer is done
         __syncwarp();
         StoreOp ops[2];
-        int nops;
-        if (f.kind == 2) {
-          // contributor: the fp32 partial goes to this CTA's slot (row-major, lane = row)
-          if constexpr (Cfg::CH == 32) {
-            stage_row_f32_sw128(sb, lane, v);
-          }
-          nops = 0;
-        } else {
-          nops = epi(m0, n_row0 + c, b, s, v, sb, ops, pre);
-        }
+        const int nops = epi(m0, n_row0 + c, b, s, v, sb, ops, pre);
         if (hc + Cfg::CH < ncols) {   // the next block's inputs, while this one stores
           const int hn = (hc + Cfg::CH) / Cfg::BN, cn = (hc + Cfg::CH) % Cfg::BN;
           pre = epi.preload(tm * Cfg::BM_U + hn * Cfg::BM + q * 32, n_row0 + cn);
@@ -594,36 +488,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
-          if (f.kind == 2) {
-            bulk_store_1d(reinterpret_cast<uint8_t*>(geo.sk_partial) +
-                              ((static_cast<size_t>(blockIdx.x) * 4 + q) * kChunks + chunk) * 4096,
-                          sb, 4096);
-          } else {
-            for (int i = 0; i < nops; ++i) {
-              const CUtensorMap* m = ops[i].which ? &tmO1 : &tmO0;
-              if (ops[i].rank == 2)
-                tma_store_2d(m, sb + ops[i].soff, ops[i].x, ops[i].y);
-              else
-                tma_store_3d(m, sb + ops[i].soff, ops[i].x, ops[i].y, ops[i].z);
-            }
+          for (int i = 0; i < nops; ++i) {
+            const CUtensorMap* m = ops[i].which ? &tmO1 : &tmO0;
+            if (ops[i].rank == 2)
+              tma_store_2d(m, sb + ops[i].soff, ops[i].x, ops[i].y);
+            else
+              tma_store_3d(m, sb + ops[i].soff, ops[i].x, ops[i].y, ops[i].z);
           }
           bulk_commit_group();
         }
-      }
-      if (f.kind == 2) {
-        // partial written and visible before the flag goes up
-        if (lane == 0) {
-          bulk_wait_group<0>();
-          fence_proxy_async_global();
-          __threadfence();
-        }
-        named_barrier(1, 128);
-        if (q == 0 && lane == 0) st_release_gpu(geo.sk_flag + blockIdx.x, 1);
-      } else if (f.kind == 1) {
-        // every epilogue warp has read the partials: clear the flags for the next call
-        named_barrier(1, 128);
-        if (q == 0 && lane == 0)
-          for (int cc = blockIdx.x + 1; cc <= f.c_last; ++cc) geo.sk_flag[cc] = 0;
       }
     }
     // every store has read its staging buffer (the writes themselves complete with the grid)
@@ -696,6 +569,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
 
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) atomicOr(err_word, kErrTimeout);
+  if (threadIdx.x == 0) stamp(geo.stamps, geo.stamp_k, kStampEnd);
   if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);

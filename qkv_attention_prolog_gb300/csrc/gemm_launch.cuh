@@ -22,7 +22,7 @@ cudaError_t launch_gemm_t(const GemmLaunch& L, const Epi& epi) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = L.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, L.a0, L.a1, L.b0, L.b1, L.o0, L.o1, L.pm, L.geo, epi, L.err);
+  return cudaLaunchKernelEx(&cfg, kern, L.a0, L.a1, L.b0, L.b1, L.o0, L.o1, L.geo, epi, L.err);
 }
 
 }  // namespace mlap

@@ -8,6 +8,7 @@
 
 #include "gemm.cuh"
 #include "epilogues.cuh"
+#include "stamps.cuh"
 
 namespace mlap {
 
@@ -16,7 +17,6 @@ namespace mlap {
 struct GemmLaunch {
   CUtensorMap a0, a1, b0, b1;   // operand maps (first / second segment)
   CUtensorMap o0, o1;           // output maps for the epilogue's TMA stores
-  CUtensorMap pm;               // stream-K partial slots (fp32 [grid*128][BN])
   GemmGeometry geo;
   int bn;
   int mt;            // 128-row tiles of A per unit (decode orientation: 1 or 2)
@@ -44,6 +44,7 @@ struct UpAbsorbParams {
   const float* dqw;             // int8 weight: dequant_scale_w_uq_qr (N*(D+Dr))
   int32_t k;                    // W^QR blocks of 32 rows kept by each head CTA (0, 1 or 2)
   int32_t R;                    // CTAs after the N head CTAs that take the other W^QR blocks
+  uint64_t* stamps;             // optional execution stamps (stamps.cuh), slot MLAP_STAMP_UP
 };
 // One CTA whose bounded mbarrier wait runs out (nothing completes the barrier) and latches
 // kErrTimeout in err_word (selftest.cu).
@@ -84,6 +85,7 @@ struct FinalizeParams {
   const float* dsx;            // full quant: h *= dsx[t] * (dsw_q | dsw_kv)[column] (null: none)
   const float* dsw_q;
   const float* dsw_kv;
+  uint64_t* stamps;            // optional execution stamps (stamps.cuh), slot MLAP_STAMP_NORM
 };
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl);
 
@@ -139,6 +141,7 @@ struct QkvParams {
   float eps;
   int32_t bf16;                // element type of qkv: 0 fp16, 1 bf16
   uint32_t* err;
+  uint64_t* stamps;            // optional execution stamps (stamps.cuh), slot MLAP_STAMP_QKV
 };
 cudaError_t launch_qkv_rnrc(const QkvParams& p, cudaStream_t stream, int sm_count);
 

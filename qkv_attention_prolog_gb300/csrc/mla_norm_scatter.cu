@@ -93,8 +93,17 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   const bool do_kv = !PARTS || (blockIdx.x & 1) == 1;
   const int c0 = do_q ? 0 : p.Hcq;                 // this CTA's columns [c0, c1) of Ntot
   const int c1 = do_kv ? p.Ntot : p.Hcq;
+  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampStart);
   grid_launch_dependents();
   grid_dependency_wait();
+  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampDep);
+  // the CTA's last stamp, at each of its (CTA-uniform) exits
+  auto finish = [&]() {
+    if (p.stamps != nullptr) {
+      __syncthreads();
+      if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampEnd);
+    }
+  };
 
   // h = sum of the K-split partials, in split order.
   const size_t split_stride = static_cast<size_t>(p.T) * p.Ntot;
@@ -131,6 +140,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     }
   }
   __syncthreads();
+  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampMain);
   if (p.dsx != nullptr) {   // full quant: dequant the exact integer products per token and column
     const float sx = p.dsx[t];
     for (int c = c0 + threadIdx.x; c < c1; c += NT)
@@ -179,10 +189,14 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     if (threadIdx.x == 0) p.scale_t[t] = scale;
   }
 
-  if (!do_kv || p.slots <= 0) return;       // empty caches: outputs only
+  if (!do_kv || p.slots <= 0) {             // empty caches: outputs only
+    finish();
+    return;
+  }
   const int64_t idx = p.cache_index[t];
   if (idx < 0 || idx >= p.slots) {
     if (idx != -1 && threadIdx.x == 0) atomicOr(p.err, kErrIndexRange);
+    finish();
     return;
   }
   // ---- c^KV (Hckv % 8 == 0)
@@ -215,6 +229,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     else
       static_cast<__nv_bfloat16*>(p.kr_cache)[idx * p.Dr + j] = __float2bfloat16_rn(v);
   }
+  finish();
 }
 
 // dst[b][i][k] = src[b][k][perm(i)], 32x32 tiles through shared memory.

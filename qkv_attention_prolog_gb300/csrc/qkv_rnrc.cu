@@ -11,7 +11,12 @@
 //   optional qBeforeQuant / kBeforeQuant / vBeforeQuant: the tensors entering Quant, dense per
 //             token (the API function's optional outputs)
 //
-// A pure HBM stream: every token's qkv row is read once and its outputs written once.
+// A pure HBM stream: every token's qkv row is read once and its outputs written once.  What
+// bounds it is how many bytes each SM keeps in flight, so every warp streams tokens on its own:
+// one persistent CTA per SM holds one shared-memory slot per warp (the token's qkv row and its
+// cos / sin rows), and a warp requests its next token with 1-D bulk copies as soon as it has read
+// the current one out of its slot.  No CTA-wide barrier sits in the token loop, so a slow warp
+// never holds the others, and with 16 warps about 200 KB of loads are in flight per SM.
 #include "internal.h"
 
 namespace mlap {
@@ -19,6 +24,8 @@ namespace mlap {
 namespace {
 
 constexpr int kD = 128;
+constexpr int kMaxWarps = 16;
+constexpr int kSmemBudget = 227 * 1024;
 
 template <bool BF16>
 struct Elem;
@@ -78,100 +85,113 @@ __device__ __forceinline__ uint2 quant8_mul(const float (&x)[8], const float* in
   return out;
 }
 
-// Tokens stream through a ring of kRing shared-memory buffers: one thread requests each token's
-// qkv row ((Nq+Nk+Nv) * D elements, contiguous) and its cos / sin rows with 1-D bulk copies,
-// kRing tokens ahead, so a CTA keeps ~50 KB of loads in flight independent of its registers.
-// Eight lanes own one head row: lane l holds elements 8l..8l+7 and 64+8l..64+8l+7, i.e. both
-// members of its RoPE pairs, so the rotation needs no exchange and the RmsNorm sum is a 3-step
-// shuffle.  The CTA has 8 * ceil(N/2) threads (N = Nq+Nk+Nv heads): every 8-lane slot processes
-// two rows of each token.  Quantisation multiplies by the reciprocal of the per-channel scale
-// (fp32); the reciprocals (and asymmetric offsets) of all k and v heads sit in shared memory
-// behind the ring.  QM: 0 no quant, 1 symmetric, 2 asymmetric.
-constexpr int kRing = 4;
-
+// Shared memory: the per-channel reciprocal quant scales of all k and v heads (and the
+// asymmetric offsets), then one slot per warp: the token's qkv row ((Nq+Nk+Nv) * D elements,
+// contiguous), its cos row and its sin row.  Inside a warp eight lanes own one head row: lane l
+// holds elements 8l..8l+7 and 64+8l..64+8l+7, both members of its RoPE pairs, so the rotation
+// needs no exchange and the RmsNorm sum is a 3-step shuffle; the warp covers four rows per step.
+// QM: 0 no quant, 1 symmetric, 2 asymmetric.
 template <bool BF16, int QM>
-__global__ void __launch_bounds__(512) qkv_rnrc_kernel(const QkvParams p) {
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) qkv_rnrc_kernel(const QkvParams p) {
   constexpr bool QUANT = QM != 0;
   constexpr bool ASYM = QM == 2;
   using E = Elem<BF16>;
   using T = typename E::T;
   extern __shared__ __align__(128) uint8_t qsm[];
-  __shared__ uint64_t full[kRing];
+  __shared__ uint64_t full[kMaxWarps];
   __shared__ int abort_sh;
   const int Nh = p.Nq + p.Nk + p.Nv;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
   const uint32_t row_bytes = static_cast<uint32_t>(Nh) * kD * sizeof(T);
-  const uint32_t buf_bytes = row_bytes + 2 * kD * sizeof(T);     // qkv row, cos, sin
-  const int l8 = threadIdx.x & 7;
-  const int slot = threadIdx.x >> 3;
-  const int nslots = blockDim.x >> 3;
-  const unsigned mask = 0xffu << (threadIdx.x & 24);              // this slot's 8 lanes
+  const uint32_t slot_bytes = row_bytes + 2 * kD * sizeof(T);     // qkv row, cos, sin
+  const int l8 = lane & 7;
+  const int sub = lane >> 3;                                       // row of the warp's step
+  const unsigned mask = 0xffu << (lane & 24);                      // this row's 8 lanes
   const int ja = l8 * 8, jb = 64 + l8 * 8;                         // the two 8-element slices
+  const int nscale = QUANT ? (p.Nk + p.Nv) * kD : 0;
+  float* inv = reinterpret_cast<float*>(qsm);                      // reciprocal scales
+  float* offs = inv + nscale;                                      // asymmetric offsets
+  uint8_t* slots = qsm + static_cast<size_t>(nscale) * (ASYM ? 8 : 4);
+  uint8_t* slot = slots + static_cast<size_t>(warp) * slot_bytes;
 
+  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_QKV, kStampStart);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRing; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kMaxWarps; ++i) mbar_init(&full[i], 1);
     abort_sh = 0;
     fence_mbarrier_init();
   }
-  __syncthreads();
-  grid_launch_dependents();
-  grid_dependency_wait();
-
-  auto request = [&](int t, int s) {
-    uint8_t* b = qsm + static_cast<size_t>(s) * buf_bytes;
-    mbar_arrive_expect_tx(&full[s], buf_bytes);
-    bulk_load_1d(b, static_cast<const uint8_t*>(p.qkv) + static_cast<size_t>(t) * row_bytes,
-                 row_bytes, &full[s]);
-    bulk_load_1d(b + row_bytes,
-                 static_cast<const uint8_t*>(p.cos) + static_cast<size_t>(t) * kD * sizeof(T),
-                 kD * sizeof(T), &full[s]);
-    bulk_load_1d(b + row_bytes + kD * sizeof(T),
-                 static_cast<const uint8_t*>(p.sin) + static_cast<size_t>(t) * kD * sizeof(T),
-                 kD * sizeof(T), &full[s]);
-  };
-  if (threadIdx.x == 0)
-    for (int s = 0; s < kRing; ++s) {
-      const int t = blockIdx.x + s * gridDim.x;
-      if (t < p.T) request(t, s);
-    }
-
-  // per-lane gamma slices; reciprocal quant scales of all k and v heads in shared memory
+  // per-lane gamma slices and the quant scales do not depend on an earlier kernel
   float ga_q[8], gb_q[8], ga_k[8], gb_k[8];
   unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_q)[l8], ga_q);
   unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_q)[8 + l8], gb_q);
   unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_k)[l8], ga_k);
   unpack8<BF16>(reinterpret_cast<const uint4*>(p.gamma_k)[8 + l8], gb_k);
-  float* inv = reinterpret_cast<float*>(qsm + static_cast<size_t>(kRing) * buf_bytes);
-  float* offs = inv + (p.Nk + p.Nv) * kD;            // asymmetric offsets, same layout
   if (QUANT) {
-    for (int i = threadIdx.x; i < (p.Nk + p.Nv) * kD; i += blockDim.x) {
+    for (int i = threadIdx.x; i < nscale; i += blockDim.x) {
       inv[i] = __frcp_rn(i < p.Nk * kD ? p.k_scale[i] : p.v_scale[i - p.Nk * kD]);
       if (ASYM) offs[i] = i < p.Nk * kD ? p.k_offset[i] : p.v_offset[i - p.Nk * kD];
     }
-    __syncthreads();
   }
+  __syncthreads();
+  grid_launch_dependents();
+  grid_dependency_wait();
+  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_QKV, kStampDep);
 
-  for (int k = 0;; ++k) {
-    const int t = blockIdx.x + k * gridDim.x;
-    if (t >= p.T) break;
-    const int s = k % kRing;
-    if (!mbar_wait(&full[s], static_cast<uint32_t>((k / kRing) & 1), &abort_sh)) abort_sh = 1;
-    const uint8_t* b = qsm + static_cast<size_t>(s) * buf_bytes;
+  const int stride = gridDim.x * nwarps;                           // tokens per round
+  auto request = [&](int t) {
+    mbar_arrive_expect_tx(&full[warp], slot_bytes);
+    bulk_load_1d(slot, static_cast<const uint8_t*>(p.qkv) + static_cast<size_t>(t) * row_bytes,
+                 row_bytes, &full[warp]);
+    bulk_load_1d(slot + row_bytes,
+                 static_cast<const uint8_t*>(p.cos) + static_cast<size_t>(t) * kD * sizeof(T),
+                 kD * sizeof(T), &full[warp]);
+    bulk_load_1d(slot + row_bytes + kD * sizeof(T),
+                 static_cast<const uint8_t*>(p.sin) + static_cast<size_t>(t) * kD * sizeof(T),
+                 kD * sizeof(T), &full[warp]);
+  };
+  int t = blockIdx.x * nwarps + warp;
+  int fills = 0;                                                   // requests made on this slot
+  if (t < p.T && lane == 0) request(t);
+  if (t < p.T) fills = 1;
+
+  for (int k = 0; t < p.T; ++k, t += stride) {
+    // the slot holds token t once its k-th fill completes; a wait that gives up skips the
+    // token's stores (its cache slots stay untouched) and ends this warp's loop
+    // (every lane waits; the warp goes on only if all of them saw the fill complete)
+    const bool landed = mbar_wait(&full[warp], static_cast<uint32_t>(k & 1), &abort_sh);
+    if (!__all_sync(0xffffffffu, landed)) break;
     float ca[8], sa[8], cb[8], sb[8];
-    const uint4* cs = reinterpret_cast<const uint4*>(b + row_bytes);
-    const uint4* sn = reinterpret_cast<const uint4*>(b + row_bytes + kD * sizeof(T));
+    const uint4* cs = reinterpret_cast<const uint4*>(slot + row_bytes);
+    const uint4* sn = reinterpret_cast<const uint4*>(slot + row_bytes + kD * sizeof(T));
     unpack8<BF16>(cs[l8], ca);
     unpack8<BF16>(cs[8 + l8], cb);
     unpack8<BF16>(sn[l8], sa);
     unpack8<BF16>(sn[8 + l8], sb);
     const int64_t idx = p.index[t];
     const bool store = idx >= 0 && idx < p.slots;
-    if (threadIdx.x == 0 && idx != -1 && !store && p.slots > 0) atomicOr(p.err, kErrIndexRange);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int h = slot + r * nslots;
-      if (h >= Nh) break;                                          // uniform in the slot
-      const uint4* row = reinterpret_cast<const uint4*>(b + static_cast<size_t>(h) * kD * sizeof(T));
-      const uint4 rawa = row[l8], rawb = row[8 + l8];
+    if (lane == 0 && idx != -1 && !store && p.slots > 0) atomicOr(p.err, kErrIndexRange);
+    // read the whole row into registers step by step; the slot is free after the last step
+    const int steps = (Nh + 3) >> 2;
+    for (int st = 0; st < steps; ++st) {
+      const int h = st * 4 + sub;
+      uint4 rawa = make_uint4(0, 0, 0, 0), rawb = make_uint4(0, 0, 0, 0);
+      if (h < Nh) {
+        const uint4* row = reinterpret_cast<const uint4*>(slot + static_cast<size_t>(h) * kD * sizeof(T));
+        rawa = row[l8];
+        rawb = row[8 + l8];
+      }
+      if (st == steps - 1) {
+        // every lane has read its last piece of the slot: request the next token into it
+        __syncwarp();
+        const int tn = t + stride;
+        if (tn < p.T) {
+          if (lane == 0) request(tn);
+          ++fills;
+        }
+      }
+      if (h >= Nh) continue;                                       // uniform in the 8 lanes
       float xa[8], xb[8];
       unpack8<BF16>(rawa, xa);
       unpack8<BF16>(rawb, xb);
@@ -248,22 +268,19 @@ __global__ void __launch_bounds__(512) qkv_rnrc_kernel(const QkvParams p) {
         }
       }
     }
-    __syncthreads();                                  // buffer s fully read
-    if (abort_sh) break;                              // uniform after the barrier
-    if (threadIdx.x == 0) {
-      const int tn = t + kRing * gridDim.x;
-      if (tn < p.T) request(tn, s);
+  }
+  if (abort_sh && lane == 0 && fills > 0) {
+    // let this warp's last request land before the CTA exits (bounded): fill number fills - 1
+    // completes the phase of parity (fills - 1) & 1
+    const uint32_t par = static_cast<uint32_t>(fills - 1) & 1u;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&full[warp], par) && globaltimer_ns() - t0 < 20000000ull) {
     }
   }
-  if (abort_sh && threadIdx.x == 0) {
-    atomicOr(p.err, kErrTimeout);
-    // let requests already issued land before the CTA exits (bounded)
-    for (int s = 0; s < kRing; ++s) {
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&full[s], 0) && !mbar_try_wait(&full[s], 1) &&
-             globaltimer_ns() - t0 < 20000000ull) {
-      }
-    }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (abort_sh) atomicOr(p.err, kErrTimeout);
+    stamp(p.stamps, MLAP_STAMP_QKV, kStampEnd);
   }
 }
 
@@ -272,10 +289,19 @@ __global__ void __launch_bounds__(512) qkv_rnrc_kernel(const QkvParams p) {
 cudaError_t launch_qkv_rnrc(const QkvParams& p, cudaStream_t stream, int sm_count) {
   const int Nh = p.Nq + p.Nk + p.Nv;
   const size_t elem = 2;   // fp16 and bf16
-  const size_t buf = static_cast<size_t>(Nh) * kD * elem + 2 * kD * elem;
+  const size_t slot = static_cast<size_t>(Nh) * kD * elem + 2 * kD * elem;
   const int qm = p.k_scale == nullptr ? 0 : (p.k_offset == nullptr ? 1 : 2);
-  const size_t smem = kRing * buf + static_cast<size_t>(qm) * (p.Nk + p.Nv) * kD * 4;
-  if (smem > 200 * 1024) return cudaErrorNotSupported;
+  const size_t scales = static_cast<size_t>(p.Nk + p.Nv) * kD * (qm == 0 ? 0 : (qm == 1 ? 4 : 8));
+  if (scales + slot > static_cast<size_t>(kSmemBudget)) return cudaErrorNotSupported;
+  int warps = static_cast<int>((kSmemBudget - scales) / slot);
+  if (warps > kMaxWarps) warps = kMaxWarps;
+  // fewer tokens than warps: no idle warps
+  int64_t blocks = sm_count;
+  if (static_cast<int64_t>(blocks) * warps > p.T) {
+    blocks = (p.T + warps - 1) / warps;
+    if (blocks < 1) blocks = 1;
+  }
+  const size_t smem = scales + static_cast<size_t>(warps) * slot;
   auto pick = [&]() {
     if (p.bf16)
       return qm == 0 ? qkv_rnrc_kernel<true, 0> : (qm == 1 ? qkv_rnrc_kernel<true, 1>
@@ -287,17 +313,9 @@ cudaError_t launch_qkv_rnrc(const QkvParams& p, cudaStream_t stream, int sm_coun
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int threads = 8 * ((Nh + 1) / 2);          // 8 lanes per row, two rows per slot
-  if (threads > 512) return cudaErrorNotSupported;
-  int per_sm = 1;   // persistent grid: exactly the CTAs that fit at once
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
-  if (e != cudaSuccess) return e;
-  int64_t blocks = static_cast<int64_t>(sm_count) * (per_sm < 1 ? 1 : per_sm);
-  if (blocks > p.T) blocks = p.T;
-  if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(threads);
+  cfg.blockDim = dim3(static_cast<unsigned>(warps * 32));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

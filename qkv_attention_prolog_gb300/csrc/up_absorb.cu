@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   const int kb_up = (p.Hcq + kUaBK - 1) / kUaBK;
   const int nh = pl.head ? (p.Hckv + kUaWRows - 1) / kUaWRows : 0;   // absorb column chunks
   const int up_rows = (pl.head ? kD : 0) + 32 * pl.nrope;   // B rows of the up-projection
+  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_UP, kStampStart);
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmCq);
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     const int pre = kb_up < kUaStages ? kb_up : kUaStages;
     for (int i = 0; i < pre; ++i) issue_w(i, i);      // weights do not depend on earlier kernels
     grid_dependency_wait();
+    stamp(p.stamps, MLAP_STAMP_UP, kStampDep);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -411,6 +413,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     bool ok = mbar_wait(up_bar, 0, abort_flag);
     if (ok) {
       tc_fence_after_sync();
+      if (q == 0 && lane == 0) stamp(p.stamps, MLAP_STAMP_UP, kStampMain);
       int col = 0;
       if (pl.head) {
         // q^C: bf16 into the K-major, 128B-swizzled A operand (token t = row t)
@@ -496,6 +499,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) atomicOr(err_word, kErrTimeout);
+  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_UP, kStampEnd);
   if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, 512);

@@ -61,6 +61,10 @@ class MlaCase:
     # input RmsNormQuant (aclnnMlaPreprocessV2) ahead of the down-projection: None (off),
     # "channel" (deqScale per hidden channel) or "tensor" (one deqScale)
     x_norm: str | None = None
+    # "paired": rope_sin/rope_cos built from positions (columns j and j + Dr/2 share an angle);
+    # "independent": every table element drawn on its own from U(-1, 1), so no column repeats
+    # another and the elementwise use of the full-width tables is what is tested
+    table_mode: str = "paired"
 
 
 # The five workloads.  Sizes, distributions and cache layouts follow the stated workload recipe.
@@ -114,6 +118,7 @@ class QkvCase:
     before_quant: bool = False # request the optional qBeforeQuant / kBeforeQuant / vBeforeQuant
     skip_frac: float = 0.01
     eps: float = 1e-6
+    table_mode: str = "paired"  # as MlaCase.table_mode
 
 
 QKV_EPILOGUE = QkvCase("qkv_rnrc_fp16_16x1024", QkvDims(B=16, S=1024, Nq=32, Nk=8, Nv=8),
@@ -240,6 +245,9 @@ def make_mla_inputs(case: MlaCase) -> dict:
         inp["rms_norm_quant_deq_scale"] = _uniform(g, (d.He if case.x_norm == "channel" else 1,),
                                                    0.5, 2.0)
         inp["rms_norm_quant_epsilon"] = case.eps
+    if case.table_mode == "independent":   # drawn last, like the RmsNormQuant parameters
+        inp["rope_sin"] = _uniform(g, (T, d.Dr), -1.0, 1.0, bf16)
+        inp["rope_cos"] = _uniform(g, (T, d.Dr), -1.0, 1.0, bf16)
     return inp
 
 
@@ -275,6 +283,9 @@ def make_qkv_inputs(case: QkvCase) -> dict:
         inp["k_cache"] = torch.randn(d.block_num, d.block_size, d.Nk, d.D, generator=g).to(f16)
         inp["v_cache"] = torch.randn(d.block_num, d.block_size, d.Nv, d.D, generator=g).to(f16)
     inp["epsilon"] = case.eps
+    if case.table_mode == "independent":   # drawn last: the other inputs stay as in "paired"
+        inp["sin"] = _uniform(g, (T, d.D), -1.0, 1.0, f16)
+        inp["cos"] = _uniform(g, (T, d.D), -1.0, 1.0, f16)
     return inp
 
 

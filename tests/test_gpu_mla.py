@@ -1,4 +1,6 @@
 """GPU parity of the MLA prolog (CUDA path through the C ABI) against the fp64 oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -50,7 +52,7 @@ SHAPES = [
     dict(B=2, S=65, He=512, Hcq=256, N=3),            # T=130: BN 256, ragged rope tail (N*Dr)
     dict(B=3, S=100, He=384, Hcq=192, Hckv=128, N=2),  # T=300: prefill orientation, ragged M
     dict(B=1, S=200, He=320, Hcq=136, Hckv=96, N=2, Dr=32),  # ragged K, Hcq, Hckv tiles
-    dict(B=40, S=1, He=256, Hcq=1536, N=16),         # stream-K up-projection, tiles cut ~7 ways
+    dict(B=40, S=1, He=256, Hcq=1536, N=16),         # 16 heads, deep K (fused decode kernel)
 ]
 
 
@@ -181,20 +183,6 @@ def test_partial_quant_shapes(kw):
     _full_check(case)
 
 
-@pytest.mark.parametrize("case", ["decode", "cut7", "pq"])
-def test_stream_k_schedule(case, monkeypatch):
-    # the opt-in stream-K schedule of the decode up-projection (tiles cut across CTAs, partials
-    # fixed up by the owning CTA) gives the same results as the oracle
-    monkeypatch.setenv("MLAP_STREAM_K", "1")
-    if case == "decode":
-        _full_check(synthetic.MLA_DECODE)
-    elif case == "pq":
-        _full_check(synthetic.MLA_PARTIAL_QUANT)
-    else:
-        _full_check(synthetic.small_mla_case("cut7", B=40, S=1, He=256, Hcq=1536, N=16,
-                                             block_num=2, n_skip=1))
-
-
 def test_full_quant_int8_cache():
     # int8 token_x / W^DQ / W^DKV|W^KR (per-token, per-channel dequant), int8 kv_cache, bf16
     # kr_cache, int8 query per token and head with dequant_scale_q_nope
@@ -286,3 +274,30 @@ def test_fused_up_absorb_shapes(kw):
     block_num = max(1, (kw["B"] * kw["S"] + 127) // 128 + 1)
     case = synthetic.small_mla_case("fused", block_num=block_num, n_skip=1, **kw)
     _full_check(case, bsh=kw["S"] > 1)
+
+
+# ---- the full-width RoPE tables are used elementwise (aclnnQkvRmsNormRopeCache "Formulas" (3)):
+# every table element drawn on its own, so cos[t, j] != cos[t, j + Dr/2]; a kernel that read
+# only one half of a row, or paired the wrong columns, fails here
+
+def test_rope_tables_independent_decode_fused():
+    # the decode workload: fused up-projection/absorb (query_rope) and the norm kernel (kr_cache)
+    _full_check(dataclasses.replace(synthetic.MLA_DECODE, table_mode="independent", seed=2001))
+
+
+def test_rope_tables_independent_separate_kernels():
+    # N = 3 heads: the up-projection and absorb run as separate GEMMs (row-range decode schedule)
+    _full_check(synthetic.small_mla_case("tables_sep", B=9, S=1, He=256, Hcq=128, N=3,
+                                         block_num=2, n_skip=1, table_mode="independent"))
+
+
+def test_rope_tables_independent_prefill_orientation():
+    # T = 300 tokens: tokens as MMA rows with TMA-staged stores (prefill orientation)
+    _full_check(synthetic.small_mla_case("tables_pf", B=3, S=100, He=384, Hcq=192, Hckv=128,
+                                         N=2, block_num=4, n_skip=1, table_mode="independent"))
+
+
+def test_rope_tables_independent_int8():
+    # partial quant with int8 caches through the fused int8 kernel
+    _full_check(dataclasses.replace(synthetic.MLA_PARTIAL_QUANT, table_mode="independent",
+                                    seed=2002))

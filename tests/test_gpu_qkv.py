@@ -1,4 +1,6 @@
 """GPU parity of QkvRmsNormRopeCache (CUDA path through the C ABI) against the fp64 oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -149,3 +151,17 @@ def test_qkv_before_quant_without_quant():
                                                            block_num=2), seed=78,
                              quant="none", before_quant=True)
     _check(case)
+
+
+# every cos/sin element drawn on its own (no column repeats its partner j +- D/2): the
+# half-and-half rule of "Formulas" (3) is applied with the tables elementwise
+def test_qkv_rope_tables_independent_full_workload():
+    _check(dataclasses.replace(synthetic.QKV_EPILOGUE, table_mode="independent", seed=2003))
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_qkv_rope_tables_independent_small(dtype):
+    case = synthetic.QkvCase("tables", synthetic.QkvDims(B=2, S=37, Nq=4, Nk=2, Nv=2,
+                                                         block_num=2), seed=79,
+                             quant="asymmetric", before_quant=True, table_mode="independent")
+    _check(case, dtype)

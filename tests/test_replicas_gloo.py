@@ -68,3 +68,34 @@ def test_two_gloo_replicas():
     for shard, qpart in res[0][2]:
         merged[shard] = qpart
     np.testing.assert_array_equal(merged, full)
+
+
+@pytest.mark.timeout(300)
+def test_bench_gpus_flag_spawns_replicas():
+    # `bench.py --gpus 2` without a launcher starts the two replicas itself (spawned processes
+    # meeting over gloo on 127.0.0.1); the reference arm runs on rank 0 and reports both ranks
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--gpus", "2", "--steps", "1", "--warmup", "0", "--workload", "tiny"],
+                         capture_output=True, text=True, timeout=280, env=env, cwd=root)
+    assert res.returncode == 0, res.stderr[-3000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+
+
+def test_bench_rejects_world_size_mismatch():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--gpus", "2", "--steps", "1"], capture_output=True, text=True,
+                         timeout=120, env=env, cwd=root)
+    assert res.returncode != 0 and "WORLD_SIZE" in (res.stderr + res.stdout)

@@ -47,15 +47,32 @@ def _fresh_outputs(t, cpu, dev):
     return u
 
 
-def test_no_alloc_matches_workspace_entry_point_twice():
+def _decode_T300():
+    # decode dimensions with 300 tokens: one K split and the tokens-as-rows GEMMs, so the
+    # partials, c^Q, q^C and scale regions of the scratch sit at other offsets than at T = 128
+    return dataclasses.replace(synthetic.MLA_DECODE, name="decode_T300",
+                               dims=dataclasses.replace(synthetic.MLA_DECODE.dims, B=300))
+
+
+CASES = {
+    "decode_T128": lambda: synthetic.MLA_DECODE,
+    "partial_quant_int8_caches_T64": lambda: synthetic.MLA_PARTIAL_QUANT,
+    "decode_T300": _decode_T300,
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_no_alloc_matches_workspace_entry_point_twice(name):
     dev = torch.device("cuda")
-    case_a = synthetic.MLA_DECODE
-    case_b = dataclasses.replace(synthetic.MLA_DECODE, seed=4242, n_skip=3)
+    case_a = CASES[name]()
+    case_b = dataclasses.replace(case_a, seed=case_a.seed + 4242, n_skip=3)
     for case in (case_a, case_b):          # two calls in a row, different inputs
         cpu, t = _tensors(case, dev)
         ref = _fresh_outputs(t, cpu, dev)
         a_ref = pkg.make_mla_args(ref, case.eps, case.eps)
-        ws = torch.empty(pkg.mlap_get_workspace_size(a_ref), dtype=torch.uint8, device=dev)
+        need = pkg.mlap_get_workspace_size(a_ref)
+        assert need <= 24 * 1024 * 1024, "case must fit the static scratch"
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
         pkg.mlap_workspace_init(ws)
         pkg.mlap_execute(a_ref, ws)
 
