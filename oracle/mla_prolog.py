@@ -115,6 +115,41 @@ def quant_per_token_head(q_n: np.ndarray):
     return codes, scale
 
 
+def up_projection_int8(codes, scale_t, weight_uq_qr, dequant_scale_w_uq_qr) -> np.ndarray:
+    """c^Q · [W^UQ | W^QR] in partial / full quant: the int8 codes times the int8 weight,
+    accumulated exactly, dequantised by scale_t[t] * dequant_scale_w_uq_qr[column] (MlaPrologV2
+    README, 参数说明 dequant_scale_w_uq_qr; reading stated in the module docstring)."""
+    acc = np.asarray(codes).astype(np.int64) @ np.asarray(weight_uq_qr).astype(np.int64)
+    return (acc.astype(np.float64) * np.asarray(scale_t, np.float64).reshape(-1, 1)
+            * np.asarray(dequant_scale_w_uq_qr, np.float64).reshape(1, -1))
+
+
+def query_outputs(u, weight_uk, rope_cos, rope_sin, Dr: int, query_int8: bool = False):
+    """From u = c^Q · [W^UQ | W^QR] (T, N*(D+Dr)), columns per head [D nope | Dr rope]: q^C =
+    bf16(nope part) (input of the W^UK matmul), q^N = q^C · W^UK per head, query = bf16(q^N) (or
+    the int8 "pertoken_head" query and its scales), query_rope = bf16(ROPE(rope part))
+    (MlaPrologV2 README, 功能说明 q^C, q^N and q^R formulas).  Returns (query, query_rope,
+    dequant_scale_q_nope or None)."""
+    w_uk = np.asarray(weight_uk, np.float64)
+    N, D, Hckv = w_uk.shape
+    u = np.asarray(u, np.float64).reshape(-1, N, D + Dr)
+    T = u.shape[0]
+    cos = np.asarray(rope_cos, np.float64).reshape(T, 1, Dr)
+    sin = np.asarray(rope_sin, np.float64).reshape(T, 1, Dr)
+    q_c = round_bf16(u[:, :, :D])                  # q^C, input of the W^UK matmul
+    q_r = u[:, :, D:]                              # c^Q · W^QR, before ROPE
+    q_n = np.empty((T, N, Hckv), np.float64)
+    for n in range(N):                             # q^N = q^C · W^UK, per head
+        q_n[:, n, :] = q_c[:, n, :] @ w_uk[n]
+    scale_q = None
+    if query_int8:
+        query, scale_q = quant_per_token_head(q_n)
+    else:
+        query = round_bf16(q_n)
+    query_rope = round_bf16(rope_half_and_half(q_r, cos, sin))
+    return query, query_rope, scale_q
+
+
 def scatter_rows(cache: np.ndarray, rows: np.ndarray, cache_index: np.ndarray) -> np.ndarray:
     """Copy of ``cache`` (BlockNum, BlockSize, 1, H) with row t stored at slot cache_index[t]
     (MlaPrologV2 README k^C = Cache(c^KV), k^R = Cache(...); "-1 skips" from
@@ -170,30 +205,17 @@ def mla_prolog(token_x, weight_dq, weight_uq_qr, weight_uk, weight_dkv_kr,
 
     # Query path: c^Q = RmsNorm(x · W^DQ), rounded to bf16 as the next matmul's input.
     h_q = down(weight_dq, dequant_scale_w_dq)
-    c_q = round_bf16(rms_norm(h_q, rmsnorm_gamma_cq, rmsnorm_epsilon_cq))
+    c_q_exact = rms_norm(h_q, rmsnorm_gamma_cq, rmsnorm_epsilon_cq)
+    c_q = round_bf16(c_q_exact)
 
     # c^Q · [W^UQ | W^QR]
+    codes = scale_t = None
     if np.asarray(weight_uq_qr).dtype == np.int8:
         codes, scale_t = dynamic_quant_per_token(c_q, smooth_scales_cq)
-        acc = codes.astype(np.int64) @ np.asarray(weight_uq_qr).astype(np.int64)   # exact
-        u = (acc.astype(np.float64) * scale_t.astype(np.float64)[:, None]
-             * np.asarray(dequant_scale_w_uq_qr, np.float64).reshape(1, -1))
+        u = up_projection_int8(codes, scale_t, weight_uq_qr, dequant_scale_w_uq_qr)
     else:
         u = c_q @ np.asarray(weight_uq_qr, np.float64)
-    u = u.reshape(T, N, D + Dr)
-    q_c = round_bf16(u[:, :, :D])                  # q^C, input of the W^UK matmul
-    q_r = u[:, :, D:]                              # c^Q · W^QR, before ROPE
-
-    w_uk = np.asarray(weight_uk, np.float64)
-    q_n = np.empty((T, N, Hckv), np.float64)
-    for n in range(N):                             # q^N = q^C · W^UK, per head
-        q_n[:, n, :] = q_c[:, n, :] @ w_uk[n]
-    scale_q = None
-    if query_int8:
-        query, scale_q = quant_per_token_head(q_n)
-    else:
-        query = round_bf16(q_n)
-    query_rope = round_bf16(rope_half_and_half(q_r, cos[:, None, :], sin[:, None, :]))
+    query, query_rope, scale_q = query_outputs(u, weight_uk, cos, sin, Dr, query_int8)
 
     # Key path: c^KV = RmsNorm(x · W^DKV), k^R = ROPE(x · W^KR)
     h_kvr = down(weight_dkv_kr, dequant_scale_w_dkv_kr)
@@ -216,7 +238,10 @@ def mla_prolog(token_x, weight_dq, weight_uq_qr, weight_uk, weight_dkv_kr,
         "kr_cache": scatter_rows(np.asarray(kr_cache), kr_rows, cache_index),
         "dequant_scale_q_nope": scale_q,
         # intermediates, exposed for tests only
+        "c_q_exact": c_q_exact,
         "c_q": c_q,
+        "c_q_codes": codes,
+        "c_q_scale": scale_t,
         "c_kv": c_kv,
         "k_r": k_r,
     }
