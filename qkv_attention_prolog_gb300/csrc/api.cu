@@ -503,6 +503,9 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   g.err = err;
   g.geo.stamps = stamps;
   g.geo.stamp_k = MLAP_STAMP_DOWN;
+  // token_x itself is the activation (not widened or normalised by a kernel of this call): the
+  // down-projection streams before the preceding kernel finishes and waits only to store
+  g.geo.act_ready = !(d.full || d.xnorm);
   g.swap = swap;
   g.mt = swap ? mt : 1;
   DownParams dp{0};

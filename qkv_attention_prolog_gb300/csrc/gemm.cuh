@@ -61,6 +61,10 @@ struct GemmGeometry {
   // Optional execution stamps (%globaltimer) of this launch, kernel slot stamp_k (stamps.cuh).
   uint64_t* stamps;
   int32_t stamp_k;
+  // 1: neither operand comes from an earlier kernel of the stream (both are inputs of the call),
+  // so loads and MMAs start at once and only the epilogue waits for the preceding kernel, before
+  // its first store (the preceding kernels may still read what it overwrites).
+  int32_t act_ready;
 };
 
 // One piece of work for a CTA: a tile and its k-block range.
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
   // for the previous kernel's results here; the producer first requests weight tiles.
   grid_launch_dependents();
   const bool producer = warp == 0 && lane == 0;
-  if (!producer) grid_dependency_wait();
+  if (!producer && !geo.act_ready) grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -344,8 +348,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
           for (int i = 0; i < pre; ++i) issue_weight(i, f0, f0.kb0 + i);
         }
       }
-      grid_dependency_wait();
-      stamp(geo.stamps, geo.stamp_k, kStampDep);
+      if (!geo.act_ready) {
+        grid_dependency_wait();
+        stamp(geo.stamps, geo.stamp_k, kStampDep);
+      }
 
       int stage = 0;
       uint32_t phase = 0;
@@ -433,6 +439,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
     uint8_t* wstage = smemE + q * 2 * Cfg::EPI_BUF;
+    if (geo.act_ready) {   // the stores wait for the preceding kernel
+      grid_dependency_wait();
+      if (q == 0 && lane == 0) stamp(geo.stamps, geo.stamp_k, kStampDep);
+    }
     int sel = 0;
     int iter = 0;
     Iter it(geo);

@@ -36,25 +36,54 @@ namespace {
 
 constexpr int kUaBK = 64;                              // K elements per stage
 constexpr int kUaA = 128 * kUaBK * 2;                  // c^Q tile: 128 tokens x 64 (16 KB)
-constexpr int kUaWRows = 192;                          // weight tile rows: D + Dr, W^UK chunks
+constexpr int kUaWRows = 192;                          // most weight rows of one stage
 constexpr int kUaB = kUaWRows * kUaBK * 2;             // 24 KB
 constexpr int kUaQc = 2 * 128 * kUaBK * 2;             // q^C operand: 128 tokens x D = 128
-constexpr int kUaBars = 512;
+constexpr int kUaBars = 1024;                          // barriers and flags, ahead of the stages
+constexpr int kUaSmemMax = 232448;                     // 227 KB opt-in per CTA
+constexpr int kUaMaxStages = 8;
 
-// STAGES operand stages (c^Q tile + bf16 weight tile); int8: RSTAGES raw weight tiles in a ring
-// of their own, filled by a second producer thread, so that more of the weight stream is in
-// flight than there are operand stages.
+// Shared memory (after 1024-B alignment): barriers, then the operand stages (c^Q tile + weight
+// tile).  bf16 weight: the stage holds exactly this CTA's weight rows (a head CTA 128 + 32k, a
+// rope CTA 32 per block), so a head CTA with one rope block fits six 36 KB stages where fixed
+// 40 KB stages fit four: more of the weight stream in flight, which is what the per-SM rate
+// depends on; q^C lives in the c^Q halves of stages 0 and 1 once the up-projection is done.
+// int8 weight: three 40 KB stages, RSTAGES raw weight tiles in a ring of their own (filled by a
+// second producer thread, so that more of the weight stream is in flight than there are
+// operand stages) and a separate q^C buffer.
 template <bool INT8>
 struct UaCfg {
   static constexpr int THREADS = INT8 ? 384 : 256;
-  static constexpr int STAGES = INT8 ? 3 : 4;   // bf16: 198 KB in all
   static constexpr int RSTAGES = INT8 ? 6 : 0;
   static constexpr int RAW = 192 * kUaBK;       // raw int8 weight tile (192 rows max)
-  static constexpr int STAGE = kUaA + kUaB;
-  static constexpr int SMEM = STAGES * STAGE + RSTAGES * RAW + kUaQc + kUaBars + 1024;
-  static_assert(STAGE % 1024 == 0 && RAW % 1024 == 0 && SMEM <= 232448, "shared memory layout");
+  static constexpr int I8_STAGES = 3;
+  static constexpr int SMEM = INT8 ? 1024 + kUaBars + I8_STAGES * (kUaA + kUaB) + RSTAGES * RAW + kUaQc
+                                   : kUaSmemMax;
+  static_assert(RAW % 1024 == 0 && SMEM <= kUaSmemMax, "shared memory layout");
 };
 constexpr uint32_t kUaUpCol = 256;                     // TMEM column of the up accumulator
+#ifdef MLAP_UA_TRACE   // pipeline timeline of one CTA into spare words of its stamps slot
+#define UA_TRACE(slot, i)                                                                         \
+  do {                                                                                            \
+    if (p.stamps != nullptr && (blockIdx.x == MLAP_UA_TRACE || blockIdx.x == MLAP_UA_TRACE2) &&  \
+        (i) < 40)                                                                                 \
+      p.stamps[MLAP_STAMP_UP * MLAP_STAMP_BLOCK + 700 + (blockIdx.x == MLAP_UA_TRACE ? 0 : 140) + \
+               (slot) * 40 + (i)] = globaltimer_ns();                                            \
+  } while (0)
+#else
+#define UA_TRACE(slot, i) \
+  do {                    \
+  } while (0)
+#endif
+// Weight k-blocks (after those prefetched into the pipeline stages) that each CTA asks L2 to
+// prefetch before it waits for the kernel ahead of it, and whether the head's W^UK follows: the
+// DRAM is otherwise idle while that kernel (the RmsNorm step) runs.
+#ifndef MLAP_UA_L2_KBLOCKS
+#define MLAP_UA_L2_KBLOCKS 0
+#endif
+#ifndef MLAP_UA_L2_UK
+#define MLAP_UA_L2_UK 0
+#endif
 constexpr int kD = 128;
 constexpr int kDr = 64;
 
@@ -120,31 +149,41 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmUk,   // W^UK rows, box 64 x 32
                      const UpAbsorbParams p, uint32_t* __restrict__ err_word) {
   using Cfg = UaCfg<INT8>;
-  constexpr int kUaStages = Cfg::STAGES;
-  constexpr int kUaStage = Cfg::STAGE;
+  constexpr int kRS = Cfg::RSTAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  constexpr int kRS = Cfg::RSTAGES;
-  uint8_t* ring_raw = smem + kUaStages * kUaStage;     // int8: raw weight tiles
-  uint8_t* qc = ring_raw + kRS * Cfg::RAW;             // q^C operand (two 64-wide K blocks)
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(qc + kUaQc);
-  uint64_t* empty_bar = full_bar + kUaStages;
-  uint64_t* rawf_bar = empty_bar + kUaStages;          // int8: raw weight tile landed
-  uint64_t* rawe_bar = rawf_bar + kRS;                 // int8: raw tile converted, slot free
-  uint64_t* up_bar = rawe_bar + (INT8 ? kRS : kUaStages);   // up accumulator complete
-  uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, up accumulator drained
-  uint64_t* ab_bar = qc_bar + 1;                       // absorb chunk h complete (h < 3)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 3);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const UaPlan pl = ua_plan(p);
   const int n = blockIdx.x;                            // head (head CTAs)
   const int kb_up = (p.Hcq + kUaBK - 1) / kUaBK;
-  const int nh = pl.head ? (p.Hckv + kUaWRows - 1) / kUaWRows : 0;   // absorb column chunks
   const int up_rows = (pl.head ? kD : 0) + 32 * pl.nrope;   // B rows of the up-projection
+  // weight rows one stage holds (also the W^UK chunk height of a head CTA), the stage size and
+  // the stage count
+  const int wrows = INT8 ? kUaWRows : up_rows;
+  const int kUaStage = kUaA + wrows * kUaBK * 2;
+  const int kUaStages =
+      INT8 ? Cfg::I8_STAGES
+           : ((kUaSmemMax - 1024 - kUaBars) / kUaStage < kUaMaxStages
+                  ? (kUaSmemMax - 1024 - kUaBars) / kUaStage : kUaMaxStages);
+  const int nh = pl.head ? (p.Hckv + wrows - 1) / wrows : 0;   // absorb column chunks (<= 4)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty_bar = full_bar + kUaMaxStages;
+  uint64_t* rawf_bar = empty_bar + kUaMaxStages;       // int8: raw weight tile landed
+  uint64_t* rawe_bar = rawf_bar + kUaMaxStages;        // int8: raw tile converted, slot free
+  uint64_t* up_bar = rawe_bar + kUaMaxStages;          // up accumulator complete
+  uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, up accumulator drained
+  uint64_t* ab_bar = qc_bar + 1;                       // absorb chunk h complete (h < 4)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* stages = smem + kUaBars;
+  uint8_t* ring_raw = stages + kUaStages * kUaStage;   // int8: raw weight tiles
+  // q^C operand, two 64-wide K blocks: int8, its own buffer; bf16, the c^Q halves of stages 0 and
+  // 1, free once the up-projection's MMAs have completed
+  uint8_t* qc0 = INT8 ? ring_raw + kRS * Cfg::RAW : stages;
+  uint8_t* qc1 = INT8 ? qc0 + kUaA : stages + kUaStage;
   if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_UP, kStampStart);
 
   if (warp == 0 && lane == 0) {
@@ -163,7 +202,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     }
     mbar_init(up_bar, 1);
     mbar_init(qc_bar, 4);
-    for (int h = 0; h < 3; ++h) mbar_init(&ab_bar[h], 1);
+    for (int h = 0; h < 4; ++h) mbar_init(&ab_bar[h], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -183,7 +222,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
 
   if (producer) {
     // ------------------------------------------------------------------ TMA producer
-    int fills[kUaStages] = {};
+    int fills[kUaMaxStages] = {};
     // head n's W^UQ rows (D), then this CTA's rope blocks: up to six 32-row boxes per tile,
     // their first weight rows computed once
     const int nbox = up_rows / 32;
@@ -195,7 +234,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     }
     auto issue_w = [&](int st, int kb) {
       if constexpr (!INT8) {   // (int8 weight tiles come from the raw producer)
-        uint8_t* b = smem + st * kUaStage + kUaA;
+        uint8_t* b = stages + st * kUaStage + kUaA;
         mbar_expect_tx(&full_bar[st], static_cast<uint32_t>(up_rows) * kUaBK * 2);
 #pragma unroll
         for (int j = 0; j < 6; ++j)
@@ -204,6 +243,17 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     };
     const int pre = kb_up < kUaStages ? kb_up : kUaStages;
     for (int i = 0; i < pre; ++i) issue_w(i, i);      // weights do not depend on earlier kernels
+    if constexpr (!INT8) {   // (int8 weight tiles: the raw producer prefetches them)
+      const int kl2 = pre + MLAP_UA_L2_KBLOCKS < kb_up ? pre + MLAP_UA_L2_KBLOCKS : kb_up;
+      for (int kb = pre; kb < kl2; ++kb)
+#pragma unroll
+        for (int j = 0; j < 6; ++j)
+          if (j < nbox) tma_prefetch_l2_2d(&tmW, kb * kUaBK, ybox[j]);
+    }
+    if (MLAP_UA_L2_UK && pl.head)
+      for (int r = 0; r < p.Hckv; r += 32)
+        for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2)
+          tma_prefetch_l2_2d(&tmUk, kb2 * kUaBK, n * p.Hckv + r);
     grid_dependency_wait();
     stamp(p.stamps, MLAP_STAMP_UP, kStampDep);
     int stage = 0;
@@ -217,27 +267,29 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         }
         issue_w(stage, kb);
       }
+      UA_TRACE(0, kb);
       mbar_arrive_expect_tx(&full_bar[stage], kUaA);
-      tma_load_2d(smem + stage * kUaStage, &tmCq, &full_bar[stage], kb * kUaBK, 0);
+      tma_load_2d(stages + stage * kUaStage, &tmCq, &full_bar[stage], kb * kUaBK, 0);
       ++fills[stage];
       if (++stage == kUaStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
-    // head n's W^UK rows, chunk h of 192 rows, K block kb2 of D
+    // head n's W^UK rows, chunk h of wrows rows, K block kb2 of D
     for (int h = 0; ok && h < nh; ++h) {
-      const int rows = p.Hckv - h * kUaWRows < kUaWRows ? p.Hckv - h * kUaWRows : kUaWRows;
+      const int rows = p.Hckv - h * wrows < wrows ? p.Hckv - h * wrows : wrows;
       for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2) {
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        uint8_t* b = smem + stage * kUaStage + kUaA;
+        uint8_t* b = stages + stage * kUaStage + kUaA;
+        UA_TRACE(0, kb_up + h * 2 + kb2);
         mbar_arrive_expect_tx(&full_bar[stage], rows * kUaBK * 2);
         for (int r = 0; r < rows; r += 32)
           tma_load_2d(b + r * 128, &tmUk, &full_bar[stage], kb2 * kUaBK,
-                      n * p.Hckv + h * kUaWRows + r);
+                      n * p.Hckv + h * wrows + r);
         ++fills[stage];
         if (++stage == kUaStages) {
           stage = 0;
@@ -270,6 +322,14 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     int rs = 0;
     uint32_t rph = 0;
     for (int kb = 0; kb < kb_up; ++kb) {
+      if (kb == kRS) {
+        // the ring is full: ask L2 for the next k-blocks while the converters catch up
+        const int kl2 = kRS + MLAP_UA_L2_KBLOCKS < kb_up ? kRS + MLAP_UA_L2_KBLOCKS : kb_up;
+        for (int k2 = kRS; k2 < kl2; ++k2)
+#pragma unroll
+          for (int j = 0; j < 6; ++j)
+            if (j < nbox) tma_prefetch_l2_2d(&tmW, k2 * kUaBK, ybox[j]);
+      }
       if (kb >= kRS && !mbar_wait(&rawe_bar[rs], rph ^ 1u, abort_flag)) break;
       uint8_t* r = ring_raw + rs * Cfg::RAW;
       mbar_arrive_expect_tx(&rawf_bar[rs], static_cast<uint32_t>(up_rows) * kUaBK);
@@ -303,8 +363,9 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
           ok = false;
           break;
         }
+        UA_TRACE(1, kb);
         tc_fence_after_sync();
-        const uint32_t a = smem_u32(smem + stage * kUaStage);
+        const uint32_t a = smem_u32(stages + stage * kUaStage);
         const uint32_t b = a + kUaA;
 #pragma unroll
         for (int kk = 0; kk < kUaBK / 16; ++kk)
@@ -318,23 +379,25 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       }
       if (ok) umma_commit(up_bar);
       if (ok && pl.head) ok = mbar_wait(qc_bar, 0, abort_flag);   // q^C staged, acc read
+      UA_TRACE(2, 0);
       if (ok && pl.head) {
         tc_fence_after_sync();
-        const uint32_t qa = smem_u32(qc);
+        const uint32_t qa[2] = {smem_u32(qc0), smem_u32(qc1)};
         for (int h = 0; ok && h < nh; ++h) {
-          const int rows = p.Hckv - h * kUaWRows < kUaWRows ? p.Hckv - h * kUaWRows : kUaWRows;
+          const int rows = p.Hckv - h * wrows < wrows ? p.Hckv - h * wrows : wrows;
           const uint32_t idesc_ab = idesc_bf16_f32(128, rows);
           for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2) {
             if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
               ok = false;
               break;
             }
+            UA_TRACE(1, kb_up + h * 2 + kb2);
             tc_fence_after_sync();
-            const uint32_t b = smem_u32(smem + stage * kUaStage) + kUaA;
+            const uint32_t b = smem_u32(stages + stage * kUaStage) + kUaA;
 #pragma unroll
             for (int kk = 0; kk < kUaBK / 16; ++kk)
-              umma_bf16_ss(tmem_base + static_cast<uint32_t>(h * kUaWRows),
-                           sdesc_kmajor_sw128(qa + kb2 * (128 * kUaBK * 2) + kk * 32),
+              umma_bf16_ss(tmem_base + static_cast<uint32_t>(h * wrows),
+                           sdesc_kmajor_sw128(qa[kb2] + kk * 32),
                            sdesc_kmajor_sw128(b + kk * 32), idesc_ab,
                            (kb2 > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&empty_bar[stage]);
@@ -361,7 +424,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         break;
       }
       const uint8_t* raw = ring_raw + rs * Cfg::RAW;
-      uint8_t* dst = smem + stage * kUaStage + kUaA;
+      uint8_t* dst = stages + stage * kUaStage + kUaA;
       for (int r = ct; r < up_rows; r += 128) convert_int8_row(raw + r * kUaBK, dst, r);
       fence_proxy_async_shared();                      // generic writes -> the tensor core
       __syncwarp();
@@ -426,7 +489,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = v[j] * st * __ldg(dq + j);
           }
-          uint8_t* row = qc + (col / kUaBK) * (128 * kUaBK * 2) + t * 128;
+          uint8_t* row = (col < kUaBK ? qc0 : qc1) + t * 128;
           const int ch0 = (col % kUaBK) / 8;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -477,21 +540,51 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       }
     }
     if (ok && pl.head) {
-      __nv_bfloat16* out = p.q_out + (static_cast<size_t>(t) * p.N + n) * p.Hckv;
-      for (int h = 0; h < nh; ++h) {
-        if (!mbar_wait(&ab_bar[h], 0, abort_flag)) break;
-        tc_fence_after_sync();
-        const int c1 = p.Hckv < (h + 1) * kUaWRows ? p.Hckv : (h + 1) * kUaWRows;
+      // query in groups of 64 columns: each lane (token) packs its 64 values into a 128-B row
+      // of the warp's 4 KB staging tile (a c^Q half of a stage, free after the up-projection;
+      // 16-B chunks XOR-swizzled by row), then eight lanes store each row as one 128-B line, four
+      // rows per instruction, instead of 32 scattered 16-B pieces
+      uint8_t* tile = stages + (INT8 ? (q >> 1) : 2 + (q >> 1)) * kUaStage + (q & 1) * 4096;
+      const int rsub = lane >> 3, ch = lane & 7;        // read-back: row rsub + 4i, chunk ch
+      int waited = 0;                                   // absorb chunks known complete
 #pragma unroll 1
-        for (int c = h * kUaWRows; c < c1; c += 32) {
-          float v[32];
-          tmem_ld32(lane_base + static_cast<uint32_t>(c), v);
-          if (live) {
-            uint4* d = reinterpret_cast<uint4*>(out + c);
+      for (int c = 0; ok && c < p.Hckv; c += 64) {
+        const int w = p.Hckv - c < 64 ? p.Hckv - c : 64;   // 64, or 32 for the last group
+        const int need = (c + w - 1) / wrows + 1;          // chunks holding columns c..c+w-1
+        while (waited < need) {
+          if (!mbar_wait(&ab_bar[waited], 0, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (q == 0 && lane == 0) UA_TRACE(2, 1 + waited);
+          ++waited;
+        }
+        if (!ok) break;
+        tc_fence_after_sync();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) d[j] = pack8(v + 8 * j);
+        for (int g = 0; g < 2; ++g) {
+          if (g * 32 >= w) break;
+          float v[32];
+          tmem_ld32(lane_base + static_cast<uint32_t>(c + 32 * g), v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(tile + lane * 128 + ((((4 * g + j) ^ (lane & 7)) & 7) << 4)) =
+                pack8(v + 8 * j);
+        }
+        __syncwarp();
+        if (ch * 8 < w) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = rsub + 4 * i;                 // token q*32 + r
+            const int tr = q * 32 + r;
+            const uint4 val =
+                *reinterpret_cast<const uint4*>(tile + r * 128 + (((ch ^ (r & 7)) & 7) << 4));
+            if (tr < p.T)
+              *reinterpret_cast<uint4*>(p.q_out + (static_cast<size_t>(tr) * p.N + n) * p.Hckv +
+                                        c + ch * 8) = val;
           }
         }
+        __syncwarp();                                   // the tile is read before it is rewritten
       }
     }
   }
