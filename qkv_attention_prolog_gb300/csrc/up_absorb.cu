@@ -78,6 +78,10 @@ constexpr uint32_t kUaUpCol = 256;                     // TMEM column of the up 
 // Weight k-blocks (after those prefetched into the pipeline stages) that each CTA asks L2 to
 // prefetch before it waits for the kernel ahead of it, and whether the head's W^UK follows: the
 // DRAM is otherwise idle while that kernel (the RmsNorm step) runs.
+// Operand stages whose weight tiles are requested before the wait on the preceding kernel.
+#ifndef MLAP_UA_PRE_STAGES
+#define MLAP_UA_PRE_STAGES 4
+#endif
 #ifndef MLAP_UA_L2_KBLOCKS
 #define MLAP_UA_L2_KBLOCKS 0
 #endif
@@ -241,7 +245,8 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
           if (j < nbox) tma_load_2d(b + j * 4096, &tmW, &full_bar[st], kb * kUaBK, ybox[j]);
       }
     };
-    const int pre = kb_up < kUaStages ? kb_up : kUaStages;
+    int pre = kb_up < kUaStages ? kb_up : kUaStages;
+    if (pre > MLAP_UA_PRE_STAGES) pre = MLAP_UA_PRE_STAGES;
     for (int i = 0; i < pre; ++i) issue_w(i, i);      // weights do not depend on earlier kernels
     if constexpr (!INT8) {   // (int8 weight tiles: the raw producer prefetches them)
       const int kl2 = pre + MLAP_UA_L2_KBLOCKS < kb_up ? pre + MLAP_UA_L2_KBLOCKS : kb_up;
