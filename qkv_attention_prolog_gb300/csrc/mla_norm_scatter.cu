@@ -95,6 +95,25 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   const int c1 = do_kv ? p.Ntot : p.Hcq;
   if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampStart);
   grid_launch_dependents();
+  // Decode (PARTS): the call's inputs this thread needs after the reduction (its gamma slice,
+  // the token's RoPE tables and cache index) are read before the wait on the down-projection,
+  // so the latency chain after it holds only the partials
+  uint4 g_pre = make_uint4(0, 0, 0, 0);
+  __nv_bfloat16 cos_pre = __float2bfloat16(0.f), sin_pre = __float2bfloat16(0.f);
+  int64_t idx_pre = -1;
+  if constexpr (PARTS) {
+    if (do_q && p.Hcq <= NT * 8 && threadIdx.x * 8 < p.Hcq)
+      g_pre = __ldg(reinterpret_cast<const uint4*>(p.gamma_cq) + threadIdx.x);
+    if (do_kv) {
+      if (p.Hckv <= NT * 8 && threadIdx.x * 8 < p.Hckv)
+        g_pre = __ldg(reinterpret_cast<const uint4*>(p.gamma_ckv) + threadIdx.x);
+      if (threadIdx.x < p.Dr) {
+        cos_pre = p.cos[static_cast<size_t>(t) * p.Dr + threadIdx.x];
+        sin_pre = p.sin[static_cast<size_t>(t) * p.Dr + threadIdx.x];
+      }
+      if (p.slots > 0) idx_pre = p.cache_index[t];
+    }
+  }
   grid_dependency_wait();
   if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampDep);
   // the CTA's last stamp, at each of its (CTA-uniform) exits
@@ -166,7 +185,13 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   } else if (p.smooth == nullptr) {
     for (int f = threadIdx.x * 8; f < p.Hcq; f += NT * 8) {
       float g[8], v[8];
-      load8_bf16(p.gamma_cq + f, g);
+      if (PARTS && p.Hcq <= NT * 8) {
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&g_pre);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g[i] = __bfloat162float(e[i]);
+      } else {
+        load8_bf16(p.gamma_cq + f, g);
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = h[f + i] * rq * g[i];
       store8_bf16(cq + f, v);
@@ -193,7 +218,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     finish();
     return;
   }
-  const int64_t idx = p.cache_index[t];
+  const int64_t idx = PARTS ? idx_pre : p.cache_index[t];
   if (idx < 0 || idx >= p.slots) {
     if (idx != -1 && threadIdx.x == 0) atomicOr(p.err, kErrIndexRange);
     finish();
@@ -202,7 +227,13 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   // ---- c^KV (Hckv % 8 == 0)
   for (int f = threadIdx.x * 8; f < p.Hckv; f += NT * 8) {
     float g[8], v[8];
-    load8_bf16(p.gamma_ckv + f, g);
+    if (PARTS && p.Hckv <= NT * 8) {
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&g_pre);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = __bfloat162float(e[i]);
+    } else {
+      load8_bf16(p.gamma_ckv + f, g);
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = hkv[f + i] * rkv * g[i];
     if (p.kv_int8) {
@@ -221,8 +252,9 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   for (int j = threadIdx.x; j < p.Dr; j += NT) {
     const float y = hkr[j];
     const float partner = j < half ? -hkr[j + half] : hkr[j - half];
-    const float c = __bfloat162float(p.cos[static_cast<size_t>(t) * p.Dr + j]);
-    const float s = __bfloat162float(p.sin[static_cast<size_t>(t) * p.Dr + j]);
+    const bool pre = PARTS && p.Dr <= NT;           // (j == threadIdx.x then)
+    const float c = __bfloat162float(pre ? cos_pre : p.cos[static_cast<size_t>(t) * p.Dr + j]);
+    const float s = __bfloat162float(pre ? sin_pre : p.sin[static_cast<size_t>(t) * p.Dr + j]);
     const float v = y * c + partner * s;
     if (p.kr_int8)
       static_cast<int8_t*>(p.kr_cache)[idx * p.Dr + j] = quant_i8(v, p.qs_ckr[j], -128, 127);

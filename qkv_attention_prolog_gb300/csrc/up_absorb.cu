@@ -36,30 +36,23 @@ namespace {
 
 constexpr int kUaBK = 64;                              // K elements per stage
 constexpr int kUaA = 128 * kUaBK * 2;                  // c^Q tile: 128 tokens x 64 (16 KB)
-constexpr int kUaWRows = 192;                          // most weight rows of one stage
-constexpr int kUaB = kUaWRows * kUaBK * 2;             // 24 KB
-constexpr int kUaQc = 2 * 128 * kUaBK * 2;             // q^C operand: 128 tokens x D = 128
 constexpr int kUaBars = 1024;                          // barriers and flags, ahead of the stages
 constexpr int kUaSmemMax = 232448;                     // 227 KB opt-in per CTA
 constexpr int kUaMaxStages = 8;
 
 // Shared memory (after 1024-B alignment): barriers, then the operand stages (c^Q tile + weight
-// tile).  bf16 weight: the stage holds exactly this CTA's weight rows (a head CTA 128 + 32k, a
-// rope CTA 32 per block), so a head CTA with one rope block fits six 36 KB stages where fixed
-// 40 KB stages fit four: more of the weight stream in flight, which is what the per-SM rate
-// depends on; q^C lives in the c^Q halves of stages 0 and 1 once the up-projection is done.
-// int8 weight: three 40 KB stages, RSTAGES raw weight tiles in a ring of their own (filled by a
-// second producer thread, so that more of the weight stream is in flight than there are
-// operand stages) and a separate q^C buffer.
+// tile), each holding exactly this CTA's weight rows (a head CTA 128 + 32k, a rope CTA 32 per
+// block), so a head CTA with one rope block fits six 36 KB stages where fixed 40 KB stages fit
+// four: more of the weight stream in flight, which is what the per-SM rate depends on.  q^C
+// lives in the c^Q halves of stages 0 and 1 once the up-projection is done.  int8 weight: after
+// the operand stages, a ring of raw int8 tiles (64 B per row), filled by a second producer thread
+// so that more of the weight stream is in flight than there are operand stages; up to six raw
+// tiles, as many as leave room for four operand stages.
 template <bool INT8>
 struct UaCfg {
   static constexpr int THREADS = INT8 ? 384 : 256;
-  static constexpr int RSTAGES = INT8 ? 6 : 0;
-  static constexpr int RAW = 192 * kUaBK;       // raw int8 weight tile (192 rows max)
-  static constexpr int I8_STAGES = 3;
-  static constexpr int SMEM = INT8 ? 1024 + kUaBars + I8_STAGES * (kUaA + kUaB) + RSTAGES * RAW + kUaQc
-                                   : kUaSmemMax;
-  static_assert(RAW % 1024 == 0 && SMEM <= kUaSmemMax, "shared memory layout");
+  static constexpr int MAX_RAW = INT8 ? 6 : 0;
+  static constexpr int SMEM = kUaSmemMax;
 };
 constexpr uint32_t kUaUpCol = 256;                     // TMEM column of the up accumulator
 #ifdef MLAP_UA_TRACE   // pipeline timeline of one CTA into spare words of its stamps slot
@@ -153,7 +146,6 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmUk,   // W^UK rows, box 64 x 32
                      const UpAbsorbParams p, uint32_t* __restrict__ err_word) {
   using Cfg = UaCfg<INT8>;
-  constexpr int kRS = Cfg::RSTAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -166,12 +158,15 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   const int up_rows = (pl.head ? kD : 0) + 32 * pl.nrope;   // B rows of the up-projection
   // weight rows one stage holds (also the W^UK chunk height of a head CTA), the stage size and
   // the stage count
-  const int wrows = INT8 ? kUaWRows : up_rows;
+  const int wrows = up_rows;
   const int kUaStage = kUaA + wrows * kUaBK * 2;
-  const int kUaStages =
-      INT8 ? Cfg::I8_STAGES
-           : ((kUaSmemMax - 1024 - kUaBars) / kUaStage < kUaMaxStages
-                  ? (kUaSmemMax - 1024 - kUaBars) / kUaStage : kUaMaxStages);
+  constexpr int kAvail = kUaSmemMax - 1024 - kUaBars;
+  const int kRawB = INT8 ? wrows * kUaBK : 0;                 // raw int8 tile bytes
+  const int kRS = INT8 ? ((kAvail - 4 * kUaStage) / kRawB < Cfg::MAX_RAW
+                              ? (kAvail - 4 * kUaStage) / kRawB : Cfg::MAX_RAW)
+                       : 0;
+  const int kUaStages = (kAvail - kRS * kRawB) / kUaStage < kUaMaxStages
+                            ? (kAvail - kRS * kRawB) / kUaStage : kUaMaxStages;
   const int nh = pl.head ? (p.Hckv + wrows - 1) / wrows : 0;   // absorb column chunks (<= 4)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty_bar = full_bar + kUaMaxStages;
@@ -184,10 +179,10 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint8_t* stages = smem + kUaBars;
   uint8_t* ring_raw = stages + kUaStages * kUaStage;   // int8: raw weight tiles
-  // q^C operand, two 64-wide K blocks: int8, its own buffer; bf16, the c^Q halves of stages 0 and
-  // 1, free once the up-projection's MMAs have completed
-  uint8_t* qc0 = INT8 ? ring_raw + kRS * Cfg::RAW : stages;
-  uint8_t* qc1 = INT8 ? qc0 + kUaA : stages + kUaStage;
+  // q^C operand, two 64-wide K blocks: the c^Q halves of stages 0 and 1, free once the
+  // up-projection's MMAs have completed
+  uint8_t* qc0 = stages;
+  uint8_t* qc1 = stages + kUaStage;
   if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_UP, kStampStart);
 
   if (warp == 0 && lane == 0) {
@@ -316,7 +311,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   } else if (raw_producer) {
     // ------------------------------------------------------------------ int8 weight producer
     // raw int8 rows of 64 B into a ring of kRS tiles, ahead of the operand stages
-    int rawfills[kRS > 0 ? kRS : 1] = {};
+    int rawfills[kUaMaxStages] = {};
     const int nbox = up_rows / 32;
     int ybox[6];
 #pragma unroll
@@ -336,7 +331,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
             if (j < nbox) tma_prefetch_l2_2d(&tmW, k2 * kUaBK, ybox[j]);
       }
       if (kb >= kRS && !mbar_wait(&rawe_bar[rs], rph ^ 1u, abort_flag)) break;
-      uint8_t* r = ring_raw + rs * Cfg::RAW;
+      uint8_t* r = ring_raw + rs * kRawB;
       mbar_arrive_expect_tx(&rawf_bar[rs], static_cast<uint32_t>(up_rows) * kUaBK);
 #pragma unroll
       for (int j = 0; j < 6; ++j)
@@ -428,7 +423,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         ok = false;
         break;
       }
-      const uint8_t* raw = ring_raw + rs * Cfg::RAW;
+      const uint8_t* raw = ring_raw + rs * kRawB;
       uint8_t* dst = stages + stage * kUaStage + kUaA;
       for (int r = ct; r < up_rows; r += 128) convert_int8_row(raw + r * kUaBK, dst, r);
       fence_proxy_async_shared();                      // generic writes -> the tensor core
@@ -549,7 +544,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       // of the warp's 4 KB staging tile (a c^Q half of a stage, free after the up-projection;
       // 16-B chunks XOR-swizzled by row), then eight lanes store each row as one 128-B line, four
       // rows per instruction, instead of 32 scattered 16-B pieces
-      uint8_t* tile = stages + (INT8 ? (q >> 1) : 2 + (q >> 1)) * kUaStage + (q & 1) * 4096;
+      uint8_t* tile = stages + (2 + (q >> 1)) * kUaStage + (q & 1) * 4096;
       const int rsub = lane >> 3, ch = lane & 7;        // read-back: row rsub + 4i, chunk ch
       int waited = 0;                                   // absorb chunks known complete
 #pragma unroll 1
