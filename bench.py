@@ -512,9 +512,12 @@ def measure_mla(args, case, dev, stream, steps, warm, world, stamp_calls, sample
 
 def _roofline(m, tensor_bound, hbm, tf_sus, peak_kind, workload):
     """Roofline entry of the dominant kernel: algorithmic bytes (FLOPs) per launch over its mean
-    span inside the pipelined calls (earliest CTA start to latest CTA end)."""
+    span inside the pipelined calls (earliest CTA start to latest CTA end).  The dominant kernel
+    is the one with the longest time from its dependency wait to its end: under programmatic
+    dependent launch a kernel starts while its predecessor runs, so its span also holds time
+    spent waiting, and the longest span need not be the kernel that takes the most of the call."""
     per, kern = m["per_kernel"], m["kern"]
-    dominant = max(per, key=lambda n: per[n]["span_us"])
+    dominant = max(per, key=lambda n: per[n]["dep_to_end_us"] or per[n]["span_us"])
     span_s = per[dominant]["span_us"] / 1e6
     if tensor_bound:
         achieved = kern[dominant]["flops"] / span_s / 1e12

@@ -552,6 +552,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       g.geo.n_tiles = seg + ceil_div(d.Hckv + d.Dr, bnd);
       g.geo.a_seg_tiles = g.geo.m_tiles;
       g.geo.b_seg_tiles = seg;
+      g.geo.n_fast = 1;   // each x tile (128 x He) is used by every weight tile while in L2
       int splits = sms / (g.geo.m_tiles * g.geo.n_tiles);
       if (splits > L.split_cap) splits = L.split_cap;
       if (splits > kb) splits = kb;

@@ -61,6 +61,9 @@ struct GemmGeometry {
   // Optional execution stamps (%globaltimer) of this launch, kernel slot stamp_k (stamps.cuh).
   uint64_t* stamps;
   int32_t stamp_k;
+  // 1: units walk the N tiles fastest (the A tiles are the large operand, e.g. the activations of
+  // the prefill down-projection); 0: the M tiles fastest.
+  int32_t n_fast;
   // 1: neither operand comes from an earlier kernel of the stream (both are inputs of the call),
   // so loads and MMAs start at once and only the epilogue waits for the preceding kernel, before
   // its first store (the preceding kernels may still read what it overwrites).
@@ -124,10 +127,17 @@ struct GemmCfg {
 
 __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& tm, int& tn, int& b,
                                             int& s) {
-  tm = u % g.m_tiles;
-  u /= g.m_tiles;
-  tn = u % g.n_tiles;
-  u /= g.n_tiles;
+  if (g.n_fast) {   // units of one A tile run together: the A tile is read from DRAM once
+    tn = u % g.n_tiles;
+    u /= g.n_tiles;
+    tm = u % g.m_tiles;
+    u /= g.m_tiles;
+  } else {
+    tm = u % g.m_tiles;
+    u /= g.m_tiles;
+    tn = u % g.n_tiles;
+    u /= g.n_tiles;
+  }
   b = u % g.batches;
   s = u / g.batches;
 }
