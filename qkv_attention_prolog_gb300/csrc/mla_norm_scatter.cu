@@ -264,6 +264,189 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   finish();
 }
 
+// Without K splits (prefill): one warp per token, eight tokens per CTA.  Lane l holds the
+// float4 columns l + 32 i of the token's row (down to NV per lane) in registers, so both sums of
+// squares, the amax of the quantised c^Q and the RoPE partner exchange stay inside the warp: no
+// block barrier between the load and the stores, and every warp keeps its whole row (8.4 KB at
+// Ntot = 2112) in flight at once.  Same arithmetic as norm_rope_scatter_kernel, term by term;
+// only the order of the two sums of squares differs (lane-strided, then a shuffle tree).
+constexpr int kWarpTokens = 8;
+constexpr int kWarpMaxDr = 256;
+constexpr int kWarpNV = 17;   // Ntot <= 32 * 4 * 17 = 2176
+
+__device__ __forceinline__ void load4_bf16(const __nv_bfloat16* p, float* out) {
+  const uint2 r = __ldg(reinterpret_cast<const uint2*>(p));
+  const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out[i] = __bfloat162float(e[i]);
+}
+
+__device__ __forceinline__ void store4_bf16(__nv_bfloat16* p, const float* v) {
+  uint2 r;
+  __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&r);
+  e[0] = __floats2bfloat162_rn(v[0], v[1]);
+  e[1] = __floats2bfloat162_rn(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) = r;
+}
+
+template <int NV>
+__global__ void __launch_bounds__(32 * kWarpTokens, 2) norm_rope_scatter_warp_kernel(
+    const FinalizeParams p) {
+  __shared__ float kr_s[kWarpTokens][kWarpMaxDr];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpTokens + warp;
+  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampStart);
+  grid_launch_dependents();
+  // the cache index is an input of the call: read before the wait on the down-projection
+  int64_t idx = -1;
+  if (t < p.T && p.slots > 0) idx = p.cache_index[t];
+  grid_dependency_wait();
+  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampDep);
+  if (t >= p.T) return;                              // warp-uniform
+
+  const int n4 = p.Ntot >> 2, q4 = p.Hcq >> 2, kv4 = (p.Hcq + p.Hckv) >> 2;
+  const float4* src = reinterpret_cast<const float4*>(p.part + static_cast<size_t>(t) * p.Ntot);
+  float4 v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane + 32 * i;
+    v[i] = c < n4 ? __ldg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (p.dsx != nullptr) {   // full quant: dequant the exact integer products per token and column
+    const float sx = p.dsx[t];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c = lane + 32 * i;
+      if (c < n4) {   // (dsw_kv covers the c^KV and the k^R columns)
+        const float* w = c < q4 ? p.dsw_q + 4 * c : p.dsw_kv + 4 * (c - q4);
+        v[i].x *= sx * w[0];
+        v[i].y *= sx * w[1];
+        v[i].z *= sx * w[2];
+        v[i].w *= sx * w[3];
+      }
+    }
+  }
+  float sq = 0.f, skv = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane + 32 * i;
+    const float s4 = v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    if (c < q4) sq += s4;
+    else if (c < kv4) skv += s4;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    skv += __shfl_xor_sync(0xffffffffu, skv, o);
+  }
+  const float rq = 1.0f / sqrtf(sq / static_cast<float>(p.Hcq) + p.eps_cq);
+  const float rkv = 1.0f / sqrtf(skv / static_cast<float>(p.Hckv) + p.eps_ckv);
+
+  // ---- c^Q: bf16, or int8 codes held exactly in bf16
+  __nv_bfloat16* cq = p.cq_out + static_cast<size_t>(t) * p.Hcq;
+  if (p.smooth == nullptr) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c = lane + 32 * i;
+      if (c < q4) {
+        float g[4], o[4];
+        load4_bf16(p.gamma_cq + 4 * c, g);
+        o[0] = v[i].x * rq * g[0];
+        o[1] = v[i].y * rq * g[1];
+        o[2] = v[i].z * rq * g[2];
+        o[3] = v[i].w * rq * g[3];
+        store4_bf16(cq + 4 * c, o);
+      }
+    }
+  } else {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c = lane + 32 * i;
+      if (c < q4) {
+        float* e = reinterpret_cast<float*>(&v[i]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int f = 4 * c + k;
+          const float cv = __bfloat162float(
+              __float2bfloat16_rn(e[k] * rq * __bfloat162float(p.gamma_cq[f])));
+          e[k] = __fmul_rn(cv, p.smooth[f]);
+          amax = fmaxf(amax, fabsf(e[k]));
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c = lane + 32 * i;
+      if (c < q4) {
+        const float* e = reinterpret_cast<const float*>(&v[i]);
+        float o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          o[k] = static_cast<float>(scale > 0.f ? quant_i8(e[k], scale, -127, 127) : 0);
+        store4_bf16(cq + 4 * c, o);               // exact: |code| <= 127
+      }
+    }
+    if (lane == 0) p.scale_t[t] = scale;
+  }
+
+  auto finish = [&]() {
+    if (lane == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampEnd);
+  };
+  if (p.slots <= 0) {                              // empty caches: outputs only
+    finish();
+    return;
+  }
+  if (idx < 0 || idx >= p.slots) {
+    if (idx != -1 && lane == 0) atomicOr(p.err, kErrIndexRange);
+    finish();
+    return;
+  }
+  // ---- c^KV, and k^R into this warp's shared row for the RoPE partner exchange
+  float* kr = kr_s[warp];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane + 32 * i;
+    if (c >= q4 && c < kv4) {
+      const int f = 4 * (c - q4);
+      float g[4], o[4];
+      load4_bf16(p.gamma_ckv + f, g);
+      o[0] = v[i].x * rkv * g[0];
+      o[1] = v[i].y * rkv * g[1];
+      o[2] = v[i].z * rkv * g[2];
+      o[3] = v[i].w * rkv * g[3];
+      if (p.kv_int8) {
+        uint32_t q;
+        int8_t* qb = reinterpret_cast<int8_t*>(&q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qb[k] = quant_i8(o[k], p.qs_ckv[f + k], -128, 127);
+        *reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.kv_cache) + idx * p.Hckv + f) = q;
+      } else {
+        store4_bf16(static_cast<__nv_bfloat16*>(p.kv_cache) + idx * p.Hckv + f, o);
+      }
+    } else if (c >= kv4 && c < n4) {
+      *reinterpret_cast<float4*>(kr + 4 * (c - kv4)) = v[i];
+    }
+  }
+  __syncwarp();
+  const int half = p.Dr >> 1;
+  for (int j = lane; j < p.Dr; j += 32) {
+    const float y = kr[j];
+    const float partner = j < half ? -kr[j + half] : kr[j - half];
+    const float c = __bfloat162float(p.cos[static_cast<size_t>(t) * p.Dr + j]);
+    const float s = __bfloat162float(p.sin[static_cast<size_t>(t) * p.Dr + j]);
+    const float o = y * c + partner * s;
+    if (p.kr_int8)
+      static_cast<int8_t*>(p.kr_cache)[idx * p.Dr + j] = quant_i8(o, p.qs_ckr[j], -128, 127);
+    else
+      static_cast<__nv_bfloat16*>(p.kr_cache)[idx * p.Dr + j] = __float2bfloat16_rn(o);
+  }
+  finish();
+}
+
 // dst[b][i][k] = src[b][k][perm(i)], 32x32 tiles through shared memory.
 template <typename E>
 __global__ void prepack_kernel(const PrepackParams p) {
@@ -496,6 +679,12 @@ cudaError_t launch_query_quant(const __nv_bfloat16* qn, int8_t* q, float* scale,
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {
   const size_t smem = static_cast<size_t>(p.Ntot) * sizeof(float);
   const bool split = p.splits > 1;
+  if (!split && p.Ntot <= 32 * 4 * kWarpNV && p.Dr <= kWarpMaxDr) {
+    // (Hcq, Hckv and Dr are multiples of 8: every float4 of a row lies in one part)
+    return launch_k(norm_rope_scatter_warp_kernel<kWarpNV>,
+                    dim3(static_cast<unsigned>((p.T + kWarpTokens - 1) / kWarpTokens)),
+                    dim3(32 * kWarpTokens), stream, pdl, p);
+  }
   // up to 8 K-splits (decode): two CTAs per token, c^Q and c^KV/k^R
   const bool parts = split && p.splits <= 8;
   auto kern = !split ? norm_rope_scatter_kernel<1, 256>
