@@ -443,6 +443,10 @@ mlap_status_t make_tmap_i8(CUtensorMap* m, const void* base, int64_t inner, int6
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
+// Token count from which the prefill-orientation bf16 GEMMs (down- and up-projection) run on CTA
+// pairs with 256-row tiles of tokens.
+constexpr int64_t kPairMinT = 1024;
+
 // The decode-orientation activation operand, read by the GEMM's cp.async loader warps.
 void set_act(GemmGeometry* g, const void* p, int64_t ld, int64_t rows, int64_t cols) {
   g->act = static_cast<const uint16_t*>(p);
@@ -540,15 +544,17 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       dp.seg_tiles = seg;
     } else {
       // N = 256 keeps the tensor pipe fed (N = 192 reached 0.68 of the sustained peak at
-      // T = 8192); the int8 weights of full quant keep 192-row tiles for their converter warps
+      // T = 8192); the int8 weights of full quant keep 192-row tiles for their converter warps.
+      // Many tokens: CTA pairs, each CTA staging 128 tokens and half of a 256-row weight tile.
       const int bnd = d.full ? 192 : 256;
       const int seg = ceil_div(d.Hcq, bnd);
+      g.cg = !d.full && d.T >= kPairMinT ? 2 : 1;
       CHECK_STATUS(make_tmap(&g.a0, xact, d.He, d.T, d.He, 128));
       g.a1 = g.a0;
-      CHECK_STATUS(wmap(&g.b0, a->weight_dq.data, d.Hcq, bnd));
-      CHECK_STATUS(wmap(&g.b1, a->weight_dkv_kr.data, d.Hckv + d.Dr, bnd));
+      CHECK_STATUS(wmap(&g.b0, a->weight_dq.data, d.Hcq, bnd / g.cg));
+      CHECK_STATUS(wmap(&g.b1, a->weight_dkv_kr.data, d.Hckv + d.Dr, bnd / g.cg));
       g.bn = bnd;
-      g.geo.m_tiles = ceil_div(d.T, 128);
+      g.geo.m_tiles = ceil_div(d.T, 128 * g.cg);
       g.geo.n_tiles = seg + ceil_div(d.Hckv + d.Dr, bnd);
       g.geo.a_seg_tiles = g.geo.m_tiles;
       g.geo.b_seg_tiles = seg;
@@ -572,7 +578,8 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     CHECK_STATUS(make_out_map(&g.o1, part + d.Hcq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                               {d.Hckv + d.Dr, d.T, g.geo.splits}, {row_b, split_b}, {32, ch_t, 1},
                               CU_TENSOR_MAP_SWIZZLE_128B));
-    g.grid = balanced_grid(g.geo.num_units, sms);
+    g.grid = g.cg == 2 ? 2 * balanced_grid(g.geo.num_units, sms / 2)
+                       : balanced_grid(g.geo.num_units, sms);
     if (d.xnorm) {
       ce = launch_rms_norm_quant(static_cast<const __nv_bfloat16*>(a->token_x.data),
                                  static_cast<const __nv_bfloat16*>(a->rms_norm_quant_gamma.data),
@@ -701,15 +708,17 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       u.geo.m_tiles = ceil_div(Mup, wrows);
       u.geo.n_tiles = 1;
     } else {
+      // many tokens, bf16 weight: CTA pairs (each CTA stages 128 tokens and 128 weight rows)
+      u.cg = !d.w_int8 && d.T >= kPairMinT ? 2 : 1;
       CHECK_STATUS(make_tmap(&u.a0, cq, d.Hcq, d.T, d.Hcq, 128));
       u.a1 = u.a0;
       if (d.w_int8)
         CHECK_STATUS(make_tmap_i8(&u.b0, a->weight_uq_qr.data, d.Hcq, Mup, 256));
       else
-        CHECK_STATUS(make_tmap(&u.b0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 256));
+        CHECK_STATUS(make_tmap(&u.b0, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 256 / u.cg));
       u.b1 = u.b0;
       u.bn = 256;
-      u.geo.m_tiles = ceil_div(d.T, 128);
+      u.geo.m_tiles = ceil_div(d.T, 128 * u.cg);
       u.geo.n_tiles = ceil_div(Mup, 256);
     }
     u.geo.a_seg_tiles = u.geo.m_tiles;
@@ -720,7 +729,8 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     u.geo.k_blocks = ceil_div(d.Hcq, 64);
     u.geo.num_units = u.geo.m_tiles * u.geo.n_tiles;
     u.grid = up_var ? static_cast<int>(std::min<int64_t>(sms, Mup / 32))
-                    : balanced_grid(u.geo.num_units, sms);
+             : u.cg == 2 ? 2 * balanced_grid(u.geo.num_units, sms / 2)
+                         : balanced_grid(u.geo.num_units, sms);
     const int ch_u = u.swap ? ch_t : 32;   // tokens per store box: one per lane unless swapped
     CHECK_STATUS(make_out_map(&u.o0, qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, {d.N * d.D, d.T},
                               {d.N * d.D * 2}, {32, ch_u}, CU_TENSOR_MAP_SWIZZLE_64B));

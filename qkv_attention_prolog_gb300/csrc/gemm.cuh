@@ -26,6 +26,15 @@
 // stream, which is what a memory-bound decode GEMM needs: the activation tile per K step is as
 // large as the weight tile, and sharing the TMA unit's requests with it halved the weight rate.
 //
+// With CG = 2 a cluster of two CTAs (a CTA pair on one TPC) computes each 256 x BN tile with
+// tcgen05.mma.cta_group::2: each CTA stages its own 128 rows of A and half of the BN rows of B,
+// the pair's first CTA issues the MMAs (M = 256), and each CTA's tensor memory receives the
+// accumulator of its own 128 rows.  Per MMA FLOP a CTA then loads and holds a third less operand
+// data, so 6 instead of 4 stages fit and more of the load latency is hidden (prefill).  Both
+// CTAs' TMA loads complete on the first CTA's full barriers; its commits arrive on the stage and
+// accumulator barriers of both CTAs; the second CTA's epilogue warps release an accumulator on
+// the first CTA's barrier.
+//
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM owner, warp 3 = idle,
 // warps 4..7 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31), warps 8..11 = int8 converters
 // (WQ) or activation loaders (ALD).
@@ -89,17 +98,20 @@ struct StoreOp {
 // WQ: 0 = bf16 weight, 1 = int8 weight in operand A, 2 = int8 weight in operand B.
 // MT: 128-row tiles of A per unit (1 or 2), each with its own TMEM accumulator.
 // ALD: operand B (the activation, decode orientation) is loaded by cp.async loader warps.
-template <int BN_, int WQ_ = 0, int MT_ = 1, int ALD_ = 0>
+template <int BN_, int WQ_ = 0, int MT_ = 1, int ALD_ = 0, int CG_ = 1>
 struct GemmCfg {
+  static constexpr int CG = CG_;                       // CTAs per MMA (cta_group)
   static constexpr int WQ = WQ_;
   static constexpr int MT = MT_;
   static constexpr int ALD = ALD_;
   static constexpr int BM = 128;                       // rows per MMA
-  static constexpr int BM_U = BM * MT;                 // rows of A per unit
+  static constexpr int BM_U = BM * MT;                 // rows of A per unit and CTA
+  static constexpr int ROWS_U = BM_U * CG;             // rows of A per unit
   static constexpr int BN = BN_;
+  static constexpr int BN_CTA = BN / CG;               // rows of B staged per CTA
   static constexpr int BK = 64;
   static constexpr int A_BYTES = BM_U * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int RAW_ROWS = WQ == 1 ? BM_U : (WQ == 2 ? BN : 0);
   static constexpr int RAW_BYTES = RAW_ROWS * BK;      // int8 weight tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + RAW_BYTES;
@@ -114,7 +126,7 @@ struct GemmCfg {
   static constexpr int ACC_COLS = 2 * MT * BN;         // double-buffered accumulators
   static constexpr uint32_t TMEM_COLS =
       ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM * CG, BN);
   static constexpr int THREADS = (WQ || ALD) ? 384 : 256;
   static constexpr uint32_t FULL_ARRIVALS = WQ ? 1 + 4 : (ALD ? 1 + 128 : 1);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16,256]");
@@ -123,6 +135,8 @@ struct GemmCfg {
   static_assert(ACC_COLS <= 512, "accumulators exceed tensor memory");
   static_assert(MT == 1 || MT == 2, "one or two row tiles per unit");
   static_assert(!(ALD && WQ), "cp.async activation loading is for bf16 weights");
+  static_assert(CG == 1 || (CG == 2 && WQ == 0 && MT == 1 && ALD == 0 && BN % 32 == 0),
+                "CTA-pair tiles: bf16 operands through TMA, one row tile, B split in halves");
 };
 
 __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& tm, int& tn, int& b,
@@ -146,10 +160,13 @@ __device__ __forceinline__ void decode_unit(const GemmGeometry& g, int u, int& t
 // (compile-time, so that the other launches carry none of its code).
 template <bool RR, int BN>
 struct FragIter {
-  int u;
+  int u, step;
   long long i, i1;
-  __device__ __forceinline__ explicit FragIter(const GemmGeometry& g) {
-    u = blockIdx.x;
+  // first unit and stride: this CTA's index and the grid (one CTA per unit), or the pair's index
+  // and the number of pairs (CTA pairs)
+  __device__ __forceinline__ FragIter(const GemmGeometry& g, int first, int stride) {
+    u = first;
+    step = stride;
     i = i1 = 0;
     if constexpr (RR) {   // chunk range of this CTA
       const long long total = static_cast<long long>(g.batches) * (g.rr_rows / 32);
@@ -183,7 +200,7 @@ struct FragIter {
     f.kb1 = ((f.s + 1) * g.k_blocks) / g.splits;
     f.row0 = 0;
     f.rows = 0;
-    u += gridDim.x;
+    u += step;
     return true;
   }
 };
@@ -231,8 +248,8 @@ __device__ __forceinline__ void convert_int8_row(const uint8_t* src_row, uint8_t
 // first A row is m0 (lane l holds row m0 + l) and first B row is n0 (v[j] is column n0 + j).  It
 // writes the block's output into the warp's staging buffer and returns the TMA stores (at most
 // two, warp-uniform) that move it to global memory through the two output tensor maps.
-template <int BN, class Epi, int WQ, int MT, int ALD>
-__global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
+template <int BN, class Epi, int WQ, int MT, int ALD, int CG>
+__global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                      const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB0,
@@ -240,8 +257,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmO0,
                      const __grid_constant__ CUtensorMap tmO1, const GemmGeometry geo,
                      const Epi epi, uint32_t* __restrict__ err_word) {
-  using Cfg = GemmCfg<BN, WQ, MT, ALD>;
+  using Cfg = GemmCfg<BN, WQ, MT, ALD, CG>;
   constexpr bool RR = Epi::kDirect;   // the row-range launches are the direct-store ones
+  static_assert(!(RR && CG == 2), "the row-range schedule runs on single CTAs");
   using Iter = FragIter<RR, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -261,6 +279,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const bool w_is_a = geo.w_op == 0;
+  // CTA pair: rank in the pair (0 issues the MMAs), the pair's units
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const bool issuer = rank == 0;
+  const int first_unit = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_step = CG == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   if (threadIdx.x == 0) stamp(geo.stamps, geo.stamp_k, kStampStart);
 
   if (warp == 0 && lane == 0) {
@@ -279,17 +302,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf_bar[i], 1);
-      mbar_init(&acce_bar[i], 4);
+      mbar_init(&acce_bar[i], 4 * CG);   // the epilogue warps of every CTA of the pair
     }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();   // the peer's barriers exist before any remote arrival
+  else __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -304,8 +333,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     if (lane == 0) {
       auto load_a = [&](int tm, int b, int kb, uint64_t* bar, void* dst) {
         const bool first = tm < geo.a_seg_tiles;
-        const int y = (first ? tm : tm - geo.a_seg_tiles) * Cfg::BM_U + b * geo.a_y_batch;
-        tma_load_2d(dst, first ? &tmA0 : &tmA1, bar, kb * Cfg::BK + b * geo.a_x_batch, y);
+        const int y = (first ? tm : tm - geo.a_seg_tiles) * Cfg::ROWS_U +
+                      static_cast<int>(rank) * Cfg::BM_U + b * geo.a_y_batch;
+        const int x = kb * Cfg::BK + b * geo.a_x_batch;
+        if constexpr (CG == 2)   // completes on the pair's first CTA's barrier
+          tma_load_2d_pair(dst, first ? &tmA0 : &tmA1, mapa_shared(smem_u32(bar), 0), x, y);
+        else
+          tma_load_2d(dst, first ? &tmA0 : &tmA1, bar, x, y);
       };
       auto load_b = [&](const Frag& f, int kb, uint64_t* bar, void* dst) {
         const int tn = f.tn, b = f.b;
@@ -316,8 +350,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
           return;
         }
         const bool first = tn < geo.b_seg_tiles;
-        const int y = (first ? tn : tn - geo.b_seg_tiles) * Cfg::BN + b * geo.b_y_batch;
-        tma_load_2d(dst, first ? &tmB0 : &tmB1, bar, kb * Cfg::BK + b * geo.b_x_batch, y);
+        const int y = (first ? tn : tn - geo.b_seg_tiles) * Cfg::BN +
+                      static_cast<int>(rank) * Cfg::BN_CTA + b * geo.b_y_batch;
+        const int x = kb * Cfg::BK + b * geo.b_x_batch;
+        if constexpr (CG == 2)
+          tma_load_2d_pair(dst, first ? &tmB0 : &tmB1, mapa_shared(smem_u32(bar), 0), x, y);
+        else
+          tma_load_2d(dst, first ? &tmB0 : &tmB1, bar, x, y);
       };
       // weight tile of stage st (bf16 into the operand buffer, or int8 into the raw buffer)
       auto issue_weight = [&](int st, const Frag& f, int kb) {
@@ -329,21 +368,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
           mbar_arrive_expect_tx(&full_bar[st], Cfg::A_BYTES);
           load_a(f.tm, f.b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
         } else if (w_is_a) {
-          mbar_expect_tx(&full_bar[st], Cfg::A_BYTES);
+          // (a pair's stage completes on its first CTA's barrier: it expects both CTAs' bytes)
+          if (issuer) mbar_expect_tx(&full_bar[st], CG * Cfg::A_BYTES);
           load_a(f.tm, f.b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
         } else {
-          mbar_expect_tx(&full_bar[st], RR ? static_cast<uint32_t>(f.rows) * Cfg::BK * 2
-                                           : static_cast<uint32_t>(Cfg::B_BYTES));
+          if (issuer)
+            mbar_expect_tx(&full_bar[st], RR ? static_cast<uint32_t>(f.rows) * Cfg::BK * 2
+                                             : static_cast<uint32_t>(CG * Cfg::B_BYTES));
           load_b(f, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
         }
       };
       auto issue_act = [&](int st, const Frag& f, int kb) {
         if (ALD) return;
         if (w_is_a) {
-          mbar_arrive_expect_tx(&full_bar[st], Cfg::B_BYTES);
+          if (issuer) mbar_arrive_expect_tx(&full_bar[st], CG * Cfg::B_BYTES);
           load_b(f, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
         } else {
-          mbar_arrive_expect_tx(&full_bar[st], Cfg::A_BYTES);
+          if (issuer) mbar_arrive_expect_tx(&full_bar[st], CG * Cfg::A_BYTES);
           load_a(f.tm, f.b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
         }
       };
@@ -351,7 +392,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
       // Weight tiles of this CTA's first stages, before the grid dependency resolves.
       int pre = 0;
       {
-        Iter it0(geo);
+        Iter it0(geo, first_unit, unit_step);
         Frag f0;
         if (it0.next(geo, f0)) {
           pre = f0.kb1 - f0.kb0 < Cfg::STAGES ? f0.kb1 - f0.kb0 : Cfg::STAGES;
@@ -366,14 +407,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      Iter it(geo);
+      Iter it(geo, first_unit, unit_step);
       Frag f;
       for (int n = 0; ok && it.next(geo, f); ++n) {
         const int kb0 = f.kb0, kb1 = f.kb1;
         for (int kb = kb0; kb < kb1; ++kb) {
           const bool prefetched = n == 0 && kb - kb0 < pre;
           if (!prefetched) {
-            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            // (a pair's stages are freed by the first CTA's MMA commits)
+            const bool empty = CG == 2 ? mbar_wait_cluster(&empty_bar[stage], phase ^ 1u, abort_flag)
+                                       : mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag);
+            if (!empty) {
               ok = false;
               break;
             }
@@ -386,9 +430,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
           }
         }
       }
-      if (*abort_flag) {
+      if (*abort_flag && issuer) {
         // Give up cleanly: let every load already issued land before the CTA exits.  The last
-        // fill of stage i has parity `phase` if i < stage (this lap), else `phase ^ 1`.
+        // fill of stage i has parity `phase` if i < stage (this lap), else `phase ^ 1`.  (A
+        // pair's second CTA waits at the end instead: its loads complete on these barriers.)
         for (int i = 0; i < Cfg::STAGES; ++i) {
           const uint32_t par = (i < stage) ? phase : (phase ^ 1u);
           const uint64_t t0 = globaltimer_ns();
@@ -403,23 +448,27 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && issuer) {
       int stage = 0;
       uint32_t phase = 0;
       int iter = 0;
       bool ok = true;
-      Iter it(geo);
+      Iter it(geo, first_unit, unit_step);
       Frag f;
       for (; ok && it.next(geo, f); ++iter) {
         const int kb0 = f.kb0, kb1 = f.kb1;
         const int buf = iter & 1;
         const uint32_t use = static_cast<uint32_t>(iter >> 1);
-        if (!mbar_wait(&acce_bar[buf], (use & 1u) ^ 1u, abort_flag)) break;
+        const bool freed = CG == 2 ? mbar_wait_cluster(&acce_bar[buf], (use & 1u) ^ 1u, abort_flag)
+                                   : mbar_wait(&acce_bar[buf], (use & 1u) ^ 1u, abort_flag);
+        if (!freed) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * MT * Cfg::BN);
         const uint32_t idesc = RR ? idesc_bf16_f32(Cfg::BM, f.rows) : Cfg::IDESC;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+          const bool landed = CG == 2 ? mbar_wait_cluster(&full_bar[stage], phase, abort_flag)
+                                      : mbar_wait(&full_bar[stage], phase, abort_flag);
+          if (!landed) {
             ok = false;
             break;
           }
@@ -429,20 +478,31 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
           const uint32_t b_addr = smem_u32(smemB + stage * Cfg::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < Cfg::BK / 16; ++kk) {
+            if constexpr (CG == 2) {
+              umma_bf16_ss_pair(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
+                                sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                                (kb > kb0 || kk > 0) ? 1u : 0u);
+            } else {
 #pragma unroll
-            for (int h = 0; h < MT; ++h)
-              umma_bf16_ss(d_tmem + h * Cfg::BN,
-                           sdesc_kmajor_sw128(a_addr + h * Cfg::BM * Cfg::BK * 2 + kk * 32),
-                           sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
-                           (kb > kb0 || kk > 0) ? 1u : 0u);
+              for (int h = 0; h < MT; ++h)
+                umma_bf16_ss(d_tmem + h * Cfg::BN,
+                             sdesc_kmajor_sw128(a_addr + h * Cfg::BM * Cfg::BK * 2 + kk * 32),
+                             sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                             (kb > kb0 || kk > 0) ? 1u : 0u);
+            }
           }
-          umma_commit(&empty_bar[stage]);   // frees this smem stage once the MMAs have read it
+          // frees this smem stage (in both CTAs of a pair) once the MMAs have read it
+          if constexpr (CG == 2) umma_commit_pair(&empty_bar[stage], 0x3);
+          else umma_commit(&empty_bar[stage]);
           if (++stage == Cfg::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit(&accf_bar[buf]);   // accumulator ready for the epilogue
+        if (ok) {   // accumulator ready for the epilogue (of both CTAs of a pair)
+          if constexpr (CG == 2) umma_commit_pair(&accf_bar[buf], 0x3);
+          else umma_commit(&accf_bar[buf]);
+        }
       }
     }
   } else if (warp >= 4 && warp < 8) {
@@ -455,7 +515,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     }
     int sel = 0;
     int iter = 0;
-    Iter it(geo);
+    Iter it(geo, first_unit, unit_step);
     Frag f;
     for (; it.next(geo, f); ++iter) {
       const int tm = f.tm, tn = f.tn, b = f.b, s = f.s;
@@ -464,14 +524,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
       const int n_row0 = RR ? f.row0 : tn * Cfg::BN;            // this piece's B rows
       const int ncols = RR ? MT * f.rows : MT * Cfg::BN;        // accumulator columns
       // inputs the epilogue of the first block needs (e.g. RoPE tables), before the wait
-      typename Epi::Pre pre = epi.preload(tm * Cfg::BM_U + q * 32, n_row0);
-      if (!mbar_wait(&accf_bar[buf], use & 1u, abort_flag)) break;
+      const int m_base = tm * Cfg::ROWS_U + static_cast<int>(rank) * Cfg::BM_U;   // this CTA's rows
+      typename Epi::Pre pre = epi.preload(m_base + q * 32, n_row0);
+      const bool ready = CG == 2 ? mbar_wait_cluster(&accf_bar[buf], use & 1u, abort_flag)
+                                 : mbar_wait(&accf_bar[buf], use & 1u, abort_flag);
+      if (!ready) break;
       tc_fence_after_sync();
       if (q == 0 && lane == 0) stamp(geo.stamps, geo.stamp_k, kStampMain);
 #pragma unroll 1
       for (int hc = 0; hc < ncols; hc += Cfg::CH) {
         const int h = hc / Cfg::BN, c = hc % Cfg::BN;
-        const int m0 = tm * Cfg::BM_U + h * Cfg::BM + q * 32;
+        const int m0 = m_base + h * Cfg::BM + q * 32;
         const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                 static_cast<uint32_t>(buf * MT * Cfg::BN + hc);
         float v[Cfg::CH];
@@ -492,7 +555,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
           // last TMEM read of this accumulator: hand it back to the MMA warp right away
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acce_bar[buf]);
+          if (lane == 0) {   // (a pair's accumulators are released on its first CTA's barrier)
+            if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(&acce_bar[buf]), 0));
+            else mbar_arrive(&acce_bar[buf]);
+          }
         }
         uint8_t* sb = wstage + sel * Cfg::EPI_BUF;
         sel ^= 1;
@@ -502,7 +568,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
         const int nops = epi(m0, n_row0 + c, b, s, v, sb, ops, pre);
         if (hc + Cfg::CH < ncols) {   // the next block's inputs, while this one stores
           const int hn = (hc + Cfg::CH) / Cfg::BN, cn = (hc + Cfg::CH) % Cfg::BN;
-          pre = epi.preload(tm * Cfg::BM_U + hn * Cfg::BM + q * 32, n_row0 + cn);
+          pre = epi.preload(m_base + hn * Cfg::BM + q * 32, n_row0 + cn);
         }
         if constexpr (Epi::kDirect) continue;   // written directly from registers
         fence_proxy_async_shared();
@@ -527,7 +593,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    Iter it(geo);
+    Iter it(geo, first_unit, unit_step);
     Frag f;
     while (ok && it.next(geo, f)) {
       for (int kb = f.kb0; kb < f.kb1; ++kb) {
@@ -557,7 +623,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    Iter it(geo);
+    Iter it(geo, first_unit, unit_step);
     Frag f;
     while (ok && it.next(geo, f)) {
       const int y0 = f.tn * Cfg::BN + f.b * geo.b_y_batch;
@@ -588,11 +654,24 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD>::THREADS, 1)
   }
 
   __syncthreads();
+  if constexpr (CG == 2) {
+    // After a timeout this CTA may still have loads in flight that complete on the other CTA's
+    // barriers: give them time to land (bounded) before the shared memory goes away.
+    if (*abort_flag) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 1000000ull) {
+      }
+    }
+    // both CTAs' epilogues have read their accumulators before the pair frees tensor memory
+    tc_fence_before_sync();
+    cluster_sync();
+  }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(err_word, kErrTimeout);
   if (threadIdx.x == 0) stamp(geo.stamps, geo.stamp_k, kStampEnd);
   if (warp == 2) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if constexpr (CG == 2) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
 }
 

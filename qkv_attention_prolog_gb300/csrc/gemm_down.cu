@@ -36,7 +36,10 @@ cudaError_t launch_down(const GemmLaunch& L, const DownParams& p) {
       default: return cudaErrorInvalidValue;
     }
   }
-  if (L.bn == 256) return launch_gemm_t<256>(L, EpiDown<false, 256, 32>{p});
+  if (L.bn == 256) {
+    if (L.cg == 2) return launch_gemm_t<256, 0, 1, 0, 2>(L, EpiDown<false, 256, 32>{p});
+    return launch_gemm_t<256>(L, EpiDown<false, 256, 32>{p});
+  }
   if (L.bn != 192) return cudaErrorInvalidValue;
   return launch_gemm_t<192>(L, EpiDown<false, 192, 32>{p});
 }

@@ -27,6 +27,7 @@ static cudaError_t launch_up_t(const GemmLaunch& L, const UpParams& p) {
   if (L.bn != 256) return cudaErrorInvalidValue;
   if constexpr (!INT8) {
     if (L.rr) return launch_gemm_t<256>(L, EpiUp<false, false, 32, true>{p});
+    if (L.cg == 2) return launch_gemm_t<256, 0, 1, 0, 2>(L, EpiUp<false, false, 32>{p});
   }
   return launch_gemm_t<256, WB>(L, EpiUp<false, INT8, 32>{p});
 }

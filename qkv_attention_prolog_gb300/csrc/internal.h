@@ -23,6 +23,7 @@ struct GemmLaunch {
   bool swap;
   bool a_int8;       // A operand is an int8 weight converted to bf16 in shared memory
   bool rr;           // row-range schedule with direct epilogue stores (decode, tokens as rows)
+  int cg;            // 2: CTA-pair tiles (256 rows of A, cta_group::2 MMAs); the grid counts CTAs
   int grid;
   cudaStream_t stream;
   bool pdl;

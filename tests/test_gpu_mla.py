@@ -54,6 +54,11 @@ SHAPES = [
     dict(B=3, S=100, He=384, Hcq=192, Hckv=128, N=2),  # T=300: prefill orientation, ragged M
     dict(B=1, S=200, He=320, Hcq=136, Hckv=96, N=2, Dr=32),  # ragged K, Hcq, Hckv tiles
     dict(B=40, S=1, He=256, Hcq=1536, N=16),         # 16 heads, deep K (fused decode kernel)
+    # from 1024 tokens the down- and up-projection run on CTA pairs (256-token tiles, each CTA
+    # half of a 256-row weight tile): ragged token tile, a W^DQ tile and a W^UQ|W^QR tile whose
+    # second half lies wholly past the weight rows
+    dict(B=3, S=400, He=512, Hcq=320, Hckv=128, N=3),
+    dict(B=2, S=512, He=384, Hcq=256, Hckv=256, N=2),  # T=1024: whole token tiles
 ]
 
 
