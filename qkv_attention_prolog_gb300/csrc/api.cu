@@ -814,9 +814,12 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     // an int8 query is quantised per token and head from a bf16 q^N staged in the workspace
     __nv_bfloat16* qn_out = d.query_int8 ? reinterpret_cast<__nv_bfloat16*>(wsb + L.qn)
                                          : static_cast<__nv_bfloat16*>(a->query.data);
+    // boxes of 32 tokens x 32 columns, or (tokens as rows, TMA stores) 32 x 64: whole lines
+    const bool wide = !b.swap && !ab_var;
     CHECK_STATUS(make_out_map(&b.o0, qn_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                              {d.Hckv, d.N, d.T}, {d.Hckv * 2, d.N * d.Hckv * 2}, {32, 1, b.swap ? ch_t : 32},
-                              CU_TENSOR_MAP_SWIZZLE_64B));
+                              {d.Hckv, d.N, d.T}, {d.Hckv * 2, d.N * d.Hckv * 2},
+                              {wide ? 64 : 32, 1, b.swap ? ch_t : 32},
+                              wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B));
     b.o1 = b.o0;
     AbsorbParams ap{ab_var ? qn_out : nullptr,
                     static_cast<int32_t>(d.T), static_cast<int32_t>(d.N),

@@ -65,6 +65,13 @@ __device__ __forceinline__ void stage_row_bf16x32(uint8_t* sb, int r, const floa
     *reinterpret_cast<uint4*>(sb + r * 64 + (((c ^ ((r >> 1) & 3)) & 3) << 4)) = pack_bf16x8(v + 8 * c);
 }
 
+// Lane-as-row writes of 64 consecutive values rounded to bf16 (8 chunks of 8, SWIZZLE_128B).
+__device__ __forceinline__ void stage_row_bf16x64(uint8_t* sb, int r, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(sb + r * 128 + (((c ^ (r & 7)) & 7) << 4)) = pack_bf16x8(v + 8 * c);
+}
+
 // Lane-as-row writes of 16 consecutive values rounded to bf16 (2 chunks of 8, SWIZZLE_32B).
 __device__ __forceinline__ void stage_row_bf16x16(uint8_t* sb, int r, const float* v) {
 #pragma unroll
@@ -94,6 +101,7 @@ struct DownParams {
 template <bool SWAP, int TILE_W, int CH>
 struct EpiDown {
   static constexpr bool kDirect = false;
+  static constexpr int kCols = CH;
   DownParams p;
   struct Pre {};
   __device__ __forceinline__ Pre preload(int, int) const { return {}; }
@@ -137,6 +145,7 @@ struct UpParams {
 template <bool SWAP, bool INT8, int CH, bool DIRECT = false>
 struct EpiUp {
   static constexpr bool kDirect = DIRECT;
+  static constexpr int kCols = CH;
   static_assert(!DIRECT || (!SWAP && !INT8), "direct stores: bf16 weight, tokens as MMA rows");
   UpParams p;
 
@@ -315,10 +324,14 @@ struct AbsorbParams {
   int32_t T, N, Hckv;
 };
 
+// CH = 64 (prefill, TMA stores): each lane stages 128 contiguous bytes of its token's row and one
+// store box covers 32 tokens x 64 columns, whole 128-byte lines of query.
 template <bool SWAP, int CH, bool DIRECT = false>
 struct EpiAbsorb {
   static constexpr bool kDirect = DIRECT;
+  static constexpr int kCols = CH;
   static_assert(!DIRECT || !SWAP, "direct stores: tokens as MMA rows");
+  static_assert(CH != 64 || (!SWAP && !DIRECT), "64-column chunks: TMA stores, tokens as rows");
   AbsorbParams p;
   struct Pre {};
   __device__ __forceinline__ Pre preload(int, int) const { return {}; }
@@ -341,7 +354,8 @@ struct EpiAbsorb {
         }
         return 0;
       }
-      stage_row_bf16x32(sb, lane, v);
+      if constexpr (CH == 64) stage_row_bf16x64(sb, lane, v);
+      else stage_row_bf16x32(sb, lane, v);
       ops[0] = {0, 3, n0, n, m0, 0};
     }
     return 1;

@@ -242,7 +242,8 @@ __device__ __forceinline__ void convert_int8_row(const uint8_t* src_row, uint8_t
 }
 
 // Epilogue functor contract (see epilogues.cuh):
-//   __device__ int operator()(int m0, int n0, int batch, int split, const float (&v)[CH],
+//   static constexpr int kCols;   // CH: the engine's chunk (32, or 16 when BN = 16), or 64
+//   __device__ int operator()(int m0, int n0, int batch, int split, const float (&v)[kCols],
 //                             uint8_t* stage, StoreOp (&ops)[2]) const;
 // called by all 32 lanes of an epilogue warp together for the 32 x CH accumulator block whose
 // first A row is m0 (lane l holds row m0 + l) and first B row is n0 (v[j] is column n0 + j).  It
@@ -261,6 +262,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
   constexpr bool RR = Epi::kDirect;   // the row-range launches are the direct-store ones
   static_assert(!(RR && CG == 2), "the row-range schedule runs on single CTAs");
   using Iter = FragIter<RR, BN>;
+  // epilogue column chunk: the engine's 32 (16 for BN = 16) unless the functor asks for 64 (one
+  // 128-byte bf16 row segment per lane and store)
+  constexpr int ECH = Epi::kCols;
+  static_assert(ECH == Cfg::CH || (ECH == 64 && Cfg::CH == 32 && BN % 64 == 0 && MT == 1),
+                "epilogue chunk");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -532,13 +538,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
       tc_fence_after_sync();
       if (q == 0 && lane == 0) stamp(geo.stamps, geo.stamp_k, kStampMain);
 #pragma unroll 1
-      for (int hc = 0; hc < ncols; hc += Cfg::CH) {
+      for (int hc = 0; hc < ncols; hc += ECH) {
         const int h = hc / Cfg::BN, c = hc % Cfg::BN;
         const int m0 = m_base + h * Cfg::BM + q * 32;
         const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                 static_cast<uint32_t>(buf * MT * Cfg::BN + hc);
-        float v[Cfg::CH];
-        if constexpr (Cfg::CH == 32) {
+        float v[ECH];
+        if constexpr (ECH == 64) {
+          uint32_t r[32], r2[32];
+          tmem_ld_32x32b_x32(t_addr, r);
+          tmem_ld_32x32b_x32(t_addr + 32, r2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] = __uint_as_float(r[j]);
+            v[32 + j] = __uint_as_float(r2[j]);
+          }
+        } else if constexpr (ECH == 32) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(t_addr, r);
           tmem_ld_wait();
@@ -551,7 +567,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
         }
-        if (hc + Cfg::CH >= ncols) {
+        if (hc + ECH >= ncols) {
           // last TMEM read of this accumulator: hand it back to the MMA warp right away
           tc_fence_before_sync();
           __syncwarp();
@@ -566,8 +582,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
         __syncwarp();
         StoreOp ops[2];
         const int nops = epi(m0, n_row0 + c, b, s, v, sb, ops, pre);
-        if (hc + Cfg::CH < ncols) {   // the next block's inputs, while this one stores
-          const int hn = (hc + Cfg::CH) / Cfg::BN, cn = (hc + Cfg::CH) % Cfg::BN;
+        if (hc + ECH < ncols) {   // the next block's inputs, while this one stores
+          const int hn = (hc + ECH) / Cfg::BN, cn = (hc + ECH) % Cfg::BN;
           pre = epi.preload(m_base + hn * Cfg::BM + q * 32, n_row0 + cn);
         }
         if constexpr (Epi::kDirect) continue;   // written directly from registers

@@ -20,7 +20,7 @@ cudaError_t launch_absorb(const GemmLaunch& L, const AbsorbParams& p) {
   }
   if (L.bn != 256) return cudaErrorInvalidValue;
   if (L.rr) return launch_gemm_t<256>(L, EpiAbsorb<false, 32, true>{p});
-  return launch_gemm_t<256>(L, EpiAbsorb<false, 32>{p});
+  return launch_gemm_t<256>(L, EpiAbsorb<false, 64>{p});   // whole 128-byte lines per store
 }
 
 }  // namespace mlap

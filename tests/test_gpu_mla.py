@@ -53,6 +53,7 @@ SHAPES = [
     dict(B=2, S=65, He=512, Hcq=256, N=3),            # T=130: BN 256, ragged rope tail (N*Dr)
     dict(B=3, S=100, He=384, Hcq=192, Hckv=128, N=2),  # T=300: prefill orientation, ragged M
     dict(B=1, S=200, He=320, Hcq=136, Hckv=96, N=2, Dr=32),  # ragged K, Hcq, Hckv tiles
+    dict(B=2, S=150, He=256, Hcq=128, Hckv=96, N=2, Dr=32),  # T=300: a query store box past Hckv
     dict(B=40, S=1, He=256, Hcq=1536, N=16),         # 16 heads, deep K (fused decode kernel)
     # from 1024 tokens the down- and up-projection run on CTA pairs (256-token tiles, each CTA
     # half of a 256-row weight tile): ragged token tile, a W^DQ tile and a W^UQ|W^QR tile whose
