@@ -510,7 +510,7 @@ def measure_mla(args, case, dev, stream, steps, warm, world, stamp_calls, sample
             "launches_per_call": launches}
 
 
-def _roofline(m, tensor_bound, hbm, tf_sus, peak_kind, workload):
+def _roofline(m, tensor_bound, hbm, tf_sus, peak_kind, workload, tf_burst=None):
     """Roofline entry of the dominant kernel: algorithmic bytes (FLOPs) per launch over its mean
     span inside the pipelined calls (earliest CTA start to latest CTA end).  The dominant kernel
     is the one with the longest time from its dependency wait to its end: under programmatic
@@ -522,7 +522,8 @@ def _roofline(m, tensor_bound, hbm, tf_sus, peak_kind, workload):
     if tensor_bound:
         achieved = kern[dominant]["flops"] / span_s / 1e12
         roof = {"bound": "tensor", "unit": "TFLOP/s", "peak": tf_sus,
-                "peak_note": "sustained bf16 (kernel timed inside a long step)"}
+                "peak_note": "sustained bf16 (kernel timed inside a long step)",
+                "frac_of_burst": round(achieved / tf_burst, 4) if tf_burst else None}
     else:
         achieved = kern[dominant]["bytes"] / span_s / 1e9
         roof = {"bound": "hbm", "unit": "GB/s", "peak": hbm}
@@ -567,7 +568,7 @@ def run_ours(args, rank, local, world):
     warm = max(3, args.warmup)
     m = measure_mla(args, case, dev, stream, steps, warm, world, args.stamp_calls)
     tensor_bound = args.workload == "prefill"
-    roof = _roofline(m, tensor_bound, hbm, tf_sus, peak_kind, args.workload)
+    roof = _roofline(m, tensor_bound, hbm, tf_sus, peak_kind, args.workload, tf_burst)
     path_roof = _path_roofline(m, hbm, tf_sus)
     e2e = run_e2e(args, case, m["cpu"], m["sets"][0], dev, stream)
     ms_step = m["ms_step"]
@@ -615,7 +616,7 @@ def run_prefill_leg(args, dev, stream, world, hbm, tf_burst, tf_sus, peak_kind):
     case = synthetic.MLA_PREFILL
     m = measure_mla(args, case, dev, stream, max(4, args.prefill_steps), 3, world,
                     min(16, args.stamp_calls))
-    roof = _roofline(m, True, hbm, tf_sus, peak_kind, "prefill")
+    roof = _roofline(m, True, hbm, tf_sus, peak_kind, "prefill", tf_burst)
     path_roof = _path_roofline(m, hbm, tf_sus)
     ms = m["ms_step"]
     out = {"workload": case.name, "us_per_call": round(ms * 1e3, 3),
