@@ -273,9 +273,10 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
 constexpr int kWarpTokens = 8;
 constexpr int kWarpMaxDr = 256;
 constexpr int kWarpNV = 17;   // Ntot <= 32 * 4 * 17 = 2176
+constexpr int kWarpMaxGamma = 32 * 4 * kWarpNV;   // Hcq + Hckv
 
-__device__ __forceinline__ void load4_bf16(const __nv_bfloat16* p, float* out) {
-  const uint2 r = __ldg(reinterpret_cast<const uint2*>(p));
+__device__ __forceinline__ void load4_bf16_smem(const __nv_bfloat16* p, float* out) {
+  const uint2 r = *reinterpret_cast<const uint2*>(p);
   const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&r);
 #pragma unroll
   for (int i = 0; i < 4; ++i) out[i] = __bfloat162float(e[i]);
@@ -292,159 +293,212 @@ __device__ __forceinline__ void store4_bf16(__nv_bfloat16* p, const float* v) {
 template <int NV>
 __global__ void __launch_bounds__(32 * kWarpTokens, 2) norm_rope_scatter_warp_kernel(
     const FinalizeParams p) {
+  // one slot per warp: the token's row (Ntot floats), then two buffers of its cos and sin rows
+  // (Dr bf16 each; fill k uses buffer k & 1, so the next token's tables cannot overwrite the ones
+  // this token's k^R still reads)
+  extern __shared__ __align__(16) float row_s[];
   __shared__ float kr_s[kWarpTokens][kWarpMaxDr];
+  __shared__ __align__(16) __nv_bfloat16 gamma_s[kWarpMaxGamma];      // gamma_cq | gamma_ckv
+  __shared__ uint64_t full[kWarpTokens];
+  __shared__ int abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarpTokens + warp;
-  if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampStart);
+  const int stride = gridDim.x * kWarpTokens;        // tokens per round of the grid
+  int t = blockIdx.x * kWarpTokens + warp;
+  const uint32_t row_bytes = static_cast<uint32_t>(p.Ntot) * 4u;   // (Ntot % 4 == 0)
+  const uint32_t tab_bytes = static_cast<uint32_t>(p.Dr) * 2u;     // (Dr % 8 == 0)
+  float* slot = row_s + static_cast<size_t>(warp) * (p.Ntot + 2 * p.Dr);
+  // the gammas are inputs of the call: into shared memory before the wait
+  for (int i = threadIdx.x; i < (p.Hcq + p.Hckv) / 8; i += 32 * kWarpTokens) {
+    const int f = 8 * i;
+    *reinterpret_cast<uint4*>(gamma_s + f) =
+        f < p.Hcq ? __ldg(reinterpret_cast<const uint4*>(p.gamma_cq + f))
+                  : __ldg(reinterpret_cast<const uint4*>(p.gamma_ckv + (f - p.Hcq)));
+  }
+  if (threadIdx.x == 0) {
+    stamp(p.stamps, MLAP_STAMP_NORM, kStampStart);
+    for (int i = 0; i < kWarpTokens; ++i) mbar_init(&full[i], 1);
+    abort_sh = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
   grid_launch_dependents();
-  // the cache index is an input of the call: read before the wait on the down-projection
-  int64_t idx = -1;
-  if (t < p.T && p.slots > 0) idx = p.cache_index[t];
   grid_dependency_wait();
   if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampDep);
-  if (t >= p.T) return;                              // warp-uniform
-
+  // the warp's token rows go through its slot: the next row is requested as soon as the current
+  // one is in registers, so its load overlaps this token's arithmetic and stores
+  auto request = [&](int tt, int fill) {
+    const bool tab = p.slots > 0;   // (the tables serve k^R, stored only with a cache)
+    mbar_arrive_expect_tx(&full[warp], row_bytes + (tab ? 2 * tab_bytes : 0u));
+    bulk_load_1d(slot, p.part + static_cast<size_t>(tt) * p.Ntot, row_bytes, &full[warp]);
+    if (tab) {
+      float* tb = slot + p.Ntot + (fill & 1) * p.Dr;
+      bulk_load_1d(tb, p.cos + static_cast<size_t>(tt) * p.Dr, tab_bytes, &full[warp]);
+      bulk_load_1d(tb + p.Dr / 2, p.sin + static_cast<size_t>(tt) * p.Dr, tab_bytes, &full[warp]);
+    }
+  };
+  int fills = 0;
+  if (t < p.T) {
+    if (lane == 0) request(t, 0);
+    fills = 1;
+  }
   const int n4 = p.Ntot >> 2, q4 = p.Hcq >> 2, kv4 = (p.Hcq + p.Hckv) >> 2;
-  const float4* src = reinterpret_cast<const float4*>(p.part + static_cast<size_t>(t) * p.Ntot);
-  float4 v[NV];
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int c = lane + 32 * i;
-    v[i] = c < n4 ? __ldg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  if (p.dsx != nullptr) {   // full quant: dequant the exact integer products per token and column
-    const float sx = p.dsx[t];
+  for (int k = 0; t < p.T; ++k, t += stride) {
+    const int64_t idx = p.slots > 0 ? p.cache_index[t] : -1;
+    const bool landed = mbar_wait(&full[warp], static_cast<uint32_t>(k & 1), &abort_sh);
+    if (!__all_sync(0xffffffffu, landed)) break;
+    float4 v[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int c = lane + 32 * i;
-      if (c < n4) {   // (dsw_kv covers the c^KV and the k^R columns)
-        const float* w = c < q4 ? p.dsw_q + 4 * c : p.dsw_kv + 4 * (c - q4);
-        v[i].x *= sx * w[0];
-        v[i].y *= sx * w[1];
-        v[i].z *= sx * w[2];
-        v[i].w *= sx * w[3];
-      }
+      v[i] = c < n4 ? reinterpret_cast<const float4*>(slot)[c] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-  }
-  float sq = 0.f, skv = 0.f;
+    if (p.dsx != nullptr) {   // full quant: dequant the exact integer products per token and column
+      const float sx = p.dsx[t];
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int c = lane + 32 * i;
-    const float s4 = v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
-    if (c < q4) sq += s4;
-    else if (c < kv4) skv += s4;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    skv += __shfl_xor_sync(0xffffffffu, skv, o);
-  }
-  const float rq = 1.0f / sqrtf(sq / static_cast<float>(p.Hcq) + p.eps_cq);
-  const float rkv = 1.0f / sqrtf(skv / static_cast<float>(p.Hckv) + p.eps_ckv);
-
-  // ---- c^Q: bf16, or int8 codes held exactly in bf16
-  __nv_bfloat16* cq = p.cq_out + static_cast<size_t>(t) * p.Hcq;
-  if (p.smooth == nullptr) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int c = lane + 32 * i;
-      if (c < q4) {
-        float g[4], o[4];
-        load4_bf16(p.gamma_cq + 4 * c, g);
-        o[0] = v[i].x * rq * g[0];
-        o[1] = v[i].y * rq * g[1];
-        o[2] = v[i].z * rq * g[2];
-        o[3] = v[i].w * rq * g[3];
-        store4_bf16(cq + 4 * c, o);
-      }
-    }
-  } else {
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int c = lane + 32 * i;
-      if (c < q4) {
-        float* e = reinterpret_cast<float*>(&v[i]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int f = 4 * c + k;
-          const float cv = __bfloat162float(
-              __float2bfloat16_rn(e[k] * rq * __bfloat162float(p.gamma_cq[f])));
-          e[k] = __fmul_rn(cv, p.smooth[f]);
-          amax = fmaxf(amax, fabsf(e[k]));
+      for (int i = 0; i < NV; ++i) {
+        const int c = lane + 32 * i;
+        if (c < n4) {   // (dsw_kv covers the c^KV and the k^R columns)
+          const float* w = c < q4 ? p.dsw_q + 4 * c : p.dsw_kv + 4 * (c - q4);
+          v[i].x *= sx * w[0];
+          v[i].y *= sx * w[1];
+          v[i].z *= sx * w[2];
+          v[i].w *= sx * w[3];
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = __fdiv_rn(amax, 127.0f);
+    float sq = 0.f, skv = 0.f;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int c = lane + 32 * i;
-      if (c < q4) {
-        const float* e = reinterpret_cast<const float*>(&v[i]);
-        float o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          o[k] = static_cast<float>(scale > 0.f ? quant_i8(e[k], scale, -127, 127) : 0);
-        store4_bf16(cq + 4 * c, o);               // exact: |code| <= 127
-      }
+      const float s4 = v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+      if (c < q4) sq += s4;
+      else if (c < kv4) skv += s4;
     }
-    if (lane == 0) p.scale_t[t] = scale;
-  }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      skv += __shfl_xor_sync(0xffffffffu, skv, o);
+    }
+    const float rq = 1.0f / sqrtf(sq / static_cast<float>(p.Hcq) + p.eps_cq);
+    const float rkv = 1.0f / sqrtf(skv / static_cast<float>(p.Hckv) + p.eps_ckv);
+    // every lane's reads of the slot have completed (the sums above consumed them): the slot
+    // takes the next row while this one is normalised and stored
+    __syncwarp();
+    if (t + stride < p.T) {
+      if (lane == 0) request(t + stride, k + 1);
+      ++fills;
+    }
 
-  auto finish = [&]() {
-    if (lane == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampEnd);
-  };
-  if (p.slots <= 0) {                              // empty caches: outputs only
-    finish();
-    return;
-  }
-  if (idx < 0 || idx >= p.slots) {
-    if (idx != -1 && lane == 0) atomicOr(p.err, kErrIndexRange);
-    finish();
-    return;
-  }
-  // ---- c^KV, and k^R into this warp's shared row for the RoPE partner exchange
-  float* kr = kr_s[warp];
+    // ---- c^Q: bf16, or int8 codes held exactly in bf16
+    __nv_bfloat16* cq = p.cq_out + static_cast<size_t>(t) * p.Hcq;
+    if (p.smooth == nullptr) {
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int c = lane + 32 * i;
-    if (c >= q4 && c < kv4) {
-      const int f = 4 * (c - q4);
-      float g[4], o[4];
-      load4_bf16(p.gamma_ckv + f, g);
-      o[0] = v[i].x * rkv * g[0];
-      o[1] = v[i].y * rkv * g[1];
-      o[2] = v[i].z * rkv * g[2];
-      o[3] = v[i].w * rkv * g[3];
-      if (p.kv_int8) {
-        uint32_t q;
-        int8_t* qb = reinterpret_cast<int8_t*>(&q);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) qb[k] = quant_i8(o[k], p.qs_ckv[f + k], -128, 127);
-        *reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.kv_cache) + idx * p.Hckv + f) = q;
-      } else {
-        store4_bf16(static_cast<__nv_bfloat16*>(p.kv_cache) + idx * p.Hckv + f, o);
+      for (int i = 0; i < NV; ++i) {
+        const int c = lane + 32 * i;
+        if (c < q4) {
+          float g[4], o[4];
+          load4_bf16_smem(gamma_s + 4 * c, g);
+          o[0] = v[i].x * rq * g[0];
+          o[1] = v[i].y * rq * g[1];
+          o[2] = v[i].z * rq * g[2];
+          o[3] = v[i].w * rq * g[3];
+          store4_bf16(cq + 4 * c, o);
+        }
       }
-    } else if (c >= kv4 && c < n4) {
-      *reinterpret_cast<float4*>(kr + 4 * (c - kv4)) = v[i];
+    } else {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int c = lane + 32 * i;
+        if (c < q4) {
+          float* e = reinterpret_cast<float*>(&v[i]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int f = 4 * c + k;
+            const float cv = __bfloat162float(
+                __float2bfloat16_rn(e[k] * rq * __bfloat162float(gamma_s[f])));
+            e[k] = __fmul_rn(cv, p.smooth[f]);
+            amax = fmaxf(amax, fabsf(e[k]));
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float scale = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int c = lane + 32 * i;
+        if (c < q4) {
+          const float* e = reinterpret_cast<const float*>(&v[i]);
+          float o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            o[k] = static_cast<float>(scale > 0.f ? quant_i8(e[k], scale, -127, 127) : 0);
+          store4_bf16(cq + 4 * c, o);               // exact: |code| <= 127
+        }
+      }
+      if (lane == 0) p.scale_t[t] = scale;
+    }
+
+    if (p.slots <= 0) continue;                     // empty caches: outputs only
+    if (idx < 0 || idx >= p.slots) {
+      if (idx != -1 && lane == 0) atomicOr(p.err, kErrIndexRange);
+      continue;
+    }
+    // ---- c^KV, and k^R into this warp's shared row for the RoPE partner exchange
+    float* kr = kr_s[warp];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c = lane + 32 * i;
+      if (c >= q4 && c < kv4) {
+        const int f = 4 * (c - q4);
+        float g[4], o[4];
+        load4_bf16_smem(gamma_s + p.Hcq + f, g);
+        o[0] = v[i].x * rkv * g[0];
+        o[1] = v[i].y * rkv * g[1];
+        o[2] = v[i].z * rkv * g[2];
+        o[3] = v[i].w * rkv * g[3];
+        if (p.kv_int8) {
+          uint32_t q;
+          int8_t* qb = reinterpret_cast<int8_t*>(&q);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) qb[k] = quant_i8(o[k], p.qs_ckv[f + k], -128, 127);
+          *reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.kv_cache) + idx * p.Hckv + f) = q;
+        } else {
+          store4_bf16(static_cast<__nv_bfloat16*>(p.kv_cache) + idx * p.Hckv + f, o);
+        }
+      } else if (c >= kv4 && c < n4) {
+        *reinterpret_cast<float4*>(kr + 4 * (c - kv4)) = v[i];
+      }
+    }
+    __syncwarp();
+    const int half = p.Dr >> 1;
+    for (int j = lane; j < p.Dr; j += 32) {
+      const float y = kr[j];
+      const float partner = j < half ? -kr[j + half] : kr[j - half];
+      const __nv_bfloat16* tb =
+          reinterpret_cast<const __nv_bfloat16*>(slot + p.Ntot + (k & 1) * p.Dr);
+      const float c = __bfloat162float(tb[j]);
+      const float s = __bfloat162float(tb[p.Dr + j]);
+      const float o = y * c + partner * s;
+      if (p.kr_int8)
+        static_cast<int8_t*>(p.kr_cache)[idx * p.Dr + j] = quant_i8(o, p.qs_ckr[j], -128, 127);
+      else
+        static_cast<__nv_bfloat16*>(p.kr_cache)[idx * p.Dr + j] = __float2bfloat16_rn(o);
     }
   }
-  __syncwarp();
-  const int half = p.Dr >> 1;
-  for (int j = lane; j < p.Dr; j += 32) {
-    const float y = kr[j];
-    const float partner = j < half ? -kr[j + half] : kr[j - half];
-    const float c = __bfloat162float(p.cos[static_cast<size_t>(t) * p.Dr + j]);
-    const float s = __bfloat162float(p.sin[static_cast<size_t>(t) * p.Dr + j]);
-    const float o = y * c + partner * s;
-    if (p.kr_int8)
-      static_cast<int8_t*>(p.kr_cache)[idx * p.Dr + j] = quant_i8(o, p.qs_ckr[j], -128, 127);
-    else
-      static_cast<__nv_bfloat16*>(p.kr_cache)[idx * p.Dr + j] = __float2bfloat16_rn(o);
+  if (abort_sh && lane == 0 && fills > 0) {
+    // let this warp's last request land before the CTA exits (bounded)
+    const uint32_t par = static_cast<uint32_t>(fills - 1) & 1u;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&full[warp], par) && globaltimer_ns() - t0 < 20000000ull) {
+    }
   }
-  finish();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (abort_sh) atomicOr(p.err, kErrTimeout);
+    stamp(p.stamps, MLAP_STAMP_NORM, kStampEnd);
+  }
 }
 
 // dst[b][i][k] = src[b][k][perm(i)], 32x32 tiles through shared memory.
@@ -681,9 +735,30 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool p
   const bool split = p.splits > 1;
   if (!split && p.Ntot <= 32 * 4 * kWarpNV && p.Dr <= kWarpMaxDr) {
     // (Hcq, Hckv and Dr are multiples of 8: every float4 of a row lies in one part)
-    return launch_k(norm_rope_scatter_warp_kernel<kWarpNV>,
-                    dim3(static_cast<unsigned>((p.T + kWarpTokens - 1) / kWarpTokens)),
-                    dim3(32 * kWarpTokens), stream, pdl, p);
+    auto wk = norm_rope_scatter_warp_kernel<kWarpNV>;
+    const size_t wsmem = static_cast<size_t>(kWarpTokens) * (p.Ntot + 2 * p.Dr) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(wk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(wsmem));
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // persistent: two CTAs per SM (the register budget), no more than the tokens need
+    int64_t blocks = 2 * static_cast<int64_t>(sms);
+    const int64_t need = (p.T + kWarpTokens - 1) / kWarpTokens;
+    if (blocks > need) blocks = need;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(32 * kWarpTokens);
+    cfg.dynamicSmemBytes = wsmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, wk, p);
   }
   // up to 8 K-splits (decode): two CTAs per token, c^Q and c^KV/k^R
   const bool parts = split && p.splits <= 8;
