@@ -805,6 +805,9 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     b.geo.a_seg_tiles = b.geo.m_tiles;
     b.geo.b_seg_tiles = b.geo.n_tiles;
     b.geo.batches = static_cast<int32_t>(d.N);
+    // tokens as rows: the two W^UK column tiles of a q^C tile run side by side, so the second
+    // read of each q^C tile hits in L2
+    if (!b.swap && !ab_var) b.geo.n_fast = 1;
     b.geo.splits = 1;
     b.geo.w_op = b.swap ? 0 : 1;
     b.geo.k_blocks = ceil_div(d.D, 64);
