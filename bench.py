@@ -111,12 +111,13 @@ def _peaks():
 
 
 # Sources of each timed kernel: a recorded DRAM traffic figure stays valid while they are unchanged.
-KERNEL_SOURCES = {
-    "up_absorb": ["up_absorb.cu", "ptx.cuh"],
-    "down": ["gemm_down.cu", "gemm.cuh", "epilogues.cuh", "gemm_launch.cuh", "ptx.cuh"],
-    "up": ["gemm_up.cu", "gemm.cuh", "epilogues.cuh", "gemm_launch.cuh", "ptx.cuh"],
-    "absorb": ["gemm_absorb.cu", "gemm.cuh", "epilogues.cuh", "gemm_launch.cuh", "ptx.cuh"],
-    "norm_scatter": ["mla_norm_scatter.cu"],
+KERNEL_SOURCES = {   # (api.cu sets each MLA kernel's grid, schedule and unit order)
+    "up_absorb": ["up_absorb.cu", "ptx.cuh", "api.cu"],
+    "down": ["gemm_down.cu", "gemm.cuh", "epilogues.cuh", "gemm_launch.cuh", "ptx.cuh", "api.cu"],
+    "up": ["gemm_up.cu", "gemm.cuh", "epilogues.cuh", "gemm_launch.cuh", "ptx.cuh", "api.cu"],
+    "absorb": ["gemm_absorb.cu", "gemm.cuh", "epilogues.cuh", "gemm_launch.cuh", "ptx.cuh",
+               "api.cu"],
+    "norm_scatter": ["mla_norm_scatter.cu", "api.cu"],
     "qkv_rnrc": ["qkv_rnrc.cu"],
 }
 
