@@ -55,32 +55,9 @@ struct UaCfg {
   static constexpr int SMEM = kUaSmemMax;
 };
 constexpr uint32_t kUaUpCol = 256;                     // TMEM column of the up accumulator
-#ifdef MLAP_UA_TRACE   // pipeline timeline of one CTA into spare words of its stamps slot
-#define UA_TRACE(slot, i)                                                                         \
-  do {                                                                                            \
-    if (p.stamps != nullptr && (blockIdx.x == MLAP_UA_TRACE || blockIdx.x == MLAP_UA_TRACE2) &&  \
-        (i) < 40)                                                                                 \
-      p.stamps[MLAP_STAMP_UP * MLAP_STAMP_BLOCK + 700 + (blockIdx.x == MLAP_UA_TRACE ? 0 : 140) + \
-               (slot) * 40 + (i)] = globaltimer_ns();                                            \
-  } while (0)
-#else
-#define UA_TRACE(slot, i) \
-  do {                    \
-  } while (0)
-#endif
-// Weight k-blocks (after those prefetched into the pipeline stages) that each CTA asks L2 to
-// prefetch before it waits for the kernel ahead of it, and whether the head's W^UK follows: the
-// DRAM is otherwise idle while that kernel (the RmsNorm step) runs.
-// Operand stages whose weight tiles are requested before the wait on the preceding kernel.
-#ifndef MLAP_UA_PRE_STAGES
-#define MLAP_UA_PRE_STAGES 4
-#endif
-#ifndef MLAP_UA_L2_KBLOCKS
-#define MLAP_UA_L2_KBLOCKS 0
-#endif
-#ifndef MLAP_UA_L2_UK
-#define MLAP_UA_L2_UK 0
-#endif
+// Operand stages whose weight tiles are requested before the wait on the preceding kernel (six
+// were slower: their loads queue ahead of the preceding kernels' own in DRAM).
+constexpr int kUaPreStages = 4;
 constexpr int kD = 128;
 constexpr int kDr = 64;
 
@@ -241,19 +218,8 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       }
     };
     int pre = kb_up < kUaStages ? kb_up : kUaStages;
-    if (pre > MLAP_UA_PRE_STAGES) pre = MLAP_UA_PRE_STAGES;
+    if (pre > kUaPreStages) pre = kUaPreStages;
     for (int i = 0; i < pre; ++i) issue_w(i, i);      // weights do not depend on earlier kernels
-    if constexpr (!INT8) {   // (int8 weight tiles: the raw producer prefetches them)
-      const int kl2 = pre + MLAP_UA_L2_KBLOCKS < kb_up ? pre + MLAP_UA_L2_KBLOCKS : kb_up;
-      for (int kb = pre; kb < kl2; ++kb)
-#pragma unroll
-        for (int j = 0; j < 6; ++j)
-          if (j < nbox) tma_prefetch_l2_2d(&tmW, kb * kUaBK, ybox[j]);
-    }
-    if (MLAP_UA_L2_UK && pl.head)
-      for (int r = 0; r < p.Hckv; r += 32)
-        for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2)
-          tma_prefetch_l2_2d(&tmUk, kb2 * kUaBK, n * p.Hckv + r);
     grid_dependency_wait();
     stamp(p.stamps, MLAP_STAMP_UP, kStampDep);
     int stage = 0;
@@ -267,7 +233,6 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         }
         issue_w(stage, kb);
       }
-      UA_TRACE(0, kb);
       mbar_arrive_expect_tx(&full_bar[stage], kUaA);
       tma_load_2d(stages + stage * kUaStage, &tmCq, &full_bar[stage], kb * kUaBK, 0);
       ++fills[stage];
@@ -285,7 +250,6 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
           break;
         }
         uint8_t* b = stages + stage * kUaStage + kUaA;
-        UA_TRACE(0, kb_up + h * 2 + kb2);
         mbar_arrive_expect_tx(&full_bar[stage], rows * kUaBK * 2);
         for (int r = 0; r < rows; r += 32)
           tma_load_2d(b + r * 128, &tmUk, &full_bar[stage], kb2 * kUaBK,
@@ -322,14 +286,6 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     int rs = 0;
     uint32_t rph = 0;
     for (int kb = 0; kb < kb_up; ++kb) {
-      if (kb == kRS) {
-        // the ring is full: ask L2 for the next k-blocks while the converters catch up
-        const int kl2 = kRS + MLAP_UA_L2_KBLOCKS < kb_up ? kRS + MLAP_UA_L2_KBLOCKS : kb_up;
-        for (int k2 = kRS; k2 < kl2; ++k2)
-#pragma unroll
-          for (int j = 0; j < 6; ++j)
-            if (j < nbox) tma_prefetch_l2_2d(&tmW, k2 * kUaBK, ybox[j]);
-      }
       if (kb >= kRS && !mbar_wait(&rawe_bar[rs], rph ^ 1u, abort_flag)) break;
       uint8_t* r = ring_raw + rs * kRawB;
       mbar_arrive_expect_tx(&rawf_bar[rs], static_cast<uint32_t>(up_rows) * kUaBK);
@@ -363,7 +319,6 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
           ok = false;
           break;
         }
-        UA_TRACE(1, kb);
         tc_fence_after_sync();
         const uint32_t a = smem_u32(stages + stage * kUaStage);
         const uint32_t b = a + kUaA;
@@ -379,7 +334,6 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       }
       if (ok) umma_commit(up_bar);
       if (ok && pl.head) ok = mbar_wait(qc_bar, 0, abort_flag);   // q^C staged, acc read
-      UA_TRACE(2, 0);
       if (ok && pl.head) {
         tc_fence_after_sync();
         const uint32_t qa[2] = {smem_u32(qc0), smem_u32(qc1)};
@@ -391,7 +345,6 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
               ok = false;
               break;
             }
-            UA_TRACE(1, kb_up + h * 2 + kb2);
             tc_fence_after_sync();
             const uint32_t b = smem_u32(stages + stage * kUaStage) + kUaA;
 #pragma unroll
@@ -556,7 +509,6 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
             ok = false;
             break;
           }
-          if (q == 0 && lane == 0) UA_TRACE(2, 1 + waited);
           ++waited;
         }
         if (!ok) break;
