@@ -205,10 +205,8 @@ struct FragIter {
   }
 };
 
-// One row of an int8 weight tile (64 values, 64 B) to bf16 in the 128B-swizzled K-major layout
-// (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7)) << 4)).  The four source chunks are visited
-// in a row-dependent order to spread shared-memory banks.  Conversion by the 2^23 magic number:
-// with u = v + 128 in [0, 255], the fp32 with bits 0x4B000000 | u is 2^23 + u exactly, so one
+// int8 to bf16 by the 2^23 magic number: with u = v + 128 in [0, 255], the fp32 with bits
+// 0x4B000000 | u is 2^23 + u exactly, so one
 // byte permute and one add give v in fp32 (exact); a bf16 holds every |v| <= 128 exactly, so the
 // upper half of the fp32 is the bf16.  This keeps the conversion on the full-rate ALU and FMA
 // pipes.
@@ -219,25 +217,26 @@ __device__ __forceinline__ uint32_t int8x2_to_bf16x2(uint32_t biased, int k0) {
   return __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
 }
 
-__device__ __forceinline__ void convert_int8_row(const uint8_t* src_row, uint8_t* dst, int r) {
+// Source chunk q of an int8 weight tile (64-B rows, four 16-B chunks each: row q / 4, chunk q % 4)
+// to bf16 in the 128B-swizzled K-major layout (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7))
+// << 4)).  The converter threads take consecutive chunks, so a warp's loads read 512 contiguous
+// bytes and every thread has the same share of the tile whatever its row count.
+__device__ __forceinline__ void convert_int8_chunk(const uint8_t* raw, uint8_t* dst, int q) {
+  const int r = q >> 2, i = q & 3;
+  const uint4 v = *reinterpret_cast<const uint4*>(raw + q * 16);
+  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                         v.w ^ 0x80808080u};
+  uint32_t out[8];
 #pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
-    const int i = (ii + r) & 3;
-    const uint4 raw = *reinterpret_cast<const uint4*>(src_row + i * 16);
-    const uint32_t w[4] = {raw.x ^ 0x80808080u, raw.y ^ 0x80808080u, raw.z ^ 0x80808080u,
-                           raw.w ^ 0x80808080u};
-    uint32_t out[8];
+  for (int k = 0; k < 4; ++k) {
+    out[2 * k] = int8x2_to_bf16x2(w[k], 0);
+    out[2 * k + 1] = int8x2_to_bf16x2(w[k], 2);
+  }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      out[2 * k] = int8x2_to_bf16x2(w[k], 0);
-      out[2 * k + 1] = int8x2_to_bf16x2(w[k], 2);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int c = 2 * i + h;
-      *reinterpret_cast<uint4*>(dst + r * 128 + (((c ^ (r & 7)) & 7) << 4)) =
-          make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
-    }
+  for (int h = 0; h < 2; ++h) {
+    const int c = 2 * i + h;
+    *reinterpret_cast<uint4*>(dst + r * 128 + (((c ^ (r & 7)) & 7) << 4)) =
+        make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
   }
 }
 
@@ -619,7 +618,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
         }
         const uint8_t* raw = smemR + stage * Cfg::RAW_BYTES;
         uint8_t* dst = WQ == 1 ? smemA + stage * Cfg::A_BYTES : smemB + stage * Cfg::B_BYTES;
-        for (int r = ct; r < Cfg::RAW_ROWS; r += 128) convert_int8_row(raw + r * Cfg::BK, dst, r);
+        for (int q = ct; q < Cfg::RAW_ROWS * 4; q += 128) convert_int8_chunk(raw, dst, q);
         fence_proxy_async_shared();              // generic writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_bar[stage]);

@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       }
       const uint8_t* raw = ring_raw + rs * kRawB;
       uint8_t* dst = stages + stage * kUaStage + kUaA;
-      for (int r = ct; r < up_rows; r += 128) convert_int8_row(raw + r * kUaBK, dst, r);
+      for (int q = ct; q < up_rows * 4; q += 128) convert_int8_chunk(raw, dst, q);
       fence_proxy_async_shared();                      // generic writes -> the tensor core
       __syncwarp();
       if (lane == 0) {
