@@ -514,7 +514,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   g.mt = swap ? mt : 1;
   DownParams dp{0};
   const int ch_t = swap ? (bn_t < 32 ? bn_t : 32) : 32;   // tokens per epilogue store box
-  // full quant: the int8 activation is widened to bf16 first (exact), the int8 weights are
+  // full quant: the int8 activation is widened to f16 first (exact), the int8 weights are
   // expanded in shared memory by the GEMM's converter warps, and the integer products are
   // dequantised per token and column after the K-split sum (norm kernel)
   const void* xact = d.full || d.xnorm ? static_cast<const void*>(wsb + L.xb) : a->token_x.data;
@@ -593,7 +593,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
     }
     if (d.full) {
       ce = launch_widen_int8(static_cast<const int8_t*>(a->token_x.data),
-                             reinterpret_cast<__nv_bfloat16*>(wsb + L.xb), d.T * d.He, stream);
+                             reinterpret_cast<__half*>(wsb + L.xb), d.T * d.He, stream);
       if (ce != cudaSuccess) return cuda_fail(ce, "token_x widening launch");
     }
     ce = launch_down(g, dp);

@@ -126,7 +126,8 @@ struct GemmCfg {
   static constexpr int ACC_COLS = 2 * MT * BN;         // double-buffered accumulators
   static constexpr uint32_t TMEM_COLS =
       ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM * CG, BN);
+  // int8 weights run in f16 (the converters' output and the int8 paths' activations), else bf16
+  static constexpr uint32_t IDESC = WQ ? idesc_f16_f32(BM * CG, BN) : idesc_bf16_f32(BM * CG, BN);
   static constexpr int THREADS = (WQ || ALD) ? 384 : 256;
   static constexpr uint32_t FULL_ARRIVALS = WQ ? 1 + 4 : (ALD ? 1 + 128 : 1);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16,256]");
@@ -205,20 +206,21 @@ struct FragIter {
   }
 };
 
-// int8 to bf16 by the 2^23 magic number: with u = v + 128 in [0, 255], the fp32 with bits
-// 0x4B000000 | u is 2^23 + u exactly, so one
-// byte permute and one add give v in fp32 (exact); a bf16 holds every |v| <= 128 exactly, so the
-// upper half of the fp32 is the bf16.  This keeps the conversion on the full-rate ALU and FMA
-// pipes.
-__device__ __forceinline__ uint32_t int8x2_to_bf16x2(uint32_t biased, int k0) {
-  const float f0 = __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7540u | k0)) - 8388736.0f;
-  const float f1 =
-      __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7540u | (k0 + 1))) - 8388736.0f;
-  return __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
+// int8 to f16 by the 2^10 magic number: with u = v + 128 in [0, 255] (v XOR 0x80 per byte), the
+// f16 with bits 0x6400 | u is 1024 + u exactly (f16 has 10 mantissa bits), so one byte permute
+// builds two such halves and one packed f16 subtraction of 1024 + 128 gives v exactly.  The int8
+// paths therefore run their MMAs with f16 operands (the c^Q codes and the widened token_x are
+// integers of magnitude <= 128 too, exact in f16): one permute and one packed subtract per two
+// values, on the full-rate pipes.
+__device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t biased, uint32_t sel) {
+  const uint32_t h = __byte_perm(biased, 0x64646464u, sel);
+  __half2 v = *reinterpret_cast<const __half2*>(&h);
+  v = __hsub2(v, __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6480u))));
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Source chunk q of an int8 weight tile (64-B rows, four 16-B chunks each: row q / 4, chunk q % 4)
-// to bf16 in the 128B-swizzled K-major layout (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7))
+// to f16 in the 128B-swizzled K-major layout (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7))
 // << 4)).  The converter threads take consecutive chunks, so a warp's loads read 512 contiguous
 // bytes and every thread has the same share of the tile whatever its row count.
 __device__ __forceinline__ void convert_int8_chunk(const uint8_t* raw, uint8_t* dst, int q) {
@@ -229,8 +231,8 @@ __device__ __forceinline__ void convert_int8_chunk(const uint8_t* raw, uint8_t* 
   uint32_t out[8];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    out[2 * k] = int8x2_to_bf16x2(w[k], 0);
-    out[2 * k + 1] = int8x2_to_bf16x2(w[k], 2);
+    out[2 * k] = int8x2_to_f16x2(w[k], 0x4140u);       // bytes 0, 1
+    out[2 * k + 1] = int8x2_to_f16x2(w[k], 0x4342u);   // bytes 2, 3
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {

@@ -79,7 +79,7 @@ struct FinalizeParams {
   int32_t kv_int8, kr_int8;
   const float* qs_ckv;
   const float* qs_ckr;
-  __nv_bfloat16* cq_out;       // (T, Hcq): bf16 c^Q, or int8 codes held exactly in bf16
+  __nv_bfloat16* cq_out;       // (T, Hcq): bf16 c^Q, or int8 codes held exactly in f16 bits
   const float* smooth;         // non-null: quantise c^Q per token
   float* scale_t;              // (T) per-token scale of the quantised c^Q
   uint32_t* err;
@@ -99,8 +99,8 @@ cudaError_t launch_rms_norm_quant(const __nv_bfloat16* x, const __nv_bfloat16* g
                                   float eps, __nv_bfloat16* out, int64_t T, int32_t He,
                                   cudaStream_t stream);
 
-// Full quant: int8 token_x widened to bf16 (exact), n elements (a multiple of 16).
-cudaError_t launch_widen_int8(const int8_t* x, __nv_bfloat16* out, int64_t n, cudaStream_t stream);
+// Full quant: int8 token_x widened to f16 (exact), n elements (a multiple of 16).
+cudaError_t launch_widen_int8(const int8_t* x, __half* out, int64_t n, cudaStream_t stream);
 
 // int8 query per token and head: rows of H bf16 values -> int8 codes (scale = amax / 127, round
 // half to even, clamp to [-127, 127]) and the per-row fp32 scale (dequant_scale_q_nope).

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   const float rq = 1.0f / sqrtf(ss.x / static_cast<float>(p.Hcq) + p.eps_cq);
   const float rkv = 1.0f / sqrtf(ss.y / static_cast<float>(p.Hckv) + p.eps_ckv);
 
-  // ---- c^Q (Hcq % 8 == 0): bf16, or int8 codes held exactly in bf16
+  // ---- c^Q (Hcq % 8 == 0): bf16, or int8 codes held exactly in f16
   __nv_bfloat16* cq = p.cq_out + static_cast<size_t>(t) * p.Hcq;
   if (!do_q) {
     // (the c^KV / k^R CTA of a token)
@@ -209,7 +209,8 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     const float scale = __fdiv_rn(amax, 127.0f);
     for (int f = threadIdx.x; f < p.Hcq; f += NT) {
       const int code = scale > 0.f ? quant_i8(h[f], scale, -127, 127) : 0;
-      cq[f] = __float2bfloat16_rn(static_cast<float>(code));   // exact: |code| <= 127
+      // f16, the operand type of the int8-weight MMAs (exact: |code| <= 127)
+      reinterpret_cast<__half*>(cq)[f] = __int2half_rn(code);
     }
     if (threadIdx.x == 0) p.scale_t[t] = scale;
   }
@@ -280,6 +281,14 @@ __device__ __forceinline__ void load4_bf16_smem(const __nv_bfloat16* p, float* o
   const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&r);
 #pragma unroll
   for (int i = 0; i < 4; ++i) out[i] = __bfloat162float(e[i]);
+}
+
+__device__ __forceinline__ void store4_f16(__half* p, const float* v) {
+  uint2 r;
+  __half2* e = reinterpret_cast<__half2*>(&r);
+  e[0] = __floats2half2_rn(v[0], v[1]);
+  e[1] = __floats2half2_rn(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) = r;
 }
 
 __device__ __forceinline__ void store4_bf16(__nv_bfloat16* p, const float* v) {
@@ -389,7 +398,7 @@ __global__ void __launch_bounds__(32 * kWarpTokens, 2) norm_rope_scatter_warp_ke
       ++fills;
     }
 
-    // ---- c^Q: bf16, or int8 codes held exactly in bf16
+    // ---- c^Q: bf16, or int8 codes held exactly in f16
     __nv_bfloat16* cq = p.cq_out + static_cast<size_t>(t) * p.Hcq;
     if (p.smooth == nullptr) {
 #pragma unroll
@@ -434,7 +443,7 @@ __global__ void __launch_bounds__(32 * kWarpTokens, 2) norm_rope_scatter_warp_ke
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             o[k] = static_cast<float>(scale > 0.f ? quant_i8(e[k], scale, -127, 127) : 0);
-          store4_bf16(cq + 4 * c, o);               // exact: |code| <= 127
+          store4_f16(reinterpret_cast<__half*>(cq) + 4 * c, o);   // f16 codes (exact)
         }
       }
       if (lane == 0) p.scale_t[t] = scale;
@@ -536,19 +545,21 @@ __global__ void prepack_kernel(const PrepackParams p) {
   }
 }
 
-// Full quant: 16 int8 values -> 16 bf16 per thread and step (exact: |v| <= 128).
-__global__ void widen_int8_kernel(const int8_t* __restrict__ x, __nv_bfloat16* __restrict__ out,
+// Full quant: 16 int8 values -> 16 f16 per thread and step (exact: |v| <= 128), the operand type
+// of the int8-weight MMAs.
+__global__ void widen_int8_kernel(const int8_t* __restrict__ x, __half* __restrict__ out,
                                   int64_t n16) {
   grid_dependency_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint4 raw = reinterpret_cast<const uint4*>(x)[i];
     const int8_t* v = reinterpret_cast<const int8_t*>(&raw);
-    float f[16];
+    uint4 o[2];
+    __half* h = reinterpret_cast<__half*>(o);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) f[k] = static_cast<float>(v[k]);
-    store8_bf16(out + i * 16, f);
-    store8_bf16(out + i * 16 + 8, f + 8);
+    for (int k = 0; k < 16; ++k) h[k] = __short2half_rn(v[k]);
+    reinterpret_cast<uint4*>(out + i * 16)[0] = o[0];
+    reinterpret_cast<uint4*>(out + i * 16)[1] = o[1];
   }
   grid_launch_dependents();   // after this thread's loads: the next grid's prefetch waits for them
 }
@@ -709,7 +720,7 @@ cudaError_t launch_rms_norm_quant(const __nv_bfloat16* x, const __nv_bfloat16* g
                   bias, deq, dpc, eps, out, He);
 }
 
-cudaError_t launch_widen_int8(const int8_t* x, __nv_bfloat16* out, int64_t n, cudaStream_t stream) {
+cudaError_t launch_widen_int8(const int8_t* x, __half* out, int64_t n, cudaStream_t stream) {
   if (n % 16) return cudaErrorInvalidValue;
   const int64_t n16 = n / 16;
   int64_t blocks = (n16 + 255) / 256;

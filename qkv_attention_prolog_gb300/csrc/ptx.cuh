@@ -357,6 +357,13 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, both operands K-major.
+// The same with f16 A and B (both operands of one MMA always have the same type).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                                   // D format: f32
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8 (A and B format 0: f16)
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format: f32
          | (1u << 7)                                 // A format: bf16

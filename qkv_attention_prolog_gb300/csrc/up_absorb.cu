@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const uint32_t idesc_up = idesc_bf16_f32(128, up_rows);
+      // (int8 weight: the converted tiles and the c^Q codes are f16; the absorb stays bf16)
+      const uint32_t idesc_up = INT8 ? idesc_f16_f32(128, up_rows) : idesc_bf16_f32(128, up_rows);
       for (int kb = 0; kb < kb_up; ++kb) {
         if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
           ok = false;
