@@ -219,26 +219,41 @@ __device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t biased, uint32_t se
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Source chunk q of an int8 weight tile (64-B rows, four 16-B chunks each: row q / 4, chunk q % 4)
-// to f16 in the 128B-swizzled K-major layout (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7))
-// << 4)).  The converter threads take consecutive chunks, so a warp's loads read 512 contiguous
-// bytes and every thread has the same share of the tile whatever its row count.
-__device__ __forceinline__ void convert_int8_chunk(const uint8_t* raw, uint8_t* dst, int q) {
-  const int r = q >> 2, i = q & 3;
-  const uint4 v = *reinterpret_cast<const uint4*>(raw + q * 16);
-  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
-                         v.w ^ 0x80808080u};
-  uint32_t out[8];
+// An int8 weight tile of `rows` 64-B rows to f16 in the 128B-swizzled K-major layout (row r,
+// 16-byte chunk c at r*128 + ((c ^ (r & 7)) << 4)), by one thread of 128: the thread takes the
+// source chunks ct, ct + 128, ... (row q / 4, chunk q % 4), so a warp's loads read 512 contiguous
+// bytes and every thread has the same share of the tile.  All of a thread's loads are issued
+// before any conversion (MAXC >= rows / 32 chunks per thread): the shared-memory latency is paid
+// once per tile instead of once per chunk.
+template <int MAXC>
+__device__ __forceinline__ void convert_int8_tile(const uint8_t* raw, uint8_t* dst, int rows,
+                                                  int ct) {
+  const int n = rows * 4;
+  uint4 v[MAXC];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    out[2 * k] = int8x2_to_f16x2(w[k], 0x4140u);       // bytes 0, 1
-    out[2 * k + 1] = int8x2_to_f16x2(w[k], 0x4342u);   // bytes 2, 3
+  for (int j = 0; j < MAXC; ++j) {
+    const int q = ct + 128 * j;
+    if (q < n) v[j] = *reinterpret_cast<const uint4*>(raw + q * 16);
   }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int c = 2 * i + h;
-    *reinterpret_cast<uint4*>(dst + r * 128 + (((c ^ (r & 7)) & 7) << 4)) =
-        make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+  for (int j = 0; j < MAXC; ++j) {
+    const int q = ct + 128 * j;
+    if (q >= n) break;
+    const int r = q >> 2, i = q & 3;
+    const uint32_t w[4] = {v[j].x ^ 0x80808080u, v[j].y ^ 0x80808080u, v[j].z ^ 0x80808080u,
+                           v[j].w ^ 0x80808080u};
+    uint32_t out[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      out[2 * k] = int8x2_to_f16x2(w[k], 0x4140u);       // bytes 0, 1
+      out[2 * k + 1] = int8x2_to_f16x2(w[k], 0x4342u);   // bytes 2, 3
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = 2 * i + h;
+      *reinterpret_cast<uint4*>(dst + r * 128 + (((c ^ (r & 7)) & 7) << 4)) =
+          make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+    }
   }
 }
 
@@ -620,7 +635,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
         }
         const uint8_t* raw = smemR + stage * Cfg::RAW_BYTES;
         uint8_t* dst = WQ == 1 ? smemA + stage * Cfg::A_BYTES : smemB + stage * Cfg::B_BYTES;
-        for (int q = ct; q < Cfg::RAW_ROWS * 4; q += 128) convert_int8_chunk(raw, dst, q);
+        constexpr int kChunks = Cfg::RAW_ROWS ? (Cfg::RAW_ROWS + 31) / 32 : 1;   // per thread
+        convert_int8_tile<kChunks>(raw, dst, Cfg::RAW_ROWS, ct);
         fence_proxy_async_shared();              // generic writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_bar[stage]);

@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       }
       const uint8_t* raw = ring_raw + rs * kRawB;
       uint8_t* dst = stages + stage * kUaStage + kUaA;
-      for (int q = ct; q < up_rows * 4; q += 128) convert_int8_chunk(raw, dst, q);
+      convert_int8_tile<6>(raw, dst, up_rows, ct);     // (up_rows <= 192)
       fence_proxy_async_shared();                      // generic writes -> the tensor core
       __syncwarp();
       if (lane == 0) {
