@@ -5,6 +5,7 @@ namespace mlap {
 
 cudaError_t launch_absorb(const GemmLaunch& L, const AbsorbParams& p) {
   if (L.swap) {
+    if (L.mt == 2 && L.bn > 128) return cudaErrorInvalidValue;   // two accumulators must fit TMEM
     switch (L.bn) {
       case 16: return L.mt == 2 ? launch_gemm_t<16, 0, 2, 1>(L, EpiAbsorb<true, 16>{p})
                            : launch_gemm_t<16, 0, 1, 1>(L, EpiAbsorb<true, 16>{p});

@@ -23,6 +23,7 @@ static cudaError_t launch_down_int8(const GemmLaunch& L, const DownParams& p) {
 cudaError_t launch_down(const GemmLaunch& L, const DownParams& p) {
   if (L.a_int8) return launch_down_int8(L, p);
   if (L.swap) {
+    if (L.mt == 2 && L.bn > 128) return cudaErrorInvalidValue;   // two accumulators must fit TMEM
     switch (L.bn) {
       case 16: return L.mt == 2 ? launch_gemm_t<16, 0, 2, 1>(L, EpiDown<true, 256, 16>{p})
                            : launch_gemm_t<16, 0, 1, 1>(L, EpiDown<true, 128, 16>{p});

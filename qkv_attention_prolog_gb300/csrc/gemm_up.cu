@@ -11,6 +11,7 @@ static cudaError_t launch_up_t(const GemmLaunch& L, const UpParams& p) {
   constexpr int WB = INT8 ? 2 : 0;   // int8 weight as operand B (prefill orientation)
   constexpr int AL = INT8 ? 0 : 1;   // bf16 weight: activation through the cp.async loaders
   if (L.swap) {
+    if (L.mt == 2 && L.bn > 128) return cudaErrorInvalidValue;   // two accumulators must fit TMEM
     switch (L.bn) {
       case 16: return L.mt == 2 ? launch_gemm_t<16, WA, 2, AL>(L, EpiUp<true, INT8, 16>{p})
                            : launch_gemm_t<16, WA, 1, AL>(L, EpiUp<true, INT8, 16>{p});
