@@ -643,12 +643,15 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   const bool fused = swap && d.N >= kFusedMinHeads &&
                      up_absorb_supported(d.T, d.N, d.D, d.Dr, d.Hckv);
   if (fused) {
-    CUtensorMap tcq, tw, tuk;
+    CUtensorMap tcq, tw, tw128, tuk, tuk128;   // (the 128-row maps serve int8 weights only)
     CHECK_STATUS(make_tmap(&tcq, cq, d.Hcq, d.T, d.Hcq, 128));
-    if (d.w_int8)
+    if (d.w_int8) {
       CHECK_STATUS(make_tmap_i8(&tw, a->weight_uq_qr.data, d.Hcq, Mup, 32));
-    else
+      CHECK_STATUS(make_tmap_i8(&tw128, a->weight_uq_qr.data, d.Hcq, Mup, 128));
+      CHECK_STATUS(make_tmap(&tuk128, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, 128));
+    } else {
       CHECK_STATUS(make_tmap(&tw, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 32));
+    }
     CHECK_STATUS(make_tmap(&tuk, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, 32));
     // an int8 query is quantised per token and head from a bf16 q^N staged in the workspace
     __nv_bfloat16* qn_out = d.query_int8 ? reinterpret_cast<__nv_bfloat16*>(wsb + L.qn)
@@ -662,7 +665,8 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                       scale_t, static_cast<const float*>(a->dequant_scale_w_uq_qr.data), 2, 0,
                       stamps};
     up_absorb_plan(sms, static_cast<int>(d.N), &ua.k, &ua.R);
-    ce = launch_up_absorb(tcq, tw, tuk, ua, d.w_int8, err, stream);
+    ce = launch_up_absorb(tcq, tw, tuk, d.w_int8 ? &tw128 : nullptr, d.w_int8 ? &tuk128 : nullptr,
+                          ua, err, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "fused up-projection/absorb launch");
     if (d.query_int8) {
       ce = launch_query_quant(qn_out, static_cast<int8_t*>(a->query.data),

@@ -56,10 +56,13 @@ void up_absorb_plan(int sms, int N, int* k, int* R);
 bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hckv);
 // tmCq: c^Q (T, Hcq) bf16, box 64 x 128, 128B-swizzled; tmW: prepacked W^UQ|W^QR
 // (N*(D+Dr) rows of Hcq), box 64 x 32, bf16 128B-swizzled or int8 unswizzled (int8 = true);
-// tmUk: prepacked W^UK (N*Hckv rows of D), box 64 x 32, 128B-swizzled.
+// tmUk: prepacked W^UK (N*Hckv rows of D), box 64 x 32, 128B-swizzled.  tmW128 / tmUk128: the
+// same two tensors with boxes of 128 rows, given for int8 weights (which selects the int8
+// kernel) and null for bf16.
 cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
-                             const CUtensorMap& tmUk, const UpAbsorbParams& p, bool int8,
-                             uint32_t* err, cudaStream_t stream);
+                             const CUtensorMap& tmUk, const CUtensorMap* tmW128,
+                             const CUtensorMap* tmUk128, const UpAbsorbParams& p, uint32_t* err,
+                             cudaStream_t stream);
 cudaError_t launch_absorb(const GemmLaunch& L, const AbsorbParams& p);
 
 // RmsNorm of c^Q (+ dynamic int8 quant) and c^KV, RoPE of k^R, cache quant and scatter; one CTA

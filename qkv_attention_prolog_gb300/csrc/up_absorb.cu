@@ -116,11 +116,22 @@ __device__ __forceinline__ UaPlan ua_plan(const UpAbsorbParams& p) {
   return pl;
 }
 
+// The int8 kernel's producers also take a head's 128 contiguous W^UQ rows, and 128 W^UK rows,
+// as one box each: at these sizes each TMA issue costs the producer thread about as much time
+// as the box it moves.  The bf16 kernel is not producer-bound and takes no extra maps (two more
+// tensor maps in its parameters cost its launch more than the larger boxes would save).
+template <bool INT8> struct UaWideMaps {
+  CUtensorMap w;    // W^UQ|W^QR rows, box 64 x 128
+  CUtensorMap uk;   // W^UK rows, box 64 x 128
+};
+template <> struct UaWideMaps<false> {};
+
 template <bool INT8>
 __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     up_absorb_kernel(const __grid_constant__ CUtensorMap tmCq,   // c^Q (T, Hcq), box 64 x 128
                      const __grid_constant__ CUtensorMap tmW,    // W^UQ|W^QR rows, box 64 x 32
                      const __grid_constant__ CUtensorMap tmUk,   // W^UK rows, box 64 x 32
+                     const __grid_constant__ UaWideMaps<INT8> wide,
                      const UpAbsorbParams p, uint32_t* __restrict__ err_word) {
   using Cfg = UaCfg<INT8>;
   extern __shared__ uint8_t smem_raw[];
@@ -166,6 +177,10 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     prefetch_tmap(&tmCq);
     prefetch_tmap(&tmW);
     prefetch_tmap(&tmUk);
+    if constexpr (INT8) {
+      prefetch_tmap(&wide.w);
+      prefetch_tmap(&wide.uk);
+    }
   }
   if (warp == 1 && lane == 0) {
     for (int i = 0; i < kUaStages; ++i) {
@@ -251,7 +266,12 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         }
         uint8_t* b = stages + stage * kUaStage + kUaA;
         mbar_arrive_expect_tx(&full_bar[stage], rows * kUaBK * 2);
-        for (int r = 0; r < rows; r += 32)
+        int r = 0;
+        if constexpr (INT8)
+          for (; r + 128 <= rows; r += 128)
+            tma_load_2d(b + r * 128, &wide.uk, &full_bar[stage], kb2 * kUaBK,
+                        n * p.Hckv + h * wrows + r);
+        for (; r < rows; r += 32)
           tma_load_2d(b + r * 128, &tmUk, &full_bar[stage], kb2 * kUaBK,
                       n * p.Hckv + h * wrows + r);
         ++fills[stage];
@@ -289,9 +309,12 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       if (kb >= kRS && !mbar_wait(&rawe_bar[rs], rph ^ 1u, abort_flag)) break;
       uint8_t* r = ring_raw + rs * kRawB;
       mbar_arrive_expect_tx(&rawf_bar[rs], static_cast<uint32_t>(up_rows) * kUaBK);
+      if constexpr (INT8)   // a head's 128 contiguous W^UQ rows as one box
+        if (pl.head) tma_load_2d(r, &wide.w, &rawf_bar[rs], kb * kUaBK, n * kD);
 #pragma unroll
       for (int j = 0; j < 6; ++j)
-        if (j < nbox) tma_load_2d(r + j * 2048, &tmW, &rawf_bar[rs], kb * kUaBK, ybox[j]);
+        if (j < nbox && !(pl.head && j < kD / 32))
+          tma_load_2d(r + j * 2048, &tmW, &rawf_bar[rs], kb * kUaBK, ybox[j]);
       ++rawfills[rs];
       if (++rs == kRS) {
         rs = 0;
@@ -577,8 +600,8 @@ bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hc
 
 template <bool INT8>
 static cudaError_t launch_ua_t(const CUtensorMap& tmCq, const CUtensorMap& tmW,
-                               const CUtensorMap& tmUk, const UpAbsorbParams& p, uint32_t* err,
-                               cudaStream_t stream) {
+                               const CUtensorMap& tmUk, const UaWideMaps<INT8>& wide,
+                               const UpAbsorbParams& p, uint32_t* err, cudaStream_t stream) {
   auto kern = up_absorb_kernel<INT8>;
   constexpr int kSmem = UaCfg<INT8>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -593,14 +616,17 @@ static cudaError_t launch_ua_t(const CUtensorMap& tmCq, const CUtensorMap& tmW,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmCq, tmW, tmUk, p, err);
+  return cudaLaunchKernelEx(&cfg, kern, tmCq, tmW, tmUk, wide, p, err);
 }
 
 cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
-                             const CUtensorMap& tmUk, const UpAbsorbParams& p, bool int8,
-                             uint32_t* err, cudaStream_t stream) {
-  return int8 ? launch_ua_t<true>(tmCq, tmW, tmUk, p, err, stream)
-              : launch_ua_t<false>(tmCq, tmW, tmUk, p, err, stream);
+                             const CUtensorMap& tmUk, const CUtensorMap* tmW128,
+                             const CUtensorMap* tmUk128, const UpAbsorbParams& p, uint32_t* err,
+                             cudaStream_t stream) {
+  if ((tmW128 == nullptr) != (tmUk128 == nullptr)) return cudaErrorInvalidValue;
+  if (tmW128)
+    return launch_ua_t<true>(tmCq, tmW, tmUk, UaWideMaps<true>{*tmW128, *tmUk128}, p, err, stream);
+  return launch_ua_t<false>(tmCq, tmW, tmUk, UaWideMaps<false>{}, p, err, stream);
 }
 
 }  // namespace mlap
