@@ -664,7 +664,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                       static_cast<int32_t>(d.Hcq), static_cast<int32_t>(d.Hckv),
                       scale_t, static_cast<const float*>(a->dequant_scale_w_uq_qr.data), 2, 0,
                       stamps};
-    up_absorb_plan(sms, static_cast<int>(d.N), &ua.k, &ua.R);
+    up_absorb_plan(sms, static_cast<int>(d.N), &ua.k, &ua.R, &ua.pair);
     ce = launch_up_absorb(tcq, tw, tuk, d.w_int8 ? &tw128 : nullptr, d.w_int8 ? &tuk128 : nullptr,
                           ua, err, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "fused up-projection/absorb launch");

@@ -44,15 +44,16 @@ struct UpAbsorbParams {
   const float* scale_t;         // int8 weight: per-token c^Q quant scale (T)
   const float* dqw;             // int8 weight: dequant_scale_w_uq_qr (N*(D+Dr))
   int32_t k;                    // W^QR blocks of 32 rows kept by each head CTA (0, 1 or 2)
-  int32_t R;                    // CTAs after the N head CTAs that take the other W^QR blocks
+  int32_t R;                    // CTAs after the head CTAs that take the other W^QR blocks
   uint64_t* stamps;             // optional execution stamps (stamps.cuh), slot MLAP_STAMP_UP
+  int32_t pair;                 // 1: two CTAs (a cluster) per head, 2N head CTAs
 };
 // One CTA whose bounded mbarrier wait runs out (nothing completes the barrier) and latches
 // kErrTimeout in err_word (selftest.cu).
 cudaError_t launch_bounded_wait_selftest(uint32_t* err_word, cudaStream_t stream);
 
-// k and R for `sms` SMs and N heads (grid = N + R)
-void up_absorb_plan(int sms, int N, int* k, int* R);
+// k, R and pair for `sms` SMs and N heads (grid = N + R, or 2N + R for pairs)
+void up_absorb_plan(int sms, int N, int* k, int* R, int* pair);
 bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hckv);
 // tmCq: c^Q (T, Hcq) bf16, box 64 x 128, 128B-swizzled; tmW: prepacked W^UQ|W^QR
 // (N*(D+Dr) rows of Hcq), box 64 x 32, bf16 128B-swizzled or int8 unswizzled (int8 = true);

@@ -195,6 +195,19 @@ __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_
       : "memory");
 }
 
+// Copy `bytes` of this CTA's shared memory into another CTA of the cluster: dst and the
+// barrier are shared::cluster addresses (mapa_shared), the copy completes as transaction bytes
+// on that barrier.  The source must have been made visible to the async proxy
+// (fence_proxy_async_shared after the generic stores).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cl, const void* src, uint32_t bytes,
+                                                  uint32_t bar_cl) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cl),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cl)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

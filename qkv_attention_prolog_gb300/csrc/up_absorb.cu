@@ -25,6 +25,13 @@
 // dequantises acc * scale_t[t] * dequant_scale_w_uq_qr[col] before q^C is rounded and q_r
 // rotated.  Every mbarrier wait is bounded; on a timeout the CTA
 // lets its issued loads land, frees TMEM and latches the error word.
+//
+// Head pairs (2N <= SMs): a head's work is split over the two CTAs of a cluster.  CTA r of the
+// pair computes q^C columns 64r..64r+63 (its 64 W^UQ rows, plus the head's rope block r), sends
+// that 64-wide K block of the absorb's A operand to the other CTA's shared memory with one bulk
+// copy per epilogue warp, and computes q^N for its half of the Hckv columns from both K blocks.
+// Each CTA then streams about half of a head's W^UQ and W^UK bytes, where with N heads on one
+// CTA each the N head CTAs carry most of the bytes and the remaining SMs little.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -55,8 +62,8 @@ struct UaCfg {
   static constexpr int SMEM = kUaSmemMax;
 };
 constexpr uint32_t kUaUpCol = 256;                     // TMEM column of the up accumulator
-// Operand stages whose weight tiles are requested before the wait on the preceding kernel (six
-// were slower: their loads queue ahead of the preceding kernels' own in DRAM).
+// Operand stages whose weight tiles the producer requests before its wait on the preceding
+// kernel (six were slower: their loads queue ahead of the preceding kernels' own in DRAM).
 constexpr int kUaPreStages = 4;
 constexpr int kD = 128;
 constexpr int kDr = 64;
@@ -90,22 +97,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 // This CTA's share: head CTA (blockIdx < N) or rope CTA, and its rope blocks g_j = g0 + gs * j,
 // j < nrope (kept in registers: the producer's issue path is latency-critical).
+// A head CTA of a pair also has its head n and its rank r in the pair.
 struct UaPlan {
   bool head;
   int nrope, g0, gs;
+  int n, r;
 };
 
+template <bool PAIR>
 __device__ __forceinline__ UaPlan ua_plan(const UpAbsorbParams& p) {
   UaPlan pl;
   const int b = blockIdx.x;
-  if (b < p.N) {
+  const int nhc = PAIR ? 2 * p.N : p.N;                // head CTAs
+  pl.n = PAIR ? b >> 1 : b;
+  pl.r = PAIR ? b & 1 : 0;
+  if (b < nhc) {   // (with k = 1 the CTA of rank r in a pair takes the head's rope block r)
     pl.head = true;
     pl.nrope = p.k;
-    pl.g0 = 2 * b;
+    pl.g0 = PAIR ? b : 2 * b;
     pl.gs = 1;
   } else {
-    const int r = b - p.N;
-    const int total = p.k == 1 ? p.N : 2 * p.N;        // blocks the rope CTAs share
+    const int r = b - nhc;
+    const int total = p.k == 1 ? (PAIR ? 0 : p.N) : 2 * p.N;   // blocks the rope CTAs share
     const int i0 = static_cast<int>(static_cast<long long>(total) * r / p.R);
     const int i1 = static_cast<int>(static_cast<long long>(total) * (r + 1) / p.R);
     pl.head = false;
@@ -126,7 +139,7 @@ template <bool INT8> struct UaWideMaps {
 };
 template <> struct UaWideMaps<false> {};
 
-template <bool INT8>
+template <bool INT8, bool PAIR>
 __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     up_absorb_kernel(const __grid_constant__ CUtensorMap tmCq,   // c^Q (T, Hcq), box 64 x 128
                      const __grid_constant__ CUtensorMap tmW,    // W^UQ|W^QR rows, box 64 x 32
@@ -140,22 +153,28 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const UaPlan pl = ua_plan(p);
-  const int n = blockIdx.x;                            // head (head CTAs)
+  const UaPlan pl = ua_plan<PAIR>(p);
+  const int n = pl.n;                                  // head (head CTAs)
   const int kb_up = (p.Hcq + kUaBK - 1) / kUaBK;
-  const int up_rows = (pl.head ? kD : 0) + 32 * pl.nrope;   // B rows of the up-projection
+  constexpr int kHRows = PAIR ? kD / 2 : kD;           // this CTA's W^UQ rows of its head
+  const int hrow0 = n * kD + kHRows * pl.r;            // the first of them
+  const int up_rows = (pl.head ? kHRows : 0) + 32 * pl.nrope;   // B rows of the up-projection
+  // this CTA's q^N columns c_lo..c_lo+cspan-1 (a pair splits the 32-column groups)
+  const int hA = PAIR ? (p.Hckv / 32 + 1) / 2 * 32 : p.Hckv;
+  const int c_lo = pl.r * hA;
+  const int cspan = pl.r == 0 ? hA : p.Hckv - hA;
   // weight rows one stage holds (also the W^UK chunk height of a head CTA), the stage size and
   // the stage count
   const int wrows = up_rows;
   const int kUaStage = kUaA + wrows * kUaBK * 2;
-  constexpr int kAvail = kUaSmemMax - 1024 - kUaBars;
+  constexpr int kAvail = kUaSmemMax - 1024 - kUaBars - (PAIR ? kUaA : 0);
   const int kRawB = INT8 ? wrows * kUaBK : 0;                 // raw int8 tile bytes
   const int kRS = INT8 ? ((kAvail - 4 * kUaStage) / kRawB < Cfg::MAX_RAW
                               ? (kAvail - 4 * kUaStage) / kRawB : Cfg::MAX_RAW)
                        : 0;
   const int kUaStages = (kAvail - kRS * kRawB) / kUaStage < kUaMaxStages
                             ? (kAvail - kRS * kRawB) / kUaStage : kUaMaxStages;
-  const int nh = pl.head ? (p.Hckv + wrows - 1) / wrows : 0;   // absorb column chunks (<= 4)
+  const int nh = pl.head ? (cspan + wrows - 1) / wrows : 0;   // absorb column chunks (<= 4)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty_bar = full_bar + kUaMaxStages;
   uint64_t* rawf_bar = empty_bar + kUaMaxStages;       // int8: raw weight tile landed
@@ -163,14 +182,18 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   uint64_t* up_bar = rawe_bar + kUaMaxStages;          // up accumulator complete
   uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, up accumulator drained
   uint64_t* ab_bar = qc_bar + 1;                       // absorb chunk h complete (h < 4)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ab_bar + 4);
+  uint64_t* qcr_bar = ab_bar + 4;                      // pair: the other CTA's K block landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qcr_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint8_t* stages = smem + kUaBars;
   uint8_t* ring_raw = stages + kUaStages * kUaStage;   // int8: raw weight tiles
   // q^C operand, two 64-wide K blocks: the c^Q halves of stages 0 and 1, free once the
-  // up-projection's MMAs have completed
+  // up-projection's MMAs have completed.  A pair computes K block r in the c^Q half of stage 0
+  // and receives the other one in a region of its own after the raw ring (the other CTA may
+  // send it before this CTA's up-projection is done).
   uint8_t* qc0 = stages;
   uint8_t* qc1 = stages + kUaStage;
+  uint8_t* qc_peer = ring_raw + kRS * kRawB;
   if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_UP, kStampStart);
 
   if (warp == 0 && lane == 0) {
@@ -194,6 +217,10 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     mbar_init(up_bar, 1);
     mbar_init(qc_bar, 4);
     for (int h = 0; h < 4; ++h) mbar_init(&ab_bar[h], 1);
+    if constexpr (PAIR) {   // completes when the other CTA's four copies (16 KB) have landed
+      mbar_init(qcr_bar, 1);
+      mbar_arrive_expect_tx(qcr_bar, kUaA);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -203,25 +230,32 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // the other CTA's barrier exists before its copy targets it
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
   grid_launch_dependents();
   const bool producer = warp == 0 && lane == 0;
   const bool raw_producer = INT8 && warp == 3 && lane == 0;   // int8 weight tiles only
-  if (!producer && !raw_producer) grid_dependency_wait();
+  // Every role but the producers waits here for the preceding kernel.  The int8 raw producer's
+  // whole warp skips the wait, so that it fills its ring before that kernel completes (a wait
+  // taken by some lanes of a warp can hold the warp's other lanes as well).  The W^UQ|W^QR
+  // producer requests its first weight stages, then waits itself; the other lanes of its warp
+  // wait here (measured: the decode call is fastest so, 1.4 us faster than with the whole warp
+  // skipping this wait and 2 us faster than with the producer waiting before its requests).
+  if (!producer && !(INT8 && warp == 3)) grid_dependency_wait();
 
   if (producer) {
     // ------------------------------------------------------------------ TMA producer
     int fills[kUaMaxStages] = {};
-    // head n's W^UQ rows (D), then this CTA's rope blocks: up to six 32-row boxes per tile,
-    // their first weight rows computed once
+    // head n's W^UQ rows (D, or this CTA's D/2 of a pair), then this CTA's rope blocks: up to
+    // six 32-row boxes per tile, their first weight rows computed once
     const int nbox = up_rows / 32;
     int ybox[6];
 #pragma unroll
     for (int j = 0; j < 6; ++j) {
-      const int jr = pl.head ? j - kD / 32 : j;       // rope block index of box j
-      ybox[j] = jr < 0 ? n * kD + 32 * j : p.N * kD + 32 * (pl.g0 + pl.gs * jr);
+      const int jr = pl.head ? j - kHRows / 32 : j;   // rope block index of box j
+      ybox[j] = jr < 0 ? hrow0 + 32 * j : p.N * kD + 32 * (pl.g0 + pl.gs * jr);
     }
     auto issue_w = [&](int st, int kb) {
       if constexpr (!INT8) {   // (int8 weight tiles come from the raw producer)
@@ -256,9 +290,9 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         phase ^= 1u;
       }
     }
-    // head n's W^UK rows, chunk h of wrows rows, K block kb2 of D
+    // head n's W^UK rows c_lo.., chunk h of wrows rows, K block kb2 of D
     for (int h = 0; ok && h < nh; ++h) {
-      const int rows = p.Hckv - h * wrows < wrows ? p.Hckv - h * wrows : wrows;
+      const int rows = cspan - h * wrows < wrows ? cspan - h * wrows : wrows;
       for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2) {
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
           ok = false;
@@ -270,10 +304,10 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         if constexpr (INT8)
           for (; r + 128 <= rows; r += 128)
             tma_load_2d(b + r * 128, &wide.uk, &full_bar[stage], kb2 * kUaBK,
-                        n * p.Hckv + h * wrows + r);
+                        n * p.Hckv + c_lo + h * wrows + r);
         for (; r < rows; r += 32)
           tma_load_2d(b + r * 128, &tmUk, &full_bar[stage], kb2 * kUaBK,
-                      n * p.Hckv + h * wrows + r);
+                      n * p.Hckv + c_lo + h * wrows + r);
         ++fills[stage];
         if (++stage == kUaStages) {
           stage = 0;
@@ -300,8 +334,8 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     int ybox[6];
 #pragma unroll
     for (int j = 0; j < 6; ++j) {
-      const int jr = pl.head ? j - kD / 32 : j;
-      ybox[j] = jr < 0 ? n * kD + 32 * j : p.N * kD + 32 * (pl.g0 + pl.gs * jr);
+      const int jr = pl.head ? j - kHRows / 32 : j;
+      ybox[j] = jr < 0 ? hrow0 + 32 * j : p.N * kD + 32 * (pl.g0 + pl.gs * jr);
     }
     int rs = 0;
     uint32_t rph = 0;
@@ -309,11 +343,12 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       if (kb >= kRS && !mbar_wait(&rawe_bar[rs], rph ^ 1u, abort_flag)) break;
       uint8_t* r = ring_raw + rs * kRawB;
       mbar_arrive_expect_tx(&rawf_bar[rs], static_cast<uint32_t>(up_rows) * kUaBK);
-      if constexpr (INT8)   // a head's 128 contiguous W^UQ rows as one box
-        if (pl.head) tma_load_2d(r, &wide.w, &rawf_bar[rs], kb * kUaBK, n * kD);
+      constexpr bool kWide = INT8 && !PAIR;   // a head's 128 contiguous W^UQ rows as one box
+      if constexpr (kWide)
+        if (pl.head) tma_load_2d(r, &wide.w, &rawf_bar[rs], kb * kUaBK, hrow0);
 #pragma unroll
       for (int j = 0; j < 6; ++j)
-        if (j < nbox && !(pl.head && j < kD / 32))
+        if (j < nbox && !(kWide && pl.head && j < kD / 32))
           tma_load_2d(r + j * 2048, &tmW, &rawf_bar[rs], kb * kUaBK, ybox[j]);
       ++rawfills[rs];
       if (++rs == kRS) {
@@ -358,11 +393,17 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       }
       if (ok) umma_commit(up_bar);
       if (ok && pl.head) ok = mbar_wait(qc_bar, 0, abort_flag);   // q^C staged, acc read
+      if constexpr (PAIR)   // the other CTA's K block (always awaited: it lands here regardless)
+        if (ok && pl.head) ok = mbar_wait_cluster(qcr_bar, 0, abort_flag);
       if (ok && pl.head) {
         tc_fence_after_sync();
-        const uint32_t qa[2] = {smem_u32(qc0), smem_u32(qc1)};
+        uint32_t qa[2] = {smem_u32(qc0), smem_u32(qc1)};
+        if constexpr (PAIR) {
+          qa[pl.r] = smem_u32(qc0);
+          qa[pl.r ^ 1] = smem_u32(qc_peer);
+        }
         for (int h = 0; ok && h < nh; ++h) {
-          const int rows = p.Hckv - h * wrows < wrows ? p.Hckv - h * wrows : wrows;
+          const int rows = cspan - h * wrows < wrows ? cspan - h * wrows : wrows;
           const uint32_t idesc_ab = idesc_bf16_f32(128, rows);
           for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2) {
             if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
@@ -458,19 +499,26 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       if (pl.head) {
         // q^C: bf16 into the K-major, 128B-swizzled A operand (token t = row t)
 #pragma unroll 1
-        for (; col < kD; col += 32) {
+        for (; col < kHRows; col += 32) {
           float v[32];
           tmem_ld32(lane_base + kUaUpCol + col, v);
-          if constexpr (INT8) {   // nope row n*D + col + j is column n*(D+Dr) + col + j
-            const float* dq = p.dqw + n * (kD + kDr) + col;
+          if constexpr (INT8) {   // nope row n*D + d is column n*(D+Dr) + d
+            const float* dq = p.dqw + n * (kD + kDr) + kHRows * pl.r + col;
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = v[j] * st * __ldg(dq + j);
           }
-          uint8_t* row = (col < kUaBK ? qc0 : qc1) + t * 128;
+          uint8_t* row = (PAIR || col < kUaBK ? qc0 : qc1) + t * 128;
           const int ch0 = (col % kUaBK) / 8;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             *reinterpret_cast<uint4*>(row + ((((ch0 + j) ^ (t & 7)) & 7) << 4)) = pack8(v + 8 * j);
+        }
+        if constexpr (PAIR) {   // this warp's 32 rows (4 KB) of the K block -> the other CTA
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0)
+            bulk_copy_to_peer(mapa_shared(smem_u32(qc_peer + q * 4096), pl.r ^ 1), qc0 + q * 4096,
+                              4096, mapa_shared(smem_u32(qcr_bar), pl.r ^ 1));
         }
       }
       // rope blocks: 32 columns = pairs p0..p0+15 (p0 = 16 * (g % 2)) of head g / 2, RoPE,
@@ -525,8 +573,8 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       const int rsub = lane >> 3, ch = lane & 7;        // read-back: row rsub + 4i, chunk ch
       int waited = 0;                                   // absorb chunks known complete
 #pragma unroll 1
-      for (int c = 0; ok && c < p.Hckv; c += 64) {
-        const int w = p.Hckv - c < 64 ? p.Hckv - c : 64;   // 64, or 32 for the last group
+      for (int c = 0; ok && c < cspan; c += 64) {
+        const int w = cspan - c < 64 ? cspan - c : 64;     // 64, or 32 for the last group
         const int need = (c + w - 1) / wrows + 1;          // chunks holding columns c..c+w-1
         while (waited < need) {
           if (!mbar_wait(&ab_bar[waited], 0, abort_flag)) {
@@ -557,7 +605,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
                 *reinterpret_cast<const uint4*>(tile + r * 128 + (((ch ^ (r & 7)) & 7) << 4));
             if (tr < p.T)
               *reinterpret_cast<uint4*>(p.q_out + (static_cast<size_t>(tr) * p.N + n) * p.Hckv +
-                                        c + ch * 8) = val;
+                                        c_lo + c + ch * 8) = val;
           }
         }
         __syncwarp();                                   // the tile is read before it is rewritten
@@ -567,6 +615,23 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) {
+    // Neither CTA of a pair exits while a copy between them may still be in flight: after a
+    // timeout, give copies issued so far time to land (bounded) on both sides of the pair's
+    // final barrier, which each CTA reaches only after its own copy was issued or skipped.
+    const bool aborted = *abort_flag != 0;
+    if (aborted) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 1000000ull) {
+      }
+    }
+    cluster_sync();
+    if (aborted) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 1000000ull) {
+      }
+    }
+  }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(err_word, kErrTimeout);
   if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_UP, kStampEnd);
   if (warp == 2) {
@@ -577,9 +642,16 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
 
 }  // namespace
 
-void up_absorb_plan(int sms, int N, int* k, int* R) {
-  // rope blocks per head CTA (k) and rope CTAs (R) so that the CTAs stream about the same weight
-  // bytes and a rope CTA takes at most 6 blocks
+void up_absorb_plan(int sms, int N, int* k, int* R, int* pair) {
+  // Head pairs when two CTAs per head fit on the SMs: each CTA keeps one rope block, no rope
+  // CTAs.  Otherwise rope blocks per head CTA (k) and rope CTAs (R) so that the CTAs stream
+  // about the same weight bytes and a rope CTA takes at most 6 blocks.
+  *pair = 2 * N <= sms ? 1 : 0;
+  if (*pair) {
+    *k = 1;
+    *R = 0;
+    return;
+  }
   *R = sms - N;
   if (*R > 0 && 2 * N <= 6 * *R) {
     *k = 0;
@@ -598,24 +670,30 @@ bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hc
          Hckv % 32 == 0;
 }
 
-template <bool INT8>
+template <bool INT8, bool PAIR>
 static cudaError_t launch_ua_t(const CUtensorMap& tmCq, const CUtensorMap& tmW,
                                const CUtensorMap& tmUk, const UaWideMaps<INT8>& wide,
                                const UpAbsorbParams& p, uint32_t* err, cudaStream_t stream) {
-  auto kern = up_absorb_kernel<INT8>;
+  auto kern = up_absorb_kernel<INT8, PAIR>;
   constexpr int kSmem = UaCfg<INT8>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.N + p.R));
+  const int grid = (PAIR ? 2 * p.N : p.N) + p.R;
+  if (PAIR && (grid & 1)) return cudaErrorInvalidValue;   // whole clusters of two
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(UaCfg<INT8>::THREADS);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = PAIR ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, tmCq, tmW, tmUk, wide, p, err);
 }
 
@@ -624,9 +702,13 @@ cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
                              const CUtensorMap* tmUk128, const UpAbsorbParams& p, uint32_t* err,
                              cudaStream_t stream) {
   if ((tmW128 == nullptr) != (tmUk128 == nullptr)) return cudaErrorInvalidValue;
-  if (tmW128)
-    return launch_ua_t<true>(tmCq, tmW, tmUk, UaWideMaps<true>{*tmW128, *tmUk128}, p, err, stream);
-  return launch_ua_t<false>(tmCq, tmW, tmUk, UaWideMaps<false>{}, p, err, stream);
+  if (tmW128) {
+    const UaWideMaps<true> wide{*tmW128, *tmUk128};
+    return p.pair ? launch_ua_t<true, true>(tmCq, tmW, tmUk, wide, p, err, stream)
+                  : launch_ua_t<true, false>(tmCq, tmW, tmUk, wide, p, err, stream);
+  }
+  return p.pair ? launch_ua_t<false, true>(tmCq, tmW, tmUk, UaWideMaps<false>{}, p, err, stream)
+                : launch_ua_t<false, false>(tmCq, tmW, tmUk, UaWideMaps<false>{}, p, err, stream);
 }
 
 }  // namespace mlap

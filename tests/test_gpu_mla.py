@@ -256,7 +256,8 @@ def test_rms_norm_quant_bsh_leaves_token_x():
                        cpu["token_x"].view(torch.int16))
 
 
-# ---- fused decode up-projection + absorb (one CTA per head, T <= 128, N >= 16, bf16 weight)
+# ---- fused decode up-projection + absorb (T <= 128, N >= 16): one CTA per head, or two CTAs
+# per head (a cluster pair splitting q^C and q^N) when 2N fits on the SMs
 
 FUSED_SHAPES = [
     dict(B=1, S=1, N=64),                                          # single token
@@ -272,6 +273,10 @@ FUSED_SHAPES = [
          cache_dtype="bf16"),                                       # ragged K, bf16 caches
     dict(B=6, S=1, He=256, Hcq=128, Hckv=64, N=128, weight_uq_qr_dtype="int8",
          cache_dtype="int8", full_quant=True),                      # full quant, int8 query
+    dict(B=9, S=1, He=256, Hcq=192, Hckv=96, N=96, weight_uq_qr_dtype="int8",
+         cache_dtype="int8"),                                       # int8, one CTA per head
+    # head pairs (2N <= SMs): the second CTA of each pair has no q^N columns
+    dict(B=5, S=1, He=256, Hcq=128, Hckv=32, N=20),
 ]
 
 
