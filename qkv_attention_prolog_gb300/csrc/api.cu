@@ -644,7 +644,10 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                      up_absorb_supported(d.T, d.N, d.D, d.Dr, d.Hckv);
   if (fused) {
     CUtensorMap tcq, tw, tw128, tuk, tuk128;   // (the 128-row maps serve int8 weights only)
-    CHECK_STATUS(make_tmap(&tcq, cq, d.Hcq, d.T, d.Hcq, 128));
+    // c^Q tiles of the token rows only (the MMA's other A rows feed accumulator lanes that are
+    // never stored)
+    const int cq_rows = d.T < 128 ? static_cast<int>((d.T + 7) / 8 * 8) : 128;
+    CHECK_STATUS(make_tmap(&tcq, cq, d.Hcq, d.T, d.Hcq, cq_rows));
     if (d.w_int8) {
       CHECK_STATUS(make_tmap_i8(&tw, a->weight_uq_qr.data, d.Hcq, Mup, 32));
       CHECK_STATUS(make_tmap_i8(&tw128, a->weight_uq_qr.data, d.Hcq, Mup, 128));
@@ -665,6 +668,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                       scale_t, static_cast<const float*>(a->dequant_scale_w_uq_qr.data), 2, 0,
                       stamps};
     up_absorb_plan(sms, static_cast<int>(d.N), &ua.k, &ua.R, &ua.pair);
+    ua.cq_rows = cq_rows;
     ce = launch_up_absorb(tcq, tw, tuk, d.w_int8 ? &tw128 : nullptr, d.w_int8 ? &tuk128 : nullptr,
                           ua, err, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "fused up-projection/absorb launch");

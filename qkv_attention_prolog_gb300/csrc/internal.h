@@ -47,6 +47,7 @@ struct UpAbsorbParams {
   int32_t R;                    // CTAs after the head CTAs that take the other W^QR blocks
   uint64_t* stamps;             // optional execution stamps (stamps.cuh), slot MLAP_STAMP_UP
   int32_t pair;                 // 1: two CTAs (a cluster) per head, 2N head CTAs
+  int32_t cq_rows;              // token rows of tmCq's box: T rounded up to 8, at most 128
 };
 // One CTA whose bounded mbarrier wait runs out (nothing completes the barrier) and latches
 // kErrTimeout in err_word (selftest.cu).
@@ -55,7 +56,7 @@ cudaError_t launch_bounded_wait_selftest(uint32_t* err_word, cudaStream_t stream
 // k, R and pair for `sms` SMs and N heads (grid = N + R, or 2N + R for pairs)
 void up_absorb_plan(int sms, int N, int* k, int* R, int* pair);
 bool up_absorb_supported(int64_t T, int64_t N, int64_t D, int64_t Dr, int64_t Hckv);
-// tmCq: c^Q (T, Hcq) bf16, box 64 x 128, 128B-swizzled; tmW: prepacked W^UQ|W^QR
+// tmCq: c^Q (T, Hcq) bf16, box 64 x p.cq_rows, 128B-swizzled; tmW: prepacked W^UQ|W^QR
 // (N*(D+Dr) rows of Hcq), box 64 x 32, bf16 128B-swizzled or int8 unswizzled (int8 = true);
 // tmUk: prepacked W^UK (N*Hckv rows of D), box 64 x 32, 128B-swizzled.  tmW128 / tmUk128: the
 // same two tensors with boxes of 128 rows, given for int8 weights (which selects the int8

@@ -195,6 +195,11 @@ __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_
       : "memory");
 }
 
+// Barrier among `count` threads (whole warps) on named barrier `id` (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Copy `bytes` of this CTA's shared memory into another CTA of the cluster: dst and the
 // barrier are shared::cluster addresses (mapa_shared), the copy completes as transaction bytes
 // on that barrier.  The source must have been made visible to the async proxy

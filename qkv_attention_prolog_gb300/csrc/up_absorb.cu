@@ -44,6 +44,8 @@ namespace {
 constexpr int kUaBK = 64;                              // K elements per stage
 constexpr int kUaA = 128 * kUaBK * 2;                  // c^Q tile: 128 tokens x 64 (16 KB)
 constexpr int kUaBars = 1024;                          // barriers and flags, ahead of the stages
+constexpr int kUaDqFloats = 192;                       // int8: staged dequant scales, after them
+static_assert(kUaDqFloats * 4 <= kUaBars, "the dequant scales of up to 192 weight rows");
 constexpr int kUaSmemMax = 232448;                     // 227 KB opt-in per CTA
 constexpr int kUaMaxStages = 8;
 
@@ -167,7 +169,9 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   // the stage count
   const int wrows = up_rows;
   const int kUaStage = kUaA + wrows * kUaBK * 2;
-  constexpr int kAvail = kUaSmemMax - 1024 - kUaBars - (PAIR ? kUaA : 0);
+  // (int8: the CTA's dequant scales follow the barriers, in a second KB ahead of the stages)
+  constexpr int kHead = INT8 ? 2 * kUaBars : kUaBars;
+  constexpr int kAvail = kUaSmemMax - 1024 - kHead - (PAIR ? kUaA : 0);
   const int kRawB = INT8 ? wrows * kUaBK : 0;                 // raw int8 tile bytes
   const int kRS = INT8 ? ((kAvail - 4 * kUaStage) / kRawB < Cfg::MAX_RAW
                               ? (kAvail - 4 * kUaStage) / kRawB : Cfg::MAX_RAW)
@@ -185,7 +189,8 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   uint64_t* qcr_bar = ab_bar + 4;                      // pair: the other CTA's K block landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qcr_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint8_t* stages = smem + kUaBars;
+  float* dq_s = reinterpret_cast<float*>(smem + kUaBars);   // int8: up_rows dequant scales
+  uint8_t* stages = smem + kHead;
   uint8_t* ring_raw = stages + kUaStages * kUaStage;   // int8: raw weight tiles
   // q^C operand, two 64-wide K blocks: the c^Q halves of stages 0 and 1, free once the
   // up-projection's MMAs have completed.  A pair computes K block r in the c^Q half of stage 0
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         }
         issue_w(stage, kb);
       }
-      mbar_arrive_expect_tx(&full_bar[stage], kUaA);
+      mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(p.cq_rows) * kUaBK * 2);
       tma_load_2d(stages + stage * kUaStage, &tmCq, &full_bar[stage], kb * kUaBK, 0);
       ++fills[stage];
       if (++stage == kUaStages) {
@@ -489,8 +494,24 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         sn[i >> 1][2 + (i & 1)] = __ldg(s + 4 + i);
       }
     }
-    // int8 weight: acc * scale_t[t] * dequant_scale_w_uq_qr[original column]
+    // int8 weight: acc * scale_t[t] * dequant_scale_w_uq_qr[original column]; the CTA's
+    // columns of dequant_scale_w_uq_qr go to shared memory while the up-projection runs
     const float st = INT8 && live ? __ldg(p.scale_t + t) : 0.f;
+    if constexpr (INT8) {
+      const int nq = pl.head ? kHRows : 0;
+      for (int i = q * 32 + lane; i < up_rows; i += 128) {
+        int c;
+        if (i < nq) {        // nope row n*D + d is column n*(D+Dr) + d
+          c = n * (kD + kDr) + kHRows * pl.r + i;
+        } else {             // rope row i of head g/2 is column D + i/2 + (i%2)*Dr/2
+          const int j = (i - nq) >> 5, ii = (i - nq) & 31;
+          const int g = pl.g0 + pl.gs * j;
+          c = (g >> 1) * (kD + kDr) + kD + (g & 1) * 16 + (ii >> 1) + (ii & 1) * (kDr / 2);
+        }
+        dq_s[i] = __ldg(p.dqw + c);
+      }
+      named_barrier_sync(1, 128);                      // the four epilogue warps
+    }
     bool ok = mbar_wait(up_bar, 0, abort_flag);
     if (ok) {
       tc_fence_after_sync();
@@ -502,10 +523,9 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         for (; col < kHRows; col += 32) {
           float v[32];
           tmem_ld32(lane_base + kUaUpCol + col, v);
-          if constexpr (INT8) {   // nope row n*D + d is column n*(D+Dr) + d
-            const float* dq = p.dqw + n * (kD + kDr) + kHRows * pl.r + col;
+          if constexpr (INT8) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = v[j] * st * __ldg(dq + j);
+            for (int j = 0; j < 32; ++j) v[j] = v[j] * st * dq_s[col + j];
           }
           uint8_t* row = (PAIR || col < kUaBK ? qc0 : qc1) + t * 128;
           const int ch0 = (col % kUaBK) / 8;
@@ -529,10 +549,9 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
         tmem_ld32(lane_base + kUaUpCol + col, y);
         const int g = pl.g0 + pl.gs * j;
         const int half = g & 1;
-        if constexpr (INT8) {   // rope row i of head g/2 is column D + i/2 + (i%2)*Dr/2
-          const float* dq = p.dqw + (g >> 1) * (kD + kDr) + kD + half * 16;
+        if constexpr (INT8) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) y[i] = y[i] * st * __ldg(dq + (i >> 1) + (i & 1) * (kDr / 2));
+          for (int i = 0; i < 32; ++i) y[i] = y[i] * st * dq_s[col + i];
         }
         if (live) {
           float c0[16], s0[16], c1[16], s1[16];
@@ -702,6 +721,8 @@ cudaError_t launch_up_absorb(const CUtensorMap& tmCq, const CUtensorMap& tmW,
                              const CUtensorMap* tmUk128, const UpAbsorbParams& p, uint32_t* err,
                              cudaStream_t stream) {
   if ((tmW128 == nullptr) != (tmUk128 == nullptr)) return cudaErrorInvalidValue;
+  if (p.cq_rows < 8 || p.cq_rows > 128 || p.cq_rows % 8 != 0 || p.cq_rows < (p.T < 128 ? p.T : 128))
+    return cudaErrorInvalidValue;
   if (tmW128) {
     const UaWideMaps<true> wide{*tmW128, *tmUk128};
     return p.pair ? launch_ua_t<true, true>(tmCq, tmW, tmUk, wide, p, err, stream)
