@@ -98,20 +98,46 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   // Decode (PARTS): the call's inputs this thread needs after the reduction (its gamma slice,
   // the token's RoPE tables and cache index) are read before the wait on the down-projection,
   // so the latency chain after it holds only the partials
+  // With partial or full quant also its scale slices: smooth_scales_cq or quant_scale_ckv (8
+  // columns, the gamma slice's), quant_scale_ckr (one column) and the full-quant dequant scales
+  // (its columns of the split sum, kPreCols at most).
+  constexpr int kPreCols = 8;
   uint4 g_pre = make_uint4(0, 0, 0, 0);
+  float4 s_pre[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  float qkr_pre = 0.f, dsx_pre = 0.f, dw_pre[kPreCols];
   __nv_bfloat16 cos_pre = __float2bfloat16(0.f), sin_pre = __float2bfloat16(0.f);
   int64_t idx_pre = -1;
+  const int f8 = threadIdx.x * 8;
   if constexpr (PARTS) {
-    if (do_q && p.Hcq <= NT * 8 && threadIdx.x * 8 < p.Hcq)
+    if (do_q && p.Hcq <= NT * 8 && f8 < p.Hcq) {
       g_pre = __ldg(reinterpret_cast<const uint4*>(p.gamma_cq) + threadIdx.x);
+      if (p.smooth != nullptr) {
+        s_pre[0] = __ldg(reinterpret_cast<const float4*>(p.smooth + f8));
+        s_pre[1] = __ldg(reinterpret_cast<const float4*>(p.smooth + f8) + 1);
+      }
+    }
     if (do_kv) {
-      if (p.Hckv <= NT * 8 && threadIdx.x * 8 < p.Hckv)
+      if (p.Hckv <= NT * 8 && f8 < p.Hckv) {
         g_pre = __ldg(reinterpret_cast<const uint4*>(p.gamma_ckv) + threadIdx.x);
+        if (p.kv_int8 && p.slots > 0) {
+          s_pre[0] = __ldg(reinterpret_cast<const float4*>(p.qs_ckv + f8));
+          s_pre[1] = __ldg(reinterpret_cast<const float4*>(p.qs_ckv + f8) + 1);
+        }
+      }
       if (threadIdx.x < p.Dr) {
         cos_pre = p.cos[static_cast<size_t>(t) * p.Dr + threadIdx.x];
         sin_pre = p.sin[static_cast<size_t>(t) * p.Dr + threadIdx.x];
+        if (p.kr_int8 && p.slots > 0) qkr_pre = __ldg(p.qs_ckr + threadIdx.x);
       }
       if (p.slots > 0) idx_pre = p.cache_index[t];
+    }
+    if (p.dsx != nullptr) {
+      dsx_pre = __ldg(p.dsx + t);
+#pragma unroll
+      for (int i = 0; i < kPreCols; ++i) {
+        const int c = c0 + static_cast<int>(threadIdx.x) + i * NT;
+        dw_pre[i] = c < c1 ? __ldg(c < p.Hcq ? p.dsw_q + c : p.dsw_kv + (c - p.Hcq)) : 0.f;
+      }
     }
   }
   grid_dependency_wait();
@@ -161,9 +187,17 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   __syncthreads();
   if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampMain);
   if (p.dsx != nullptr) {   // full quant: dequant the exact integer products per token and column
-    const float sx = p.dsx[t];
-    for (int c = c0 + threadIdx.x; c < c1; c += NT)
-      h[c] *= sx * (c < p.Hcq ? p.dsw_q[c] : p.dsw_kv[c - p.Hcq]);
+    if (PARTS && c1 - c0 <= kPreCols * NT) {
+#pragma unroll
+      for (int i = 0; i < kPreCols; ++i) {
+        const int c = c0 + static_cast<int>(threadIdx.x) + i * NT;
+        if (c < c1) h[c] *= dsx_pre * dw_pre[i];
+      }
+    } else {
+      const float sx = p.dsx[t];
+      for (int c = c0 + threadIdx.x; c < c1; c += NT)
+        h[c] *= sx * (c < p.Hcq ? p.dsw_q[c] : p.dsw_kv[c - p.Hcq]);
+    }
     __syncthreads();
   }
 
@@ -197,20 +231,48 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
       store8_bf16(cq + f, v);
     }
   } else {
+    // eight columns per thread (gamma and smooth_scales_cq read before the wait when they fit)
     float amax = 0.f;
-    for (int f = threadIdx.x; f < p.Hcq; f += NT) {
-      const float c = __bfloat162float(
-          __float2bfloat16_rn(h[f] * rq * __bfloat162float(p.gamma_cq[f])));
-      const float s = __fmul_rn(c, p.smooth[f]);
-      h[f] = s;                                   // own element only: no race
-      amax = fmaxf(amax, fabsf(s));
+    for (int f = f8; f < p.Hcq; f += NT * 8) {
+      float g[8], sm[8];
+      if (PARTS && p.Hcq <= NT * 8) {
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&g_pre);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g[i] = __bfloat162float(e[i]);
+        const float* ps = reinterpret_cast<const float*>(s_pre);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sm[i] = ps[i];
+      } else {
+        load8_bf16(p.gamma_cq + f, g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sm[i] = __ldg(p.smooth + f + i);
+      }
+      float4* h4 = reinterpret_cast<float4*>(h + f);
+      float v[8];
+      *reinterpret_cast<float4*>(v) = h4[0];
+      *reinterpret_cast<float4*>(v + 4) = h4[1];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float c = __bfloat162float(__float2bfloat16_rn(v[i] * rq * g[i]));
+        v[i] = __fmul_rn(c, sm[i]);
+        amax = fmaxf(amax, fabsf(v[i]));
+      }
+      h4[0] = *reinterpret_cast<const float4*>(v);   // own columns only: no race
+      h4[1] = *reinterpret_cast<const float4*>(v + 4);
     }
     amax = block_max<NT>(amax, reinterpret_cast<float*>(red));
     const float scale = __fdiv_rn(amax, 127.0f);
-    for (int f = threadIdx.x; f < p.Hcq; f += NT) {
-      const int code = scale > 0.f ? quant_i8(h[f], scale, -127, 127) : 0;
+    for (int f = f8; f < p.Hcq; f += NT * 8) {
+      const float4* h4 = reinterpret_cast<const float4*>(h + f);
+      float v[8];
+      *reinterpret_cast<float4*>(v) = h4[0];
+      *reinterpret_cast<float4*>(v + 4) = h4[1];
       // f16, the operand type of the int8-weight MMAs (exact: |code| <= 127)
-      reinterpret_cast<__half*>(cq)[f] = __int2half_rn(code);
+      uint4 r;
+      __half* e = reinterpret_cast<__half*>(&r);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) e[i] = __int2half_rn(scale > 0.f ? quant_i8(v[i], scale, -127, 127) : 0);
+      *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(cq) + f) = r;
     }
     if (threadIdx.x == 0) p.scale_t[t] = scale;
   }
@@ -240,8 +302,10 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     if (p.kv_int8) {
       uint2 q;
       int8_t* qb = reinterpret_cast<int8_t*>(&q);
+      const float* qs = PARTS && p.Hckv <= NT * 8 ? reinterpret_cast<const float*>(s_pre)
+                                                  : p.qs_ckv + f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) qb[i] = quant_i8(v[i], p.qs_ckv[f + i], -128, 127);
+      for (int i = 0; i < 8; ++i) qb[i] = quant_i8(v[i], qs[i], -128, 127);
       *reinterpret_cast<uint2*>(static_cast<int8_t*>(p.kv_cache) + idx * p.Hckv + f) = q;
     } else {
       store8_bf16(static_cast<__nv_bfloat16*>(p.kv_cache) + idx * p.Hckv + f, v);
@@ -258,7 +322,8 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     const float s = __bfloat162float(pre ? sin_pre : p.sin[static_cast<size_t>(t) * p.Dr + j]);
     const float v = y * c + partner * s;
     if (p.kr_int8)
-      static_cast<int8_t*>(p.kr_cache)[idx * p.Dr + j] = quant_i8(v, p.qs_ckr[j], -128, 127);
+      static_cast<int8_t*>(p.kr_cache)[idx * p.Dr + j] =
+          quant_i8(v, pre ? qkr_pre : p.qs_ckr[j], -128, 127);
     else
       static_cast<__nv_bfloat16*>(p.kr_cache)[idx * p.Dr + j] = __float2bfloat16_rn(v);
   }
