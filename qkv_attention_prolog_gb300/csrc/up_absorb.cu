@@ -184,10 +184,11 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
   uint64_t* rawf_bar = empty_bar + kUaMaxStages;       // int8: raw weight tile landed
   uint64_t* rawe_bar = rawf_bar + kUaMaxStages;        // int8: raw tile converted, slot free
   uint64_t* up_bar = rawe_bar + kUaMaxStages;          // up accumulator complete
-  uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, up accumulator drained
+  uint64_t* qc_bar = up_bar + 1;                       // q^C in smem, its accumulator read
   uint64_t* ab_bar = qc_bar + 1;                       // absorb chunk h complete (h < 4)
   uint64_t* qcr_bar = ab_bar + 4;                      // pair: the other CTA's K block landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qcr_bar + 1);
+  uint64_t* rp_bar = qcr_bar + 1;                      // rope columns of the accumulator read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rp_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* dq_s = reinterpret_cast<float*>(smem + kUaBars);   // int8: up_rows dequant scales
   uint8_t* stages = smem + kHead;
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
     }
     mbar_init(up_bar, 1);
     mbar_init(qc_bar, 4);
+    mbar_init(rp_bar, 4);
     for (int h = 0; h < 4; ++h) mbar_init(&ab_bar[h], 1);
     if constexpr (PAIR) {   // completes when the other CTA's four copies (16 KB) have landed
       mbar_init(qcr_bar, 1);
@@ -407,9 +409,18 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
           qa[pl.r] = smem_u32(qc0);
           qa[pl.r ^ 1] = smem_u32(qc_peer);
         }
+        bool rope_read = false;
         for (int h = 0; ok && h < nh; ++h) {
           const int rows = cspan - h * wrows < wrows ? cspan - h * wrows : wrows;
           const uint32_t idesc_ab = idesc_bf16_f32(128, rows);
+          // a chunk whose accumulator columns reach the up accumulator's rope columns waits for
+          // the epilogue to have read them (the q^C columns were read before qc_bar)
+          if (!rope_read && h * wrows + rows > static_cast<int>(kUaUpCol) + kHRows) {
+            ok = mbar_wait(rp_bar, 0, abort_flag);
+            rope_read = true;
+            tc_fence_after_sync();
+            if (!ok) break;
+          }
           for (int kb2 = 0; kb2 < kD / kUaBK; ++kb2) {
             if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
               ok = false;
@@ -533,12 +544,15 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
           for (int j = 0; j < 4; ++j)
             *reinterpret_cast<uint4*>(row + ((((ch0 + j) ^ (t & 7)) & 7) << 4)) = pack8(v + 8 * j);
         }
-        if constexpr (PAIR) {   // this warp's 32 rows (4 KB) of the K block -> the other CTA
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0)
+        // q^C is complete: the absorb may start while the rope blocks below are rotated
+        tc_fence_before_sync();
+        fence_proxy_async_shared();                    // q^C stores -> visible to the MMA
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR)   // this warp's 32 rows (4 KB) of the K block -> the other CTA
             bulk_copy_to_peer(mapa_shared(smem_u32(qc_peer + q * 4096), pl.r ^ 1), qc0 + q * 4096,
                               4096, mapa_shared(smem_u32(qcr_bar), pl.r ^ 1));
+          mbar_arrive(qc_bar);
         }
       }
       // rope blocks: 32 columns = pairs p0..p0+15 (p0 = 16 * (g % 2)) of head g / 2, RoPE,
@@ -576,11 +590,10 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
           db[1] = pack8(ob + 8);
         }
       }
-      if (pl.head) {
+      if (pl.head) {   // the rope columns have been read
         tc_fence_before_sync();
-        fence_proxy_async_shared();                    // q^C stores -> visible to the MMA
         __syncwarp();
-        if (lane == 0) mbar_arrive(qc_bar);
+        if (lane == 0) mbar_arrive(rp_bar);
       }
     }
     if (ok && pl.head) {
