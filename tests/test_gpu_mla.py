@@ -277,6 +277,8 @@ FUSED_SHAPES = [
          cache_dtype="int8"),                                       # int8, one CTA per head
     # head pairs (2N <= SMs): the second CTA of each pair has no q^N columns
     dict(B=5, S=1, He=256, Hcq=128, Hckv=32, N=20),
+    # head pairs on 144 of the SMs
+    dict(B=3, S=1, He=256, Hcq=128, Hckv=64, N=72),
     # head pairs with the int8 query: the two CTAs write 64 and 32 columns of each (token, head)
     # row of the bf16 q^N that the query quant reads
     dict(B=7, S=1, He=256, Hcq=128, Hckv=96, N=20, weight_uq_qr_dtype="int8",
