@@ -154,12 +154,20 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
   const size_t split_stride = static_cast<size_t>(p.T) * p.Ntot;
   const float* src = p.part + static_cast<size_t>(t) * p.Ntot;
   if ((p.Ntot % 4) == 0) {                       // rows start 16-byte aligned (Hcq % 8 == 0)
+    // with at most 8 splits, two columns per thread and round, all their split loads issued
+    // before the sums (one L2 round trip where the c^Q CTA's 384 float4 columns take two per
+    // thread; with 16 splits the second column's loads would not fit the registers)
+    constexpr int kCols = MAXS <= 8 ? 2 : 1;
     const int ncols = c1 / 4;
-    for (int c = c0 / 4 + threadIdx.x; c < ncols; c += NT) {
-      float4 v[MAXS];
+    for (int c = c0 / 4 + threadIdx.x; c < ncols; c += kCols * NT) {
+      const int c2 = kCols == 2 ? c + NT : ncols;
+      float4 v[MAXS], w[MAXS];
 #pragma unroll
       for (int s = 0; s < MAXS; ++s)
-        if (s < p.splits) v[s] = __ldg(reinterpret_cast<const float4*>(src + s * split_stride) + c);
+        if (s < p.splits) {
+          v[s] = __ldg(reinterpret_cast<const float4*>(src + s * split_stride) + c);
+          if (c2 < ncols) w[s] = __ldg(reinterpret_cast<const float4*>(src + s * split_stride) + c2);
+        }
       float4 a = v[0];
 #pragma unroll
       for (int s = 1; s < MAXS; ++s)
@@ -170,6 +178,18 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
           a.w += v[s].w;
         }
       reinterpret_cast<float4*>(h)[c] = a;
+      if (c2 < ncols) {
+        float4 b = w[0];
+#pragma unroll
+        for (int s = 1; s < MAXS; ++s)
+          if (s < p.splits) {
+            b.x += w[s].x;
+            b.y += w[s].y;
+            b.z += w[s].z;
+            b.w += w[s].w;
+          }
+        reinterpret_cast<float4*>(h)[c2] = b;
+      }
     }
   } else {
     for (int c = c0 + threadIdx.x; c < c1; c += NT) {
