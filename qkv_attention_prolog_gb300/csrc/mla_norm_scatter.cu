@@ -150,9 +150,18 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
     }
   };
 
-  // h = sum of the K-split partials, in split order.
+  // h = sum of the K-split partials, in split order.  Without the full-quant dequant the sums of
+  // squares are taken from the registers here (a float4 column lies in one part: Hcq and Hckv
+  // are multiples of 8), so no barrier and no pass over h precede the reduction.
   const size_t split_stride = static_cast<size_t>(p.T) * p.Ntot;
   const float* src = p.part + static_cast<size_t>(t) * p.Ntot;
+  const bool reg_ss = (p.Ntot % 4) == 0 && p.dsx == nullptr;
+  float2 ssr = make_float2(0.f, 0.f);
+  auto add_ss = [&](int c, const float4& x) {   // column c (float4 units) of the row
+    const float q = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+    if (4 * c < p.Hcq) ssr.x += q;
+    else if (4 * c < p.Hcq + p.Hckv) ssr.y += q;
+  };
   if ((p.Ntot % 4) == 0) {                       // rows start 16-byte aligned (Hcq % 8 == 0)
     // with at most 8 splits, two columns per thread and round, all their split loads issued
     // before the sums (one L2 round trip where the c^Q CTA's 384 float4 columns take two per
@@ -178,6 +187,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
           a.w += v[s].w;
         }
       reinterpret_cast<float4*>(h)[c] = a;
+      add_ss(c, a);
       if (c2 < ncols) {
         float4 b = w[0];
 #pragma unroll
@@ -189,6 +199,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
             b.w += w[s].w;
           }
         reinterpret_cast<float4*>(h)[c2] = b;
+        add_ss(c2, b);
       }
     }
   } else {
@@ -204,8 +215,8 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
       h[c] = a;
     }
   }
-  __syncthreads();
   if (threadIdx.x == 0) stamp(p.stamps, MLAP_STAMP_NORM, kStampMain);
+  if (!reg_ss) __syncthreads();
   if (p.dsx != nullptr) {   // full quant: dequant the exact integer products per token and column
     if (PARTS && c1 - c0 <= kPreCols * NT) {
 #pragma unroll
@@ -223,12 +234,15 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
 
   // sums of squares of the c^Q and c^KV parts, one reduction
   const float* hkv = h + p.Hcq;
-  float2 ss = make_float2(0.f, 0.f);
-  if (do_q)
-    for (int f = threadIdx.x; f < p.Hcq; f += NT) ss.x += h[f] * h[f];
-  if (do_kv)
-    for (int f = threadIdx.x; f < p.Hckv; f += NT) ss.y += hkv[f] * hkv[f];
-  ss = block_sum2<NT>(ss, red);
+  float2 ss = ssr;
+  if (!reg_ss) {
+    ss = make_float2(0.f, 0.f);
+    if (do_q)
+      for (int f = threadIdx.x; f < p.Hcq; f += NT) ss.x += h[f] * h[f];
+    if (do_kv)
+      for (int f = threadIdx.x; f < p.Hckv; f += NT) ss.y += hkv[f] * hkv[f];
+  }
+  ss = block_sum2<NT>(ss, red);                 // (its barrier also orders h before the reads)
   const float rq = 1.0f / sqrtf(ss.x / static_cast<float>(p.Hcq) + p.eps_cq);
   const float rkv = 1.0f / sqrtf(ss.y / static_cast<float>(p.Hckv) + p.eps_ckv);
 
