@@ -23,7 +23,9 @@ namespace {
 
 constexpr int kMaxSplits = 16;   // upper bound on the down-projection's K splits
 
-template <int NT>
+// Block reductions (every thread gets the result).  The buffer may be written again by a later
+// reduction only with kReuse, which adds the barrier that lets every thread read it first.
+template <int NT, bool kReuse = false>
 __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -39,11 +41,11 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
     r.x += red[i].x;
     r.y += red[i].y;
   }
-  __syncthreads();
+  if (kReuse) __syncthreads();
   return r;
 }
 
-template <int NT>
+template <int NT, bool kReuse = false>
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -53,7 +55,7 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   float r = 0.f;
 #pragma unroll
   for (int i = 0; i < NT / 32; ++i) r = fmaxf(r, red[i]);
-  __syncthreads();
+  if (kReuse) __syncthreads();
   return r;
 }
 
@@ -87,7 +89,8 @@ __device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float* v) {
 template <int MAXS, int NT, bool PARTS = false>
 __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizeParams p) {
   extern __shared__ float h[];
-  __shared__ float2 red[NT / 32];
+  __shared__ float2 red[NT / 32];                  // the sums of squares (each buffer is used
+  __shared__ float redm[NT / 32];                  // once: no barrier after its reduction)
   const int t = PARTS ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const bool do_q = !PARTS || (blockIdx.x & 1) == 0;
   const bool do_kv = !PARTS || (blockIdx.x & 1) == 1;
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(NT) norm_rope_scatter_kernel(const FinalizePar
       h4[0] = *reinterpret_cast<const float4*>(v);   // own columns only: no race
       h4[1] = *reinterpret_cast<const float4*>(v + 4);
     }
-    amax = block_max<NT>(amax, reinterpret_cast<float*>(red));
+    amax = block_max<NT>(amax, redm);
     const float scale = __fdiv_rn(amax, 127.0f);
     for (int f = f8; f < p.Hcq; f += NT * 8) {
       const float4* h4 = reinterpret_cast<const float4*>(h + f);
