@@ -21,10 +21,14 @@
 // Roles: warp 0 lane 0 TMA producer, warp 1 lane 0 MMA issuer, warp 2 TMEM owner, warps 4..7
 // epilogue (warp 4 + q owns TMEM lanes 32q..32q+31, i.e. tokens 32q..32q+31).  With an int8
 // W^UQ|W^QR (partial and full quant) warp 3 lane 0 loads the raw int8 tiles into a ring of
-// their own, warps 8..11 expand each into the bf16 operand layout (exact), and the epilogue
-// dequantises acc * scale_t[t] * dequant_scale_w_uq_qr[col] before q^C is rounded and q_r
-// rotated.  Every mbarrier wait is bounded; on a timeout the CTA
-// lets its issued loads land, frees TMEM and latches the error word.
+// their own (starting before the preceding kernel completes), warps 8..11 expand each into the
+// f16 operand layout (exact; the c^Q codes are f16 too), and the epilogue dequantises
+// acc * scale_t[t] * dequant_scale_w_uq_qr[col] (the CTA's columns of the scales staged in
+// shared memory while the up-projection runs) before q^C is rounded and q_r rotated.  The
+// epilogue releases q^C to the absorb MMAs before it rotates the rope blocks.  c^Q tiles carry
+// the token rows only (T rounded up to 8); the MMA's other A rows feed accumulator lanes that
+// are never stored.  Every mbarrier wait is bounded; on a timeout the CTA lets its issued
+// loads land, frees TMEM and latches the error word.
 //
 // Head pairs (2N <= SMs): a head's work is split over the two CTAs of a cluster.  CTA r of the
 // pair computes q^C columns 64r..64r+63 (its 64 W^UQ rows, plus the head's rope block r), sends
