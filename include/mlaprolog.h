@@ -24,9 +24,9 @@
  *     sets a human-readable reason retrievable with mlap_last_error() (thread-local).
  *   - The kernels of a call use programmatic dependent launch: each may start while the kernel
  *     before it in the stream is finishing and read the inputs it only reads (weights, RoPE
- *     tables, norm parameters and scales, and token_x outside full quant and the input
- *     RmsNormQuant) before it waits for that kernel; outputs, caches and the workspace are
- *     written only after that wait.  A caller's own kernel
+ *     tables, norm parameters and scales, token_x outside full quant and the input
+ *     RmsNormQuant, and qkv for qkvrnrc_execute) before it waits for that kernel; outputs,
+ *     caches and the workspace are written only after that wait.  A caller's own kernel
  *     that immediately precedes a call in the stream and itself triggers programmatic dependent
  *     launch (griddepcontrol.launch_dependents) must therefore not write those inputs; any other
  *     preceding stream work (copies, kernels without that trigger) is complete before the call's
