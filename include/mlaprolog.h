@@ -24,13 +24,13 @@
  *     sets a human-readable reason retrievable with mlap_last_error() (thread-local).
  *   - The kernels of a call use programmatic dependent launch: each may start while the kernel
  *     before it in the stream is finishing and read the inputs it only reads (weights, RoPE
- *     tables, norm parameters and scales, token_x outside full quant and the input
- *     RmsNormQuant, and qkv for qkvrnrc_execute) before it waits for that kernel; outputs,
- *     caches and the workspace are written only after that wait.  A caller's own kernel
- *     that immediately precedes a call in the stream and itself triggers programmatic dependent
- *     launch (griddepcontrol.launch_dependents) must therefore not write those inputs; any other
- *     preceding stream work (copies, kernels without that trigger) is complete before the call's
- *     first kernel starts.
+ *     tables, norm parameters and scales, token_x outside the input RmsNormQuant and outside
+ *     full quant beyond 256 tokens, and qkv for qkvrnrc_execute) before it waits for that
+ *     kernel; outputs, caches and the workspace are written only after that wait.  A caller's
+ *     own kernel that immediately precedes a call in the stream and itself triggers
+ *     programmatic dependent launch (griddepcontrol.launch_dependents) must therefore not write
+ *     those inputs; any other preceding stream work (copies, kernels without that trigger) is
+ *     complete before the call's first kernel starts.
  */
 #ifndef MLAPROLOG_H
 #define MLAPROLOG_H
@@ -272,7 +272,8 @@ const char* mlap_last_error(void);
  * up-projection and absorb where one kernel runs both (decode: T <= 128, N >= 16, D = 128,
  * Dr = 64, Hckv <= 512 and a multiple of 32); MLAP_STAMP_ABSORB the separate absorb;
  * MLAP_STAMP_QKV the QkvRmsNormRopeCache kernel (qkvrnrc_execute_stamped).  The small helper
- * kernels (input RmsNormQuant, token_x widening, int8 query quantisation) record nothing.
+ * kernels (input RmsNormQuant, full-quant token_x widening beyond 256 tokens, int8 query
+ * quantisation) record nothing.
  * Same errors as the execute calls, plus MLAP_ERR_NULL for a NULL `stamps`.  Stamps are
  * profiling aids with the resolution of %globaltimer; nothing in the results depends on them. */
 #define MLAP_STAMP_KERNELS 5
@@ -306,9 +307,9 @@ mlap_status_t qkvrnrc_execute_stamped(const qkvrnrc_args_t* args, void* workspac
  *   - Shapes whose workspace (mlap_get_workspace_size) exceeds MLAP_NO_ALLOC_SCRATCH_BYTES are
  *     rejected with MLAP_ERR_WORKSPACE before any device work.  With the decode shapes
  *     (He 7168, Hcq 1536, Hckv 512, N 128, D 128, Dr 64) in the non-quant scenario without
- *     the input RmsNormQuant (which adds T * He * 2 bytes, as full quant does), calls with T <= 147 or
- *     257 <= T <= 568 tokens fit (up to 256 tokens the down-projection keeps up to 16 K-split
- *     partials, above that one).
+ *     the input RmsNormQuant (which adds T * He * 2 bytes, as full quant does beyond 256
+ *     tokens), calls with T <= 147 or 257 <= T <= 568 tokens fit (up to 256 tokens the
+ *     down-projection keeps up to 16 K-split partials, above that one).
  *   - Every call looks up the array's device address on the current device (the first lookup on
  *     a device may load the library's device code there); make the first call on each device
  *     before any stream capture on it.

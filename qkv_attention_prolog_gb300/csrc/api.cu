@@ -353,9 +353,10 @@ MlaWs mla_ws_layout(const MlaDims& d) {
   off += align_up(static_cast<size_t>(d.T) * d.N * d.D * 2, 256);
   w.scale = off;
   off += align_up(static_cast<size_t>(d.T) * 4, 256);
-  w.xb = off;   // the down-projection's bf16 operand when it is not token_x itself: token_x
-                // widened (full quant) or after the input RmsNormQuant
-  if (d.full || d.xnorm) off += align_up(static_cast<size_t>(d.T) * d.He * 2, 256);
+  w.xb = off;   // the down-projection's 16-bit operand when it is not token_x itself: token_x
+                // widened (full quant outside the decode orientation) or after the input
+                // RmsNormQuant
+  if ((d.full && !swap) || d.xnorm) off += align_up(static_cast<size_t>(d.T) * d.He * 2, 256);
   w.qn = off;   // int8 query: q^N in bf16 before the per-token-head quant
   if (d.query_int8) off += align_up(static_cast<size_t>(d.T) * d.N * d.Hckv * 2, 256);
   w.total = off;
@@ -507,17 +508,20 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   g.err = err;
   g.geo.stamps = stamps;
   g.geo.stamp_k = MLAP_STAMP_DOWN;
-  // token_x itself is the activation (not widened or normalised by a kernel of this call): the
+  // token_x itself is the activation (not normalised by a kernel of this call, and not widened:
+  // in the decode orientation the converter warps expand full quant's int8 token_x tiles): the
   // down-projection streams before the preceding kernel finishes and waits only to store
-  g.geo.act_ready = !(d.full || d.xnorm);
+  const bool widen = d.full && !swap;
+  g.geo.act_ready = !(widen || d.xnorm);
   g.swap = swap;
   g.mt = swap ? mt : 1;
   DownParams dp{0};
   const int ch_t = swap ? (bn_t < 32 ? bn_t : 32) : 32;   // tokens per epilogue store box
-  // full quant: the int8 activation is widened to f16 first (exact), the int8 weights are
-  // expanded in shared memory by the GEMM's converter warps, and the integer products are
-  // dequantised per token and column after the K-split sum (norm kernel)
-  const void* xact = d.full || d.xnorm ? static_cast<const void*>(wsb + L.xb) : a->token_x.data;
+  // full quant: the int8 weights (and, in the decode orientation, the int8 token_x tiles) are
+  // expanded to f16 in shared memory by the GEMM's converter warps (exact); otherwise token_x is
+  // widened to f16 by a kernel first.  The integer products are dequantised per token and
+  // column after the K-split sum (norm kernel).
+  const void* xact = widen || d.xnorm ? static_cast<const void*>(wsb + L.xb) : a->token_x.data;
   g.a_int8 = d.full;
   auto wmap = [&](CUtensorMap* m, const void* w, int64_t rows, int box) {
     return d.full ? make_tmap_i8(m, w, d.He, rows, box) : make_tmap(m, w, d.He, rows, d.He, box);
@@ -528,7 +532,10 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
       const int seg = ceil_div(d.Hcq, wrows);
       CHECK_STATUS(wmap(&g.a0, a->weight_dq.data, d.Hcq, wrows));
       CHECK_STATUS(wmap(&g.a1, a->weight_dkv_kr.data, d.Hckv + d.Dr, wrows));
-      CHECK_STATUS(make_tmap(&g.b0, xact, d.He, d.T, d.He, bn_t));
+      if (d.full)
+        CHECK_STATUS(make_tmap_i8(&g.b0, a->token_x.data, d.He, d.T, bn_t));
+      else
+        CHECK_STATUS(make_tmap(&g.b0, xact, d.He, d.T, d.He, bn_t));
       g.b1 = g.b0;
       g.bn = bn_t;
       g.geo.m_tiles = seg + ceil_div(d.Hckv + d.Dr, wrows);
@@ -591,7 +598,7 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                                  static_cast<int32_t>(d.He), stream);
       if (ce != cudaSuccess) return cuda_fail(ce, "input RmsNormQuant launch");
     }
-    if (d.full) {
+    if (widen) {
       ce = launch_widen_int8(static_cast<const int8_t*>(a->token_x.data),
                              reinterpret_cast<__half*>(wsb + L.xb), d.T * d.He, stream);
       if (ce != cudaSuccess) return cuda_fail(ce, "token_x widening launch");

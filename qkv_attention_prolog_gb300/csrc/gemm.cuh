@@ -95,7 +95,9 @@ struct StoreOp {
   uint32_t soff;
 };
 
-// WQ: 0 = bf16 weight, 1 = int8 weight in operand A, 2 = int8 weight in operand B.
+// WQ: 0 = bf16 weight, 1 = int8 weight in operand A, 2 = int8 weight in operand B, 3 = int8
+//     weight in operand A and int8 activation in operand B (decode orientation, full quant: both
+//     raw tiles arrive on the stage's raw barrier and the converter warps expand both).
 // MT: 128-row tiles of A per unit (1 or 2), each with its own TMEM accumulator.
 // ALD: operand B (the activation, decode orientation) is loaded by cp.async loader warps.
 template <int BN_, int WQ_ = 0, int MT_ = 1, int ALD_ = 0, int CG_ = 1>
@@ -112,8 +114,10 @@ struct GemmCfg {
   static constexpr int BK = 64;
   static constexpr int A_BYTES = BM_U * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
-  static constexpr int RAW_ROWS = WQ == 1 ? BM_U : (WQ == 2 ? BN : 0);
-  static constexpr int RAW_BYTES = RAW_ROWS * BK;      // int8 weight tile
+  static constexpr int RAW_ROWS = (WQ == 1 || WQ == 3) ? BM_U : (WQ == 2 ? BN : 0);
+  static constexpr int RAW_ACT_ROWS = WQ == 3 ? BN : 0;   // int8 activation rows (WQ = 3)
+  static constexpr int RAW_W_BYTES = RAW_ROWS * BK;       // int8 weight tile
+  static constexpr int RAW_BYTES = RAW_W_BYTES + RAW_ACT_ROWS * BK;   // a stage's int8 tiles
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + RAW_BYTES;
   static constexpr int SMEM_LIMIT = 232448;            // 227 KB opt-in per CTA
   static constexpr int RESERVED = 1024 + 512;          // alignment slack + barriers
@@ -384,8 +388,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
       auto issue_weight = [&](int st, const Frag& f, int kb) {
         if constexpr (WQ != 0) {
           mbar_arrive_expect_tx(&rawf_bar[st], Cfg::RAW_BYTES);
-          if (WQ == 1) load_a(f.tm, f.b, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES);
+          if (WQ == 1 || WQ == 3) load_a(f.tm, f.b, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES);
           else load_b(f, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES);
+          // the int8 activation tile rides with the weight's (an input of the call: no wait)
+          if (WQ == 3)
+            load_b(f, kb, &rawf_bar[st], smemR + st * Cfg::RAW_BYTES + Cfg::RAW_W_BYTES);
         } else if (ALD) {
           mbar_arrive_expect_tx(&full_bar[st], Cfg::A_BYTES);
           load_a(f.tm, f.b, kb, &full_bar[st], smemA + st * Cfg::A_BYTES);
@@ -402,6 +409,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
       };
       auto issue_act = [&](int st, const Frag& f, int kb) {
         if (ALD) return;
+        if (WQ == 3) {   // the activation came with the weight's raw tiles: only the arrival
+          mbar_arrive(&full_bar[st]);
+          return;
+        }
         if (w_is_a) {
           if (issuer) mbar_arrive_expect_tx(&full_bar[st], CG * Cfg::B_BYTES);
           load_b(f, kb, &full_bar[st], smemB + st * Cfg::B_BYTES);
@@ -634,9 +645,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
           break;
         }
         const uint8_t* raw = smemR + stage * Cfg::RAW_BYTES;
-        uint8_t* dst = WQ == 1 ? smemA + stage * Cfg::A_BYTES : smemB + stage * Cfg::B_BYTES;
+        uint8_t* dst = (WQ == 1 || WQ == 3) ? smemA + stage * Cfg::A_BYTES
+                                            : smemB + stage * Cfg::B_BYTES;
         constexpr int kChunks = Cfg::RAW_ROWS ? (Cfg::RAW_ROWS + 31) / 32 : 1;   // per thread
         convert_int8_tile<kChunks>(raw, dst, Cfg::RAW_ROWS, ct);
+        if constexpr (WQ == 3) {   // the int8 activation tile into operand B
+          constexpr int kActChunks = (Cfg::RAW_ACT_ROWS + 31) / 32;
+          convert_int8_tile<kActChunks>(raw + Cfg::RAW_W_BYTES, smemB + stage * Cfg::B_BYTES,
+                                        Cfg::RAW_ACT_ROWS, ct);
+        }
         fence_proxy_async_shared();              // generic writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_bar[stage]);

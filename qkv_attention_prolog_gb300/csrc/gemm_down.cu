@@ -3,16 +3,17 @@
 
 namespace mlap {
 
-// Full quant: int8 W^DQ and W^DKV|W^KR expanded to bf16 by the converter warps (exact); the
-// activation is the bf16-widened int8 token_x.
+// Full quant: int8 W^DQ and W^DKV|W^KR expanded to f16 by the converter warps (exact).  Decode
+// orientation: the converters expand the int8 token_x tiles too (WQ = 3), so the activation is
+// an input of the call; otherwise the activation is the f16-widened token_x.
 static cudaError_t launch_down_int8(const GemmLaunch& L, const DownParams& p) {
   if (L.swap) {
     switch (L.bn) {
-      case 16: return launch_gemm_t<16, 1, 1>(L, EpiDown<true, 128, 16>{p});
-      case 32: return launch_gemm_t<32, 1, 1>(L, EpiDown<true, 128, 32>{p});
-      case 64: return launch_gemm_t<64, 1, 1>(L, EpiDown<true, 128, 32>{p});
-      case 128: return launch_gemm_t<128, 1, 1>(L, EpiDown<true, 128, 32>{p});
-      case 256: return launch_gemm_t<256, 1, 1>(L, EpiDown<true, 128, 32>{p});
+      case 16: return launch_gemm_t<16, 3, 1>(L, EpiDown<true, 128, 16>{p});
+      case 32: return launch_gemm_t<32, 3, 1>(L, EpiDown<true, 128, 32>{p});
+      case 64: return launch_gemm_t<64, 3, 1>(L, EpiDown<true, 128, 32>{p});
+      case 128: return launch_gemm_t<128, 3, 1>(L, EpiDown<true, 128, 32>{p});
+      case 256: return launch_gemm_t<256, 3, 1>(L, EpiDown<true, 128, 32>{p});
       default: return cudaErrorInvalidValue;
     }
   }
