@@ -24,13 +24,13 @@
  *     sets a human-readable reason retrievable with mlap_last_error() (thread-local).
  *   - The kernels of a call use programmatic dependent launch: each may start while the kernel
  *     before it in the stream is finishing and read the inputs it only reads (weights, RoPE
- *     tables, norm parameters and scales, token_x outside the input RmsNormQuant and outside
- *     full quant beyond 256 tokens, and qkv for qkvrnrc_execute) before it waits for that
- *     kernel; outputs, caches and the workspace are written only after that wait.  A caller's
- *     own kernel that immediately precedes a call in the stream and itself triggers
- *     programmatic dependent launch (griddepcontrol.launch_dependents) must therefore not write
- *     those inputs; any other preceding stream work (copies, kernels without that trigger) is
- *     complete before the call's first kernel starts.
+ *     tables, norm parameters and scales, token_x outside full quant beyond 256 tokens, and qkv
+ *     for qkvrnrc_execute) before it waits for that kernel; outputs, caches and the workspace
+ *     are written only after that wait.  A caller's own kernel that immediately precedes a call
+ *     in the stream and itself triggers programmatic dependent launch
+ *     (griddepcontrol.launch_dependents) must therefore not write those inputs; any other
+ *     preceding stream work (copies, kernels without that trigger) is complete before the
+ *     call's first kernel starts.
  */
 #ifndef MLAPROLOG_H
 #define MLAPROLOG_H

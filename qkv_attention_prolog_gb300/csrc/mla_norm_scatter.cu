@@ -12,7 +12,8 @@
 //   int8 caches: rne(value / quant_scale[j]) saturated to [-128, 127] ("Formulas" (4) division).
 //   cache_index = -1 skips the token; other values outside [0, slots) are skipped and latched.
 //   full quant: h *= dequant_scale_x[t] * dequant_scale_w[column] after the split sum (the int8
-//   products are exact), and the two helper kernels below (token_x widening, int8 query).
+//   products are exact), and the two helper kernels below (token_x widening beyond 256 tokens,
+//   int8 query).
 // rms_norm_quant_kernel: the optional input RmsNormQuant that runs ahead of the down-projection.
 // With Nkv = 1 and a dense (BlockNum, BlockSize, 1, H) cache, slot i is row i of the cache.
 #include "internal.h"
@@ -744,7 +745,6 @@ __global__ void __launch_bounds__(NT) rms_norm_quant_kernel(
     for (int v = 0; v < NV; ++v)
       if (threadIdx.x + v * NT < nvec) load_params(threadIdx.x + v * NT, g[v], b[v], d[v]);
   }
-  grid_dependency_wait();
   const uint4* row = reinterpret_cast<const uint4*>(x + static_cast<size_t>(blockIdx.x) * He);
   uint4 raw[NV];
 #pragma unroll
@@ -765,6 +765,9 @@ __global__ void __launch_bounds__(NT) rms_norm_quant_kernel(
     }
   }
   const float2 tot = block_sum2<NT>(make_float2(ss, 0.f), red);
+  // token_x is an input of the call: its row and sum of squares come before the wait on the
+  // preceding kernel; only the stores of x' (which that kernel may still read) wait
+  grid_dependency_wait();
   grid_launch_dependents();
   const float r = 1.0f / sqrtf(tot.x / static_cast<float>(He) + eps);
   __nv_bfloat16* dst = out + static_cast<size_t>(blockIdx.x) * He;
@@ -839,8 +842,9 @@ cudaError_t launch_query_quant(const __nv_bfloat16* qn, int8_t* q, float* scale,
   if ((H % 8) || H > 8 * 32 * kQqVec) return cudaErrorInvalidValue;
   const int64_t blocks = (rows * 32 + 255) / 256;
   if (blocks < 1) return cudaSuccess;
+  // (programmatic dependent launch: the kernel waits for q^N with griddepcontrol.wait)
   return launch_k(query_quant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), stream,
-                  false, qn, q, scale, rows, H);
+                  true, qn, q, scale, rows, H);
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t stream, bool pdl) {
