@@ -202,6 +202,11 @@ def test_full_quant_bf16_cache():
 
 FULL_QUANT_SHAPES = [
     dict(B=5, S=1, He=256, Hcq=128, N=3, cache_dtype="int8"),              # decode orientation
+    # decode orientation, the int8 token_x tiles expanded by the converter warps at every token
+    # tile width above 16 (32, 128 and 256 rows); He = 272 and 336 end in a partial K block
+    dict(B=24, S=1, He=272, Hcq=128, N=2, cache_dtype="int8"),
+    dict(B=100, S=1, He=512, Hcq=256, N=2, cache_dtype="bf16"),
+    dict(B=200, S=1, He=336, Hcq=128, Hckv=96, N=2, Dr=32, cache_dtype="int8"),
     dict(B=3, S=100, He=384, Hcq=192, Hckv=128, N=2, cache_dtype="int8"),   # prefill orientation
     dict(B=2, S=150, He=256, Hcq=144, Hckv=96, N=2, Dr=32, cache_dtype="bf16"),
 ]
