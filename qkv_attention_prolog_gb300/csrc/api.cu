@@ -650,14 +650,18 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
   const bool fused = swap && d.N >= kFusedMinHeads &&
                      up_absorb_supported(d.T, d.N, d.D, d.Dr, d.Hckv);
   if (fused) {
-    CUtensorMap tcq, tw, tw128, tuk, tuk128;   // (the 128-row maps serve int8 weights only)
+    CUtensorMap tcq, tw, tw128, tuk, tuk128;   // (the wide maps serve int8 weights only: a head
+                                               // CTA's W^UQ rows, 128 or 64 in a pair, and
+                                               // 128 W^UK rows per box)
     // c^Q tiles of the token rows only (the MMA's other A rows feed accumulator lanes that are
     // never stored)
     const int cq_rows = d.T < 128 ? static_cast<int>((d.T + 7) / 8 * 8) : 128;
     CHECK_STATUS(make_tmap(&tcq, cq, d.Hcq, d.T, d.Hcq, cq_rows));
+    int ua_k = 0, ua_r = 0, ua_pair = 0;
+    up_absorb_plan(sms, static_cast<int>(d.N), &ua_k, &ua_r, &ua_pair);
     if (d.w_int8) {
       CHECK_STATUS(make_tmap_i8(&tw, a->weight_uq_qr.data, d.Hcq, Mup, 32));
-      CHECK_STATUS(make_tmap_i8(&tw128, a->weight_uq_qr.data, d.Hcq, Mup, 128));
+      CHECK_STATUS(make_tmap_i8(&tw128, a->weight_uq_qr.data, d.Hcq, Mup, ua_pair ? 64 : 128));
       CHECK_STATUS(make_tmap(&tuk128, a->weight_uk.data, d.D, d.N * d.Hckv, d.D, 128));
     } else {
       CHECK_STATUS(make_tmap(&tw, a->weight_uq_qr.data, d.Hcq, Mup, d.Hcq, 32));
@@ -674,7 +678,9 @@ mlap_status_t mla_run(const mlap_args_t* a, void* ws, size_t ws_bytes, cudaStrea
                       static_cast<int32_t>(d.Hcq), static_cast<int32_t>(d.Hckv),
                       scale_t, static_cast<const float*>(a->dequant_scale_w_uq_qr.data), 2, 0,
                       stamps};
-    up_absorb_plan(sms, static_cast<int>(d.N), &ua.k, &ua.R, &ua.pair);
+    ua.k = ua_k;
+    ua.R = ua_r;
+    ua.pair = ua_pair;
     ua.cq_rows = cq_rows;
     ce = launch_up_absorb(tcq, tw, tuk, d.w_int8 ? &tw128 : nullptr, d.w_int8 ? &tuk128 : nullptr,
                           ua, err, stream);

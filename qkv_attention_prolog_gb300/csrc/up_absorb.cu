@@ -135,12 +135,13 @@ __device__ __forceinline__ UaPlan ua_plan(const UpAbsorbParams& p) {
   return pl;
 }
 
-// The int8 kernel's producers also take a head's 128 contiguous W^UQ rows, and 128 W^UK rows,
-// as one box each: at these sizes each TMA issue costs the producer thread about as much time
-// as the box it moves.  The bf16 kernel is not producer-bound and takes no extra maps (two more
-// tensor maps in its parameters cost its launch more than the larger boxes would save).
+// The int8 kernel's producers also take a head CTA's contiguous W^UQ rows (128, or the 64 of a
+// pair CTA), and 128 W^UK rows, as one box each: at these sizes each TMA issue costs the
+// producer thread about as much time as the box it moves.  The bf16 kernel is not
+// producer-bound and takes no extra maps (two more tensor maps in its parameters cost its
+// launch more than the larger boxes would save).
 template <bool INT8> struct UaWideMaps {
-  CUtensorMap w;    // W^UQ|W^QR rows, box 64 x 128
+  CUtensorMap w;    // W^UQ|W^QR rows, box 64 x 128 (64 x 64 for head pairs)
   CUtensorMap uk;   // W^UK rows, box 64 x 128
 };
 template <> struct UaWideMaps<false> {};
@@ -354,12 +355,12 @@ __global__ void __launch_bounds__(UaCfg<INT8>::THREADS, 1)
       if (kb >= kRS && !mbar_wait(&rawe_bar[rs], rph ^ 1u, abort_flag)) break;
       uint8_t* r = ring_raw + rs * kRawB;
       mbar_arrive_expect_tx(&rawf_bar[rs], static_cast<uint32_t>(up_rows) * kUaBK);
-      constexpr bool kWide = INT8 && !PAIR;   // a head's 128 contiguous W^UQ rows as one box
-      if constexpr (kWide)
+      // a head CTA's contiguous W^UQ rows (128, or 64 in a pair) as one box
+      if constexpr (INT8)
         if (pl.head) tma_load_2d(r, &wide.w, &rawf_bar[rs], kb * kUaBK, hrow0);
 #pragma unroll
       for (int j = 0; j < 6; ++j)
-        if (j < nbox && !(kWide && pl.head && j < kD / 32))
+        if (j < nbox && !(pl.head && j < kHRows / 32))
           tma_load_2d(r + j * 2048, &tmW, &rawf_bar[rs], kb * kUaBK, ybox[j]);
       ++rawfills[rs];
       if (++rs == kRS) {
