@@ -281,9 +281,13 @@ def test_full_quant_scenarios():
     # an int8 query row is quantised from registers: Hckv <= 1024
     assert _status(_args(_mla(Hckv=1024, w_int8=True, cache_int8=True, full=True)))[0] == 0
     assert _status(_args(_mla(Hckv=1032, w_int8=True, cache_int8=True, full=True)))[0] == 4
-    # full quant needs its own workspace regions (widened x, staged q^N)
-    assert _status(_args(_mla(w_int8=True, cache_int8=True, full=True)))[1] > \
-        _status(_args(_mla(w_int8=True, cache_int8=True)))[1]
+    # full quant's own workspace regions: q^N staged in bf16 ahead of the int8 query, and from
+    # 257 tokens (prefill orientation) token_x widened to f16 for the down-projection; up to 256
+    # tokens the down-projection's converter warps expand the int8 token_x tiles themselves
+    for T, widened in ((128, 0), (256, 0), (512, 512 * 7168 * 2)):
+        extra = (_status(_args(_mla(T=T, w_int8=True, cache_int8=True, full=True)))[1]
+                 - _status(_args(_mla(T=T, w_int8=True, cache_int8=True)))[1])
+        assert extra == T * 128 * 512 * 2 + widened, (T, extra)
 
 
 def test_rms_norm_quant_validation():
