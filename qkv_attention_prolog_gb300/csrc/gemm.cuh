@@ -11,9 +11,11 @@
 // One operand is a weight (`w_op`).  Its first pipeline stages are requested before the kernel
 // waits on the previous kernel in the stream (programmatic dependent launch), so the weight
 // stream starts while the producer of the activations is still finishing.  With WQ != 0 the
-// weight is int8: TMA brings the raw int8 tile and four converter warps expand it to bf16 in the
-// swizzled operand layout (exact for |v| <= 127); the MMA then runs in bf16 with fp32
-// accumulation, which is exact for integer partial sums below 2^24.
+// weight is int8: TMA brings the raw int8 tile and four converter warps expand it to f16 in the
+// swizzled operand layout (exact for every int8 value); the MMA then runs in f16 with fp32
+// accumulation, which is exact for integer partial sums below 2^24.  With WQ = 3 (full quant,
+// decode orientation) the int8 activation tile comes with the weight tile and is expanded the
+// same way, so the activation needs no kernel of its own and is read before the dependency.
 //
 // In the decode orientation a unit may hold MT = 2 row tiles of A (256 weight rows): one TMA box
 // brings both, and two MMAs per K step share the B tile, so each weight byte costs half the
@@ -631,7 +633,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, WQ, MT, ALD, CG>::THREADS, 1)
     // every store has read its staging buffer (the writes themselves complete with the grid)
     if (lane == 0) bulk_wait_group_read<0>();
   } else if (WQ != 0 && warp >= 8) {
-    // ------------------------------------------------------------------ int8 -> bf16 converters
+    // ------------------------------------------------------------------ int8 -> f16 converters
     const int ct = threadIdx.x - 256;
     int stage = 0;
     uint32_t phase = 0;
