@@ -28,6 +28,7 @@ import io
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -122,12 +123,22 @@ KERNEL_SOURCES = {   # (api.cu sets each MLA kernel's grid, schedule and unit or
 }
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def code_only(text):
+    """A C++/CUDA source without its comments, trailing spaces and blank lines: what the compiler
+    sees, so that editing a comment leaves a recorded traffic figure valid."""
+    body = _COMMENT.sub("", text)
+    return "\n".join(line.rstrip() for line in body.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel_key):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "qkv_attention_prolog_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel_key]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -30,3 +30,11 @@ def test_decode_weights_dominate():
     kern, path_bytes, _ = bench.mla_model(d)
     # per-kernel figures add each intermediate once written and once read
     assert kern["down"]["bytes"] + kern["up"]["bytes"] + kern["absorb"]["bytes"] > path_bytes - 1e6
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    # a recorded DRAM traffic figure stays valid across comment edits, not across code edits
+    code = "int a = 1;  // one\n/* block\n   comment */\n\n__global__ void k() { a += 2; }\n"
+    assert bench.code_only(code) == bench.code_only(code.replace("// one", "// the first"))
+    assert bench.code_only(code) == bench.code_only("int a = 1;\n__global__ void k() { a += 2; }")
+    assert bench.code_only(code) != bench.code_only(code.replace("a += 2", "a += 3"))
