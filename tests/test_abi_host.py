@@ -320,3 +320,18 @@ def test_rms_norm_quant_validation():
     assert _status(_args(_mla(xnorm="channel", w_int8=True, full=True)))[0] == 4
     assert _status(_args(_mla(He=10496, xnorm="channel")))[0] == 4
     assert _status(_args(_mla(He=10240, xnorm="channel")))[0] == 0
+
+
+def test_no_alloc_checks_its_scratch_limit_before_device_work():
+    # the allocation-free call validates and sizes like the workspace call, and refuses shapes
+    # beyond its static scratch (MLAP_ERR_WORKSPACE) before touching a device; an empty call
+    # returns at once
+    lib = _lib.load()
+    assert _status(_args(_mla(T=200)))[1] > 24 * 1024 * 1024
+    assert lib.mlap_execute_no_alloc(ctypes.byref(_args(_mla(T=200))), None) == 5
+    assert "static scratch" in lib.mlap_last_error().decode()
+    assert lib.mlap_execute_no_alloc(ctypes.byref(_args(_mla(T=0))), None) == 0
+    t = _mla(T=64)
+    t.pop("token_x")                    # the same validation as the workspace call, first
+    bad = _status(_args(t))[0]
+    assert bad != 0 and lib.mlap_execute_no_alloc(ctypes.byref(_args(t)), None) == bad
