@@ -511,9 +511,10 @@ def measure_mla(args, case, dev, stream, steps, warm, world, stamp_calls, sample
         kern["up_absorb"] = {
             "bytes": kern["up"]["bytes"] + kern["absorb"]["bytes"] - 2 * d.T * d.N * d.D * 2,
             "flops": kern["up"]["flops"] + kern["absorb"]["flops"]}
-    # down, norm/scatter, up (+ absorb); full quant adds the token_x widening and, with an int8
-    # query, its per-token-head quantisation; the input RmsNormQuant adds its own kernel
-    launches = (len(per) + (1 + c_int8 if case.full_quant else 0)
+    # down, norm/scatter, up (+ absorb); full quant adds, with an int8 query, its per-token-head
+    # quantisation, and beyond 256 tokens the token_x widening (up to 256 the down-projection's
+    # converter warps expand token_x); the input RmsNormQuant adds its own kernel
+    launches = (len(per) + ((int(c_int8) + int(d.T > 256)) if case.full_quant else 0)
                 + (1 if case.x_norm is not None else 0))
     return {"case": case, "cpu": cpu, "sets": sets, "kern": kern, "path_bytes": path_bytes,
             "path_flops": path_flops, "ms_step": ms_step, "steps": steps, "n_sets": n_sets,

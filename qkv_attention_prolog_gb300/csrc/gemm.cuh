@@ -215,7 +215,7 @@ struct FragIter {
 // int8 to f16 by the 2^10 magic number: with u = v + 128 in [0, 255] (v XOR 0x80 per byte), the
 // f16 with bits 0x6400 | u is 1024 + u exactly (f16 has 10 mantissa bits), so one byte permute
 // builds two such halves and one packed f16 subtraction of 1024 + 128 gives v exactly.  The int8
-// paths therefore run their MMAs with f16 operands (the c^Q codes and the widened token_x are
+// paths therefore run their MMAs with f16 operands (the c^Q codes and full quant's token_x are
 // integers of magnitude <= 128 too, exact in f16): one permute and one packed subtract per two
 // values, on the full-rate pipes.
 __device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t biased, uint32_t sel) {

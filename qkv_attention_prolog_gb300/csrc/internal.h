@@ -104,7 +104,8 @@ cudaError_t launch_rms_norm_quant(const __nv_bfloat16* x, const __nv_bfloat16* g
                                   float eps, __nv_bfloat16* out, int64_t T, int32_t He,
                                   cudaStream_t stream);
 
-// Full quant: int8 token_x widened to f16 (exact), n elements (a multiple of 16).
+// Full quant beyond 256 tokens: int8 token_x widened to f16 (exact), n elements (a multiple of
+// 16).
 cudaError_t launch_widen_int8(const int8_t* x, __half* out, int64_t n, cudaStream_t stream);
 
 // int8 query per token and head: rows of H bf16 values -> int8 codes (scale = amax / 127, round
